@@ -1,0 +1,171 @@
+"""FP64 CPU oracle for exact scaled-dot-product attention.
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The product library
+never imports this package and shares no code with it.
+
+The arithmetic lives in ``attn_oracle.c`` (plain double-precision loops over
+the definition, OpenMP across rows); this module compiles it with gcc and
+marshals NumPy float64 arrays in and out.  Every input is first upcast to
+float64, which is exact for BF16 and FP16.
+
+Functions
+---------
+attn_fwd(q, k, v, causal, scale, rows=None) -> (o, lse)
+    O = softmax(scale * Q K^T) V and the natural-log row logsumexp
+    ("FlashAttention hardware-aware analysis" (huaweicloud), section one,
+    part 2; "Understanding online softmax in Flash Attention from scratch",
+    section 3.1).
+attn_bwd(q, k, v, dout, causal, scale, qrows=None, kcols=None) -> (dq, dk, dv)
+    chain rule of the same definition ("Understanding FlashAttention,
+    Part 2", section 2.4, Figs 16-19).
+
+Pins (tests/test_oracle_pins.py): hand-derived closed forms under
+tests/golden/, brute force with Python ``math`` on tiny inputs, the two-block
+merge rule of the huaweicloud page (section two), the all-equal-scores closed
+form, one-hot rows at scores near 1000, causal row 0, finite differences and
+an independent autograd evaluation for the backward, and the invariants
+sum_j dV_j = sum_i dO_i, sum_j dK_j = 0, and K/V permutation symmetry.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+
+def build(force: bool = False, src: str = SOURCE, out: str = _LIB) -> str:
+    """Compile the oracle source into a shared library (gcc, OpenMP, IEEE semantics)."""
+    if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    tmp = out + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           src, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _as_f64(x) -> np.ndarray:
+    if hasattr(x, "detach"):  # a torch tensor: upcast exactly, then view as NumPy
+        x = x.detach().to("cpu").double().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _rows(r):
+    if r is None:
+        return None
+    return np.ascontiguousarray(np.asarray(r, dtype=np.int64).reshape(-1))
+
+
+class Oracle:
+    """One loaded copy of the oracle library (the default one, or a test build)."""
+
+    def __init__(self, libpath: str):
+        lib = ctypes.CDLL(libpath)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        lib.oracle_attn_fwd.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
+                                        P, I64, P, P]
+        lib.oracle_attn_fwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_double,
+                                        P, I64, P, I64, P, P, P]
+        lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = libpath
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def attn_fwd(self, q, k, v, causal: bool, scale: float, rows=None):
+        """Exact attention forward in FP64.
+
+        q: [..., N, d]; k, v: [..., Nk, d] with the same leading dims (Nk == N
+        when causal).  Returns (o, lse) with shapes [..., R, d] and [..., R],
+        R = N or len(rows).
+        """
+        q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+        if q.ndim < 2 or k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+            raise ValueError("q must be [..., N, d] and k, v [..., Nk, d] with matching dims")
+        lead, (N, d), Nk = q.shape[:-2], q.shape[-2:], k.shape[-2]
+        BH = int(np.prod(lead)) if lead else 1
+        rr = _rows(rows)
+        R = N if rr is None else rr.size
+        o = np.empty((BH, R, d), np.float64)
+        lse = np.empty((BH, R), np.float64)
+        rc = self.lib.oracle_attn_fwd(_ptr(q), _ptr(k), _ptr(v), BH, N, Nk, d, int(bool(causal)),
+                                      float(scale), _ptr(rr), 0 if rr is None else rr.size,
+                                      _ptr(o), _ptr(lse))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_fwd failed (bad argument or out of memory)")
+        return o.reshape(*lead, R, d), lse.reshape(*lead, R)
+
+    def attn_bwd(self, q, k, v, dout, causal: bool, scale: float, qrows=None, kcols=None,
+                 want_dq: bool = True, want_dkv: bool = True):
+        """Exact attention backward in FP64: gradients of sum(dO * O).
+
+        Returns (dq, dk, dv); dq covers ``qrows`` (all rows if None), dk and dv
+        cover ``kcols`` (all keys if None).  A skipped output is None.
+        """
+        q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+        if not (q.shape == k.shape == v.shape == do.shape) or q.ndim < 2:
+            raise ValueError("q, k, v, dout must share one [..., N, d] shape")
+        lead, (N, d) = q.shape[:-2], q.shape[-2:]
+        BH = int(np.prod(lead)) if lead else 1
+        qr, kc = _rows(qrows), _rows(kcols)
+        nq = N if qr is None else qr.size
+        nk = N if kc is None else kc.size
+        dq = np.empty((BH, nq, d), np.float64) if want_dq else None
+        dk = np.empty((BH, nk, d), np.float64) if want_dkv else None
+        dv = np.empty((BH, nk, d), np.float64) if want_dkv else None
+        rc = self.lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d,
+                                      int(bool(causal)), float(scale),
+                                      _ptr(qr), 0 if qr is None else qr.size,
+                                      _ptr(kc), 0 if kc is None else kc.size,
+                                      _ptr(dq), _ptr(dk), _ptr(dv))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_bwd failed (bad argument or out of memory)")
+        shp = lambda a, r: None if a is None else a.reshape(*lead, r, d)
+        return shp(dq, nq), shp(dk, nk), shp(dv, nk)
+
+
+def default() -> Oracle:
+    """The oracle built from this package's source (compiled on first use)."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP loops run on."""
+    return default().num_threads()
+
+
+def attn_fwd(q, k, v, causal: bool, scale: float, rows=None):
+    return default().attn_fwd(q, k, v, causal, scale, rows)
+
+
+def attn_bwd(q, k, v, dout, causal: bool, scale: float, qrows=None, kcols=None,
+             want_dq: bool = True, want_dkv: bool = True):
+    return default().attn_bwd(q, k, v, dout, causal, scale, qrows, kcols, want_dq, want_dkv)
+
+
+attn_fwd.__doc__ = Oracle.attn_fwd.__doc__
+attn_bwd.__doc__ = Oracle.attn_bwd.__doc__

@@ -1,0 +1,329 @@
+"""Checks that pin the FP64 oracle to facts fixed outside it.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+if the oracle disagrees with a closed form, a brute-force evaluation, an
+identity the pages state, or an independent library evaluation.  The test
+suite runs every pin on the real oracle (all must pass) and on deliberately
+broken builds of the oracle (each must be caught by at least one pin).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "closed_form_fwd.json")
+
+_EXPR_NAMES = {"log": math.log, "exp": math.exp, "sqrt": math.sqrt}
+
+
+def _expr(x) -> float:
+    """Evaluate a fixture entry: a number, or an expression in log/exp/sqrt."""
+    if isinstance(x, (int, float)):
+        return float(x)
+    return float(eval(str(x), {"__builtins__": {}}, dict(_EXPR_NAMES)))
+
+
+def _arr(rows):
+    return np.array([[_expr(x) for x in r] for r in rows], dtype=np.float64)
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    assert np.all(np.isfinite(a)), f"{what}: non-finite values"
+    err = np.max(np.abs(a - b) / np.maximum(1.0, np.abs(b))) if a.size else 0.0
+    assert err <= tol, f"{what}: error {err:.3e} > {tol:.1e}"
+
+
+# ---------------------------------------------------------------------------
+# forward pins
+
+
+def pin_golden_closed_forms(orc):
+    """Hand-derived cases (tests/golden/closed_form_fwd.json)."""
+    cases = json.load(open(GOLDEN))["cases"]
+    for c in cases:
+        q, k, v = _arr(c["q"]), _arr(c["k"]), _arr(c["v"])
+        o, lse = orc.attn_fwd(q, k, v, c["causal"], c["scale"])
+        _close(o, _arr(c["o"]), 1e-12, c["name"] + " O")
+        _close(lse, np.array([_expr(x) for x in c["lse"]]), 1e-12, c["name"] + " LSE")
+
+
+def brute_force_fwd(q, k, v, causal, scale):
+    """exp(S)/sum exp(S) with Python floats, no max subtraction (small scores only)."""
+    N, d = len(q), len(q[0])
+    o, lse = [], []
+    for i in range(N):
+        keys = range(i + 1) if causal else range(len(k))
+        w = {}
+        for j in keys:
+            w[j] = math.exp(scale * math.fsum(q[i][t] * k[j][t] for t in range(d)))
+        z = math.fsum(w.values())
+        o.append([math.fsum(w[j] * v[j][t] for j in keys) / z for t in range(len(v[0]))])
+        lse.append(math.log(z))
+    return np.array(o), np.array(lse)
+
+
+def pin_brute_force(orc):
+    """Direct softmax on tiny inputs in pure-Python float64."""
+    rng = np.random.default_rng(11)
+    for (N, Nk, d, causal) in [(4, 4, 4, False), (4, 4, 4, True), (5, 3, 2, False),
+                               (6, 6, 3, True), (1, 1, 5, True), (3, 7, 1, False)]:
+        q = rng.uniform(-1.5, 1.5, (N, d))
+        k = rng.uniform(-1.5, 1.5, (Nk, d))
+        v = rng.uniform(-2, 2, (Nk, d))
+        scale = 1.0 / math.sqrt(d)
+        o_ref, lse_ref = brute_force_fwd(q.tolist(), k.tolist(), v.tolist(), causal, scale)
+        o, lse = orc.attn_fwd(q, k, v, causal, scale)
+        _close(o, o_ref, 1e-12, f"brute force O {N}x{Nk}x{d} causal={causal}")
+        _close(lse, lse_ref, 1e-12, f"brute force LSE {N}x{Nk}x{d} causal={causal}")
+
+
+def pin_rows_sum_to_one(orc):
+    """With V = I the output is P itself: rows sum to 1, entries >= 0, masked ones exactly 0."""
+    rng = np.random.default_rng(12)
+    for causal in (False, True):
+        N = d = 9
+        q = rng.normal(size=(N, d)) * 3
+        k = rng.normal(size=(N, d)) * 3
+        P, _ = orc.attn_fwd(q, k, np.eye(N), causal, 0.7)
+        _close(P.sum(axis=1), np.ones(N), 1e-12, "row sums of P")
+        assert np.all(P >= 0.0), "P has negative entries"
+        if causal:
+            assert np.all(np.triu(P, 1) == 0.0), "causal P has weight above the diagonal"
+
+
+def pin_equal_scores(orc):
+    """Q = 0: every score is 0, so O_i is the mean of the visible V rows and LSE_i = ln(#visible)."""
+    rng = np.random.default_rng(13)
+    N, d = 23, 6
+    k = rng.normal(size=(N, d))
+    v = rng.normal(size=(N, d))
+    o, lse = orc.attn_fwd(np.zeros((N, d)), k, v, False, 0.3)
+    _close(o, np.broadcast_to(v.mean(axis=0), (N, d)), 1e-12, "Q=0 non-causal O")
+    _close(lse, np.full(N, math.log(N)), 1e-12, "Q=0 non-causal LSE")
+    o, lse = orc.attn_fwd(np.zeros((N, d)), k, v, True, 0.3)
+    mean_prefix = np.cumsum(v, axis=0) / np.arange(1, N + 1)[:, None]
+    _close(o, mean_prefix, 1e-12, "Q=0 causal O")
+    _close(lse, np.log(np.arange(1, N + 1)), 1e-12, "Q=0 causal LSE")
+
+
+def merge_states(a, b):
+    """Two-block merge of (m, l, O) with O normalised, as the huaweicloud page's section two
+    states it: m = max(mA, mB); l = e^(mA-m) lA + e^(mB-m) lB;
+    O = (lA e^(mA-m) OA + lB e^(mB-m) OB) / l."""
+    (ma, la, oa), (mb, lb, ob) = a, b
+    m = np.maximum(ma, mb)
+    ea = np.where(np.isneginf(ma), 0.0, np.exp(ma - m))
+    eb = np.where(np.isneginf(mb), 0.0, np.exp(mb - m))
+    l = ea * la + eb * lb
+    o = ((la * ea)[:, None] * oa + (lb * eb)[:, None] * ob) / l[:, None]
+    return m, l, o
+
+
+def pin_merge_rule(orc):
+    """Oracle on key blocks, merged by the page's rule, equals the oracle on all keys
+    (two blocks, and k blocks merged one after another as in the induction argument)."""
+    rng = np.random.default_rng(14)
+    N, Nk, d = 17, 41, 8
+    q = rng.normal(size=(N, d)) * 2
+    k = rng.normal(size=(Nk, d)) * 2
+    v = rng.normal(size=(Nk, d))
+    scale = 1 / math.sqrt(d)
+    o_full, lse_full = orc.attn_fwd(q, k, v, False, scale)
+
+    def state(lo, hi):
+        o, lse = orc.attn_fwd(q, k[lo:hi], v[lo:hi], False, scale)
+        return lse, np.ones(N), o          # (m, l) = (LSE, 1) represents the same block
+
+    for cut in (1, 16, 40):
+        m, l, o = merge_states(state(0, cut), state(cut, Nk))
+        _close(o, o_full, 1e-12, f"two-block merge O (cut {cut})")
+        _close(m + np.log(l), lse_full, 1e-12, f"two-block merge LSE (cut {cut})")
+    # k blocks, starting from the initial state O = 0, l = 0, m = -inf
+    st = (np.full(N, -np.inf), np.zeros(N), np.zeros((N, d)))
+    for lo in range(0, Nk, 7):
+        st = merge_states(st, state(lo, min(lo + 7, Nk)))
+    _close(st[2], o_full, 1e-12, "k-block merge O")
+    _close(st[0] + np.log(st[1]), lse_full, 1e-12, "k-block merge LSE")
+
+
+def online_simulator(q, k, v, causal, scale, br, bc, deferred):
+    """FP64 restatement of the tiled forward that the huaweicloud page's section three
+    simulates: K/V blocks outer, Q blocks inner, running (m, l, O) per row with the
+    rescale factor exp(m_prev - m_new).  deferred=False keeps O normalised after every
+    block (the page's simulator); deferred=True keeps it unnormalised and divides by l
+    once at the end (the second-generation ordering)."""
+    N, d = q.shape
+    Nk = k.shape[0]
+    O = np.zeros((N, d))
+    l = np.zeros(N)
+    m = np.full(N, -np.inf)
+    for j in range(0, Nk, bc):
+        for i in range(0, N, br):
+            s = scale * q[i:i + br] @ k[j:j + bc].T
+            if causal:
+                rows = np.arange(i, min(i + br, N))[:, None]
+                cols = np.arange(j, min(j + bc, Nk))[None, :]
+                s = np.where(cols > rows, -np.inf, s)
+            m_prev, l_prev = m[i:i + br], l[i:i + br]
+            m_new = np.maximum(m_prev, s.max(axis=1))
+            p = np.exp(s - m_new[:, None])
+            alpha = np.where(np.isneginf(m_prev), 0.0, np.exp(m_prev - m_new))
+            l_new = alpha * l_prev + p.sum(axis=1)
+            if deferred:
+                O[i:i + br] = alpha[:, None] * O[i:i + br] + p @ v[j:j + bc]
+            else:
+                O[i:i + br] = ((alpha * l_prev)[:, None] * O[i:i + br] + p @ v[j:j + bc]) / l_new[:, None]
+            m[i:i + br], l[i:i + br] = m_new, l_new
+    if deferred:
+        O = O / l[:, None]
+    return O, m + np.log(l)
+
+
+def pin_online_recurrence(orc):
+    """The online-softmax recurrence, run block by block, reaches the oracle's exact result."""
+    rng = np.random.default_rng(15)
+    for (N, d, br, bc, causal) in [(37, 8, 8, 16, False), (37, 8, 16, 8, True), (64, 4, 64, 1, True)]:
+        q = rng.normal(size=(N, d)) * 3
+        k = rng.normal(size=(N, d)) * 3
+        v = rng.normal(size=(N, d))
+        o_ref, lse_ref = orc.attn_fwd(q, k, v, causal, 0.5)
+        for deferred in (False, True):
+            o, lse = online_simulator(q, k, v, causal, 0.5, br, bc, deferred)
+            _close(o_ref, o, 1e-12, f"online recurrence O (deferred={deferred}, causal={causal})")
+            _close(lse_ref, lse, 1e-12, f"online recurrence LSE (deferred={deferred}, causal={causal})")
+
+
+def pin_one_hot_large_scores(orc):
+    """A key boosted by ~1000 wins every row outright: O_i = V_j* and LSE_i = S_ij* exactly
+    in float64 (every other term is below e^-900, which underflows to 0 next to 1)."""
+    rng = np.random.default_rng(16)
+    N, d = 33, 16
+    q = rng.normal(size=(N, d))
+    k = rng.normal(size=(N, d))
+    v = rng.normal(size=(N, d))
+    q[:, d - 1] = 1.0
+    js = N - 1
+    k[js, d - 1] = 1000.0 * math.sqrt(d)
+    scale = 1 / math.sqrt(d)
+    o, lse = orc.attn_fwd(q, k, v, False, scale)
+    _close(o, np.broadcast_to(v[js], (N, d)), 1e-12, "one-hot O")
+    s_star = np.array([scale * math.fsum(q[i] * k[js]) for i in range(N)])
+    _close(lse, s_star, 1e-12, "one-hot LSE")
+    # scores of several hundred both ways stay finite
+    o, lse = orc.attn_fwd(q * 20, k * 20, v, False, scale)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), "large scores overflowed"
+    assert np.max(np.abs(lse)) > 300, "the large-score case did not reach large scores"
+
+
+def pin_causal_first_row(orc):
+    """Causal row 0 sees only key 0: O_0 = V_0, LSE_0 = S_00; N = 1 gives O = V."""
+    rng = np.random.default_rng(17)
+    N, d = 12, 5
+    q, k, v = (rng.normal(size=(N, d)) for _ in range(3))
+    o, lse = orc.attn_fwd(q, k, v, True, 0.9)
+    _close(o[0], v[0], 1e-12, "causal O_0")
+    _close(lse[0], 0.9 * math.fsum(q[0] * k[0]), 1e-12, "causal LSE_0")
+    o, lse = orc.attn_fwd(q[:1], k[:1], v[:1], False, 0.9)
+    _close(o, v[:1], 1e-12, "N=1 O")
+
+
+def pin_permutation_symmetry(orc):
+    """Non-causal attention does not depend on the order of the (key, value) pairs."""
+    rng = np.random.default_rng(18)
+    N, d = 19, 7
+    q, k, v = (rng.normal(size=(N, d)) for _ in range(3))
+    perm = rng.permutation(N)
+    o1, l1 = orc.attn_fwd(q, k, v, False, 0.4)
+    o2, l2 = orc.attn_fwd(q, k[perm], v[perm], False, 0.4)
+    _close(o1, o2, 1e-12, "permuted K/V O")
+    _close(l1, l2, 1e-12, "permuted K/V LSE")
+
+
+def pin_sampled_rows(orc):
+    """Asking for a subset of rows or keys returns exactly those rows of the full result."""
+    rng = np.random.default_rng(19)
+    BH, N, d = 2, 21, 4
+    q, k, v, do = (rng.normal(size=(BH, N, d)) for _ in range(4))
+    rows = [20, 0, 7, 7]
+    for causal in (False, True):
+        o, lse = orc.attn_fwd(q, k, v, causal, 0.5)
+        os_, ls_ = orc.attn_fwd(q, k, v, causal, 0.5, rows=rows)
+        assert np.array_equal(os_, o[:, rows]) and np.array_equal(ls_, lse[:, rows])
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, causal, 0.5)
+        dqs, dks, dvs = orc.attn_bwd(q, k, v, do, causal, 0.5, qrows=rows, kcols=[3, 20])
+        assert np.array_equal(dqs, dq[:, rows])
+        assert np.array_equal(dks, dk[:, [3, 20]]) and np.array_equal(dvs, dv[:, [3, 20]])
+
+
+# ---------------------------------------------------------------------------
+# backward pins
+
+
+def pin_bwd_finite_differences(orc):
+    """Central differences of L = sum(dO * O), O from the oracle's forward, match the gradients."""
+    rng = np.random.default_rng(20)
+    for causal in (False, True):
+        N, d = 6, 3
+        q, k, v, do = (rng.normal(size=(N, d)) for _ in range(4))
+        scale = 0.8
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, causal, scale)
+        h = 1e-6
+        for name, x, g in (("dQ", q, dq), ("dK", k, dk), ("dV", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = {"dQ": (xp, k, v), "dK": (q, xp, v), "dV": (q, k, xp)}[name]
+                args_m = {"dQ": (xm, k, v), "dK": (q, xm, v), "dV": (q, k, xm)}[name]
+                lp = np.sum(do * orc.attn_fwd(*args_p, causal, scale)[0])
+                lm = np.sum(do * orc.attn_fwd(*args_m, causal, scale)[0])
+                num[idx] = (lp - lm) / (2 * h)
+            err = np.max(np.abs(num - g)) / max(1e-3, np.max(np.abs(g)))
+            assert err < 1e-6, f"{name} vs finite differences (causal={causal}): {err:.2e}"
+
+
+def pin_bwd_invariants(orc):
+    """Rows of P sum to 1, so sum_j dV_j = sum_i dO_i; rows of dS sum to 0, so sum_j dK_j = 0."""
+    rng = np.random.default_rng(21)
+    for causal in (False, True):
+        N, d = 29, 8
+        q, k, v, do = (rng.normal(size=(N, d)) * 2 for _ in range(4))
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, causal, 0.35)
+        _close(dv.sum(axis=0), do.sum(axis=0), 1e-11, f"sum dV = sum dO (causal={causal})")
+        assert np.max(np.abs(dk.sum(axis=0))) < 1e-11 * max(1.0, np.abs(dk).max()), \
+            f"sum dK != 0 (causal={causal})"
+
+
+def pin_bwd_autograd(orc):
+    """FP64 torch autograd through an explicit softmax formula (an independent library path)."""
+    rng = np.random.default_rng(22)
+    for causal in (False, True):
+        N, d = 13, 6
+        arrs = [rng.normal(size=(2, N, d)) for _ in range(4)]
+        q, k, v = (torch.tensor(a, requires_grad=True) for a in arrs[:3])
+        do = torch.tensor(arrs[3])
+        s = 0.45 * q @ k.transpose(-1, -2)
+        if causal:
+            s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+        o = torch.softmax(s, dim=-1) @ v
+        (o * do).sum().backward()
+        dq, dk, dv = orc.attn_bwd(arrs[0], arrs[1], arrs[2], arrs[3], causal, 0.45)
+        _close(dq, q.grad.numpy(), 1e-10, "dQ vs autograd")
+        _close(dk, k.grad.numpy(), 1e-10, "dK vs autograd")
+        _close(dv, v.grad.numpy(), 1e-10, "dV vs autograd")
+
+
+ALL_PINS = [
+    pin_golden_closed_forms, pin_brute_force, pin_rows_sum_to_one, pin_equal_scores,
+    pin_merge_rule, pin_online_recurrence, pin_one_hot_large_scores, pin_causal_first_row,
+    pin_permutation_symmetry, pin_sampled_rows, pin_bwd_finite_differences,
+    pin_bwd_invariants, pin_bwd_autograd,
+]

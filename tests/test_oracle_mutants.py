@@ -1,0 +1,46 @@
+"""Plant plausible mistakes in a private copy of the oracle's C source and check that
+the pins catch every one of them (a pin that passes a broken oracle pins nothing)."""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+# (description, text in attn_oracle.c, replacement)
+MUTANTS = [
+    ("softmax scale dropped", "s[j] = scale * acc;", "s[j] = acc;"),
+    ("no division by l", "double p = exp(s[j] - m) / l;", "double p = exp(s[j] - m);"),
+    ("LSE without the max", "lse[bh * nout + r] = m + log(l);", "lse[bh * nout + r] = log(l);"),
+    ("l without the max shift", "l += exp(s[j] - m);", "l += exp(s[j]);"),
+    ("causal mask one key late", "return causal ? (i + 1) : N;",
+     "return causal ? (i + 2 > N ? N : i + 2) : N;"),
+    ("V rows reversed", "const double *vj = vh + j * d;", "const double *vj = vh + (nk - 1 - j) * d;"),
+    ("dP with transposed indices", "dp += doh[i * d + t] * vh[j * d + t];",
+     "dp += doh[j * d + t] * vh[i * d + t];"),
+    ("dS sign flipped", "double ds = p * (dp - c[i]);", "double ds = p * (c[i] - dp);"),
+    ("dS without the row term", "double ds = p * (dp - c[i]);", "double ds = p * dp;"),
+    ("row term without P", "acc += p * dp;", "acc += dp;"),
+    ("dV from Q instead of dO", "gv[t] += p * doh[i * d + t];", "gv[t] += p * qh[i * d + t];"),
+    ("dK without scale", "gk[t] += scale * ds * qh[i * d + t];", "gk[t] += ds * qh[i * d + t];"),
+    ("dQ from V instead of K", "g[t] += scale * ds * kh[j * d + t];", "g[t] += scale * ds * vh[j * d + t];"),
+    ("causal backward sees every query", "int64_t i0 = causal ? j : 0;", "int64_t i0 = 0;"),
+]
+
+
+@pytest.mark.parametrize("desc,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, desc, old, new):
+    src = open(oracle.SOURCE).read()
+    assert old in src, f"mutation site for '{desc}' not found in the oracle source"
+    mutated = src.replace(old, new)
+    c_path = os.path.join(tmp_path, "mutant.c")
+    open(c_path, "w").write(mutated)
+    lib = oracle.build(force=True, src=c_path, out=os.path.join(tmp_path, "libmutant.so"))
+    orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, RuntimeError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the mutant '{desc}'"
