@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark: one training-step attention pass (forward + backward) per step.
+
+Workload (the fwd/bwd configuration): B=2, H=16, N=8192, d=128, BF16, causal,
+Q, K, V, dO iid N(0,1) from a fixed seed.  One step = attn_fwd followed by the
+three backward stages (prepare, dK/dV, dQ) through the C ABI, inputs resident
+in HBM.  FLOPs per step are the algorithmic count: forward 4*B*H*N^2*d plus
+backward 10*B*H*N^2*d, both halved for causal.  The inputs (4 x 64 MiB) exceed
+the 129 MB L2, so no flush runs between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
+workload (the heads are independent; there is no exchange step), the elapsed
+time is the max over ranks and `value` counts the work of all ranks.
+`--impl reference` times the FP64 CPU oracle on a bounded slice of the same
+workload (rank 0 only).
+
+Prints ONE JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s (4*B*H*N^2*d fwd + 10*B*H*N^2*d bwd, halved causal) at 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD = "c5"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true", help="skip the long-sequence forward side numbers")
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def config_dict(w, n_gpus):
+    return {"workload": f"training-step attention B={w.B} H={w.H} N={w.N} d={w.d} {w.dtype} causal fwd+bwd",
+            "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": True, "dtype": w.dtype,
+            "parallelism": f"replicas x{n_gpus}" if n_gpus > 1 else "single GPU",
+            "l2": "no flush: inputs 256 MiB > 129 MB L2"}
+
+
+def step_flops(w):
+    return workloads.fwd_flops(w.B, w.H, w.N, w.d, True) + workloads.bwd_flops(w.B, w.H, w.N, w.d, True)
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9 or not (t0 - 0.05 <= ts <= t1 + 0.15):
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- peaks and profiles
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tiled_online_softmax_attention_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel)
+    if not ent or ent.get("source_digest") != source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- our arm
+
+
+def run_ours(args, w, ws_, rank, local):
+    import tiled_online_softmax_attention_gb300 as attn
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    attn.load(build_if_missing=True)
+    x = workloads.inputs(WORKLOAD)
+    B, H, N, d = w.B, w.H, w.N, w.d
+    scale = w.scale
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    wsp = torch.empty(nbytes, device=dev, dtype=torch.uint8)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    dt = q.dtype
+
+    def check(rc, what):
+        if rc != attn.ATTN_OK:
+            raise RuntimeError(f"{what}: {attn.attn_status_string(rc)}")
+
+    names = ["fwd", "bwd_prepare", "bwd_dkdv", "bwd_dq"]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        check(attn.attn_fwd(q, k, v, o, lse, B, H, N, d, dt, True, scale, status, stream), "attn_fwd")
+        if ev is not None:
+            ev[1].record(stream)
+        check(attn.attn_bwd_prepare(o, do, lse, wsp, nbytes, B, H, N, d, dt, stream), "attn_bwd_prepare")
+        if ev is not None:
+            ev[2].record(stream)
+        check(attn.attn_bwd_dkdv(q, k, v, do, wsp, nbytes, dk, dv, B, H, N, d, dt, True, scale, status, stream),
+              "attn_bwd_dkdv")
+        if ev is not None:
+            ev[3].record(stream)
+        check(attn.attn_bwd_dq(q, k, v, do, wsp, nbytes, dq, B, H, N, d, dt, True, scale, status, stream),
+              "attn_bwd_dq")
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler is not None:
+        time.sleep(0.3)
+    barrier(ws_)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(ws_)
+    clocks = sampler.stop(wall0, wall1) if sampler is not None else None
+    if int(status.item()) != 0:
+        raise RuntimeError("device-side wait expired in the timed region")
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = allreduce_max(elapsed_ms, ws_, dev)
+    per_kernel = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / args.steps for j, n in enumerate(names)}
+
+    # Algorithmic FLOPs per launch (causal halves every N x N product):
+    unit = 2.0 * B * H * N * N * d / 2          # one N x N x d product, causal
+    kflops = {"fwd": 2 * unit, "bwd_prepare": 0.0, "bwd_dkdv": 4 * unit, "bwd_dq": 1 * unit}
+    kbytes = {"bwd_prepare": 2 * B * H * N * d * 2 + B * H * N * 4 + nbytes}   # read O, dO, lse; write D, LSE2
+    flops = step_flops(w)
+    value = ws_ * args.steps * flops / (elapsed_ms * 1e-3) / 1e12
+    pk = peaks()
+    dom = max(per_kernel, key=per_kernel.get)
+    achieved = kflops[dom] / (per_kernel[dom] * 1e-3) / 1e12
+    roofline = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                "traffic": recorded_traffic(dom), "peak_source": pk["source"] + " bf16 burst",
+                "flops_per_launch": kflops[dom]}
+    kernels = {}
+    for n in names:
+        ent = {"ms": round(per_kernel[n], 4)}
+        if kflops[n]:
+            ent["tflops"] = round(kflops[n] / (per_kernel[n] * 1e-3) / 1e12, 1)
+            ent["frac_of_peak"] = round(kflops[n] / (per_kernel[n] * 1e-3) / 1e12 / pk["bf16_tflops"], 4)
+        else:
+            ent["gbs"] = round(kbytes[n] / (per_kernel[n] * 1e-3) / 1e9, 1)
+        kernels[n] = ent
+
+    e2e = run_e2e(args, w, x, dev, ws_)
+    extra = None if args.no_extra else long_forward(attn, dev)
+    return {"value": value, "ms_per_step": elapsed_ms / args.steps, "roofline": roofline, "kernels": kernels,
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 4 * args.steps, "extra": extra}
+
+
+def run_e2e(args, w, x, dev, ws_):
+    """Same metric through the public API with host buffers: pinned H2D of Q, K, V, dO and D2H of the
+    three gradients inside the timed region, every step."""
+    import tiled_online_softmax_attention_gb300 as attn
+
+    hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dout"))
+    outs = [torch.empty_like(hq).pin_memory() for _ in range(3)]
+    steps = max(3, min(args.steps, 50))
+
+    def one():
+        q, k, v, do = (t.to(dev, non_blocking=True) for t in (hq, hk, hv, hdo))
+        o, lse = attn.forward(q, k, v, causal=True, scale=w.scale)
+        g = attn.backward(q, k, v, o, lse, do, causal=True, scale=w.scale)
+        for h, t in zip(outs, g):
+            h.copy_(t, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    barrier(ws_)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = allreduce_max(a.elapsed_time(b), ws_, dev)
+    nb = hq.numel() * hq.element_size()
+    return {"value": ws_ * steps * step_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": 4 * nb, "d2h_bytes_per_step": 3 * nb, "steps": steps}
+
+
+def long_forward(attn, dev):
+    """Side numbers: the long-sequence forward (B=1, H=32, N=16384, d=128, bf16), both masks."""
+    w = workloads.WORKLOADS["c3"]
+    x = workloads.inputs("c3")
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    out = {}
+    for causal in (False, True):
+        f = workloads.fwd_flops(w.B, w.H, w.N, w.d, causal)
+        for _ in range(3):
+            attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, causal, w.scale)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record()
+        for _ in range(reps):
+            attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, causal, w.scale)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        out["causal" if causal else "non_causal"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+    return {"long_forward_B1_H32_N16384_d128": out}
+
+
+# ---------------------------------------------------------------- oracle (CPU) timings
+
+
+def oracle_slice(x, b, h, n_tok):
+    """The causal top-left n_tok x n_tok block of one head: exactly the work its first n_tok queries do."""
+    return tuple(x[n][b, h, :n_tok] for n in ("q", "k", "v", "dout"))
+
+
+def time_oracle(x, w, heads, n_tok):
+    import oracle
+
+    t0 = time.perf_counter()
+    for (b, h) in heads:
+        q, k, v, do = oracle_slice(x, b, h, n_tok)
+        oracle.attn_fwd(q, k, v, True, w.scale)
+        oracle.attn_bwd(q, k, v, do, True, w.scale)
+    sec = time.perf_counter() - t0
+    flops = len(heads) * (workloads.fwd_flops(1, 1, n_tok, w.d, True) + workloads.bwd_flops(1, 1, n_tok, w.d, True))
+    return sec, flops
+
+
+def cpu_baseline(x, w):
+    import oracle
+
+    heads, n_tok = [(0, 0)], 4096
+    sec, flops = time_oracle(x, w, heads, n_tok)
+    return {"value": flops / sec / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"FP64 oracle forward+backward on head (0,0), first {n_tok} tokens (causal top-left block), "
+                      f"{sec:.1f} s"}
+
+
+def run_reference(args, w):
+    import oracle
+
+    x = workloads.inputs(WORKLOAD)
+    n_tok = 2048
+    for i in range(args.warmup):
+        time_oracle(x, w, [(0, i % w.H)], n_tok)
+    total_s, total_f = 0.0, 0.0
+    for i in range(args.steps):
+        s, f = time_oracle(x, w, [(i // w.H % w.B, i % w.H)], n_tok)
+        total_s += s
+        total_f += f
+    value = total_f / total_s / 1e12
+    sample = f"FP64 oracle forward+backward, one head per step, first {n_tok} tokens (causal top-left block)"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+_PG = None
+
+
+def init_dist(ws_, local):
+    global _PG
+    if ws_ > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        _PG = dist
+
+
+def barrier(ws_):
+    if ws_ > 1 and _PG is not None:
+        _PG.barrier()
+
+
+def allreduce_max(val: float, ws_, dev):
+    if ws_ > 1 and _PG is not None:
+        t = torch.tensor([val], dtype=torch.float64, device=dev)
+        _PG.all_reduce(t, op=_PG.ReduceOp.MAX)
+        return float(t.item())
+    return val
+
+
+def main():
+    args = parse()
+    ws_, rank, local = dist_env()
+    w = workloads.WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    init_dist(ws_, local)
+    r = run_ours(args, w, ws_, rank, local)
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(r["value"], 2), "unit": UNIT, "n_gpus": ws_, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(r["ms_per_step"], 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config_dict(w, ws_), "roofline": r["roofline"], "kernels": r["kernels"],
+                "e2e": r["e2e"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
+        if r["extra"]:
+            line["extra"] = r["extra"]
+        if ws_ == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(workloads.inputs(WORKLOAD), w)
+        print(json.dumps(line), flush=True)
+    if ws_ > 1 and _PG is not None:
+        _PG.barrier()
+        _PG.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) tiled online-softmax attention library.
+ *
+ * Exact scaled-dot-product attention over [B, H, N, d] tensors:
+ *
+ *   O = softmax(scale * Q K^T) V
+ *
+ * ("FlashAttention hardware-aware analysis" (huaweicloud), section one, part 2,
+ * and the PyTorch scaled_dot_product_attention call of section five, part 1,
+ * whose [Batch, Heads, Seq_Len, Head_Dim] layout and is_causal flag this ABI
+ * keeps.)  The forward pass streams K/V tiles through the online-softmax
+ * recurrence (running row max m and row sum l, partial output rescaled by
+ * exp(m_old - m_new); huaweicloud page, section two; "Understanding online
+ * softmax in Flash Attention from scratch", section 3.1), defers the 1/l
+ * normalisation to the end, and saves the per-row logsumexp.  The backward
+ * pass recomputes P tile by tile from that logsumexp ("Understanding
+ * FlashAttention, Part 2", section 2.4; huaweicloud page, section four,
+ * part 1: recomputation) and never stores an N x N matrix.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are dense, row-major [B][H][N][d] with d fastest ("contiguous"),
+ *    in the 16-bit type given by `dt`.  lse is float32 [B][H][N].
+ *  - All pointers are DEVICE pointers on the current CUDA device unless stated.
+ *    Every base pointer must be 16-byte aligned.  The caller owns all memory;
+ *    the library allocates nothing on the device and keeps no state between
+ *    calls.
+ *  - d must be 64 or 128 (the head dimensions the huaweicloud page's section
+ *    five, part 2 recommends); anything else returns ATTN_ERR_UNSUPPORTED.
+ *    N >= 1 may be any value (ragged last tiles are masked, never padded in
+ *    memory).  B, H >= 1 and B*H*N*d < 2^31.
+ *  - causal != 0 keeps key j for query i iff j <= i (the lower triangle,
+ *    huaweicloud page, section five, part 3); tiles wholly above the
+ *    diagonal are skipped, not masked.
+ *  - scale multiplies Q K^T; pass 1/sqrt(d) for standard attention.  It must
+ *    be finite and positive.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Argument errors are returned before anything is
+ *    launched.  A launch failure returns ATTN_ERR_CUDA.
+ *  - dev_status (nullable) is a device int the caller zeroes; a kernel whose
+ *    bounded wait on an mbarrier expires (a hardware or library fault, never
+ *    a normal outcome) stores ATTN_ERR_TIMEOUT there, abandons its tile and
+ *    exits cleanly.  Read it after synchronising the stream.
+ *  - On any error the output buffers' contents are unspecified.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad scale, ws too small */
+    ATTN_ERR_UNSUPPORTED = 2,   /* d not in {64, 128}, unknown dtype, device is not sm_103 */
+    ATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call or a launch failed */
+    ATTN_ERR_TIMEOUT = 4        /* (device-side only) a bounded wait expired */
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- forward pass.
+ *   q, k, v : [B][H][N][d] inputs (read only).
+ *   o       : [B][H][N][d] output, O = softmax(scale*QK^T) V rounded to dt.
+ *   lse     : [B][H][N] float32 output, natural-log logsumexp of the scaled
+ *             scores of each row, lse_i = m_i + ln l_i (the saved statistics
+ *             of "Understanding FlashAttention, Part 2", section 2.2).
+ *   o and lse must not overlap the inputs.
+ */
+ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                     int *dev_status, void *stream);
+
+/*
+ * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd needs:
+ * two float32 vectors per row (D_i = rowsum(dO_i * O_i), and the logsumexp in
+ * base 2), padded to whole 128-row tiles: 2 * B*H*ceil(N/128)*128 * 4 bytes.
+ * Returns 0 for invalid sizes.
+ */
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * attn_bwd -- backward pass: gradients of a loss L given dout = dL/dO.
+ *   q, k, v, o, dout : [B][H][N][d] (o is the output of attn_fwd on q, k, v).
+ *   lse              : [B][H][N] float32 from the same attn_fwd call.
+ *   dq, dk, dv       : [B][H][N][d] outputs in dt:
+ *                        dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+ *                        dQ = scale dS K,  dK = scale dS^T Q,
+ *                      with D_i = rowsum(dO_i * O_i) and P recomputed from lse
+ *                      ("Understanding FlashAttention, Part 2", section 2.4,
+ *                      Figs 16-20).
+ *   workspace        : device scratch of at least attn_bwd_workspace_bytes();
+ *                      16-byte aligned; contents need not be initialised and
+ *                      are clobbered.  The caller owns it.
+ *   Outputs must not overlap inputs or each other.
+ */
+ATTN_API attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                     void *workspace, size_t workspace_bytes,
+                     int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                     int *dev_status, void *stream);
+
+/*
+ * The three stages attn_bwd runs, in order, on one stream.  They are exported
+ * so that a caller can time them one by one or run the two independent
+ * gradient stages on two streams once the preparation has finished.  Argument
+ * meanings, layouts and errors are those of attn_bwd.
+ *
+ * attn_bwd_prepare -- fills the workspace: D_i = rowsum(dO_i * O_i) (the
+ *   softmax-Jacobian row term of "Understanding FlashAttention, Part 2",
+ *   section 2.4, Fig 18) and the logsumexp in base 2, for every row; rows of
+ *   the last partial 128-row tile get D = 0 and an infinite logsumexp.
+ * attn_bwd_dkdv -- dK and dV, one 128-key tile per CTA (reads the workspace).
+ * attn_bwd_dq   -- dQ, one 128-query tile per CTA (reads the workspace).
+ */
+ATTN_API attn_status attn_bwd_prepare(const void *o, const void *dout, const float *lse,
+                             void *workspace, size_t workspace_bytes,
+                             int B, int H, int N, int d, attn_dtype dt, void *stream);
+ATTN_API attn_status attn_bwd_dkdv(const void *q, const void *k, const void *v, const void *dout,
+                          const void *workspace, size_t workspace_bytes, void *dk, void *dv,
+                          int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                          int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_dq(const void *q, const void *k, const void *v, const void *dout,
+                        const void *workspace, size_t workspace_bytes, void *dq,
+                        int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                        int *dev_status, void *stream);
+
+/* attn_status_string -- a static, human-readable name for a status code. */
+ATTN_API const char *attn_status_string(attn_status s);
+
+/*
+ * attn_selftest_bounded_wait -- exercises the library's bounded mbarrier wait
+ * on the device: one tiny kernel waits on a barrier that nothing completes,
+ * gives up after `limit_ns` nanoseconds (clamped to [1 us, 1 s]) and stores
+ * ATTN_ERR_TIMEOUT into *dev_status (device int, must be non-null).  It
+ * checks the failure-reporting path without faulting or hanging the GPU.
+ */
+ATTN_API attn_status attn_selftest_bounded_wait(int *dev_status, uint64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,103 @@
+"""Helpers for the GPU parity tests: guarded output buffers, calls through the
+C ABI with a device status word, and the error measures the tolerances use."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import tiled_online_softmax_attention_gb300 as attn
+
+PAD = 4096                  # guard elements on each side of every output buffer
+SENTINEL16 = 0x7E5A         # a NaN pattern in both bf16 and fp16
+SENTINEL32 = 0x7FC5A5A5     # an fp32 NaN pattern
+
+# Tolerances (GPU result upcast to float64 against the float64 oracle).
+O_MAX_ABS = 1e-2
+LSE_REL = 1e-3              # |d lse| / max(|lse_ref|, 1)
+GRAD_REL_L2 = 2e-2
+
+
+class Guarded:
+    """An output tensor with sentinel-filled guard zones before and after it."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        n = int(np.prod(shape))
+        self.n = n
+        self.buf = torch.empty(n + 2 * PAD, dtype=dtype, device=device)
+        self.raw = self.buf.view(torch.int16 if dtype.itemsize == 2 else torch.int32)
+        s = SENTINEL16 if dtype.itemsize == 2 else SENTINEL32
+        if dtype.itemsize == 4:
+            s = s - (1 << 32) if s >= (1 << 31) else s
+        self.sentinel = s
+        self.raw.fill_(s)
+        self.t = self.buf[PAD:PAD + n].view(shape)
+
+    def intact(self) -> bool:
+        head = self.raw[:PAD]
+        tail = self.raw[PAD + self.n:]
+        return bool((head == self.sentinel).all().item() and (tail == self.sentinel).all().item())
+
+
+def run_fwd(q, k, v, causal, scale=None, stream=None):
+    """attn_fwd through the C ABI with guarded outputs; returns (o, lse) on the device."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = Guarded((B, H, N, d), q.dtype)
+    lse = Guarded((B, H, N), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd(q, k, v, o.t, lse.t, B, H, N, d, q.dtype, causal, scale, status, stream)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert o.intact() and lse.intact(), "the forward wrote outside its outputs"
+    return o.t, lse.t
+
+
+def run_bwd(q, k, v, o, lse, dout, causal, scale=None, stream=None):
+    """attn_bwd through the C ABI with guarded outputs; returns (dq, dk, dv)."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    outs = [Guarded((B, H, N, d), q.dtype) for _ in range(3)]
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_bwd(q, k, v, o, dout, lse, outs[0].t, outs[1].t, outs[2].t, ws.t, nbytes, B, H, N, d,
+                       q.dtype, causal, scale, status, stream)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert all(g.intact() for g in outs) and ws.intact(), "the backward wrote outside its buffers"
+    return tuple(g.t for g in outs)
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def o_err(o, ref):
+    return float(np.max(np.abs(f64(o) - ref))) if ref.size else 0.0
+
+
+def lse_err(lse, ref):
+    return float(np.max(np.abs(f64(lse) - ref) / np.maximum(np.abs(ref), 1.0))) if ref.size else 0.0
+
+
+def rel_l2(g, ref):
+    g = f64(g) if hasattr(g, "detach") else g
+    den = float(np.linalg.norm(ref))
+    return float(np.linalg.norm(g - ref)) / max(den, 1e-30)
+
+
+def sample_rows(N, extra=24, seed=0):
+    """Rows at both ends, on tile boundaries and at random."""
+    rows = {0, 1, N - 1, N - 2}
+    for t in range(128, N, 128):
+        rows.update({t - 1, t})
+    rows = sorted(r for r in rows if 0 <= r < N)
+    rng = np.random.default_rng(seed)
+    if len(rows) > 40:
+        rows = sorted(set(rng.choice(rows, 40, replace=False).tolist()) | {0, N - 1})
+    rows = sorted(set(rows) | set(rng.integers(0, N, extra).tolist()))
+    return np.array(rows, dtype=np.int64)

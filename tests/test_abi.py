@@ -1,0 +1,111 @@
+"""The C ABI without a GPU: the library builds for sm_103a, loads, exports every
+entry point include/attn.h declares, and rejects bad arguments before it touches
+CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tiled_online_softmax_attention_gb300 as attn
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "attn.h")
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(attn.EXPORTS)
+
+
+def test_library_loads_and_exports_every_symbol():
+    lib = attn.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_library_exports_nothing_else():
+    out = os.popen(f"nm -D --defined-only {attn.LIB_PATH}").read()
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert {s for s in exported if s.startswith("attn_")} == set(attn.EXPORTS)
+
+
+def test_status_strings():
+    assert attn.attn_status_string(0) == "ATTN_OK"
+    assert attn.attn_status_string(4) == "ATTN_ERR_TIMEOUT"
+    assert attn.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def test_workspace_size():
+    assert attn.attn_bwd_workspace_bytes(2, 16, 8192, 128) == 2 * 32 * 8192 * 4
+    assert attn.attn_bwd_workspace_bytes(2, 8, 4097, 128) == 2 * 16 * 4224 * 4
+    assert attn.attn_bwd_workspace_bytes(1, 1, 1, 64) == 2 * 128 * 4
+    assert attn.attn_bwd_workspace_bytes(1, 1, 0, 64) == 0
+    assert attn.attn_bwd_workspace_bytes(1, 1, 16, 96) == 0
+
+
+# fake, aligned, non-overlapping "device" addresses: validation fails before any CUDA call
+A = [0x10000000 * (i + 1) for i in range(12)]
+
+
+def fwd(**kw):
+    args = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], B=1, H=2, N=256, d=128, dt=0, causal=0, scale=0.088, stream=0)
+    args.update(kw)
+    return attn.attn_fwd(**args)
+
+
+def bwd(**kw):
+    args = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8],
+                workspace=A[9], workspace_bytes=1 << 20, B=1, H=2, N=256, d=128, dt=0, causal=1, scale=0.088, stream=0)
+    args.update(kw)
+    return attn.attn_bwd(**args)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=A[3] + 8), attn.ATTN_ERR_INVALID_ARG),          # misaligned
+    (dict(lse=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(N=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(dt=7), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=A[0]), attn.ATTN_ERR_INVALID_ARG),               # output aliases an input
+    (dict(B=1 << 12, H=1 << 12, N=1 << 8), attn.ATTN_ERR_INVALID_ARG),  # > 2^31 elements
+])
+def test_fwd_rejects(kw, status):
+    assert fwd(**kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dq=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=2 * 2 * 256 * 4 - 4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(dk=A[6]), attn.ATTN_ERR_INVALID_ARG),              # two outputs alias
+    (dict(dv=A[2]), attn.ATTN_ERR_INVALID_ARG),              # output aliases an input
+    (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),       # workspace aliases an input
+    (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
+])
+def test_bwd_rejects(kw, status):
+    assert bwd(**kw) == status
+
+
+def test_selftest_needs_status_pointer():
+    assert attn.attn_selftest_bounded_wait(None, 1000, stream=0) == attn.ATTN_ERR_INVALID_ARG
+
+
+def test_stage_entry_points_validate():
+    assert attn.attn_bwd_prepare(A[3], A[4], A[5], A[9], 16, 1, 2, 256, 128, 0, stream=0) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd_prepare(A[3], A[4], None, A[9], 1 << 20, 1, 2, 256, 128, 0, stream=0) == \
+        attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd_dkdv(A[0], A[1], A[2], A[4], A[9], 1 << 20, A[7], A[7], 1, 2, 256, 128, 0, 1, 0.1,
+                              stream=0) == attn.ATTN_ERR_INVALID_ARG      # dk == dv
+    assert attn.attn_bwd_dq(A[0], A[1], A[2], A[4], A[9], 1 << 20, A[6], 1, 2, 256, 80, 0, 1, 0.1,
+                            stream=0) == attn.ATTN_ERR_UNSUPPORTED

@@ -1,0 +1,202 @@
+"""Exact tiled online-softmax attention for one GB300 (sm_103a).
+
+A thin ctypes binding over ``libattn.so`` (the C ABI in ``include/attn.h``):
+argument marshalling only, every step of the computation runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing
+or cannot load, every call raises.
+
+Low level (same names and argument order as the C ABI; tensors may be passed
+where the C ABI takes device pointers, and ``stream=None`` means torch's
+current stream):
+
+    attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_bwd_workspace_bytes(B, H, N, d)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+             B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_bwd_prepare / attn_bwd_dkdv / attn_bwd_dq   (the three stages of attn_bwd)
+    attn_status_string(status)
+    attn_selftest_bounded_wait(dev_status, limit_ns, stream=None)
+
+Convenience wrappers over torch tensors of shape [B, H, N, d]:
+
+    forward(q, k, v, causal=False, scale=None)            -> (o, lse)
+    backward(q, k, v, o, lse, dout, causal=False, scale=None) -> (dq, dk, dv)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_CUDA = 3
+ATTN_ERR_TIMEOUT = 4
+ATTN_BF16 = 0
+ATTN_FP16 = 1
+
+LIB_PATH = _build.LIB
+EXPORTS = ("attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+           "attn_bwd_dq", "attn_status_string", "attn_selftest_bounded_wait")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {attn_status_string(status)}")
+
+
+def load(build_if_missing: bool = True):
+    """Load libattn.so (building it in-tree first if it is absent or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libattn.so not found at {LIB_PATH}; run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_fwd.restype = I
+    lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_bwd_workspace_bytes.restype = SZ
+    lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd.restype = I
+    lib.attn_bwd_prepare.argtypes = [P, P, P, P, SZ, I, I, I, I, I, P]
+    lib.attn_bwd_prepare.restype = I
+    lib.attn_bwd_dkdv.argtypes = [P, P, P, P, P, SZ, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_dkdv.restype = I
+    lib.attn_bwd_dq.argtypes = [P, P, P, P, P, SZ, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_dq.restype = I
+    lib.attn_status_string.argtypes = [I]
+    lib.attn_status_string.restype = ctypes.c_char_p
+    lib.attn_selftest_bounded_wait.argtypes = [P, ctypes.c_uint64, P]
+    lib.attn_selftest_bounded_wait.restype = I
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() or None
+    return int(x) or None
+
+
+def _stream(s):
+    if s is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream or None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream or None
+    return int(s) or None
+
+
+def _dt(x):
+    if isinstance(x, int):
+        return x
+    import torch
+
+    if x == torch.bfloat16:
+        return ATTN_BF16
+    if x == torch.float16:
+        return ATTN_FP16
+    raise ValueError(f"unsupported dtype {x}")
+
+
+def attn_status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                               _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_workspace_bytes(B, H, N, d) -> int:
+    return int(load().attn_bwd_workspace_bytes(int(B), int(H), int(N), int(d)))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, dt, causal, scale,
+             dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), _ptr(workspace), int(workspace_bytes), int(B), int(H), int(N), int(d),
+                               _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_prepare(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream=None) -> int:
+    return int(load().attn_bwd_prepare(_ptr(o), _ptr(dout), _ptr(lse), _ptr(workspace), int(workspace_bytes),
+                                       int(B), int(H), int(N), int(d), _dt(dt), _stream(stream)))
+
+
+def attn_bwd_dkdv(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, d, dt, causal, scale,
+                  dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(workspace), int(workspace_bytes),
+                                    _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), _dt(dt),
+                                    int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_dq(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, d, dt, causal, scale,
+                dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(workspace), int(workspace_bytes),
+                                  _ptr(dq), int(B), int(H), int(N), int(d), _dt(dt), int(bool(causal)),
+                                  float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_selftest_bounded_wait(dev_status, limit_ns, stream=None) -> int:
+    return int(load().attn_selftest_bounded_wait(_ptr(dev_status), int(limit_ns), _stream(stream)))
+
+
+# ---------------------------------------------------------------- torch convenience
+
+
+def _check(t, name):
+    import torch
+
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dim() == 4):
+        raise ValueError(f"{name} must be a CUDA tensor of shape [B, H, N, d]")
+    return t.contiguous()
+
+
+def forward(q, k, v, causal: bool = False, scale=None, dev_status=None, out=None):
+    """O = softmax(scale Q K^T) V and the row logsumexp; q, k, v: [B, H, N, d] bf16/fp16 CUDA tensors."""
+    import torch
+
+    q, k, v = _check(q, "q"), _check(k, "k"), _check(v, "v")
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share shape and dtype")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o, lse = out if out is not None else (torch.empty_like(q), torch.empty((B, H, N), device=q.device,
+                                                                            dtype=torch.float32))
+    st = attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale, dev_status)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale=None, dev_status=None, workspace=None,
+             out=None):
+    """dQ, dK, dV of sum(dout * O) for O = forward(q, k, v); all [B, H, N, d] CUDA tensors."""
+    import torch
+
+    q, k, v, o, dout = (_check(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")))
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = attn_bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    st = attn_bwd(q, k, v, o, dout, lse.contiguous(), dq, dk, dv, workspace, workspace.numel(), B, H, N, d,
+                  q.dtype, causal, scale, dev_status)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv

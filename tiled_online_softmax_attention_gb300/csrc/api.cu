@@ -1,0 +1,283 @@
+// api.cu -- the C ABI declared in include/attn.h: argument validation, TMA
+// descriptor encoding and kernel dispatch.  Nothing here allocates device
+// memory or keeps state between calls (the driver entry point for the tensor
+// map encoder is looked up once and cached).
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <initializer_list>
+#include <vector>
+
+#include "../../include/attn.h"
+#include "common.cuh"
+
+namespace {
+
+using attn::kTileM;
+
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait; a healthy wait takes microseconds
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("ATTN_WAIT_LIMIT_NS");
+    if (!s) return kDefaultWaitLimitNs;
+    const unsigned long long x = std::strtoull(s, nullptr, 10);
+    return x ? static_cast<uint64_t>(x) : kDefaultWaitLimitNs;
+  }();
+  return v;
+}
+
+// 3-D map over a [BH][N][d] 16-bit tensor: box {64, 128, 1}, 128-byte swizzle,
+// out-of-range rows read as zero and are dropped on store.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale) {
+  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dt != ATTN_BF16 && dt != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
+  const int64_t total = static_cast<int64_t>(B) * H * N * d;
+  if (total >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+attn_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;  // built for sm_103a only
+  return ATTN_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+  }
+  return "ATTN_ERR_UNKNOWN";
+}
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                     int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  attn_status st = check_sizes(B, H, N, d, dt, scale);
+  if (st != ATTN_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(in, tb, o, tb) || overlaps(in, tb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, tb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_device()) != ATTN_OK) return st;
+
+  attn::FwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_o, o, BH, N, d, bf16))
+    return ATTN_ERR_CUDA;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.N = N;
+  a.BH = BH;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = wait_limit_ns();
+  if (attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const size_t npad = (static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM;
+  return 2 * static_cast<size_t>(B) * H * npad * sizeof(float);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validation shared by the backward entry points.  `ins` are [B,H,N,d] inputs,
+// `outs` are [B,H,N,d] outputs (may be null entries when a stage does not write
+// them); the workspace must hold attn_bwd_workspace_bytes().
+attn_status check_bwd(std::initializer_list<const void*> ins, const float* lse,
+                      std::initializer_list<void*> outs, const void* ws, size_t ws_bytes, bool ws_out, int B,
+                      int H, int N, int d, attn_dtype dt, float scale) {
+  attn_status st = check_sizes(B, H, N, d, dt, scale);
+  if (st != ATTN_OK) return st;
+  for (const void* p : ins)
+    if (!aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  for (void* p : outs)
+    if (!aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return ATTN_ERR_INVALID_ARG;
+  if (lse && !aligned16(lse)) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
+  if (ws_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
+  for (void* out : outs) {
+    for (const void* in : ins)
+      if (overlaps(in, tb, out, tb)) return ATTN_ERR_INVALID_ARG;
+    if ((lse && overlaps(lse, lb, out, tb)) || overlaps(ws, need, out, tb)) return ATTN_ERR_INVALID_ARG;
+    for (void* other : outs)
+      if (other != out && overlaps(other, tb, out, tb)) return ATTN_ERR_INVALID_ARG;
+  }
+  {
+    // two identical output pointers are an overlap too
+    std::vector<void*> v(outs);
+    for (size_t i = 0; i < v.size(); ++i)
+      for (size_t j = i + 1; j < v.size(); ++j)
+        if (v[i] == v[j]) return ATTN_ERR_INVALID_ARG;
+  }
+  if (ws_out) {
+    for (const void* in : ins)
+      if (overlaps(in, tb, ws, need)) return ATTN_ERR_INVALID_ARG;
+    if (lse && overlaps(lse, lb, ws, need)) return ATTN_ERR_INVALID_ARG;
+  }
+  return check_device();
+}
+
+void fill_bwd(attn::BwdArgs& a, const void* ws, int B, int H, int N, int causal, float scale, int* dev_status) {
+  const int BH = B * H;
+  const int npad = static_cast<int>((static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM);
+  a.lse2 = static_cast<float*>(const_cast<void*>(ws));
+  a.delta = static_cast<float*>(const_cast<void*>(ws)) + static_cast<size_t>(BH) * npad;
+  a.dev_status = dev_status;
+  a.N = N;
+  a.Npad = npad;
+  a.BH = BH;
+  a.causal = causal ? 1 : 0;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = wait_limit_ns();
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_prepare(const void* o, const void* dout, const float* lse, void* workspace,
+                             size_t workspace_bytes, int B, int H, int N, int d, attn_dtype dt, void* stream) {
+  if (!lse) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_bwd({o, dout}, lse, {}, workspace, workspace_bytes, true, B, H, N, d, dt, 1.f);
+  if (st != ATTN_OK) return st;
+  attn::BwdArgs a{};
+  fill_bwd(a, workspace, B, H, N, 0, 1.f, nullptr);
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  if (attn::launch_bwd_pre(a, d, dt == ATTN_BF16, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                          size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int d, attn_dtype dt,
+                          int causal, float scale, int* dev_status, void* stream) {
+  attn_status st = check_bwd({q, k, v, dout}, nullptr, {dk, dv}, workspace, workspace_bytes, false, B, H, N, d, dt,
+                             scale);
+  if (st != ATTN_OK) return st;
+  attn::BwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
+      !make_map(&a.tm_dk, dk, BH, N, d, bf16) || !make_map(&a.tm_dv, dv, BH, N, d, bf16))
+    return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, causal, scale, dev_status);
+  if (attn::launch_bwd_dkdv(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                        size_t workspace_bytes, void* dq, int B, int H, int N, int d, attn_dtype dt, int causal,
+                        float scale, int* dev_status, void* stream) {
+  attn_status st =
+      check_bwd({q, k, v, dout}, nullptr, {dq}, workspace, workspace_bytes, false, B, H, N, d, dt, scale);
+  if (st != ATTN_OK) return st;
+  attn::BwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
+      !make_map(&a.tm_dq, dq, BH, N, d, bf16))
+    return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, causal, scale, dev_status);
+  if (attn::launch_bwd_dq(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                     int B, int H, int N, int d, attn_dtype dt, int causal, float scale, int* dev_status,
+                     void* stream) {
+  if (!lse) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_bwd({q, k, v, o, dout}, lse, {dq, dk, dv}, workspace, workspace_bytes, true, B, H, N, d,
+                             dt, scale);
+  if (st != ATTN_OK) return st;
+  if ((st = attn_bwd_prepare(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
+  if ((st = attn_bwd_dkdv(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, d, dt, causal, scale,
+                          dev_status, stream)) != ATTN_OK)
+    return st;
+  return attn_bwd_dq(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, d, dt, causal, scale, dev_status,
+                     stream);
+}
+
+attn_status attn_selftest_bounded_wait(int* dev_status, uint64_t limit_ns, void* stream) {
+  if (!dev_status) return ATTN_ERR_INVALID_ARG;
+  if (limit_ns < 1000ull) limit_ns = 1000ull;
+  if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+  attn_status st = check_device();
+  if (st != ATTN_OK) return st;
+  if (attn::launch_wait_selftest(dev_status, limit_ns, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+}  // extern "C"

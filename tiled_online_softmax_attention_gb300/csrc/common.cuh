@@ -1,0 +1,50 @@
+// common.cuh -- launch parameters shared by the host API (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+// Tiles: 128 query rows x 128 keys for every kernel (one TMEM lane per row).
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+
+struct FwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H][N][d], box {64, 128, 1}, 128B swizzle
+  float* lse;                          // [B*H][N]
+  int* dev_status;                     // nullable
+  int N;
+  int BH;
+  int causal;
+  float scale_log2;                    // scale * log2(e)
+  uint64_t wait_limit_ns;
+};
+
+struct BwdArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;  // inputs, as in FwdArgs
+  CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs
+  const void* o;                        // [B*H][N][d] forward output
+  const void* dout;                     // [B*H][N][d]
+  const float* lse;                     // [B*H][N]
+  float* lse2;                          // workspace [B*H][Npad]: lse * log2(e); +inf on padding rows
+  float* delta;                         // workspace [B*H][Npad]: rowsum(dO * O); 0 on padding rows
+  int* dev_status;
+  int N;
+  int Npad;                             // N rounded up to a multiple of 128
+  int BH;
+  int causal;
+  float scale;
+  float scale_log2;
+  uint64_t wait_limit_ns;
+};
+
+// Launchers (fwd.cu / bwd.cu); return the CUDA launch status.
+cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_wait_selftest(int* dev_status, uint64_t limit_ns, cudaStream_t s);
+
+}  // namespace attn
