@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true", help="skip the long-sequence forward side numbers")
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     return p.parse_args()
 
 
@@ -253,7 +254,7 @@ def run_ours(args, w, ws_, rank, local):
             ent["gbs"] = round(kbytes[n] / (per_kernel[n] * 1e-3) / 1e9, 1)
         kernels[n] = ent
 
-    e2e = run_e2e(args, w, x, dev, ws_)
+    e2e = None if args.no_e2e else run_e2e(args, w, x, dev, ws_)
     extra = None if args.no_extra else long_forward(attn, dev)
     return {"value": value, "ms_per_step": elapsed_ms / args.steps, "roofline": roofline, "kernels": kernels,
             "clocks": clocks, "e2e": e2e, "gpu_launches": 4 * args.steps, "extra": extra}

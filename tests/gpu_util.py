@@ -90,6 +90,18 @@ def rel_l2(g, ref):
     return float(np.linalg.norm(g - ref)) / max(den, 1e-30)
 
 
+ZERO_GRAD_ABS = 1e-3
+
+
+def grad_err(g, ref):
+    """Relative L2 error; for a reference that is exactly zero (one visible key makes dS = 0,
+    so dQ = dK = 0) the absolute residue, scaled so that ZERO_GRAD_ABS maps to GRAD_REL_L2."""
+    g = f64(g) if hasattr(g, "detach") else g
+    if not np.any(ref):
+        return float(np.max(np.abs(g))) / ZERO_GRAD_ABS * GRAD_REL_L2 if g.size else 0.0
+    return rel_l2(g, ref)
+
+
 def sample_rows(N, extra=24, seed=0):
     """Rows at both ends, on tile boundaries and at random."""
     rows = {0, 1, N - 1, N - 2}

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import workloads
-from gpu_util import GRAD_REL_L2, f64, rel_l2, run_bwd, run_fwd, sample_rows
+from gpu_util import GRAD_REL_L2, f64, grad_err, run_bwd, run_fwd, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -30,7 +30,7 @@ def test_bwd_small(N, d, causal, dtype):
     rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], causal, scale)
     for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
         assert np.all(np.isfinite(f64(g))), name + " non-finite"
-        e = rel_l2(g, r)
+        e = grad_err(g, r)
         assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e} (N={N} d={d} causal={causal} {dtype})"
 
 
@@ -47,7 +47,7 @@ def test_bwd_training_step_sampled():
         rq, rk, rv = oracle.attn_bwd(x["q"][b, h], x["k"][b, h], x["v"][b, h], x["dout"][b, h], True, w.scale,
                                      qrows=rows, kcols=rows)
         for name, g, r in (("dQ", dq[b, h, rows], rq), ("dK", dk[b, h, rows], rk), ("dV", dv[b, h, rows], rv)):
-            e = rel_l2(g, r)
+            e = grad_err(g, r)
             assert e <= GRAD_REL_L2, f"c5 head ({b},{h}) {name} relative L2 {e:.3e}"
 
 
