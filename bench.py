@@ -21,7 +21,6 @@ Prints ONE JSON line on rank 0.
 from __future__ import annotations
 
 import argparse
-import datetime as _dt
 import hashlib
 import json
 import math
@@ -136,10 +135,14 @@ def peaks():
         return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def source_digest():
+KERNEL_SOURCES = {"fwd": ["fwd.cu"], "bwd_prepare": ["bwd.cu"], "bwd_dkdv": ["bwd.cu"], "bwd_dq": ["bwd.cu"]}
+
+
+def source_digest(kernel: str):
+    """Hash of the source files a kernel is compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tiled_online_softmax_attention_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES[kernel] + ["ptx.cuh", "common.cuh"]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -152,7 +155,7 @@ def recorded_traffic(kernel: str):
     except (OSError, ValueError):
         return None
     ent = d.get(kernel)
-    if not ent or ent.get("source_digest") != source_digest():
+    if not ent or ent.get("source_digest") != source_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
