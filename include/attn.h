@@ -136,6 +136,42 @@ ATTN_API attn_status attn_bwd_dq(const void *q, const void *k, const void *v, co
                         int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
                         int *dev_status, void *stream);
 
+/*
+ * attn_bwd_noalloc -- attn_bwd for callers that cannot allocate device memory.
+ * (The pages have no counterpart to this entry point; it exists for
+ * integration, not for the method.)
+ *
+ * Some callers have no way to hand attn_bwd its workspace: a plugin whose host
+ * framework owns every byte of device memory through its own allocator, an
+ * engine that fixes its memory budget once at start-up, or a foreign-function
+ * caller that reaches the GPU only through this C ABI and has no CUDA runtime
+ * of its own to call cudaMalloc with.  This entry point takes the workspace
+ * from a fixed array of ATTN_NOALLOC_SCRATCH_BYTES (8 MiB) in the library's own
+ * device image instead; every GPU that loads the library holds that array
+ * until the process exits.  The caller still passes every input and output.
+ *
+ *  - Arguments, layouts and results are those of attn_bwd without the
+ *    workspace pair; the results equal attn_bwd's (same kernels).
+ *  - Limit: the workspace attn_bwd would need, attn_bwd_workspace_bytes(B, H,
+ *    N, d) = 8 * B*H*ceil(N/128)*128 bytes, must fit in the array, i.e.
+ *    B*H*ceil(N/128)*128 <= 1048576 rows (for example 128 heads of N = 8192).
+ *    Larger sizes return ATTN_ERR_INVALID_ARG before anything is launched.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.  The first
+ *    call on each device looks up the array's device address once, with that
+ *    device current (cudaGetSymbolAddress); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and it keeps the last call's contents;
+ *    nothing needs clearing because the preparation stage rewrites every value
+ *    the gradient stages read.  Calls that overlap on the GPU (on different
+ *    streams, or from different host threads without ordering) race on the
+ *    array and produce wrong gradients: order them.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+ATTN_API attn_status attn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                             int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                             int *dev_status, void *stream);
+
 /* attn_status_string -- a static, human-readable name for a status code. */
 ATTN_API const char *attn_status_string(attn_status s);
 

@@ -14,6 +14,8 @@ current stream):
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
              B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
     attn_bwd_prepare / attn_bwd_dkdv / attn_bwd_dq   (the three stages of attn_bwd)
+    attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, dt, causal, scale, ...)
+                                                     (attn_bwd with library-owned scratch)
     attn_status_string(status)
     attn_selftest_bounded_wait(dev_status, limit_ns, stream=None)
 
@@ -40,7 +42,7 @@ ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
 EXPORTS = ("attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_status_string", "attn_selftest_bounded_wait")
+           "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
 
@@ -74,6 +76,8 @@ def load(build_if_missing: bool = True):
     lib.attn_bwd_dkdv.restype = I
     lib.attn_bwd_dq.argtypes = [P, P, P, P, P, SZ, P, I, I, I, I, I, I, F, P, P]
     lib.attn_bwd_dq.restype = I
+    lib.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_noalloc.restype = I
     lib.attn_status_string.argtypes = [I]
     lib.attn_status_string.restype = ctypes.c_char_p
     lib.attn_selftest_bounded_wait.argtypes = [P, ctypes.c_uint64, P]
@@ -149,6 +153,13 @@ def attn_bwd_dq(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, d, dt, c
     return int(load().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(workspace), int(workspace_bytes),
                                   _ptr(dq), int(B), int(H), int(N), int(d), _dt(dt), int(bool(causal)),
                                   float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, dt, causal, scale, dev_status=None,
+                     stream=None) -> int:
+    return int(load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), _dt(dt),
+                                       int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
 
 
 def attn_selftest_bounded_wait(dev_status, limit_ns, stream=None) -> int:
