@@ -1,34 +1,49 @@
 // fwd.cu -- forward attention kernel for sm_103a.
 //
-// One CTA computes one 128-row query tile of one (batch, head) and streams the
-// K/V tiles of that head through shared memory (FA2 loop order: queries outer,
-// keys inner; "FlashAttention hardware-aware analysis" (huaweicloud), section
-// four, part 2).  Per key tile j:
+// One CTA computes two 128-row query tiles (Q0, Q1) of one (batch, head) and
+// streams that head's K/V tiles through shared memory once for both (FA2 loop
+// order: queries outer, keys inner; "FlashAttention hardware-aware analysis"
+// (huaweicloud), section four, part 2).  Per key tile j and query tile i:
 //
-//   S_j   = Q K_j^T                 tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
-//   m_new = max(m, rowmax S_j)      online-softmax recurrence (huaweicloud page,
-//   P_j   = exp(S_j - m_new)        section two; "Understanding online softmax in
+//   S_i   = Q_i K_j^T               tcgen05.mma, SMEM x SMEM -> TMEM (fp32)
+//   m_new = max(m, rowmax S_i)      online-softmax recurrence (huaweicloud page,
+//   P_i   = exp(S_i - m_new)        section two; "Understanding online softmax in
 //   l     = l e^(m-m_new) + rowsum  Flash Attention from scratch", section 3.1),
-//   O     = O e^(m-m_new) + P_j V_j in the base-2 domain: exponents are
-//                                   scale*log2(e)*S, so exp becomes ex2
+//   O_i   = O_i e^(m-m_new) + P_i V_j   in the base-2 domain (exponents are
+//                                   scale*log2(e)*S, so exp becomes ex2)
 //
-// O stays in tensor memory for the whole loop and is divided by l once at the
+// O_i stays in tensor memory for the whole loop and is divided by l once at the
 // end (deferred normalisation; hotelren.com FA1/FA2 comparison, section 2.1.2).
 // The row logsumexp m + ln l is saved for the backward pass.  Nothing of size
 // N x N ever leaves the SM.
 //
-// Warp roles (192 threads):
-//   warp 0     TMA producer: Q once, then K_j and V_j into a STAGES-deep ring
-//   warp 1     TMEM owner and MMA issuer (one elected lane)
-//   warps 2-5  softmax: thread r owns query row r (TMEM lane r): masks, row max,
-//              ex2, row sum, P -> TMEM (16-bit), O rescale, epilogue
+// The two query tiles exist so that the tensor core always has work: while the
+// softmax warps of tile 0 turn S_0 into P_0, the MMA warp runs P_1 V and
+// Q_1 K^T for tile 1, and the other way round.  The MMA issue order per key
+// tile is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).  S_i(j+1) overwrites the
+// columns P_i(j) was read from by PV_i(j); the two products are issued by one
+// thread in that order and the tensor core executes one thread's MMAs in order.
 //
-// Tensor memory (512 columns): S at 0..127 (fp32), P at 128..191 (16-bit pairs),
-// O at 256..256+d-1 (fp32).
+// Rescaling is lazy: a row's reference maximum only moves when the new row max
+// exceeds it by more than 2^8 (in exp2 units), so exponentials stay <= 256 and
+// the O rescale (a TMEM read-modify-write) is skipped on almost every tile.
+// Because O, l and the final logsumexp all use the same reference maximum, the
+// result is exact; only the moment of rescaling changes.
+//
+// Warp roles (512 threads, four warpgroups):
+//   warpgroup 0  warp 0 TMA producer (Q0, Q1 once; then K_j, V_j into a ring),
+//                warp 1 TMEM owner and MMA issuer (one elected lane)
+//   warpgroup 1  softmax of query tile 0 (thread r owns row r = TMEM lane r)
+//   warpgroup 2  softmax of query tile 1
+//   warpgroup 3  correction (O rescale when a reference max moves) and the
+//                epilogue of both tiles (O / l -> 16-bit -> swizzled SMEM -> TMA store)
+//
+// Tensor memory (512 columns): S_0 at 0, S_1 at 128 (fp32; P_i is written as
+// 16-bit pairs over the first 64 columns of S_i), O_0 at 256, O_1 at 256 + d.
 //
 // Causal: key tiles wholly above the diagonal are never loaded (the huaweicloud
-// page's section five, part 3); only the diagonal tile and the ragged last tile
-// are masked.  The grid is walked longest-tile-first.
+// page's section five, part 3); only diagonal and ragged tiles are masked.  The
+// grid is walked head by head, longest query pair first within a head.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -40,30 +55,37 @@ struct FwdLayout {
   static constexpr int KB = D / 64;                  // 64-column (128-byte) blocks per row
   static constexpr int TILE = kTileM * D * 2;        // bytes of one 128 x D 16-bit tile
   static constexpr int BLK = kTileM * 128;           // bytes of one 128-row x 64-col block
-  static constexpr int STAGES = (D == 128) ? 3 : 4;  // K/V ring depth
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
-  static constexpr int OFF_V = OFF_K + STAGES * TILE;
-  static constexpr int OFF_BAR = OFF_V + STAGES * TILE;
-  static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
-  static constexpr uint32_t TM_S = 0, TM_P = 128, TM_O = 256, TM_COLS = 512;
+  static constexpr int NSLOT = (D == 128) ? 4 : 8;   // K/V ring entries, one tile each
+  static constexpr int OFF_Q = 0;                    // Q0, Q1 (later the O staging tiles)
+  static constexpr int OFF_KV = 2 * TILE;
+  static constexpr int OFF_AUX = OFF_KV + NSLOT * TILE;
+  static constexpr int AUX_BAR = 0;                  // up to 64 mbarriers
+  static constexpr int AUX_ALPHA = 512;              // float[2][128]: rescale factor per row
+  static constexpr int AUX_M = AUX_ALPHA + 1024;     // float[2][128]: final reference max
+  static constexpr int AUX_L = AUX_M + 1024;         // float[2][128]: final row sum
+  static constexpr int AUX_MISC = AUX_L + 1024;      // abort flag, TMEM address
+  static constexpr int AUX_BYTES = AUX_MISC + 64;
+  static constexpr int SMEM = OFF_AUX + AUX_BYTES + 1024;  // + alignment slack
+  static constexpr uint32_t TM_O = 256, TM_COLS = 512;
+  static constexpr uint32_t tm_s(int i) { return 128u * i; }
+  static constexpr uint32_t tm_o(int i) { return TM_O + D * i; }
 };
 
-constexpr int kFwdThreads = 192;
+constexpr int kFwdThreads = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// Barrier slots (uint64 each) after OFF_BAR.
 enum : int {
-  B_QFULL = 0,
-  B_SFULL = 1,
-  B_SFREE = 2,
-  B_PFULL = 3,
-  B_ORDY = 4,
-  B_DRAIN = 5,
-  B_KFULL = 6,   // + stage
-  B_VFULL = 10,  // + stage
-  B_EMPTY = 14,  // + stage
-  B_COUNT = 18
+  B_Q = 0,         // + tile
+  B_SFULL = 2,     // + tile: S_i computed (MMA commit)
+  B_PFULL = 4,     // + tile: P_i written (128 softmax arrivals)
+  B_STAT = 6,      // + tile: rescale factors of this key tile published (128 arrivals)
+  B_CORR = 8,      // + tile: O_i rescaled if needed (128 correction arrivals)
+  B_ODONE = 10,    // + tile: P_i V_j done (MMA commit)
+  B_FIN = 12,      // + tile: final m, l published (128 arrivals)
+  B_DRAIN = 14,
+  B_KVFULL = 16,   // + slot
+  B_KVEMPTY = 24,  // + slot
+  B_COUNT = 32
 };
 
 template <int D, bool BF16>
@@ -73,34 +95,39 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t sQ = sb + L::OFF_Q;
-  const uint32_t sK = sb + L::OFF_K;
-  const uint32_t sV = sb + L::OFF_V;
-  const uint32_t bars = sb + L::OFF_BAR;
+  uint8_t* aux = smem + L::OFF_AUX;
+  const uint32_t bars = sb + L::OFF_AUX + L::AUX_BAR;
   auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * B_COUNT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * B_COUNT + 8);
+  float* alpha_s = reinterpret_cast<float*>(aux + L::AUX_ALPHA);
+  float* m_s = reinterpret_cast<float*>(aux + L::AUX_M);
+  float* l_s = reinterpret_cast<float*>(aux + L::AUX_L);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(aux + L::AUX_MISC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux + L::AUX_MISC + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_qt = (a.N + kTileM - 1) / kTileM;
-  const int qt = n_qt - 1 - static_cast<int>(blockIdx.x) / a.BH;  // longest causal tiles first
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
-  const int q0 = qt * kTileM;
-  const int n_kt = (a.N + kTileN - 1) / kTileN;
-  const int n_kv = a.causal ? min(qt + 1, n_kt) : n_kt;
+  const int n_t = (a.N + kTileM - 1) / kTileM;
+  const int n_pairs = (n_t + 1) / 2;
+  const int bh = static_cast<int>(blockIdx.x) / n_pairs;
+  const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x) % n_pairs;  // longest causal pair first
+  int n_kv[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) n_kv[i] = a.causal ? min(2 * pr + i + 1, n_t) : n_t;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_SFULL), 1);
-    mbar_init(bar(B_SFREE), 128);
-    mbar_init(bar(B_PFULL), 128);
-    mbar_init(bar(B_ORDY), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(B_Q + i), 1);
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_PFULL + i), 128);
+      mbar_init(bar(B_STAT + i), 128);
+      mbar_init(bar(B_CORR + i), 128);
+      mbar_init(bar(B_ODONE + i), 1);
+      mbar_init(bar(B_FIN + i), 128);
+    }
     mbar_init(bar(B_DRAIN), 1);
-    for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(bar(B_KFULL + s), 1);
-      mbar_init(bar(B_VFULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1);
+    for (int s = 0; s < L::NSLOT; ++s) {
+      mbar_init(bar(B_KVFULL + s), 1);
+      mbar_init(bar(B_KVEMPTY + s), 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -114,107 +141,139 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtl wc{abort_flag, a.dev_status, a.wait_limit_ns};
+  const int wg = warp >> 2;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+  // Register split: 64 (control) + 2 x 184 (softmax) + 80 (correction) per lane quadruple
+  // = 128 x 512 threads, the launch allotment.
+  if (wg == 0) {
+    setmaxnreg_dec<64>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
       prefetch_tmap(&a.tm_q);
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
       prefetch_tmap(&a.tm_o);
-      mbar_arrive_expect_tx(bar(B_QFULL), L::TILE);
-      for (int kb = 0; kb < L::KB; ++kb) tma_load_3d(sQ + kb * L::BLK, &a.tm_q, bar(B_QFULL), kb * 64, q0, bh);
+      for (int i = 0; i < 2; ++i) {
+        mbar_arrive_expect_tx(bar(B_Q + i), L::TILE);
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(sb + L::OFF_Q + i * L::TILE + kb * L::BLK, &a.tm_q, bar(B_Q + i), kb * 64,
+                      (2 * pr + i) * kTileM, bh);
+      }
+      const int n_loads = 2 * n_kv[1];  // K_j, V_j alternately
       int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % L::STAGES;
-        if (j >= L::STAGES && !mbar_wait(bar(B_EMPTY + s), ((j / L::STAGES) - 1) & 1, wc)) break;
-        const uint32_t dk = sK + s * L::TILE, dv = sV + s * L::TILE;
-        mbar_arrive_expect_tx(bar(B_KFULL + s), L::TILE);
-        for (int kb = 0; kb < L::KB; ++kb) tma_load_3d(dk + kb * L::BLK, &a.tm_k, bar(B_KFULL + s), kb * 64, j * kTileN, bh);
-        mbar_arrive_expect_tx(bar(B_VFULL + s), L::TILE);
-        for (int kb = 0; kb < L::KB; ++kb) tma_load_3d(dv + kb * L::BLK, &a.tm_v, bar(B_VFULL + s), kb * 64, j * kTileN, bh);
-        issued = j + 1;
+      for (int ld = 0; ld < n_loads; ++ld) {
+        const int s = ld % L::NSLOT;
+        if (ld >= L::NSLOT && !mbar_wait(bar(B_KVEMPTY + s), ((ld / L::NSLOT) - 1) & 1, wc)) break;
+        const CUtensorMap* m = (ld & 1) ? &a.tm_v : &a.tm_k;
+        mbar_arrive_expect_tx(bar(B_KVFULL + s), L::TILE);
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(B_KVFULL + s), kb * 64,
+                      (ld >> 1) * kTileN, bh);
+        issued = ld + 1;
       }
       // Let every copy this thread started land before the CTA can exit.
-      mbar_wait(bar(B_QFULL), 0, wc);
-      for (int j = (issued > L::STAGES ? issued - L::STAGES : 0); j < issued; ++j) {
-        const int s = j % L::STAGES, ph = (j / L::STAGES) & 1;
-        mbar_wait(bar(B_KFULL + s), ph, wc);
-        mbar_wait(bar(B_VFULL + s), ph, wc);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+      mbar_wait(bar(B_Q + 0), 0, wc);
+      mbar_wait(bar(B_Q + 1), 0, wc);
+      for (int ld = (issued > L::NSLOT ? issued - L::NSLOT : 0); ld < issued; ++ld)
+        mbar_wait(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc_qk = idesc_f16(kTileM, kTileN, BF16, false, false);
       constexpr uint32_t idesc_pv = idesc_f16(kTileM, D, BF16, false, true);
-      bool ok = mbar_wait(bar(B_QFULL), 0, wc);
-      auto issue_pv = [&](int t) -> bool {
-        const int s = t % L::STAGES, ph = (t / L::STAGES) & 1;
-        if (!mbar_wait(bar(B_PFULL), t & 1, wc)) return false;
-        if (!mbar_wait(bar(B_VFULL + s), ph, wc)) return false;
-        tc_fence_after();
-        const uint32_t v_base = sV + s * L::TILE;
-#pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k) {
-          // 16 keys = two 8-row groups of 128 bytes; d blocks are L::BLK apart.
-          const uint64_t bd = sdesc_sw128(v_base + k * 2048, L::BLK, 1024);
-          mma_ts(tmem + L::TM_O, tmem + L::TM_P + k * 8, bd, idesc_pv, (t > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(bar(B_ORDY));
-        tc_commit(bar(B_EMPTY + s));
-        return true;
-      };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % L::STAGES, ph = (j / L::STAGES) & 1;
-        if (!mbar_wait(bar(B_KFULL + s), ph, wc)) { ok = false; break; }
-        if (j > 0 && !mbar_wait(bar(B_SFREE), (j - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_base = sK + s * L::TILE;
+      auto full = [&](int ld) { return mbar_wait(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc); };
+      auto issue_s = [&](int i, int j) {
+        const uint32_t qb = sb + L::OFF_Q + i * L::TILE;
+        const uint32_t kbase = sb + L::OFF_KV + ((2 * j) % L::NSLOT) * L::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * L::BLK + (k & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + off, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_base + off, 16, 1024);
-          mma_ss(tmem + L::TM_S, ad, bd, idesc_qk, k > 0 ? 1u : 0u);
+          mma_ss(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk,
+                 k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(B_SFULL));
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        tc_commit(bar(B_SFULL + i));
+      };
+      auto issue_pv = [&](int i, int j) {
+        const uint32_t vbase = sb + L::OFF_KV + ((2 * j + 1) % L::NSLOT) * L::TILE;
+#pragma unroll
+        for (int k = 0; k < kTileN / 16; ++k)
+          mma_ts(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8, sdesc_sw128(vbase + k * 2048, L::BLK, 1024),
+                 idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(B_ODONE + i));
+      };
+      bool ok = mbar_wait(bar(B_Q + 0), 0, wc) && full(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        ok = mbar_wait(bar(B_Q + 1), 0, wc);
       }
-      if (ok) issue_pv(n_kv - 1);
+      if (ok) {
+        tc_fence_after();
+        issue_s(1, 0);
+        tc_commit(bar(B_KVEMPTY + 0));
+      }
+      for (int j = 0; ok && j < n_kv[1]; ++j) {
+        bool v_ready = false, k_next_ready = false;
+        if (j < n_kv[0]) {
+          if (!(ok = full(2 * j + 1) && mbar_wait(bar(B_PFULL + 0), j & 1, wc) &&
+                     (j == 0 || mbar_wait(bar(B_CORR + 0), (j - 1) & 1, wc))))
+            break;
+          v_ready = true;
+          tc_fence_after();
+          issue_pv(0, j);
+          if (j + 1 < n_kv[0]) {
+            if (!(ok = full(2 * j + 2))) break;
+            k_next_ready = true;
+            tc_fence_after();
+            issue_s(0, j + 1);
+          }
+        }
+        if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait(bar(B_PFULL + 1), j & 1, wc) &&
+                   (j == 0 || mbar_wait(bar(B_CORR + 1), (j - 1) & 1, wc))))
+          break;
+        tc_fence_after();
+        issue_pv(1, j);
+        tc_commit(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
+        if (j + 1 < n_kv[1]) {
+          if (!(ok = k_next_ready || full(2 * j + 2))) break;
+          tc_fence_after();
+          issue_s(1, j + 1);
+          tc_commit(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
+        }
+      }
       // Drain: nothing may still write tensor memory when it is released.
       tc_commit(bar(B_DRAIN));
       mbar_wait(bar(B_DRAIN), 0, wc);
     }
-  } else {
-    // ------------------------------------------------------------ softmax warps
-    const int wq = warp & 3;                     // TMEM lane quarter of this warp
-    const int row = wq * 32 + lane;              // row in the tile == TMEM lane
-    const int grow = q0 + row;                   // row in the sequence
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+  } else if (wg <= 2) {
+    // ------------------------------------------------------------ softmax of tile i
+    setmaxnreg_inc<184>();
+    const int i = wg - 1;
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int grow = (2 * pr + i) * kTileM + row;
+    const uint32_t t_s = tmem + (static_cast<uint32_t>(wq * 32) << 16) + L::tm_s(i);
     const float sl2 = a.scale_log2;
-    float m = -INFINITY;  // running max of scale*log2(e)*S
-    float l = 0.f;        // running sum of ex2(.. - m)
+    float m = -INFINITY;  // reference max (scale*log2(e) units) used by the exponentials
+    float l = 0.f;        // row sum of ex2(. - m)
     bool ok = true;
-
-    for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(bar(B_SFULL), j & 1, wc)) { ok = false; break; }
+    for (int j = 0; j < n_kv[i]; ++j) {
+      if (!mbar_wait_warp(bar(B_SFULL + i), j & 1, wc)) { ok = false; break; }
       tc_fence_after();
       float s[128];
       {
-        uint32_t sr[128];
-        tmem_ld_x128(t_lane + L::TM_S, sr);
 #pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t sr[64];
+          tmem_ld_x64(t_s + 64 * h, sr);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) s[64 * h + c] = __uint_as_float(sr[c]);
+        }
       }
-      tc_fence_before();
-      mbar_arrive(bar(B_SFREE));
-
       const int k0 = j * kTileN;
       const bool tail = k0 + kTileN > a.N;
-      const bool diag = a.causal && (k0 + kTileN - 1 > q0);
+      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM);
       if (tail || diag) {
-        int lim = a.N - k0;                       // keys past the end of the sequence
+        int lim = a.N - k0;                           // keys past the end of the sequence
         if (a.causal) lim = min(lim, grow - k0 + 1);  // keys after this query
 #pragma unroll
         for (int c = 0; c < kTileN; ++c)
@@ -223,9 +282,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       float mx = s[0];
 #pragma unroll
       for (int c = 1; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx * sl2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // a row with nothing visible yet
-      const float alpha = ex2(m - m_use);                     // 0 on the first tile
+      mx *= sl2;
+      // Move the reference max only when it is exceeded by more than 2^8.
+      const float m_new = (mx - m > kRescaleThreshold) ? mx : m;
+      const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);  // 0 on the first tile
+      if (j > 0) {
+        alpha_s[i * 128 + row] = alpha;
+        mbar_arrive(bar(B_STAT + i));
+      }
+      m = m_new;
+      const float m_use = (m == -INFINITY) ? 0.f : m;  // a row with nothing visible yet
       float rs = 0.f;
       uint32_t pk[64];
 #pragma unroll
@@ -236,64 +302,88 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         pk[c / 2] = pack2<BF16>(p0, p1);
       }
       l = fmaf(l, alpha, rs);
-      m = m_new;
-
-      if (j > 0) {
-        // O and the P columns are busy until the previous P V product is done.
-        if (!mbar_wait_warp(bar(B_ORDY), (j - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
+      tmem_st_x64(t_s, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(B_PFULL + i));
+    }
+    if (ok) {
+      m_s[i * 128 + row] = (m == -INFINITY) ? 0.f : m;
+      l_s[i * 128 + row] = l;
+      mbar_arrive(bar(B_FIN + i));
+    }
+  } else {
+    // ------------------------------------------------------------ correction + epilogue
+    setmaxnreg_dec<80>();
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    bool ok = true;
+    for (int j = 1; ok && j < n_kv[1]; ++j) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        if (j >= n_kv[i]) continue;
+        if (!(ok = mbar_wait_warp(bar(B_STAT + i), (j - 1) & 1, wc))) break;
+        const float alpha = alpha_s[i * 128 + row];
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          // O_i holds the sum up to key tile j-1: wait for that product, then rescale.
+          if (!(ok = mbar_wait_warp(bar(B_ODONE + i), (j - 1) & 1, wc))) break;
+          tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
-            tmem_ld_x32(t_lane + L::TM_O + cc * 32, o);
+            tmem_ld_x32(t_lane + L::tm_o(i) + cc * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st_x32(t_lane + L::TM_O + cc * 32, o);
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st_x32(t_lane + L::tm_o(i) + cc * 32, o);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        mbar_arrive(bar(B_CORR + i));
+      }
+    }
+    // Epilogue: O_i / l -> 16-bit -> swizzled staging over Q_i -> TMA store; logsumexp.
+#pragma unroll 1
+    for (int i = 0; i < 2; ++i) {
+      const bool ok_i = ok && mbar_wait_warp(bar(B_FIN + i), 0, wc) &&
+                        mbar_wait_warp(bar(B_ODONE + i), (n_kv[i] - 1) & 1, wc);
+      const int q0 = (2 * pr + i) * kTileM;
+      if (ok_i) {
+        tc_fence_after();
+        const float mf = m_s[i * 128 + row];
+        const float lf = l_s[i * 128 + row];
+        const float inv_l = 1.f / lf;
+        uint8_t* stage = smem + L::OFF_Q + i * L::TILE;  // Q_i is no longer read
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(t_lane + L::tm_o(i) + cc * 32, o);
+          uint32_t pkd[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pkd[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
+          const int kb = (cc * 32) / 64;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = ((cc * 32) % 64) / 8 + q;
+            uint4* dst = reinterpret_cast<uint4*>(stage + kb * L::BLK + row * 128 + ((ch ^ (row & 7)) << 4));
+            *dst = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
           }
         }
+        if (q0 + row < a.N)  // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
+          a.lse[static_cast<size_t>(bh) * a.N + q0 + row] = (mf + __log2f(lf)) * 0.69314718055994531f;
+        fence_proxy_async_smem();
       }
-      tmem_st_x64(t_lane + L::TM_P, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(B_PFULL));
-    }
-
-    // ---------------------------------------------------------- epilogue
-    if (ok) ok = mbar_wait_warp(bar(B_ORDY), (n_kv - 1) & 1, wc);
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      uint8_t* stage = smem + L::OFF_Q;  // Q is no longer read once the last S is done
-#pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld_x32(t_lane + L::TM_O + cc * 32, o);
-        uint32_t pkd[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pkd[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        // 32 columns = four 16-byte chunks of the 128B-swizzled row.
-        const int kb = (cc * 32) / 64;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = ((cc * 32) % 64) / 8 + q;
-          uint4* dst = reinterpret_cast<uint4*>(stage + kb * L::BLK + row * 128 + ((ch ^ (row & 7)) << 4));
-          *dst = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
-        }
+      ok = ok && ok_i;
+      named_bar_sync(1, 128);
+      if (warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < a.N) {
+        for (int kb = 0; kb < L::KB; ++kb)
+          tma_store_3d(&a.tm_o, sb + L::OFF_Q + i * L::TILE + kb * L::BLK, kb * 64, q0, bh);
+        bulk_commit();
       }
-      if (grow < a.N) {
-        // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
-        a.lse[static_cast<size_t>(bh) * a.N + grow] = (m + __log2f(l)) * 0.69314718055994531f;
-      }
-      fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0 && !*abort_flag) {
-      for (int kb = 0; kb < L::KB; ++kb) tma_store_3d(&a.tm_o, sQ + kb * L::BLK, kb * 64, q0, bh);
-      bulk_commit();
-      bulk_wait_read_all();
-    }
+    if (warp == 12 && lane == 0) bulk_wait_read_all();
   }
 
   tc_fence_before();
@@ -310,9 +400,9 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   auto k = fwd_kernel<D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
-  const int n_qt = (a.N + kTileM - 1) / kTileM;
-  dim3 grid(n_qt * a.BH);
-  k<<<grid, kFwdThreads, L::SMEM, st>>>(a);
+  const int n_t = (a.N + kTileM - 1) / kTileM;
+  const int n_pairs = (n_t + 1) / 2;
+  k<<<dim3(n_pairs * a.BH), kFwdThreads, L::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 
