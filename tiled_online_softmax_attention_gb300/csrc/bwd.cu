@@ -31,7 +31,7 @@
 namespace attn {
 namespace {
 
-constexpr int kBwdThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 elementwise + epilogue
+constexpr int kBwdThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 idle, warpgroups 1-2 element-wise + epilogue
 
 // ------------------------------------------------------------------ bwd_pre
 
@@ -109,6 +109,19 @@ __device__ __forceinline__ void stage_row_chunk(uint8_t* stage, int row, int cc,
 }
 
 // ------------------------------------------------------------------ bwd_dkdv
+//
+// Warp roles (384 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warpgroups 1
+// and 2 the element-wise work, warpgroup 1 on queries 0-63 of every tile and
+// warpgroup 2 on queries 64-127 (every tensor-core product keeps N >= 128: the
+// tcgen05.mma issue cost does not shrink below N = 128).  Per query tile the MMA
+// warp issues, in this order,
+//   S^T = K Q^T | dP^T = V dO^T | dV += P^T dO | dK += dS^T Q
+// and the element-wise work is split in two phases so that each overlaps a
+// product: P^T = ex2(c S^T - LSE2) while dP^T is computed, then
+// dS^T = P^T (dP^T - D) while dV is computed.  P^T and dS^T go back as 16-bit
+// pairs over the first half of each warpgroup's own S^T / dP^T columns.  The next
+// tile's S^T / dP^T overwrite those columns; one thread issues every product and
+// the tensor core executes one thread's MMAs in order.
 
 template <int D>
 struct DkdvLayout {
@@ -120,21 +133,21 @@ struct DkdvLayout {
   static constexpr int OFF_ST = 2 * T::TILE;
   static constexpr int OFF_BAR = OFF_ST + STAGES * STAGE_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  // per-stage offsets
   static constexpr int S_Q = 0, S_DO = T::TILE, S_L = 2 * T::TILE, S_D = 2 * T::TILE + 512;
-  // tensor memory columns
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TM_COLS = 512;
 };
 
 enum : int {
   K_KVFULL = 0,
-  K_STFULL = 1,
-  K_PFULL = 2,
-  K_MM2 = 3,
-  K_DRAIN = 4,
-  K_QFULL = 5,   // + stage
-  K_EMPTY = 9,   // + stage
-  K_COUNT = 13
+  K_SFULL = 1,    // S^T computed (MMA commit)
+  K_DPFULL = 2,   // dP^T computed (MMA commit)
+  K_PREADY = 3,   // P^T written (256 arrivals)
+  K_DSREADY = 4,  // dS^T written (256 arrivals)
+  K_DONE = 5,
+  K_DRAIN = 6,
+  K_QFULL = 7,    // + stage
+  K_EMPTY = 11,   // + stage
+  K_COUNT = 15
 };
 
 template <int D, bool BF16>
@@ -153,17 +166,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileN - 1) / kTileN;
-  const int kt = static_cast<int>(blockIdx.x) / a.BH;  // low key tiles see the most queries
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int bh = static_cast<int>(blockIdx.x) / n_t;  // head-major; low key tiles see the most queries
+  const int kt = static_cast<int>(blockIdx.x) % n_t;
   const int k0 = kt * kTileN;
-  const int i_begin = a.causal ? kt : 0;               // query tiles before the key tile are masked out
+  const int i_begin = a.causal ? kt : 0;  // query tiles before the key tile are masked out
   const int n_iter = n_t - i_begin;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(K_KVFULL), 1);
-    mbar_init(bar(K_STFULL), 1);
-    mbar_init(bar(K_PFULL), 128);
-    mbar_init(bar(K_MM2), 1);
+    mbar_init(bar(K_SFULL), 1);
+    mbar_init(bar(K_DPFULL), 1);
+    mbar_init(bar(K_PREADY), 256);
+    mbar_init(bar(K_DSREADY), 256);
+    mbar_init(bar(K_DONE), 1);
     mbar_init(bar(K_DRAIN), 1);
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(bar(K_QFULL + s), 1);
@@ -216,109 +231,136 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);  // K-major x K-major
+      constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
       constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // TMEM x MN-major
       bool ok = mbar_wait(bar(K_KVFULL), 0, wc);
       for (int t = 0; ok && t < n_iter; ++t) {
         const int s = t % L::STAGES;
-        if (!mbar_wait(bar(K_QFULL + s), (t / L::STAGES) & 1, wc)) { ok = false; break; }
-        // S^T, dP^T overwrite the columns that held P^T, dS^T of the previous tile.
-        if (t > 0 && !mbar_wait(bar(K_MM2), (t - 1) & 1, wc)) { ok = false; break; }
+        if (!(ok = mbar_wait(bar(K_QFULL + s), (t / L::STAGES) & 1, wc))) break;
         tc_fence_after();
         const uint32_t st = stage_base(s);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024),
-                 sdesc_sw128(st + L::S_Q + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+          mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024), sdesc_sw128(st + L::S_Q + off, 16, 1024),
+                 idesc_s, k > 0 ? 1u : 0u);
         }
+        tc_commit(bar(K_SFULL));
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
           mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
                  sdesc_sw128(st + L::S_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(K_STFULL));
-        if (!mbar_wait(bar(K_PFULL), t & 1, wc)) { ok = false; break; }
+        tc_commit(bar(K_DPFULL));
+        if (!(ok = mbar_wait(bar(K_PREADY), t & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k) {
-          const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + k * 8, sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024),
-                 idesc_g, acc);
-          mma_ts(tmem + L::TM_DK, tmem + L::TM_DP + k * 8, sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024),
-                 idesc_g, acc);
-        }
-        tc_commit(bar(K_MM2));
+        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of half h at S^T + 64h
+          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + 64 * (k >> 2) + 8 * (k & 3),
+                 sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+        if (!(ok = mbar_wait(bar(K_DSREADY), t & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTileM / 16; ++k)
+          mma_ts(tmem + L::TM_DK, tmem + L::TM_DP + 64 * (k >> 2) + 8 * (k & 3),
+                 sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
         tc_commit(bar(K_EMPTY + s));
       }
+      if (ok) tc_commit(bar(K_DONE));
       tc_commit(bar(K_DRAIN));
       mbar_wait(bar(K_DRAIN), 0, wc);
     }
-  } else {
+  } else if (warp >= 4) {
+    const int h = (warp >> 2) - 1;      // query half of every tile this warpgroup handles
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;    // key row within the tile == TMEM lane
+    const int row = wq * 32 + lane;     // key row within the tile == TMEM lane
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sl2 = a.scale_log2;
-    bool ok = n_iter > 0;
+    bool ok = true;
     for (int t = 0; t < n_iter; ++t) {
       const int s = t % L::STAGES;
       const int qt = i_begin + t;
-      if (!mbar_wait_warp(bar(K_QFULL + s), (t / L::STAGES) & 1, wc)) { ok = false; break; }
-      if (!mbar_wait_warp(bar(K_STFULL), t & 1, wc)) { ok = false; break; }
+      if (!(ok = mbar_wait_warp(bar(K_QFULL + s), (t / L::STAGES) & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(bar(K_SFULL), t & 1, wc))) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_L);
-      const float* dlt = reinterpret_cast<const float*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D);
+      const float4* l4 = reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_L) + 16 * h;
+      const float4* d4 = reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D) + 16 * h;
       // causal diagonal tile: query c sees key `row` only if c >= row
-      const int first_visible = (a.causal && qt == kt) ? row : 0;
+      const int first_visible = (a.causal && qt == kt) ? row - 64 * h : 0;  // relative to this half
+      float p[64];
+      // Phase 1: P^T for this half's 64 queries (overlaps the dP^T product).
 #pragma unroll
-      for (int ch = 0; ch < kTileM / 32; ++ch) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld_x32(t_lane + L::TM_S + ch * 32, sv);
-        tmem_ld_x32(t_lane + L::TM_DP + ch * 32, dpv);
-        uint32_t ppk[16], dpk[16];
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sv[32];
+        tmem_ld_x32(t_lane + L::TM_S + 64 * h + 32 * ch, sv);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int c = ch * 32 + i;
-          float p0 = ex2(fmaf(__uint_as_float(sv[i]), sl2, -lse2[c]));
-          float p1 = ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, -lse2[c + 1]));
-          if (c < first_visible) p0 = 0.f;
-          if (c + 1 < first_visible) p1 = 0.f;
-          const float d0 = p0 * (__uint_as_float(dpv[i]) - dlt[c]);
-          const float d1 = p1 * (__uint_as_float(dpv[i + 1]) - dlt[c + 1]);
-          ppk[i / 2] = pack2<BF16>(p0, p1);
-          dpk[i / 2] = pack2<BF16>(d0, d1);
+        for (int v = 0; v < 8; ++v) {
+          const float4 lv = l4[8 * ch + v];
+          const int c = 32 * ch + 4 * v;
+          p[c + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
+          p[c + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
+          p[c + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
+          p[c + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
         }
-        // 16-bit P^T / dS^T overwrite columns of S^T / dP^T this thread has already read.
-        tmem_st_x16(t_lane + L::TM_S + ch * 16, ppk);
-        tmem_st_x16(t_lane + L::TM_DP + ch * 16, dpk);
+      }
+      if (first_visible > 0) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < first_visible) p[c] = 0.f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+        tmem_st_x32(t_lane + L::TM_S + 64 * h, pk);  // over columns this thread has read
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(K_PFULL));
+      mbar_arrive(bar(K_PREADY));
+      // Phase 2: dS^T = P^T (dP^T - D) (overlaps the dV product).
+      if (!(ok = mbar_wait_warp(bar(K_DPFULL), t & 1, wc))) break;
+      tc_fence_after();
+      uint32_t dk[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dv[32];
+        tmem_ld_x32(t_lane + L::TM_DP + 64 * h + 32 * ch, dv);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 dd = d4[8 * ch + v];
+          const int c = 32 * ch + 4 * v;
+          dk[c / 2] = pack2<BF16>(p[c] * (__uint_as_float(dv[4 * v]) - dd.x),
+                                  p[c + 1] * (__uint_as_float(dv[4 * v + 1]) - dd.y));
+          dk[c / 2 + 1] = pack2<BF16>(p[c + 2] * (__uint_as_float(dv[4 * v + 2]) - dd.z),
+                                      p[c + 3] * (__uint_as_float(dv[4 * v + 3]) - dd.w));
+        }
+      }
+      tmem_st_x32(t_lane + L::TM_DP + 64 * h, dk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(K_DSREADY));
     }
-    if (ok) ok = mbar_wait_warp(bar(K_MM2), (n_iter - 1) & 1, wc);
+    if (ok) ok = mbar_wait_warp(bar(K_DONE), 0, wc);
+    // Epilogue: warpgroup 1 writes dV, warpgroup 2 writes scale * dK, each through a
+    // swizzled staging tile over the stage-0 dO / Q buffers (every product is done).
+    uint8_t* stage = smem + L::OFF_ST + (h == 0 ? L::S_DO : L::S_Q);
     if (ok) {
       tc_fence_after();
-      // All products are done: the stage-0 Q and dO buffers become staging tiles.
-      uint8_t* st_dk = smem + L::OFF_ST + L::S_Q;
-      uint8_t* st_dv = smem + L::OFF_ST + L::S_DO;
+      const uint32_t col = (h == 0) ? L::TM_DV : L::TM_DK;
+      const float mul = (h == 0) ? 1.f : a.scale;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld_x32(t_lane + L::TM_DV + cc * 32, v);
-        stage_row_chunk<D, BF16>(st_dv, row, cc, v, 1.f);
-        tmem_ld_x32(t_lane + L::TM_DK + cc * 32, v);
-        stage_row_chunk<D, BF16>(st_dk, row, cc, v, a.scale);
+        tmem_ld_x32(t_lane + col + cc * 32, v);
+        stage_row_chunk<D, BF16>(stage, row, cc, v, mul);
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0 && !*abort_flag) {
-      for (int kb = 0; kb < T::KB; ++kb) {
-        tma_store_3d(&a.tm_dk, sb + L::OFF_ST + L::S_Q + kb * T::BLK, kb * 64, k0, bh);
-        tma_store_3d(&a.tm_dv, sb + L::OFF_ST + L::S_DO + kb * T::BLK, kb * 64, k0, bh);
-      }
+    named_bar_sync(1 + h, 128);
+    if ((warp & 3) == 0 && lane == 0 && ok && !*abort_flag) {
+      const CUtensorMap* m = (h == 0) ? &a.tm_dv : &a.tm_dk;
+      for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(m, smem_u32(stage) + kb * T::BLK, kb * 64, k0, bh);
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -333,6 +375,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 }
 
 // ------------------------------------------------------------------ bwd_dq
+//
+// Same warp roles; warpgroup 1 handles keys 0-63 of every key tile, warpgroup 2
+// keys 64-127.  dS has its own tensor-memory columns, so the MMA warp can issue
+// the next tile's S as soon as the element-wise warps have read this one:
+//   S(j) | dP(j) | S(j+1) | dQ += dS(j) K_j | dP(j+1) | S(j+2) | ...
+// P = ex2(c S - LSE2) is computed while dP runs, dS = P (dP - D) while the next S
+// runs.
 
 template <int D>
 struct DqLayout {
@@ -349,14 +398,15 @@ struct DqLayout {
 
 enum : int {
   Q_QFULL = 0,
-  Q_SFULL = 1,
-  Q_SFREE = 2,
-  Q_DSFULL = 3,
-  Q_DQDONE = 4,
-  Q_DRAIN = 5,
-  Q_KVFULL = 6,  // + stage
-  Q_EMPTY = 10,  // + stage
-  Q_COUNT = 14
+  Q_SFULL = 1,    // S computed (MMA commit)
+  Q_DPFULL = 2,   // dP computed (MMA commit)
+  Q_SCONS = 3,    // S read by both warpgroups (256 arrivals)
+  Q_DSREADY = 4,  // dS written (256 arrivals)
+  Q_DONE = 5,
+  Q_DRAIN = 6,
+  Q_KVFULL = 7,   // + stage
+  Q_EMPTY = 11,   // + stage
+  Q_COUNT = 15
 };
 
 template <int D, bool BF16>
@@ -375,17 +425,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
-  const int qt = n_t - 1 - static_cast<int>(blockIdx.x) / a.BH;  // longest causal tiles first
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int bh = static_cast<int>(blockIdx.x) / n_t;            // head-major
+  const int qt = n_t - 1 - static_cast<int>(blockIdx.x) % n_t;  // longest causal tiles first
   const int q0 = qt * kTileM;
   const int n_kv = a.causal ? qt + 1 : n_t;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_QFULL), 1);
     mbar_init(bar(Q_SFULL), 1);
-    mbar_init(bar(Q_SFREE), 128);
-    mbar_init(bar(Q_DSFULL), 128);
-    mbar_init(bar(Q_DQDONE), 1);
+    mbar_init(bar(Q_DPFULL), 1);
+    mbar_init(bar(Q_SCONS), 256);
+    mbar_init(bar(Q_DSREADY), 256);
+    mbar_init(bar(Q_DONE), 1);
     mbar_init(bar(Q_DRAIN), 1);
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(bar(Q_KVFULL + s), 1);
@@ -434,103 +485,120 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);
       constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);
-      bool ok = mbar_wait(bar(Q_QFULL), 0, wc);
-      auto issue_dq = [&](int t) -> bool {
-        const int s = t % L::STAGES;
-        if (!mbar_wait(bar(Q_DSFULL), t & 1, wc)) return false;
-        tc_fence_after();
-        const uint32_t kbase = sb + L::OFF_K + s * T::TILE;
-#pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)
-          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DS + k * 8, sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g,
-                 (t > 0 || k > 0) ? 1u : 0u);
-        tc_commit(bar(Q_DQDONE));
-        tc_commit(bar(Q_EMPTY + s));
-        return true;
-      };
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % L::STAGES;
-        if (!mbar_wait(bar(Q_KVFULL + s), (j / L::STAGES) & 1, wc)) { ok = false; break; }
-        if (j > 0 && !mbar_wait(bar(Q_SFREE), (j - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kbase = sb + L::OFF_K + s * T::TILE;
-        const uint32_t vbase = sb + L::OFF_V + s * T::TILE;
+      auto kv_full = [&](int j) { return mbar_wait(bar(Q_KVFULL + j % L::STAGES), (j / L::STAGES) & 1, wc); };
+      auto issue_s = [&](int j) {
+        const uint32_t kbase = sb + L::OFF_K + (j % L::STAGES) * T::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
           mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_Q + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
                  idesc_s, k > 0 ? 1u : 0u);
         }
+        tc_commit(bar(Q_SFULL));
+      };
+      auto issue_dp = [&](int j) {
+        const uint32_t vbase = sb + L::OFF_V + (j % L::STAGES) * T::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
           mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_DO + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024),
                  idesc_s, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(Q_SFULL));
-        if (j > 0 && !issue_dq(j - 1)) { ok = false; break; }
+        tc_commit(bar(Q_DPFULL));
+      };
+      bool ok = mbar_wait(bar(Q_QFULL), 0, wc) && kv_full(0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
       }
-      if (ok) issue_dq(n_kv - 1);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv) {
+          // The next S may overwrite S(j) once both warpgroups have read it.
+          if (!(ok = kv_full(j + 1) && mbar_wait(bar(Q_SCONS), j & 1, wc))) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
+        if (!(ok = mbar_wait(bar(Q_DSREADY), j & 1, wc))) break;
+        tc_fence_after();
+        const uint32_t kbase = sb + L::OFF_K + (j % L::STAGES) * T::TILE;
+#pragma unroll
+        for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of half h at TM_DS + 32h
+          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DS + 32 * (k >> 2) + 8 * (k & 3),
+                 sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g, (j > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(Q_EMPTY + j % L::STAGES));
+        if (j + 1 < n_kv) issue_dp(j + 1);  // dP(j) was read before dS(j) was published
+      }
+      if (ok) tc_commit(bar(Q_DONE));
       tc_commit(bar(Q_DRAIN));
       mbar_wait(bar(Q_DRAIN), 0, wc);
     }
-  } else {
+  } else if (warp >= 4) {
+    const int h = (warp >> 2) - 1;  // key half of every tile this warpgroup handles
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const int grow = q0 + row;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sl2 = a.scale_log2;
-    const size_t w = static_cast<size_t>(bh) * a.Npad + grow;   // grow < Npad always
+    const size_t w = static_cast<size_t>(bh) * a.Npad + grow;  // grow < Npad always
     const float lse2 = a.lse2[w];
     const float dlt = a.delta[w];
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait_warp(bar(Q_SFULL), j & 1, wc)) { ok = false; break; }
+      if (!(ok = mbar_wait_warp(bar(Q_SFULL), j & 1, wc))) break;
       tc_fence_after();
-      const int kbeg = j * kTileN;
-      int lim = a.N - kbeg;                               // keys past the end
-      if (a.causal) lim = min(lim, grow - kbeg + 1);      // keys after this query
-      uint32_t dsp[64];
+      const int kbeg = j * kTileN + 64 * h;
+      int lim = a.N - kbeg;                           // keys past the end
+      if (a.causal) lim = min(lim, grow - kbeg + 1);  // keys after this query
+      float p[64];
 #pragma unroll
-      for (int ch = 0; ch < kTileN / 32; ++ch) {
-        uint32_t sv[32], dpv[32];
-        tmem_ld_x32(t_lane + L::TM_S + ch * 32, sv);
-        tmem_ld_x32(t_lane + L::TM_DP + ch * 32, dpv);
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sv[32];
+        tmem_ld_x32(t_lane + L::TM_S + 64 * h + 32 * ch, sv);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int c = ch * 32 + i;
-          float p0 = ex2(fmaf(__uint_as_float(sv[i]), sl2, -lse2));
-          float p1 = ex2(fmaf(__uint_as_float(sv[i + 1]), sl2, -lse2));
-          if (c >= lim) p0 = 0.f;
-          if (c + 1 >= lim) p1 = 0.f;
-          dsp[c / 2] = pack2<BF16>(p0 * (__uint_as_float(dpv[i]) - dlt), p1 * (__uint_as_float(dpv[i + 1]) - dlt));
+        for (int e = 0; e < 32; ++e) p[32 * ch + e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
+      }
+      tc_fence_before();
+      mbar_arrive(bar(Q_SCONS));
+      if (lim < 64) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= lim) p[c] = 0.f;
+      }
+      if (!(ok = mbar_wait_warp(bar(Q_DPFULL), j & 1, wc))) break;
+      tc_fence_after();
+      uint32_t dsp[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dv[32];
+        tmem_ld_x32(t_lane + L::TM_DP + 64 * h + 32 * ch, dv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const int c = 32 * ch + e;
+          dsp[c / 2] = pack2<BF16>(p[c] * (__uint_as_float(dv[e]) - dlt), p[c + 1] * (__uint_as_float(dv[e + 1]) - dlt));
         }
       }
-      tc_fence_before();
-      mbar_arrive(bar(Q_SFREE));
-      if (j > 0) {
-        if (!mbar_wait_warp(bar(Q_DQDONE), (j - 1) & 1, wc)) { ok = false; break; }
-        tc_fence_after();
-      }
-      tmem_st_x64(t_lane + L::TM_DS, dsp);
+      // dS(j-1) in these columns was read by the dQ product that completed before dP(j).
+      tmem_st_x32(t_lane + L::TM_DS + 32 * h, dsp);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(Q_DSFULL));
+      mbar_arrive(bar(Q_DSREADY));
     }
-    if (ok) ok = mbar_wait_warp(bar(Q_DQDONE), (n_kv - 1) & 1, wc);
+    if (ok) ok = mbar_wait_warp(bar(Q_DONE), 0, wc);
     if (ok) {
       tc_fence_after();
-      uint8_t* stage = smem + L::OFF_Q;
+      uint8_t* stage = smem + L::OFF_Q;  // Q is no longer read once every product is done
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c32 = 2 * cc + h;  // this warpgroup's 32-column chunks
         uint32_t v[32];
-        tmem_ld_x32(t_lane + L::TM_DQ + cc * 32, v);
-        stage_row_chunk<D, BF16>(stage, row, cc, v, a.scale);
+        tmem_ld_x32(t_lane + L::TM_DQ + c32 * 32, v);
+        stage_row_chunk<D, BF16>(stage, row, c32, v, a.scale);
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (warp == 2 && lane == 0 && !*abort_flag) {
+    named_bar_sync(1, 256);
+    if (warp == 4 && lane == 0 && ok && !*abort_flag) {
       for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(&a.tm_dq, sb + L::OFF_Q + kb * T::BLK, kb * 64, q0, bh);
       bulk_commit();
       bulk_wait_read_all();

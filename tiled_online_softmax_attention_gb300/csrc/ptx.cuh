@@ -281,6 +281,16 @@ __device__ __forceinline__ void tmem_ld_x128(uint32_t taddr, uint32_t (&r)[128])
       : "memory");
 }
 
+// r[0..8) -> 8 consecutive 32-bit columns of this thread's TMEM lane (asynchronous;
+// tmem_st_wait() makes it complete).
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+      :
+      : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
 // r[0..16) -> 16 consecutive 32-bit columns of this thread's TMEM lane (asynchronous;
 // tmem_st_wait() makes it complete).
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&r)[16]) {
