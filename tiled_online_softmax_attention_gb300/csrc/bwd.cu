@@ -166,8 +166,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileN - 1) / kTileN;
-  const int bh = static_cast<int>(blockIdx.x) / n_t;  // head-major; low key tiles see the most queries
-  const int kt = static_cast<int>(blockIdx.x) % n_t;
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const int bh = wi.bh;
+  const int kt = wi.rank;  // low key tiles see the most queries: they go first
   const int k0 = kt * kTileN;
   const int i_begin = a.causal ? kt : 0;  // query tiles before the key tile are masked out
   const int n_iter = n_t - i_begin;
@@ -425,8 +426,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
-  const int bh = static_cast<int>(blockIdx.x) / n_t;            // head-major
-  const int qt = n_t - 1 - static_cast<int>(blockIdx.x) % n_t;  // longest causal tiles first
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const int bh = wi.bh;
+  const int qt = n_t - 1 - wi.rank;  // longest causal tiles first
   const int q0 = qt * kTileM;
   const int n_kv = a.causal ? qt + 1 : n_t;
 

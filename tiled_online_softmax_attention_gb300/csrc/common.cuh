@@ -40,6 +40,31 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
 };
 
+// Order in which CTAs take work.  Heads go in groups of up to 8: within a group
+// the CTAs walk the tile index (rank 0 first), so the CTAs running at one time
+// share a few heads' K/V in L2, and the longest causal tiles of every group start
+// before its short ones (no long tile is left for the end of the grid).
+struct WorkItem {
+  int bh;    // (batch, head)
+  int rank;  // 0 .. n_units-1 in dispatch order within the head
+};
+__device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
+  constexpr int kGroup = 8;
+  const int full = BH / kGroup;
+  const int per_group = kGroup * n_units;
+  int g, y, gs;
+  if (x < full * per_group) {
+    g = x / per_group;
+    y = x % per_group;
+    gs = kGroup;
+  } else {
+    g = full;
+    y = x - full * per_group;
+    gs = BH - full * kGroup;
+  }
+  return {g * kGroup + y % gs, y / gs};
+}
+
 // Launchers (fwd.cu / bwd.cu); return the CUDA launch status.
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);

@@ -43,7 +43,7 @@
 //
 // Causal: key tiles wholly above the diagonal are never loaded (the huaweicloud
 // page's section five, part 3); only diagonal and ragged tiles are masked.  The
-// grid is walked head by head, longest query pair first within a head.
+// grid is walked in groups of heads, longest query pairs first (work_item).
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -108,8 +108,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
   const int n_pairs = (n_t + 1) / 2;
-  const int bh = static_cast<int>(blockIdx.x) / n_pairs;
-  const int pr = n_pairs - 1 - static_cast<int>(blockIdx.x) % n_pairs;  // longest causal pair first
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_pairs);
+  const int bh = wi.bh;
+  const int pr = n_pairs - 1 - wi.rank;  // longest causal pair first
   int n_kv[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) n_kv[i] = a.causal ? min(2 * pr + i + 1, n_t) : n_t;
