@@ -31,7 +31,13 @@
 namespace attn {
 namespace {
 
-constexpr int kBwdThreads = 384;  // warp 0 TMA, warp 1 MMA, warps 2-3 idle, warpgroups 1-2 element-wise + epilogue
+// Warp roles of the two gradient kernels: warp 0 TMA, warp 1 TMEM owner + MMA issuer,
+// warps 2-3 idle, then kEw warpgroups of element-wise work, warpgroup w owning 32
+// of the 128 columns of every tile (four warps per scheduler keep the exponentials'
+// latency hidden).
+constexpr int kEw = 4;
+constexpr int kEwCols = 128 / kEw;  // tile columns per element-wise warpgroup
+constexpr int kBwdThreads = 128 * (1 + kEw);
 
 // ------------------------------------------------------------------ bwd_pre
 
@@ -110,10 +116,9 @@ __device__ __forceinline__ void stage_row_chunk(uint8_t* stage, int row, int cc,
 
 // ------------------------------------------------------------------ bwd_dkdv
 //
-// Warp roles (384 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warpgroups 1
-// and 2 the element-wise work, warpgroup 1 on queries 0-63 of every tile and
-// warpgroup 2 on queries 64-127 (every tensor-core product keeps N >= 128: the
-// tcgen05.mma issue cost does not shrink below N = 128).  Per query tile the MMA
+// Element-wise warpgroup w handles queries 32w..32w+31 of every tile (every
+// tensor-core product keeps N >= 128: the tcgen05.mma issue cost does not shrink
+// below N = 128).  Per query tile the MMA
 // warp issues, in this order,
 //   S^T = K Q^T | dP^T = V dO^T | dV += P^T dO | dK += dS^T Q
 // and the element-wise work is split in two phases so that each overlaps a
@@ -141,8 +146,8 @@ enum : int {
   K_KVFULL = 0,
   K_SFULL = 1,    // S^T computed (MMA commit)
   K_DPFULL = 2,   // dP^T computed (MMA commit)
-  K_PREADY = 3,   // P^T written (256 arrivals)
-  K_DSREADY = 4,  // dS^T written (256 arrivals)
+  K_PREADY = 3,   // P^T written (all element-wise threads)
+  K_DSREADY = 4,  // dS^T written (all element-wise threads)
   K_DONE = 5,
   K_DRAIN = 6,
   K_QFULL = 7,    // + stage
@@ -177,8 +182,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     mbar_init(bar(K_KVFULL), 1);
     mbar_init(bar(K_SFULL), 1);
     mbar_init(bar(K_DPFULL), 1);
-    mbar_init(bar(K_PREADY), 256);
-    mbar_init(bar(K_DSREADY), 256);
+    mbar_init(bar(K_PREADY), 128 * kEw);
+    mbar_init(bar(K_DSREADY), 128 * kEw);
     mbar_init(bar(K_DONE), 1);
     mbar_init(bar(K_DRAIN), 1);
     for (int s = 0; s < L::STAGES; ++s) {
@@ -257,14 +262,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         if (!(ok = mbar_wait(bar(K_PREADY), t & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of half h at S^T + 64h
-          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + 64 * (k >> 2) + 8 * (k & 3),
+        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
+          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
                  sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
         if (!(ok = mbar_wait(bar(K_DSREADY), t & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < kTileM / 16; ++k)
-          mma_ts(tmem + L::TM_DK, tmem + L::TM_DP + 64 * (k >> 2) + 8 * (k & 3),
+          mma_ts(tmem + L::TM_DK, tmem + L::TM_DP + kEwCols * (k >> 1) + 8 * (k & 1),
                  sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
         tc_commit(bar(K_EMPTY + s));
       }
@@ -273,10 +278,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       mbar_wait(bar(K_DRAIN), 0, wc);
     }
   } else if (warp >= 4) {
-    const int h = (warp >> 2) - 1;      // query half of every tile this warpgroup handles
+    const int h = (warp >> 2) - 1;      // this warpgroup's 32 query columns of every tile
     const int wq = warp & 3;
     const int row = wq * 32 + lane;     // key row within the tile == TMEM lane
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t t_s = t_lane + L::TM_S + kEwCols * h, t_dp = t_lane + L::TM_DP + kEwCols * h;
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int t = 0; t < n_iter; ++t) {
@@ -285,36 +291,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       if (!(ok = mbar_wait_warp(bar(K_QFULL + s), (t / L::STAGES) & 1, wc))) break;
       if (!(ok = mbar_wait_warp(bar(K_SFULL), t & 1, wc))) break;
       tc_fence_after();
-      const float4* l4 = reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_L) + 16 * h;
-      const float4* d4 = reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D) + 16 * h;
+      const float4* l4 =
+          reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_L) + (kEwCols / 4) * h;
+      const float4* d4 =
+          reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D) + (kEwCols / 4) * h;
       // causal diagonal tile: query c sees key `row` only if c >= row
-      const int first_visible = (a.causal && qt == kt) ? row - 64 * h : 0;  // relative to this half
-      float p[64];
-      // Phase 1: P^T for this half's 64 queries (overlaps the dP^T product).
+      const int first_visible = (a.causal && qt == kt) ? row - kEwCols * h : 0;  // relative to these columns
+      float p[kEwCols];
+      // Phase 1: P^T for this warpgroup's queries (overlaps the dP^T product).
+      {
+        uint32_t sv[kEwCols];
+        tmem_ld_x32(t_s, sv);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sv[32];
-        tmem_ld_x32(t_lane + L::TM_S + 64 * h + 32 * ch, sv);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 lv = l4[8 * ch + v];
-          const int c = 32 * ch + 4 * v;
-          p[c + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
-          p[c + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
-          p[c + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
-          p[c + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
+        for (int v = 0; v < kEwCols / 4; ++v) {
+          const float4 lv = l4[v];
+          p[4 * v + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
+          p[4 * v + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
+          p[4 * v + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
+          p[4 * v + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
         }
       }
       if (first_visible > 0) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kEwCols; ++c)
           if (c < first_visible) p[c] = 0.f;
       }
       {
-        uint32_t pk[32];
+        uint32_t pk[kEwCols / 2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
-        tmem_st_x32(t_lane + L::TM_S + 64 * h, pk);  // over columns this thread has read
+        for (int c = 0; c < kEwCols; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+        tmem_st_x16(t_s, pk);  // over columns this thread has read
       }
       tmem_st_wait();
       tc_fence_before();
@@ -322,45 +328,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       // Phase 2: dS^T = P^T (dP^T - D) (overlaps the dV product).
       if (!(ok = mbar_wait_warp(bar(K_DPFULL), t & 1, wc))) break;
       tc_fence_after();
-      uint32_t dk[32];
+      {
+        uint32_t dv[kEwCols], dk[kEwCols / 2];
+        tmem_ld_x32(t_dp, dv);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t dv[32];
-        tmem_ld_x32(t_lane + L::TM_DP + 64 * h + 32 * ch, dv);
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 dd = d4[8 * ch + v];
-          const int c = 32 * ch + 4 * v;
-          dk[c / 2] = pack2<BF16>(p[c] * (__uint_as_float(dv[4 * v]) - dd.x),
-                                  p[c + 1] * (__uint_as_float(dv[4 * v + 1]) - dd.y));
-          dk[c / 2 + 1] = pack2<BF16>(p[c + 2] * (__uint_as_float(dv[4 * v + 2]) - dd.z),
-                                      p[c + 3] * (__uint_as_float(dv[4 * v + 3]) - dd.w));
+        for (int v = 0; v < kEwCols / 4; ++v) {
+          const float4 dd = d4[v];
+          dk[2 * v] = pack2<BF16>(p[4 * v] * (__uint_as_float(dv[4 * v]) - dd.x),
+                                  p[4 * v + 1] * (__uint_as_float(dv[4 * v + 1]) - dd.y));
+          dk[2 * v + 1] = pack2<BF16>(p[4 * v + 2] * (__uint_as_float(dv[4 * v + 2]) - dd.z),
+                                      p[4 * v + 3] * (__uint_as_float(dv[4 * v + 3]) - dd.w));
         }
+        tmem_st_x16(t_dp, dk);
       }
-      tmem_st_x32(t_lane + L::TM_DP + 64 * h, dk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(K_DSREADY));
     }
     if (ok) ok = mbar_wait_warp(bar(K_DONE), 0, wc);
-    // Epilogue: warpgroup 1 writes dV, warpgroup 2 writes scale * dK, each through a
-    // swizzled staging tile over the stage-0 dO / Q buffers (every product is done).
-    uint8_t* stage = smem + L::OFF_ST + (h == 0 ? L::S_DO : L::S_Q);
+    // Epilogue: warpgroups 0-1 write dV, 2-3 write scale * dK (each half of the d
+    // columns), through swizzled staging tiles over the stage-0 dO / Q buffers
+    // (every product is done).
+    const int which = h >> 1;  // 0: dV, 1: dK
+    uint8_t* stage = smem + L::OFF_ST + (which == 0 ? L::S_DO : L::S_Q);
     if (ok) {
       tc_fence_after();
-      const uint32_t col = (h == 0) ? L::TM_DV : L::TM_DK;
-      const float mul = (h == 0) ? 1.f : a.scale;
+      const uint32_t col = (which == 0) ? L::TM_DV : L::TM_DK;
+      const float mul = (which == 0) ? 1.f : a.scale;
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = (h & 1) * (D / 64); cc < ((h & 1) + 1) * (D / 64); ++cc) {
         uint32_t v[32];
         tmem_ld_x32(t_lane + col + cc * 32, v);
         stage_row_chunk<D, BF16>(stage, row, cc, v, mul);
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1 + h, 128);
-    if ((warp & 3) == 0 && lane == 0 && ok && !*abort_flag) {
-      const CUtensorMap* m = (h == 0) ? &a.tm_dv : &a.tm_dk;
+    named_bar_sync(1 + which, 256);
+    if ((h & 1) == 0 && (warp & 3) == 0 && lane == 0 && ok && !*abort_flag) {
+      const CUtensorMap* m = (which == 0) ? &a.tm_dv : &a.tm_dk;
       for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(m, smem_u32(stage) + kb * T::BLK, kb * 64, k0, bh);
       bulk_commit();
       bulk_wait_read_all();
@@ -377,8 +382,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 
 // ------------------------------------------------------------------ bwd_dq
 //
-// Same warp roles; warpgroup 1 handles keys 0-63 of every key tile, warpgroup 2
-// keys 64-127.  dS has its own tensor-memory columns, so the MMA warp can issue
+// Same warp roles; element-wise warpgroup w handles keys 32w..32w+31 of every
+// key tile.  dS has its own tensor-memory columns, so the MMA warp can issue
 // the next tile's S as soon as the element-wise warps have read this one:
 //   S(j) | dP(j) | S(j+1) | dQ += dS(j) K_j | dP(j+1) | S(j+2) | ...
 // P = ex2(c S - LSE2) is computed while dP runs, dS = P (dP - D) while the next S
@@ -401,8 +406,8 @@ enum : int {
   Q_QFULL = 0,
   Q_SFULL = 1,    // S computed (MMA commit)
   Q_DPFULL = 2,   // dP computed (MMA commit)
-  Q_SCONS = 3,    // S read by both warpgroups (256 arrivals)
-  Q_DSREADY = 4,  // dS written (256 arrivals)
+  Q_SCONS = 3,    // S read by every element-wise thread
+  Q_DSREADY = 4,  // dS written by every element-wise thread
   Q_DONE = 5,
   Q_DRAIN = 6,
   Q_KVFULL = 7,   // + stage
@@ -436,8 +441,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     mbar_init(bar(Q_QFULL), 1);
     mbar_init(bar(Q_SFULL), 1);
     mbar_init(bar(Q_DPFULL), 1);
-    mbar_init(bar(Q_SCONS), 256);
-    mbar_init(bar(Q_DSREADY), 256);
+    mbar_init(bar(Q_SCONS), 128 * kEw);
+    mbar_init(bar(Q_DSREADY), 128 * kEw);
     mbar_init(bar(Q_DONE), 1);
     mbar_init(bar(Q_DRAIN), 1);
     for (int s = 0; s < L::STAGES; ++s) {
@@ -525,8 +530,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tc_fence_after();
         const uint32_t kbase = sb + L::OFF_K + (j % L::STAGES) * T::TILE;
 #pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of half h at TM_DS + 32h
-          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DS + 32 * (k >> 2) + 8 * (k & 3),
+        for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of keys 2c, 2c+1 in column c
+          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DS + 8 * k,
                  sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g, (j > 0 || k > 0) ? 1u : 0u);
         tc_commit(bar(Q_EMPTY + j % L::STAGES));
         if (j + 1 < n_kv) issue_dp(j + 1);  // dP(j) was read before dS(j) was published
@@ -536,7 +541,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       mbar_wait(bar(Q_DRAIN), 0, wc);
     }
   } else if (warp >= 4) {
-    const int h = (warp >> 2) - 1;  // key half of every tile this warpgroup handles
+    const int h = (warp >> 2) - 1;  // this warpgroup's 32 key columns of every tile
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const int grow = q0 + row;
@@ -549,39 +554,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = mbar_wait_warp(bar(Q_SFULL), j & 1, wc))) break;
       tc_fence_after();
-      const int kbeg = j * kTileN + 64 * h;
+      const int kbeg = j * kTileN + kEwCols * h;
       int lim = a.N - kbeg;                           // keys past the end
       if (a.causal) lim = min(lim, grow - kbeg + 1);  // keys after this query
-      float p[64];
+      float p[kEwCols];
+      {
+        uint32_t sv[kEwCols];
+        tmem_ld_x32(t_lane + L::TM_S + kEwCols * h, sv);
+        tc_fence_before();
+        mbar_arrive(bar(Q_SCONS));
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sv[32];
-        tmem_ld_x32(t_lane + L::TM_S + 64 * h + 32 * ch, sv);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) p[32 * ch + e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
+        for (int e = 0; e < kEwCols; ++e) p[e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
       }
-      tc_fence_before();
-      mbar_arrive(bar(Q_SCONS));
-      if (lim < 64) {
+      if (lim < kEwCols) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
+        for (int c = 0; c < kEwCols; ++c)
           if (c >= lim) p[c] = 0.f;
       }
       if (!(ok = mbar_wait_warp(bar(Q_DPFULL), j & 1, wc))) break;
       tc_fence_after();
-      uint32_t dsp[32];
+      {
+        uint32_t dv[kEwCols], dsp[kEwCols / 2];
+        tmem_ld_x32(t_lane + L::TM_DP + kEwCols * h, dv);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t dv[32];
-        tmem_ld_x32(t_lane + L::TM_DP + 64 * h + 32 * ch, dv);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int c = 32 * ch + e;
-          dsp[c / 2] = pack2<BF16>(p[c] * (__uint_as_float(dv[e]) - dlt), p[c + 1] * (__uint_as_float(dv[e + 1]) - dlt));
-        }
+        for (int e = 0; e < kEwCols; e += 2)
+          dsp[e / 2] = pack2<BF16>(p[e] * (__uint_as_float(dv[e]) - dlt), p[e + 1] * (__uint_as_float(dv[e + 1]) - dlt));
+        // dS(j-1) in these columns was read by the dQ product that completed before dP(j).
+        tmem_st_x16(t_lane + L::TM_DS + (kEwCols / 2) * h, dsp);
       }
-      // dS(j-1) in these columns was read by the dQ product that completed before dP(j).
-      tmem_st_x32(t_lane + L::TM_DS + 32 * h, dsp);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(Q_DSREADY));
@@ -591,15 +591,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       tc_fence_after();
       uint8_t* stage = smem + L::OFF_Q;  // Q is no longer read once every product is done
 #pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c32 = 2 * cc + h;  // this warpgroup's 32-column chunks
+      for (int c32 = h; c32 < D / 32; c32 += kEw) {  // this warpgroup's 32-column chunks
         uint32_t v[32];
         tmem_ld_x32(t_lane + L::TM_DQ + c32 * 32, v);
         stage_row_chunk<D, BF16>(stage, row, c32, v, a.scale);
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 256);
+    named_bar_sync(1, 128 * kEw);
     if (warp == 4 && lane == 0 && ok && !*abort_flag) {
       for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(&a.tm_dq, sb + L::OFF_Q + kb * T::BLK, kb * 64, q0, bh);
       bulk_commit();

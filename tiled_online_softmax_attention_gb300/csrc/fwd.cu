@@ -262,13 +262,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tc_fence_after();
       float s[128];
       {
+        // Four loads in flight, one wait: a TMEM load issued while the tensor core
+        // runs the other tile's products takes several times its idle latency.
+        uint32_t sr[128];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t sr[64];
-          tmem_ld_x64(t_s + 64 * h, sr);
+        for (int q = 0; q < 4; ++q) tmem_ld_x32_async(t_s + 32 * q, sr + 32 * q);
+        tmem_ld_wait(sr);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) s[64 * h + c] = __uint_as_float(sr[c]);
-        }
+        for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       }
       const int k0 = j * kTileN;
       const bool tail = k0 + kTileN > a.N;
