@@ -264,35 +264,91 @@ def run_ours(args, w, ws_, rank, local):
 
 
 def run_e2e(args, w, x, dev, ws_):
-    """Same metric through the public API with host buffers: pinned H2D of Q, K, V, dO and D2H of the
-    three gradients inside the timed region, every step."""
+    """Same metric through the public API with host buffers: every step copies its Q, K, V,
+    dO from pinned host memory to the device and its three gradients back, inside the
+    timed region.  Reported two ways: serial (copy in, compute, copy out, one stream) and
+    pipelined (double-buffered: step k+1's inputs and step k-1's gradients move on copy
+    streams while step k computes, as a training loop would overlap them)."""
     import tiled_online_softmax_attention_gb300 as attn
 
     hq, hk, hv, hdo = (x[n].pin_memory() for n in ("q", "k", "v", "dout"))
-    outs = [torch.empty_like(hq).pin_memory() for _ in range(3)]
+    hin = (hq, hk, hv, hdo)
+    hout = [[torch.empty_like(hq).pin_memory() for _ in range(3)] for _ in range(2)]
     steps = max(3, min(args.steps, 50))
+    nb = hq.numel() * hq.element_size()
+    B, H, N = w.B, w.H, w.N
 
-    def one():
-        q, k, v, do = (t.to(dev, non_blocking=True) for t in (hq, hk, hv, hdo))
+    def serial_step():
+        q, k, v, do = (t.to(dev, non_blocking=True) for t in hin)
         o, lse = attn.forward(q, k, v, causal=True, scale=w.scale)
         g = attn.backward(q, k, v, o, lse, do, causal=True, scale=w.scale)
-        for h, t in zip(outs, g):
+        for h, t in zip(hout[0], g):
             h.copy_(t, non_blocking=True)
 
-    for _ in range(3):
-        one()
-    barrier(ws_)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
-    torch.cuda.synchronize()
-    ms = allreduce_max(a.elapsed_time(b), ws_, dev)
-    nb = hq.numel() * hq.element_size()
-    return {"value": ws_ * steps * step_flops(w) / (ms * 1e-3) / 1e12, "unit": UNIT,
-            "h2d_bytes_per_step": 4 * nb, "d2h_bytes_per_step": 3 * nb, "steps": steps}
+    def timed(fn):
+        for i in range(3):
+            fn(i, 3)
+        torch.cuda.synchronize()
+        barrier(ws_)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(steps):
+            fn(i, steps)
+        torch.cuda.current_stream().wait_stream(h2d)
+        torch.cuda.current_stream().wait_stream(d2h)
+        b.record()
+        torch.cuda.synchronize()
+        return allreduce_max(a.elapsed_time(b), ws_, dev)
+
+    # pipelined: two device input sets and two output sets
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    comp = torch.cuda.current_stream(dev)
+    din = [[torch.empty_like(t, device=dev) for t in hin] for _ in range(2)]
+    dres = [(torch.empty_like(din[0][0]), torch.empty((B, H, N), device=dev, dtype=torch.float32),
+             torch.empty_like(din[0][0]), torch.empty_like(din[0][0]), torch.empty_like(din[0][0]))
+            for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    out_ready = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+    for e in in_free + out_free:
+        e.record(comp)
+
+    def load(i):
+        s = i % 2
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(in_free[s])
+            for dt, ht in zip(din[s], hin):
+                dt.copy_(ht, non_blocking=True)
+            in_ready[s].record(h2d)
+
+    def pipelined_step(i, n):
+        s = i % 2
+        if i == 0:
+            load(0)
+        if i + 1 < n:
+            load(i + 1)  # the next step's inputs move while this one computes
+        comp.wait_event(in_ready[s])
+        comp.wait_event(out_free[s])
+        q, k, v, do = din[s]
+        o, lse, dq, dk, dv = dres[s]
+        attn.forward(q, k, v, causal=True, scale=w.scale, out=(o, lse))
+        attn.backward(q, k, v, o, lse, do, causal=True, scale=w.scale, out=(dq, dk, dv))
+        in_free[s].record(comp)
+        out_ready[s].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(out_ready[s])
+            for ht, dt in zip(hout[s], (dq, dk, dv)):
+                ht.copy_(dt, non_blocking=True)
+            out_free[s].record(d2h)
+
+    ms_serial = timed(lambda i, n: serial_step())
+    ms_pipe = timed(pipelined_step)
+    flops = step_flops(w)
+    return {"value": ws_ * steps * flops / (ms_pipe * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": 4 * nb, "d2h_bytes_per_step": 3 * nb, "steps": steps,
+            "mode": "pipelined: step k+1's H2D and step k-1's D2H overlap step k's kernels",
+            "serial_value": ws_ * steps * flops / (ms_serial * 1e-3) / 1e12}
 
 
 def long_forward(attn, dev):

@@ -41,49 +41,67 @@ constexpr int kBwdThreads = 128 * (1 + kEw);
 
 // ------------------------------------------------------------------ bwd_pre
 
+// D = D/8 lanes per row, 16 bytes of O and of dO per lane; a warp covers 32/(D/8) rows
+// per step and kPreUnroll steps with every load issued before any arithmetic.
+constexpr int kPreUnroll = 4;
+
+template <int D, bool BF16>
+__device__ __forceinline__ float dot8(const uint4& x, const uint4& y) {
+  const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float x0, x1, y0, y1;
+    if constexpr (BF16) {
+      x0 = __uint_as_float(xs[i] << 16);
+      x1 = __uint_as_float(xs[i] & 0xffff0000u);
+      y0 = __uint_as_float(ys[i] << 16);
+      y1 = __uint_as_float(ys[i] & 0xffff0000u);
+    } else {
+      const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xs[i]));
+      const float2 yf = __half22float2(*reinterpret_cast<const __half2*>(&ys[i]));
+      x0 = xf.x, x1 = xf.y, y0 = yf.x, y1 = yf.y;
+    }
+    acc = fmaf(x0, y0, acc);
+    acc = fmaf(x1, y1, acc);
+  }
+  return acc;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int LPR = D / 8;         // lanes per row
+  constexpr int RPW = 32 / LPR;      // rows per warp step
   const int lane = threadIdx.x & 31;
+  const int64_t warp_global = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t rows = static_cast<int64_t>(a.BH) * a.Npad;
-  if (warp_global >= rows) return;
-  const int bh = static_cast<int>(warp_global / a.Npad);
-  const int r = static_cast<int>(warp_global % a.Npad);
-  float dsum = 0.f;
-  float l2 = INFINITY;
-  if (r < a.N) {
-    const size_t base = (static_cast<size_t>(bh) * a.N + r) * D;
-    constexpr int PER = D / 32;  // 16-bit elements per lane (2 or 4)
-    const uint16_t* op = reinterpret_cast<const uint16_t*>(a.o) + base + lane * PER;
-    const uint16_t* dp = reinterpret_cast<const uint16_t*>(a.dout) + base + lane * PER;
-    uint16_t ov[PER], dv[PER];
-    if constexpr (PER == 4) {
-      *reinterpret_cast<uint2*>(ov) = *reinterpret_cast<const uint2*>(op);
-      *reinterpret_cast<uint2*>(dv) = *reinterpret_cast<const uint2*>(dp);
-    } else {
-      *reinterpret_cast<uint32_t*>(ov) = *reinterpret_cast<const uint32_t*>(op);
-      *reinterpret_cast<uint32_t*>(dv) = *reinterpret_cast<const uint32_t*>(dp);
-    }
+  const int sub = lane / LPR, col = lane % LPR;
+  uint4 ov[kPreUnroll], dv[kPreUnroll];
+  int64_t rr[kPreUnroll];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      float x, y;
-      if constexpr (BF16) {
-        x = __uint_as_float(static_cast<uint32_t>(ov[i]) << 16);
-        y = __uint_as_float(static_cast<uint32_t>(dv[i]) << 16);
-      } else {
-        x = __half2float(__ushort_as_half(ov[i]));
-        y = __half2float(__ushort_as_half(dv[i]));
+  for (int u = 0; u < kPreUnroll; ++u) {
+    rr[u] = (warp_global * kPreUnroll + u) * RPW + sub;
+    ov[u] = dv[u] = make_uint4(0, 0, 0, 0);
+    if (rr[u] < rows) {
+      const int bh = static_cast<int>(rr[u] / a.Npad), r = static_cast<int>(rr[u] % a.Npad);
+      if (r < a.N) {
+        const size_t off = ((static_cast<size_t>(bh) * a.N + r) * D) * 2 + col * 16;
+        ov[u] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.o) + off);
+        dv[u] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off);
       }
-      dsum = fmaf(x, y, dsum);
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
-    l2 = a.lse[static_cast<size_t>(bh) * a.N + r] * 1.4426950408889634f;
   }
-  if (lane == 0) {
-    const size_t w = static_cast<size_t>(bh) * a.Npad + r;
-    a.delta[w] = dsum;
-    a.lse2[w] = l2;
+#pragma unroll
+  for (int u = 0; u < kPreUnroll; ++u) {
+    float dsum = dot8<D, BF16>(ov[u], dv[u]);
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+    if (col == 0 && rr[u] < rows) {
+      const int bh = static_cast<int>(rr[u] / a.Npad), r = static_cast<int>(rr[u] % a.Npad);
+      const size_t w = static_cast<size_t>(bh) * a.Npad + r;
+      a.delta[w] = (r < a.N) ? dsum : 0.f;
+      a.lse2[w] = (r < a.N) ? a.lse[static_cast<size_t>(bh) * a.N + r] * 1.4426950408889634f : INFINITY;
+    }
   }
 }
 
@@ -617,7 +635,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 template <int D, bool BF16>
 cudaError_t launch_pre_t(const BwdArgs& a, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(a.BH) * a.Npad;
-  const int64_t blocks = (rows * 32 + 255) / 256;
+  const int64_t rows_per_block = (256 / 32) * kPreUnroll * (32 / (D / 8));
+  const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
   bwd_pre_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
