@@ -373,7 +373,44 @@ def long_forward(attn, dev):
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / reps
         out["causal" if causal else "non_causal"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
-    return {"long_forward_B1_H32_N16384_d128": out}
+    res = {"long_forward_B1_H32_N16384_d128": out}
+    res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
+    return res
+
+
+def split_forward(attn, dev):
+    """One head of 16384 tokens: 64 query-tile pairs cannot fill 152 SMs alone; the
+    split-KV forward cuts each pair's keys into ranges (then merges them)."""
+    B, H, N, d = 1, 1, 16384, 128
+    x = workloads.draw(B, H, N, d, "bf16", seed=5)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    sc = 1.0 / math.sqrt(d)
+    out = {}
+    for causal in (False, True):
+        f = workloads.fwd_flops(B, H, N, d, causal)
+        ent = {}
+        for ns in (1, 2, 4, 8):
+            nb = attn.attn_fwd_splitkv_workspace_bytes(B, H, N, d, ns)
+            ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+            if ns == 1:
+                call = lambda: attn.attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, sc)
+            else:
+                call = lambda: attn.attn_fwd_splitkv(q, k, v, o, lse, ws, nb, B, H, N, d, q.dtype, causal, sc, ns)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(20):
+                call()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / 20
+            ent["attn_fwd" if ns == 1 else f"splits_{ns}"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+        out["causal" if causal else "non_causal"] = ent
+    return out
 
 
 # ---------------------------------------------------------------- oracle (CPU) timings

@@ -83,6 +83,29 @@ ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void 
                      int *dev_status, void *stream);
 
 /*
+ * attn_fwd_splitkv -- the forward pass for shapes with too few query tiles to fill
+ * the GPU (few heads, long sequences): every pair of 128-row query tiles has its key
+ * tiles cut into n_splits contiguous ranges, each processed by its own CTA, which
+ * writes its range's normalised partial output and logsumexp; a merge kernel then
+ * combines the ranges with the two-block merge rule of "FlashAttention
+ * hardware-aware analysis" (huaweicloud), section two:
+ *   M = max_s lse_s,  O = sum_s e^(lse_s - M) O_s / sum_s e^(lse_s - M),
+ *   lse = M + ln sum_s e^(lse_s - M).
+ * Results equal attn_fwd's up to rounding (the partials are kept in float32).
+ *   n_splits  : 1..64; a pair with fewer visible key tiles than n_splits uses as
+ *               many ranges as it has tiles.
+ *   workspace : device scratch of attn_fwd_splitkv_workspace_bytes(B, H, N, d,
+ *               n_splits) = n_splits*B*H*N*(d+1)*4 bytes, 16-byte aligned, owned by
+ *               the caller, clobbered.  It must not overlap any other argument.
+ * Everything else (layouts, causal, scale, errors) is as for attn_fwd.
+ */
+ATTN_API size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
+ATTN_API attn_status attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                             void *workspace, size_t workspace_bytes,
+                             int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                             int n_splits, int *dev_status, void *stream);
+
+/*
  * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd needs:
  * two float32 vectors per row (D_i = rowsum(dO_i * O_i), and the logsumexp in
  * base 2), padded to whole 128-row tiles: 2 * B*H*ceil(N/128)*128 * 4 bytes.

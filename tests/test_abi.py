@@ -109,3 +109,17 @@ def test_stage_entry_points_validate():
                               stream=0) == attn.ATTN_ERR_INVALID_ARG      # dk == dv
     assert attn.attn_bwd_dq(A[0], A[1], A[2], A[4], A[9], 1 << 20, A[6], 1, 2, 256, 80, 0, 1, 0.1,
                             stream=0) == attn.ATTN_ERR_UNSUPPORTED
+
+
+def test_splitkv_validates():
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 128, 4) == 4 * 2 * 256 * 129 * 4
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 128, 0) == 0
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 128, 65) == 0
+    args = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], workspace=A[9], workspace_bytes=1 << 24, B=1, H=2,
+                N=256, d=128, dt=0, causal=1, scale=0.088, n_splits=4, stream=0)
+    for kw, st in [(dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(n_splits=65), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG), (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=80), attn.ATTN_ERR_UNSUPPORTED)]:
+        a2 = dict(args)
+        a2.update(kw)
+        assert attn.attn_fwd_splitkv(**a2) == st, kw

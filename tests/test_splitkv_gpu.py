@@ -1,0 +1,68 @@
+"""Split-KV forward (key ranges in separate CTAs, merged by the two-block rule) against
+the FP64 oracle, element by element, and against attn_fwd."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_online_softmax_attention_gb300 as attn
+import workloads
+from gpu_util import LSE_REL, O_MAX_ABS, Guarded, f64, lse_err, o_err, run_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+def run_split(q, k, v, causal, n_splits, scale=None):
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = Guarded((B, H, N, d), q.dtype)
+    lse = Guarded((B, H, N), torch.float32)
+    nbytes = attn.attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_splitkv(q, k, v, o.t, lse.t, ws.t, nbytes, B, H, N, d, q.dtype, causal, scale, n_splits,
+                               status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert o.intact() and lse.intact() and ws.intact(), "split-KV wrote outside its buffers"
+    return o.t, lse.t
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 3, 8])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 129, 300, 1000])
+def test_splitkv_vs_oracle(N, d, causal, n_splits):
+    x = workloads.draw(1, 3, N, d, "bf16", seed=3000 + N + d + n_splits)
+    o, lse = run_split(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal, n_splits)
+    o_ref, lse_ref = oracle.attn_fwd(x["q"], x["k"], x["v"], causal, 1.0 / math.sqrt(d))
+    assert o_err(o, o_ref) <= O_MAX_ABS
+    assert lse_err(lse, lse_ref) <= LSE_REL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_long_single_head_matches_fwd(causal):
+    """One head of 16384 tokens, 4 ranges: sampled rows against the oracle, all rows
+    against attn_fwd."""
+    x = workloads.draw(1, 1, 16384, 128, "bf16", seed=77)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o, lse = run_split(q, k, v, causal, 4)
+    o1, l1 = run_fwd(q, k, v, causal)
+    assert float((o.float() - o1.float()).abs().max()) <= O_MAX_ABS
+    assert float(((lse - l1).abs() / l1.abs().clamp_min(1)).max()) <= LSE_REL
+    rows = np.array([0, 1, 127, 128, 8191, 8192, 16383])
+    o_ref, lse_ref = oracle.attn_fwd(x["q"][0, 0], x["k"][0, 0], x["v"][0, 0], causal, 1 / math.sqrt(128), rows=rows)
+    assert float(np.max(np.abs(f64(o)[0, 0, rows] - o_ref))) <= O_MAX_ABS
+    assert float(np.max(np.abs(f64(lse)[0, 0, rows] - lse_ref) / np.maximum(np.abs(lse_ref), 1))) <= LSE_REL
+
+
+def test_splitkv_stress_fp16():
+    """The numerics-stress workload (scores near +-1000, one-hot rows, uniform rows) through 3 ranges."""
+    x = workloads.inputs("c4")
+    o, lse = run_split(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), False, 3)
+    o_ref, lse_ref = oracle.attn_fwd(x["q"], x["k"], x["v"], False, 1 / math.sqrt(128))
+    assert o_err(o, o_ref) <= O_MAX_ABS
+    assert lse_err(lse, lse_ref) <= LSE_REL

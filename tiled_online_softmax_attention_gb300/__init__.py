@@ -10,6 +10,9 @@ where the C ABI takes device pointers, and ``stream=None`` means torch's
 current stream):
 
     attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
+    attn_fwd_splitkv(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, dt, causal, scale,
+                     n_splits, dev_status=None, stream=None)
     attn_bwd_workspace_bytes(B, H, N, d)
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
              B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
@@ -41,7 +44,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -66,6 +69,10 @@ def load(build_if_missing: bool = True):
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.attn_fwd.restype = I
+    lib.attn_fwd_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.attn_fwd_splitkv_workspace_bytes.restype = SZ
+    lib.attn_fwd_splitkv.argtypes = [P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, P, P]
+    lib.attn_fwd_splitkv.restype = I
     lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_bwd_workspace_bytes.restype = SZ
     lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, P, P]
@@ -123,6 +130,18 @@ def attn_status_string(status: int) -> str:
 def attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None) -> int:
     return int(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
                                _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits) -> int:
+    return int(load().attn_fwd_splitkv_workspace_bytes(int(B), int(H), int(N), int(d), int(n_splits)))
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, dt, causal, scale, n_splits,
+                     dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                       int(workspace_bytes), int(B), int(H), int(N), int(d), _dt(dt),
+                                       int(bool(causal)), float(scale), int(n_splits), _ptr(dev_status),
+                                       _stream(stream)))
 
 
 def attn_bwd_workspace_bytes(B, H, N, d) -> int:

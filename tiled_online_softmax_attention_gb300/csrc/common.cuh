@@ -13,6 +13,7 @@ constexpr int kTileN = 128;
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H][N][d], box {64, 128, 1}, 128B swizzle
+  void* o;                             // [B*H][N][d] output (the merge kernel writes it directly)
   float* lse;                          // [B*H][N]
   int* dev_status;                     // nullable
   int N;
@@ -20,6 +21,11 @@ struct FwdArgs {
   int causal;
   float scale_log2;                    // scale * log2(e)
   uint64_t wait_limit_ns;
+  // split-KV only: n_splits key ranges per query-tile pair, each writing its normalised
+  // partial output and logsumexp for the merge kernel
+  int n_splits;
+  float* part_o;                       // [n_splits][B*H][N][d] fp32
+  float* part_lse;                     // [n_splits][B*H][N] fp32 (natural log; -inf: empty range)
 };
 
 struct BwdArgs {
@@ -67,6 +73,7 @@ __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
 
 // Launchers (fwd.cu / bwd.cu); return the CUDA launch status.
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);

@@ -88,7 +88,11 @@ enum : int {
   B_COUNT = 32
 };
 
-template <int D, bool BF16>
+// SPLIT: the CTA covers one of a.n_splits contiguous ranges of the pair's key tiles and
+// writes its range's normalised partial O (fp32) and logsumexp instead of the output;
+// attn_merge_kernel combines the ranges with the two-block merge of the huaweicloud
+// page's section two.
+template <int D, bool BF16, bool SPLIT>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -108,12 +112,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
   const int n_pairs = (n_t + 1) / 2;
-  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_pairs);
+  const int split = SPLIT ? static_cast<int>(blockIdx.x) % a.n_splits : 0;
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x) / (SPLIT ? a.n_splits : 1), a.BH, n_pairs);
   const int bh = wi.bh;
   const int pr = n_pairs - 1 - wi.rank;  // longest causal pair first
-  int n_kv[2];
+  int n_kv[2];  // key tiles each query tile visits, starting at key tile kv0
 #pragma unroll
   for (int i = 0; i < 2; ++i) n_kv[i] = a.causal ? min(2 * pr + i + 1, n_t) : n_t;
+  int kv0 = 0;
+  if constexpr (SPLIT) {
+    // Ranges cut tile 0's visible tiles evenly; tile 1's one extra causal tile joins the
+    // last range.  A pair with fewer tiles than ranges leaves the surplus ranges empty.
+    const int ns = min(a.n_splits, n_kv[0]);
+    if (split >= ns) {
+      for (int r = threadIdx.x; r < 2 * kTileM; r += blockDim.x) {
+        const int grow = 2 * pr * kTileM + r;
+        if (grow < a.N) a.part_lse[(static_cast<size_t>(split) * a.BH + bh) * a.N + grow] = -INFINITY;
+      }
+      return;
+    }
+    kv0 = split * n_kv[0] / ns;
+    const int hi0 = (split + 1) * n_kv[0] / ns;
+    n_kv[1] = (split == ns - 1 ? n_kv[1] : hi0) - kv0;
+    n_kv[0] = hi0 - kv0;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -169,7 +191,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mbar_arrive_expect_tx(bar(B_KVFULL + s), L::TILE);
         for (int kb = 0; kb < L::KB; ++kb)
           tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(B_KVFULL + s), kb * 64,
-                      (ld >> 1) * kTileN, bh);
+                      (kv0 + (ld >> 1)) * kTileN, bh);
         issued = ld + 1;
       }
       // Let every copy this thread started land before the CTA can exit.
@@ -271,7 +293,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       }
-      const int k0 = j * kTileN;
+      const int k0 = (kv0 + j) * kTileN;
       const bool tail = k0 + kTileN > a.N;
       const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM);
       if (tail || diag) {
@@ -351,7 +373,27 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const bool ok_i = ok && mbar_wait_warp(bar(B_FIN + i), 0, wc) &&
                         mbar_wait_warp(bar(B_ODONE + i), (n_kv[i] - 1) & 1, wc);
       const int q0 = (2 * pr + i) * kTileM;
-      if (ok_i) {
+      if (SPLIT && ok_i) {
+        tc_fence_after();
+        const float mf = m_s[i * 128 + row];
+        const float lf = l_s[i * 128 + row];
+        const float inv_l = 1.f / lf;
+        const size_t prow = (static_cast<size_t>(split) * a.BH + bh) * a.N + q0 + row;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld_x32(t_lane + L::tm_o(i) + cc * 32, o);
+          if (q0 + row < a.N) {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                   __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+          }
+        }
+        if (q0 + row < a.N) a.part_lse[prow] = (mf + __log2f(lf)) * 0.69314718055994531f;
+      }
+      if (!SPLIT && ok_i) {
         tc_fence_after();
         const float mf = m_s[i * 128 + row];
         const float lf = l_s[i * 128 + row];
@@ -379,7 +421,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       ok = ok && ok_i;
       named_bar_sync(1, 128);
-      if (warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < a.N) {
+      if (!SPLIT && warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < a.N) {
         for (int kb = 0; kb < L::KB; ++kb)
           tma_store_3d(&a.tm_o, sb + L::OFF_Q + i * L::TILE + kb * L::BLK, kb * 64, q0, bh);
         bulk_commit();
@@ -396,23 +438,82 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool SPLIT>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   using L = FwdLayout<D>;
-  auto k = fwd_kernel<D, BF16>;
+  auto k = fwd_kernel<D, BF16, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
   const int n_pairs = (n_t + 1) / 2;
-  k<<<dim3(n_pairs * a.BH), kFwdThreads, L::SMEM, st>>>(a);
+  k<<<dim3(n_pairs * a.BH * (SPLIT ? a.n_splits : 1)), kFwdThreads, L::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+// Merge of the split-KV partials, one warp per row: M = max_s lse_s,
+// O = sum_s e^(lse_s - M) O_s / sum_s e^(lse_s - M), lse = M + ln sum_s e^(lse_s - M).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdArgs a) {
+  constexpr int PER = D / 32;  // columns per lane
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
+  const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (r >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < a.n_splits; ++s) mx = fmaxf(mx, a.part_lse[s * rows + r]);
+  float acc[PER];
+#pragma unroll
+  for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+  float den = 0.f;
+  for (int s = 0; s < a.n_splits; ++s) {
+    const float ls = a.part_lse[s * rows + r];
+    if (ls == -INFINITY) continue;  // an empty range contributes nothing
+    const float wgt = __expf(ls - mx);
+    den += wgt;
+    const float* src = a.part_o + (s * rows + r) * D + lane * PER;
+    if constexpr (PER == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] = fmaf(wgt, v.x, acc[0]);
+      acc[1] = fmaf(wgt, v.y, acc[1]);
+      acc[2] = fmaf(wgt, v.z, acc[2]);
+      acc[3] = fmaf(wgt, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] = fmaf(wgt, v.x, acc[0]);
+      acc[1] = fmaf(wgt, v.y, acc[1]);
+    }
+  }
+  const float inv = 1.f / den;
+  uint32_t pk[PER / 2];
+#pragma unroll
+  for (int c = 0; c < PER; c += 2) pk[c / 2] = pack2<BF16>(acc[c] * inv, acc[c + 1] * inv);
+  uint8_t* dst = static_cast<uint8_t*>(a.o) + (r * D + lane * PER) * 2;
+  if constexpr (PER == 4)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+  else
+    *reinterpret_cast<uint32_t*>(dst) = pk[0];
+  if (lane == 0) a.lse[r] = mx + __logf(den);
+}
+
+template <int D, bool BF16>
+cudaError_t launch_split_t(const FwdArgs& a, cudaStream_t st) {
+  cudaError_t e = launch_fwd_t<D, BF16, true>(a, st);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
+  merge_kernel<D, BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
-  if (d == 128) return bf16 ? launch_fwd_t<128, true>(a, s) : launch_fwd_t<128, false>(a, s);
-  return bf16 ? launch_fwd_t<64, true>(a, s) : launch_fwd_t<64, false>(a, s);
+  if (d == 128) return bf16 ? launch_fwd_t<128, true, false>(a, s) : launch_fwd_t<128, false, false>(a, s);
+  return bf16 ? launch_fwd_t<64, true, false>(a, s) : launch_fwd_t<64, false, false>(a, s);
+}
+
+cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 128) return bf16 ? launch_split_t<128, true>(a, s) : launch_split_t<128, false>(a, s);
+  return bf16 ? launch_split_t<64, true>(a, s) : launch_split_t<64, false>(a, s);
 }
 
 }  // namespace attn
