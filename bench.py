@@ -375,7 +375,36 @@ def long_forward(attn, dev):
         out["causal" if causal else "non_causal"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
     res = {"long_forward_B1_H32_N16384_d128": out}
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
+    res["forward_by_workload"] = forward_by_workload(attn, dev)
     return res
+
+
+def forward_by_workload(attn, dev):
+    """Forward TFLOP/s on the parity workloads c1, c2, c4 (both masks where they have them)."""
+    out = {}
+    for name in ("c1", "c2", "c4"):
+        w = workloads.WORKLOADS[name]
+        x = workloads.inputs(name)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+        for causal in w.causal:
+            call = lambda: attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, causal, w.scale)
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 50
+            a.record()
+            for _ in range(reps):
+                call()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / reps
+            f = workloads.fwd_flops(w.B, w.H, w.N, w.d, causal)
+            out[f"{name}_{'causal' if causal else 'non_causal'}"] = {"ms": round(ms, 4),
+                                                                    "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+    return out
 
 
 def split_forward(attn, dev):
