@@ -19,13 +19,21 @@ attn_fwd(q, k, v, causal, scale, rows=None) -> (o, lse)
 attn_bwd(q, k, v, dout, causal, scale, qrows=None, kcols=None) -> (dq, dk, dv)
     chain rule of the same definition ("Understanding FlashAttention,
     Part 2", section 2.4, Figs 16-19).
+dequant_e4m3(codes, scales, block_rows=128) -> float64 array
+    value of each E4M3 code times the scale of its block of rows (FP8 with
+    per-block scale factors: huaweicloud page, section four, part 3).
+attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal, scale) -> (o, lse)
+    attn_fwd of the dequantised inputs.
 
 Pins (tests/test_oracle_pins.py): hand-derived closed forms under
 tests/golden/, brute force with Python ``math`` on tiny inputs, the two-block
 merge rule of the huaweicloud page (section two), the all-equal-scores closed
 form, one-hot rows at scores near 1000, causal row 0, finite differences and
-an independent autograd evaluation for the backward, and the invariants
-sum_j dV_j = sum_i dO_i, sum_j dK_j = 0, and K/V permutation symmetry.
+an independent autograd evaluation for the backward, the invariants
+sum_j dV_j = sum_i dO_i, sum_j dK_j = 0, and K/V permutation symmetry; for
+the FP8 decoding, closed-form codes of the format definition, all 256 codes
+against PyTorch's float8_e4m3fn conversion, and a brute-force block
+dequantisation.
 """
 from __future__ import annotations
 
@@ -84,6 +92,10 @@ class Oracle:
         lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_double,
                                         P, I64, P, I64, P, P, P]
         lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = ctypes.c_double
+        lib.oracle_dequant_e4m3.argtypes = [P, P, I64, I64, I64, I64, P]
+        lib.oracle_dequant_e4m3.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -114,6 +126,45 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("oracle_attn_fwd failed (bad argument or out of memory)")
         return o.reshape(*lead, R, d), lse.reshape(*lead, R)
+
+    def e4m3_value(self, code: int) -> float:
+        """The real number one E4M3 code (0..255) stands for (NaN for the NaN codes)."""
+        return float(self.lib.oracle_e4m3_value(int(code) & 0xFF))
+
+    def dequant_e4m3(self, codes, scales, block_rows: int = 128):
+        """Block dequantisation: codes [..., N, d] (uint8 E4M3 bytes, or a float8_e4m3fn
+        tensor), scales [..., ceil(N / block_rows)] float32 -> float64 [..., N, d]."""
+        if hasattr(codes, "detach"):  # a torch tensor
+            import torch
+
+            codes = codes.detach().to("cpu")
+            if codes.dtype != torch.uint8:
+                codes = codes.view(torch.uint8)
+            codes = codes.numpy()
+        if hasattr(scales, "detach"):
+            scales = scales.detach().to("cpu").numpy()
+        c = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+        sc = np.ascontiguousarray(np.asarray(scales, dtype=np.float32))
+        if c.ndim < 2:
+            raise ValueError("codes must be [..., N, d]")
+        lead, (N, d) = c.shape[:-2], c.shape[-2:]
+        nblk = -(-N // int(block_rows))
+        if sc.shape != tuple(lead) + (nblk,):
+            raise ValueError(f"scales must be {tuple(lead) + (nblk,)}, got {sc.shape}")
+        BH = int(np.prod(lead)) if lead else 1
+        out = np.empty(c.shape, np.float64)
+        if self.lib.oracle_dequant_e4m3(_ptr(c), _ptr(sc), BH, N, d, int(block_rows), _ptr(out)) != 0:
+            raise RuntimeError("oracle_dequant_e4m3 failed (bad argument)")
+        return out
+
+    def attn_fwd_fp8(self, q8, k8, v8, q_scale, k_scale, v_scale, causal: bool, scale: float,
+                     rows=None, block_rows: int = 128):
+        """Exact FP64 attention of block-scaled E4M3 inputs: the inputs are dequantised
+        (dequant_e4m3) and passed to attn_fwd.  Returns (o, lse) as attn_fwd does."""
+        q = self.dequant_e4m3(q8, q_scale, block_rows)
+        k = self.dequant_e4m3(k8, k_scale, block_rows)
+        v = self.dequant_e4m3(v8, v_scale, block_rows)
+        return self.attn_fwd(q, k, v, causal, scale, rows)
 
     def attn_bwd(self, q, k, v, dout, causal: bool, scale: float, qrows=None, kcols=None,
                  want_dq: bool = True, want_dkv: bool = True):
@@ -169,3 +220,16 @@ def attn_bwd(q, k, v, dout, causal: bool, scale: float, qrows=None, kcols=None,
 
 attn_fwd.__doc__ = Oracle.attn_fwd.__doc__
 attn_bwd.__doc__ = Oracle.attn_bwd.__doc__
+
+
+def dequant_e4m3(codes, scales, block_rows: int = 128):
+    return default().dequant_e4m3(codes, scales, block_rows)
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool, scale: float, rows=None,
+                 block_rows: int = 128):
+    return default().attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal, scale, rows, block_rows)
+
+
+dequant_e4m3.__doc__ = Oracle.dequant_e4m3.__doc__
+attn_fwd_fp8.__doc__ = Oracle.attn_fwd_fp8.__doc__

@@ -33,6 +33,11 @@
  * c_i is summed from its definition, not taken from rowsum(dO * O), so the
  * GPU path's shortcut through O is checked rather than shared.
  *
+ * FP8 inputs with block scaling (huaweicloud page, section four, part 3: FP8
+ * with per-block scale factors) are decoded to the real numbers they stand for
+ * (oracle_dequant_e4m3) and then go through the same exact forward; the oracle
+ * never rounds anything to FP8 itself.
+ *
  * Layout: every tensor is [BH][N][d] row-major, d fastest, float64.
  * Threads: OpenMP over rows (and over key columns in the backward).
  */
@@ -246,4 +251,48 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
     }
     free(m); free(l); free(c);
     return failed ? -1 : 0;
+}
+
+/*
+ * The value of one E4M3 code (the OCP 8-bit floating-point format, the variant
+ * without infinities): bit 7 sign S, bits 6-3 exponent E (bias 7), bits 2-0
+ * mantissa M.
+ *   E = 0             (-1)^S * 2^-6 * (M / 8)          subnormals and +-0
+ *   0 < E, not NaN    (-1)^S * 2^(E - 7) * (1 + M / 8)  largest: S.1111.110 = 448
+ *   E = 15, M = 7     NaN
+ */
+double oracle_e4m3_value(uint8_t code)
+{
+    const int sgn = code >> 7;
+    const int e = (code >> 3) & 15;
+    const int man = code & 7;
+    double mag;
+    if (e == 15 && man == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)man / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)man / 8.0, e - 7);
+    return sgn ? -mag : mag;
+}
+
+/*
+ * Block dequantisation: out[bh][n][c] = value(codes[bh][n][c]) * scales[bh][n / block_rows],
+ * with codes [BH][N][d] E4M3 and scales [BH][ceil(N / block_rows)] float32 (one scale
+ * per block of block_rows consecutive rows of one head).  Returns 0, or -1 on a bad
+ * argument.
+ */
+int oracle_dequant_e4m3(const uint8_t *codes, const float *scales, int64_t BH, int64_t N,
+                        int64_t d, int64_t block_rows, double *out)
+{
+    if (BH < 0 || N < 1 || d < 1 || block_rows < 1 || !codes || !scales || !out) return -1;
+    const int64_t nblk = (N + block_rows - 1) / block_rows;
+#pragma omp parallel for schedule(static)
+    for (int64_t bh = 0; bh < BH; ++bh)
+        for (int64_t n = 0; n < N; ++n) {
+            const double sc = (double)scales[bh * nblk + n / block_rows];
+            const int64_t base = (bh * N + n) * d;
+            for (int64_t c = 0; c < d; ++c)
+                out[base + c] = oracle_e4m3_value(codes[base + c]) * sc;
+        }
+    return 0;
 }

@@ -321,9 +321,93 @@ def pin_bwd_autograd(orc):
         _close(dv, v.grad.numpy(), 1e-10, "dV vs autograd")
 
 
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) decoding and block dequantisation
+
+# Codes worked out by hand from the E4M3 definition (sign, 4 exponent bits with bias 7,
+# 3 mantissa bits; E = 0 subnormal 2^-6 * M/8; S.1111.111 NaN, no infinities).
+E4M3_CLOSED_FORMS = [
+    (0x00, 0.0),                  # +0
+    (0x01, 2.0 ** -9),            # smallest subnormal: 2^-6 * 1/8
+    (0x07, 7 * 2.0 ** -9),        # largest subnormal
+    (0x08, 2.0 ** -6),            # smallest normal: E = 1, M = 0
+    (0x38, 1.0),                  # E = 7
+    (0x3C, 1.5),                  # E = 7, M = 4
+    (0x40, 2.0),                  # E = 8
+    (0x77, 240.0),                # E = 14, M = 7: 2^7 * 15/8
+    (0x7E, 448.0),                # E = 15, M = 6: the largest finite value
+    (0xB8, -1.0),
+    (0xFE, -448.0),
+]
+
+
+def pin_e4m3_closed_forms(orc):
+    """E4M3 codes against values derived by hand from the format definition."""
+    for code, val in E4M3_CLOSED_FORMS:
+        got = orc.e4m3_value(code)
+        assert got == val, f"e4m3 code {code:#04x}: {got!r} != {val!r}"
+    assert math.copysign(1.0, orc.e4m3_value(0x80)) == -1.0 and orc.e4m3_value(0x80) == 0.0, "-0"
+    assert math.isnan(orc.e4m3_value(0x7F)) and math.isnan(orc.e4m3_value(0xFF)), "NaN codes"
+
+
+def _torch_e4m3_table():
+    return torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+
+
+def pin_e4m3_all_codes_vs_torch(orc):
+    """All 256 codes against PyTorch's float8_e4m3fn conversion (an independent library)."""
+    ref = _torch_e4m3_table()
+    got = np.array([orc.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "NaN codes differ from float8_e4m3fn"
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]), "decoded values differ from float8_e4m3fn"
+
+
+def pin_dequant_brute_force(orc):
+    """Block dequantisation against a Python loop over rows with the PyTorch decode table."""
+    rng = np.random.default_rng(30)
+    table = _torch_e4m3_table()
+    for N, block in ((300, 128), (23, 7), (5, 128)):
+        BH, d = 2, 3
+        codes = rng.integers(0, 256, size=(BH, N, d)).astype(np.uint8)
+        codes[np.isnan(table[codes])] = 0x38
+        nblk = -(-N // block)
+        scales = (2.0 ** rng.uniform(-8, 8, size=(BH, nblk))).astype(np.float32)
+        got = orc.dequant_e4m3(codes, scales, block)
+        for bh in range(BH):
+            for n in range(N):
+                for c in range(d):
+                    want = table[codes[bh, n, c]] * float(scales[bh, n // block])
+                    assert got[bh, n, c] == want, f"dequant [{bh},{n},{c}] (block {block})"
+
+
+def pin_fp8_attention_brute_force(orc):
+    """attn_fwd_fp8 on tiny inputs against brute force over the hand-dequantised values."""
+    rng = np.random.default_rng(31)
+    table = _torch_e4m3_table()
+    N, d, block = 9, 4, 4
+    nblk = -(-N // block)
+    arrs, deq = [], []
+    for t in range(3):
+        codes = rng.integers(0, 256, size=(1, N, d)).astype(np.uint8)
+        codes[np.isnan(table[codes])] = 0x30
+        codes[np.abs(table[codes]) > 4] = 0x38  # keep scores small for the brute force
+        sc = np.array([[0.25, 0.5, 1.0]], np.float32) * (t + 1)  # one scale per 4-row block
+        arrs.append((codes, sc))
+        deq.append([[table[codes[0, n, c]] * float(sc[0, n // block]) for c in range(d)] for n in range(N)])
+    for causal in (False, True):
+        o, lse = orc.attn_fwd_fp8(arrs[0][0], arrs[1][0], arrs[2][0], arrs[0][1], arrs[1][1], arrs[2][1],
+                                  causal, 0.3, block_rows=block)
+        bo, bl = brute_force_fwd(deq[0], deq[1], deq[2], causal, 0.3)
+        _close(o[0], bo, 1e-12, f"fp8 O (causal={causal})")
+        _close(lse[0], bl, 1e-12, f"fp8 LSE (causal={causal})")
+
+
 ALL_PINS = [
     pin_golden_closed_forms, pin_brute_force, pin_rows_sum_to_one, pin_equal_scores,
     pin_merge_rule, pin_online_recurrence, pin_one_hot_large_scores, pin_causal_first_row,
     pin_permutation_symmetry, pin_sampled_rows, pin_bwd_finite_differences,
     pin_bwd_invariants, pin_bwd_autograd,
+    pin_e4m3_closed_forms, pin_e4m3_all_codes_vs_torch, pin_dequant_brute_force,
+    pin_fp8_attention_brute_force,
 ]

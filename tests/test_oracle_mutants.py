@@ -25,6 +25,14 @@ MUTANTS = [
     ("dK without scale", "gk[t] += scale * ds * qh[i * d + t];", "gk[t] += ds * qh[i * d + t];"),
     ("dQ from V instead of K", "g[t] += scale * ds * kh[j * d + t];", "g[t] += scale * ds * vh[j * d + t];"),
     ("causal backward sees every query", "int64_t i0 = causal ? j : 0;", "int64_t i0 = 0;"),
+    ("e4m3 exponent bias 8", "mag = ldexp(1.0 + (double)man / 8.0, e - 7);",
+     "mag = ldexp(1.0 + (double)man / 8.0, e - 8);"),
+    ("e4m3 mantissa in sixteenths", "mag = ldexp(1.0 + (double)man / 8.0, e - 7);",
+     "mag = ldexp(1.0 + (double)man / 16.0, e - 7);"),
+    ("e4m3 subnormals at 2^-7", "mag = ldexp((double)man / 8.0, -6);", "mag = ldexp((double)man / 8.0, -7);"),
+    ("e4m3 sign dropped", "return sgn ? -mag : mag;", "return mag;"),
+    ("block scale indexed by row modulo", "scales[bh * nblk + n / block_rows]", "scales[bh * nblk + n % nblk]"),
+    ("one scale per head", "scales[bh * nblk + n / block_rows]", "scales[bh * nblk]"),
 ]
 
 

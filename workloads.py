@@ -98,6 +98,54 @@ def _stress_edits(q, k):
     k[:, 1, N - 1, d - 1] = 1000.0 * math.sqrt(d)
 
 
+E4M3_MAX = 448.0  # largest finite E4M3 value
+
+
+def quantize_e4m3(x, block_rows: int = 128, pow2: bool = False):
+    """Block-scaled E4M3 encoding of x [..., N, d] (float32).
+
+    Each block of ``block_rows`` consecutive rows of one head gets one float32 scale,
+    absmax / 448 (rounded up to a power of two when ``pow2``; 1 for an all-zero block),
+    and the codes are x / scale rounded to nearest even E4M3.  Returns (codes as uint8
+    [..., N, d], scales float32 [..., ceil(N / block_rows)]).
+    """
+    *lead, N, d = x.shape
+    nblk = -(-N // block_rows)
+    pad = nblk * block_rows - N
+    xp = torch.nn.functional.pad(x.float(), (0, 0, 0, pad)).reshape(*lead, nblk, block_rows, d)
+    amax = xp.abs().amax(dim=(-2, -1))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    if pow2:
+        scale = torch.exp2(torch.ceil(torch.log2(scale)))
+    codes = (xp / scale[..., None, None]).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    codes = codes.reshape(*lead, nblk * block_rows, d)[..., :N, :].contiguous().view(torch.uint8)
+    return codes, scale.to(torch.float32).contiguous()
+
+
+def draw_fp8(B, H, N, d, seed=0, block_spread=0.0, pow2=False, block_rows=128):
+    """Block-scaled E4M3 inputs: FP32 randn Q, K, V (drawn as in ``draw``); with
+    ``block_spread`` > 0 every block of ``block_rows`` rows of every head and tensor is
+    multiplied by 2^u, u uniform in [-block_spread, block_spread] (drawn after V, in the
+    order Q, K, V), so that block scales differ; then each tensor is quantised with
+    ``quantize_e4m3``.  Returns a dict of CPU tensors q8, k8, v8 (uint8 [B,H,N,d]) and
+    q_scale, k_scale, v_scale (float32 [B,H,ceil(N/block_rows)])."""
+    g = torch.Generator().manual_seed(int(seed))
+    shape = (B, H, N, d)
+    xs = [torch.randn(shape, generator=g, dtype=torch.float32) for _ in range(3)]
+    nblk = -(-N // block_rows)
+    if block_spread > 0:
+        for x in xs:
+            u = (torch.rand((B, H, nblk), generator=g, dtype=torch.float32) * 2 - 1) * block_spread
+            f = torch.exp2(u).repeat_interleave(block_rows, dim=-1)[..., :N]
+            x.mul_(f[..., None])
+    out = {}
+    for name, x in zip(("q", "k", "v"), xs):
+        codes, sc = quantize_e4m3(x, block_rows, pow2)
+        out[name + "8"] = codes
+        out[name + "_scale"] = sc
+    return out
+
+
 def inputs(name: str):
     """Inputs of a named workload (CPU tensors, 16-bit)."""
     w = WORKLOADS[name]
