@@ -106,6 +106,34 @@ ATTN_API attn_status attn_fwd_splitkv(const void *q, const void *k, const void *
                              int n_splits, int *dev_status, void *stream);
 
 /*
+ * attn_fwd_fp8 -- forward pass on FP8 inputs with per-block scale factors (the FP8
+ * support with block-wise scaling of "FlashAttention hardware-aware analysis"
+ * (huaweicloud), section four, part 3).
+ *   q8, k8, v8 : [B][H][N][d] E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3
+ *                mantissa bits; no infinities, S.1111.111 is NaN; largest 448),
+ *                16-byte aligned.
+ *   q_scale, k_scale, v_scale : float32 [B][H][ceil(N/128)], 4-byte aligned: the
+ *                scale of each block of 128 consecutive rows of one head.  The value
+ *                an input stands for is X[b,h,n,:] = e4m3(X8[b,h,n,:]) *
+ *                x_scale[b,h,n/128].  Scales must be finite and > 0 (else the output
+ *                is unspecified; nothing faults).
+ *   o, lse     : as for attn_fwd, with o in the 16-bit type out_dt: the attention of
+ *                the dequantised Q, K, V and its natural-log logsumexp.
+ * d must be 128 (else ATTN_ERR_UNSUPPORTED).  Both products run on the tensor cores'
+ * 8-bit path: S = Q8 K8^T exactly (times the two block scales and `scale`), and P V
+ * with P rounded to E4M3 after V's block scale is folded into it.  Accuracy: the
+ * logsumexp as attn_fwd's; each output element differs from the exact attention of the
+ * dequantised inputs by at most 2^-4 times the attention of |V| (the E4M3 rounding of
+ * P), plus 2^-8 |O| (rounding to out_dt), plus the flush of probabilities below 2^-12
+ * of the row's largest term.  Other conventions (causal, scale, dev_status, errors,
+ * overlap rules) are as for attn_fwd.
+ */
+ATTN_API attn_status attn_fwd_fp8(const void *q8, const void *k8, const void *v8, const float *q_scale,
+                         const float *k_scale, const float *v_scale, void *o, float *lse,
+                         int B, int H, int N, int d, attn_dtype out_dt, int causal, float scale,
+                         int *dev_status, void *stream);
+
+/*
  * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd needs:
  * two float32 vectors per row (D_i = rowsum(dO_i * O_i), and the logsumexp in
  * base 2), padded to whole 128-row tiles: 2 * B*H*ceil(N/128)*128 * 4 bytes.

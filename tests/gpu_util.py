@@ -55,6 +55,23 @@ def run_fwd(q, k, v, causal, scale=None, stream=None):
     return o.t, lse.t
 
 
+def run_fwd_fp8(x, causal, scale=None, out_dtype=torch.bfloat16, stream=None):
+    """attn_fwd_fp8 through the C ABI with guarded outputs.  ``x`` holds device tensors
+    q8, k8, v8 (uint8 [B,H,N,d]) and q_scale, k_scale, v_scale; returns (o, lse)."""
+    B, H, N, d = x["q8"].shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = Guarded((B, H, N, d), out_dtype)
+    lse = Guarded((B, H, N), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_fp8(x["q8"], x["k8"], x["v8"], x["q_scale"], x["k_scale"], x["v_scale"], o.t, lse.t,
+                           B, H, N, d, out_dtype, causal, scale, status, stream)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert o.intact() and lse.intact(), "the FP8 forward wrote outside its outputs"
+    return o.t, lse.t
+
+
 def run_bwd(q, k, v, o, lse, dout, causal, scale=None, stream=None):
     """attn_bwd through the C ABI with guarded outputs; returns (dq, dk, dv)."""
     B, H, N, d = q.shape

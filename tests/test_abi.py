@@ -123,3 +123,26 @@ def test_splitkv_validates():
         a2 = dict(args)
         a2.update(kw)
         assert attn.attn_fwd_splitkv(**a2) == st, kw
+
+
+def fwd_fp8(**kw):
+    args = dict(q8=A[0], k8=A[1], v8=A[2], q_scale=A[5], k_scale=A[6], v_scale=A[7], o=A[3], lse=A[4], B=1, H=2,
+                N=256, d=128, out_dt=0, causal=0, scale=0.088, stream=0)
+    args.update(kw)
+    return attn.attn_fwd_fp8(**args)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q8=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v8=A[2] + 4), attn.ATTN_ERR_INVALID_ARG),          # misaligned codes
+    (dict(k_scale=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(v_scale=A[7] + 2), attn.ATTN_ERR_INVALID_ARG),     # misaligned scales
+    (dict(d=64), attn.ATTN_ERR_UNSUPPORTED),                 # E4M3 inputs: d = 128 only
+    (dict(out_dt=5), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(N=0), attn.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), attn.ATTN_ERR_INVALID_ARG),
+    (dict(o=A[1]), attn.ATTN_ERR_INVALID_ARG),               # output aliases an input
+    (dict(q_scale=A[4] + 16), attn.ATTN_ERR_INVALID_ARG),    # scales inside lse
+])
+def test_fwd_fp8_rejects(kw, status):
+    assert fwd_fp8(**kw) == status

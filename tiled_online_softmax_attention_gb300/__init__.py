@@ -10,6 +10,8 @@ where the C ABI takes device pointers, and ``stream=None`` means torch's
 current stream):
 
     attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, out_dt, causal, scale,
+                 dev_status=None, stream=None)
     attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
     attn_fwd_splitkv(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, dt, causal, scale,
                      n_splits, dev_status=None, stream=None)
@@ -25,6 +27,8 @@ current stream):
 Convenience wrappers over torch tensors of shape [B, H, N, d]:
 
     forward(q, k, v, causal=False, scale=None)            -> (o, lse)
+    forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None,
+                out_dtype=torch.bfloat16)                 -> (o, lse)
     backward(q, k, v, o, lse, dout, causal=False, scale=None) -> (dq, dk, dv)
 """
 from __future__ import annotations
@@ -44,7 +48,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -68,6 +72,8 @@ def load(build_if_missing: bool = True):
     lib = ctypes.CDLL(LIB_PATH)
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_fwd_fp8.restype = I
     lib.attn_fwd.restype = I
     lib.attn_fwd_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
     lib.attn_fwd_splitkv_workspace_bytes.restype = SZ
@@ -130,6 +136,13 @@ def attn_status_string(status: int) -> str:
 def attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None) -> int:
     return int(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
                                _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, out_dt, causal, scale,
+                 dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale), _ptr(v_scale),
+                                   _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d), _dt(out_dt),
+                                   int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
 
 
 def attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits) -> int:
@@ -210,6 +223,33 @@ def forward(q, k, v, causal: bool = False, scale=None, dev_status=None, out=None
     st = attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale, dev_status)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd")
+    return o, lse
+
+
+def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, scale=None, out_dtype=None,
+                dev_status=None, out=None):
+    """Attention of block-scaled E4M3 inputs: q8, k8, v8 [B, H, N, d] uint8 (or float8_e4m3fn)
+    CUDA tensors, scales [B, H, ceil(N/128)] float32 CUDA tensors.  Returns (o, lse), o in
+    ``out_dtype`` (bf16 by default)."""
+    import torch
+
+    q8, k8, v8 = _check(q8, "q8"), _check(k8, "k8"), _check(v8, "v8")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or v8.shape != q8.shape or any(t.element_size() != 1 for t in (q8, k8, v8)):
+        raise ValueError("q8, k8, v8 must share one shape and hold one byte per element")
+    nblk = -(-N // 128)
+    scales = []
+    for t, n in ((q_scale, "q_scale"), (k_scale, "k_scale"), (v_scale, "v_scale")):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.numel() == B * H * nblk):
+            raise ValueError(f"{n} must be a float32 CUDA tensor of {B * H * nblk} scales [B, H, ceil(N/128)]")
+        scales.append(t.contiguous())
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    o, lse = out if out is not None else (torch.empty((B, H, N, d), device=q8.device, dtype=out_dtype),
+                                          torch.empty((B, H, N), device=q8.device, dtype=torch.float32))
+    st = attn_fwd_fp8(q8, k8, v8, *scales, o, lse, B, H, N, d, o.dtype, causal, scale, dev_status)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
     return o, lse
 
 

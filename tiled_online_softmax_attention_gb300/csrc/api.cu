@@ -62,7 +62,23 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16)
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a [BH][N][d] tensor of E4M3 bytes: box {128, 128, 1} (one 128-byte row
+// block at d = 128), 128-byte swizzle, zero fill past the end.
+bool make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N) * d};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(kTileM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale) {
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
@@ -131,6 +147,47 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
   if (attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
+                         const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H, int N,
+                         int d, attn_dtype out_dt, int causal, float scale, int* dev_status, void* stream) {
+  attn_status st = check_sizes(B, H, N, d, out_dt, scale);
+  if (st != ATTN_OK) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned4(q_scale) || !aligned4(k_scale) || !aligned4(v_scale)) return ATTN_ERR_INVALID_ARG;
+  const int n_t = (N + kTileM - 1) / kTileM;
+  const size_t ib = static_cast<size_t>(B) * H * N * d, ob = ib * 2, lb = static_cast<size_t>(B) * H * N * 4;
+  const size_t sb = static_cast<size_t>(B) * H * n_t * 4;
+  for (const void* in : {q8, k8, v8})
+    if (overlaps(in, ib, o, ob) || overlaps(in, ib, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  for (const void* sc : {static_cast<const void*>(q_scale), static_cast<const void*>(k_scale),
+                         static_cast<const void*>(v_scale)})
+    if (overlaps(sc, sb, o, ob) || overlaps(sc, sb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  if (overlaps(o, ob, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_device()) != ATTN_OK) return st;
+
+  attn::FwdArgs a{};
+  const bool bf16 = out_dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map_e4m3(&a.tm_q, q8, BH, N, d) || !make_map_e4m3(&a.tm_k, k8, BH, N, d) ||
+      !make_map_e4m3(&a.tm_v, v8, BH, N, d) || !make_map(&a.tm_o, o, BH, N, d, bf16))
+    return ATTN_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.N = N;
+  a.BH = BH;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = wait_limit_ns();
+  a.q_scale = q_scale;
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  if (attn::launch_fwd_fp8(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 

@@ -12,7 +12,7 @@ constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 
 struct FwdArgs {
-  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H][N][d], box {64, 128, 1}, 128B swizzle
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H][N][d], 128-byte boxes x 128 rows, 128B swizzle
   void* o;                             // [B*H][N][d] output (the merge kernel writes it directly)
   float* lse;                          // [B*H][N]
   int* dev_status;                     // nullable
@@ -26,6 +26,10 @@ struct FwdArgs {
   int n_splits;
   float* part_o;                       // [n_splits][B*H][N][d] fp32
   float* part_lse;                     // [n_splits][B*H][N] fp32 (natural log; -inf: empty range)
+  // E4M3 inputs only: one scale per 128-row block of each head, [B*H][ceil(N/128)]
+  const float* q_scale;
+  const float* k_scale;
+  const float* v_scale;
 };
 
 struct BwdArgs {
@@ -74,6 +78,7 @@ __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
 // Launchers (fwd.cu / bwd.cu); return the CUDA launch status.
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);

@@ -50,14 +50,17 @@
 namespace attn {
 namespace {
 
-template <int D>
+template <int D, bool FP8>
 struct FwdLayout {
-  static constexpr int KB = D / 64;                  // 64-column (128-byte) blocks per row
-  static constexpr int TILE = kTileM * D * 2;        // bytes of one 128 x D 16-bit tile
-  static constexpr int BLK = kTileM * 128;           // bytes of one 128-row x 64-col block
-  static constexpr int NSLOT = (D == 128) ? 4 : 8;   // K/V ring entries, one tile each
-  static constexpr int OFF_Q = 0;                    // Q0, Q1 (later the O staging tiles)
-  static constexpr int OFF_KV = 2 * TILE;
+  static constexpr int ELEM = FP8 ? 1 : 2;           // input bytes per element
+  static constexpr int KB_IN = D * ELEM / 128;       // 128-byte blocks per input row
+  static constexpr int KB = D / 64;                  // 128-byte blocks per 16-bit output row
+  static constexpr int TILE = kTileM * D * ELEM;     // bytes of one 128-row input tile
+  static constexpr int OTILE = kTileM * D * 2;       // bytes of one 128-row 16-bit output tile
+  static constexpr int BLK = kTileM * 128;           // bytes of one 128-row x 128-byte block
+  static constexpr int NSLOT = (TILE == 32768) ? 4 : 8;  // K/V ring entries, one tile each
+  static constexpr int OFF_Q = 0;                    // Q_i at i * OTILE (later O_i's staging)
+  static constexpr int OFF_KV = 2 * OTILE;
   static constexpr int OFF_AUX = OFF_KV + NSLOT * TILE;
   static constexpr int AUX_BAR = 0;                  // up to 64 mbarriers
   static constexpr int AUX_ALPHA = 512;              // float[2][128]: rescale factor per row
@@ -74,6 +77,16 @@ struct FwdLayout {
 constexpr int kFwdThreads = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// E4M3 inputs.  The second product reads P as E4M3, so P is formed on a scale where the
+// format is accurate: P~ = 2^(w - m + kPExp), with w = the log2-domain score plus
+// log2 of its key block's V scale (the V scale is folded into P, see the softmax) and
+// m the row's reference max of w.  kPExp is an integer, so the entry at the reference
+// max is exactly 2^6 and every entry within 2^-12 of it is a normal E4M3 number
+// (relative rounding error <= 2^-4); the reference max moves when exceeded by more than
+// 2^2.5, so P~ <= 2^8.5 < 448, the largest E4M3 value.
+constexpr float kRescaleThresholdFp8 = 2.5f;
+constexpr float kPExp = 6.0f;
+
 enum : int {
   B_Q = 0,         // + tile
   B_SFULL = 2,     // + tile: S_i computed (MMA commit)
@@ -88,13 +101,19 @@ enum : int {
   B_COUNT = 32
 };
 
+// FP8: Q, K, V are E4M3 with one float32 scale per 128-row block of each head (FP8 with
+// per-block scale factors, huaweicloud page, section four, part 3); S = Q8 K8^T runs on
+// kind::f8f6f4, the per-tile factor q_scale * k_scale joins the softmax scale, and P~ V8
+// runs on kind::f8f6f4 with P~ in E4M3.  The output stays 16-bit.
+//
 // SPLIT: the CTA covers one of a.n_splits contiguous ranges of the pair's key tiles and
 // writes its range's normalised partial O (fp32) and logsumexp instead of the output;
 // attn_merge_kernel combines the ranges with the two-block merge of the huaweicloud
 // page's section two.
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool FP8>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
-  using L = FwdLayout<D>;
+  static_assert(!(FP8 && SPLIT) && (!FP8 || D == 128), "E4M3 inputs: d = 128, no split");
+  using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -178,8 +197,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       prefetch_tmap(&a.tm_o);
       for (int i = 0; i < 2; ++i) {
         mbar_arrive_expect_tx(bar(B_Q + i), L::TILE);
-        for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(sb + L::OFF_Q + i * L::TILE + kb * L::BLK, &a.tm_q, bar(B_Q + i), kb * 64,
+        for (int kb = 0; kb < L::KB_IN; ++kb)
+          tma_load_3d(sb + L::OFF_Q + i * L::OTILE + kb * L::BLK, &a.tm_q, bar(B_Q + i), kb * (128 / L::ELEM),
                       (2 * pr + i) * kTileM, bh);
       }
       const int n_loads = 2 * n_kv[1];  // K_j, V_j alternately
@@ -189,8 +208,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         if (ld >= L::NSLOT && !mbar_wait(bar(B_KVEMPTY + s), ((ld / L::NSLOT) - 1) & 1, wc)) break;
         const CUtensorMap* m = (ld & 1) ? &a.tm_v : &a.tm_k;
         mbar_arrive_expect_tx(bar(B_KVFULL + s), L::TILE);
-        for (int kb = 0; kb < L::KB; ++kb)
-          tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(B_KVFULL + s), kb * 64,
+        for (int kb = 0; kb < L::KB_IN; ++kb)
+          tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(B_KVFULL + s), kb * (128 / L::ELEM),
                       (kv0 + (ld >> 1)) * kTileN, bh);
         issued = ld + 1;
       }
@@ -201,26 +220,38 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mbar_wait(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc_qk = idesc_f16(kTileM, kTileN, BF16, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(kTileM, D, BF16, false, true);
+      constexpr uint32_t idesc_qk =
+          FP8 ? idesc_e4m3(kTileM, kTileN, false, false) : idesc_f16(kTileM, kTileN, BF16, false, false);
+      constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3(kTileM, D, false, true) : idesc_f16(kTileM, D, BF16, false, true);
       auto full = [&](int ld) { return mbar_wait(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc); };
       auto issue_s = [&](int i, int j) {
-        const uint32_t qb = sb + L::OFF_Q + i * L::TILE;
+        const uint32_t qb = sb + L::OFF_Q + i * L::OTILE;
         const uint32_t kbase = sb + L::OFF_KV + ((2 * j) % L::NSLOT) * L::TILE;
+        // One MMA per 32 bytes of the rows (K = 16 16-bit or 32 8-bit elements).
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < D * L::ELEM / 32; ++k) {
           const uint32_t off = (k >> 2) * L::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk,
-                 k > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            mma_ss_f8(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                      idesc_qk, k > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                   idesc_qk, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(B_SFULL + i));
       };
       auto issue_pv = [&](int i, int j) {
         const uint32_t vbase = sb + L::OFF_KV + ((2 * j + 1) % L::NSLOT) * L::TILE;
+        // One MMA per 32 keys' bytes of P (8 TMEM columns); V advances 32 / ELEM key rows.
 #pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)
-          mma_ts(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8, sdesc_sw128(vbase + k * 2048, L::BLK, 1024),
-                 idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        for (int k = 0; k < kTileN * L::ELEM / 32; ++k) {
+          if constexpr (FP8)
+            mma_ts_f8(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
+                      sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          else
+            mma_ts(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
+                   sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+        }
         tc_commit(bar(B_ODONE + i));
       };
       bool ok = mbar_wait(bar(B_Q + 0), 0, wc) && full(0);
@@ -275,11 +306,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int row = wq * 32 + lane;
     const int grow = (2 * pr + i) * kTileM + row;
     const uint32_t t_s = tmem + (static_cast<uint32_t>(wq * 32) << 16) + L::tm_s(i);
-    const float sl2 = a.scale_log2;
+    float sl2 = a.scale_log2;
     float m = -INFINITY;  // reference max (scale*log2(e) units) used by the exponentials
     float l = 0.f;        // row sum of ex2(. - m)
     bool ok = true;
+    // E4M3: block scales of this query tile and of the next key tile (loaded a tile ahead).
+    float ks_next = 1.f, vs_next = 1.f;
+    if constexpr (FP8) {
+      const int qt = 2 * pr + i;  // the second tile of the last pair may lie past the end
+      if (qt < n_t) sl2 *= a.q_scale[static_cast<size_t>(bh) * n_t + qt];
+      if (n_kv[i] > 0) {
+        ks_next = a.k_scale[static_cast<size_t>(bh) * n_t + kv0];
+        vs_next = a.v_scale[static_cast<size_t>(bh) * n_t + kv0];
+      }
+    }
     for (int j = 0; j < n_kv[i]; ++j) {
+      float tsc = sl2, gj = 0.f, inv_vs = 1.f;  // score factor; log2 and inverse of V's scale
+      if constexpr (FP8) {
+        tsc = sl2 * ks_next;
+        gj = __log2f(vs_next);
+        inv_vs = 1.f / vs_next;
+        if (j + 1 < n_kv[i]) {
+          ks_next = a.k_scale[static_cast<size_t>(bh) * n_t + kv0 + j + 1];
+          vs_next = a.v_scale[static_cast<size_t>(bh) * n_t + kv0 + j + 1];
+        }
+      }
       if (!mbar_wait_warp(bar(B_SFULL + i), j & 1, wc)) { ok = false; break; }
       tc_fence_after();
       float s[128];
@@ -306,9 +357,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       float mx = s[0];
 #pragma unroll
       for (int c = 1; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
-      mx *= sl2;
-      // Move the reference max only when it is exceeded by more than 2^8.
-      const float m_new = (mx - m > kRescaleThreshold) ? mx : m;
+      if constexpr (FP8)
+        mx = mx * tsc + gj;  // tsc > 0: the max of the scaled scores, plus V's block term
+      else
+        mx *= tsc;
+      // Move the reference max only when it is exceeded by more than the threshold.
+      const float m_new = (mx - m > (FP8 ? kRescaleThresholdFp8 : kRescaleThreshold)) ? mx : m;
       const float alpha = (m_new == m) ? 1.f : ex2(m - m_new);  // 0 on the first tile
       if (j > 0) {
         alpha_s[i * 128 + row] = alpha;
@@ -317,22 +371,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       m = m_new;
       const float m_use = (m == -INFINITY) ? 0.f : m;  // a row with nothing visible yet
       float rs = 0.f;
-      uint32_t pk[64];
+      if constexpr (FP8) {
+        // P~ = 2^(S tsc + g_j - m + kPExp) carries V's block scale, so P~ V8 accumulates
+        // the dequantised product; the row sum takes it out again (l = sum P~ / vscale_j),
+        // and O / l is then the softmax average of the dequantised V rows.
+        const float bias = gj + kPExp - m_use;
+        uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < kTileN; c += 2) {
-        const float p0 = ex2(fmaf(s[c], sl2, -m_use));
-        const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
-        rs += p0 + p1;
-        pk[c / 2] = pack2<BF16>(p0, p1);
+        for (int c = 0; c < kTileN; c += 4) {
+          const float p0 = ex2(fmaf(s[c], tsc, bias));
+          const float p1 = ex2(fmaf(s[c + 1], tsc, bias));
+          const float p2 = ex2(fmaf(s[c + 2], tsc, bias));
+          const float p3 = ex2(fmaf(s[c + 3], tsc, bias));
+          rs += (p0 + p1) + (p2 + p3);
+          pk[c / 4] = pack4_e4m3(p0, p1, p2, p3);
+        }
+        l = fmaf(l, alpha, rs * inv_vs);
+        tmem_st_x32(t_s, pk);
+      } else {
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < kTileN; c += 2) {
+          const float p0 = ex2(fmaf(s[c], tsc, -m_use));
+          const float p1 = ex2(fmaf(s[c + 1], tsc, -m_use));
+          rs += p0 + p1;
+          pk[c / 2] = pack2<BF16>(p0, p1);
+        }
+        l = fmaf(l, alpha, rs);
+        tmem_st_x64(t_s, pk);
       }
-      l = fmaf(l, alpha, rs);
-      tmem_st_x64(t_s, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(B_PFULL + i));
     }
     if (ok) {
-      m_s[i * 128 + row] = (m == -INFINITY) ? 0.f : m;
+      // E4M3: l carries the factor 2^kPExp of P~; the logsumexp is m - kPExp + log2 l.
+      m_s[i * 128 + row] = (m == -INFINITY) ? 0.f : (FP8 ? m - kPExp : m);
       l_s[i * 128 + row] = l;
       mbar_arrive(bar(B_FIN + i));
     }
@@ -398,7 +472,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         const float mf = m_s[i * 128 + row];
         const float lf = l_s[i * 128 + row];
         const float inv_l = 1.f / lf;
-        uint8_t* stage = smem + L::OFF_Q + i * L::TILE;  // Q_i is no longer read
+        uint8_t* stage = smem + L::OFF_Q + i * L::OTILE;  // Q_i is no longer read
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -423,7 +497,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       named_bar_sync(1, 128);
       if (!SPLIT && warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < a.N) {
         for (int kb = 0; kb < L::KB; ++kb)
-          tma_store_3d(&a.tm_o, sb + L::OFF_Q + i * L::TILE + kb * L::BLK, kb * 64, q0, bh);
+          tma_store_3d(&a.tm_o, sb + L::OFF_Q + i * L::OTILE + kb * L::BLK, kb * 64, q0, bh);
         bulk_commit();
       }
     }
@@ -438,10 +512,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
 }
 
-template <int D, bool BF16, bool SPLIT>
+template <int D, bool BF16, bool SPLIT, bool FP8 = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
-  using L = FwdLayout<D>;
-  auto k = fwd_kernel<D, BF16, SPLIT>;
+  using L = FwdLayout<D, FP8>;
+  auto k = fwd_kernel<D, BF16, SPLIT, FP8>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -514,6 +588,11 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
   if (d == 128) return bf16 ? launch_split_t<128, true>(a, s) : launch_split_t<128, false>(a, s);
   return bf16 ? launch_split_t<64, true>(a, s) : launch_split_t<64, false>(a, s);
+}
+
+cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s) {
+  if (d != 128) return cudaErrorInvalidValue;
+  return bf16_out ? launch_fwd_t<128, true, false, true>(a, s) : launch_fwd_t<128, false, false, true>(a, s);
 }
 
 }  // namespace attn
