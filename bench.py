@@ -376,7 +376,39 @@ def long_forward(attn, dev):
     res = {"long_forward_B1_H32_N16384_d128": out}
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
+    res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     return res
+
+
+def fp8_forward(attn, dev):
+    """The long-sequence forward on block-scaled E4M3 inputs (attn_fwd_fp8), both masks,
+    against the 8-bit tensor peak: the measured bf16 peak times the nominal fp8/bf16
+    ratio (4.5 / 2.25 PFLOP/s)."""
+    B, H, N, d = 1, 32, 16384, 128
+    x = {k: t.to(dev) for k, t in workloads.draw_fp8(B, H, N, d, seed=2).items()}
+    o = torch.empty((B, H, N, d), device=dev, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    pk = peaks()
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    out = {"peak_tflops": round(fp8_peak, 1), "peak_source": pk["source"] + " bf16 x 2 (nominal fp8/bf16)"}
+    for causal in (False, True):
+        call = lambda: attn.attn_fwd_fp8(x["q8"], x["k8"], x["v8"], x["q_scale"], x["k_scale"], x["v_scale"], o, lse,
+                                         B, H, N, d, o.dtype, causal, 1.0 / math.sqrt(d))
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record()
+        for _ in range(reps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        tf = workloads.fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
+        out["causal" if causal else "non_causal"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
+                                                     "frac_of_fp8_peak": round(tf / fp8_peak, 3)}
+    return out
 
 
 def forward_by_workload(attn, dev):

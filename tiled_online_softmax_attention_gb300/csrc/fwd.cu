@@ -354,9 +354,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int c = 0; c < kTileN; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // Row max: a tree for E4M3 tiles; one running chain for 16-bit tiles, where the
+      // tree measured 2 % slower (the chain's latency hides behind the other tile's MMAs).
+      float mx;
+      if constexpr (FP8) {
+        mx = rowmax128(s);
+      } else {
+        mx = s[0];
 #pragma unroll
-      for (int c = 1; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 1; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
+      }
       if constexpr (FP8)
         mx = mx * tsc + gj;  // tsc > 0: the max of the scaled scores, plus V's block term
       else
@@ -370,22 +377,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       m = m_new;
       const float m_use = (m == -INFINITY) ? 0.f : m;  // a row with nothing visible yet
-      float rs = 0.f;
+      float rs = 0.f;  // row sum of this tile's exponentials
       if constexpr (FP8) {
         // P~ = 2^(S tsc + g_j - m + kPExp) carries V's block scale, so P~ V8 accumulates
         // the dequantised product; the row sum takes it out again (l = sum P~ / vscale_j),
         // and O / l is then the softmax average of the dequantised V rows.
         const float bias = gj + kPExp - m_use;
         uint32_t pk[32];
+        float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < kTileN; c += 4) {
           const float p0 = ex2(fmaf(s[c], tsc, bias));
           const float p1 = ex2(fmaf(s[c + 1], tsc, bias));
           const float p2 = ex2(fmaf(s[c + 2], tsc, bias));
           const float p3 = ex2(fmaf(s[c + 3], tsc, bias));
-          rs += (p0 + p1) + (p2 + p3);
+          r4[(c / 4) & 3] += (p0 + p1) + (p2 + p3);
           pk[c / 4] = pack4_e4m3(p0, p1, p2, p3);
         }
+        rs = (r4[0] + r4[1]) + (r4[2] + r4[3]);
         l = fmaf(l, alpha, rs * inv_vs);
         tmem_st_x32(t_s, pk);
       } else {

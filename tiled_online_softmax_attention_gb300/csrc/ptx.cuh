@@ -256,6 +256,30 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Maximum of 128 values: eight independent chains of three-input maxima, then a
+// two-level combine.  A single running maximum would be a chain of 127 dependent
+// operations, several hundred cycles of latency on every tile.
+__device__ __forceinline__ float rowmax128(const float (&s)[128]) {
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = max3f(s[k], s[k + 8], s[k + 16]);
+#pragma unroll
+  for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m[k] = max3f(m[k], s[c + k], s[c + k + 8]);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = fmaxf(m[k], s[120 + k]);
+  return fmaxf(max3f(m[0], m[1], m[2]), max3f(max3f(m[3], m[4], m[5]), m[6], m[7]));
+}
+
 // Two floats -> packed 16-bit pair (lo in bits 0-15), round to nearest even.
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
