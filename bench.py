@@ -377,7 +377,34 @@ def long_forward(attn, dev):
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
+    res["d256_forward_B1_H16_N16384_d256"] = d256_forward(attn, dev)
     return res
+
+
+def d256_forward(attn, dev):
+    """Head dimension 256 (one query tile per CTA): B=1, H=16, N=16384, bf16, both masks."""
+    B, H, N, d = 1, 16, 16384, 256
+    x = workloads.draw(B, H, N, d, "bf16", seed=13)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    out = {}
+    for causal in (False, True):
+        call = lambda: attn.attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, 1.0 / math.sqrt(d))
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 10
+        a.record()
+        for _ in range(reps):
+            call()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        out["causal" if causal else "non_causal"] = {
+            "ms": round(ms, 4), "tflops": round(workloads.fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12, 1)}
+    return out
 
 
 def fp8_forward(attn, dev):

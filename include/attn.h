@@ -26,7 +26,8 @@
  *    the library allocates nothing on the device and keeps no state between
  *    calls.
  *  - d must be 64 or 128 (the head dimensions the huaweicloud page's section
- *    five, part 2 recommends); anything else returns ATTN_ERR_UNSUPPORTED.
+ *    five, part 2 recommends); attn_fwd also takes 256 (listed with them in its
+ *    part 1).  Anything else returns ATTN_ERR_UNSUPPORTED.
  *    N >= 1 may be any value (ragged last tiles are masked, never padded in
  *    memory).  B, H >= 1 and B*H*N*d < 2^31.
  *  - causal != 0 keeps key j for query i iff j <= i (the lower triangle,
@@ -62,7 +63,7 @@ extern "C" {
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, bad scale, ws too small */
-    ATTN_ERR_UNSUPPORTED = 2,   /* d not in {64, 128}, unknown dtype, device is not sm_103 */
+    ATTN_ERR_UNSUPPORTED = 2,   /* d not supported by the call, unknown dtype, device is not sm_103 */
     ATTN_ERR_CUDA = 3,          /* a CUDA runtime/driver call or a launch failed */
     ATTN_ERR_TIMEOUT = 4        /* (device-side only) a bounded wait expired */
 } attn_status;
@@ -77,6 +78,8 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
  *             scores of each row, lse_i = m_i + ln l_i (the saved statistics
  *             of "Understanding FlashAttention, Part 2", section 2.2).
  *   o and lse must not overlap the inputs.
+ *   d may be 64, 128 or 256 (at 256 each CTA owns one 128-row query tile; the
+ *   backward entry points do not take 256).
  */
 ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale,

@@ -72,7 +72,8 @@ def bwd(**kw):
     (dict(N=0), attn.ATTN_ERR_INVALID_ARG),
     (dict(B=-1), attn.ATTN_ERR_INVALID_ARG),
     (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
-    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=512), attn.ATTN_ERR_UNSUPPORTED),
     (dict(dt=7), attn.ATTN_ERR_UNSUPPORTED),
     (dict(scale=0.0), attn.ATTN_ERR_INVALID_ARG),
     (dict(scale=float("nan")), attn.ATTN_ERR_INVALID_ARG),
@@ -91,6 +92,7 @@ def test_fwd_rejects(kw, status):
     (dict(dv=A[2]), attn.ATTN_ERR_INVALID_ARG),              # output aliases an input
     (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),       # workspace aliases an input
     (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),                # the forward alone takes 256
     (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
 ])
 def test_bwd_rejects(kw, status):
@@ -119,7 +121,8 @@ def test_splitkv_validates():
                 N=256, d=128, dt=0, causal=1, scale=0.088, n_splits=4, stream=0)
     for kw, st in [(dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(n_splits=65), attn.ATTN_ERR_INVALID_ARG),
                    (dict(workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG), (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),
-                   (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=80), attn.ATTN_ERR_UNSUPPORTED)]:
+                   (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=80), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(d=256), attn.ATTN_ERR_UNSUPPORTED)]:
         a2 = dict(args)
         a2.update(kw)
         assert attn.attn_fwd_splitkv(**a2) == st, kw

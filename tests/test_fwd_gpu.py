@@ -28,7 +28,7 @@ def check_full(x, causal, scale=None, label=""):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 2, 127, 128, 129, 255, 256, 300, 513])
 def test_fwd_small(N, d, causal, dtype):
@@ -36,10 +36,27 @@ def test_fwd_small(N, d, causal, dtype):
     check_full(x, causal, label=f"N={N} d={d} causal={causal} {dtype}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fwd_non_default_scale_and_large_scores(causal):
-    x = workloads.draw(1, 3, 300, 128, "fp16", seed=7, qk_mult=8.0)
-    check_full(x, causal, scale=0.3, label="scale 0.3, scores ~ +-1000")
+def test_fwd_non_default_scale_and_large_scores(causal, d):
+    x = workloads.draw(1, 3, 300, d, "fp16", seed=7, qk_mult=8.0 * math.sqrt(128 / d))
+    check_full(x, causal, scale=0.3, label=f"d={d} scale 0.3, scores ~ +-1000")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_d256_long_sampled(causal):
+    """Head dimension 256 on a long sequence (B=1, H=16, N=8192): sampled rows of three heads."""
+    B, H, N, d = 1, 16, 8192, 256
+    x = workloads.draw(B, H, N, d, "bf16", seed=12)
+    o, lse = run_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), causal)
+    o_cpu, lse_cpu = f64(o), f64(lse)
+    rows = sample_rows(N, seed=12)
+    for h in (0, 7, 15):
+        o_ref, lse_ref = oracle.attn_fwd(x["q"][0, h], x["k"][0, h], x["v"][0, h], causal, 1 / 16.0, rows=rows)
+        eo = o_err(o[0, h], o_ref, rows)
+        el = float(np.max(np.abs(lse_cpu[0, h, rows] - lse_ref) / np.maximum(np.abs(lse_ref), 1)))
+        assert eo <= O_MAX_ABS, f"d=256 head {h} O max-abs {eo:.3e}"
+        assert el <= LSE_REL, f"d=256 head {h} LSE rel {el:.3e}"
 
 
 @pytest.mark.parametrize("name,causal", [("c1", False), ("c2", False), ("c2", True), ("c4", False)])
@@ -74,7 +91,7 @@ def test_fwd_workload_sampled(name, causal):
     rows = sample_rows(w.N, seed=w.seed)
     for (b, h) in [(0, 0), (w.B - 1, w.H - 1), (0, w.H // 2)]:
         o_ref, lse_ref = oracle.attn_fwd(x["q"][b, h], x["k"][b, h], x["v"][b, h], causal, w.scale, rows=rows)
-        eo = float(np.max(np.abs(o_cpu[b, h, rows] - o_ref)))
+        eo = o_err(o[b, h], o_ref, rows)
         el = float(np.max(np.abs(lse_cpu[b, h, rows] - lse_ref) / np.maximum(np.abs(lse_ref), 1)))
         assert eo <= O_MAX_ABS, f"{name} head ({b},{h}) O max-abs {eo:.3e}"
         assert el <= LSE_REL, f"{name} head ({b},{h}) LSE rel {el:.3e}"

@@ -80,10 +80,11 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale) {
+// d = 256 is accepted only where the caller says so (the plain forward).
+attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale, bool allow_d256 = false) {
   if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && !(allow_d256 && d == 256)) return ATTN_ERR_UNSUPPORTED;
   if (dt != ATTN_BF16 && dt != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
   const int64_t total = static_cast<int64_t>(B) * H * N * d;
   if (total >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
@@ -123,7 +124,7 @@ const char* attn_status_string(attn_status s) {
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
                      int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale);
+  attn_status st = check_sizes(B, H, N, d, dt, scale, true);
   if (st != ATTN_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
@@ -146,7 +147,9 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
-  if (attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaError_t e = d == 256 ? attn::launch_fwd256(a, bf16, static_cast<cudaStream_t>(stream))
+                                 : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 

@@ -79,6 +79,7 @@ __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);
+cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
