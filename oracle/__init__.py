@@ -89,7 +89,7 @@ class Oracle:
         lib.oracle_attn_fwd.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
                                         P, I64, P, P]
         lib.oracle_attn_fwd.restype = ctypes.c_int
-        lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_double,
+        lib.oracle_attn_bwd.argtypes = [P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
                                         P, I64, P, I64, P, P, P]
         lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
@@ -107,8 +107,9 @@ class Oracle:
     def attn_fwd(self, q, k, v, causal: bool, scale: float, rows=None):
         """Exact attention forward in FP64.
 
-        q: [..., N, d]; k, v: [..., Nk, d] with the same leading dims (Nk == N
-        when causal).  Returns (o, lse) with shapes [..., R, d] and [..., R],
+        q: [..., N, d]; k, v: [..., Nk, d] with the same leading dims (causal
+        needs Nk >= N and aligns the mask to the last key: query i sees keys
+        j <= i + Nk - N).  Returns (o, lse) with shapes [..., R, d] and [..., R],
         R = N or len(rows).
         """
         q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -170,21 +171,23 @@ class Oracle:
                  want_dq: bool = True, want_dkv: bool = True):
         """Exact attention backward in FP64: gradients of sum(dO * O).
 
+        q, dout: [..., N, d]; k, v: [..., Nk, d] (masking as in attn_fwd).
         Returns (dq, dk, dv); dq covers ``qrows`` (all rows if None), dk and dv
         cover ``kcols`` (all keys if None).  A skipped output is None.
         """
         q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
-        if not (q.shape == k.shape == v.shape == do.shape) or q.ndim < 2:
-            raise ValueError("q, k, v, dout must share one [..., N, d] shape")
-        lead, (N, d) = q.shape[:-2], q.shape[-2:]
+        if not (q.shape == do.shape and k.shape == v.shape) or q.ndim < 2 or \
+                q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+            raise ValueError("q, dout must be [..., N, d] and k, v [..., Nk, d] with matching dims")
+        lead, (N, d), Nk = q.shape[:-2], q.shape[-2:], k.shape[-2]
         BH = int(np.prod(lead)) if lead else 1
         qr, kc = _rows(qrows), _rows(kcols)
         nq = N if qr is None else qr.size
-        nk = N if kc is None else kc.size
+        nk = Nk if kc is None else kc.size
         dq = np.empty((BH, nq, d), np.float64) if want_dq else None
         dk = np.empty((BH, nk, d), np.float64) if want_dkv else None
         dv = np.empty((BH, nk, d), np.float64) if want_dkv else None
-        rc = self.lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, d,
+        rc = self.lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, Nk, d,
                                       int(bool(causal)), float(scale),
                                       _ptr(qr), 0 if qr is None else qr.size,
                                       _ptr(kc), 0 if kc is None else kc.size,

@@ -19,7 +19,10 @@
  *
  * Causal masking keeps key j for query i iff j <= i; masked scores are -inf,
  * so their probabilities are exactly zero (huaweicloud page, section five,
- * part 3: the lower-triangular causal mask).
+ * part 3: the lower-triangular causal mask).  With Nq queries and Nk >= Nq
+ * keys the triangle is aligned to the last key: query i sees keys
+ * j <= i + (Nk - Nq), so the last query sees every key (a block of new
+ * queries after Nk - Nq earlier positions); Nq = Nk is the square case.
  *
  * The backward pass is the chain rule of the same definition
  * ("Understanding FlashAttention, Part 2", section 2.4, Figs 16-19):
@@ -84,13 +87,14 @@ static void row_stats(const double *s, int64_t nkeys, double *m_out, double *l_o
     *l_out = l;
 }
 
-static int64_t visible_keys(int64_t i, int64_t N, int causal)
+/* Keys visible to query i of Nq, with Nk keys (causal needs Nk >= Nq). */
+static int64_t visible_keys(int64_t i, int64_t Nq, int64_t Nk, int causal)
 {
-    return causal ? (i + 1) : N;
+    return causal ? (i + (Nk - Nq) + 1) : Nk;
 }
 
 /*
- * Forward.  q is [BH][N][d]; k and v are [BH][Nk][d] (Nk == N when causal).
+ * Forward.  q is [BH][N][d]; k and v are [BH][Nk][d] (Nk >= N when causal).
  * rows == NULL: every query row, o is [BH][N][d], lse is [BH][N].
  * rows != NULL: only rows[0..nrows), o is [BH][nrows][d], lse is [BH][nrows].
  * Returns 0, or -1 on a bad argument or an allocation failure.
@@ -100,7 +104,7 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
                     const int64_t *rows, int64_t nrows, double *o, double *lse)
 {
     if (BH < 0 || N < 1 || Nk < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
-    if (causal && Nk != N) return -1;
+    if (causal && Nk < N) return -1;
     int64_t nout = rows ? nrows : N;
     if (rows)
         for (int64_t r = 0; r < nrows; ++r)
@@ -121,7 +125,7 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
                 const double *qi = q + (bh * N + i) * d;
                 const double *kh = k + bh * Nk * d;
                 const double *vh = v + bh * Nk * d;
-                int64_t nk = visible_keys(i, Nk, causal);
+                int64_t nk = visible_keys(i, N, Nk, causal);
                 double m, l;
                 score_row(qi, kh, nk, d, scale, s);
                 row_stats(s, nk, &m, &l);
@@ -141,28 +145,30 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
 }
 
 /*
- * Backward.  Gradients of L = sum(dO * O) with respect to Q, K and V.
+ * Backward.  Gradients of L = sum(dO * O) with respect to Q, K and V; q and dout
+ * are [BH][N][d], k and v [BH][Nk][d] (Nk >= N when causal).
  * qrows == NULL: dq for every row ([BH][N][d]); else dq is [BH][nq][d] for
- * the listed query rows.  kcols == NULL: dk, dv for every key ([BH][N][d]);
+ * the listed query rows.  kcols == NULL: dk, dv for every key ([BH][Nk][d]);
  * else [BH][nk][d] for the listed keys.  Any of dq, dk/dv may be NULL to skip it.
  */
 int oracle_attn_bwd(const double *q, const double *k, const double *v,
-                    const double *dout, int64_t BH, int64_t N, int64_t d,
+                    const double *dout, int64_t BH, int64_t N, int64_t Nk, int64_t d,
                     int causal, double scale,
                     const int64_t *qrows, int64_t nq,
                     const int64_t *kcols, int64_t nk,
                     double *dq, double *dk, double *dv)
 {
-    if (BH < 0 || N < 1 || d < 1 || !q || !k || !v || !dout) return -1;
+    if (BH < 0 || N < 1 || Nk < 1 || d < 1 || !q || !k || !v || !dout) return -1;
+    if (causal && Nk < N) return -1;
     if ((dk == NULL) != (dv == NULL)) return -1;
     int64_t nqo = qrows ? nq : N;
-    int64_t nko = kcols ? nk : N;
+    int64_t nko = kcols ? nk : Nk;
     if (qrows)
         for (int64_t r = 0; r < nq; ++r)
             if (qrows[r] < 0 || qrows[r] >= N) return -1;
     if (kcols)
         for (int64_t r = 0; r < nk; ++r)
-            if (kcols[r] < 0 || kcols[r] >= N) return -1;
+            if (kcols[r] < 0 || kcols[r] >= Nk) return -1;
 
     double *m = (double *)malloc(sizeof(double) * (size_t)N);
     double *l = (double *)malloc(sizeof(double) * (size_t)N);
@@ -172,14 +178,14 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
 
     for (int64_t bh = 0; bh < BH && !failed; ++bh) {
         const double *qh = q + bh * N * d;
-        const double *kh = k + bh * N * d;
-        const double *vh = v + bh * N * d;
+        const double *kh = k + bh * Nk * d;
+        const double *vh = v + bh * Nk * d;
         const double *doh = dout + bh * N * d;
 
         /* 1. per-row softmax statistics and c_i = sum_k P_ik dP_ik */
 #pragma omp parallel
         {
-            double *s = (double *)malloc(sizeof(double) * (size_t)N);
+            double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
             if (!s) {
 #pragma omp atomic write
                 failed = 1;
@@ -187,7 +193,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
 #pragma omp for schedule(dynamic, 8)
             for (int64_t i = 0; i < N; ++i) {
                 if (!s) continue;
-                int64_t nkv = visible_keys(i, N, causal);
+                int64_t nkv = visible_keys(i, N, Nk, causal);
                 score_row(qh + i * d, kh, nkv, d, scale, s);
                 row_stats(s, nkv, &m[i], &l[i]);
                 double acc = 0.0;
@@ -208,7 +214,7 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
 #pragma omp parallel for schedule(dynamic, 8)
             for (int64_t r = 0; r < nqo; ++r) {
                 int64_t i = qrows ? qrows[r] : r;
-                int64_t nkv = visible_keys(i, N, causal);
+                int64_t nkv = visible_keys(i, N, Nk, causal);
                 double *g = dq + (bh * nqo + r) * d;
                 for (int64_t t = 0; t < d; ++t) g[t] = 0.0;
                 for (int64_t j = 0; j < nkv; ++j) {
@@ -232,7 +238,8 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v,
                 double *gk = dk + (bh * nko + r) * d;
                 double *gv = dv + (bh * nko + r) * d;
                 for (int64_t t = 0; t < d; ++t) { gk[t] = 0.0; gv[t] = 0.0; }
-                int64_t i0 = causal ? j : 0;               /* queries that see key j */
+                int64_t i0 = causal ? j - (Nk - N) : 0;    /* queries that see key j */
+                if (i0 < 0) i0 = 0;
                 for (int64_t i = i0; i < N; ++i) {
                     double sij = 0.0, dp = 0.0;
                     for (int64_t t = 0; t < d; ++t) {

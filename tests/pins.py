@@ -55,11 +55,12 @@ def pin_golden_closed_forms(orc):
 
 
 def brute_force_fwd(q, k, v, causal, scale):
-    """exp(S)/sum exp(S) with Python floats, no max subtraction (small scores only)."""
+    """exp(S)/sum exp(S) with Python floats, no max subtraction (small scores only).
+    Causal with Nk >= N keys: query i sees keys j <= i + Nk - N."""
     N, d = len(q), len(q[0])
     o, lse = [], []
     for i in range(N):
-        keys = range(i + 1) if causal else range(len(k))
+        keys = range(i + len(k) - N + 1) if causal else range(len(k))
         w = {}
         for j in keys:
             w[j] = math.exp(scale * math.fsum(q[i][t] * k[j][t] for t in range(d)))
@@ -73,7 +74,8 @@ def pin_brute_force(orc):
     """Direct softmax on tiny inputs in pure-Python float64."""
     rng = np.random.default_rng(11)
     for (N, Nk, d, causal) in [(4, 4, 4, False), (4, 4, 4, True), (5, 3, 2, False),
-                               (6, 6, 3, True), (1, 1, 5, True), (3, 7, 1, False)]:
+                               (6, 6, 3, True), (1, 1, 5, True), (3, 7, 1, False),
+                               (3, 7, 2, True), (1, 5, 3, True)]:
         q = rng.uniform(-1.5, 1.5, (N, d))
         k = rng.uniform(-1.5, 1.5, (Nk, d))
         v = rng.uniform(-2, 2, (Nk, d))
@@ -269,9 +271,10 @@ def pin_sampled_rows(orc):
 def pin_bwd_finite_differences(orc):
     """Central differences of L = sum(dO * O), O from the oracle's forward, match the gradients."""
     rng = np.random.default_rng(20)
-    for causal in (False, True):
-        N, d = 6, 3
-        q, k, v, do = (rng.normal(size=(N, d)) for _ in range(4))
+    for causal, N, Nk in ((False, 6, 6), (True, 6, 6), (False, 4, 7), (True, 4, 7)):
+        d = 3
+        q, do = (rng.normal(size=(N, d)) for _ in range(2))
+        k, v = (rng.normal(size=(Nk, d)) for _ in range(2))
         scale = 0.8
         dq, dk, dv = orc.attn_bwd(q, k, v, do, causal, scale)
         h = 1e-6
@@ -287,7 +290,7 @@ def pin_bwd_finite_differences(orc):
                 lm = np.sum(do * orc.attn_fwd(*args_m, causal, scale)[0])
                 num[idx] = (lp - lm) / (2 * h)
             err = np.max(np.abs(num - g)) / max(1e-3, np.max(np.abs(g)))
-            assert err < 1e-6, f"{name} vs finite differences (causal={causal}): {err:.2e}"
+            assert err < 1e-6, f"{name} vs finite differences (causal={causal}, {N}x{Nk}): {err:.2e}"
 
 
 def pin_bwd_invariants(orc):
@@ -403,11 +406,30 @@ def pin_fp8_attention_brute_force(orc):
         _close(lse[0], bl, 1e-12, f"fp8 LSE (causal={causal})")
 
 
+def pin_rect_causal_is_a_suffix(orc):
+    """Nq < Nk causal = the last Nq query rows of the square causal problem over all Nk
+    positions: forward rows, dQ rows, and dK/dV with dO zero on the first Nk - Nq rows."""
+    rng = np.random.default_rng(32)
+    Nk, Nq, d = 9, 4, 3
+    qf, k, v, dof = (rng.normal(size=(Nk, d)) for _ in range(4))
+    dof[:Nk - Nq] = 0.0
+    q, do = qf[Nk - Nq:], dof[Nk - Nq:]
+    o_sq, lse_sq = orc.attn_fwd(qf, k, v, True, 0.7)
+    o, lse = orc.attn_fwd(q, k, v, True, 0.7)
+    _close(o, o_sq[Nk - Nq:], 1e-13, "rect causal O = suffix of square")
+    _close(lse, lse_sq[Nk - Nq:], 1e-13, "rect causal LSE = suffix of square")
+    dq_sq, dk_sq, dv_sq = orc.attn_bwd(qf, k, v, dof, True, 0.7)
+    dq, dk, dv = orc.attn_bwd(q, k, v, do, True, 0.7)
+    _close(dq, dq_sq[Nk - Nq:], 1e-12, "rect causal dQ = suffix of square")
+    _close(dk, dk_sq, 1e-12, "rect causal dK = square with dO zero on the prefix")
+    _close(dv, dv_sq, 1e-12, "rect causal dV = square with dO zero on the prefix")
+
+
 ALL_PINS = [
     pin_golden_closed_forms, pin_brute_force, pin_rows_sum_to_one, pin_equal_scores,
     pin_merge_rule, pin_online_recurrence, pin_one_hot_large_scores, pin_causal_first_row,
     pin_permutation_symmetry, pin_sampled_rows, pin_bwd_finite_differences,
     pin_bwd_invariants, pin_bwd_autograd,
     pin_e4m3_closed_forms, pin_e4m3_all_codes_vs_torch, pin_dequant_brute_force,
-    pin_fp8_attention_brute_force,
+    pin_fp8_attention_brute_force, pin_rect_causal_is_a_suffix,
 ]

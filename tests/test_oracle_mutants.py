@@ -13,8 +13,8 @@ MUTANTS = [
     ("no division by l", "double p = exp(s[j] - m) / l;", "double p = exp(s[j] - m);"),
     ("LSE without the max", "lse[bh * nout + r] = m + log(l);", "lse[bh * nout + r] = log(l);"),
     ("l without the max shift", "l += exp(s[j] - m);", "l += exp(s[j]);"),
-    ("causal mask one key late", "return causal ? (i + 1) : N;",
-     "return causal ? (i + 2 > N ? N : i + 2) : N;"),
+    ("causal mask one key late", "return causal ? (i + (Nk - Nq) + 1) : Nk;",
+     "return causal ? (i + (Nk - Nq) + 2 > Nk ? Nk : i + (Nk - Nq) + 2) : Nk;"),
     ("V rows reversed", "const double *vj = vh + j * d;", "const double *vj = vh + (nk - 1 - j) * d;"),
     ("dP with transposed indices", "dp += doh[i * d + t] * vh[j * d + t];",
      "dp += doh[j * d + t] * vh[i * d + t];"),
@@ -24,7 +24,7 @@ MUTANTS = [
     ("dV from Q instead of dO", "gv[t] += p * doh[i * d + t];", "gv[t] += p * qh[i * d + t];"),
     ("dK without scale", "gk[t] += scale * ds * qh[i * d + t];", "gk[t] += ds * qh[i * d + t];"),
     ("dQ from V instead of K", "g[t] += scale * ds * kh[j * d + t];", "g[t] += scale * ds * vh[j * d + t];"),
-    ("causal backward sees every query", "int64_t i0 = causal ? j : 0;", "int64_t i0 = 0;"),
+    ("causal backward sees every query", "int64_t i0 = causal ? j - (Nk - N) : 0;", "int64_t i0 = 0;"),
     ("e4m3 exponent bias 8", "mag = ldexp(1.0 + (double)man / 8.0, e - 7);",
      "mag = ldexp(1.0 + (double)man / 8.0, e - 8);"),
     ("e4m3 mantissa in sixteenths", "mag = ldexp(1.0 + (double)man / 8.0, e - 7);",
@@ -33,6 +33,10 @@ MUTANTS = [
     ("e4m3 sign dropped", "return sgn ? -mag : mag;", "return mag;"),
     ("block scale indexed by row modulo", "scales[bh * nblk + n / block_rows]", "scales[bh * nblk + n % nblk]"),
     ("one scale per head", "scales[bh * nblk + n / block_rows]", "scales[bh * nblk]"),
+    ("rectangular causal aligned to the first key", "return causal ? (i + (Nk - Nq) + 1) : Nk;",
+     "return causal ? (i + 1) : Nk;"),
+    ("rectangular causal backward without the offset", "int64_t i0 = causal ? j - (Nk - N) : 0;",
+     "int64_t i0 = causal ? j : 0;"),
 ]
 
 

@@ -17,7 +17,9 @@ def test_rejects_bad_arguments():
     q = np.zeros((4, 2))
     with pytest.raises(ValueError):
         oracle.attn_fwd(q, np.zeros((4, 3)), np.zeros((4, 3)), False, 1.0)
-    with pytest.raises(RuntimeError):          # causal needs as many keys as queries
-        oracle.attn_fwd(q, np.zeros((5, 2)), np.zeros((5, 2)), True, 1.0)
+    with pytest.raises(RuntimeError):          # causal needs at least as many keys as queries
+        oracle.attn_fwd(q, np.zeros((3, 2)), np.zeros((3, 2)), True, 1.0)
+    with pytest.raises(RuntimeError):
+        oracle.attn_bwd(q, np.zeros((3, 2)), np.zeros((3, 2)), q, True, 1.0)
     with pytest.raises(RuntimeError):          # sampled row out of range
         oracle.attn_fwd(q, q, q, False, 1.0, rows=[4])
