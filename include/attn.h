@@ -86,6 +86,21 @@ ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void 
                      int *dev_status, void *stream);
 
 /*
+ * attn_fwd_rect -- attn_fwd with Nq queries against Nk keys (cross-attention, or a
+ * block of new queries attending to earlier positions as well).
+ *   q, o    : [B][H][Nq][d];  k, v : [B][H][Nk][d];  lse : [B][H][Nq].
+ *   causal  : the lower triangle of the huaweicloud page's section five, part 3,
+ *             aligned to the last key: query i sees key j iff j <= i + (Nk - Nq),
+ *             so the queries are the last Nq of Nk positions.  Needs Nk >= Nq
+ *             (else ATTN_ERR_INVALID_ARG); Nq = Nk is attn_fwd.
+ * Everything else (d in {64, 128, 256}, dtypes, scale, errors) is as for attn_fwd;
+ * the size limit applies to B*H*max(Nq, Nk)*d.
+ */
+ATTN_API attn_status attn_fwd_rect(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int H, int Nq, int Nk, int d, attn_dtype dt, int causal, float scale,
+                          int *dev_status, void *stream);
+
+/*
  * attn_fwd_splitkv -- the forward pass for shapes with too few query tiles to fill
  * the GPU (few heads, long sequences): every pair of 128-row query tiles has its key
  * tiles cut into n_splits contiguous ranges, each processed by its own CTA, which
@@ -164,6 +179,18 @@ ATTN_API attn_status attn_bwd(const void *q, const void *k, const void *v, const
                      void *workspace, size_t workspace_bytes,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
                      int *dev_status, void *stream);
+
+/*
+ * attn_bwd_rect -- attn_bwd for attn_fwd_rect's shapes: q, o, dout, dq [B][H][Nq][d],
+ * k, v, dk, dv [B][H][Nk][d], lse [B][H][Nq]; the workspace is
+ * attn_bwd_workspace_bytes(B, H, Nq, d).  Causal masking and Nk >= Nq as in
+ * attn_fwd_rect; d in {64, 128}.  Everything else is as for attn_bwd.
+ */
+ATTN_API attn_status attn_bwd_rect(const void *q, const void *k, const void *v, const void *o,
+                          const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                          void *workspace, size_t workspace_bytes,
+                          int B, int H, int Nq, int Nk, int d, attn_dtype dt, int causal, float scale,
+                          int *dev_status, void *stream);
 
 /*
  * The three stages attn_bwd runs, in order, on one stream.  They are exported

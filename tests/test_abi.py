@@ -149,3 +149,22 @@ def fwd_fp8(**kw):
 ])
 def test_fwd_fp8_rejects(kw, status):
     assert fwd_fp8(**kw) == status
+
+
+def test_rect_validates():
+    fa = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], B=1, H=2, Nq=256, Nk=512, d=128, dt=0, causal=1,
+              scale=0.088, stream=0)
+    for kw, st in [(dict(Nq=600), attn.ATTN_ERR_INVALID_ARG),        # causal needs Nk >= Nq
+                   (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(o=A[1] + 256 * 128 * 2 * 2), attn.ATTN_ERR_INVALID_ARG)]:  # o inside k (Nk rows)
+        a2 = dict(fa)
+        a2.update(kw)
+        assert attn.attn_fwd_rect(**a2) == st, kw
+    ba = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8], workspace=A[9],
+              workspace_bytes=1 << 20, B=1, H=2, Nq=256, Nk=512, d=128, dt=0, causal=1, scale=0.088, stream=0)
+    for kw, st in [(dict(Nq=600), attn.ATTN_ERR_INVALID_ARG), (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(dk=A[7], dv=A[7] + 512 * 128 * 2), attn.ATTN_ERR_INVALID_ARG),  # dv inside dk's Nk rows
+                   (dict(workspace_bytes=16), attn.ATTN_ERR_INVALID_ARG)]:
+        a2 = dict(ba)
+        a2.update(kw)
+        assert attn.attn_bwd_rect(**a2) == st, kw

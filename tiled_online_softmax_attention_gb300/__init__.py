@@ -10,6 +10,9 @@ where the C ABI takes device pointers, and ``stream=None`` means torch's
 current stream):
 
     attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_fwd_rect(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_bwd_rect(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                  B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None)
     attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, out_dt, causal, scale,
                  dev_status=None, stream=None)
     attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
@@ -48,7 +51,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -72,6 +75,10 @@ def load(build_if_missing: bool = True):
     lib = ctypes.CDLL(LIB_PATH)
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_fwd_rect.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
+    lib.attn_fwd_rect.restype = I
+    lib.attn_bwd_rect.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_rect.restype = I
     lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.attn_fwd_fp8.restype = I
     lib.attn_fwd.restype = I
@@ -136,6 +143,20 @@ def attn_status_string(status: int) -> str:
 def attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None) -> int:
     return int(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
                                _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_fwd_rect(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(Nq), int(Nk),
+                                    int(d), _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status),
+                                    _stream(stream)))
+
+
+def attn_bwd_rect(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Nq, Nk, d, dt, causal, scale,
+                  dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(workspace), int(workspace_bytes), int(B), int(H), int(Nq),
+                                    int(Nk), int(d), _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status),
+                                    _stream(stream)))
 
 
 def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, out_dt, causal, scale,
@@ -210,19 +231,24 @@ def _check(t, name):
 
 
 def forward(q, k, v, causal: bool = False, scale=None, dev_status=None, out=None):
-    """O = softmax(scale Q K^T) V and the row logsumexp; q, k, v: [B, H, N, d] bf16/fp16 CUDA tensors."""
+    """O = softmax(scale Q K^T) V and the row logsumexp; q: [B, H, Nq, d], k, v: [B, H, Nk, d]
+    bf16/fp16 CUDA tensors (Nk != Nq goes through attn_fwd_rect; causal then needs Nk >= Nq)."""
     import torch
 
     q, k, v = _check(q, "q"), _check(k, "k"), _check(v, "v")
     B, H, N, d = q.shape
-    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share shape and dtype")
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q must be [B, H, Nq, d] and k, v [B, H, Nk, d], all of one dtype")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o, lse = out if out is not None else (torch.empty_like(q), torch.empty((B, H, N), device=q.device,
                                                                             dtype=torch.float32))
-    st = attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale, dev_status)
+    if Nk == N:
+        st, name = attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale, dev_status), "attn_fwd"
+    else:
+        st, name = attn_fwd_rect(q, k, v, o, lse, B, H, N, Nk, d, q.dtype, causal, scale, dev_status), "attn_fwd_rect"
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fwd")
+        raise AttnError(st, name)
     return o, lse
 
 
@@ -255,16 +281,24 @@ def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sca
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale=None, dev_status=None, workspace=None,
              out=None):
-    """dQ, dK, dV of sum(dout * O) for O = forward(q, k, v); all [B, H, N, d] CUDA tensors."""
+    """dQ, dK, dV of sum(dout * O) for O = forward(q, k, v); q, o, dout [B, H, Nq, d], k, v
+    [B, H, Nk, d] CUDA tensors (Nk != Nq goes through attn_bwd_rect)."""
     import torch
 
     q, k, v, o, dout = (_check(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")))
     B, H, N, d = q.shape
+    Nk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     nbytes = attn_bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
     dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    if Nk != N:
+        st = attn_bwd_rect(q, k, v, o, dout, lse.contiguous(), dq, dk, dv, workspace, workspace.numel(), B, H, N, Nk,
+                           d, q.dtype, causal, scale, dev_status)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_bwd_rect")
+        return dq, dk, dv
     st = attn_bwd(q, k, v, o, dout, lse.contiguous(), dq, dk, dv, workspace, workspace.numel(), B, H, N, d,
                   q.dtype, causal, scale, dev_status)
     if st != ATTN_OK:

@@ -80,13 +80,15 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// d = 256 is accepted only where the caller says so (the plain forward).
-attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale, bool allow_d256 = false) {
-  if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID_ARG;
+// d = 256 is accepted only where the caller says so (the forward).  Nk = key length.
+attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale, bool allow_d256 = false,
+                        int Nk = -1) {
+  if (Nk < 0) Nk = N;
+  if (B < 1 || H < 1 || N < 1 || Nk < 1) return ATTN_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128 && !(allow_d256 && d == 256)) return ATTN_ERR_UNSUPPORTED;
   if (dt != ATTN_BF16 && dt != ATTN_FP16) return ATTN_ERR_UNSUPPORTED;
-  const int64_t total = static_cast<int64_t>(B) * H * N * d;
+  const int64_t total = static_cast<int64_t>(B) * H * (N > Nk ? N : Nk) * d;
   if (total >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
@@ -122,27 +124,38 @@ const char* attn_status_string(attn_status s) {
   return "ATTN_ERR_UNKNOWN";
 }
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+}  // extern "C"
+
+namespace {
+
+// The forward for Nq queries against Nk keys (Nk = Nq for attn_fwd).
+attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int Nk,
                      int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale, true);
+  attn_status st = check_sizes(B, H, N, d, dt, scale, true, Nk);
   if (st != ATTN_OK) return st;
+  if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return ATTN_ERR_INVALID_ARG;
-  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
-  for (const void* in : {q, k, v})
-    if (overlaps(in, tb, o, tb) || overlaps(in, tb, lse, lb)) return ATTN_ERR_INVALID_ARG;
-  if (overlaps(o, tb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(B) * H * N * d * 2, kb = static_cast<size_t>(B) * H * Nk * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  for (const void* in : {q, k, v}) {
+    const size_t ib = in == q ? qb : kb;
+    if (overlaps(in, ib, o, qb) || overlaps(in, ib, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, qb, lse, lb)) return ATTN_ERR_INVALID_ARG;
   if ((st = check_device()) != ATTN_OK) return st;
 
   attn::FwdArgs a{};
   const bool bf16 = dt == ATTN_BF16;
   const int BH = B * H;
-  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
-      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_o, o, BH, N, d, bf16))
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_o, o, BH, N, d, bf16))
     return ATTN_ERR_CUDA;
   a.lse = lse;
   a.dev_status = dev_status;
   a.N = N;
+  a.Nk = Nk;
+  a.cofs = causal ? Nk - N : 0;
   a.BH = BH;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -151,6 +164,20 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                                  : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                     int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, dt, causal, scale, dev_status, stream);
+}
+
+attn_status attn_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                          int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status, stream);
 }
 
 attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
@@ -183,6 +210,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const f
   a.lse = lse;
   a.dev_status = dev_status;
   a.N = N;
+  a.Nk = N;
   a.BH = BH;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -227,6 +255,7 @@ attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* 
   a.lse = lse;
   a.dev_status = dev_status;
   a.N = N;
+  a.Nk = N;
   a.BH = BH;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -248,52 +277,58 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
 
 namespace {
 
-// Validation shared by the backward entry points.  `ins` are [B,H,N,d] inputs,
-// `outs` are [B,H,N,d] outputs (may be null entries when a stage does not write
-// them); the workspace must hold attn_bwd_workspace_bytes().
-attn_status check_bwd(std::initializer_list<const void*> ins, const float* lse,
-                      std::initializer_list<void*> outs, const void* ws, size_t ws_bytes, bool ws_out, int B,
-                      int H, int N, int d, attn_dtype dt, float scale) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale);
+// A tensor argument and its size in bytes.
+struct Buf {
+  const void* p;
+  size_t bytes;
+};
+
+// Validation shared by the backward entry points: every input and output 16-byte
+// aligned and non-null, no output overlapping an input, the logsumexp, the workspace
+// or another output, and (when the call writes the workspace) no input or the
+// logsumexp inside the workspace, which must hold attn_bwd_workspace_bytes().
+attn_status check_bwd(std::initializer_list<Buf> ins, const float* lse, std::initializer_list<Buf> outs,
+                      const void* ws, size_t ws_bytes, bool ws_out, int B, int H, int N, int Nk, int d,
+                      attn_dtype dt, float scale, int causal) {
+  attn_status st = check_sizes(B, H, N, d, dt, scale, false, Nk);
   if (st != ATTN_OK) return st;
-  for (const void* p : ins)
-    if (!aligned16(p)) return ATTN_ERR_INVALID_ARG;
-  for (void* p : outs)
-    if (!aligned16(p)) return ATTN_ERR_INVALID_ARG;
+  if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
+  for (const Buf& b : ins)
+    if (!aligned16(b.p)) return ATTN_ERR_INVALID_ARG;
+  for (const Buf& b : outs)
+    if (!aligned16(b.p)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(ws)) return ATTN_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
   if (ws_bytes < need) return ATTN_ERR_INVALID_ARG;
-  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
-  for (void* out : outs) {
-    for (const void* in : ins)
-      if (overlaps(in, tb, out, tb)) return ATTN_ERR_INVALID_ARG;
-    if ((lse && overlaps(lse, lb, out, tb)) || overlaps(ws, need, out, tb)) return ATTN_ERR_INVALID_ARG;
-    for (void* other : outs)
-      if (other != out && overlaps(other, tb, out, tb)) return ATTN_ERR_INVALID_ARG;
-  }
-  {
-    // two identical output pointers are an overlap too
-    std::vector<void*> v(outs);
-    for (size_t i = 0; i < v.size(); ++i)
-      for (size_t j = i + 1; j < v.size(); ++j)
-        if (v[i] == v[j]) return ATTN_ERR_INVALID_ARG;
+  const size_t lb = static_cast<size_t>(B) * H * N * 4;
+  const std::vector<Buf> o(outs);
+  for (size_t i = 0; i < o.size(); ++i) {
+    for (const Buf& in : ins)
+      if (overlaps(in.p, in.bytes, o[i].p, o[i].bytes)) return ATTN_ERR_INVALID_ARG;
+    if ((lse && overlaps(lse, lb, o[i].p, o[i].bytes)) || overlaps(ws, need, o[i].p, o[i].bytes))
+      return ATTN_ERR_INVALID_ARG;
+    for (size_t j = i + 1; j < o.size(); ++j)  // identical pointers are an overlap too
+      if (o[i].p == o[j].p || overlaps(o[i].p, o[i].bytes, o[j].p, o[j].bytes)) return ATTN_ERR_INVALID_ARG;
   }
   if (ws_out) {
-    for (const void* in : ins)
-      if (overlaps(in, tb, ws, need)) return ATTN_ERR_INVALID_ARG;
+    for (const Buf& in : ins)
+      if (overlaps(in.p, in.bytes, ws, need)) return ATTN_ERR_INVALID_ARG;
     if (lse && overlaps(lse, lb, ws, need)) return ATTN_ERR_INVALID_ARG;
   }
   return check_device();
 }
 
-void fill_bwd(attn::BwdArgs& a, const void* ws, int B, int H, int N, int causal, float scale, int* dev_status) {
+void fill_bwd(attn::BwdArgs& a, const void* ws, int B, int H, int N, int Nk, int causal, float scale,
+              int* dev_status) {
   const int BH = B * H;
   const int npad = static_cast<int>((static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM);
   a.lse2 = static_cast<float*>(const_cast<void*>(ws));
   a.delta = static_cast<float*>(const_cast<void*>(ws)) + static_cast<size_t>(BH) * npad;
   a.dev_status = dev_status;
   a.N = N;
+  a.Nk = Nk;
+  a.cofs = causal ? Nk - N : 0;
   a.Npad = npad;
   a.BH = BH;
   a.causal = causal ? 1 : 0;
@@ -302,17 +337,17 @@ void fill_bwd(attn::BwdArgs& a, const void* ws, int B, int H, int N, int causal,
   a.wait_limit_ns = wait_limit_ns();
 }
 
-}  // namespace
+size_t qbytes(int B, int H, int N, int d) { return static_cast<size_t>(B) * H * N * d * 2; }
 
-extern "C" {
-
-attn_status attn_bwd_prepare(const void* o, const void* dout, const float* lse, void* workspace,
-                             size_t workspace_bytes, int B, int H, int N, int d, attn_dtype dt, void* stream) {
+attn_status prepare_impl(const void* o, const void* dout, const float* lse, void* workspace, size_t workspace_bytes,
+                         int B, int H, int N, int d, attn_dtype dt, void* stream) {
   if (!lse) return ATTN_ERR_INVALID_ARG;
-  attn_status st = check_bwd({o, dout}, lse, {}, workspace, workspace_bytes, true, B, H, N, d, dt, 1.f);
+  const size_t qb = qbytes(B, H, N, d);
+  attn_status st = check_bwd({{o, qb}, {dout, qb}}, lse, {}, workspace, workspace_bytes, true, B, H, N, N, d, dt,
+                             1.f, 0);
   if (st != ATTN_OK) return st;
   attn::BwdArgs a{};
-  fill_bwd(a, workspace, B, H, N, 0, 1.f, nullptr);
+  fill_bwd(a, workspace, B, H, N, N, 0, 1.f, nullptr);
   a.o = o;
   a.dout = dout;
   a.lse = lse;
@@ -321,56 +356,97 @@ attn_status attn_bwd_prepare(const void* o, const void* dout, const float* lse, 
   return ATTN_OK;
 }
 
-attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
-                          size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int d, attn_dtype dt,
-                          int causal, float scale, int* dev_status, void* stream) {
-  attn_status st = check_bwd({q, k, v, dout}, nullptr, {dk, dv}, workspace, workspace_bytes, false, B, H, N, d, dt,
-                             scale);
+attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                      size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
+                      int causal, float scale, int* dev_status, void* stream) {
+  const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
+  attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
+                             workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
   if (st != ATTN_OK) return st;
   attn::BwdArgs a{};
   const bool bf16 = dt == ATTN_BF16;
   const int BH = B * H;
-  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
-      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
-      !make_map(&a.tm_dk, dk, BH, N, d, bf16) || !make_map(&a.tm_dv, dv, BH, N, d, bf16))
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
+      !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) || !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
     return ATTN_ERR_CUDA;
-  fill_bwd(a, workspace, B, H, N, causal, scale, dev_status);
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status);
   if (attn::launch_bwd_dkdv(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+attn_status dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                    size_t workspace_bytes, void* dq, int B, int H, int N, int Nk, int d, attn_dtype dt, int causal,
+                    float scale, int* dev_status, void* stream) {
+  const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
+  attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dq, qb}}, workspace,
+                             workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
+  if (st != ATTN_OK) return st;
+  attn::BwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
+      !make_map(&a.tm_dq, dq, BH, N, d, bf16))
+    return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status);
+  if (attn::launch_bwd_dq(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
+                     int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  if (!lse) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
+  attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},
+                             workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal);
+  if (st != ATTN_OK) return st;
+  if ((st = prepare_impl(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
+  if ((st = dkdv_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
+                      dev_status, stream)) != ATTN_OK)
+    return st;
+  return dq_impl(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, Nk, d, dt, causal, scale, dev_status,
+                 stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_prepare(const void* o, const void* dout, const float* lse, void* workspace,
+                             size_t workspace_bytes, int B, int H, int N, int d, attn_dtype dt, void* stream) {
+  return prepare_impl(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream);
+}
+
+attn_status attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+                          size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int d, attn_dtype dt,
+                          int causal, float scale, int* dev_status, void* stream) {
+  return dkdv_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, N, d, dt, causal, scale, dev_status,
+                   stream);
 }
 
 attn_status attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                         size_t workspace_bytes, void* dq, int B, int H, int N, int d, attn_dtype dt, int causal,
                         float scale, int* dev_status, void* stream) {
-  attn_status st =
-      check_bwd({q, k, v, dout}, nullptr, {dq}, workspace, workspace_bytes, false, B, H, N, d, dt, scale);
-  if (st != ATTN_OK) return st;
-  attn::BwdArgs a{};
-  const bool bf16 = dt == ATTN_BF16;
-  const int BH = B * H;
-  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
-      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
-      !make_map(&a.tm_dq, dq, BH, N, d, bf16))
-    return ATTN_ERR_CUDA;
-  fill_bwd(a, workspace, B, H, N, causal, scale, dev_status);
-  if (attn::launch_bwd_dq(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  return dq_impl(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, N, d, dt, causal, scale, dev_status,
+                 stream);
 }
 
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale, int* dev_status,
                      void* stream) {
-  if (!lse) return ATTN_ERR_INVALID_ARG;
-  attn_status st = check_bwd({q, k, v, o, dout}, lse, {dq, dk, dv}, workspace, workspace_bytes, true, B, H, N, d,
-                             dt, scale);
-  if (st != ATTN_OK) return st;
-  if ((st = attn_bwd_prepare(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
-  if ((st = attn_bwd_dkdv(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, d, dt, causal, scale,
-                          dev_status, stream)) != ATTN_OK)
-    return st;
-  return attn_bwd_dq(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, d, dt, causal, scale, dev_status,
-                     stream);
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
+                  dev_status, stream);
+}
+
+attn_status attn_bwd_rect(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int B, int H, int Nq, int Nk, int d, attn_dtype dt, int causal, float scale,
+                          int* dev_status, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Nq, Nk, d, dt, causal, scale,
+                  dev_status, stream);
 }
 
 attn_status attn_selftest_bounded_wait(int* dev_status, uint64_t limit_ns, void* stream) {

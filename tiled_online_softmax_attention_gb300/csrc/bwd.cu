@@ -188,12 +188,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_t = (a.N + kTileN - 1) / kTileN;
-  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const int n_t = (a.N + kTileM - 1) / kTileM;    // query tiles
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_tk);
   const int bh = wi.bh;
   const int kt = wi.rank;  // low key tiles see the most queries: they go first
   const int k0 = kt * kTileN;
-  const int i_begin = a.causal ? kt : 0;  // query tiles before the key tile are masked out
+  // Query tiles wholly before the key tile's first key (query i sees key j iff
+  // j <= i + cofs) are masked out.
+  const int i_begin = a.causal ? max(0, k0 - a.cofs) / kTileM : 0;
   const int n_iter = n_t - i_begin;
 
   if (threadIdx.x == 0) {
@@ -313,8 +316,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_L) + (kEwCols / 4) * h;
       const float4* d4 =
           reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D) + (kEwCols / 4) * h;
-      // causal diagonal tile: query c sees key `row` only if c >= row
-      const int first_visible = (a.causal && qt == kt) ? row - kEwCols * h : 0;  // relative to these columns
+      // causal: query column c (query qt*128 + 32h + c) sees key k0 + row only if
+      // qt*128 + 32h + c + cofs >= k0 + row
+      const int first_visible = a.causal ? k0 + row - a.cofs - qt * kTileM - kEwCols * h : 0;
       float p[kEwCols];
       // Phase 1: P^T for this warpgroup's queries (overlaps the dP^T product).
       {
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tiles first
   const int q0 = qt * kTileM;
-  const int n_kv = a.causal ? qt + 1 : n_t;
+  const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_QFULL), 1);
@@ -573,8 +577,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       if (!(ok = mbar_wait_warp(bar(Q_SFULL), j & 1, wc))) break;
       tc_fence_after();
       const int kbeg = j * kTileN + kEwCols * h;
-      int lim = a.N - kbeg;                           // keys past the end
-      if (a.causal) lim = min(lim, grow - kbeg + 1);  // keys after this query
+      int lim = a.Nk - kbeg;                                   // keys past the end
+      if (a.causal) lim = min(lim, grow + a.cofs - kbeg + 1);  // keys after this query
       float p[kEwCols];
       {
         uint32_t sv[kEwCols];
@@ -646,8 +650,8 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t st) {
   auto k = bwd_dkdv_kernel<D, BF16>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvLayout<D>::SMEM);
   if (e != cudaSuccess) return e;
-  const int n_t = (a.N + kTileN - 1) / kTileN;
-  k<<<n_t * a.BH, kBwdThreads, DkdvLayout<D>::SMEM, st>>>(a);
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;
+  k<<<n_tk * a.BH, kBwdThreads, DkdvLayout<D>::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,9 @@ struct FwdArgs {
   void* o;                             // [B*H][N][d] output (the merge kernel writes it directly)
   float* lse;                          // [B*H][N]
   int* dev_status;                     // nullable
-  int N;
+  int N;                               // queries per head
+  int Nk;                              // keys per head (tm_k, tm_v rows)
+  int cofs;                            // causal: query i sees keys j <= i + cofs (cofs = Nk - N)
   int BH;
   int causal;
   float scale_log2;                    // scale * log2(e)
@@ -27,10 +29,19 @@ struct FwdArgs {
   float* part_o;                       // [n_splits][B*H][N][d] fp32
   float* part_lse;                     // [n_splits][B*H][N] fp32 (natural log; -inf: empty range)
   // E4M3 inputs only: one scale per 128-row block of each head, [B*H][ceil(N/128)]
-  const float* q_scale;
-  const float* k_scale;
+  const float* q_scale;                // [B*H][ceil(N/128)]
+  const float* k_scale;                // [B*H][ceil(Nk/128)]
   const float* v_scale;
 };
+
+// Key tiles query tile qt (rows qt*128 .. qt*128+127) has to visit: every key tile when
+// not causal, else those holding a key j <= the tile's last row + cofs.
+__host__ __device__ __forceinline__ int visible_key_tiles(int qt, int Nk, int causal, int cofs) {
+  const int n_tk = (Nk + 127) / 128;
+  if (!causal) return n_tk;
+  const int last = qt * 128 + 127 + cofs;
+  return min(last / 128 + 1, n_tk);
+}
 
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // inputs, as in FwdArgs
@@ -41,7 +52,9 @@ struct BwdArgs {
   float* lse2;                          // workspace [B*H][Npad]: lse * log2(e); +inf on padding rows
   float* delta;                         // workspace [B*H][Npad]: rowsum(dO * O); 0 on padding rows
   int* dev_status;
-  int N;
+  int N;                                // queries per head
+  int Nk;                               // keys per head
+  int cofs;                             // causal: query i sees keys j <= i + cofs (cofs = Nk - N)
   int Npad;                             // N rounded up to a multiple of 128
   int BH;
   int causal;

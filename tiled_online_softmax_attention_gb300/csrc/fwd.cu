@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_t = (a.N + kTileM - 1) / kTileM;
+  const int n_t = (a.N + kTileM - 1) / kTileM;    // query tiles
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles
   const int n_pairs = (n_t + 1) / 2;
   const int split = SPLIT ? static_cast<int>(blockIdx.x) % a.n_splits : 0;
   const WorkItem wi = work_item(static_cast<int>(blockIdx.x) / (SPLIT ? a.n_splits : 1), a.BH, n_pairs);
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const int pr = n_pairs - 1 - wi.rank;  // longest causal pair first
   int n_kv[2];  // key tiles each query tile visits, starting at key tile kv0
 #pragma unroll
-  for (int i = 0; i < 2; ++i) n_kv[i] = a.causal ? min(2 * pr + i + 1, n_t) : n_t;
+  for (int i = 0; i < 2; ++i) n_kv[i] = visible_key_tiles(2 * pr + i, a.Nk, a.causal, a.cofs);
   int kv0 = 0;
   if constexpr (SPLIT) {
     // Ranges cut tile 0's visible tiles evenly; tile 1's one extra causal tile joins the
@@ -316,8 +317,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const int qt = 2 * pr + i;  // the second tile of the last pair may lie past the end
       if (qt < n_t) sl2 *= a.q_scale[static_cast<size_t>(bh) * n_t + qt];
       if (n_kv[i] > 0) {
-        ks_next = a.k_scale[static_cast<size_t>(bh) * n_t + kv0];
-        vs_next = a.v_scale[static_cast<size_t>(bh) * n_t + kv0];
+        ks_next = a.k_scale[static_cast<size_t>(bh) * n_tk + kv0];
+        vs_next = a.v_scale[static_cast<size_t>(bh) * n_tk + kv0];
       }
     }
     for (int j = 0; j < n_kv[i]; ++j) {
@@ -327,8 +328,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         gj = __log2f(vs_next);
         inv_vs = 1.f / vs_next;
         if (j + 1 < n_kv[i]) {
-          ks_next = a.k_scale[static_cast<size_t>(bh) * n_t + kv0 + j + 1];
-          vs_next = a.v_scale[static_cast<size_t>(bh) * n_t + kv0 + j + 1];
+          ks_next = a.k_scale[static_cast<size_t>(bh) * n_tk + kv0 + j + 1];
+          vs_next = a.v_scale[static_cast<size_t>(bh) * n_tk + kv0 + j + 1];
         }
       }
       if (!mbar_wait_warp(bar(B_SFULL + i), j & 1, wc)) { ok = false; break; }
@@ -345,11 +346,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       }
       const int k0 = (kv0 + j) * kTileN;
-      const bool tail = k0 + kTileN > a.N;
-      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM);
+      const bool tail = k0 + kTileN > a.Nk;
+      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM + a.cofs);
       if (tail || diag) {
-        int lim = a.N - k0;                           // keys past the end of the sequence
-        if (a.causal) lim = min(lim, grow - k0 + 1);  // keys after this query
+        int lim = a.Nk - k0;                                   // keys past the end of the sequence
+        if (a.causal) lim = min(lim, grow + a.cofs - k0 + 1);  // keys after this query
 #pragma unroll
         for (int c = 0; c < kTileN; ++c)
           if (c >= lim) s[c] = -INFINITY;

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_t);
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tile first
-  const int n_kv = a.causal ? qt + 1 : n_t;
+  const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(F_Q), 1);
@@ -215,11 +215,11 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
         for (int cc = 0; cc < 128; ++cc) s[cc] = __uint_as_float(sr[cc]);
       }
       const int k0 = j * kTileN;
-      const bool tail = k0 + kTileN > a.N;
-      const bool diag = a.causal && (k0 + kTileN - 1 > qt * kTileM);
+      const bool tail = k0 + kTileN > a.Nk;
+      const bool diag = a.causal && (k0 + kTileN - 1 > qt * kTileM + a.cofs);
       if (tail || diag) {
-        int lim = a.N - k0;                           // keys past the end of the sequence
-        if (a.causal) lim = min(lim, grow - k0 + 1);  // keys after this query
+        int lim = a.Nk - k0;                                   // keys past the end of the sequence
+        if (a.causal) lim = min(lim, grow + a.cofs - k0 + 1);  // keys after this query
 #pragma unroll
         for (int cc = 0; cc < kTileN; ++cc)
           if (cc >= lim) s[cc] = -INFINITY;
