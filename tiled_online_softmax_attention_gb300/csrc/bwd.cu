@@ -260,12 +260,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
       constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // TMEM x MN-major
-      bool ok = mbar_wait(bar(K_KVFULL), 0, wc);
-      for (int t = 0; ok && t < n_iter; ++t) {
-        const int s = t % L::STAGES;
-        if (!(ok = mbar_wait(bar(K_QFULL + s), (t / L::STAGES) & 1, wc))) break;
-        tc_fence_after();
-        const uint32_t st = stage_base(s);
+      // S^T of the next query tile goes between dV and dK: S^T(t+1) overwrites P^T(t),
+      // which dV(t) (issued before it) reads, and the element-wise warps keep P(t) in
+      // registers for dS^T(t).  So the P^T work of a tile overlaps dK(t-1) and dP^T(t),
+      // and the dS^T work overlaps dV(t) and S^T(t+1): two products each instead of one.
+      auto issue_st = [&](int t) {
+        const uint32_t st = stage_base(t % L::STAGES);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
@@ -273,6 +273,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
                  idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(K_SFULL));
+      };
+      bool ok = mbar_wait(bar(K_KVFULL), 0, wc);
+      if (ok && n_iter > 0 && (ok = mbar_wait(bar(K_QFULL + 0), 0, wc))) {
+        tc_fence_after();
+        issue_st(0);
+      }
+      for (int t = 0; ok && t < n_iter; ++t) {
+        const int s = t % L::STAGES;
+        const uint32_t st = stage_base(s);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
@@ -286,6 +295,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
           mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
                  sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+        if (t + 1 < n_iter) {
+          if (!(ok = mbar_wait(bar(K_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
+          tc_fence_after();
+          issue_st(t + 1);
+        }
         if (!(ok = mbar_wait(bar(K_DSREADY), t & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
