@@ -63,16 +63,18 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
 };
 
-// Order in which CTAs take work.  Heads go in groups of up to 8: within a group
+// Order in which CTAs take work.  Heads go in groups of up to kGroup: within a group
 // the CTAs walk the tile index (rank 0 first), so the CTAs running at one time
 // share a few heads' K/V in L2, and the longest causal tiles of every group start
-// before its short ones (no long tile is left for the end of the grid).
+// before its short ones (no long tile is left for the end of the grid).  Groups of 8
+// suit d <= 128; at d = 256 a head's K/V is twice as large and groups of 2 measured
+// fastest (8 overflowed L2: 5x the input bytes read from DRAM).
 struct WorkItem {
   int bh;    // (batch, head)
   int rank;  // 0 .. n_units-1 in dispatch order within the head
 };
+template <int kGroup = 8>
 __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
-  constexpr int kGroup = 8;
   const int full = BH / kGroup;
   const int per_group = kGroup * n_units;
   int g, y, gs;

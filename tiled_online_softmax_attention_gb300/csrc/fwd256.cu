@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
-  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_t);
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tile first
   const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
