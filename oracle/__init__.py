@@ -24,6 +24,10 @@ dequant_e4m3(codes, scales, block_rows=128) -> float64 array
     per-block scale factors: huaweicloud page, section four, part 3).
 attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal, scale) -> (o, lse)
     attn_fwd of the dequantised inputs.
+attn_fwd_dropout / attn_bwd_dropout(..., t, seed)
+    the same with dropout on the probabilities: keep iff a Philox4x32-10 byte
+    >= t, kept probabilities scaled by 256 / (256 - t) (definition in the C
+    source; "Understanding FlashAttention, Part 2", section 2.4 names dropout).
 
 Pins (tests/test_oracle_pins.py): hand-derived closed forms under
 tests/golden/, brute force with Python ``math`` on tiny inputs, the two-block
@@ -96,6 +100,17 @@ class Oracle:
         lib.oracle_e4m3_value.restype = ctypes.c_double
         lib.oracle_dequant_e4m3.argtypes = [P, P, I64, I64, I64, I64, P]
         lib.oracle_dequant_e4m3.restype = ctypes.c_int
+        U32 = ctypes.c_uint32
+        lib.oracle_philox4x32_10.argtypes = [P, P, P]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_dropout_factor.argtypes = [I64, I64, I64, ctypes.c_int, U32, U32]
+        lib.oracle_dropout_factor.restype = ctypes.c_double
+        lib.oracle_attn_fwd_dropout.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
+                                                ctypes.c_int, U32, U32, P, I64, P, P]
+        lib.oracle_attn_fwd_dropout.restype = ctypes.c_int
+        lib.oracle_attn_bwd_dropout.argtypes = [P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
+                                                ctypes.c_int, U32, U32, P, I64, P, I64, P, P, P]
+        lib.oracle_attn_bwd_dropout.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
         self.lib = lib
@@ -167,6 +182,64 @@ class Oracle:
         v = self.dequant_e4m3(v8, v_scale, block_rows)
         return self.attn_fwd(q, k, v, causal, scale, rows)
 
+    def philox(self, counter, key):
+        """Philox4x32-10 of a 4-word counter and a 2-word key -> 4 uint32 words."""
+        c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32).reshape(4))
+        k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32).reshape(2))
+        out = np.zeros(4, np.uint32)
+        self.lib.oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+        return out
+
+    def dropout_factor(self, bh, i, j, t, seed):
+        """Z_ij of the dropout definition: 0 or 256 / (256 - t)."""
+        seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+        return float(self.lib.oracle_dropout_factor(int(bh), int(i), int(j), int(t), seed & 0xFFFFFFFF, seed >> 32))
+
+    def attn_fwd_dropout(self, q, k, v, causal: bool, scale: float, t: int, seed: int, rows=None):
+        """attn_fwd with dropout on the probabilities (threshold t in 0..255, 64-bit seed)."""
+        q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+        if q.ndim < 2 or k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+            raise ValueError("q must be [..., N, d] and k, v [..., Nk, d] with matching dims")
+        lead, (N, d), Nk = q.shape[:-2], q.shape[-2:], k.shape[-2]
+        BH = int(np.prod(lead)) if lead else 1
+        rr = _rows(rows)
+        R = N if rr is None else rr.size
+        o = np.empty((BH, R, d), np.float64)
+        lse = np.empty((BH, R), np.float64)
+        seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+        rc = self.lib.oracle_attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), BH, N, Nk, d, int(bool(causal)),
+                                              float(scale), int(t), seed & 0xFFFFFFFF, seed >> 32, _ptr(rr),
+                                              0 if rr is None else rr.size, _ptr(o), _ptr(lse))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_fwd_dropout failed (bad argument or out of memory)")
+        return o.reshape(*lead, R, d), lse.reshape(*lead, R)
+
+    def attn_bwd_dropout(self, q, k, v, dout, causal: bool, scale: float, t: int, seed: int, qrows=None,
+                         kcols=None, want_dq: bool = True, want_dkv: bool = True):
+        """attn_bwd with dropout on the probabilities (same t and seed as the forward)."""
+        q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+        if not (q.shape == do.shape and k.shape == v.shape) or q.ndim < 2 or \
+                q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
+            raise ValueError("q, dout must be [..., N, d] and k, v [..., Nk, d] with matching dims")
+        lead, (N, d), Nk = q.shape[:-2], q.shape[-2:], k.shape[-2]
+        BH = int(np.prod(lead)) if lead else 1
+        qr, kc = _rows(qrows), _rows(kcols)
+        nq = N if qr is None else qr.size
+        nk = Nk if kc is None else kc.size
+        dq = np.empty((BH, nq, d), np.float64) if want_dq else None
+        dk = np.empty((BH, nk, d), np.float64) if want_dkv else None
+        dv = np.empty((BH, nk, d), np.float64) if want_dkv else None
+        seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+        rc = self.lib.oracle_attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, Nk, d,
+                                              int(bool(causal)), float(scale), int(t), seed & 0xFFFFFFFF,
+                                              seed >> 32, _ptr(qr), 0 if qr is None else qr.size,
+                                              _ptr(kc), 0 if kc is None else kc.size,
+                                              _ptr(dq), _ptr(dk), _ptr(dv))
+        if rc != 0:
+            raise RuntimeError("oracle_attn_bwd_dropout failed (bad argument or out of memory)")
+        shp = lambda a, r: None if a is None else a.reshape(*lead, r, d)
+        return shp(dq, nq), shp(dk, nk), shp(dv, nk)
+
     def attn_bwd(self, q, k, v, dout, causal: bool, scale: float, qrows=None, kcols=None,
                  want_dq: bool = True, want_dkv: bool = True):
         """Exact attention backward in FP64: gradients of sum(dO * O).
@@ -236,3 +309,16 @@ def attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool, scale: flo
 
 dequant_e4m3.__doc__ = Oracle.dequant_e4m3.__doc__
 attn_fwd_fp8.__doc__ = Oracle.attn_fwd_fp8.__doc__
+
+
+def attn_fwd_dropout(q, k, v, causal: bool, scale: float, t: int, seed: int, rows=None):
+    return default().attn_fwd_dropout(q, k, v, causal, scale, t, seed, rows)
+
+
+def attn_bwd_dropout(q, k, v, dout, causal: bool, scale: float, t: int, seed: int, qrows=None, kcols=None,
+                     want_dq: bool = True, want_dkv: bool = True):
+    return default().attn_bwd_dropout(q, k, v, dout, causal, scale, t, seed, qrows, kcols, want_dq, want_dkv)
+
+
+attn_fwd_dropout.__doc__ = Oracle.attn_fwd_dropout.__doc__
+attn_bwd_dropout.__doc__ = Oracle.attn_bwd_dropout.__doc__

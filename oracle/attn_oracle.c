@@ -41,6 +41,10 @@
  * (oracle_dequant_e4m3) and then go through the same exact forward; the oracle
  * never rounds anything to FP8 itself.
  *
+ * Dropout (oracle_attn_fwd_dropout / oracle_attn_bwd_dropout, at the end of this
+ * file) multiplies each probability by a keep factor drawn from Philox4x32-10; the
+ * definition is written out there.
+ *
  * Layout: every tensor is [BH][N][d] row-major, d fastest, float64.
  * Threads: OpenMP over rows (and over key columns in the backward).
  */
@@ -302,4 +306,222 @@ int oracle_dequant_e4m3(const uint8_t *codes, const float *scales, int64_t BH, i
                 out[base + c] = oracle_e4m3_value(codes[base + c]) * sc;
         }
     return 0;
+}
+
+/*
+ * Dropout on the attention probabilities ("Understanding FlashAttention, Part 2",
+ * section 2.4: the recomputing backward "also covers masking and dropout").  The
+ * pages fix no random-number semantics; this library defines them:
+ *
+ *   Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy
+ *   as 1, 2, 3", SC 2011): counter (c0, c1, c2, c3), key (k0, k1); ten rounds of
+ *     (c0, c1, c2, c3) <- (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0))
+ *   with M0 = 0xD2511F53, M1 = 0xCD9E8D57, the key bumped by (0x9E3779B9, 0xBB67AE85)
+ *   after every round.
+ *
+ *   Element (bh, i, j) (head bh, query i, key j) reads byte j mod 16 of
+ *   Philox(counter = (j / 16, i, bh, 0), key = (seed_lo, seed_hi)), bytes taken
+ *   little-endian from the four output words in order.  It is kept iff that byte is
+ *   >= t, t = round(256 p) in 0..255 (so the drop probability is t / 256), and a kept
+ *   probability is scaled by 1 / (1 - t / 256):
+ *     O = (P o Z) V,   Z_ij = keep_ij * 256 / (256 - t),
+ *   while the saved logsumexp is still that of the scores (dropout comes after the
+ *   softmax).  Backward: dV = (P o Z)^T dO, dP~ = dO V^T, dS = P o (Z o dP~ - c) with
+ *   c_i = sum_k P_ik Z_ik dP~_ik (= rowsum(dO o O)), dQ = scale dS K, dK = scale dS^T Q.
+ */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Z_ij of the definition above: 0 (dropped) or 256 / (256 - t) (kept). */
+double oracle_dropout_factor(int64_t bh, int64_t i, int64_t j, int t, uint32_t seed_lo, uint32_t seed_hi)
+{
+    if (t <= 0) return 1.0;
+    const uint32_t ctr[4] = {(uint32_t)(j / 16), (uint32_t)i, (uint32_t)bh, 0u};
+    const uint32_t key[2] = {seed_lo, seed_hi};
+    uint32_t w[4];
+    oracle_philox4x32_10(ctr, key, w);
+    const int b = (int)(j % 16);
+    const uint32_t byte = (w[b / 4] >> (8 * (b % 4))) & 0xFFu;
+    return byte >= (uint32_t)t ? 256.0 / (256.0 - t) : 0.0;
+}
+
+/*
+ * Forward with dropout: as oracle_attn_fwd (square or Nk >= N keys), with every
+ * probability multiplied by its Z_ij before the sum over keys; lse is unchanged.
+ */
+int oracle_attn_fwd_dropout(const double *q, const double *k, const double *v,
+                            int64_t BH, int64_t N, int64_t Nk, int64_t d, int causal, double scale,
+                            int t, uint32_t seed_lo, uint32_t seed_hi,
+                            const int64_t *rows, int64_t nrows, double *o, double *lse)
+{
+    if (BH < 0 || N < 1 || Nk < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
+    if (t < 0 || t > 255 || (causal && Nk < N)) return -1;
+    int64_t nout = rows ? nrows : N;
+    if (rows)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= N) return -1;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+        if (!s) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4) collapse(2)
+        for (int64_t bh = 0; bh < BH; ++bh) {
+            for (int64_t r = 0; r < nout; ++r) {
+                if (!s) continue;
+                int64_t i = rows ? rows[r] : r;
+                const double *qi = q + (bh * N + i) * d;
+                const double *kh = k + bh * Nk * d;
+                const double *vh = v + bh * Nk * d;
+                int64_t nk = visible_keys(i, N, Nk, causal);
+                double m, l;
+                score_row(qi, kh, nk, d, scale, s);
+                row_stats(s, nk, &m, &l);
+                double *oi = o + (bh * nout + r) * d;
+                for (int64_t c = 0; c < d; ++c) oi[c] = 0.0;
+                for (int64_t j = 0; j < nk; ++j) {
+                    double pz = exp(s[j] - m) / l * oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    const double *vj = vh + j * d;
+                    for (int64_t c = 0; c < d; ++c) oi[c] += pz * vj[c];
+                }
+                lse[bh * nout + r] = m + log(l);
+            }
+        }
+        free(s);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
+ * Backward with dropout (definition above); arguments as oracle_attn_bwd plus t and
+ * the seed.  c_i is summed from its definition, sum_k P_ik Z_ik dP~_ik.
+ */
+int oracle_attn_bwd_dropout(const double *q, const double *k, const double *v,
+                            const double *dout, int64_t BH, int64_t N, int64_t Nk, int64_t d,
+                            int causal, double scale, int t, uint32_t seed_lo, uint32_t seed_hi,
+                            const int64_t *qrows, int64_t nq,
+                            const int64_t *kcols, int64_t nk,
+                            double *dq, double *dk, double *dv)
+{
+    if (BH < 0 || N < 1 || Nk < 1 || d < 1 || !q || !k || !v || !dout) return -1;
+    if (t < 0 || t > 255 || (causal && Nk < N)) return -1;
+    if ((dk == NULL) != (dv == NULL)) return -1;
+    int64_t nqo = qrows ? nq : N;
+    int64_t nko = kcols ? nk : Nk;
+    if (qrows)
+        for (int64_t r = 0; r < nq; ++r)
+            if (qrows[r] < 0 || qrows[r] >= N) return -1;
+    if (kcols)
+        for (int64_t r = 0; r < nk; ++r)
+            if (kcols[r] < 0 || kcols[r] >= Nk) return -1;
+
+    double *m = (double *)malloc(sizeof(double) * (size_t)N);
+    double *l = (double *)malloc(sizeof(double) * (size_t)N);
+    double *c = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!m || !l || !c) { free(m); free(l); free(c); return -1; }
+    int failed = 0;
+
+    for (int64_t bh = 0; bh < BH && !failed; ++bh) {
+        const double *qh = q + bh * N * d;
+        const double *kh = k + bh * Nk * d;
+        const double *vh = v + bh * Nk * d;
+        const double *doh = dout + bh * N * d;
+
+        /* 1. row statistics and c_i = sum_k P_ik Z_ik dP~_ik */
+#pragma omp parallel
+        {
+            double *s = (double *)malloc(sizeof(double) * (size_t)Nk);
+            if (!s) {
+#pragma omp atomic write
+                failed = 1;
+            }
+#pragma omp for schedule(dynamic, 8)
+            for (int64_t i = 0; i < N; ++i) {
+                if (!s) continue;
+                int64_t nkv = visible_keys(i, N, Nk, causal);
+                score_row(qh + i * d, kh, nkv, d, scale, s);
+                row_stats(s, nkv, &m[i], &l[i]);
+                double acc = 0.0;
+                for (int64_t j = 0; j < nkv; ++j) {
+                    double p = exp(s[j] - m[i]) / l[i];
+                    double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double dpt = 0.0;                      /* dP~_ij = dO_i . V_j */
+                    for (int64_t x = 0; x < d; ++x) dpt += doh[i * d + x] * vh[j * d + x];
+                    acc += p * z * dpt;
+                }
+                c[i] = acc;
+            }
+            free(s);
+        }
+        if (failed) break;
+
+        /* 2. dQ_i = scale * sum_j dS_ij K_j */
+        if (dq) {
+#pragma omp parallel for schedule(dynamic, 8)
+            for (int64_t r = 0; r < nqo; ++r) {
+                int64_t i = qrows ? qrows[r] : r;
+                int64_t nkv = visible_keys(i, N, Nk, causal);
+                double *g = dq + (bh * nqo + r) * d;
+                for (int64_t x = 0; x < d; ++x) g[x] = 0.0;
+                for (int64_t j = 0; j < nkv; ++j) {
+                    double sij = 0.0, dpt = 0.0;
+                    for (int64_t x = 0; x < d; ++x) {
+                        sij += qh[i * d + x] * kh[j * d + x];
+                        dpt += doh[i * d + x] * vh[j * d + x];
+                    }
+                    double p = exp(scale * sij - m[i]) / l[i];
+                    double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double ds = p * (z * dpt - c[i]);
+                    for (int64_t x = 0; x < d; ++x) g[x] += scale * ds * kh[j * d + x];
+                }
+            }
+        }
+
+        /* 3. dV_j = sum_i P_ij Z_ij dO_i ;  dK_j = scale * sum_i dS_ij Q_i */
+        if (dk) {
+#pragma omp parallel for schedule(dynamic, 8)
+            for (int64_t r = 0; r < nko; ++r) {
+                int64_t j = kcols ? kcols[r] : r;
+                double *gk = dk + (bh * nko + r) * d;
+                double *gv = dv + (bh * nko + r) * d;
+                for (int64_t x = 0; x < d; ++x) { gk[x] = 0.0; gv[x] = 0.0; }
+                int64_t i0 = causal ? j - (Nk - N) : 0;    /* queries that see key j */
+                if (i0 < 0) i0 = 0;
+                for (int64_t i = i0; i < N; ++i) {
+                    double sij = 0.0, dpt = 0.0;
+                    for (int64_t x = 0; x < d; ++x) {
+                        sij += qh[i * d + x] * kh[j * d + x];
+                        dpt += doh[i * d + x] * vh[j * d + x];
+                    }
+                    double p = exp(scale * sij - m[i]) / l[i];
+                    double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double ds = p * (z * dpt - c[i]);
+                    for (int64_t x = 0; x < d; ++x) {
+                        gv[x] += p * z * doh[i * d + x];
+                        gk[x] += scale * ds * qh[i * d + x];
+                    }
+                }
+            }
+        }
+    }
+    free(m); free(l); free(c);
+    return failed ? -1 : 0;
 }

@@ -425,6 +425,127 @@ def pin_rect_causal_is_a_suffix(orc):
     _close(dv, dv_sq, 1e-12, "rect causal dV = square with dO zero on the prefix")
 
 
+# ---------------------------------------------------------------------------
+# dropout
+
+PHILOX_KAT = os.path.join(os.path.dirname(__file__), "golden", "philox4x32_10_kat.json")
+
+
+def pin_philox_known_answers(orc):
+    """Philox4x32-10 against the generator's published known-answer vectors."""
+    for vec in json.load(open(PHILOX_KAT))["vectors"]:
+        ctr = [int(x, 16) for x in vec["counter"]]
+        key = [int(x, 16) for x in vec["key"]]
+        want = [int(x, 16) for x in vec["output"]]
+        got = [int(x) for x in orc.philox(ctr, key)]
+        assert got == want, f"philox({vec['counter']}, {vec['key']}) = {[hex(g) for g in got]}"
+
+
+def pin_dropout_mask_definition(orc):
+    """The keep factor follows its definition: byte j mod 16 (little-endian over the four
+    words) of Philox((j // 16, i, bh, 0), seed) compared with t, kept ones scaled by
+    256 / (256 - t); t = 0 keeps everything with factor 1."""
+    seed = 0x0123456789ABCDEF
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    rng = np.random.default_rng(37)
+    cases = [(0, 0, 0), (3, 17, 40), (1, 1000, 4095), (2, 5, 15)]
+    cases += [tuple(int(x) for x in (rng.integers(0, 64), rng.integers(0, 5000), rng.integers(0, 5000)))
+              for _ in range(60)]
+    for (bh, i, j) in cases:
+        w = orc.philox([j // 16, i, bh, 0], key)
+        b = j % 16
+        byte = (int(w[b // 4]) >> (8 * (b % 4))) & 0xFF
+        for t in (0, 1, 64, 128, 200, 255):
+            want = 1.0 if t == 0 else (256.0 / (256 - t) if byte >= t else 0.0)
+            assert orc.dropout_factor(bh, i, j, t, seed) == want, f"dropout factor at {(bh, i, j, t)}"
+
+
+def pin_dropout_rate_and_unbiased(orc):
+    """The dropped fraction is t/256 within a binomial bound, and averaging O over many
+    seeds gives the plain attention (the 256 / (256 - t) scale makes dropout unbiased)."""
+    t = 77
+    n = 0
+    dropped = 0
+    for bh in range(2):
+        for i in range(40):
+            for j in range(64):
+                n += 1
+                dropped += orc.dropout_factor(bh, i, j, t, 99) == 0.0
+    p = t / 256
+    assert abs(dropped / n - p) < 4 * math.sqrt(p * (1 - p) / n), f"dropped fraction {dropped / n:.4f} vs {p:.4f}"
+    rng = np.random.default_rng(33)
+    q, k, v = (rng.normal(size=(6, 4)) for _ in range(3))
+    o_ref, _ = orc.attn_fwd(q, k, v, False, 0.5)
+    S = 400
+    acc = np.zeros_like(o_ref)
+    acc2 = np.zeros_like(o_ref)
+    for seed in range(S):
+        o, _ = orc.attn_fwd_dropout(q, k, v, False, 0.5, t, seed)
+        acc += o
+        acc2 += o * o
+    mean = acc / S
+    sd = np.sqrt(np.maximum(acc2 / S - mean ** 2, 1e-30) / S)
+    assert np.all(np.abs(mean - o_ref) < 5 * sd + 1e-12), "dropout output is biased"
+
+
+def pin_dropout_t0_is_plain(orc):
+    """t = 0 keeps every probability: forward and backward equal the plain oracle's bits."""
+    rng = np.random.default_rng(34)
+    q, k, v, do = (rng.normal(size=(2, 9, 3)) for _ in range(4))
+    for causal in (False, True):
+        o, lse = orc.attn_fwd(q, k, v, causal, 0.6)
+        od, lsed = orc.attn_fwd_dropout(q, k, v, causal, 0.6, 0, 5)
+        assert np.array_equal(o, od) and np.array_equal(lse, lsed)
+        g = orc.attn_bwd(q, k, v, do, causal, 0.6)
+        gd = orc.attn_bwd_dropout(q, k, v, do, causal, 0.6, 0, 5)
+        for a, b in zip(g, gd):
+            assert np.array_equal(a, b)
+
+
+def pin_dropout_brute_force(orc):
+    """Tiny inputs: O = sum_j softmax_ij Z_ij V_j with Python floats and the keep factors;
+    the logsumexp is the plain one."""
+    rng = np.random.default_rng(35)
+    for (N, Nk, causal) in [(5, 5, False), (5, 5, True), (3, 20, True)]:
+        q = rng.uniform(-1, 1, (N, 3))
+        k = rng.uniform(-1, 1, (Nk, 3))
+        v = rng.uniform(-2, 2, (Nk, 3))
+        t, seed = 100, 0xDEADBEEF12345
+        o, lse = orc.attn_fwd_dropout(q, k, v, causal, 0.7, t, seed)
+        for i in range(N):
+            keys = range(i + Nk - N + 1) if causal else range(Nk)
+            w = {j: math.exp(0.7 * math.fsum(q[i][x] * k[j][x] for x in range(3))) for j in keys}
+            z = math.fsum(w.values())
+            for c in range(3):
+                ref = math.fsum(w[j] / z * orc.dropout_factor(0, i, j, t, seed) * v[j][c] for j in keys)
+                assert abs(o[i][c] - ref) <= 1e-12 * max(1.0, abs(ref)), f"dropout brute force O[{i},{c}]"
+            assert abs(lse[i] - math.log(z)) <= 1e-12 * max(1.0, abs(math.log(z)))
+
+
+def pin_dropout_bwd_finite_differences(orc):
+    """Central differences of sum(dO * O_dropout) with the mask fixed by the seed."""
+    rng = np.random.default_rng(36)
+    t, seed = 90, 4242
+    for causal, N, Nk in ((False, 5, 5), (True, 5, 7)):
+        q, do = (rng.normal(size=(N, 3)) for _ in range(2))
+        k, v = (rng.normal(size=(Nk, 3)) for _ in range(2))
+        dq, dk, dv = orc.attn_bwd_dropout(q, k, v, do, causal, 0.8, t, seed)
+        h = 1e-6
+        for name, x, g in (("dQ", q, dq), ("dK", k, dk), ("dV", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                ap = {"dQ": (xp, k, v), "dK": (q, xp, v), "dV": (q, k, xp)}[name]
+                am = {"dQ": (xm, k, v), "dK": (q, xm, v), "dV": (q, k, xm)}[name]
+                lp = np.sum(do * orc.attn_fwd_dropout(*ap, causal, 0.8, t, seed)[0])
+                lm = np.sum(do * orc.attn_fwd_dropout(*am, causal, 0.8, t, seed)[0])
+                num[idx] = (lp - lm) / (2 * h)
+            err = np.max(np.abs(num - g)) / max(1e-3, np.max(np.abs(g)))
+            assert err < 1e-6, f"dropout {name} vs finite differences (causal={causal}): {err:.2e}"
+
+
 ALL_PINS = [
     pin_golden_closed_forms, pin_brute_force, pin_rows_sum_to_one, pin_equal_scores,
     pin_merge_rule, pin_online_recurrence, pin_one_hot_large_scores, pin_causal_first_row,
@@ -432,4 +553,6 @@ ALL_PINS = [
     pin_bwd_invariants, pin_bwd_autograd,
     pin_e4m3_closed_forms, pin_e4m3_all_codes_vs_torch, pin_dequant_brute_force,
     pin_fp8_attention_brute_force, pin_rect_causal_is_a_suffix,
+    pin_philox_known_answers, pin_dropout_mask_definition, pin_dropout_rate_and_unbiased,
+    pin_dropout_t0_is_plain, pin_dropout_brute_force, pin_dropout_bwd_finite_differences,
 ]

@@ -37,6 +37,16 @@ MUTANTS = [
      "return causal ? (i + 1) : Nk;"),
     ("rectangular causal backward without the offset", "int64_t i0 = causal ? j - (Nk - N) : 0;",
      "int64_t i0 = causal ? j : 0;"),
+    ("philox multiplier off by two", "(uint64_t)0xD2511F53u * c0", "(uint64_t)0xD2511F55u * c0"),
+    ("philox key bump dropped", "k1 += 0xBB67AE85u;", ""),
+    ("dropout without the rescale", "return byte >= (uint32_t)t ? 256.0 / (256.0 - t) : 0.0;",
+     "return byte >= (uint32_t)t ? 1.0 : 0.0;"),
+    ("dropout bytes big-endian", "(w[b / 4] >> (8 * (b % 4)))", "(w[b / 4] >> (24 - 8 * (b % 4)))"),
+    ("dropout counter fields swapped", "{(uint32_t)(j / 16), (uint32_t)i, (uint32_t)bh, 0u}",
+     "{(uint32_t)(i / 16), (uint32_t)j, (uint32_t)bh, 0u}"),
+    ("dropout row term without the keep factor", "acc += p * z * dpt;", "acc += p * dpt;"),
+    ("dropout dV without the keep factor", "gv[x] += p * z * doh[i * d + x];", "gv[x] += p * doh[i * d + x];"),
+    ("dropout dS without the keep factor", "double ds = p * (z * dpt - c[i]);", "double ds = p * (dpt - c[i]);"),
 ]
 
 
