@@ -378,7 +378,39 @@ def long_forward(attn, dev):
     res["forward_by_workload"] = forward_by_workload(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     res["d256_forward_B1_H16_N16384_d256"] = d256_forward(attn, dev)
+    res["dropout_training_step_p0.1"] = dropout_step(attn, dev)
     return res
+
+
+def dropout_step(attn, dev):
+    """The training-step workload (forward + backward) with dropout p = 0.1, against the
+    same step without dropout; FLOPs counted as without dropout."""
+    w = workloads.WORKLOADS["c5"]
+    x = workloads.inputs("c5")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    nb = attn.attn_bwd_workspace_bytes(w.B, w.H, w.N, w.d)
+    ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+    out = {}
+    for p in (0.0, 0.1):
+        def step():
+            attn.attn_fwd_dropout(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, True, w.scale, p, 1234)
+            attn.attn_bwd_dropout(q, k, v, o, do, lse, dq, dk, dv, ws, nb, w.B, w.H, w.N, w.d, q.dtype, True,
+                                  w.scale, p, 1234)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record()
+        for _ in range(reps):
+            step()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        out[f"p{p}"] = {"ms": round(ms, 4), "tflops": round(step_flops(w) / (ms * 1e-3) / 1e12, 1)}
+    return out
 
 
 def d256_forward(attn, dev):

@@ -101,6 +101,33 @@ ATTN_API attn_status attn_fwd_rect(const void *q, const void *k, const void *v, 
                           int *dev_status, void *stream);
 
 /*
+ * attn_fwd_dropout / attn_bwd_dropout -- attn_fwd / attn_bwd with dropout on the
+ * attention probabilities (the recomputing backward of "Understanding
+ * FlashAttention, Part 2", section 2.4, also covers dropout).  The pages fix no
+ * random-number semantics; this library's are:
+ *   t = round(256 * p_drop), p_drop finite in [0, 1) with t <= 255 (else
+ *   ATTN_ERR_INVALID_ARG); the drop probability is t / 256.
+ *   Element (bh, i, j) (bh = b*H + h, query i, key j) reads byte j mod 16 of
+ *   Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3",
+ *   SC 2011) at counter (j / 16, i, bh, 0) with key (seed low 32 bits, seed high
+ *   32 bits), bytes taken little-endian from the four output words in order; it is
+ *   kept iff that byte >= t.
+ *   O = (P o Z) V with Z = keep * 256 / (256 - t); lse is the logsumexp of the
+ *   scores, as without dropout.  The backward must get the same p_drop and seed:
+ *   dV = (P o Z)^T dO, dS = P o (Z o dP - D), D_i = rowsum(dO_i o O_i).
+ * d in {64, 128}; square shapes.  Everything else is as for attn_fwd / attn_bwd.
+ * p_drop = 0 runs the plain kernels.
+ */
+ATTN_API attn_status attn_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                             float p_drop, uint64_t seed, int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_dropout(const void *q, const void *k, const void *v, const void *o,
+                             const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                             void *workspace, size_t workspace_bytes,
+                             int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                             float p_drop, uint64_t seed, int *dev_status, void *stream);
+
+/*
  * attn_fwd_splitkv -- the forward pass for shapes with too few query tiles to fill
  * the GPU (few heads, long sequences): every pair of 128-row query tiles has its key
  * tiles cut into n_splits contiguous ranges, each processed by its own CTA, which

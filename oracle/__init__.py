@@ -106,10 +106,10 @@ class Oracle:
         lib.oracle_dropout_factor.argtypes = [I64, I64, I64, ctypes.c_int, U32, U32]
         lib.oracle_dropout_factor.restype = ctypes.c_double
         lib.oracle_attn_fwd_dropout.argtypes = [P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
-                                                ctypes.c_int, U32, U32, P, I64, P, P]
+                                                ctypes.c_int, U32, U32, I64, P, I64, P, P]
         lib.oracle_attn_fwd_dropout.restype = ctypes.c_int
         lib.oracle_attn_bwd_dropout.argtypes = [P, P, P, P, I64, I64, I64, I64, ctypes.c_int, ctypes.c_double,
-                                                ctypes.c_int, U32, U32, P, I64, P, I64, P, P, P]
+                                                ctypes.c_int, U32, U32, I64, P, I64, P, I64, P, P, P]
         lib.oracle_attn_bwd_dropout.restype = ctypes.c_int
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -195,8 +195,9 @@ class Oracle:
         seed = int(seed) & 0xFFFFFFFFFFFFFFFF
         return float(self.lib.oracle_dropout_factor(int(bh), int(i), int(j), int(t), seed & 0xFFFFFFFF, seed >> 32))
 
-    def attn_fwd_dropout(self, q, k, v, causal: bool, scale: float, t: int, seed: int, rows=None):
-        """attn_fwd with dropout on the probabilities (threshold t in 0..255, 64-bit seed)."""
+    def attn_fwd_dropout(self, q, k, v, causal: bool, scale: float, t: int, seed: int, rows=None, bh0: int = 0):
+        """attn_fwd with dropout on the probabilities (threshold t in 0..255, 64-bit seed); the
+        arrays' heads are heads bh0, bh0 + 1, ... of the mask."""
         q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
         if q.ndim < 2 or k.shape != v.shape or q.shape[:-2] != k.shape[:-2] or q.shape[-1] != k.shape[-1]:
             raise ValueError("q must be [..., N, d] and k, v [..., Nk, d] with matching dims")
@@ -208,14 +209,14 @@ class Oracle:
         lse = np.empty((BH, R), np.float64)
         seed = int(seed) & 0xFFFFFFFFFFFFFFFF
         rc = self.lib.oracle_attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), BH, N, Nk, d, int(bool(causal)),
-                                              float(scale), int(t), seed & 0xFFFFFFFF, seed >> 32, _ptr(rr),
+                                              float(scale), int(t), seed & 0xFFFFFFFF, seed >> 32, int(bh0), _ptr(rr),
                                               0 if rr is None else rr.size, _ptr(o), _ptr(lse))
         if rc != 0:
             raise RuntimeError("oracle_attn_fwd_dropout failed (bad argument or out of memory)")
         return o.reshape(*lead, R, d), lse.reshape(*lead, R)
 
     def attn_bwd_dropout(self, q, k, v, dout, causal: bool, scale: float, t: int, seed: int, qrows=None,
-                         kcols=None, want_dq: bool = True, want_dkv: bool = True):
+                         kcols=None, want_dq: bool = True, want_dkv: bool = True, bh0: int = 0):
         """attn_bwd with dropout on the probabilities (same t and seed as the forward)."""
         q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
         if not (q.shape == do.shape and k.shape == v.shape) or q.ndim < 2 or \
@@ -232,7 +233,7 @@ class Oracle:
         seed = int(seed) & 0xFFFFFFFFFFFFFFFF
         rc = self.lib.oracle_attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(do), BH, N, Nk, d,
                                               int(bool(causal)), float(scale), int(t), seed & 0xFFFFFFFF,
-                                              seed >> 32, _ptr(qr), 0 if qr is None else qr.size,
+                                              seed >> 32, int(bh0), _ptr(qr), 0 if qr is None else qr.size,
                                               _ptr(kc), 0 if kc is None else kc.size,
                                               _ptr(dq), _ptr(dk), _ptr(dv))
         if rc != 0:
@@ -311,13 +312,13 @@ dequant_e4m3.__doc__ = Oracle.dequant_e4m3.__doc__
 attn_fwd_fp8.__doc__ = Oracle.attn_fwd_fp8.__doc__
 
 
-def attn_fwd_dropout(q, k, v, causal: bool, scale: float, t: int, seed: int, rows=None):
-    return default().attn_fwd_dropout(q, k, v, causal, scale, t, seed, rows)
+def attn_fwd_dropout(q, k, v, causal: bool, scale: float, t: int, seed: int, rows=None, bh0: int = 0):
+    return default().attn_fwd_dropout(q, k, v, causal, scale, t, seed, rows, bh0)
 
 
 def attn_bwd_dropout(q, k, v, dout, causal: bool, scale: float, t: int, seed: int, qrows=None, kcols=None,
-                     want_dq: bool = True, want_dkv: bool = True):
-    return default().attn_bwd_dropout(q, k, v, dout, causal, scale, t, seed, qrows, kcols, want_dq, want_dkv)
+                     want_dq: bool = True, want_dkv: bool = True, bh0: int = 0):
+    return default().attn_bwd_dropout(q, k, v, dout, causal, scale, t, seed, qrows, kcols, want_dq, want_dkv, bh0)
 
 
 attn_fwd_dropout.__doc__ = Oracle.attn_fwd_dropout.__doc__

@@ -363,10 +363,11 @@ double oracle_dropout_factor(int64_t bh, int64_t i, int64_t j, int t, uint32_t s
 /*
  * Forward with dropout: as oracle_attn_fwd (square or Nk >= N keys), with every
  * probability multiplied by its Z_ij before the sum over keys; lse is unchanged.
+ * The arrays hold heads bh0 .. bh0 + BH - 1 (the head index enters the keep mask).
  */
 int oracle_attn_fwd_dropout(const double *q, const double *k, const double *v,
                             int64_t BH, int64_t N, int64_t Nk, int64_t d, int causal, double scale,
-                            int t, uint32_t seed_lo, uint32_t seed_hi,
+                            int t, uint32_t seed_lo, uint32_t seed_hi, int64_t bh0,
                             const int64_t *rows, int64_t nrows, double *o, double *lse)
 {
     if (BH < 0 || N < 1 || Nk < 1 || d < 1 || !q || !k || !v || !o || !lse) return -1;
@@ -398,7 +399,7 @@ int oracle_attn_fwd_dropout(const double *q, const double *k, const double *v,
                 double *oi = o + (bh * nout + r) * d;
                 for (int64_t c = 0; c < d; ++c) oi[c] = 0.0;
                 for (int64_t j = 0; j < nk; ++j) {
-                    double pz = exp(s[j] - m) / l * oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double pz = exp(s[j] - m) / l * oracle_dropout_factor(bh0 + bh, i, j, t, seed_lo, seed_hi);
                     const double *vj = vh + j * d;
                     for (int64_t c = 0; c < d; ++c) oi[c] += pz * vj[c];
                 }
@@ -411,12 +412,14 @@ int oracle_attn_fwd_dropout(const double *q, const double *k, const double *v,
 }
 
 /*
- * Backward with dropout (definition above); arguments as oracle_attn_bwd plus t and
- * the seed.  c_i is summed from its definition, sum_k P_ik Z_ik dP~_ik.
+ * Backward with dropout (definition above); arguments as oracle_attn_bwd plus t, the
+ * seed and the first head's index bh0.  c_i is summed from its definition,
+ * sum_k P_ik Z_ik dP~_ik.
  */
 int oracle_attn_bwd_dropout(const double *q, const double *k, const double *v,
                             const double *dout, int64_t BH, int64_t N, int64_t Nk, int64_t d,
                             int causal, double scale, int t, uint32_t seed_lo, uint32_t seed_hi,
+                            int64_t bh0,
                             const int64_t *qrows, int64_t nq,
                             const int64_t *kcols, int64_t nk,
                             double *dq, double *dk, double *dv)
@@ -462,7 +465,7 @@ int oracle_attn_bwd_dropout(const double *q, const double *k, const double *v,
                 double acc = 0.0;
                 for (int64_t j = 0; j < nkv; ++j) {
                     double p = exp(s[j] - m[i]) / l[i];
-                    double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double z = oracle_dropout_factor(bh0 + bh, i, j, t, seed_lo, seed_hi);
                     double dpt = 0.0;                      /* dP~_ij = dO_i . V_j */
                     for (int64_t x = 0; x < d; ++x) dpt += doh[i * d + x] * vh[j * d + x];
                     acc += p * z * dpt;
@@ -488,7 +491,7 @@ int oracle_attn_bwd_dropout(const double *q, const double *k, const double *v,
                         dpt += doh[i * d + x] * vh[j * d + x];
                     }
                     double p = exp(scale * sij - m[i]) / l[i];
-                    double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double z = oracle_dropout_factor(bh0 + bh, i, j, t, seed_lo, seed_hi);
                     double ds = p * (z * dpt - c[i]);
                     for (int64_t x = 0; x < d; ++x) g[x] += scale * ds * kh[j * d + x];
                 }
@@ -512,7 +515,7 @@ int oracle_attn_bwd_dropout(const double *q, const double *k, const double *v,
                         dpt += doh[i * d + x] * vh[j * d + x];
                     }
                     double p = exp(scale * sij - m[i]) / l[i];
-                    double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);
+                    double z = oracle_dropout_factor(bh0 + bh, i, j, t, seed_lo, seed_hi);
                     double ds = p * (z * dpt - c[i]);
                     for (int64_t x = 0; x < d; ++x) {
                         gv[x] += p * z * doh[i * d + x];

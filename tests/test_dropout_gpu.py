@@ -1,0 +1,157 @@
+"""Dropout (attn_fwd_dropout / attn_bwd_dropout) against the FP64 oracle with the same
+keep mask (Philox4x32-10, definition in include/attn.h), through the C ABI.
+
+Tolerances: dropout scales the kept probabilities by Z = 256 / (256 - t), so output
+magnitudes, and the rounding errors that scale with them, grow by Z; the O bound is
+O_MAX_ABS * Z plus the output type's half-ulp.  The logsumexp is the undropped one and
+keeps its bound; gradients keep their relative-L2 bound."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tiled_online_softmax_attention_gb300 as attn
+import workloads
+from gpu_util import GRAD_REL_L2, LSE_REL, O_MAX_ABS, Guarded, f64, grad_err, half_ulp, lse_err, o_err, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def t_of(p):
+    return int(round(256 * p))
+
+
+def run_fwd_drop(q, k, v, causal, scale, p, seed):
+    B, H, N, d = q.shape
+    o = Guarded((B, H, N, d), q.dtype)
+    lse = Guarded((B, H, N), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_dropout(q, k, v, o.t, lse.t, B, H, N, d, q.dtype, causal, scale, p, seed, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and o.intact() and lse.intact()
+    return o.t, lse.t
+
+
+def run_bwd_drop(q, k, v, o, lse, do, causal, scale, p, seed):
+    B, H, N, d = q.shape
+    outs = [Guarded((B, H, N, d), q.dtype) for _ in range(3)]
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_bwd_dropout(q, k, v, o, do, lse, outs[0].t, outs[1].t, outs[2].t, ws.t, nbytes, B, H, N, d,
+                               q.dtype, causal, scale, p, seed, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and all(g.intact() for g in outs) and ws.intact()
+    return tuple(g.t for g in outs)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 127, 128, 129, 300, 513])
+def test_dropout_fwd_bwd(N, causal, d, p):
+    x = workloads.draw(1, 2, N, d, "bf16", seed=3000 + N + d, with_dout=True)
+    scale = 1.0 / math.sqrt(d)
+    seed = 0x5EED0000 + N
+    t = t_of(p)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = run_fwd_drop(q, k, v, causal, scale, p, seed)
+    ro, rl = oracle.attn_fwd_dropout(x["q"], x["k"], x["v"], causal, scale, t, seed)
+    z = 256.0 / (256 - t)
+    assert o_err(o, ro) <= O_MAX_ABS * z, f"O error {o_err(o, ro):.3e}"
+    assert lse_err(lse, rl) <= LSE_REL
+    g = run_bwd_drop(q, k, v, o, lse, do, causal, scale, p, seed)
+    r = oracle.attn_bwd_dropout(x["q"], x["k"], x["v"], x["dout"], causal, scale, t, seed)
+    if N == 1:
+        # One key: P = 1 and the exact dS = Z dP - D is 0, so dQ = dK = 0.  The GPU's D is
+        # rowsum(dO o O) of the 16-bit O = round(Z V), off from Z dP by at most
+        # sum_c |dO_c| half_ulp(O_c); dQ = scale dS K and dK = scale dS Q inherit that.
+        o_ref = ro[..., 0, :]
+        dsum = np.sum(np.abs(x["dout"].double().numpy()[..., 0, :]) * half_ulp(o_ref, torch.bfloat16), axis=-1)
+        for gg, other in ((g[0], x["k"]), (g[1], x["q"])):
+            bound = scale * (dsum[..., None] * 1.01 + 1e-6) * np.abs(other.double().numpy()[..., 0, :])
+            assert np.all(np.abs(f64(gg)[..., 0, :]) <= bound + 1e-6), "N=1 gradient residue above its bound"
+        assert grad_err(g[2], r[2]) <= GRAD_REL_L2
+        return
+    for name, gg, rr in zip(("dQ", "dK", "dV"), g, r):
+        e = grad_err(gg, rr)
+        assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e} (N={N} d={d} causal={causal} p={p})"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_dropout_fp16_and_bf16(dtype):
+    x = workloads.draw(2, 3, 700, 128, dtype, seed=31, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = run_fwd_drop(q, k, v, True, 0.09, 0.2, 77)
+    ro, rl = oracle.attn_fwd_dropout(x["q"], x["k"], x["v"], True, 0.09, t_of(0.2), 77)
+    assert o_err(o, ro) <= O_MAX_ABS * 256 / (256 - t_of(0.2)) and lse_err(lse, rl) <= LSE_REL
+    g = run_bwd_drop(q, k, v, o, lse, do, True, 0.09, 0.2, 77)
+    r = oracle.attn_bwd_dropout(x["q"], x["k"], x["v"], x["dout"], True, 0.09, t_of(0.2), 77)
+    for gg, rr in zip(g, r):
+        assert grad_err(gg, rr) <= GRAD_REL_L2
+
+
+def test_dropout_mask_exact():
+    """Q = 0 makes every visible probability 1/n; with V_j the unit vector e_j, O_ij * n is
+    exactly the keep factor Z_ij of key j < d: the GPU's mask equals the oracle's, bit for bit
+    of the keep decision."""
+    B, H, N, d = 1, 3, 128, 128
+    for causal in (False, True):
+        q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+        k = torch.randn((B, H, N, d), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+        v = torch.eye(d, dtype=torch.bfloat16).expand(B, H, N, d).contiguous().cuda()
+        p, seed = 0.3, 0xABCDEF0123
+        t = t_of(p)
+        o, _ = run_fwd_drop(q, k, v, causal, 0.1, p, seed)
+        o = f64(o)
+        kept = 0
+        for h in range(H):
+            for i in range(N):
+                n = i + 1 if causal else N
+                for j in range(n):
+                    zref = oracle.default().dropout_factor(h, i, j, t, seed)
+                    got = o[0, h, i, j] * n
+                    assert (got > 0) == (zref > 0), f"keep decision differs at head {h}, query {i}, key {j}"
+                    kept += zref > 0
+        total = H * (N * (N + 1) // 2 if causal else N * N)
+        assert abs(1 - kept / total - t / 256) < 0.02
+
+
+def test_dropout_zero_is_plain_and_seeds_differ():
+    x = workloads.draw(1, 2, 400, 128, "bf16", seed=8)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    o0, l0 = run_fwd_drop(q, k, v, True, 0.088, 0.0, 1)
+    o1, l1 = attn.forward(q, k, v, True, 0.088)
+    assert torch.equal(o0, o1) and torch.equal(l0, l1)
+    oa, _ = run_fwd_drop(q, k, v, True, 0.088, 0.25, 1)
+    ob, _ = run_fwd_drop(q, k, v, True, 0.088, 0.25, 1)
+    oc, _ = run_fwd_drop(q, k, v, True, 0.088, 0.25, 2)
+    assert torch.equal(oa, ob) and not torch.equal(oa, oc)
+
+
+def test_dropout_training_step_sampled():
+    """The training-step shape (B=2, H=16, N=8192, d=128, causal) with p = 0.1: sampled
+    query rows (O, LSE, dQ) and key rows (dK, dV) of two heads."""
+    w = workloads.WORKLOADS["c5"]
+    x = workloads.inputs("c5")
+    p, seed = 0.1, 20260101
+    t = t_of(p)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = run_fwd_drop(q, k, v, True, w.scale, p, seed)
+    dq, dk, dv = run_bwd_drop(q, k, v, o, lse, do, True, w.scale, p, seed)
+    rows = sample_rows(w.N, extra=8, seed=9)
+    for (b, h) in [(0, 0), (w.B - 1, w.H - 1)]:
+        bh = b * w.H + h
+        qb, kb, vb, dob = (x[n][b, h] for n in ("q", "k", "v", "dout"))
+        ro, rl = oracle.attn_fwd_dropout(qb, kb, vb, True, w.scale, t, seed, rows=rows, bh0=bh)
+        assert o_err(o[b, h], ro, rows) <= O_MAX_ABS * 256 / (256 - t)
+        assert float(np.max(np.abs(f64(lse[b, h])[rows] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+        rq, rk, rv = oracle.attn_bwd_dropout(qb, kb, vb, dob, True, w.scale, t, seed, qrows=rows, kcols=rows, bh0=bh)
+        for name, gg, rr in (("dQ", f64(dq[b, h])[rows], rq), ("dK", f64(dk[b, h])[rows], rk),
+                             ("dV", f64(dv[b, h])[rows], rv)):
+            e = grad_err(gg, rr)
+            assert e <= GRAD_REL_L2, f"head ({b},{h}) {name} relative L2 {e:.3e}"

@@ -11,6 +11,9 @@ current stream):
 
     attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
     attn_fwd_rect(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None, stream=None)
+    attn_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                     B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None, stream=None)
     attn_bwd_rect(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
                   B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None)
     attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, out_dt, causal, scale,
@@ -51,7 +54,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -75,6 +78,11 @@ def load(build_if_missing: bool = True):
     lib = ctypes.CDLL(LIB_PATH)
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
+    U64 = ctypes.c_uint64
+    lib.attn_fwd_dropout.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, U64, P, P]
+    lib.attn_fwd_dropout.restype = I
+    lib.attn_bwd_dropout.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, F, U64, P, P]
+    lib.attn_bwd_dropout.restype = I
     lib.attn_fwd_rect.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P]
     lib.attn_fwd_rect.restype = I
     lib.attn_bwd_rect.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, P, P]
@@ -143,6 +151,21 @@ def attn_status_string(status: int) -> str:
 def attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None) -> int:
     return int(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
                                _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None,
+                     stream=None) -> int:
+    return int(load().attn_fwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
+                                       _dt(dt), int(bool(causal)), float(scale), float(p_drop),
+                                       int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, dt, causal, scale,
+                     p_drop, seed, dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_dropout(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), int(B), int(H),
+                                       int(N), int(d), _dt(dt), int(bool(causal)), float(scale), float(p_drop),
+                                       int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status), _stream(stream)))
 
 
 def attn_fwd_rect(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None) -> int:

@@ -78,6 +78,30 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
 }
 
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Dropout parameters: t = round(256 p) in 0..255 (0 = no dropout) and the 64-bit seed.
+struct Dropout {
+  uint32_t t = 0;
+  uint64_t seed = 0;
+};
+
+// p must be finite and in [0, 1) with round(256 p) <= 255.
+bool dropout_from_p(float p, uint64_t seed, Dropout* out) {
+  if (!(std::isfinite(p) && p >= 0.f && p < 1.f)) return false;
+  const long t = std::lround(256.0 * static_cast<double>(p));
+  if (t > 255) return false;
+  out->t = static_cast<uint32_t>(t);
+  out->seed = seed;
+  return true;
+}
+
+template <class Args>
+void set_dropout(Args& a, const Dropout& dr) {
+  a.drop_t = dr.t;
+  a.seed_lo = static_cast<uint32_t>(dr.seed);
+  a.seed_hi = static_cast<uint32_t>(dr.seed >> 32);
+  a.drop_scale = 256.f / static_cast<float>(256 - static_cast<int>(dr.t));
+}
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // d = 256 is accepted only where the caller says so (the forward).  Nk = key length.
@@ -130,8 +154,9 @@ namespace {
 
 // The forward for Nq queries against Nk keys (Nk = Nq for attn_fwd).
 attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int Nk,
-                     int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale, true, Nk);
+                     int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
+                     const Dropout& dr = Dropout{}) {
+  attn_status st = check_sizes(B, H, N, d, dt, scale, dr.t == 0, Nk);
   if (st != ATTN_OK) return st;
   if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -160,8 +185,10 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
-  const cudaError_t e = d == 256 ? attn::launch_fwd256(a, bf16, static_cast<cudaStream_t>(stream))
-                                 : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
+  set_dropout(a, dr);
+  const cudaError_t e = d == 256  ? attn::launch_fwd256(a, bf16, static_cast<cudaStream_t>(stream))
+                        : dr.t > 0 ? attn::launch_fwd_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
+                                   : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -178,6 +205,14 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 attn_status attn_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                           int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status, stream);
+}
+
+attn_status attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                             int d, attn_dtype dt, int causal, float scale, float p_drop, uint64_t seed,
+                             int* dev_status, void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, dt, causal, scale, dev_status, stream, dr);
 }
 
 attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
@@ -320,7 +355,8 @@ attn_status check_bwd(std::initializer_list<Buf> ins, const float* lse, std::ini
 }
 
 void fill_bwd(attn::BwdArgs& a, const void* ws, int B, int H, int N, int Nk, int causal, float scale,
-              int* dev_status) {
+              int* dev_status, const Dropout& dr = Dropout{}) {
+  set_dropout(a, dr);
   const int BH = B * H;
   const int npad = static_cast<int>((static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM);
   a.lse2 = static_cast<float*>(const_cast<void*>(ws));
@@ -358,7 +394,7 @@ attn_status prepare_impl(const void* o, const void* dout, const float* lse, void
 
 attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                       size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
-                      int causal, float scale, int* dev_status, void* stream) {
+                      int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
                              workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
@@ -370,14 +406,16 @@ attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* d
       !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
       !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) || !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
     return ATTN_ERR_CUDA;
-  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status);
-  if (attn::launch_bwd_dkdv(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
+  const cudaError_t e = dr.t > 0 ? attn::launch_bwd_dkdv_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
+                                 : attn::launch_bwd_dkdv(a, d, bf16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 
 attn_status dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                     size_t workspace_bytes, void* dq, int B, int H, int N, int Nk, int d, attn_dtype dt, int causal,
-                    float scale, int* dev_status, void* stream) {
+                    float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dq, qb}}, workspace,
                              workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
@@ -389,14 +427,17 @@ attn_status dq_impl(const void* q, const void* k, const void* v, const void* dou
       !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
       !make_map(&a.tm_dq, dq, BH, N, d, bf16))
     return ATTN_ERR_CUDA;
-  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status);
-  if (attn::launch_bwd_dq(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
+  const cudaError_t e = dr.t > 0 ? attn::launch_bwd_dq_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
+                                 : attn::launch_bwd_dq(a, d, bf16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
-                     int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+                     int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
+                     const Dropout& dr = Dropout{}) {
   if (!lse) return ATTN_ERR_INVALID_ARG;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},
@@ -404,10 +445,10 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if (st != ATTN_OK) return st;
   if ((st = prepare_impl(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
   if ((st = dkdv_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
-                      dev_status, stream)) != ATTN_OK)
+                      dev_status, stream, dr)) != ATTN_OK)
     return st;
   return dq_impl(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, Nk, d, dt, causal, scale, dev_status,
-                 stream);
+                 stream, dr);
 }
 
 }  // namespace
@@ -439,6 +480,16 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      void* stream) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
                   dev_status, stream);
+}
+
+attn_status attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                             int B, int H, int N, int d, attn_dtype dt, int causal, float scale, float p_drop,
+                             uint64_t seed, int* dev_status, void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
+                  dev_status, stream, dr);
 }
 
 attn_status attn_bwd_rect(const void* q, const void* k, const void* v, const void* o, const void* dout,

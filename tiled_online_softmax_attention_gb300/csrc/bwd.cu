@@ -23,6 +23,10 @@
 //             S, dP and dQ in tensor memory, dS in 16 bits feeds dQ.
 // Recomputing S and dP in both tile orders costs two extra N x N x d products
 // (seven instead of five) and buys independence from floating-point atomics.
+//
+// DROP (dropout, with the forward's keep mask and scale Z = keep * 256 / (256 - t)):
+//   dV = (P o Z)^T dO,  dS = P o (Z o dP - D); D = rowsum(dO o O) still equals
+//   sum_k P_ik Z_ik dP_ik because O is the dropped-out output.
 #include <cuda_fp16.h>
 
 #include "common.cuh"
@@ -155,7 +159,9 @@ struct DkdvLayout {
   static constexpr int OFF_V = T::TILE;
   static constexpr int OFF_ST = 2 * T::TILE;
   static constexpr int OFF_BAR = OFF_ST + STAGES * STAGE_BYTES;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static constexpr int OFF_DROP = OFF_BAR + 256;           // dropout: 1 KB per element-wise warp
+  static constexpr int DROP_BYTES = 32 * 4 * kEw * 32;
+  static constexpr int SMEM = OFF_DROP + 1024;             // + DROP_BYTES with dropout
   static constexpr int S_Q = 0, S_DO = T::TILE, S_L = 2 * T::TILE, S_D = 2 * T::TILE + 512;
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TM_COLS = 512;
 };
@@ -173,7 +179,7 @@ enum : int {
   K_COUNT = 15
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
   using L = DkdvLayout<D>;
   using T = BwdTiles<D>;
@@ -319,10 +325,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t t_s = t_lane + L::TM_S + kEwCols * h, t_dp = t_lane + L::TM_DP + kEwCols * h;
     const float sl2 = a.scale_log2;
+    // dropout: this warp's 32 x 32 block of keep bytes goes through 1 KB of shared memory
+    // (written by query, read by key) so that each thread gets its key's 32 queries
+    uint8_t* dbuf = smem + L::OFF_DROP + (warp - 4) * 1024;
     bool ok = true;
     for (int t = 0; t < n_iter; ++t) {
       const int s = t % L::STAGES;
       const int qt = i_begin + t;
+      uint32_t keepbits = 0xffffffffu;  // bit c: query column c keeps this key
+      if constexpr (DROP) {
+        // Lane L draws the keep bytes of query qt*128 + 32h + L for keys k0 + 32wq .. +31.
+        const uint32_t qi = static_cast<uint32_t>(qt * kTileM + kEwCols * h + lane);
+        const uint32_t jg = static_cast<uint32_t>((k0 + 32 * wq) / 16);
+        uint32_t w0[4], w1[4];
+        philox4x32_10(jg, qi, static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w0);
+        philox4x32_10(jg + 1, qi, static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w1);
+        uint4* dst = reinterpret_cast<uint4*>(dbuf + lane * 32);
+        dst[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+        dst[1] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        __syncwarp();
+        keepbits = 0;
+#pragma unroll
+        for (int c = 0; c < kEwCols; ++c) keepbits |= (dbuf[c * 32 + lane] >= a.drop_t ? 1u : 0u) << c;
+        __syncwarp();  // the buffer is rewritten for the next tile
+      }
       if (!(ok = mbar_wait_warp(bar(K_QFULL + s), (t / L::STAGES) & 1, wc))) break;
       if (!(ok = mbar_wait_warp(bar(K_SFULL), t & 1, wc))) break;
       tc_fence_after();
@@ -354,8 +380,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       }
       {
         uint32_t pk[kEwCols / 2];
+        if constexpr (DROP) {  // dV takes P o Z
+          const float zs = a.drop_scale;
 #pragma unroll
-        for (int c = 0; c < kEwCols; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+          for (int c = 0; c < kEwCols; c += 2)
+            pk[c / 2] = pack2<BF16>(((keepbits >> c) & 1u) ? p[c] * zs : 0.f,
+                                    ((keepbits >> (c + 1)) & 1u) ? p[c + 1] * zs : 0.f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kEwCols; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+        }
         tmem_st_x16(t_s, pk);  // over columns this thread has read
       }
       tmem_st_wait();
@@ -367,6 +401,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       {
         uint32_t dv[kEwCols], dk[kEwCols / 2];
         tmem_ld_x32(t_dp, dv);
+        if constexpr (DROP) {  // dP <- Z o dP
+          const float zs = a.drop_scale;
+#pragma unroll
+          for (int c = 0; c < kEwCols; ++c)
+            dv[c] = __float_as_uint(((keepbits >> c) & 1u) ? __uint_as_float(dv[c]) * zs : 0.f);
+        }
 #pragma unroll
         for (int v = 0; v < kEwCols / 4; ++v) {
           const float4 dd = d4[v];
@@ -451,7 +491,7 @@ enum : int {
   Q_COUNT = 15
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
   using L = DqLayout<D>;
   using T = BwdTiles<D>;
@@ -588,6 +628,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const float dlt = a.delta[w];
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
+      uint32_t keepw[8];  // dropout: 0xFF in byte (c % 4) of word c / 4 if key column c is kept
+      if constexpr (DROP) {
+        const uint32_t jg = static_cast<uint32_t>((j * kTileN + kEwCols * h) / 16);
+        uint32_t w[4];
+        const uint32_t tt = a.drop_t * 0x01010101u;
+        philox4x32_10(jg, static_cast<uint32_t>(grow), static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) keepw[q] = __vcmpgeu4(w[q], tt);
+        philox4x32_10(jg + 1, static_cast<uint32_t>(grow), static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) keepw[4 + q] = __vcmpgeu4(w[q], tt);
+      }
       if (!(ok = mbar_wait_warp(bar(Q_SFULL), j & 1, wc))) break;
       tc_fence_after();
       const int kbeg = j * kTileN + kEwCols * h;
@@ -612,6 +664,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       {
         uint32_t dv[kEwCols], dsp[kEwCols / 2];
         tmem_ld_x32(t_lane + L::TM_DP + kEwCols * h, dv);
+        if constexpr (DROP) {  // dP <- Z o dP
+          const float zs = a.drop_scale;
+#pragma unroll
+          for (int e = 0; e < kEwCols; ++e)
+            dv[e] = __float_as_uint(((keepw[e / 4] >> (8 * (e % 4))) & 1u) ? __uint_as_float(dv[e]) * zs : 0.f);
+        }
 #pragma unroll
         for (int e = 0; e < kEwCols; e += 2)
           dsp[e / 2] = pack2<BF16>(p[e] * (__uint_as_float(dv[e]) - dlt), p[e + 1] * (__uint_as_float(dv[e + 1]) - dlt));
@@ -659,19 +717,20 @@ cudaError_t launch_pre_t(const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP = false>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t st) {
-  auto k = bwd_dkdv_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvLayout<D>::SMEM);
+  auto k = bwd_dkdv_kernel<D, BF16, DROP>;
+  constexpr int smem = DkdvLayout<D>::SMEM + (DROP ? DkdvLayout<D>::DROP_BYTES : 0);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int n_tk = (a.Nk + kTileN - 1) / kTileN;
-  k<<<n_tk * a.BH, kBwdThreads, DkdvLayout<D>::SMEM, st>>>(a);
+  k<<<n_tk * a.BH, kBwdThreads, smem, st>>>(a);
   return cudaGetLastError();
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool DROP = false>
 cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t st) {
-  auto k = bwd_dq_kernel<D, BF16>;
+  auto k = bwd_dq_kernel<D, BF16, DROP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -706,6 +765,18 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_dkdv_t) }
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_dq_t) }
 #undef ATTN_DISPATCH
+
+#define ATTN_DISPATCH_DROP(fn)                                                          \
+  if (d == 128) return bf16 ? fn<128, true, true>(a, s) : fn<128, false, true>(a, s); \
+  return bf16 ? fn<64, true, true>(a, s) : fn<64, false, true>(a, s);
+
+cudaError_t launch_bwd_dkdv_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  ATTN_DISPATCH_DROP(launch_dkdv_t)
+}
+cudaError_t launch_bwd_dq_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  ATTN_DISPATCH_DROP(launch_dq_t)
+}
+#undef ATTN_DISPATCH_DROP
 
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t limit_ns, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(dev_status, limit_ns);

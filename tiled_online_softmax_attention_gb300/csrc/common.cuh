@@ -32,6 +32,10 @@ struct FwdArgs {
   const float* q_scale;                // [B*H][ceil(N/128)]
   const float* k_scale;                // [B*H][ceil(Nk/128)]
   const float* v_scale;
+  // dropout only: keep (bh, i, j) iff its Philox byte >= drop_t; kept ones scaled by drop_scale
+  uint32_t drop_t;
+  uint32_t seed_lo, seed_hi;
+  float drop_scale;                    // 256 / (256 - drop_t)
 };
 
 // Key tiles query tile qt (rows qt*128 .. qt*128+127) has to visit: every key tile when
@@ -61,6 +65,10 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   uint64_t wait_limit_ns;
+  // dropout only, as in FwdArgs
+  uint32_t drop_t;
+  uint32_t seed_lo, seed_hi;
+  float drop_scale;
 };
 
 // Order in which CTAs take work.  Heads go in groups of up to kGroup: within a group
@@ -95,6 +103,9 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_dkdv_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_dq_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);

@@ -106,13 +106,20 @@ enum : int {
 // kind::f8f6f4, the per-tile factor q_scale * k_scale joins the softmax scale, and P~ V8
 // runs on kind::f8f6f4 with P~ in E4M3.  The output stays 16-bit.
 //
+// DROP: dropout on the probabilities ("Understanding FlashAttention, Part 2", section 2.4
+// names it): P(i, j) is kept iff byte j mod 16 of Philox4x32-10 at counter
+// (j / 16, i, bh, 0), keyed by the seed, is >= a.drop_t; the row sum l keeps every
+// probability (dropout follows the softmax) and the epilogue scales O by
+// 256 / (256 - drop_t).
+//
 // SPLIT: the CTA covers one of a.n_splits contiguous ranges of the pair's key tiles and
 // writes its range's normalised partial O (fp32) and logsumexp instead of the output;
 // attn_merge_kernel combines the ranges with the two-block merge of the huaweicloud
 // page's section two.
-template <int D, bool BF16, bool SPLIT, bool FP8>
+template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
   static_assert(!(FP8 && SPLIT) && (!FP8 || D == 128), "E4M3 inputs: d = 128, no split");
+  static_assert(!DROP || (!FP8 && !SPLIT), "dropout: 16-bit inputs, no split");
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -332,6 +339,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           vs_next = a.v_scale[static_cast<size_t>(bh) * n_tk + kv0 + j + 1];
         }
       }
+      // Dropout keep masks of this row's 128 keys, drawn while S is being computed:
+      // keep[g] holds 0xFF in every byte (key 16g + 4q + b in byte b of word q) kept.
+      uint32_t keep[8][4];
+      if constexpr (DROP) {
+        const uint32_t tt = a.drop_t * 0x01010101u;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint32_t w[4];
+          philox4x32_10(static_cast<uint32_t>((kv0 + j) * (kTileN / 16) + g), static_cast<uint32_t>(grow),
+                        static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) keep[g][q] = __vcmpgeu4(w[q], tt);
+        }
+      }
       if (!mbar_wait_warp(bar(B_SFULL + i), j & 1, wc)) { ok = false; break; }
       tc_fence_after();
       float s[128];
@@ -406,6 +427,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           const float p1 = ex2(fmaf(s[c + 1], tsc, -m_use));
           rs += p0 + p1;
           pk[c / 2] = pack2<BF16>(p0, p1);
+          if constexpr (DROP)  // both 16-bit halves: all ones if kept, zero if dropped
+            pk[c / 2] &= __byte_perm(keep[c / 16][(c % 16) / 4], 0u, (c % 4) ? 0x3322u : 0x1100u);
         }
         l = fmaf(l, alpha, rs);
         tmem_st_x64(t_s, pk);
@@ -481,7 +504,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tc_fence_after();
         const float mf = m_s[i * 128 + row];
         const float lf = l_s[i * 128 + row];
-        const float inv_l = 1.f / lf;
+        const float inv_l = (DROP ? a.drop_scale : 1.f) / lf;
         uint8_t* stage = smem + L::OFF_Q + i * L::OTILE;  // Q_i is no longer read
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -522,10 +545,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
 }
 
-template <int D, bool BF16, bool SPLIT, bool FP8 = false>
+template <int D, bool BF16, bool SPLIT, bool FP8 = false, bool DROP = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   using L = FwdLayout<D, FP8>;
-  auto k = fwd_kernel<D, BF16, SPLIT, FP8>;
+  auto k = fwd_kernel<D, BF16, SPLIT, FP8, DROP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -598,6 +621,12 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
   if (d == 128) return bf16 ? launch_split_t<128, true>(a, s) : launch_split_t<128, false>(a, s);
   return bf16 ? launch_split_t<64, true>(a, s) : launch_split_t<64, false>(a, s);
+}
+
+cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 128)
+    return bf16 ? launch_fwd_t<128, true, false, false, true>(a, s) : launch_fwd_t<128, false, false, false, true>(a, s);
+  return bf16 ? launch_fwd_t<64, true, false, false, true>(a, s) : launch_fwd_t<64, false, false, false, true>(a, s);
 }
 
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s) {

@@ -300,6 +300,48 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a0, float a1, float a2, flo
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
+// ---------------------------------------------------------------- dropout random bits
+
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC 2011): ten rounds of multiply-xor on the counter (c0..c3), the key
+// (k0, k1) bumped by the golden-ratio-derived constants after every round.
+__device__ __forceinline__ void philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                              uint32_t k1, uint32_t (&out)[4]) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c0, hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2, hi1 = __umulhi(0xCD9E8D57u, c2);
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+// Keep bits of 16 consecutive keys j0..j0+15 (j0 a multiple of 16) of query i in head bh:
+// bit b set iff byte b of Philox((j0/16, i, bh, 0), seed) (little-endian over the four
+// words) is >= t.
+__device__ __forceinline__ uint32_t dropout_keep16(uint32_t jgroup, uint32_t i, uint32_t bh, uint32_t t,
+                                                   uint32_t seed_lo, uint32_t seed_hi) {
+  uint32_t w[4];
+  philox4x32_10(jgroup, i, bh, 0u, seed_lo, seed_hi, w);
+  const uint32_t tt = t * 0x01010101u;
+  uint32_t bits = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t ge = __vcmpgeu4(w[q], tt);  // 0xFF in every byte >= t
+#pragma unroll
+    for (int b = 0; b < 4; ++b) bits |= ((ge >> (8 * b + 7)) & 1u) << (4 * q + b);
+  }
+  return bits;
+}
+
 // ---------------------------------------------------------------- TMEM loads / stores
 // 32x32b shape: warp w may touch TMEM lanes 32*(w%4) .. 32*(w%4)+31, one lane per thread.
 
