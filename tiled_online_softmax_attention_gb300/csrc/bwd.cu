@@ -464,16 +464,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 //   S(j) | dP(j) | S(j+1) | dQ += dS(j) K_j | dP(j+1) | S(j+2) | ...
 // P = ex2(c S - LSE2) is computed while dP runs, dS = P (dP - D) while the next S
 // runs.
+//
+// K and V stream through separate rings: K(j) is read by S(j) and dQ(j), V(j) only by
+// dP(j), and S(j+1) is issued about when dQ(j-1) frees K's slot.  With one shared
+// two-slot ring every S waited a whole load; three K slots give each K load an
+// iteration of slack, and V's two slots free at dP(j), well ahead of dP(j+2).
 
 template <int D>
 struct DqLayout {
   using T = BwdTiles<D>;
-  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int KST = (D == 128) ? 3 : 4;  // K ring slots
+  static constexpr int VST = (D == 128) ? 2 : 4;  // V ring slots
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = T::TILE;
   static constexpr int OFF_K = 2 * T::TILE;
-  static constexpr int OFF_V = OFF_K + STAGES * T::TILE;
-  static constexpr int OFF_BAR = OFF_V + STAGES * T::TILE;
+  static constexpr int OFF_V = OFF_K + KST * T::TILE;
+  static constexpr int OFF_BAR = OFF_V + VST * T::TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_DS = 384, TM_COLS = 512;
 };
@@ -486,9 +492,11 @@ enum : int {
   Q_DSREADY = 4,  // dS written by every element-wise thread
   Q_DONE = 5,
   Q_DRAIN = 6,
-  Q_KVFULL = 7,   // + stage
-  Q_EMPTY = 11,   // + stage
-  Q_COUNT = 15
+  Q_KFULL = 7,    // + K slot
+  Q_KEMPTY = 11,  // + K slot
+  Q_VFULL = 15,   // + V slot
+  Q_VEMPTY = 19,  // + V slot
+  Q_COUNT = 23
 };
 
 template <int D, bool BF16, bool DROP>
@@ -521,9 +529,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     mbar_init(bar(Q_DSREADY), 128 * kEw);
     mbar_init(bar(Q_DONE), 1);
     mbar_init(bar(Q_DRAIN), 1);
-    for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(bar(Q_KVFULL + s), 1);
-      mbar_init(bar(Q_EMPTY + s), 1);
+    for (int s = 0; s < L::KST; ++s) {
+      mbar_init(bar(Q_KFULL + s), 1);
+      mbar_init(bar(Q_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < L::VST; ++s) {
+      mbar_init(bar(Q_VFULL + s), 1);
+      mbar_init(bar(Q_VEMPTY + s), 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -549,28 +561,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tma_load_3d(sb + L::OFF_Q + kb * T::BLK, &a.tm_q, bar(Q_QFULL), kb * 64, q0, bh);
         tma_load_3d(sb + L::OFF_DO + kb * T::BLK, &a.tm_do, bar(Q_QFULL), kb * 64, q0, bh);
       }
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j % L::STAGES;
-        if (j >= L::STAGES && !mbar_wait(bar(Q_EMPTY + s), ((j / L::STAGES) - 1) & 1, wc)) break;
-        mbar_arrive_expect_tx(bar(Q_KVFULL + s), 2 * T::TILE);
-        for (int kb = 0; kb < T::KB; ++kb) {
-          tma_load_3d(sb + L::OFF_K + s * T::TILE + kb * T::BLK, &a.tm_k, bar(Q_KVFULL + s), kb * 64, j * kTileN, bh);
-          tma_load_3d(sb + L::OFF_V + s * T::TILE + kb * T::BLK, &a.tm_v, bar(Q_KVFULL + s), kb * 64, j * kTileN, bh);
-        }
-        issued = j + 1;
+        // K(j) waits for dQ(j - KST) to free its slot, V(j) for dP(j - VST); in the
+        // tensor core's order dQ(j - 3) precedes dP(j - 2), so neither wait holds up a
+        // load the other could have started.
+        const int ks = j % L::KST;
+        if (j >= L::KST && !mbar_wait(bar(Q_KEMPTY + ks), ((j / L::KST) - 1) & 1, wc)) break;
+        mbar_arrive_expect_tx(bar(Q_KFULL + ks), T::TILE);
+        for (int kb = 0; kb < T::KB; ++kb)
+          tma_load_3d(sb + L::OFF_K + ks * T::TILE + kb * T::BLK, &a.tm_k, bar(Q_KFULL + ks), kb * 64, j * kTileN, bh);
+        k_issued = j + 1;
+        const int vs = j % L::VST;
+        if (j >= L::VST && !mbar_wait(bar(Q_VEMPTY + vs), ((j / L::VST) - 1) & 1, wc)) break;
+        mbar_arrive_expect_tx(bar(Q_VFULL + vs), T::TILE);
+        for (int kb = 0; kb < T::KB; ++kb)
+          tma_load_3d(sb + L::OFF_V + vs * T::TILE + kb * T::BLK, &a.tm_v, bar(Q_VFULL + vs), kb * 64, j * kTileN, bh);
+        v_issued = j + 1;
       }
       mbar_wait(bar(Q_QFULL), 0, wc);
-      for (int j = (issued > L::STAGES ? issued - L::STAGES : 0); j < issued; ++j)
-        mbar_wait(bar(Q_KVFULL + j % L::STAGES), (j / L::STAGES) & 1, wc);
+      for (int j = (k_issued > L::KST ? k_issued - L::KST : 0); j < k_issued; ++j)
+        mbar_wait(bar(Q_KFULL + j % L::KST), (j / L::KST) & 1, wc);
+      for (int j = (v_issued > L::VST ? v_issued - L::VST : 0); j < v_issued; ++j)
+        mbar_wait(bar(Q_VFULL + j % L::VST), (j / L::VST) & 1, wc);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);
       constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);
-      auto kv_full = [&](int j) { return mbar_wait(bar(Q_KVFULL + j % L::STAGES), (j / L::STAGES) & 1, wc); };
+      auto k_full = [&](int j) { return mbar_wait(bar(Q_KFULL + j % L::KST), (j / L::KST) & 1, wc); };
+      auto v_full = [&](int j) { return mbar_wait(bar(Q_VFULL + j % L::VST), (j / L::VST) & 1, wc); };
       auto issue_s = [&](int j) {
-        const uint32_t kbase = sb + L::OFF_K + (j % L::STAGES) * T::TILE;
+        const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
@@ -580,7 +602,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tc_commit(bar(Q_SFULL));
       };
       auto issue_dp = [&](int j) {
-        const uint32_t vbase = sb + L::OFF_V + (j % L::STAGES) * T::TILE;
+        const uint32_t vbase = sb + L::OFF_V + (j % L::VST) * T::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
@@ -588,29 +610,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
                  idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(Q_DPFULL));
+        tc_commit(bar(Q_VEMPTY + j % L::VST));
       };
-      bool ok = mbar_wait(bar(Q_QFULL), 0, wc) && kv_full(0);
+      bool ok = mbar_wait(bar(Q_QFULL), 0, wc) && k_full(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
+        ok = v_full(0);
+      }
+      if (ok) {
+        tc_fence_after();
         issue_dp(0);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         if (j + 1 < n_kv) {
           // The next S may overwrite S(j) once both warpgroups have read it.
-          if (!(ok = kv_full(j + 1) && mbar_wait(bar(Q_SCONS), j & 1, wc))) break;
+          if (!(ok = k_full(j + 1) && mbar_wait(bar(Q_SCONS), j & 1, wc))) break;
           tc_fence_after();
           issue_s(j + 1);
         }
         if (!(ok = mbar_wait(bar(Q_DSREADY), j & 1, wc))) break;
         tc_fence_after();
-        const uint32_t kbase = sb + L::OFF_K + (j % L::STAGES) * T::TILE;
+        const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
 #pragma unroll
         for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of keys 2c, 2c+1 in column c
           mma_ts(tmem + L::TM_DQ, tmem + L::TM_DS + 8 * k,
                  sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g, (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit(bar(Q_EMPTY + j % L::STAGES));
-        if (j + 1 < n_kv) issue_dp(j + 1);  // dP(j) was read before dS(j) was published
+        tc_commit(bar(Q_KEMPTY + j % L::KST));
+        if (j + 1 < n_kv) {  // dP(j) was read before dS(j) was published
+          if (!(ok = v_full(j + 1))) break;
+          tc_fence_after();
+          issue_dp(j + 1);
+        }
       }
       if (ok) tc_commit(bar(Q_DONE));
       tc_commit(bar(Q_DRAIN));
