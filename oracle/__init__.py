@@ -24,6 +24,9 @@ dequant_e4m3(codes, scales, block_rows=128) -> float64 array
     per-block scale factors: huaweicloud page, section four, part 3).
 attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal, scale) -> (o, lse)
     attn_fwd of the dequantised inputs.
+attn_fwd_varlen(q, k, v, cu_q, cu_k, causal, scale) / attn_bwd_varlen(...)
+    packed [tokens, H, d] sequences with offsets cu_q, cu_k: attn_fwd /
+    attn_bwd of every sequence's own slices.
 attn_fwd_dropout / attn_bwd_dropout(..., t, seed)
     the same with dropout on the probabilities: keep iff a Philox4x32-10 byte
     >= t, kept probabilities scaled by 256 / (256 - t) (definition in the C
@@ -323,3 +326,42 @@ def attn_bwd_dropout(q, k, v, dout, causal: bool, scale: float, t: int, seed: in
 
 attn_fwd_dropout.__doc__ = Oracle.attn_fwd_dropout.__doc__
 attn_bwd_dropout.__doc__ = Oracle.attn_bwd_dropout.__doc__
+
+
+def _cu(cu):
+    return [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
+
+
+def attn_fwd_varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float):
+    """Variable-length packed attention: q [Tq, H, d], k, v [Tk, H, d], sequence b owning query
+    tokens cu_q[b] .. cu_q[b+1]-1 and key tokens cu_k[b] .. cu_k[b+1]-1.  Each sequence and head
+    is attn_fwd of its own slices (causal aligned to the sequence's last key).  Returns
+    (o [Tq, H, d], lse [H, Tq])."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    cq, ck = _cu(cu_q), _cu(cu_k)
+    Tq, H, d = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((H, Tq))
+    for b in range(len(cq) - 1):
+        qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+        if cq[b + 1] == cq[b]:
+            continue
+        ob, lb = attn_fwd(q[qs].transpose(1, 0, 2), k[ks].transpose(1, 0, 2), v[ks].transpose(1, 0, 2), causal, scale)
+        o[qs] = ob.transpose(1, 0, 2)
+        lse[:, qs] = lb
+    return o, lse
+
+
+def attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, causal: bool, scale: float):
+    """Gradients of sum(dO * O) for attn_fwd_varlen: (dq [Tq, H, d], dk, dv [Tk, H, d])."""
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    cq, ck = _cu(cu_q), _cu(cu_k)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(len(cq) - 1):
+        qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+        if cq[b + 1] == cq[b] or ck[b + 1] == ck[b]:
+            continue
+        t = lambda x, s_: x[s_].transpose(1, 0, 2)
+        gq, gk, gv = attn_bwd(t(q, qs), t(k, ks), t(v, ks), t(do, qs), causal, scale)
+        dq[qs], dk[ks], dv[ks] = gq.transpose(1, 0, 2), gk.transpose(1, 0, 2), gv.transpose(1, 0, 2)
+    return dq, dk, dv

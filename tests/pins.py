@@ -546,6 +546,34 @@ def pin_dropout_bwd_finite_differences(orc):
             assert err < 1e-6, f"dropout {name} vs finite differences (causal={causal}): {err:.2e}"
 
 
+# ---------------------------------------------------------------------------
+# variable-length packed sequences
+
+
+def pin_varlen_brute_force(orc):
+    """Packed sequences [tokens, H, d] with offsets: brute force per sequence and head with
+    Python floats, including an empty sequence and, with causal, Nk > Nq per sequence."""
+    import oracle as oracle_mod
+
+    rng = np.random.default_rng(38)
+    H, d = 2, 3
+    cu_q, cu_k = [0, 3, 3, 8], [0, 5, 7, 13]
+    q = rng.uniform(-1, 1, (cu_q[-1], H, d))
+    k = rng.uniform(-1, 1, (cu_k[-1], H, d))
+    v = rng.uniform(-2, 2, (cu_k[-1], H, d))
+    for causal in (False, True):
+        o, lse = oracle_mod.attn_fwd_varlen(q, k, v, cu_q, cu_k, causal, 0.8)
+        for b in range(3):
+            for h in range(H):
+                qb = q[cu_q[b]:cu_q[b + 1], h].tolist()
+                if not qb:
+                    continue
+                kb, vb = k[cu_k[b]:cu_k[b + 1], h].tolist(), v[cu_k[b]:cu_k[b + 1], h].tolist()
+                bo, bl = brute_force_fwd(qb, kb, vb, causal, 0.8)
+                _close(o[cu_q[b]:cu_q[b + 1], h], bo, 1e-12, f"varlen O seq {b} head {h} causal={causal}")
+                _close(lse[h, cu_q[b]:cu_q[b + 1]], bl, 1e-12, f"varlen LSE seq {b} head {h}")
+
+
 ALL_PINS = [
     pin_golden_closed_forms, pin_brute_force, pin_rows_sum_to_one, pin_equal_scores,
     pin_merge_rule, pin_online_recurrence, pin_one_hot_large_scores, pin_causal_first_row,
@@ -555,4 +583,5 @@ ALL_PINS = [
     pin_fp8_attention_brute_force, pin_rect_causal_is_a_suffix,
     pin_philox_known_answers, pin_dropout_mask_definition, pin_dropout_rate_and_unbiased,
     pin_dropout_t0_is_plain, pin_dropout_brute_force, pin_dropout_bwd_finite_differences,
+    pin_varlen_brute_force,
 ]
