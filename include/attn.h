@@ -101,6 +101,30 @@ ATTN_API attn_status attn_fwd_rect(const void *q, const void *k, const void *v, 
                           int *dev_status, void *stream);
 
 /*
+ * attn_fwd_varlen / attn_bwd_varlen -- a batch of B sequences of different lengths packed
+ * along the token axis (no padding): q, o, dout, dq are [Tq][H][d], k, v, dk, dv
+ * [Tk][H][d], lse [H][Tq] float32.  cu_q and cu_k are DEVICE int32 arrays of B + 1
+ * token offsets (cu[0] = 0, non-decreasing, cu[B] <= T): sequence b owns query tokens
+ * cu_q[b] .. cu_q[b+1]-1 and key tokens cu_k[b] .. cu_k[b+1]-1, and each sequence and
+ * head is the attention of its own rows (causal as in attn_fwd_rect: aligned to the
+ * sequence's last key).  max_q, max_k bound the lengths (they size the grid); lengths
+ * are clamped to them and to [0, T], so a malformed table cannot make the kernels
+ * write outside the buffers, but its results are unspecified.  A sequence with no key,
+ * or causal with fewer keys than queries, gets O = 0, lse = -inf and zero gradients.
+ * The backward workspace is attn_bwd_workspace_bytes(B, H, max_q, d).  d in {64, 128}.
+ * Everything else is as for attn_fwd / attn_bwd.
+ */
+ATTN_API attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                            const int *cu_q, const int *cu_k, int B, int H, int max_q, int max_k,
+                            int Tq, int Tk, int d, attn_dtype dt, int causal, float scale,
+                            int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                            const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                            void *workspace, size_t workspace_bytes, const int *cu_q, const int *cu_k,
+                            int B, int H, int max_q, int max_k, int Tq, int Tk, int d, attn_dtype dt,
+                            int causal, float scale, int *dev_status, void *stream);
+
+/*
  * attn_fwd_dropout / attn_bwd_dropout -- attn_fwd / attn_bwd with dropout on the
  * attention probabilities (the recomputing backward of "Understanding
  * FlashAttention, Part 2", section 2.4, also covers dropout).  The pages fix no

@@ -11,6 +11,9 @@ current stream):
 
     attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
     attn_fwd_rect(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status=None, stream=None)
+    attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, ...)
+    attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, cu_q, cu_k,
+                    B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, ...)
     attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None, stream=None)
     attn_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
                      B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None, stream=None)
@@ -54,7 +57,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -79,6 +82,10 @@ def load(build_if_missing: bool = True):
     P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     U64 = ctypes.c_uint64
+    lib.attn_fwd_varlen.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, P, P]
+    lib.attn_fwd_varlen.restype = I
+    lib.attn_bwd_varlen.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, P, P, I, I, I, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_varlen.restype = I
     lib.attn_fwd_dropout.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, U64, P, P]
     lib.attn_fwd_dropout.restype = I
     lib.attn_bwd_dropout.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, F, U64, P, P]
@@ -151,6 +158,21 @@ def attn_status_string(status: int) -> str:
 def attn_fwd(q, k, v, o, lse, B, H, N, d, dt, causal, scale, dev_status=None, stream=None) -> int:
     return int(load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(N), int(d),
                                _dt(dt), int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, dev_status=None,
+                    stream=None) -> int:
+    return int(load().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(cu_q), _ptr(cu_k), int(B),
+                                      int(H), int(max_q), int(max_k), int(Tq), int(Tk), int(d), _dt(dt),
+                                      int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, cu_q, cu_k, B, H, max_q, max_k, Tq,
+                    Tk, d, dt, causal, scale, dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                      _ptr(dv), _ptr(workspace), int(workspace_bytes), _ptr(cu_q), _ptr(cu_k), int(B),
+                                      int(H), int(max_q), int(max_k), int(Tq), int(Tk), int(d), _dt(dt),
+                                      int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
 
 
 def attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None,

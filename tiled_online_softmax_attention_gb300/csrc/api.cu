@@ -62,6 +62,21 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16)
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over a packed [T][H][d] 16-bit tensor, dimensions (d, H, T): box {64, 1, 128}
+// puts 128 tokens of one head in shared memory exactly as make_map's box does.
+bool make_map_packed(CUtensorMap* m, const void* base, int H, int T, int d, bool bf16) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTileM)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 3-D map over a [BH][N][d] tensor of E4M3 bytes: box {128, 128, 1} (one 128-byte row
 // block at d = 128), 128-byte swizzle, zero fill past the end.
 bool make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
@@ -205,6 +220,47 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 attn_status attn_fwd_rect(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                           int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
   return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status, stream);
+}
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
+                            const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk, int d,
+                            attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale);
+  if (st != ATTN_OK) return st;
+  if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H * ((max_q + 255) / 256) >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned4(cu_q) ||
+      !aligned4(cu_k))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(Tq) * H * d * 2, kb = static_cast<size_t>(Tk) * H * d * 2;
+  const size_t lb = static_cast<size_t>(H) * Tq * 4, cb = static_cast<size_t>(B + 1) * 4;
+  for (const void* in : {q, k, v, static_cast<const void*>(cu_q), static_cast<const void*>(cu_k)}) {
+    const size_t ib = in == q ? qb : (in == k || in == v) ? kb : cb;
+    if (overlaps(in, ib, o, qb) || overlaps(in, ib, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  }
+  if (overlaps(o, qb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  if ((st = check_device()) != ATTN_OK) return st;
+
+  attn::FwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  if (!make_map_packed(&a.tm_q, q, H, Tq, d, bf16) || !make_map_packed(&a.tm_k, k, H, Tk, d, bf16) ||
+      !make_map_packed(&a.tm_v, v, H, Tk, d, bf16) || !make_map_packed(&a.tm_o, o, H, Tq, d, bf16))
+    return ATTN_ERR_CUDA;
+  a.o = o;
+  a.lse = lse;
+  a.dev_status = dev_status;
+  a.N = max_q;
+  a.Nk = max_k;
+  a.BH = B * H;
+  a.H = H;
+  a.Tq = Tq;
+  a.cu_q = cu_q;
+  a.cu_k = cu_k;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = wait_limit_ns();
+  if (attn::launch_fwd_varlen(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
 }
 
 attn_status attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -490,6 +546,58 @@ attn_status attn_bwd_dropout(const void* q, const void* k, const void* v, const 
   if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
                   dev_status, stream, dr);
+}
+
+attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            const int* cu_q, const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk,
+                            int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale);  // H * tokens * d < 2^31
+  if (st != ATTN_OK) return st;
+  if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
+  const int64_t tiles = static_cast<int64_t>(B) * H * ((max_q > max_k ? max_q : max_k) + kTileM - 1) / kTileM;
+  if (tiles >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;  // grid sizes
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(lse) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || !aligned4(cu_q) ||
+      !aligned4(cu_k))
+    return ATTN_ERR_INVALID_ARG;
+  // the workspace rows are the padded rows of the longest sequence, per (sequence, head)
+  const size_t need = attn_bwd_workspace_bytes(B, H, max_q, d);
+  if (need == 0 || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(Tq) * H * d * 2, kb = static_cast<size_t>(Tk) * H * d * 2;
+  const size_t cb = static_cast<size_t>(B + 1) * 4, lb = static_cast<size_t>(H) * Tq * 4;
+  const Buf ins[] = {{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}, {cu_q, cb}, {cu_k, cb}, {lse, lb}};
+  const Buf outs[] = {{dq, qb}, {dk, kb}, {dv, kb}, {workspace, need}};
+  for (int i = 0; i < 4; ++i) {
+    for (const Buf& in : ins)
+      if (overlaps(in.p, in.bytes, outs[i].p, outs[i].bytes)) return ATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i].p, outs[i].bytes, outs[j].p, outs[j].bytes)) return ATTN_ERR_INVALID_ARG;
+  }
+  if ((st = check_device()) != ATTN_OK) return st;
+
+  attn::BwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  if (!make_map_packed(&a.tm_q, q, H, Tq, d, bf16) || !make_map_packed(&a.tm_k, k, H, Tk, d, bf16) ||
+      !make_map_packed(&a.tm_v, v, H, Tk, d, bf16) || !make_map_packed(&a.tm_do, dout, H, Tq, d, bf16))
+    return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, max_q, max_k, causal, scale, dev_status);
+  a.cofs = 0;  // per sequence, from the offsets
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.H = H;
+  a.Tq = Tq;
+  a.cu_q = cu_q;
+  a.cu_k = cu_k;
+  a.dq_out = dq;
+  a.dk_out = dk;
+  a.dv_out = dv;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess || attn::launch_bwd_dkdv_varlen(a, d, bf16, s) != cudaSuccess ||
+      attn::launch_bwd_dq_varlen(a, d, bf16, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
 }
 
 attn_status attn_bwd_rect(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -72,7 +72,9 @@ __device__ __forceinline__ float dot8(const uint4& x, const uint4& y) {
   return acc;
 }
 
-template <int D, bool BF16>
+// VARLEN: rows (bh, r) of one packed sequence read token tq0 + r of head hh; rows past
+// the sequence, and every row of a degenerate sequence, get LSE2 = +inf and D = 0.
+template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int LPR = D / 8;         // lanes per row
   constexpr int RPW = 32 / LPR;      // rows per warp step
@@ -88,8 +90,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
     ov[u] = dv[u] = make_uint4(0, 0, 0, 0);
     if (rr[u] < rows) {
       const int bh = static_cast<int>(rr[u] / a.Npad), r = static_cast<int>(rr[u] % a.Npad);
-      if (r < a.N) {
-        const size_t off = ((static_cast<size_t>(bh) * a.N + r) * D) * 2 + col * 16;
+      bool valid = r < a.N;
+      size_t off = ((static_cast<size_t>(bh) * a.N + r) * D) * 2 + col * 16;
+      if constexpr (VARLEN) {
+        const SeqView sv = seq_view(a, bh);
+        valid = r < sv.N && !sv.degenerate;
+        off = ((static_cast<size_t>(sv.tq0 + r) * a.H + sv.hh) * D) * 2 + col * 16;
+      }
+      if (valid) {
         ov[u] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.o) + off);
         dv[u] = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(a.dout) + off);
       }
@@ -103,8 +111,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Bw
     if (col == 0 && rr[u] < rows) {
       const int bh = static_cast<int>(rr[u] / a.Npad), r = static_cast<int>(rr[u] % a.Npad);
       const size_t w = static_cast<size_t>(bh) * a.Npad + r;
-      a.delta[w] = (r < a.N) ? dsum : 0.f;
-      a.lse2[w] = (r < a.N) ? a.lse[static_cast<size_t>(bh) * a.N + r] * 1.4426950408889634f : INFINITY;
+      bool valid = r < a.N;
+      size_t li = static_cast<size_t>(bh) * a.N + r;
+      if constexpr (VARLEN) {
+        const SeqView sv = seq_view(a, bh);
+        valid = r < sv.N && !sv.degenerate;
+        li = static_cast<size_t>(sv.hh) * a.Tq + sv.tq0 + r;
+      }
+      a.delta[w] = valid ? dsum : 0.f;
+      a.lse2[w] = valid ? a.lse[li] * 1.4426950408889634f : INFINITY;
     }
   }
 }
@@ -179,8 +194,32 @@ enum : int {
   K_COUNT = 15
 };
 
-template <int D, bool BF16, bool DROP>
+// Write zero rows k0 .. k0+127 (those below n) of a packed [T][H][D] gradient for head hh.
+template <int D>
+__device__ __forceinline__ void zero_rows_packed(void* base, int H, int hh, int t0, int k0, int n) {
+  for (int r = threadIdx.x; r < kTileN; r += blockDim.x) {
+    if (k0 + r >= n) continue;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + ((static_cast<size_t>(t0 + k0 + r) * H + hh) * D) * 2);
+    for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// 32 columns (chunk cc) of this thread's row, scaled, to a packed [T][H][D] tensor row.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row_chunk_packed(void* base, size_t row_elem, int cc, const uint32_t (&v)[32],
+                                                       float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + (row_elem + cc * 32) * 2);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+template <int D, bool BF16, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = DkdvLayout<D>;
   using T = BwdTiles<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -194,15 +233,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_t = (a.N + kTileM - 1) / kTileM;    // query tiles
-  const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles (of the longest sequence)
   const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_tk);
   const int bh = wi.bh;
   const int kt = wi.rank;  // low key tiles see the most queries: they go first
   const int k0 = kt * kTileN;
+  int N = a.N, cofs = a.cofs, hh = 0, tq0 = 0, tk0 = 0, Nk = a.Nk;
+  if constexpr (VARLEN) {
+    const SeqView sv = seq_view(a, bh);
+    N = sv.N, Nk = sv.Nk, cofs = sv.cofs, hh = sv.hh, tq0 = sv.tq0, tk0 = sv.tk0;
+    if (k0 >= Nk) return;  // this key tile lies past the sequence's keys (whole CTA)
+    if (sv.degenerate || N <= 0) {
+      zero_rows_packed<D>(a.dk_out, a.H, hh, tk0, k0, Nk);
+      zero_rows_packed<D>(a.dv_out, a.H, hh, tk0, k0, Nk);
+      return;
+    }
+  }
+  const int n_t = (N + kTileM - 1) / kTileM;  // query tiles
   // Query tiles wholly before the key tile's first key (query i sees key j iff
   // j <= i + cofs) are masked out.
-  const int i_begin = a.causal ? max(0, k0 - a.cofs) / kTileM : 0;
+  const int i_begin = a.causal ? max(0, k0 - cofs) / kTileM : 0;
   const int n_iter = n_t - i_begin;
 
   if (threadIdx.x == 0) {
@@ -239,8 +289,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bar(K_KVFULL), 2 * T::TILE);
       for (int kb = 0; kb < T::KB; ++kb) {
-        tma_load_3d(sb + L::OFF_K + kb * T::BLK, &a.tm_k, bar(K_KVFULL), kb * 64, k0, bh);
-        tma_load_3d(sb + L::OFF_V + kb * T::BLK, &a.tm_v, bar(K_KVFULL), kb * 64, k0, bh);
+        tma_load_3d(sb + L::OFF_K + kb * T::BLK, &a.tm_k, bar(K_KVFULL), kb * 64, VARLEN ? hh : k0,
+                    VARLEN ? tk0 + k0 : bh);
+        tma_load_3d(sb + L::OFF_V + kb * T::BLK, &a.tm_v, bar(K_KVFULL), kb * 64, VARLEN ? hh : k0,
+                    VARLEN ? tk0 + k0 : bh);
       }
       int issued = 0;
       for (int t = 0; t < n_iter; ++t) {
@@ -250,8 +302,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
         const uint32_t st = stage_base(s);
         mbar_arrive_expect_tx(bar(K_QFULL + s), 2 * T::TILE + 1024);
         for (int kb = 0; kb < T::KB; ++kb) {
-          tma_load_3d(st + L::S_Q + kb * T::BLK, &a.tm_q, bar(K_QFULL + s), kb * 64, q0, bh);
-          tma_load_3d(st + L::S_DO + kb * T::BLK, &a.tm_do, bar(K_QFULL + s), kb * 64, q0, bh);
+          tma_load_3d(st + L::S_Q + kb * T::BLK, &a.tm_q, bar(K_QFULL + s), kb * 64, VARLEN ? hh : q0,
+                      VARLEN ? tq0 + q0 : bh);
+          tma_load_3d(st + L::S_DO + kb * T::BLK, &a.tm_do, bar(K_QFULL + s), kb * 64, VARLEN ? hh : q0,
+                      VARLEN ? tq0 + q0 : bh);
         }
         const size_t w = static_cast<size_t>(bh) * a.Npad + q0;
         bulk_load(st + L::S_L, a.lse2 + w, 512, bar(K_QFULL + s));
@@ -358,7 +412,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
           reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D) + (kEwCols / 4) * h;
       // causal: query column c (query qt*128 + 32h + c) sees key k0 + row only if
       // qt*128 + 32h + c + cofs >= k0 + row
-      const int first_visible = a.causal ? k0 + row - a.cofs - qt * kTileM - kEwCols * h : 0;
+      const int first_visible = a.causal ? k0 + row - cofs - qt * kTileM - kEwCols * h : 0;
       float p[kEwCols];
       // Phase 1: P^T for this warpgroup's queries (overlaps the dP^T product).
       {
@@ -435,12 +489,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       for (int cc = (h & 1) * (D / 64); cc < ((h & 1) + 1) * (D / 64); ++cc) {
         uint32_t v[32];
         tmem_ld_x32(t_lane + col + cc * 32, v);
-        stage_row_chunk<D, BF16>(stage, row, cc, v, mul);
+        if constexpr (VARLEN) {  // rows of this sequence only, straight to global memory
+          if (k0 + row < Nk)
+            store_row_chunk_packed<D, BF16>(which == 0 ? a.dv_out : a.dk_out,
+                                            (static_cast<size_t>(tk0 + k0 + row) * a.H + hh) * D, cc, v, mul);
+        } else {
+          stage_row_chunk<D, BF16>(stage, row, cc, v, mul);
+        }
       }
       fence_proxy_async_smem();
     }
     named_bar_sync(1 + which, 256);
-    if ((h & 1) == 0 && (warp & 3) == 0 && lane == 0 && ok && !*abort_flag) {
+    if (!VARLEN && (h & 1) == 0 && (warp & 3) == 0 && lane == 0 && ok && !*abort_flag) {
       const CUtensorMap* m = (which == 0) ? &a.tm_dv : &a.tm_dk;
       for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(m, smem_u32(stage) + kb * T::BLK, kb * 64, k0, bh);
       bulk_commit();
@@ -499,8 +559,9 @@ enum : int {
   Q_COUNT = 23
 };
 
-template <int D, bool BF16, bool DROP>
+template <int D, bool BF16, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = DqLayout<D>;
   using T = BwdTiles<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -519,7 +580,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tiles first
   const int q0 = qt * kTileM;
-  const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
+  int N = a.N, Nk = a.Nk, cofs = a.cofs, hh = 0, tq0 = 0, tk0 = 0;
+  if constexpr (VARLEN) {
+    const SeqView sv = seq_view(a, bh);
+    N = sv.N, Nk = sv.Nk, cofs = sv.cofs, hh = sv.hh, tq0 = sv.tq0, tk0 = sv.tk0;
+    if (q0 >= sv.N) return;  // this query tile lies past the sequence's end (whole CTA)
+    if (sv.degenerate) {
+      zero_rows_packed<D>(a.dq_out, a.H, hh, tq0, q0, sv.N);
+      return;
+    }
+  }
+  const int n_kv = visible_key_tiles(qt, Nk, a.causal, cofs);
 
   if (threadIdx.x == 0) {
     mbar_init(bar(Q_QFULL), 1);
@@ -558,8 +629,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       prefetch_tmap(&a.tm_do);
       mbar_arrive_expect_tx(bar(Q_QFULL), 2 * T::TILE);
       for (int kb = 0; kb < T::KB; ++kb) {
-        tma_load_3d(sb + L::OFF_Q + kb * T::BLK, &a.tm_q, bar(Q_QFULL), kb * 64, q0, bh);
-        tma_load_3d(sb + L::OFF_DO + kb * T::BLK, &a.tm_do, bar(Q_QFULL), kb * 64, q0, bh);
+        tma_load_3d(sb + L::OFF_Q + kb * T::BLK, &a.tm_q, bar(Q_QFULL), kb * 64, VARLEN ? hh : q0,
+                    VARLEN ? tq0 + q0 : bh);
+        tma_load_3d(sb + L::OFF_DO + kb * T::BLK, &a.tm_do, bar(Q_QFULL), kb * 64, VARLEN ? hh : q0,
+                    VARLEN ? tq0 + q0 : bh);
       }
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_kv; ++j) {
@@ -570,13 +643,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         if (j >= L::KST && !mbar_wait(bar(Q_KEMPTY + ks), ((j / L::KST) - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(bar(Q_KFULL + ks), T::TILE);
         for (int kb = 0; kb < T::KB; ++kb)
-          tma_load_3d(sb + L::OFF_K + ks * T::TILE + kb * T::BLK, &a.tm_k, bar(Q_KFULL + ks), kb * 64, j * kTileN, bh);
+          tma_load_3d(sb + L::OFF_K + ks * T::TILE + kb * T::BLK, &a.tm_k, bar(Q_KFULL + ks), kb * 64,
+                      VARLEN ? hh : j * kTileN, VARLEN ? tk0 + j * kTileN : bh);
         k_issued = j + 1;
         const int vs = j % L::VST;
         if (j >= L::VST && !mbar_wait(bar(Q_VEMPTY + vs), ((j / L::VST) - 1) & 1, wc)) break;
         mbar_arrive_expect_tx(bar(Q_VFULL + vs), T::TILE);
         for (int kb = 0; kb < T::KB; ++kb)
-          tma_load_3d(sb + L::OFF_V + vs * T::TILE + kb * T::BLK, &a.tm_v, bar(Q_VFULL + vs), kb * 64, j * kTileN, bh);
+          tma_load_3d(sb + L::OFF_V + vs * T::TILE + kb * T::BLK, &a.tm_v, bar(Q_VFULL + vs), kb * 64,
+                      VARLEN ? hh : j * kTileN, VARLEN ? tk0 + j * kTileN : bh);
         v_issued = j + 1;
       }
       mbar_wait(bar(Q_QFULL), 0, wc);
@@ -674,8 +749,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       if (!(ok = mbar_wait_warp(bar(Q_SFULL), j & 1, wc))) break;
       tc_fence_after();
       const int kbeg = j * kTileN + kEwCols * h;
-      int lim = a.Nk - kbeg;                                   // keys past the end
-      if (a.causal) lim = min(lim, grow + a.cofs - kbeg + 1);  // keys after this query
+      int lim = Nk - kbeg;                                   // keys past the end
+      if (a.causal) lim = min(lim, grow + cofs - kbeg + 1);  // keys after this query
       float p[kEwCols];
       {
         uint32_t sv[kEwCols];
@@ -719,12 +794,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       for (int c32 = h; c32 < D / 32; c32 += kEw) {  // this warpgroup's 32-column chunks
         uint32_t v[32];
         tmem_ld_x32(t_lane + L::TM_DQ + c32 * 32, v);
-        stage_row_chunk<D, BF16>(stage, row, c32, v, a.scale);
+        if constexpr (VARLEN) {  // rows of this sequence only, straight to global memory
+          if (grow < N)
+            store_row_chunk_packed<D, BF16>(a.dq_out, (static_cast<size_t>(tq0 + grow) * a.H + hh) * D, c32, v,
+                                            a.scale);
+        } else {
+          stage_row_chunk<D, BF16>(stage, row, c32, v, a.scale);
+        }
       }
       fence_proxy_async_smem();
     }
     named_bar_sync(1, 128 * kEw);
-    if (warp == 4 && lane == 0 && ok && !*abort_flag) {
+    if (!VARLEN && warp == 4 && lane == 0 && ok && !*abort_flag) {
       for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(&a.tm_dq, sb + L::OFF_Q + kb * T::BLK, kb * 64, q0, bh);
       bulk_commit();
       bulk_wait_read_all();
@@ -739,18 +820,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN = false>
 cudaError_t launch_pre_t(const BwdArgs& a, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(a.BH) * a.Npad;
   const int64_t rows_per_block = (256 / 32) * kPreUnroll * (32 / (D / 8));
   const int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-  bwd_pre_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  bwd_pre_kernel<D, BF16, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool DROP = false>
+template <int D, bool BF16, bool DROP = false, bool VARLEN = false>
 cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t st) {
-  auto k = bwd_dkdv_kernel<D, BF16, DROP>;
+  auto k = bwd_dkdv_kernel<D, BF16, DROP, VARLEN>;
   constexpr int smem = DkdvLayout<D>::SMEM + (DROP ? DkdvLayout<D>::DROP_BYTES : 0);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -759,9 +840,9 @@ cudaError_t launch_dkdv_t(const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <int D, bool BF16, bool DROP = false>
+template <int D, bool BF16, bool DROP = false, bool VARLEN = false>
 cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t st) {
-  auto k = bwd_dq_kernel<D, BF16, DROP>;
+  auto k = bwd_dq_kernel<D, BF16, DROP, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -808,6 +889,19 @@ cudaError_t launch_bwd_dq_dropout(const BwdArgs& a, int d, bool bf16, cudaStream
   ATTN_DISPATCH_DROP(launch_dq_t)
 }
 #undef ATTN_DISPATCH_DROP
+
+cudaError_t launch_bwd_pre_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 128) return bf16 ? launch_pre_t<128, true, true>(a, s) : launch_pre_t<128, false, true>(a, s);
+  return bf16 ? launch_pre_t<64, true, true>(a, s) : launch_pre_t<64, false, true>(a, s);
+}
+cudaError_t launch_bwd_dkdv_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 128) return bf16 ? launch_dkdv_t<128, true, false, true>(a, s) : launch_dkdv_t<128, false, false, true>(a, s);
+  return bf16 ? launch_dkdv_t<64, true, false, true>(a, s) : launch_dkdv_t<64, false, false, true>(a, s);
+}
+cudaError_t launch_bwd_dq_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 128) return bf16 ? launch_dq_t<128, true, false, true>(a, s) : launch_dq_t<128, false, false, true>(a, s);
+  return bf16 ? launch_dq_t<64, true, false, true>(a, s) : launch_dq_t<64, false, false, true>(a, s);
+}
 
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t limit_ns, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(dev_status, limit_ns);

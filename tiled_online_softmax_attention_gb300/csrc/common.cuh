@@ -36,6 +36,13 @@ struct FwdArgs {
   uint32_t drop_t;
   uint32_t seed_lo, seed_hi;
   float drop_scale;                    // 256 / (256 - drop_t)
+  // variable-length packed sequences only: tensors [tokens][H][d] (maps over (d, H, tokens)),
+  // sequence b = bh / H owns query tokens cu_q[b] .. cu_q[b+1]-1 and key tokens
+  // cu_k[b] .. cu_k[b+1]-1; N and Nk are the longest lengths (grid size); lse is [H][Tq]
+  int H;
+  int Tq;
+  const int* cu_q;
+  const int* cu_k;
 };
 
 // Key tiles query tile qt (rows qt*128 .. qt*128+127) has to visit: every key tile when
@@ -69,7 +76,37 @@ struct BwdArgs {
   uint32_t drop_t;
   uint32_t seed_lo, seed_hi;
   float drop_scale;
+  // variable-length packed sequences only, as in FwdArgs (N, Nk: the longest lengths;
+  // Npad: N rounded up; lse [H][Tq]; the workspace keeps [B*H][Npad])
+  int H;
+  int Tq;
+  const int* cu_q;
+  const int* cu_k;
+  void* dq_out;                         // packed gradients, written row by row
+  void* dk_out;
+  void* dv_out;
 };
+
+// One packed sequence as a kernel sees it: lengths clamped to the caller's bounds, the
+// first query and key tokens, the head, and whether it is degenerate (no key, or causal
+// with fewer keys than queries: every row of it gets O = 0, lse = -inf, zero gradients).
+struct SeqView {
+  int N, Nk, cofs, hh, tq0, tk0;
+  bool degenerate;
+};
+template <class Args>
+__device__ __forceinline__ SeqView seq_view(const Args& a, int bh) {
+  const int b = bh / a.H;
+  SeqView v;
+  v.hh = bh % a.H;
+  v.tq0 = min(max(a.cu_q[b], 0), a.Tq);
+  v.tk0 = max(a.cu_k[b], 0);
+  v.N = min(min(max(a.cu_q[b + 1], v.tq0), a.Tq) - v.tq0, a.N);
+  v.Nk = min(max(a.cu_k[b + 1] - v.tk0, 0), a.Nk);
+  v.cofs = a.causal ? v.Nk - v.N : 0;
+  v.degenerate = v.Nk <= 0 || (a.causal && v.Nk < v.N);
+  return v;
+}
 
 // Order in which CTAs take work.  Heads go in groups of up to kGroup: within a group
 // the CTAs walk the tile index (rank 0 first), so the CTAs running at one time
@@ -104,8 +141,12 @@ cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s)
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_varlen(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_pre_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_dkdv_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_dq_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);

@@ -112,14 +112,20 @@ enum : int {
 // probability (dropout follows the softmax) and the epilogue scales O by
 // 256 / (256 - drop_t).
 //
+// VARLEN: variable-length packed sequences ([tokens][H][d] with offsets): the CTA reads
+// its sequence's token range, loads tiles at (column, head, token) coordinates, masks
+// with the sequence's own lengths and writes O rows with plain stores, so that a
+// partial last tile never touches the next sequence's rows.
+//
 // SPLIT: the CTA covers one of a.n_splits contiguous ranges of the pair's key tiles and
 // writes its range's normalised partial O (fp32) and logsumexp instead of the output;
 // attn_merge_kernel combines the ranges with the two-block merge of the huaweicloud
 // page's section two.
-template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP>
+template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP, bool VARLEN>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
   static_assert(!(FP8 && SPLIT) && (!FP8 || D == 128), "E4M3 inputs: d = 128, no split");
   static_assert(!DROP || (!FP8 && !SPLIT), "dropout: 16-bit inputs, no split");
+  static_assert(!VARLEN || (!FP8 && !SPLIT && !DROP), "packed sequences: plain 16-bit forward");
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -143,9 +149,42 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const WorkItem wi = work_item(static_cast<int>(blockIdx.x) / (SPLIT ? a.n_splits : 1), a.BH, n_pairs);
   const int bh = wi.bh;
   const int pr = n_pairs - 1 - wi.rank;  // longest causal pair first
+  // Lengths this CTA works with (one sequence's in VARLEN mode), and where its rows sit:
+  // TMA coordinates (row, head-or-bh) and the first query / key token.
+  int N = a.N, Nk = a.Nk, cofs = a.cofs;
+  int hh = 0, tq0 = 0, tk0 = 0;
+  if constexpr (VARLEN) {
+    // The offsets are the caller's; seq_view clamps them so that a malformed table
+    // cannot send a store outside o or lse.
+    const SeqView sv = seq_view(a, bh);
+    hh = sv.hh;
+    tq0 = sv.tq0;
+    tk0 = sv.tk0;
+    N = sv.N;
+    Nk = sv.Nk;
+    cofs = sv.cofs;
+    if (2 * pr * kTileM >= N) return;  // this pair lies past the sequence's end (whole CTA)
+    if (sv.degenerate) {
+      // No key at all, or causal rows that would see none: O = 0 and lse = -inf for the
+      // pair's rows (documented), without starting the pipeline.
+      for (int r = threadIdx.x; r < 2 * kTileM; r += blockDim.x) {
+        const int gr = 2 * pr * kTileM + r;
+        if (gr >= N) continue;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) + ((static_cast<size_t>(tq0 + gr) * a.H + hh) * D) * 2);
+        for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        a.lse[static_cast<size_t>(hh) * a.Tq + tq0 + gr] = -INFINITY;
+      }
+      return;
+    }
+  }
+  // TMA coordinates of query row r / key row r: (row, bh) or, packed, (head, token)
+  auto qc1 = [&](int r) { return VARLEN ? hh : r; };
+  auto qc2 = [&](int r) { return VARLEN ? tq0 + r : bh; };
+  auto kc1 = [&](int r) { return VARLEN ? hh : r; };
+  auto kc2 = [&](int r) { return VARLEN ? tk0 + r : bh; };
   int n_kv[2];  // key tiles each query tile visits, starting at key tile kv0
 #pragma unroll
-  for (int i = 0; i < 2; ++i) n_kv[i] = visible_key_tiles(2 * pr + i, a.Nk, a.causal, a.cofs);
+  for (int i = 0; i < 2; ++i) n_kv[i] = visible_key_tiles(2 * pr + i, Nk, a.causal, cofs);
   int kv0 = 0;
   if constexpr (SPLIT) {
     // Ranges cut tile 0's visible tiles evenly; tile 1's one extra causal tile joins the
@@ -207,7 +246,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mbar_arrive_expect_tx(bar(B_Q + i), L::TILE);
         for (int kb = 0; kb < L::KB_IN; ++kb)
           tma_load_3d(sb + L::OFF_Q + i * L::OTILE + kb * L::BLK, &a.tm_q, bar(B_Q + i), kb * (128 / L::ELEM),
-                      (2 * pr + i) * kTileM, bh);
+                      qc1((2 * pr + i) * kTileM), qc2((2 * pr + i) * kTileM));
       }
       const int n_loads = 2 * n_kv[1];  // K_j, V_j alternately
       int issued = 0;
@@ -218,7 +257,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         mbar_arrive_expect_tx(bar(B_KVFULL + s), L::TILE);
         for (int kb = 0; kb < L::KB_IN; ++kb)
           tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(B_KVFULL + s), kb * (128 / L::ELEM),
-                      (kv0 + (ld >> 1)) * kTileN, bh);
+                      kc1((kv0 + (ld >> 1)) * kTileN), kc2((kv0 + (ld >> 1)) * kTileN));
         issued = ld + 1;
       }
       // Let every copy this thread started land before the CTA can exit.
@@ -367,11 +406,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       }
       const int k0 = (kv0 + j) * kTileN;
-      const bool tail = k0 + kTileN > a.Nk;
-      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM + a.cofs);
+      const bool tail = k0 + kTileN > Nk;
+      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM + cofs);
       if (tail || diag) {
-        int lim = a.Nk - k0;                                   // keys past the end of the sequence
-        if (a.causal) lim = min(lim, grow + a.cofs - k0 + 1);  // keys after this query
+        int lim = Nk - k0;                                   // keys past the end of the sequence
+        if (a.causal) lim = min(lim, grow + cofs - k0 + 1);  // keys after this query
 #pragma unroll
         for (int c = 0; c < kTileN; ++c)
           if (c >= lim) s[c] = -INFINITY;
@@ -514,21 +553,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pkd[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-          const int kb = (cc * 32) / 64;
+          if constexpr (VARLEN) {  // this row of this sequence, straight to global memory
+            if (q0 + row < N) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) +
+                                                    ((static_cast<size_t>(tq0 + q0 + row) * a.H + hh) * D + cc * 32) * 2);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int ch = ((cc * 32) % 64) / 8 + q;
-            uint4* dst = reinterpret_cast<uint4*>(stage + kb * L::BLK + row * 128 + ((ch ^ (row & 7)) << 4));
-            *dst = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
+              for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
+            }
+          } else {
+            const int kb = (cc * 32) / 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int ch = ((cc * 32) % 64) / 8 + q;
+              uint4* dst = reinterpret_cast<uint4*>(stage + kb * L::BLK + row * 128 + ((ch ^ (row & 7)) << 4));
+              *dst = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
+            }
           }
         }
-        if (q0 + row < a.N)  // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
-          a.lse[static_cast<size_t>(bh) * a.N + q0 + row] = (mf + __log2f(lf)) * 0.69314718055994531f;
+        // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
+        if (q0 + row < N) {
+          const size_t li = VARLEN ? static_cast<size_t>(hh) * a.Tq + tq0 + q0 + row : static_cast<size_t>(bh) * N + q0 + row;
+          a.lse[li] = (mf + __log2f(lf)) * 0.69314718055994531f;
+        }
         fence_proxy_async_smem();
       }
       ok = ok && ok_i;
       named_bar_sync(1, 128);
-      if (!SPLIT && warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < a.N) {
+      if (!SPLIT && !VARLEN && warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < N) {
         for (int kb = 0; kb < L::KB; ++kb)
           tma_store_3d(&a.tm_o, sb + L::OFF_Q + i * L::OTILE + kb * L::BLK, kb * 64, q0, bh);
         bulk_commit();
@@ -545,10 +596,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
 }
 
-template <int D, bool BF16, bool SPLIT, bool FP8 = false, bool DROP = false>
+template <int D, bool BF16, bool SPLIT, bool FP8 = false, bool DROP = false, bool VARLEN = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
   using L = FwdLayout<D, FP8>;
-  auto k = fwd_kernel<D, BF16, SPLIT, FP8, DROP>;
+  auto k = fwd_kernel<D, BF16, SPLIT, FP8, DROP, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, L::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -627,6 +678,14 @@ cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t 
   if (d == 128)
     return bf16 ? launch_fwd_t<128, true, false, false, true>(a, s) : launch_fwd_t<128, false, false, false, true>(a, s);
   return bf16 ? launch_fwd_t<64, true, false, false, true>(a, s) : launch_fwd_t<64, false, false, false, true>(a, s);
+}
+
+cudaError_t launch_fwd_varlen(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 128)
+    return bf16 ? launch_fwd_t<128, true, false, false, false, true>(a, s)
+                : launch_fwd_t<128, false, false, false, false, true>(a, s);
+  return bf16 ? launch_fwd_t<64, true, false, false, false, true>(a, s)
+              : launch_fwd_t<64, false, false, false, false, true>(a, s);
 }
 
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s) {
