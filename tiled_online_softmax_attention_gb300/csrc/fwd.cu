@@ -149,9 +149,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const WorkItem wi = work_item(static_cast<int>(blockIdx.x) / (SPLIT ? a.n_splits : 1), a.BH, n_pairs);
   const int bh = wi.bh;
   const int pr = n_pairs - 1 - wi.rank;  // longest causal pair first
-  // Lengths this CTA works with (one sequence's in VARLEN mode), and where its rows sit:
-  // TMA coordinates (row, head-or-bh) and the first query / key token.
-  int N = a.N, Nk = a.Nk, cofs = a.cofs;
+  // Lengths this CTA works with: one sequence's in VARLEN mode, else the kernel
+  // parameters themselves (read through accessors so that the plain kernel keeps using
+  // the parameters directly; holding them in registers measured 4 % slower).  Plus where
+  // the rows sit: the head and the first query / key token of the sequence.
+  int vN = 0, vNk = 0, vcofs = 0;
   int hh = 0, tq0 = 0, tk0 = 0;
   if constexpr (VARLEN) {
     // The offsets are the caller's; seq_view clamps them so that a malformed table
@@ -160,9 +162,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     hh = sv.hh;
     tq0 = sv.tq0;
     tk0 = sv.tk0;
-    N = sv.N;
-    Nk = sv.Nk;
-    cofs = sv.cofs;
+    vN = sv.N;
+    vNk = sv.Nk;
+    vcofs = sv.cofs;
+    const int N = vN;
     if (2 * pr * kTileM >= N) return;  // this pair lies past the sequence's end (whole CTA)
     if (sv.degenerate) {
       // No key at all, or causal rows that would see none: O = 0 and lse = -inf for the
@@ -177,6 +180,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       return;
     }
   }
+  auto N_ = [&]() -> int {
+    if constexpr (VARLEN) return vN; else return a.N;
+  };
+  auto Nk_ = [&]() -> int {
+    if constexpr (VARLEN) return vNk; else return a.Nk;
+  };
+  auto cofs_ = [&]() -> int {
+    if constexpr (VARLEN) return vcofs; else return a.cofs;
+  };
   // TMA coordinates of query row r / key row r: (row, bh) or, packed, (head, token)
   auto qc1 = [&](int r) { return VARLEN ? hh : r; };
   auto qc2 = [&](int r) { return VARLEN ? tq0 + r : bh; };
@@ -184,7 +196,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   auto kc2 = [&](int r) { return VARLEN ? tk0 + r : bh; };
   int n_kv[2];  // key tiles each query tile visits, starting at key tile kv0
 #pragma unroll
-  for (int i = 0; i < 2; ++i) n_kv[i] = visible_key_tiles(2 * pr + i, Nk, a.causal, cofs);
+  for (int i = 0; i < 2; ++i) n_kv[i] = visible_key_tiles(2 * pr + i, Nk_(), a.causal, cofs_());
   int kv0 = 0;
   if constexpr (SPLIT) {
     // Ranges cut tile 0's visible tiles evenly; tile 1's one extra causal tile joins the
@@ -406,11 +418,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
       }
       const int k0 = (kv0 + j) * kTileN;
-      const bool tail = k0 + kTileN > Nk;
-      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM + cofs);
+      const bool tail = k0 + kTileN > Nk_();
+      const bool diag = a.causal && (k0 + kTileN - 1 > (2 * pr + i) * kTileM + cofs_());
       if (tail || diag) {
-        int lim = Nk - k0;                                   // keys past the end of the sequence
-        if (a.causal) lim = min(lim, grow + cofs - k0 + 1);  // keys after this query
+        int lim = Nk_() - k0;                                   // keys past the end of the sequence
+        if (a.causal) lim = min(lim, grow + cofs_() - k0 + 1);  // keys after this query
 #pragma unroll
         for (int c = 0; c < kTileN; ++c)
           if (c >= lim) s[c] = -INFINITY;
@@ -554,7 +566,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           for (int e = 0; e < 16; ++e)
             pkd[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
           if constexpr (VARLEN) {  // this row of this sequence, straight to global memory
-            if (q0 + row < N) {
+            if (q0 + row < N_()) {
               uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) +
                                                     ((static_cast<size_t>(tq0 + q0 + row) * a.H + hh) * D + cc * 32) * 2);
 #pragma unroll
@@ -571,15 +583,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
         }
         // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
-        if (q0 + row < N) {
-          const size_t li = VARLEN ? static_cast<size_t>(hh) * a.Tq + tq0 + q0 + row : static_cast<size_t>(bh) * N + q0 + row;
+        if (q0 + row < N_()) {
+          const size_t li = VARLEN ? static_cast<size_t>(hh) * a.Tq + tq0 + q0 + row : static_cast<size_t>(bh) * N_() + q0 + row;
           a.lse[li] = (mf + __log2f(lf)) * 0.69314718055994531f;
         }
         fence_proxy_async_smem();
       }
       ok = ok && ok_i;
       named_bar_sync(1, 128);
-      if (!SPLIT && !VARLEN && warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < N) {
+      if (!SPLIT && !VARLEN && warp == 12 && lane == 0 && ok_i && !*abort_flag && q0 < N_()) {
         for (int kb = 0; kb < L::KB; ++kb)
           tma_store_3d(&a.tm_o, sb + L::OFF_Q + i * L::OTILE + kb * L::BLK, kb * 64, q0, bh);
         bulk_commit();
