@@ -35,6 +35,9 @@ current stream):
 
 Convenience wrappers over torch tensors of shape [B, H, N, d]:
 
+    attention(q, k, v, causal=False, scale=None, dropout_p=0.0, seed=0)  -> o
+        (differentiable: a torch.autograd.Function over the forward / backward calls)
+
     forward(q, k, v, causal=False, scale=None)            -> (o, lse)
     forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal=False, scale=None,
                 out_dtype=torch.bfloat16)                 -> (o, lse)
@@ -349,3 +352,77 @@ def backward(q, k, v, o, lse, dout, causal: bool = False, scale=None, dev_status
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------- autograd
+
+
+def _autograd_function():
+    import torch
+
+    class _Attention(torch.autograd.Function):
+        """O = softmax(scale Q K^T) V through attn_fwd / attn_fwd_rect / attn_fwd_dropout,
+        with the matching backward entry point; argument marshalling only."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, dropout_p, seed):
+            q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+            B, H, N, d = q.shape
+            Nk = k.shape[2]
+            o = torch.empty_like(q)
+            lse = torch.empty((B, H, N), device=q.device, dtype=torch.float32)
+            if dropout_p > 0:
+                if Nk != N:
+                    raise ValueError("dropout needs Nq == Nk")
+                st, name = attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale, dropout_p, seed), \
+                    "attn_fwd_dropout"
+            elif Nk != N:
+                st, name = attn_fwd_rect(q, k, v, o, lse, B, H, N, Nk, d, q.dtype, causal, scale), "attn_fwd_rect"
+            else:
+                st, name = attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale), "attn_fwd"
+            if st != ATTN_OK:
+                raise AttnError(st, name)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.args = (causal, scale, dropout_p, seed)
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            causal, scale, dropout_p, seed = ctx.args
+            do = do.contiguous()
+            B, H, N, d = q.shape
+            Nk = k.shape[2]
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            nb = attn_bwd_workspace_bytes(B, H, N, d)
+            ws = torch.empty(max(nb, 16), device=q.device, dtype=torch.uint8)
+            if dropout_p > 0:
+                st, name = attn_bwd_dropout(q, k, v, o, do, lse, dq, dk, dv, ws, ws.numel(), B, H, N, d, q.dtype,
+                                            causal, scale, dropout_p, seed), "attn_bwd_dropout"
+            elif Nk != N:
+                st, name = attn_bwd_rect(q, k, v, o, do, lse, dq, dk, dv, ws, ws.numel(), B, H, N, Nk, d, q.dtype,
+                                         causal, scale), "attn_bwd_rect"
+            else:
+                st, name = attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, ws.numel(), B, H, N, d, q.dtype, causal,
+                                    scale), "attn_bwd"
+            if st != ATTN_OK:
+                raise AttnError(st, name)
+            return dq, dk, dv, None, None, None, None
+
+    return _Attention
+
+
+_ATTN_FN = None
+
+
+def attention(q, k, v, causal: bool = False, scale=None, dropout_p: float = 0.0, seed: int = 0):
+    """Differentiable attention on [B, H, N, d] bf16/fp16 CUDA tensors (k, v may have their
+    own length Nk; dropout needs Nk == Nq): the forward and backward of this library behind a
+    torch.autograd.Function.  Pass a fresh ``seed`` per call when dropout_p > 0."""
+    global _ATTN_FN
+    if _ATTN_FN is None:
+        _ATTN_FN = _autograd_function()
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n)
+    scale = 1.0 / math.sqrt(q.shape[-1]) if scale is None else float(scale)
+    return _ATTN_FN.apply(q, k, v, bool(causal), scale, float(dropout_p), int(seed))
