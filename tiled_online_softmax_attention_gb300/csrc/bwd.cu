@@ -541,7 +541,12 @@ struct DqLayout {
   static constexpr int OFF_V = OFF_K + KST * T::TILE;
   static constexpr int OFF_BAR = OFF_V + VST * T::TILE;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_DS = 384, TM_COLS = 512;
+  // Q and dO are copied into tensor memory once (16-bit pairs) and feed S = Q K^T and
+  // dP = dO V^T from there, so those products read only K or V from shared memory: with
+  // both operands in shared memory a 128 x 128 x 16 product reads 8 KB, 64 cycles of the
+  // SM's 128 B/cycle, and the kernel was bound by shared-memory bandwidth.  dS goes over
+  // the first half of each warpgroup's own dP columns.
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256, TM_Q = 384, TM_DO = 384 + D / 2, TM_COLS = 512;
 };
 
 enum : int {
@@ -556,7 +561,8 @@ enum : int {
   Q_KEMPTY = 11,  // + K slot
   Q_VFULL = 15,   // + V slot
   Q_VEMPTY = 19,  // + V slot
-  Q_COUNT = 23
+  Q_QTM = 23,     // Q and dO copied into tensor memory (all element-wise threads)
+  Q_COUNT = 24
 };
 
 template <int D, bool BF16, bool DROP, bool VARLEN>
@@ -597,6 +603,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     mbar_init(bar(Q_SFULL), 1);
     mbar_init(bar(Q_DPFULL), 1);
     mbar_init(bar(Q_SCONS), 128 * kEw);
+    mbar_init(bar(Q_QTM), 128 * kEw);
     mbar_init(bar(Q_DSREADY), 128 * kEw);
     mbar_init(bar(Q_DONE), 1);
     mbar_init(bar(Q_DRAIN), 1);
@@ -666,28 +673,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
       constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);
       auto k_full = [&](int j) { return mbar_wait(bar(Q_KFULL + j % L::KST), (j / L::KST) & 1, wc); };
       auto v_full = [&](int j) { return mbar_wait(bar(Q_VFULL + j % L::VST), (j / L::VST) & 1, wc); };
-      auto issue_s = [&](int j) {
+      auto issue_s = [&](int j) {  // S = Q K^T, Q from tensor memory (16 elements = 8 columns per step)
         const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_Q + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                 idesc_s, k > 0 ? 1u : 0u);
+          mma_ts(tmem + L::TM_S, tmem + L::TM_Q + 8 * k, sdesc_sw128(kbase + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(Q_SFULL));
       };
-      auto issue_dp = [&](int j) {
+      auto issue_dp = [&](int j) {  // dP = dO V^T, dO from tensor memory
         const uint32_t vbase = sb + L::OFF_V + (j % L::VST) * T::TILE;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_DO + off, 16, 1024), sdesc_sw128(vbase + off, 16, 1024),
-                 idesc_s, k > 0 ? 1u : 0u);
+          mma_ts(tmem + L::TM_DP, tmem + L::TM_DO + 8 * k, sdesc_sw128(vbase + off, 16, 1024), idesc_s,
+                 k > 0 ? 1u : 0u);
         }
         tc_commit(bar(Q_DPFULL));
         tc_commit(bar(Q_VEMPTY + j % L::VST));
       };
-      bool ok = mbar_wait(bar(Q_QFULL), 0, wc) && k_full(0);
+      bool ok = mbar_wait(bar(Q_QTM), 0, wc) && k_full(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -708,8 +714,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tc_fence_after();
         const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
 #pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of keys 2c, 2c+1 in column c
-          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DS + 8 * k,
+        for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of warpgroup w's keys at dP + 32w
+          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DP + kEwCols * (k >> 1) + 8 * (k & 1),
                  sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g, (j > 0 || k > 0) ? 1u : 0u);
         tc_commit(bar(Q_KEMPTY + j % L::KST));
         if (j + 1 < n_kv) {  // dP(j) was read before dS(j) was published
@@ -732,8 +738,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
     const size_t w = static_cast<size_t>(bh) * a.Npad + grow;  // grow < Npad always
     const float lse2 = a.lse2[w];
     const float dlt = a.delta[w];
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    bool ok = mbar_wait_warp(bar(Q_QFULL), 0, wc);
+    if (ok) {
+      // Copy this row's D/4 columns of Q and of dO (warpgroup h's share) from the
+      // 128-byte-swizzled shared tiles into tensor memory.
+      constexpr int CPW = D / kEw;  // columns per warpgroup: 32 (d = 128) or 16 (d = 64)
+      const int c0 = CPW * h;
+      const int kb = c0 / 64, ch0 = (c0 % 64) / 8;
+      uint32_t qv[CPW / 2], ov[CPW / 2];
+#pragma unroll
+      for (int q = 0; q < CPW / 8; ++q) {
+        const int off = kb * T::BLK + row * 128 + (((ch0 + q) ^ (row & 7)) << 4);
+        const uint4 a4 = *reinterpret_cast<const uint4*>(smem + L::OFF_Q + off);
+        const uint4 b4 = *reinterpret_cast<const uint4*>(smem + L::OFF_DO + off);
+        qv[4 * q] = a4.x, qv[4 * q + 1] = a4.y, qv[4 * q + 2] = a4.z, qv[4 * q + 3] = a4.w;
+        ov[4 * q] = b4.x, ov[4 * q + 1] = b4.y, ov[4 * q + 2] = b4.z, ov[4 * q + 3] = b4.w;
+      }
+      if constexpr (CPW == 32) {
+        tmem_st_x16(t_lane + L::TM_Q + CPW / 2 * h, qv);
+        tmem_st_x16(t_lane + L::TM_DO + CPW / 2 * h, ov);
+      } else {
+        tmem_st_x8(t_lane + L::TM_Q + CPW / 2 * h, qv);
+        tmem_st_x8(t_lane + L::TM_DO + CPW / 2 * h, ov);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(Q_QTM));
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
       uint32_t keepw[8];  // dropout: 0xFF in byte (c % 4) of word c / 4 if key column c is kept
       if constexpr (DROP) {
         const uint32_t jg = static_cast<uint32_t>((j * kTileN + kEwCols * h) / 16);
@@ -779,8 +811,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
 #pragma unroll
         for (int e = 0; e < kEwCols; e += 2)
           dsp[e / 2] = pack2<BF16>(p[e] * (__uint_as_float(dv[e]) - dlt), p[e + 1] * (__uint_as_float(dv[e + 1]) - dlt));
-        // dS(j-1) in these columns was read by the dQ product that completed before dP(j).
-        tmem_st_x16(t_lane + L::TM_DS + (kEwCols / 2) * h, dsp);
+        // dS goes over the first half of this warpgroup's dP columns, which this thread
+        // has read; dP(j+1) is issued after dQ(j), the product that reads dS(j).
+        tmem_st_x16(t_lane + L::TM_DP + kEwCols * h, dsp);
       }
       tmem_st_wait();
       tc_fence_before();
