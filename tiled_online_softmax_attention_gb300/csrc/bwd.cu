@@ -519,11 +519,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
 // ------------------------------------------------------------------ bwd_dq
 //
 // Same warp roles; element-wise warpgroup w handles keys 32w..32w+31 of every
-// key tile.  dS has its own tensor-memory columns, so the MMA warp can issue
-// the next tile's S as soon as the element-wise warps have read this one:
+// key tile.  Q and dO sit in tensor memory for the whole loop (copied there once),
+// dS goes over the first half of each warpgroup's dP columns, and S has its own
+// columns, so the MMA warp issues the next tile's S as soon as the element-wise
+// warps have read this one:
 //   S(j) | dP(j) | S(j+1) | dQ += dS(j) K_j | dP(j+1) | S(j+2) | ...
 // P = ex2(c S - LSE2) is computed while dP runs, dS = P (dP - D) while the next S
-// runs.
+// runs; dP(j+1) comes after dQ(j), which reads dS(j) from dP(j)'s columns.
 //
 // K and V stream through separate rings: K(j) is read by S(j) and dQ(j), V(j) only by
 // dP(j), and S(j+1) is issued about when dQ(j-1) frees K's slot.  With one shared
