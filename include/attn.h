@@ -224,6 +224,9 @@ ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *                      16-byte aligned; contents need not be initialised and
  *                      are clobbered.  The caller owns it.
  *   Outputs must not overlap inputs or each other.
+ *   d in {64, 128, 256}.  At d = 256 the gradients come from three kernels (dV and dK,
+ *   one 128-key tile per CTA each, and dQ, one 128-query tile per CTA), each
+ *   streaming its operands in 128-column halves: the same gradients, in more passes.
  */
 ATTN_API attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, void *dq, void *dk, void *dv,
@@ -235,7 +238,7 @@ ATTN_API attn_status attn_bwd(const void *q, const void *k, const void *v, const
  * attn_bwd_rect -- attn_bwd for attn_fwd_rect's shapes: q, o, dout, dq [B][H][Nq][d],
  * k, v, dk, dv [B][H][Nk][d], lse [B][H][Nq]; the workspace is
  * attn_bwd_workspace_bytes(B, H, Nq, d).  Causal masking and Nk >= Nq as in
- * attn_fwd_rect; d in {64, 128}.  Everything else is as for attn_bwd.
+ * attn_fwd_rect; d in {64, 128, 256}.  Everything else is as for attn_bwd.
  */
 ATTN_API attn_status attn_bwd_rect(const void *q, const void *k, const void *v, const void *o,
                           const void *dout, const float *lse, void *dq, void *dk, void *dv,
@@ -253,7 +256,8 @@ ATTN_API attn_status attn_bwd_rect(const void *q, const void *k, const void *v, 
  *   softmax-Jacobian row term of "Understanding FlashAttention, Part 2",
  *   section 2.4, Fig 18) and the logsumexp in base 2, for every row; rows of
  *   the last partial 128-row tile get D = 0 and an infinite logsumexp.
- * attn_bwd_dkdv -- dK and dV, one 128-key tile per CTA (reads the workspace).
+ * attn_bwd_dkdv -- dK and dV, one 128-key tile per CTA (reads the workspace; at
+ *   d = 256 two launches, dV then dK).
  * attn_bwd_dq   -- dQ, one 128-query tile per CTA (reads the workspace).
  */
 ATTN_API attn_status attn_bwd_prepare(const void *o, const void *dout, const float *lse,

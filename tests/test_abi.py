@@ -46,6 +46,7 @@ def test_workspace_size():
     assert attn.attn_bwd_workspace_bytes(1, 1, 1, 64) == 2 * 128 * 4
     assert attn.attn_bwd_workspace_bytes(1, 1, 0, 64) == 0
     assert attn.attn_bwd_workspace_bytes(1, 1, 16, 96) == 0
+    assert attn.attn_bwd_workspace_bytes(1, 2, 300, 256) == 2 * 2 * 384 * 4
 
 
 # fake, aligned, non-overlapping "device" addresses: validation fails before any CUDA call
@@ -92,7 +93,8 @@ def test_fwd_rejects(kw, status):
     (dict(dv=A[2]), attn.ATTN_ERR_INVALID_ARG),              # output aliases an input
     (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),       # workspace aliases an input
     (dict(d=32), attn.ATTN_ERR_UNSUPPORTED),
-    (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),                # the forward alone takes 256
+    (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256, workspace_bytes=16), attn.ATTN_ERR_INVALID_ARG),  # 256 passes the d check
     (dict(scale=-1.0), attn.ATTN_ERR_INVALID_ARG),
 ])
 def test_bwd_rejects(kw, status):
@@ -162,7 +164,8 @@ def test_rect_validates():
         assert attn.attn_fwd_rect(**a2) == st, kw
     ba = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8], workspace=A[9],
               workspace_bytes=1 << 20, B=1, H=2, Nq=256, Nk=512, d=128, dt=0, causal=1, scale=0.088, stream=0)
-    for kw, st in [(dict(Nq=600), attn.ATTN_ERR_INVALID_ARG), (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    for kw, st in [(dict(Nq=600), attn.ATTN_ERR_INVALID_ARG), (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(d=256, workspace_bytes=16), attn.ATTN_ERR_INVALID_ARG),
                    (dict(dk=A[7], dv=A[7] + 512 * 128 * 2), attn.ATTN_ERR_INVALID_ARG),  # dv inside dk's Nk rows
                    (dict(workspace_bytes=16), attn.ATTN_ERR_INVALID_ARG)]:
         a2 = dict(ba)

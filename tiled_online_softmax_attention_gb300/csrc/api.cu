@@ -359,7 +359,7 @@ attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* 
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
   const size_t npad = (static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM;
   return 2 * static_cast<size_t>(B) * H * npad * sizeof(float);
 }
@@ -381,7 +381,7 @@ struct Buf {
 attn_status check_bwd(std::initializer_list<Buf> ins, const float* lse, std::initializer_list<Buf> outs,
                       const void* ws, size_t ws_bytes, bool ws_out, int B, int H, int N, int Nk, int d,
                       attn_dtype dt, float scale, int causal) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale, false, Nk);
+  attn_status st = check_sizes(B, H, N, d, dt, scale, true, Nk);
   if (st != ATTN_OK) return st;
   if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
   for (const Buf& b : ins)
@@ -451,6 +451,7 @@ attn_status prepare_impl(const void* o, const void* dout, const float* lse, void
 attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                       size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
                       int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
+  if (d == 256 && dr.t > 0) return ATTN_ERR_UNSUPPORTED;  // d = 256 kernels have no dropout
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
                              workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
@@ -463,8 +464,10 @@ attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* d
       !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) || !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
     return ATTN_ERR_CUDA;
   fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
-  const cudaError_t e = dr.t > 0 ? attn::launch_bwd_dkdv_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
-                                 : attn::launch_bwd_dkdv(a, d, bf16, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == 256 ? attn::launch_bwd256_dkdv(a, bf16, s)
+                        : dr.t > 0 ? attn::launch_bwd_dkdv_dropout(a, d, bf16, s)
+                                   : attn::launch_bwd_dkdv(a, d, bf16, s);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -472,6 +475,7 @@ attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* d
 attn_status dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                     size_t workspace_bytes, void* dq, int B, int H, int N, int Nk, int d, attn_dtype dt, int causal,
                     float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
+  if (d == 256 && dr.t > 0) return ATTN_ERR_UNSUPPORTED;  // d = 256 kernels have no dropout
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dq, qb}}, workspace,
                              workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
@@ -484,8 +488,10 @@ attn_status dq_impl(const void* q, const void* k, const void* v, const void* dou
       !make_map(&a.tm_dq, dq, BH, N, d, bf16))
     return ATTN_ERR_CUDA;
   fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
-  const cudaError_t e = dr.t > 0 ? attn::launch_bwd_dq_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
-                                 : attn::launch_bwd_dq(a, d, bf16, static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = d == 256 ? attn::launch_bwd256_dq(a, bf16, s)
+                        : dr.t > 0 ? attn::launch_bwd_dq_dropout(a, d, bf16, s)
+                                   : attn::launch_bwd_dq(a, d, bf16, s);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
@@ -494,6 +500,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
                      const Dropout& dr = Dropout{}) {
+  if (d == 256 && dr.t > 0) return ATTN_ERR_UNSUPPORTED;  // d = 256 kernels have no dropout
   if (!lse) return ATTN_ERR_INVALID_ARG;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},

@@ -908,7 +908,10 @@ __global__ void wait_selftest_kernel(int* dev_status, uint64_t limit_ns) {
   if (d == 128) return bf16 ? fn<128, true>(a, s) : fn<128, false>(a, s); \
   return bf16 ? fn<64, true>(a, s) : fn<64, false>(a, s);
 
-cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_pre_t) }
+cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 256) return bf16 ? launch_pre_t<256, true>(a, s) : launch_pre_t<256, false>(a, s);
+  ATTN_DISPATCH(launch_pre_t)
+}
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_dkdv_t) }
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_dq_t) }
 #undef ATTN_DISPATCH
