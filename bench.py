@@ -377,7 +377,7 @@ def long_forward(attn, dev):
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
-    res["d256_forward_B1_H16_N16384_d256"] = d256_forward(attn, dev)
+    res["d256_forward_and_step_B1_H16_N16384"] = d256_side(attn, dev)
     res["dropout_training_step_p0.1"] = dropout_step(attn, dev)
     return res
 
@@ -413,29 +413,44 @@ def dropout_step(attn, dev):
     return out
 
 
-def d256_forward(attn, dev):
-    """Head dimension 256 (one query tile per CTA): B=1, H=16, N=16384, bf16, both masks."""
+def d256_side(attn, dev):
+    """Head dimension 256: B=1, H=16, N=16384, bf16, both masks; the forward alone (one
+    query tile per CTA) and the training step (forward + the three-kernel backward)."""
     B, H, N, d = 1, 16, 16384, 256
-    x = workloads.draw(B, H, N, d, "bf16", seed=13)
-    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-    o = torch.empty_like(q)
+    x = workloads.draw(B, H, N, d, "bf16", seed=13, with_dout=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
     lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
-    out = {}
-    for causal in (False, True):
-        call = lambda: attn.attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, 1.0 / math.sqrt(d))
+    nb = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+    scale = 1.0 / math.sqrt(d)
+
+    def timed(call, reps):
         for _ in range(3):
             call()
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 10
         a.record()
         for _ in range(reps):
             call()
         b.record()
         torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
+        return a.elapsed_time(b) / reps
+
+    out = {}
+    for causal in (False, True):
+        fwd = lambda: attn.attn_fwd(q, k, v, o, lse, B, H, N, d, q.dtype, causal, scale)
+
+        def step():
+            fwd()
+            attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, nb, B, H, N, d, q.dtype, causal, scale)
+        ms = timed(fwd, 10)
+        ms_step = timed(step, 5)
+        ff = workloads.fwd_flops(B, H, N, d, causal)
+        fs = ff + workloads.bwd_flops(B, H, N, d, causal)
         out["causal" if causal else "non_causal"] = {
-            "ms": round(ms, 4), "tflops": round(workloads.fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12, 1)}
+            "ms": round(ms, 4), "tflops": round(ff / (ms * 1e-3) / 1e12, 1),
+            "step_ms": round(ms_step, 4), "step_tflops": round(fs / (ms_step * 1e-3) / 1e12, 1)}
     return out
 
 

@@ -19,6 +19,11 @@
 // needed twice in one step (Q in dK, K in dQ) is fetched twice.  This costs products
 // (16 half-tile units per step against 10 algorithmic) and load traffic, and buys a fit.
 //
+// The MMA warp runs one product ahead of the element-wise warps: the next step's S (or
+// S^T) is issued as soon as the element-wise warps have read the current one into
+// registers, so it overlaps their dS work (dV kernel: S^T is double-buffered in tensor
+// memory and the next S^T overlaps the P^T work).
+//
 // Warp roles as in bwd.cu: warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2-3 idle,
 // four element-wise warpgroups of 32 columns each.  Every wait is bounded.
 #include "common.cuh"
@@ -31,61 +36,102 @@ constexpr int D2 = 256;
 constexpr int kEw2 = 4;
 constexpr int kEwCols2 = 128 / kEw2;
 constexpr int kThreads2 = 128 * (1 + kEw2);
+constexpr int kEwThreads2 = 128 * kEw2;
 constexpr int kBlk = kTileM * 128;        // one 128-row x 64-column block (16 KB)
 constexpr int kTile = kTileM * D2 * 2;    // one 128-row x 256-column tile (64 KB)
 constexpr int kHalf = kTileM * 128 * 2;   // one 128-row x 128-column half (32 KB)
+constexpr int kSmemMax = 232448;          // opt-in shared memory per CTA
+constexpr int kStatusLayout = 3;          // ATTN_ERR_CUDA: the shared-memory window is misaligned
 
-// Barriers (shared by the three kernels; unused ones are simply never waited on).
+// Barriers (shared by the three kernels; unused ones are never waited on).
 enum : int {
   R_STAT = 0,     // stationary tiles loaded
-  R_SFULL = 1,    // S / S^T computed
-  R_DPFULL = 2,   // dP / dP^T computed
-  R_PREADY = 3,   // P^T written (element-wise threads)
-  R_DSREADY = 4,  // dS / dS^T written (element-wise threads)
-  R_DONE = 5,
-  R_DRAIN = 6,
-  R_FULL = 7,     // + ring slot
-  R_EMPTY = 11,   // + ring slot
-  R_COUNT = 15
+  R_SFULL = 1,    // + buffer: S / S^T computed (the dV kernel has two buffers)
+  R_DPFULL = 3,   // dP / dP^T computed
+  R_PREADY = 4,   // + buffer: P^T written (dV kernel)
+  R_SREAD = 6,    // S / S^T read into registers (dK, dQ kernels)
+  R_DSREADY = 7,  // dS / dS^T written
+  R_DONE = 8,
+  R_DRAIN = 9,
+  R_FULL = 10,    // + ring slot (at most 5)
+  R_EMPTY = 15,   // + ring slot
+  R_COUNT = 20
 };
+constexpr int kMaxSlots = R_EMPTY - R_FULL;
 
-template <int NSLOT, int STATIONARY>
+// Shared memory: STATIONARY 64 KB tiles, NSLOT 32 KB ring slots, LBYTES of per-query
+// values staged by the element-wise warps, the barriers.  Dynamic shared memory starts
+// 1024-byte aligned in practice; the slack left below the opt-in limit covers a
+// misaligned start up to SLACK bytes, and a kernel that finds more reports
+// kStatusLayout and returns before touching anything.
+template <int NSLOT, int STATIONARY, int LBYTES>
 struct Layout256 {
-  static constexpr int OFF_ST = 0;                              // STATIONARY 64 KB tiles
-  static constexpr int OFF_RING = STATIONARY * kTile;           // NSLOT halves
-  static constexpr int OFF_L = OFF_RING + NSLOT * kHalf;        // 16 warps x (LSE2[32], D[32])
-  static constexpr int OFF_BAR = OFF_L + 4096;
-  static constexpr int SMEM = OFF_BAR + 256 + 1024;
+  static_assert(NSLOT <= kMaxSlots, "ring slots");
+  static constexpr int OFF_ST = 0;
+  static constexpr int OFF_RING = STATIONARY * kTile;
+  static constexpr int OFF_L = OFF_RING + NSLOT * kHalf;
+  static constexpr int OFF_BAR = OFF_L + LBYTES;
+  static constexpr int NEED = OFF_BAR + 256;
+  static constexpr int SMEM = NEED + 1024 < kSmemMax ? NEED + 1024 : kSmemMax;
+  static constexpr int SLACK = SMEM - NEED;
+  static_assert(SLACK >= 0, "shared memory");
+  static_assert(8 * R_COUNT + 16 <= 256, "barrier area");
   static_assert(NSLOT * kHalf >= kTile, "the epilogue stages a 256-column tile over the ring");
 };
 
-// Common prologue: barriers, TMEM allocation.  Returns the TMEM base address.
-__device__ __forceinline__ uint32_t prologue256(uint32_t bars, int nslot, volatile int* abort_flag,
-                                                uint32_t* tmem_slot, int ew_count) {
-  const int warp = threadIdx.x >> 5;
+// Common CTA state of the three kernels.
+struct Cta {
+  uint8_t* smem;
+  uint32_t sb, bars, tmem;
+  volatile int* abort_flag;
+};
+
+// Aligns the layout, initialises the barriers and allocates all 512 TMEM columns.
+// Returns false (status reported, nothing else done) when the slack does not cover
+// the shared-memory window's misalignment; uniform over the CTA.
+template <class L, int NSLOT>
+__device__ __forceinline__ bool cta_setup(uint8_t* raw, int* dev_status, Cta& c) {
+  const uintptr_t p = reinterpret_cast<uintptr_t>(raw);
+  const uintptr_t al = (p + 1023) & ~static_cast<uintptr_t>(1023);
+  if (al - p > static_cast<uintptr_t>(L::SLACK)) {
+    if (threadIdx.x == 0 && dev_status) atomicExch(dev_status, kStatusLayout);
+    return false;
+  }
+  c.smem = reinterpret_cast<uint8_t*>(al);
+  c.sb = smem_u32(c.smem);
+  c.bars = c.sb + L::OFF_BAR;
+  c.abort_flag = reinterpret_cast<volatile int*>(c.smem + L::OFF_BAR + 8 * R_COUNT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(c.smem + L::OFF_BAR + 8 * R_COUNT + 8);
   if (threadIdx.x == 0) {
-    mbar_init(bars + 8 * R_STAT, 1);
-    mbar_init(bars + 8 * R_SFULL, 1);
-    mbar_init(bars + 8 * R_DPFULL, 1);
-    mbar_init(bars + 8 * R_PREADY, ew_count);
-    mbar_init(bars + 8 * R_DSREADY, ew_count);
-    mbar_init(bars + 8 * R_DONE, 1);
-    mbar_init(bars + 8 * R_DRAIN, 1);
-    for (int s = 0; s < nslot; ++s) {
-      mbar_init(bars + 8 * (R_FULL + s), 1);
-      mbar_init(bars + 8 * (R_EMPTY + s), 1);
+    for (int i = 0; i < R_FULL; ++i) {
+      const bool ew = i == R_PREADY || i == R_PREADY + 1 || i == R_SREAD || i == R_DSREADY;
+      mbar_init(c.bars + 8 * i, ew ? kEwThreads2 : 1);
     }
-    *abort_flag = 0;
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(c.bars + 8 * (R_FULL + s), 1);
+      mbar_init(c.bars + 8 * (R_EMPTY + s), 1);
+    }
+    *c.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 1) {
+  if ((threadIdx.x >> 5) == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  return *tmem_slot;
+  c.tmem = *tmem_slot;
+  return true;
+}
+
+__device__ __forceinline__ void teardown256(uint32_t tmem) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 // Ring of 32 KB half tiles.  Item c sits in slot c % NSLOT; the producer and the MMA
@@ -99,233 +145,274 @@ struct Ring {
   __device__ uint32_t empty(int item) const { return bars + 8 * (R_EMPTY + item % NSLOT); }
 };
 
-// Producer: load column half `half` (columns 128 half .. +127) of the 128-row tile at
-// `row` of head `bh` as the ring's next item, once the item NSLOT earlier has been
-// released.
+// Producer: the two column halves (columns 0..127, 128..255) of the 128-row tile at
+// `row` of head `bh`, as the ring's next two items, each once the item NSLOT earlier
+// has been released.
 template <int NSLOT>
-__device__ __forceinline__ bool load_half(Ring<NSLOT>& r, const CUtensorMap* m, int half, int row, int bh,
+__device__ __forceinline__ bool load_tile(Ring<NSLOT>& r, const CUtensorMap* m, int row, int bh,
                                           const WaitCtl& wc) {
-  const int c = r.c;
-  if (c >= NSLOT && !mbar_wait(r.empty(c), ((c / NSLOT) - 1) & 1, wc)) return false;
-  mbar_arrive_expect_tx(r.full(c), kHalf);
-  for (int b = 0; b < 2; ++b) tma_load_3d(r.slot_addr(c) + b * kBlk, m, r.full(c), 128 * half + 64 * b, row, bh);
-  ++r.c;
+  for (int half = 0; half < 2; ++half) {
+    const int c = r.c;
+    if (c >= NSLOT && !mbar_wait(r.empty(c), ((c / NSLOT) - 1) & 1, wc)) return false;
+    mbar_arrive_expect_tx(r.full(c), kHalf);
+    for (int b = 0; b < 2; ++b) tma_load_3d(r.slot_addr(c) + b * kBlk, m, r.full(c), 128 * half + 64 * b, row, bh);
+    ++r.c;
+  }
   return true;
 }
 
-// Element-wise warps of the key-tile kernels: each stages the 32 per-query values its
-// warpgroup needs (LSE2, and D when `dl` is given) in its own 256-byte slice of shared
-// memory, read back as broadcast float4s.  The lane's own values are fetched before the
-// wait for S^T, so the global load overlaps it.
-struct RowStage {
-  float* w;  // this warp's slice: [0, 32) LSE2, [32, 64) D
-  __device__ void put(float l, float d) {
-    __syncwarp();
-    w[threadIdx.x & 31] = l;
-    w[32 + (threadIdx.x & 31)] = d;
-    __syncwarp();
+// Producer's end: the stationary tiles and the last items have landed (no copy in
+// flight when the CTA exits).
+template <int NSLOT>
+__device__ __forceinline__ void producer_drain(const Ring<NSLOT>& r, uint32_t stat_bar, const WaitCtl& wc) {
+  mbar_wait(stat_bar, 0, wc);
+  for (int c = (r.c > NSLOT ? r.c - NSLOT : 0); c < r.c; ++c) mbar_wait(r.full(c), (c / NSLOT) & 1, wc);
+}
+
+// The MMA warp's side of the ring.
+template <int NSLOT>
+struct RingUse {
+  Ring<NSLOT> r;
+  const WaitCtl* wc;
+  __device__ bool next() { return mbar_wait(r.full(r.c), (r.c / NSLOT) & 1, *wc); }
+  __device__ uint32_t addr() const { return r.slot_addr(r.c); }
+  __device__ void release() {
+    tc_commit(r.empty(r.c));
+    ++r.c;
   }
-  __device__ const float4* lse4() const { return reinterpret_cast<const float4*>(w); }
-  __device__ const float4* d4() const { return reinterpret_cast<const float4*>(w + 32); }
 };
 
-// S^T-style product over d = 256 as two halves: D (+)= A_stat[:, half] B_half^T, both
-// K-major; A is a stationary 4-block tile, B the ring item.
-__device__ __forceinline__ void mma_half_kk(uint32_t d_tmem, uint32_t a_stat, uint32_t b_item, int half,
-                                            uint32_t idesc, bool first) {
+// D = A_stat B^T over d = 256, both K-major: A a stationary 4-block tile, B the next two
+// ring items (its column halves); commits `done` once issued.
+template <int NSLOT>
+__device__ __forceinline__ bool mma_kk256(RingUse<NSLOT>& u, uint32_t d_tmem, uint32_t a_stat, uint32_t idesc,
+                                          uint32_t done) {
+  for (int h = 0; h < 2; ++h) {
+    if (!u.next()) return false;
+    tc_fence_after();
+    const uint32_t b_item = u.addr();
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const int k = 8 * half + kk;
-    const uint32_t aoff = (k >> 2) * kBlk + (k & 3) * 32;
-    const uint32_t boff = (kk >> 2) * kBlk + (kk & 3) * 32;
-    mma_ss(d_tmem, sdesc_sw128(a_stat + aoff, 16, 1024), sdesc_sw128(b_item + boff, 16, 1024), idesc,
-           (first && kk == 0) ? 0u : 1u);
+    for (int kk = 0; kk < 8; ++kk) {
+      const int k = 8 * h + kk;
+      const uint32_t aoff = (k >> 2) * kBlk + (k & 3) * 32;
+      const uint32_t boff = (kk >> 2) * kBlk + (kk & 3) * 32;
+      mma_ss(d_tmem, sdesc_sw128(a_stat + aoff, 16, 1024), sdesc_sw128(b_item + boff, 16, 1024), idesc,
+             (h == 0 && kk == 0) ? 0u : 1u);
+    }
+    u.release();
+  }
+  tc_commit(done);
+  return true;
+}
+
+// acc[:, 128h .. 128h+127] (+)= A_tmem B_h for both halves h: A the 16-bit operand the
+// element-wise warpgroups wrote (warpgroup w: 16 columns at a_tmem + 32w), B the next two
+// ring items (rows = the contraction, MN-major).
+template <int NSLOT>
+__device__ __forceinline__ bool mma_ts256(RingUse<NSLOT>& u, uint32_t acc, uint32_t a_tmem, uint32_t idesc,
+                                          bool first) {
+  for (int h = 0; h < 2; ++h) {
+    if (!u.next()) return false;
+    tc_fence_after();
+    const uint32_t b_item = u.addr();
+#pragma unroll
+    for (int k = 0; k < kTileM / 16; ++k)
+      mma_ts(acc + 128 * h, a_tmem + kEwCols2 * (k >> 1) + 8 * (k & 1), sdesc_sw128(b_item + k * 2048, kBlk, 1024),
+             idesc, (first && k == 0) ? 0u : 1u);
+    u.release();
+  }
+  return true;
+}
+
+// The key-tile kernels' element-wise warps need 32 per-query values (LSE2, D) per
+// warpgroup: each warp stages them in its own 128-byte slice of shared memory (the
+// lane's own value fetched from global memory beforehand) and reads them back as
+// broadcast float4s.
+struct RowStage {
+  float* w;
+  __device__ const float4* put(float x) {
+    __syncwarp();
+    w[threadIdx.x & 31] = x;
+    __syncwarp();
+    return reinterpret_cast<const float4*>(w);
+  }
+};
+
+// P for this thread's 32 columns from S in registers: 2^(s scale log2e - lse2), lse2 one
+// per column (lse4) or one for the row (lse_row, when lse4 is null).
+__device__ __forceinline__ void softmax_cols(const uint32_t (&sv)[kEwCols2], float sl2, const float4* lse4,
+                                             float lse_row, float (&p)[kEwCols2]) {
+  if (lse4) {
+#pragma unroll
+    for (int v = 0; v < kEwCols2 / 4; ++v) {
+      const float4 lv = lse4[v];
+      p[4 * v + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
+      p[4 * v + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
+      p[4 * v + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
+      p[4 * v + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < kEwCols2; ++e) p[e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse_row));
   }
 }
 
-// Gradient product into one 128-column half: D (+)= A_tmem B_half, A the 16-bit P^T /
-// dS^T / dS written by warpgroup w at a_tmem + 32w (16 columns), B MN-major.
-__device__ __forceinline__ void mma_half_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_item, uint32_t idesc,
-                                            bool first) {
+// Zero p[e] for e < lo and for e >= hi (the masked columns).
+__device__ __forceinline__ void mask_cols(float (&p)[kEwCols2], int lo, int hi) {
+  if (lo > 0 || hi < kEwCols2) {
 #pragma unroll
-  for (int k = 0; k < kTileM / 16; ++k)
-    mma_ts(d_tmem, a_tmem + kEwCols2 * (k >> 1) + 8 * (k & 1), sdesc_sw128(b_item + k * 2048, kBlk, 1024), idesc,
-           (first && k == 0) ? 0u : 1u);
+    for (int e = 0; e < kEwCols2; ++e)
+      if (e < lo || e >= hi) p[e] = 0.f;
+  }
 }
 
 // Epilogue: this thread's row of a 256-column fp32 accumulator (its warpgroup's 64
-// columns), scaled, as 16-bit into a 128B-swizzled staging tile; then one thread
-// stores the tile with TMA.
+// columns), scaled, as 16-bit into a 128B-swizzled staging tile over the ring; then one
+// TMA store of the 128 x 256 tile at row `row0` of head `bh`.
 template <bool BF16>
-__device__ __forceinline__ void stage_acc256(uint8_t* stage, uint32_t t_acc, int row, int h, float mul) {
+__device__ __forceinline__ void epilogue256(bool ok, const Cta& c, int off_ring, uint32_t t_acc, int row, int h,
+                                            float mul, uint32_t done_bar, const WaitCtl& wc, const CUtensorMap* m,
+                                            int row0, int bh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* stage = c.smem + off_ring;
+  if (ok) ok = mbar_wait_warp(done_bar, 0, wc);
+  if (ok) {
+    tc_fence_after();
 #pragma unroll 1
-  for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
-    uint32_t v[32];
-    tmem_ld_x32(t_acc + cc * 32, v);
-    uint32_t pk[16];
+    for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
+      uint32_t v[32];
+      tmem_ld_x32(t_acc + cc * 32, v);
+      uint32_t pk[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-    const int kb = (cc * 32) / 64;
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int ch = ((cc * 32) % 64) / 8 + q;
-      uint4* dst = reinterpret_cast<uint4*>(stage + kb * kBlk + row * 128 + ((ch ^ (row & 7)) << 4));
-      *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      for (int q = 0; q < 4; ++q) {
+        const int ch = (cc & 1) * 4 + q;  // 16-byte chunk within the 64-column block cc / 2
+        uint4* dst = reinterpret_cast<uint4*>(stage + (cc >> 1) * kBlk + row * 128 + ((ch ^ (row & 7)) << 4));
+        *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      }
     }
+    fence_proxy_async_smem();
+  }
+  named_bar_sync(1, kEwThreads2);
+  if (warp == 4 && lane == 0 && ok && !*c.abort_flag) {
+    for (int b = 0; b < 4; ++b) tma_store_3d(m, c.sb + off_ring + b * kBlk, 64 * b, row0, bh);
+    bulk_commit();
+    bulk_wait_read_all();
   }
 }
 
 // ------------------------------------------------------------------ dV
-// TMEM: S^T at 0 (P^T over its first columns), dV at 256..511 (halves at 256, 384).
+// TMEM: S^T in two buffers at 0 and 128 (P^T over the first columns of each), dV at
+// 256..511.  MMA order: S^T(0) | S^T(1) dV(0) | S^T(2) dV(1) | ...; ring items
+// Q(0) | Q(1) dO(0) | Q(2) dO(1) | ...
+constexpr int kDvSlots = 5;
+using LayoutDv = Layout256<kDvSlots, 1, 16 * 128>;
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_constant__ BwdArgs a) {
-  constexpr int NSLOT = 4;
-  using L = Layout256<NSLOT, 1>;
+  constexpr int NSLOT = kDvSlots;
+  using L = LayoutDv;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bars = sb + L::OFF_BAR;
-  auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * R_COUNT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * R_COUNT + 8);
+  Cta c;
+  if (!cta_setup<L, NSLOT>(smem_raw, a.dev_status, c)) return;
+  auto bar = [&](int i) -> uint32_t { return c.bars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM, n_tk = (a.Nk + kTileN - 1) / kTileN;
   const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_tk);
   const int bh = wi.bh, k0 = wi.rank * kTileN;
   const int i_begin = a.causal ? max(0, k0 - a.cofs) / kTileM : 0;
   const int n_iter = n_t - i_begin;
-  const uint32_t tmem = prologue256(bars, NSLOT, abort_flag, tmem_slot, 128 * kEw2);
-  const WaitCtl wc{abort_flag, a.dev_status, a.wait_limit_ns};
-  constexpr uint32_t TM_S = 0, TM_DV = 256;
+  const WaitCtl wc{c.abort_flag, a.dev_status, a.wait_limit_ns};
+  constexpr uint32_t TM_DV = 256;
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(bar(R_STAT), kTile);
-    for (int b = 0; b < 4; ++b) tma_load_3d(sb + L::OFF_ST + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, k0, bh);
-    Ring<NSLOT> r{sb + L::OFF_RING, bars};
-    bool ok = true;
-    for (int t = 0; ok && t < n_iter; ++t) {  // per query tile: Q halves, then dO halves
+    for (int b = 0; b < 4; ++b) tma_load_3d(c.sb + L::OFF_ST + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, k0, bh);
+    Ring<NSLOT> r{c.sb + L::OFF_RING, c.bars};
+    bool ok = n_iter <= 0 || load_tile(r, &a.tm_q, i_begin * kTileM, bh, wc);
+    for (int t = 0; ok && t < n_iter; ++t) {
       const int q0 = (i_begin + t) * kTileM;
-      ok = load_half(r, &a.tm_q, 0, q0, bh, wc) && load_half(r, &a.tm_q, 1, q0, bh, wc) &&
-           load_half(r, &a.tm_do, 0, q0, bh, wc) && load_half(r, &a.tm_do, 1, q0, bh, wc);
+      if (t + 1 < n_iter) ok = load_tile(r, &a.tm_q, q0 + kTileM, bh, wc);
+      ok = ok && load_tile(r, &a.tm_do, q0, bh, wc);
     }
-    mbar_wait(bar(R_STAT), 0, wc);
-    for (int c = (r.c > NSLOT ? r.c - NSLOT : 0); c < r.c; ++c) mbar_wait(r.full(c), (c / NSLOT) & 1, wc);
+    producer_drain(r, bar(R_STAT), wc);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);
     constexpr uint32_t idesc_g = idesc_f16(kTileM, 128, BF16, false, true);
-    Ring<NSLOT> r{sb + L::OFF_RING, bars};
-    auto next = [&]() -> bool { return mbar_wait(r.full(r.c), (r.c / NSLOT) & 1, wc); };
-    auto release = [&]() { tc_commit(r.empty(r.c)); ++r.c; };
+    RingUse<NSLOT> u{Ring<NSLOT>{c.sb + L::OFF_RING, c.bars}, &wc};
+    const uint32_t kst = c.sb + L::OFF_ST;
     bool ok = mbar_wait(bar(R_STAT), 0, wc);
-    auto issue_st = [&]() -> bool {  // S^T = K Q^T over both column halves
-      for (int h = 0; h < 2; ++h) {
-        if (!next()) return false;
-        tc_fence_after();
-        mma_half_kk(tmem + TM_S, sb + L::OFF_ST, r.slot_addr(r.c), h, idesc_s, h == 0);
-        release();
-      }
-      tc_commit(bar(R_SFULL));
-      return true;
-    };
-    if (ok && n_iter > 0) ok = issue_st();
+    if (ok && n_iter > 0) ok = mma_kk256(u, c.tmem, kst, idesc_s, bar(R_SFULL));
     for (int t = 0; ok && t < n_iter; ++t) {
-      if (!(ok = mbar_wait(bar(R_PREADY), t & 1, wc))) break;
-      for (int h = 0; ok && h < 2; ++h) {  // dV[:, half] += P^T dO[:, half]
-        if (!(ok = next())) break;
-        tc_fence_after();
-        mma_half_ts(tmem + TM_DV + 128 * h, tmem + TM_S, r.slot_addr(r.c), idesc_g, t == 0);
-        release();
-      }
-      if (ok && t + 1 < n_iter) ok = issue_st();  // overwrites P^T(t) after dV(t) read it
+      const uint32_t buf = 128u * (t & 1);
+      // S^T(t+1) into the other buffer (its P^T(t-1) was read by dV(t-1), issued earlier)
+      if (t + 1 < n_iter && !(ok = mma_kk256(u, c.tmem + (128u - buf), kst, idesc_s, bar(R_SFULL + ((t + 1) & 1)))))
+        break;
+      if (!(ok = mbar_wait(bar(R_PREADY + (t & 1)), (t >> 1) & 1, wc))) break;
+      ok = mma_ts256(u, c.tmem + TM_DV, c.tmem + buf, idesc_g, t == 0);
     }
     if (ok) tc_commit(bar(R_DONE));
     tc_commit(bar(R_DRAIN));
     mbar_wait(bar(R_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1, wq = warp & 3, row = wq * 32 + lane;  // row: key within the tile
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sl2 = a.scale_log2;
-    RowStage rs{reinterpret_cast<float*>(smem + L::OFF_L) + (warp - 4) * 64};
+    RowStage rs{reinterpret_cast<float*>(c.smem + L::OFF_L) + (warp - 4) * 32};
     bool ok = true;
     for (int t = 0; t < n_iter; ++t) {
       const int qt = i_begin + t;
+      const uint32_t col = 128u * (t & 1) + kEwCols2 * h;
       const float my_l = a.lse2[static_cast<size_t>(bh) * a.Npad + qt * kTileM + kEwCols2 * h + lane];
-      if (!(ok = mbar_wait_warp(bar(R_SFULL), t & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(bar(R_SFULL + (t & 1)), (t >> 1) & 1, wc))) break;
       tc_fence_after();
-      rs.put(my_l, 0.f);
-      const float4* l4 = rs.lse4();
-      const int first_visible = a.causal ? k0 + row - a.cofs - qt * kTileM - kEwCols2 * h : 0;
-      uint32_t sv[kEwCols2];
-      tmem_ld_x32(t_lane + TM_S + kEwCols2 * h, sv);
+      const float4* l4 = rs.put(my_l);
       float p[kEwCols2];
-#pragma unroll
-      for (int v = 0; v < kEwCols2 / 4; ++v) {
-        const float4 lv = l4[v];
-        p[4 * v + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
-        p[4 * v + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
-        p[4 * v + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
-        p[4 * v + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
+      {
+        uint32_t sv[kEwCols2];
+        tmem_ld_x32(t_lane + col, sv);
+        softmax_cols(sv, sl2, l4, 0.f, p);
       }
-      if (first_visible > 0) {
-#pragma unroll
-        for (int c = 0; c < kEwCols2; ++c)
-          if (c < first_visible) p[c] = 0.f;
-      }
+      if (a.causal) mask_cols(p, k0 + row - a.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
       uint32_t pk[kEwCols2 / 2];
 #pragma unroll
-      for (int c = 0; c < kEwCols2; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
-      tmem_st_x16(t_lane + TM_S + kEwCols2 * h, pk);  // over columns this thread has read
+      for (int e = 0; e < kEwCols2; e += 2) pk[e / 2] = pack2<BF16>(p[e], p[e + 1]);
+      tmem_st_x16(t_lane + col, pk);  // over columns this thread has read
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(R_PREADY));
+      mbar_arrive(bar(R_PREADY + (t & 1)));
     }
-    if (ok) ok = mbar_wait_warp(bar(R_DONE), 0, wc);
-    if (ok) {
-      tc_fence_after();
-      stage_acc256<BF16>(smem + L::OFF_RING, t_lane + TM_DV, row, h, 1.f);
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1, 128 * kEw2);
-    if (warp == 4 && lane == 0 && ok && !*abort_flag) {
-      for (int b = 0; b < 4; ++b) tma_store_3d(&a.tm_dv, sb + L::OFF_RING + b * kBlk, 64 * b, k0, bh);
-      bulk_commit();
-      bulk_wait_read_all();
-    }
+    epilogue256<BF16>(ok, c, L::OFF_RING, t_lane + TM_DV, row, h, 1.f, bar(R_DONE), wc, &a.tm_dv, k0, bh);
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  teardown256(c.tmem);
 }
 
 // ------------------------------------------------------------------ dK
-// TMEM: S^T at 0, dP^T at 128 (dS^T over its first columns), dK at 256..511.
+// TMEM: S^T at 0, dP^T at 128 (dS^T over its first columns), dK at 256..511.  MMA order:
+// S^T(0) dP^T(0) | S^T(1) dK(0) dP^T(1) | S^T(2) dK(1) dP^T(2) | ...; ring items
+// Q(0) dO(0) | Q(1) Q(0) dO(1) | Q(2) Q(1) dO(2) | ...
+constexpr int kDkSlots = 3;
+using LayoutDk = Layout256<kDkSlots, 2, 16 * 128>;
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_constant__ BwdArgs a) {
-  constexpr int NSLOT = 2;
-  using L = Layout256<NSLOT, 2>;  // K, V stationary
+  constexpr int NSLOT = kDkSlots;
+  using L = LayoutDk;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bars = sb + L::OFF_BAR;
-  auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * R_COUNT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * R_COUNT + 8);
+  Cta c;
+  if (!cta_setup<L, NSLOT>(smem_raw, a.dev_status, c)) return;
+  auto bar = [&](int i) -> uint32_t { return c.bars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM, n_tk = (a.Nk + kTileN - 1) / kTileN;
   const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_tk);
   const int bh = wi.bh, k0 = wi.rank * kTileN;
   const int i_begin = a.causal ? max(0, k0 - a.cofs) / kTileM : 0;
   const int n_iter = n_t - i_begin;
-  const uint32_t tmem = prologue256(bars, NSLOT, abort_flag, tmem_slot, 128 * kEw2);
-  const WaitCtl wc{abort_flag, a.dev_status, a.wait_limit_ns};
+  const WaitCtl wc{c.abort_flag, a.dev_status, a.wait_limit_ns};
   constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DK = 256;
-  const uint32_t st_k = sb + L::OFF_ST, st_v = sb + L::OFF_ST + kTile;
+  const uint32_t st_k = c.sb + L::OFF_ST, st_v = c.sb + L::OFF_ST + kTile;
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(bar(R_STAT), 2 * kTile);
@@ -333,56 +420,44 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       tma_load_3d(st_k + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, k0, bh);
       tma_load_3d(st_v + b * kBlk, &a.tm_v, bar(R_STAT), 64 * b, k0, bh);
     }
-    Ring<NSLOT> r{sb + L::OFF_RING, bars};
-    bool ok = true;
-    for (int t = 0; ok && t < n_iter; ++t) {  // Q halves, dO halves, Q halves again
+    Ring<NSLOT> r{c.sb + L::OFF_RING, c.bars};
+    const int q_first = i_begin * kTileM;
+    bool ok = n_iter <= 0 || (load_tile(r, &a.tm_q, q_first, bh, wc) && load_tile(r, &a.tm_do, q_first, bh, wc));
+    for (int t = 0; ok && t < n_iter; ++t) {
       const int q0 = (i_begin + t) * kTileM;
-      ok = load_half(r, &a.tm_q, 0, q0, bh, wc) && load_half(r, &a.tm_q, 1, q0, bh, wc) && load_half(r, &a.tm_do, 0, q0, bh, wc) &&
-           load_half(r, &a.tm_do, 1, q0, bh, wc) && load_half(r, &a.tm_q, 0, q0, bh, wc) &&
-           load_half(r, &a.tm_q, 1, q0, bh, wc);
+      if (t + 1 < n_iter) ok = load_tile(r, &a.tm_q, q0 + kTileM, bh, wc);
+      ok = ok && load_tile(r, &a.tm_q, q0, bh, wc);
+      if (ok && t + 1 < n_iter) ok = load_tile(r, &a.tm_do, q0 + kTileM, bh, wc);
     }
-    mbar_wait(bar(R_STAT), 0, wc);
-    for (int c = (r.c > NSLOT ? r.c - NSLOT : 0); c < r.c; ++c) mbar_wait(r.full(c), (c / NSLOT) & 1, wc);
+    producer_drain(r, bar(R_STAT), wc);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);
     constexpr uint32_t idesc_g = idesc_f16(kTileM, 128, BF16, false, true);
-    Ring<NSLOT> r{sb + L::OFF_RING, bars};
-    auto next = [&]() -> bool { return mbar_wait(r.full(r.c), (r.c / NSLOT) & 1, wc); };
-    auto release = [&]() { tc_commit(r.empty(r.c)); ++r.c; };
+    RingUse<NSLOT> u{Ring<NSLOT>{c.sb + L::OFF_RING, c.bars}, &wc};
     bool ok = mbar_wait(bar(R_STAT), 0, wc);
+    if (ok && n_iter > 0)
+      ok = mma_kk256(u, c.tmem + TM_S, st_k, idesc_s, bar(R_SFULL)) &&
+           mma_kk256(u, c.tmem + TM_DP, st_v, idesc_s, bar(R_DPFULL));
     for (int t = 0; ok && t < n_iter; ++t) {
-      for (int h = 0; ok && h < 2; ++h) {  // S^T = K Q^T (overwrites S^T(t-1), read before dS^T(t-1))
-        if (!(ok = next())) break;
+      if (t + 1 < n_iter) {  // S^T(t+1) once S^T(t) is in registers
+        if (!(ok = mbar_wait(bar(R_SREAD), t & 1, wc))) break;
         tc_fence_after();
-        mma_half_kk(tmem + TM_S, st_k, r.slot_addr(r.c), h, idesc_s, h == 0);
-        release();
+        if (!(ok = mma_kk256(u, c.tmem + TM_S, st_k, idesc_s, bar(R_SFULL)))) break;
       }
-      if (!ok) break;
-      tc_commit(bar(R_SFULL));
-      for (int h = 0; ok && h < 2; ++h) {  // dP^T = V dO^T (overwrites dS^T(t-1), read by dK(t-1))
-        if (!(ok = next())) break;
-        tc_fence_after();
-        mma_half_kk(tmem + TM_DP, st_v, r.slot_addr(r.c), h, idesc_s, h == 0);
-        release();
-      }
-      if (!ok) break;
-      tc_commit(bar(R_DPFULL));
       if (!(ok = mbar_wait(bar(R_DSREADY), t & 1, wc))) break;
-      for (int h = 0; ok && h < 2; ++h) {  // dK[:, half] += dS^T Q[:, half]
-        if (!(ok = next())) break;
-        tc_fence_after();
-        mma_half_ts(tmem + TM_DK + 128 * h, tmem + TM_DP, r.slot_addr(r.c), idesc_g, t == 0);
-        release();
-      }
+      tc_fence_after();
+      if (!(ok = mma_ts256(u, c.tmem + TM_DK, c.tmem + TM_DP, idesc_g, t == 0))) break;
+      // dP^T(t+1) overwrites dS^T(t) after dK(t), issued above, has read it
+      if (t + 1 < n_iter && !(ok = mma_kk256(u, c.tmem + TM_DP, st_v, idesc_s, bar(R_DPFULL)))) break;
     }
     if (ok) tc_commit(bar(R_DONE));
     tc_commit(bar(R_DRAIN));
     mbar_wait(bar(R_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1, wq = warp & 3, row = wq * 32 + lane;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sl2 = a.scale_log2;
-    RowStage rs{reinterpret_cast<float*>(smem + L::OFF_L) + (warp - 4) * 64};
+    RowStage rs{reinterpret_cast<float*>(c.smem + L::OFF_L) + (warp - 4) * 32};
     bool ok = true;
     for (int t = 0; t < n_iter; ++t) {
       const int qt = i_begin + t;
@@ -390,28 +465,17 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       const float my_l = a.lse2[wrow], my_d = a.delta[wrow];
       if (!(ok = mbar_wait_warp(bar(R_SFULL), t & 1, wc))) break;
       tc_fence_after();
-      rs.put(my_l, my_d);
-      const float4* l4 = rs.lse4();
-      const float4* d4 = rs.d4();
-      const int first_visible = a.causal ? k0 + row - a.cofs - qt * kTileM - kEwCols2 * h : 0;
       float p[kEwCols2];
       {
+        const float4* l4 = rs.put(my_l);
         uint32_t sv[kEwCols2];
         tmem_ld_x32(t_lane + TM_S + kEwCols2 * h, sv);
-#pragma unroll
-        for (int v = 0; v < kEwCols2 / 4; ++v) {
-          const float4 lv = l4[v];
-          p[4 * v + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
-          p[4 * v + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
-          p[4 * v + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
-          p[4 * v + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
-        }
+        tc_fence_before();
+        mbar_arrive(bar(R_SREAD));
+        softmax_cols(sv, sl2, l4, 0.f, p);
       }
-      if (first_visible > 0) {
-#pragma unroll
-        for (int c = 0; c < kEwCols2; ++c)
-          if (c < first_visible) p[c] = 0.f;
-      }
+      if (a.causal) mask_cols(p, k0 + row - a.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
+      const float4* d4 = rs.put(my_d);
       if (!(ok = mbar_wait_warp(bar(R_DPFULL), t & 1, wc))) break;
       tc_fence_after();
       {
@@ -431,50 +495,33 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       tc_fence_before();
       mbar_arrive(bar(R_DSREADY));
     }
-    if (ok) ok = mbar_wait_warp(bar(R_DONE), 0, wc);
-    if (ok) {
-      tc_fence_after();
-      stage_acc256<BF16>(smem + L::OFF_RING, t_lane + TM_DK, row, h, a.scale);
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1, 128 * kEw2);
-    if (warp == 4 && lane == 0 && ok && !*abort_flag) {
-      for (int b = 0; b < 4; ++b) tma_store_3d(&a.tm_dk, sb + L::OFF_RING + b * kBlk, 64 * b, k0, bh);
-      bulk_commit();
-      bulk_wait_read_all();
-    }
+    epilogue256<BF16>(ok, c, L::OFF_RING, t_lane + TM_DK, row, h, a.scale, bar(R_DONE), wc, &a.tm_dk, k0, bh);
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  teardown256(c.tmem);
 }
 
 // ------------------------------------------------------------------ dQ
-// TMEM: S at 0, dP at 128 (dS over its first columns), dQ at 256..511.
+// TMEM: S at 0, dP at 128 (dS over its first columns), dQ at 256..511.  MMA order:
+// S(0) dP(0) | S(1) dQ(0) dP(1) | ...; ring items K(0) V(0) | K(1) K(0) V(1) | ...
+constexpr int kDqSlots = 3;
+using LayoutDq = Layout256<kDqSlots, 2, 0>;
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_constant__ BwdArgs a) {
-  constexpr int NSLOT = 2;
-  using L = Layout256<NSLOT, 2>;  // Q, dO stationary
+  constexpr int NSLOT = kDqSlots;
+  using L = LayoutDq;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  const uint32_t sb = smem_u32(smem);
-  const uint32_t bars = sb + L::OFF_BAR;
-  auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * R_COUNT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * R_COUNT + 8);
+  Cta c;
+  if (!cta_setup<L, NSLOT>(smem_raw, a.dev_status, c)) return;
+  auto bar = [&](int i) -> uint32_t { return c.bars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
   const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_t);
   const int bh = wi.bh, qt = n_t - 1 - wi.rank, q0 = qt * kTileM;
   const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
-  const uint32_t tmem = prologue256(bars, NSLOT, abort_flag, tmem_slot, 128 * kEw2);
-  const WaitCtl wc{abort_flag, a.dev_status, a.wait_limit_ns};
+  const WaitCtl wc{c.abort_flag, a.dev_status, a.wait_limit_ns};
   constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
-  const uint32_t st_q = sb + L::OFF_ST, st_do = sb + L::OFF_ST + kTile;
+  const uint32_t st_q = c.sb + L::OFF_ST, st_do = c.sb + L::OFF_ST + kTile;
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(bar(R_STAT), 2 * kTile);
@@ -482,54 +529,41 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
       tma_load_3d(st_q + b * kBlk, &a.tm_q, bar(R_STAT), 64 * b, q0, bh);
       tma_load_3d(st_do + b * kBlk, &a.tm_do, bar(R_STAT), 64 * b, q0, bh);
     }
-    Ring<NSLOT> r{sb + L::OFF_RING, bars};
-    bool ok = true;
-    for (int j = 0; ok && j < n_kv; ++j) {  // K halves, V halves, K halves again
+    Ring<NSLOT> r{c.sb + L::OFF_RING, c.bars};
+    bool ok = n_kv <= 0 || (load_tile(r, &a.tm_k, 0, bh, wc) && load_tile(r, &a.tm_v, 0, bh, wc));
+    for (int j = 0; ok && j < n_kv; ++j) {
       const int kr = j * kTileN;
-      ok = load_half(r, &a.tm_k, 0, kr, bh, wc) && load_half(r, &a.tm_k, 1, kr, bh, wc) &&
-           load_half(r, &a.tm_v, 0, kr, bh, wc) && load_half(r, &a.tm_v, 1, kr, bh, wc) &&
-           load_half(r, &a.tm_k, 0, kr, bh, wc) && load_half(r, &a.tm_k, 1, kr, bh, wc);
+      if (j + 1 < n_kv) ok = load_tile(r, &a.tm_k, kr + kTileN, bh, wc);
+      ok = ok && load_tile(r, &a.tm_k, kr, bh, wc);
+      if (ok && j + 1 < n_kv) ok = load_tile(r, &a.tm_v, kr + kTileN, bh, wc);
     }
-    mbar_wait(bar(R_STAT), 0, wc);
-    for (int c = (r.c > NSLOT ? r.c - NSLOT : 0); c < r.c; ++c) mbar_wait(r.full(c), (c / NSLOT) & 1, wc);
+    producer_drain(r, bar(R_STAT), wc);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);
     constexpr uint32_t idesc_g = idesc_f16(kTileM, 128, BF16, false, true);
-    Ring<NSLOT> r{sb + L::OFF_RING, bars};
-    auto next = [&]() -> bool { return mbar_wait(r.full(r.c), (r.c / NSLOT) & 1, wc); };
-    auto release = [&]() { tc_commit(r.empty(r.c)); ++r.c; };
+    RingUse<NSLOT> u{Ring<NSLOT>{c.sb + L::OFF_RING, c.bars}, &wc};
     bool ok = mbar_wait(bar(R_STAT), 0, wc);
+    if (ok && n_kv > 0)
+      ok = mma_kk256(u, c.tmem + TM_S, st_q, idesc_s, bar(R_SFULL)) &&
+           mma_kk256(u, c.tmem + TM_DP, st_do, idesc_s, bar(R_DPFULL));
     for (int j = 0; ok && j < n_kv; ++j) {
-      for (int h = 0; ok && h < 2; ++h) {  // S = Q K^T (overwrites S(j-1), read before dS(j-1))
-        if (!(ok = next())) break;
+      if (j + 1 < n_kv) {  // S(j+1) once S(j) is in registers
+        if (!(ok = mbar_wait(bar(R_SREAD), j & 1, wc))) break;
         tc_fence_after();
-        mma_half_kk(tmem + TM_S, st_q, r.slot_addr(r.c), h, idesc_s, h == 0);
-        release();
+        if (!(ok = mma_kk256(u, c.tmem + TM_S, st_q, idesc_s, bar(R_SFULL)))) break;
       }
-      if (!ok) break;
-      tc_commit(bar(R_SFULL));
-      for (int h = 0; ok && h < 2; ++h) {  // dP = dO V^T (overwrites dS(j-1), read by dQ(j-1))
-        if (!(ok = next())) break;
-        tc_fence_after();
-        mma_half_kk(tmem + TM_DP, st_do, r.slot_addr(r.c), h, idesc_s, h == 0);
-        release();
-      }
-      if (!ok) break;
-      tc_commit(bar(R_DPFULL));
       if (!(ok = mbar_wait(bar(R_DSREADY), j & 1, wc))) break;
-      for (int h = 0; ok && h < 2; ++h) {  // dQ[:, half] += dS K[:, half]
-        if (!(ok = next())) break;
-        tc_fence_after();
-        mma_half_ts(tmem + TM_DQ + 128 * h, tmem + TM_DP, r.slot_addr(r.c), idesc_g, j == 0);
-        release();
-      }
+      tc_fence_after();
+      if (!(ok = mma_ts256(u, c.tmem + TM_DQ, c.tmem + TM_DP, idesc_g, j == 0))) break;
+      // dP(j+1) overwrites dS(j) after dQ(j), issued above, has read it
+      if (j + 1 < n_kv && !(ok = mma_kk256(u, c.tmem + TM_DP, st_do, idesc_s, bar(R_DPFULL)))) break;
     }
     if (ok) tc_commit(bar(R_DONE));
     tc_commit(bar(R_DRAIN));
     mbar_wait(bar(R_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1, wq = warp & 3, row = wq * 32 + lane, grow = q0 + row;
-    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float sl2 = a.scale_log2;
     const size_t w = static_cast<size_t>(bh) * a.Npad + grow;  // grow < Npad always
     const float lse2 = a.lse2[w], dlt = a.delta[w];
@@ -537,21 +571,18 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
     for (int j = 0; j < n_kv; ++j) {
       if (!(ok = mbar_wait_warp(bar(R_SFULL), j & 1, wc))) break;
       tc_fence_after();
-      const int kbeg = j * kTileN + kEwCols2 * h;
-      int lim = a.Nk - kbeg;                                     // keys past the end
-      if (a.causal) lim = min(lim, grow + a.cofs - kbeg + 1);  // keys after this query
       float p[kEwCols2];
       {
         uint32_t sv[kEwCols2];
         tmem_ld_x32(t_lane + TM_S + kEwCols2 * h, sv);
-#pragma unroll
-        for (int e = 0; e < kEwCols2; ++e) p[e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
+        tc_fence_before();
+        mbar_arrive(bar(R_SREAD));
+        softmax_cols(sv, sl2, nullptr, lse2, p);
       }
-      if (lim < kEwCols2) {
-#pragma unroll
-        for (int c = 0; c < kEwCols2; ++c)
-          if (c >= lim) p[c] = 0.f;
-      }
+      const int kbeg = j * kTileN + kEwCols2 * h;
+      int lim = a.Nk - kbeg;                                     // keys past the end
+      if (a.causal) lim = min(lim, grow + a.cofs - kbeg + 1);  // keys after this query
+      mask_cols(p, 0, lim);
       if (!(ok = mbar_wait_warp(bar(R_DPFULL), j & 1, wc))) break;
       tc_fence_after();
       {
@@ -566,25 +597,9 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
       tc_fence_before();
       mbar_arrive(bar(R_DSREADY));
     }
-    if (ok) ok = mbar_wait_warp(bar(R_DONE), 0, wc);
-    if (ok) {
-      tc_fence_after();
-      stage_acc256<BF16>(smem + L::OFF_RING, t_lane + TM_DQ, row, h, a.scale);
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1, 128 * kEw2);
-    if (warp == 4 && lane == 0 && ok && !*abort_flag) {
-      for (int b = 0; b < 4; ++b) tma_store_3d(&a.tm_dq, sb + L::OFF_RING + b * kBlk, 64 * b, q0, bh);
-      bulk_commit();
-      bulk_wait_read_all();
-    }
+    epilogue256<BF16>(ok, c, L::OFF_RING, t_lane + TM_DQ, row, h, a.scale, bar(R_DONE), wc, &a.tm_dq, q0, bh);
   }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
+  teardown256(c.tmem);
 }
 
 template <class K>
@@ -599,17 +614,17 @@ cudaError_t launch256(K k, int smem, int grid, const BwdArgs& a, cudaStream_t st
 
 cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s) {
   const int grid = (a.Nk + kTileN - 1) / kTileN * a.BH;
-  cudaError_t e = bf16 ? launch256(bwd256_dv_kernel<true>, Layout256<4, 1>::SMEM, grid, a, s)
-                       : launch256(bwd256_dv_kernel<false>, Layout256<4, 1>::SMEM, grid, a, s);
+  cudaError_t e = bf16 ? launch256(bwd256_dv_kernel<true>, LayoutDv::SMEM, grid, a, s)
+                       : launch256(bwd256_dv_kernel<false>, LayoutDv::SMEM, grid, a, s);
   if (e != cudaSuccess) return e;
-  return bf16 ? launch256(bwd256_dk_kernel<true>, Layout256<2, 2>::SMEM, grid, a, s)
-              : launch256(bwd256_dk_kernel<false>, Layout256<2, 2>::SMEM, grid, a, s);
+  return bf16 ? launch256(bwd256_dk_kernel<true>, LayoutDk::SMEM, grid, a, s)
+              : launch256(bwd256_dk_kernel<false>, LayoutDk::SMEM, grid, a, s);
 }
 
 cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s) {
   const int grid = (a.N + kTileM - 1) / kTileM * a.BH;
-  return bf16 ? launch256(bwd256_dq_kernel<true>, Layout256<2, 2>::SMEM, grid, a, s)
-              : launch256(bwd256_dq_kernel<false>, Layout256<2, 2>::SMEM, grid, a, s);
+  return bf16 ? launch256(bwd256_dq_kernel<true>, LayoutDq::SMEM, grid, a, s)
+              : launch256(bwd256_dq_kernel<false>, LayoutDq::SMEM, grid, a, s);
 }
 
 }  // namespace attn
