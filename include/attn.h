@@ -41,7 +41,10 @@
  *  - dev_status (nullable) is a device int the caller zeroes; a kernel whose
  *    bounded wait on an mbarrier expires (a hardware or library fault, never
  *    a normal outcome) stores ATTN_ERR_TIMEOUT there, abandons its tile and
- *    exits cleanly.  Read it after synchronising the stream.
+ *    exits cleanly.  Read it after synchronising the stream.  (The d = 256
+ *    backward kernels also store ATTN_ERR_CUDA there, and do nothing, if
+ *    their dynamic shared memory does not start within 768 bytes of a
+ *    1024-byte boundary; it starts on one on current drivers.)
  *  - On any error the output buffers' contents are unspecified.
  */
 #ifndef ATTN_GB300_H
