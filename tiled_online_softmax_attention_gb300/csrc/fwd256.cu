@@ -247,14 +247,26 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       }
       m = m_new;
       const float m_use = (m == -INFINITY) ? 0.f : m;  // a row with nothing visible yet
-      float rs = 0.f;
+      // Paired f32x2 arithmetic for the exponent arguments and the row sum (fewer
+      // issue slots for the softmax warps; see the d <= 128 forward).
       uint32_t pk[64];
+      const uint64_t sl2x2 = f32x2_pack(sl2, sl2), negm2 = f32x2_pack(-m_use, -m_use);
+      uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
       for (int cc = 0; cc < kTileN; cc += 2) {
-        const float p0 = ex2(fmaf(s[cc], sl2, -m_use));
-        const float p1 = ex2(fmaf(s[cc + 1], sl2, -m_use));
-        rs += p0 + p1;
+        float x0, x1;
+        f32x2_unpack(f32x2_fma(f32x2_pack(s[cc], s[cc + 1]), sl2x2, negm2), x0, x1);
+        const float p0 = ex2(x0);
+        const float p1 = ex2(x1);
+        acc2[(cc / 2) & 1] = f32x2_add(acc2[(cc / 2) & 1], f32x2_pack(p0, p1));
         pk[cc / 2] = pack2<BF16>(p0, p1);
+      }
+      float rs;
+      {
+        float a0, a1, b0, b1;
+        f32x2_unpack(acc2[0], a0, a1);
+        f32x2_unpack(acc2[1], b0, b1);
+        rs = (a0 + a1) + (b0 + b1);
       }
       l = fmaf(l, alpha, rs);
       tmem_st_x64(t_lane + 128u * buf, pk);
