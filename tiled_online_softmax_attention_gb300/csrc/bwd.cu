@@ -416,15 +416,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
       float p[kEwCols];
       // Phase 1: P^T for this warpgroup's queries (overlaps the dP^T product).
       {
+        // p = 2^(s sl2 - lse2) as 2^-(lse2 - s sl2): one paired fma per two columns, and
+        // bit-identical to the scalar form (round-to-nearest is symmetric under negation).
         uint32_t sv[kEwCols];
         tmem_ld_x32(t_s, sv);
+        const uint64_t nsl2 = f32x2_pack(-sl2, -sl2);
 #pragma unroll
         for (int v = 0; v < kEwCols / 4; ++v) {
           const float4 lv = l4[v];
-          p[4 * v + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
-          p[4 * v + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
-          p[4 * v + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
-          p[4 * v + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
+          float x0, x1, x2, x3;
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v]), __uint_as_float(sv[4 * v + 1])), nsl2,
+                                 f32x2_pack(lv.x, lv.y)), x0, x1);
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v + 2]), __uint_as_float(sv[4 * v + 3])), nsl2,
+                                 f32x2_pack(lv.z, lv.w)), x2, x3);
+          p[4 * v + 0] = ex2(-x0);
+          p[4 * v + 1] = ex2(-x1);
+          p[4 * v + 2] = ex2(-x2);
+          p[4 * v + 3] = ex2(-x3);
         }
       }
       if (first_visible > 0) {
@@ -462,12 +470,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
             dv[c] = __float_as_uint(((keepbits >> c) & 1u) ? __uint_as_float(dv[c]) * zs : 0.f);
         }
 #pragma unroll
-        for (int v = 0; v < kEwCols / 4; ++v) {
+        for (int v = 0; v < kEwCols / 4; ++v) {  // paired sub and mul, two columns each
           const float4 dd = d4[v];
-          dk[2 * v] = pack2<BF16>(p[4 * v] * (__uint_as_float(dv[4 * v]) - dd.x),
-                                  p[4 * v + 1] * (__uint_as_float(dv[4 * v + 1]) - dd.y));
-          dk[2 * v + 1] = pack2<BF16>(p[4 * v + 2] * (__uint_as_float(dv[4 * v + 2]) - dd.z),
-                                      p[4 * v + 3] * (__uint_as_float(dv[4 * v + 3]) - dd.w));
+          float a0, a1, b0, b1;
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[4 * v], p[4 * v + 1]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[4 * v]), __uint_as_float(dv[4 * v + 1])),
+                                           f32x2_pack(dd.x, dd.y))), a0, a1);
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[4 * v + 2], p[4 * v + 3]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[4 * v + 2]), __uint_as_float(dv[4 * v + 3])),
+                                           f32x2_pack(dd.z, dd.w))), b0, b1);
+          dk[2 * v] = pack2<BF16>(a0, a1);
+          dk[2 * v + 1] = pack2<BF16>(b0, b1);
         }
         tmem_st_x16(t_dp, dk);
       }
@@ -791,8 +804,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
         tmem_ld_x32(t_lane + L::TM_S + kEwCols * h, sv);
         tc_fence_before();
         mbar_arrive(bar(Q_SCONS));
+        const uint64_t sl2x2 = f32x2_pack(sl2, sl2), nl2 = f32x2_pack(-lse2, -lse2);
 #pragma unroll
-        for (int e = 0; e < kEwCols; ++e) p[e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2));
+        for (int e = 0; e < kEwCols; e += 2) {  // one paired fma per two columns
+          float x0, x1;
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl2), x0, x1);
+          p[e] = ex2(x0);
+          p[e + 1] = ex2(x1);
+        }
       }
       if (lim < kEwCols) {
 #pragma unroll
@@ -810,9 +829,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
           for (int e = 0; e < kEwCols; ++e)
             dv[e] = __float_as_uint(((keepw[e / 4] >> (8 * (e % 4))) & 1u) ? __uint_as_float(dv[e]) * zs : 0.f);
         }
+        const uint64_t dlt2 = f32x2_pack(dlt, dlt);
 #pragma unroll
-        for (int e = 0; e < kEwCols; e += 2)
-          dsp[e / 2] = pack2<BF16>(p[e] * (__uint_as_float(dv[e]) - dlt), p[e + 1] * (__uint_as_float(dv[e + 1]) - dlt));
+        for (int e = 0; e < kEwCols; e += 2) {  // paired sub and mul
+          float a0, a1;
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[e], p[e + 1]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), dlt2)),
+                       a0, a1);
+          dsp[e / 2] = pack2<BF16>(a0, a1);
+        }
         // dS goes over the first half of this warpgroup's dP columns, which this thread
         // has read; dP(j+1) is issued after dQ(j), the product that reads dS(j).
         tmem_st_x16(t_lane + L::TM_DP + kEwCols * h, dsp);

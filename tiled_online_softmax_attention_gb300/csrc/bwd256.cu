@@ -242,18 +242,32 @@ struct RowStage {
 // per column (lse4) or one for the row (lse_row, when lse4 is null).
 __device__ __forceinline__ void softmax_cols(const uint32_t (&sv)[kEwCols2], float sl2, const float4* lse4,
                                              float lse_row, float (&p)[kEwCols2]) {
+  // Paired fma per two columns; per column lse2 as 2^-(lse2 - s sl2), bit-identical to
+  // the scalar form since round-to-nearest is symmetric under negation.
   if (lse4) {
+    const uint64_t nsl2 = f32x2_pack(-sl2, -sl2);
 #pragma unroll
     for (int v = 0; v < kEwCols2 / 4; ++v) {
       const float4 lv = lse4[v];
-      p[4 * v + 0] = ex2(fmaf(__uint_as_float(sv[4 * v + 0]), sl2, -lv.x));
-      p[4 * v + 1] = ex2(fmaf(__uint_as_float(sv[4 * v + 1]), sl2, -lv.y));
-      p[4 * v + 2] = ex2(fmaf(__uint_as_float(sv[4 * v + 2]), sl2, -lv.z));
-      p[4 * v + 3] = ex2(fmaf(__uint_as_float(sv[4 * v + 3]), sl2, -lv.w));
+      float x0, x1, x2, x3;
+      f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v]), __uint_as_float(sv[4 * v + 1])), nsl2,
+                             f32x2_pack(lv.x, lv.y)), x0, x1);
+      f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v + 2]), __uint_as_float(sv[4 * v + 3])), nsl2,
+                             f32x2_pack(lv.z, lv.w)), x2, x3);
+      p[4 * v + 0] = ex2(-x0);
+      p[4 * v + 1] = ex2(-x1);
+      p[4 * v + 2] = ex2(-x2);
+      p[4 * v + 3] = ex2(-x3);
     }
   } else {
+    const uint64_t sl2x2 = f32x2_pack(sl2, sl2), nl2 = f32x2_pack(-lse_row, -lse_row);
 #pragma unroll
-    for (int e = 0; e < kEwCols2; ++e) p[e] = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse_row));
+    for (int e = 0; e < kEwCols2; e += 2) {
+      float x0, x1;
+      f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), sl2x2, nl2), x0, x1);
+      p[e] = ex2(x0);
+      p[e + 1] = ex2(x1);
+    }
   }
 }
 
@@ -482,12 +496,17 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
         uint32_t dv[kEwCols2], ds[kEwCols2 / 2];
         tmem_ld_x32(t_lane + TM_DP + kEwCols2 * h, dv);
 #pragma unroll
-        for (int v = 0; v < kEwCols2 / 4; ++v) {
+        for (int v = 0; v < kEwCols2 / 4; ++v) {  // paired sub and mul, two columns each
           const float4 dd = d4[v];
-          ds[2 * v] = pack2<BF16>(p[4 * v] * (__uint_as_float(dv[4 * v]) - dd.x),
-                                  p[4 * v + 1] * (__uint_as_float(dv[4 * v + 1]) - dd.y));
-          ds[2 * v + 1] = pack2<BF16>(p[4 * v + 2] * (__uint_as_float(dv[4 * v + 2]) - dd.z),
-                                      p[4 * v + 3] * (__uint_as_float(dv[4 * v + 3]) - dd.w));
+          float a0, a1, b0, b1;
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[4 * v], p[4 * v + 1]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[4 * v]), __uint_as_float(dv[4 * v + 1])),
+                                           f32x2_pack(dd.x, dd.y))), a0, a1);
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[4 * v + 2], p[4 * v + 3]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[4 * v + 2]), __uint_as_float(dv[4 * v + 3])),
+                                           f32x2_pack(dd.z, dd.w))), b0, b1);
+          ds[2 * v] = pack2<BF16>(a0, a1);
+          ds[2 * v + 1] = pack2<BF16>(b0, b1);
         }
         tmem_st_x16(t_lane + TM_DP + kEwCols2 * h, ds);  // over columns this thread has read
       }
@@ -588,9 +607,15 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
       {
         uint32_t dv[kEwCols2], ds[kEwCols2 / 2];
         tmem_ld_x32(t_lane + TM_DP + kEwCols2 * h, dv);
+        const uint64_t dlt2 = f32x2_pack(dlt, dlt);
 #pragma unroll
-        for (int e = 0; e < kEwCols2; e += 2)
-          ds[e / 2] = pack2<BF16>(p[e] * (__uint_as_float(dv[e]) - dlt), p[e + 1] * (__uint_as_float(dv[e + 1]) - dlt));
+        for (int e = 0; e < kEwCols2; e += 2) {  // paired sub and mul
+          float a0, a1;
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[e], p[e + 1]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])), dlt2)),
+                       a0, a1);
+          ds[e / 2] = pack2<BF16>(a0, a1);
+        }
         tmem_st_x16(t_lane + TM_DP + kEwCols2 * h, ds);  // over columns this thread has read
       }
       tmem_st_wait();
