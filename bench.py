@@ -486,8 +486,12 @@ def fp8_forward(attn, dev):
 
 
 def forward_by_workload(attn, dev):
-    """Forward TFLOP/s on the parity workloads c1, c2, c4 (both masks where they have them)."""
+    """Forward TFLOP/s on the parity workloads c1, c2, c4 (both masks where they have them).
+    c1 and c2 are short sequences: they also get HBM GB/s (algorithmic bytes: Q, K, V read,
+    O and the logsumexp written, over the time), timed one call at a time with L2 flushed
+    (a 256 MiB write) before each, since their inputs would otherwise stay in the 129 MB L2."""
     out = {}
+    flush = torch.empty(256 << 20, device=dev, dtype=torch.uint8)
     for name in ("c1", "c2", "c4"):
         w = workloads.WORKLOADS[name]
         x = workloads.inputs(name)
@@ -508,8 +512,21 @@ def forward_by_workload(attn, dev):
             torch.cuda.synchronize()
             ms = a.elapsed_time(b) / reps
             f = workloads.fwd_flops(w.B, w.H, w.N, w.d, causal)
-            out[f"{name}_{'causal' if causal else 'non_causal'}"] = {"ms": round(ms, 4),
-                                                                    "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+            ent = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+            if name in ("c1", "c2"):
+                nbytes = 4 * q.numel() * q.element_size() + lse.numel() * 4  # Q, K, V, O + lse
+                tot = 0.0
+                for _ in range(20):
+                    flush.zero_()
+                    a.record()
+                    call()
+                    b.record()
+                    torch.cuda.synchronize()
+                    tot += a.elapsed_time(b)
+                ms_cold = tot / 20
+                ent.update({"ms_l2_flushed": round(ms_cold, 4),
+                            "hbm_gbs_l2_flushed": round(nbytes / (ms_cold * 1e-3) / 1e9, 1)})
+            out[f"{name}_{'causal' if causal else 'non_causal'}"] = ent
     return out
 
 
