@@ -57,3 +57,33 @@ def test_bwd_deterministic():
     g2 = gpu_grads(x, True, 1 / math.sqrt(128))
     for a, b in zip(g1, g2):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [100, 300, 1000])
+def test_bwd_one_grid_equals_stages(N, d, causal):
+    """attn_bwd runs dK/dV and dQ as one grid; the stage entry points launch them one by
+    one.  Same kernels' arithmetic, so the same bytes."""
+    from gpu_util import Guarded
+    import tiled_online_softmax_attention_gb300 as attn
+
+    B, H = 2, 3
+    x = workloads.draw(B, H, N, d, "bf16", seed=4000 + N + d, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, causal, scale)
+    g = run_bwd(q, k, v, o, lse, do, causal, scale)
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    dq, dk, dv = (Guarded((B, H, N, d), q.dtype) for _ in range(3))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert attn.attn_bwd_prepare(o, do, lse, ws.t, nbytes, B, H, N, d, q.dtype) == attn.ATTN_OK
+    assert attn.attn_bwd_dkdv(q, k, v, do, ws.t, nbytes, dk.t, dv.t, B, H, N, d, q.dtype, causal, scale,
+                              status) == attn.ATTN_OK
+    assert attn.attn_bwd_dq(q, k, v, do, ws.t, nbytes, dq.t, B, H, N, d, q.dtype, causal, scale,
+                            status) == attn.ATTN_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and dq.intact() and dk.intact() and dv.intact() and ws.intact()
+    for a, b in zip((dq.t, dk.t, dv.t), g):
+        assert torch.equal(a, b)

@@ -507,11 +507,26 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
                              workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal);
   if (st != ATTN_OK) return st;
   if ((st = prepare_impl(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
-  if ((st = dkdv_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
-                      dev_status, stream, dr)) != ATTN_OK)
-    return st;
-  return dq_impl(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, Nk, d, dt, causal, scale, dev_status,
-                 stream, dr);
+  if (d == 256) {
+    if ((st = dkdv_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
+                        dev_status, stream, dr)) != ATTN_OK)
+      return st;
+    return dq_impl(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, Nk, d, dt, causal, scale, dev_status,
+                   stream, dr);
+  }
+  // d <= 128: dK/dV and dQ as one grid (arguments already validated above)
+  attn::BwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
+      !make_map(&a.tm_dq, dq, BH, N, d, bf16) || !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
+    return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = dr.t > 0 ? attn::launch_bwd_grads_dropout(a, d, bf16, s) : attn::launch_bwd_grads(a, d, bf16, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace

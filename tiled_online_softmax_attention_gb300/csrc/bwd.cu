@@ -217,8 +217,10 @@ __device__ __forceinline__ void store_row_chunk_packed(void* base, size_t row_el
   for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
+// The dK/dV CTA for work unit `block` (its body; the kernels below launch it).  `a` is
+// the kernel's __grid_constant__ parameter, so the tensor maps stay in parameter space.
 template <int D, bool BF16, bool DROP, bool VARLEN>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+__device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
   static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = DkdvLayout<D>;
   using T = BwdTiles<D>;
@@ -234,7 +236,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_c
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles (of the longest sequence)
-  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_tk);
+  const WorkItem wi = work_item(block, a.BH, n_tk);
   const int bh = wi.bh;
   const int kt = wi.rank;  // low key tiles see the most queries: they go first
   const int k0 = kt * kTileN;
@@ -580,8 +582,9 @@ enum : int {
   Q_COUNT = 24
 };
 
+// The dQ CTA for work unit `block` (its body; the kernels below launch it).
 template <int D, bool BF16, bool DROP, bool VARLEN>
-__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+__device__ __forceinline__ void dq_body(const BwdArgs& a, int block) {
   static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = DqLayout<D>;
   using T = BwdTiles<D>;
@@ -597,7 +600,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
-  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const WorkItem wi = work_item(block, a.BH, n_t);
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tiles first
   const int q0 = qt * kTileM;
@@ -880,6 +883,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_con
   }
 }
 
+template <int D, bool BF16, bool DROP, bool VARLEN>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdArgs a) {
+  dkdv_body<D, BF16, DROP, VARLEN>(a, static_cast<int>(blockIdx.x));
+}
+
+template <int D, bool BF16, bool DROP, bool VARLEN>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdArgs a) {
+  dq_body<D, BF16, DROP, VARLEN>(a, static_cast<int>(blockIdx.x));
+}
+
+// Both gradient stages in one grid: the first n_dkdv CTAs are dK/dV units, the rest dQ
+// units.  The two stages are independent once the preparation pass has run, and the
+// block scheduler starts the dQ CTAs as the dK/dV CTAs retire, so the end of one stage
+// overlaps the start of the other instead of draining the GPU between two launches.
+template <int D, bool BF16, bool DROP>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_grads_kernel(const __grid_constant__ BwdArgs a, int n_dkdv) {
+  const int b = static_cast<int>(blockIdx.x);
+  if (b < n_dkdv)
+    dkdv_body<D, BF16, DROP, false>(a, b);
+  else
+    dq_body<D, BF16, DROP, false>(a, b - n_dkdv);
+}
+
 template <int D, bool BF16, bool VARLEN = false>
 cudaError_t launch_pre_t(const BwdArgs& a, cudaStream_t st) {
   const int64_t rows = static_cast<int64_t>(a.BH) * a.Npad;
@@ -907,6 +933,19 @@ cudaError_t launch_dq_t(const BwdArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
   k<<<n_t * a.BH, kBwdThreads, DqLayout<D>::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16, bool DROP = false>
+cudaError_t launch_grads_t(const BwdArgs& a, cudaStream_t st) {
+  auto k = bwd_grads_kernel<D, BF16, DROP>;
+  constexpr int smem_kv = DkdvLayout<D>::SMEM + (DROP ? DkdvLayout<D>::DROP_BYTES : 0);
+  constexpr int smem = smem_kv > DqLayout<D>::SMEM ? smem_kv : DqLayout<D>::SMEM;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_dkdv = (a.Nk + kTileN - 1) / kTileN * a.BH;
+  const int n_dq = (a.N + kTileM - 1) / kTileM * a.BH;
+  k<<<n_dkdv + n_dq, kBwdThreads, smem, st>>>(a, n_dkdv);
   return cudaGetLastError();
 }
 
@@ -939,6 +978,7 @@ cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
 }
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_dkdv_t) }
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_dq_t) }
+cudaError_t launch_bwd_grads(const BwdArgs& a, int d, bool bf16, cudaStream_t s) { ATTN_DISPATCH(launch_grads_t) }
 #undef ATTN_DISPATCH
 
 #define ATTN_DISPATCH_DROP(fn)                                                          \
@@ -950,6 +990,9 @@ cudaError_t launch_bwd_dkdv_dropout(const BwdArgs& a, int d, bool bf16, cudaStre
 }
 cudaError_t launch_bwd_dq_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
   ATTN_DISPATCH_DROP(launch_dq_t)
+}
+cudaError_t launch_bwd_grads_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  ATTN_DISPATCH_DROP(launch_grads_t)
 }
 #undef ATTN_DISPATCH_DROP
 

@@ -150,6 +150,9 @@ cudaError_t launch_bwd_dq_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+// dK/dV and dQ in one grid (the preparation pass must have run)
+cudaError_t launch_bwd_grads(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd_grads_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s);  // d = 256: dV, then dK
 cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t limit_ns, cudaStream_t s);
