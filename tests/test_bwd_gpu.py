@@ -87,3 +87,22 @@ def test_bwd_one_grid_equals_stages(N, d, causal):
     assert int(status.item()) == 0 and dq.intact() and dk.intact() and dv.intact() and ws.intact()
     for a, b in zip((dq.t, dk.t, dv.t), g):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_bwd_on_a_side_stream(d):
+    """attn_bwd launched on a non-default stream (inputs produced on the default stream and
+    ordered by an event) gives the default stream's bytes."""
+    B, H, N = 1, 2, 700
+    x = workloads.draw(B, H, N, d, "bf16", seed=4500 + d, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, True, scale)
+    g0 = run_bwd(q, k, v, o, lse, do, True, scale)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        g1 = run_bwd(q, k, v, o, lse, do, True, scale, stream=s)
+    torch.cuda.synchronize()
+    for a, b in zip(g0, g1):
+        assert torch.equal(a, b)
