@@ -375,6 +375,7 @@ def long_forward(attn, dev):
         out["causal" if causal else "non_causal"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
     res = {"long_forward_B1_H32_N16384_d128": out}
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
+    res["decode_B1_H32_Nq128_Nk32768_d128"] = decode_forward(attn, dev)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     res["d256_forward_and_step_B1_H16_N16384"] = d256_side(attn, dev)
@@ -561,6 +562,49 @@ def split_forward(attn, dev):
             torch.cuda.synchronize()
             ms = a.elapsed_time(b) / 20
             ent["attn_fwd" if ns == 1 else f"splits_{ns}"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+        out["causal" if causal else "non_causal"] = ent
+    return out
+
+
+def decode_forward(attn, dev):
+    """Decode-like shape: B=1, H=32, 128 new queries against 32768 keys (causal: the
+    queries are the last 128 positions), d=128.  attn_fwd_rect has one query-tile pair
+    per head (32 CTAs); attn_fwd_splitkv_rect cuts the keys into ranges.  FLOPs: two
+    Nq x Nk x d products (causal: the visible part, the last 128 rows of the triangle)."""
+    B, H, Nq, Nk, d = 1, 32, 128, 32768, 128
+    g = torch.Generator().manual_seed(17)
+    q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), device=dev, dtype=torch.float32)
+    sc = 1.0 / math.sqrt(d)
+    out = {}
+    for causal in (False, True):
+        visible = Nq * Nk - (Nq * (Nq - 1) // 2 if causal else 0)
+        f = 4.0 * B * H * visible * d
+        ent = {}
+        for ns in (1, 4, 8, 16):
+            nb = attn.attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, ns)
+            ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+            if ns == 1:
+                call = lambda: attn.attn_fwd_rect(q, k, v, o, lse, B, H, Nq, Nk, d, q.dtype, causal, sc)
+            else:
+                call = lambda: attn.attn_fwd_splitkv_rect(q, k, v, o, lse, ws, nb, B, H, Nq, Nk, d, q.dtype, causal,
+                                                          sc, ns)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(20):
+                call()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / 20
+            kv_gbs = 2 * B * H * Nk * d * 2 / (ms * 1e-3) / 1e9
+            ent["attn_fwd_rect" if ns == 1 else f"splits_{ns}"] = {
+                "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1), "kv_read_gbs": round(kv_gbs, 1)}
         out["causal" if causal else "non_causal"] = ent
     return out
 

@@ -178,6 +178,19 @@ ATTN_API attn_status attn_fwd_splitkv(const void *q, const void *k, const void *
                              int n_splits, int *dev_status, void *stream);
 
 /*
+ * attn_fwd_splitkv_rect -- attn_fwd_splitkv for attn_fwd_rect's shapes: Nq queries
+ * against Nk keys, q, o [B][H][Nq][d], k, v [B][H][Nk][d], lse [B][H][Nq], causal
+ * aligned to the last key (Nk >= Nq).  Meant for few queries over a long key sequence
+ * (decoding a block of new tokens after a long prefix), where the query tiles alone
+ * leave most of the GPU idle.  The workspace is attn_fwd_splitkv_workspace_bytes(B, H,
+ * Nq, d, n_splits).  Everything else is as for attn_fwd_splitkv / attn_fwd_rect.
+ */
+ATTN_API attn_status attn_fwd_splitkv_rect(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  void *workspace, size_t workspace_bytes,
+                                  int B, int H, int Nq, int Nk, int d, attn_dtype dt, int causal,
+                                  float scale, int n_splits, int *dev_status, void *stream);
+
+/*
  * attn_fwd_fp8 -- forward pass on FP8 inputs with per-block scale factors (the FP8
  * support with block-wise scaling of "FlashAttention hardware-aware analysis"
  * (huaweicloud), section four, part 3).

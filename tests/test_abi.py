@@ -130,6 +130,19 @@ def test_splitkv_validates():
         assert attn.attn_fwd_splitkv(**a2) == st, kw
 
 
+def test_splitkv_rect_validates():
+    args = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], workspace=A[9], workspace_bytes=1 << 24, B=1, H=2,
+                Nq=128, Nk=4096, d=128, dt=0, causal=1, scale=0.088, n_splits=4, stream=0)
+    for kw, st in [(dict(Nq=600, Nk=500), attn.ATTN_ERR_INVALID_ARG),       # causal needs Nk >= Nq
+                   (dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(o=A[1] + 128 * 128 * 2 * 2), attn.ATTN_ERR_INVALID_ARG),  # o inside k (Nk rows)
+                   (dict(workspace_bytes=4 * 2 * 128 * 129 * 4 - 4), attn.ATTN_ERR_INVALID_ARG),  # sized by Nq
+                   (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG)]:
+        a2 = dict(args)
+        a2.update(kw)
+        assert attn.attn_fwd_splitkv_rect(**a2) == st, kw
+
+
 def fwd_fp8(**kw):
     args = dict(q8=A[0], k8=A[1], v8=A[2], q_scale=A[5], k_scale=A[6], v_scale=A[7], o=A[3], lse=A[4], B=1, H=2,
                 N=256, d=128, out_dt=0, causal=0, scale=0.088, stream=0)

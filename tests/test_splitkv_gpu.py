@@ -66,3 +66,58 @@ def test_splitkv_stress_fp16():
     o_ref, lse_ref = oracle.attn_fwd(x["q"], x["k"], x["v"], False, 1 / math.sqrt(128))
     assert o_err(o, o_ref) <= O_MAX_ABS
     assert lse_err(lse, lse_ref) <= LSE_REL
+
+
+def run_split_rect(q, k, v, causal, n_splits, scale=None):
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o = Guarded((B, H, Nq, d), q.dtype)
+    lse = Guarded((B, H, Nq), torch.float32)
+    nbytes = attn.attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, n_splits)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_splitkv_rect(q, k, v, o.t, lse.t, ws.t, nbytes, B, H, Nq, Nk, d, q.dtype, causal, scale,
+                                    n_splits, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert o.intact() and lse.intact() and ws.intact(), "split-KV wrote outside its buffers"
+    return o.t, lse.t
+
+
+def draw_rect(B, H, Nq, Nk, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+@pytest.mark.parametrize("n_splits", [2, 5])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(1, 1000), (64, 4097), (128, 3000), (200, 2000), (300, 300), (513, 700)])
+def test_splitkv_rect_vs_oracle(Nq, Nk, d, causal, n_splits):
+    """Few queries against many keys (causal: the queries are the last Nq of Nk positions)."""
+    q, k, v = draw_rect(1, 2, Nq, Nk, d, seed=Nq * 31 + Nk + d + n_splits)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_split_rect(q.cuda(), k.cuda(), v.cuda(), causal, n_splits, scale)
+    ro, rl = oracle.attn_fwd(q, k, v, causal, scale)
+    assert o_err(o, ro) <= O_MAX_ABS, f"O error {o_err(o, ro):.3e}"
+    assert lse_err(lse, rl) <= LSE_REL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_rect_decode_shape_sampled(causal):
+    """B=1, H=8, 128 new queries after 32640 earlier positions (Nk = 32768), 16 ranges:
+    sampled rows of three heads against the oracle."""
+    B, H, Nq, Nk, d = 1, 8, 128, 32768, 128
+    q, k, v = draw_rect(B, H, Nq, Nk, d, seed=91)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_split_rect(q.cuda(), k.cuda(), v.cuda(), causal, 16, scale)
+    rows = [0, 1, 17, 63, 64, 100, 126, 127]
+    for h in (0, 4, 7):
+        ro, rl = oracle.attn_fwd(q[0, h], k[0, h], v[0, h], causal, scale, rows=rows)
+        assert o_err(o[0, h], ro, rows) <= O_MAX_ABS
+        assert float(np.max(np.abs(f64(lse[0, h])[rows] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL

@@ -22,6 +22,8 @@ current stream):
     attn_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, N, d, out_dt, causal, scale,
                  dev_status=None, stream=None)
     attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits)
+    attn_fwd_splitkv_rect(q, k, v, o, lse, workspace, workspace_bytes, B, H, Nq, Nk, d, dt, causal,
+                          scale, n_splits, dev_status=None, stream=None)
     attn_fwd_splitkv(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, dt, causal, scale,
                      n_splits, dev_status=None, stream=None)
     attn_bwd_workspace_bytes(B, H, N, d)
@@ -60,7 +62,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_rect", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -104,6 +106,8 @@ def load(build_if_missing: bool = True):
     lib.attn_fwd_splitkv_workspace_bytes.restype = SZ
     lib.attn_fwd_splitkv.argtypes = [P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, I, P, P]
     lib.attn_fwd_splitkv.restype = I
+    lib.attn_fwd_splitkv_rect.argtypes = [P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, I, P, P]
+    lib.attn_fwd_splitkv_rect.restype = I
     lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_bwd_workspace_bytes.restype = SZ
     lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, P, P]
@@ -224,6 +228,14 @@ def attn_fwd_splitkv(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, d, dt
                                        int(workspace_bytes), int(B), int(H), int(N), int(d), _dt(dt),
                                        int(bool(causal)), float(scale), int(n_splits), _ptr(dev_status),
                                        _stream(stream)))
+
+
+def attn_fwd_splitkv_rect(q, k, v, o, lse, workspace, workspace_bytes, B, H, Nq, Nk, d, dt, causal, scale,
+                          n_splits, dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd_splitkv_rect(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                            int(workspace_bytes), int(B), int(H), int(Nq), int(Nk), int(d),
+                                            _dt(dt), int(bool(causal)), float(scale), int(n_splits),
+                                            _ptr(dev_status), _stream(stream)))
 
 
 def attn_bwd_workspace_bytes(B, H, N, d) -> int:

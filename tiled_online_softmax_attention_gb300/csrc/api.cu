@@ -321,39 +321,53 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits
 attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, void* workspace,
                              size_t workspace_bytes, int B, int H, int N, int d, attn_dtype dt, int causal,
                              float scale, int n_splits, int* dev_status, void* stream) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale);
+  return attn_fwd_splitkv_rect(q, k, v, o, lse, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
+                               n_splits, dev_status, stream);
+}
+
+attn_status attn_fwd_splitkv_rect(const void* q, const void* k, const void* v, void* o, float* lse,
+                                  void* workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk, int d,
+                                  attn_dtype dt, int causal, float scale, int n_splits, int* dev_status,
+                                  void* stream) {
+  attn_status st = check_sizes(B, H, Nq, d, dt, scale, false, Nk);
   if (st != ATTN_OK) return st;
+  if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > 64) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
     return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_fwd_splitkv_workspace_bytes(B, H, N, d, n_splits);
+  const size_t need = attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, n_splits);
   if (workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
-  const size_t tb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
-  for (const void* in : {q, k, v})
-    if (overlaps(in, tb, o, tb) || overlaps(in, tb, lse, lb) || overlaps(in, tb, workspace, need))
+  const size_t qb = static_cast<size_t>(B) * H * Nq * d * 2, kb = static_cast<size_t>(B) * H * Nk * d * 2;
+  const size_t lb = static_cast<size_t>(B) * H * Nq * 4;
+  const void* ins[] = {q, k, v};
+  const size_t in_bytes[] = {qb, kb, kb};
+  for (int i = 0; i < 3; ++i)
+    if (overlaps(ins[i], in_bytes[i], o, qb) || overlaps(ins[i], in_bytes[i], lse, lb) ||
+        overlaps(ins[i], in_bytes[i], workspace, need))
       return ATTN_ERR_INVALID_ARG;
-  if (overlaps(o, tb, lse, lb) || overlaps(o, tb, workspace, need) || overlaps(lse, lb, workspace, need))
+  if (overlaps(o, qb, lse, lb) || overlaps(o, qb, workspace, need) || overlaps(lse, lb, workspace, need))
     return ATTN_ERR_INVALID_ARG;
   if ((st = check_device()) != ATTN_OK) return st;
 
   attn::FwdArgs a{};
   const bool bf16 = dt == ATTN_BF16;
   const int BH = B * H;
-  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, N, d, bf16) ||
-      !make_map(&a.tm_v, v, BH, N, d, bf16) || !make_map(&a.tm_o, o, BH, N, d, bf16))
+  if (!make_map(&a.tm_q, q, BH, Nq, d, bf16) || !make_map(&a.tm_k, k, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_o, o, BH, Nq, d, bf16))
     return ATTN_ERR_CUDA;
   a.o = o;
   a.lse = lse;
   a.dev_status = dev_status;
-  a.N = N;
-  a.Nk = N;
+  a.N = Nq;
+  a.Nk = Nk;
+  a.cofs = causal ? Nk - Nq : 0;
   a.BH = BH;
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
   a.n_splits = n_splits;
   a.part_o = static_cast<float*>(workspace);
-  a.part_lse = static_cast<float*>(workspace) + static_cast<size_t>(n_splits) * BH * N * d;
+  a.part_lse = static_cast<float*>(workspace) + static_cast<size_t>(n_splits) * BH * Nq * d;
   if (attn::launch_fwd_split(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }

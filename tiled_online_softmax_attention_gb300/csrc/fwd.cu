@@ -121,8 +121,11 @@ enum : int {
 // writes its range's normalised partial O (fp32) and logsumexp instead of the output;
 // attn_merge_kernel combines the ranges with the two-block merge of the huaweicloud
 // page's section two.
-template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP, bool VARLEN>
-__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
+// The CTA's body; PAD: its pair's second query tile lies wholly past the last query
+// (a sequence of an odd number of tiles, or a few queries against many keys), so only
+// tile 0 runs.  `a` is the kernel's __grid_constant__ parameter.
+template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP, bool VARLEN, bool PAD>
+__device__ __forceinline__ void fwd_body(const FwdArgs& a) {
   static_assert(!(FP8 && SPLIT) && (!FP8 || D == 128), "E4M3 inputs: d = 128, no split");
   static_assert(!DROP || (!FP8 && !SPLIT), "dropout: 16-bit inputs, no split");
   static_assert(!VARLEN || (!FP8 && !SPLIT && !DROP), "packed sequences: plain 16-bit forward");
@@ -214,6 +217,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     n_kv[1] = (split == ns - 1 ? n_kv[1] : hi0) - kv0;
     n_kv[0] = hi0 - kv0;
   }
+  if constexpr (PAD) n_kv[1] = 0;  // the padding tile visits no key tile
+  const int n_steps = PAD ? n_kv[0] : n_kv[1];  // key tiles the pair visits (n_kv[1] >= n_kv[0])
 
   // Warpgroup hand-offs arrive once per warp for 16-bit tiles and once per thread for
   // E4M3 tiles: each measured about 1 % faster than the other form on its own path.
@@ -269,7 +274,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           tma_load_3d(sb + L::OFF_Q + i * L::OTILE + kb * L::BLK, &a.tm_q, bar(B_Q + i), kb * (128 / L::ELEM),
                       qc1((2 * pr + i) * kTileM), qc2((2 * pr + i) * kTileM));
       }
-      const int n_loads = 2 * n_kv[1];  // K_j, V_j alternately
+      const int n_loads = 2 * n_steps;  // K_j, V_j alternately
       int issued = 0;
       for (int ld = 0; ld < n_loads; ++ld) {
         const int s = ld % L::NSLOT;
@@ -322,6 +327,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
         tc_commit(bar(B_ODONE + i));
       };
+      constexpr bool has1 = !PAD;
       bool ok = mbar_wait(bar(B_Q + 0), 0, wc) && full(0);
       if (ok) {
         tc_fence_after();
@@ -330,10 +336,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       if (ok) {
         tc_fence_after();
-        issue_s(1, 0);
+        if (has1) issue_s(1, 0);
         tc_commit(bar(B_KVEMPTY + 0));
       }
-      for (int j = 0; ok && j < n_kv[1]; ++j) {
+      for (int j = 0; ok && j < n_steps; ++j) {
         bool v_ready = false, k_next_ready = false;
         if (j < n_kv[0]) {
           if (!(ok = full(2 * j + 1) && mbar_wait(bar(B_PFULL + 0), j & 1, wc) &&
@@ -349,16 +355,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             issue_s(0, j + 1);
           }
         }
-        if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait(bar(B_PFULL + 1), j & 1, wc) &&
-                   (j == 0 || mbar_wait(bar(B_CORR + 1), (j - 1) & 1, wc))))
-          break;
-        tc_fence_after();
-        issue_pv(1, j);
-        tc_commit(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
-        if (j + 1 < n_kv[1]) {
-          if (!(ok = k_next_ready || full(2 * j + 2))) break;
+        if (has1) {
+          if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait(bar(B_PFULL + 1), j & 1, wc) &&
+                     (j == 0 || mbar_wait(bar(B_CORR + 1), (j - 1) & 1, wc))))
+            break;
           tc_fence_after();
-          issue_s(1, j + 1);
+          issue_pv(1, j);
+        }
+        tc_commit(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
+        if (j + 1 < n_steps) {
+          if (has1) {  // (without tile 1, tile 0's S(j+1) above was the slot's last use)
+            if (!(ok = k_next_ready || full(2 * j + 2))) break;
+            tc_fence_after();
+            issue_s(1, j + 1);
+          }
           tc_commit(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
         }
       }
@@ -530,7 +540,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
-    for (int j = 1; ok && j < n_kv[1]; ++j) {
+    for (int j = 1; ok && j < n_steps; ++j) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         if (j >= n_kv[i]) continue;
@@ -557,6 +567,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     // Epilogue: O_i / l -> 16-bit -> swizzled staging over Q_i -> TMA store; logsumexp.
 #pragma unroll 1
     for (int i = 0; i < 2; ++i) {
+      if (PAD && i == 1) continue;  // the padding tile: nothing to store
       const bool ok_i = ok && mbar_wait_warp(bar(B_FIN + i), 0, wc) &&
                         mbar_wait_warp(bar(B_ODONE + i), (n_kv[i] - 1) & 1, wc);
       const int q0 = (2 * pr + i) * kTileM;
@@ -635,6 +646,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     tc_fence_after();
     tmem_dealloc(tmem, L::TM_COLS);
   }
+}
+
+template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP, bool VARLEN>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdArgs a) {
+  // Which body this CTA runs: the same pair and length the body derives.
+  const int n_pairs = ((a.N + kTileM - 1) / kTileM + 1) / 2;
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x) / (SPLIT ? a.n_splits : 1), a.BH, n_pairs);
+  const int pr = n_pairs - 1 - wi.rank;
+  int N = a.N;
+  if constexpr (VARLEN) N = seq_view(a, wi.bh).N;
+  if ((2 * pr + 1) * kTileM >= N)
+    fwd_body<D, BF16, SPLIT, FP8, DROP, VARLEN, true>(a);
+  else
+    fwd_body<D, BF16, SPLIT, FP8, DROP, VARLEN, false>(a);
 }
 
 template <int D, bool BF16, bool SPLIT, bool FP8 = false, bool DROP = false, bool VARLEN = false>
