@@ -53,3 +53,33 @@ def test_32k_sequence_sampled(causal):
         for name, g, r in (("dQ", dq[0, h, rows], rq), ("dK", dk[0, h, rows], rk), ("dV", dv[0, h, rows], rv)):
             e = grad_err(g, r)
             assert e <= GRAD_REL_L2, f"head {h} {name} relative L2 {e:.3e}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_largest_element_count(d):
+    """The most elements a call takes, B*H*N*d just under 2^31 (131071 or 262143 heads of
+    one 128-row tile): every element index of the tensors is exercised.  Forward and
+    backward, causal; all outputs finite, and three heads (first, middle, last) against
+    the oracle.  Inputs are drawn on the device from a seeded generator."""
+    B, N = 1, 128
+    H = (1 << 31) // (N * d) - 1
+    g = torch.Generator(device="cuda").manual_seed(70 + d)
+
+    def draw():
+        return torch.randn((B, H, N, d), device="cuda", generator=g).to(torch.bfloat16)
+
+    q, k, v, do = draw(), draw(), draw(), draw()
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, True, scale)
+    dq, dk, dv = run_bwd(q, k, v, o, lse, do, True, scale)
+    for t in (o, lse, dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
+    for h in (0, H // 2, H - 1):
+        qh, kh, vh, dh = (t[0, h].cpu() for t in (q, k, v, do))
+        ro, rl = oracle.attn_fwd(qh, kh, vh, True, scale)
+        assert o_err(o[0, h], ro) <= O_MAX_ABS
+        assert float(np.max(np.abs(f64(lse[0, h]) - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+        refs = oracle.attn_bwd(qh, kh, vh, dh, True, scale)
+        for name, gr, r in zip(("dQ", "dK", "dV"), (dq[0, h], dk[0, h], dv[0, h]), refs):
+            e = grad_err(gr, r)
+            assert e <= GRAD_REL_L2, f"head {h} {name} relative L2 {e:.3e}"
