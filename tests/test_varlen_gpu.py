@@ -132,3 +132,43 @@ def test_varlen_long_batch_sampled():
                                ("dV", dv[cu[b] + rows, h], rv)):
                 e = grad_err(g, r)
                 assert e <= GRAD_REL_L2, f"sequence {b} head {h} {name} relative L2 {e:.3e}"
+
+
+def random_batches(n, seed=77):
+    import random
+
+    rnd = random.Random(seed)
+    out = []
+    for i in range(n):
+        B = rnd.randint(1, 6)
+        causal = rnd.random() < 0.5
+        d = rnd.choice([64, 128])
+        dtype = rnd.choice(["bf16", "fp16"])
+        lq, lk = [], []
+        for _ in range(B):
+            q = rnd.choice([0, 1, 63, 127, 128, 129, 200, 300, 513])
+            if causal:
+                k = q + rnd.choice([0, 1, 50, 200])
+            else:
+                k = rnd.choice([1, 5, 128, 257, 600]) if q > 0 else rnd.choice([0, 7])
+            lq.append(q)
+            lk.append(k)
+        if sum(lq) == 0:
+            lq[0], lk[0] = 5, max(lk[0], 5)
+        out.append((i, tuple(lq), tuple(lk), causal, d, dtype))
+    return out
+
+
+@pytest.mark.parametrize("i,lens_q,lens_k,causal,d,dtype", random_batches(40))
+def test_varlen_random_batches(i, lens_q, lens_k, causal, d, dtype):
+    """Seeded random batches of 1-6 sequences (empty ones included), forward and backward."""
+    x = packed(list(lens_q), list(lens_k), 2, d, dtype, seed=600 + i)
+    scale = 1.0 / math.sqrt(d)
+    o, lse, dq, dk, dv = run_varlen(x, causal, scale)
+    ro, rl = oracle.attn_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal, scale)
+    assert float(np.max(np.abs(f64(o) - ro) - half_ulp(ro, o.dtype))) <= O_MAX_ABS
+    assert float(np.max(np.abs(f64(lse) - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+    rq, rk, rv = oracle.attn_bwd_varlen(x["q"], x["k"], x["v"], x["dout"], x["cu_q"], x["cu_k"], causal, scale)
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        e = grad_err(g, r)
+        assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e}"
