@@ -114,7 +114,7 @@ ATTN_API attn_status attn_fwd_rect(const void *q, const void *k, const void *v, 
  * are clamped to them and to [0, T], so a malformed table cannot make the kernels
  * write outside the buffers, but its results are unspecified.  A sequence with no key,
  * or causal with fewer keys than queries, gets O = 0, lse = -inf and zero gradients.
- * The backward workspace is attn_bwd_workspace_bytes(B, H, max_q, d).  d in {64, 128}.
+ * The backward workspace is attn_bwd_workspace_bytes(B, H, max_q, d).  d in {64, 128, 256}.
  * Everything else is as for attn_fwd / attn_bwd.
  */
 ATTN_API attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,

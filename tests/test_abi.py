@@ -212,7 +212,7 @@ def test_varlen_validates():
               Tq=600, Tk=600, d=128, dt=0, causal=1, scale=0.088, stream=0)
     for kw, st in [(dict(B=0), attn.ATTN_ERR_INVALID_ARG), (dict(Tk=0), attn.ATTN_ERR_INVALID_ARG),
                    (dict(cu_q=A[5] + 2), attn.ATTN_ERR_INVALID_ARG), (dict(cu_k=0), attn.ATTN_ERR_INVALID_ARG),
-                   (dict(d=256), attn.ATTN_ERR_UNSUPPORTED), (dict(o=A[0]), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(d=192), attn.ATTN_ERR_UNSUPPORTED), (dict(o=A[0]), attn.ATTN_ERR_INVALID_ARG),
                    (dict(lse=A[3] + 16), attn.ATTN_ERR_INVALID_ARG)]:
         a2 = dict(fa)
         a2.update(kw)

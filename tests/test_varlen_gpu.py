@@ -60,7 +60,7 @@ LENS = [1, 127, 300, 0, 129, 513, 64]
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("extra_keys", [False, True])
 def test_varlen_fwd_bwd(extra_keys, causal, d, dtype):
@@ -80,8 +80,9 @@ def test_varlen_fwd_bwd(extra_keys, causal, d, dtype):
         assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e} (causal={causal} d={d} {dtype} extra={extra_keys})"
 
 
-def test_varlen_single_sequence_equals_attn_fwd():
-    N, H, d = 700, 4, 128
+@pytest.mark.parametrize("d", [128, 256])
+def test_varlen_single_sequence_equals_attn_fwd(d):
+    N, H = 700, 4
     x = packed([N], [N], H, d, "bf16", seed=5)
     o, lse, dq, dk, dv = run_varlen(x, True, 0.1)
     q, k, v, do = (x[n].permute(1, 0, 2).unsqueeze(0).contiguous().cuda() for n in ("q", "k", "v", "dout"))
@@ -92,11 +93,12 @@ def test_varlen_single_sequence_equals_attn_fwd():
         assert torch.equal(a.permute(1, 0, 2), b[0])
 
 
-def test_varlen_degenerate_sequences():
+@pytest.mark.parametrize("d", [64, 256])
+def test_varlen_degenerate_sequences(d):
     """A sequence without keys, and causal with fewer keys than queries: O = 0, lse = -inf,
     zero gradients; their neighbours are unaffected."""
     lens_q, lens_k = [200, 150, 300], [200, 0, 100]
-    x = packed(lens_q, lens_k, 2, 64, "bf16", seed=6)
+    x = packed(lens_q, lens_k, 2, d, "bf16", seed=6)
     o, lse, dq, dk, dv = run_varlen(x, True, 0.125)
     cq, ck = x["cu_q"].tolist(), x["cu_k"].tolist()
     go, gl = f64(o), f64(lse)
@@ -142,7 +144,7 @@ def random_batches(n, seed=77):
     for i in range(n):
         B = rnd.randint(1, 6)
         causal = rnd.random() < 0.5
-        d = rnd.choice([64, 128])
+        d = rnd.choice([64, 128, 256])
         dtype = rnd.choice(["bf16", "fp16"])
         lq, lk = [], []
         for _ in range(B):

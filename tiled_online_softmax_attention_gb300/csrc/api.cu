@@ -225,10 +225,10 @@ attn_status attn_fwd_rect(const void* q, const void* k, const void* v, void* o, 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
                             const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk, int d,
                             attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
-  attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale);
+  attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale, true);  // d = 256 too
   if (st != ATTN_OK) return st;
   if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(B) * H * ((max_q + 255) / 256) >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H * ((max_q + 127) / 128) >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned4(cu_q) ||
       !aligned4(cu_k))
     return ATTN_ERR_INVALID_ARG;
@@ -259,7 +259,9 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
-  if (attn::launch_fwd_varlen(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaError_t e = d == 256 ? attn::launch_fwd256_varlen(a, bf16, static_cast<cudaStream_t>(stream))
+                                 : attn::launch_fwd_varlen(a, d, bf16, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 
@@ -588,7 +590,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                             const int* cu_q, const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk,
                             int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
-  attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale);  // H * tokens * d < 2^31
+  attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale, true);  // H * tokens * d < 2^31
   if (st != ATTN_OK) return st;
   if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
   const int64_t tiles = static_cast<int64_t>(B) * H * ((max_q > max_k ? max_q : max_k) + kTileM - 1) / kTileM;
@@ -630,9 +632,14 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   a.dk_out = dk;
   a.dv_out = dv;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess || attn::launch_bwd_dkdv_varlen(a, d, bf16, s) != cudaSuccess ||
-      attn::launch_bwd_dq_varlen(a, d, bf16, s) != cudaSuccess)
-    return ATTN_ERR_CUDA;
+  if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess) return ATTN_ERR_CUDA;
+  const cudaError_t e = d == 256 ? (attn::launch_bwd256_dkdv_varlen(a, bf16, s) == cudaSuccess
+                                        ? attn::launch_bwd256_dq_varlen(a, bf16, s)
+                                        : cudaErrorLaunchFailure)
+                                 : (attn::launch_bwd_dkdv_varlen(a, d, bf16, s) == cudaSuccess
+                                        ? attn::launch_bwd_dq_varlen(a, d, bf16, s)
+                                        : cudaErrorLaunchFailure);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
 }
 

@@ -997,6 +997,7 @@ cudaError_t launch_bwd_grads_dropout(const BwdArgs& a, int d, bool bf16, cudaStr
 #undef ATTN_DISPATCH_DROP
 
 cudaError_t launch_bwd_pre_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 256) return bf16 ? launch_pre_t<256, true, true>(a, s) : launch_pre_t<256, false, true>(a, s);
   if (d == 128) return bf16 ? launch_pre_t<128, true, true>(a, s) : launch_pre_t<128, false, true>(a, s);
   return bf16 ? launch_pre_t<64, true, true>(a, s) : launch_pre_t<64, false, true>(a, s);
 }

@@ -145,17 +145,18 @@ struct Ring {
   __device__ uint32_t empty(int item) const { return bars + 8 * (R_EMPTY + item % NSLOT); }
 };
 
-// Producer: the two column halves (columns 0..127, 128..255) of the 128-row tile at
-// `row` of head `bh`, as the ring's next two items, each once the item NSLOT earlier
-// has been released.
+// Producer: the two column halves (columns 0..127, 128..255) of a 128-row tile, as the
+// ring's next two items, each once the item NSLOT earlier has been released.  (y, z) are
+// the tile's TMA coordinates: (first row, head-batch), or (head, first token) in a packed
+// [tokens][H][d] tensor.
 template <int NSLOT>
-__device__ __forceinline__ bool load_tile(Ring<NSLOT>& r, const CUtensorMap* m, int row, int bh,
+__device__ __forceinline__ bool load_tile(Ring<NSLOT>& r, const CUtensorMap* m, int y, int z,
                                           const WaitCtl& wc) {
   for (int half = 0; half < 2; ++half) {
     const int c = r.c;
     if (c >= NSLOT && !mbar_wait(r.empty(c), ((c / NSLOT) - 1) & 1, wc)) return false;
     mbar_arrive_expect_tx(r.full(c), kHalf);
-    for (int b = 0; b < 2; ++b) tma_load_3d(r.slot_addr(c) + b * kBlk, m, r.full(c), 128 * half + 64 * b, row, bh);
+    for (int b = 0; b < 2; ++b) tma_load_3d(r.slot_addr(c) + b * kBlk, m, r.full(c), 128 * half + 64 * b, y, z);
     ++r.c;
   }
   return true;
@@ -238,6 +239,32 @@ struct RowStage {
   }
 };
 
+// The lengths a CTA works with and where its rows sit: the kernel parameters, or (VARLEN)
+// one packed sequence's (seq_view), whose rows are token t0 + r of head hh.
+struct Lens {
+  int N, Nk, cofs, hh, tq0, tk0;
+  bool degenerate;
+};
+template <bool VARLEN>
+__device__ __forceinline__ Lens lens_of(const BwdArgs& a, int bh) {
+  if constexpr (VARLEN) {
+    const SeqView v = seq_view(a, bh);
+    return {v.N, v.Nk, v.cofs, v.hh, v.tq0, v.tk0, v.degenerate || v.N <= 0};
+  } else {
+    return {a.N, a.Nk, a.cofs, 0, 0, 0, false};
+  }
+}
+
+// Zero rows r0 .. min(r0 + 128, n) - 1 of head hh of a packed [T][H][256] tensor whose
+// sequence starts at token t0 (the gradients of a sequence that has no softmax).
+__device__ __forceinline__ void zero_rows256(void* base, int H, int hh, int t0, int r0, int n) {
+  for (int r = threadIdx.x; r < kTileM; r += blockDim.x) {
+    if (r0 + r >= n) continue;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + ((static_cast<size_t>(t0 + r0 + r) * H + hh) * D2) * 2);
+    for (int c = 0; c < D2 / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // P for this thread's 32 columns from S in registers: 2^(s scale log2e - lse2), lse2 one
 // per column (lse4) or one for the row (lse_row, when lse4 is null).
 __device__ __forceinline__ void softmax_cols(const uint32_t (&sv)[kEwCols2], float sl2, const float4* lse4,
@@ -283,13 +310,36 @@ __device__ __forceinline__ void mask_cols(float (&p)[kEwCols2], int lo, int hi) 
 // Epilogue: this thread's row of a 256-column fp32 accumulator (its warpgroup's 64
 // columns), scaled, as 16-bit into a 128B-swizzled staging tile over the ring; then one
 // TMA store of the 128 x 256 tile at row `row0` of head `bh`.
-template <bool BF16>
+// VARLEN: the rows go straight to the packed tensor `out` (row r0 + row of the sequence
+// at token t0, head hh; rows >= n are not written) instead of through a TMA store.
+template <bool BF16, bool VARLEN>
 __device__ __forceinline__ void epilogue256(bool ok, const Cta& c, int off_ring, uint32_t t_acc, int row, int h,
                                             float mul, uint32_t done_bar, const WaitCtl& wc, const CUtensorMap* m,
-                                            int row0, int bh) {
+                                            int row0, int bh, void* out, int H, int hh, int t0, int n) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* stage = c.smem + off_ring;
   if (ok) ok = mbar_wait_warp(done_bar, 0, wc);
+  if constexpr (VARLEN) {
+    if (ok) {
+      tc_fence_after();
+      const size_t elem0 = (static_cast<size_t>(t0 + row0 + row) * H + hh) * D2;
+#pragma unroll 1
+      for (int cc = 2 * h; cc < 2 * h + 2; ++cc) {
+        uint32_t v[32];
+        tmem_ld_x32(t_acc + cc * 32, v);  // every lane loads (warp-wide); only rows < n store
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+        if (row0 + row < n) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(out) + (elem0 + cc * 32) * 2);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+    }
+    return;
+  }
   if (ok) {
     tc_fence_after();
 #pragma unroll 1
@@ -324,32 +374,43 @@ __device__ __forceinline__ void epilogue256(bool ok, const Cta& c, int off_ring,
 constexpr int kDvSlots = 5;
 using LayoutDv = Layout256<kDvSlots, 1, 16 * 128>;
 
-template <bool BF16>
+template <bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int NSLOT = kDvSlots;
   using L = LayoutDv;
   extern __shared__ uint8_t smem_raw[];
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles (of the longest sequence)
+  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_tk);
+  const int bh = wi.bh, k0 = wi.rank * kTileN;
+  const Lens q = lens_of<VARLEN>(a, bh);
+  if (VARLEN && k0 >= q.Nk) return;  // past the sequence's keys (whole CTA)
+  if (VARLEN && q.degenerate) {      // no softmax for this sequence: zero gradients
+    zero_rows256(a.dv_out, a.H, q.hh, q.tk0, k0, q.Nk);
+    return;
+  }
   Cta c;
   if (!cta_setup<L, NSLOT>(smem_raw, a.dev_status, c)) return;
   auto bar = [&](int i) -> uint32_t { return c.bars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_t = (a.N + kTileM - 1) / kTileM, n_tk = (a.Nk + kTileN - 1) / kTileN;
-  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_tk);
-  const int bh = wi.bh, k0 = wi.rank * kTileN;
-  const int i_begin = a.causal ? max(0, k0 - a.cofs) / kTileM : 0;
+  const int n_t = (q.N + kTileM - 1) / kTileM;
+  const int i_begin = a.causal ? max(0, k0 - q.cofs) / kTileM : 0;
   const int n_iter = n_t - i_begin;
+  auto qy = [&](int r) { return VARLEN ? q.hh : r; };  // TMA coordinates of query row r
+  auto qz = [&](int r) { return VARLEN ? q.tq0 + r : bh; };
   const WaitCtl wc{c.abort_flag, a.dev_status, a.wait_limit_ns};
   constexpr uint32_t TM_DV = 256;
 
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(bar(R_STAT), kTile);
-    for (int b = 0; b < 4; ++b) tma_load_3d(c.sb + L::OFF_ST + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, k0, bh);
+    for (int b = 0; b < 4; ++b)
+      tma_load_3d(c.sb + L::OFF_ST + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, VARLEN ? q.hh : k0,
+                  VARLEN ? q.tk0 + k0 : bh);
     Ring<NSLOT> r{c.sb + L::OFF_RING, c.bars};
-    bool ok = n_iter <= 0 || load_tile(r, &a.tm_q, i_begin * kTileM, bh, wc);
+    bool ok = n_iter <= 0 || load_tile(r, &a.tm_q, qy(i_begin * kTileM), qz(i_begin * kTileM), wc);
     for (int t = 0; ok && t < n_iter; ++t) {
       const int q0 = (i_begin + t) * kTileM;
-      if (t + 1 < n_iter) ok = load_tile(r, &a.tm_q, q0 + kTileM, bh, wc);
-      ok = ok && load_tile(r, &a.tm_do, q0, bh, wc);
+      if (t + 1 < n_iter) ok = load_tile(r, &a.tm_q, qy(q0 + kTileM), qz(q0 + kTileM), wc);
+      ok = ok && load_tile(r, &a.tm_do, qy(q0), qz(q0), wc);
     }
     producer_drain(r, bar(R_STAT), wc);
   } else if (warp == 1 && lane == 0) {
@@ -389,7 +450,7 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
         tmem_ld_x32(t_lane + col, sv);
         softmax_cols(sv, sl2, l4, 0.f, p);
       }
-      if (a.causal) mask_cols(p, k0 + row - a.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
+      if (a.causal) mask_cols(p, k0 + row - q.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
       uint32_t pk[kEwCols2 / 2];
 #pragma unroll
       for (int e = 0; e < kEwCols2; e += 2) pk[e / 2] = pack2<BF16>(p[e], p[e + 1]);
@@ -398,7 +459,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
       tc_fence_before();
       mbar_arrive(bar(R_PREADY + (t & 1)));
     }
-    epilogue256<BF16>(ok, c, L::OFF_RING, t_lane + TM_DV, row, h, 1.f, bar(R_DONE), wc, &a.tm_dv, k0, bh);
+    epilogue256<BF16, VARLEN>(ok, c, L::OFF_RING, t_lane + TM_DV, row, h, 1.f, bar(R_DONE), wc, &a.tm_dv, k0, bh,
+                              a.dv_out, a.H, q.hh, q.tk0, q.Nk);
   }
   teardown256(c.tmem);
 }
@@ -410,20 +472,29 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
 constexpr int kDkSlots = 3;
 using LayoutDk = Layout256<kDkSlots, 2, 16 * 128>;
 
-template <bool BF16>
+template <bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int NSLOT = kDkSlots;
   using L = LayoutDk;
   extern __shared__ uint8_t smem_raw[];
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;  // key tiles (of the longest sequence)
+  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_tk);
+  const int bh = wi.bh, k0 = wi.rank * kTileN;
+  const Lens q = lens_of<VARLEN>(a, bh);
+  if (VARLEN && k0 >= q.Nk) return;  // past the sequence's keys (whole CTA)
+  if (VARLEN && q.degenerate) {      // no softmax for this sequence: zero gradients
+    zero_rows256(a.dk_out, a.H, q.hh, q.tk0, k0, q.Nk);
+    return;
+  }
   Cta c;
   if (!cta_setup<L, NSLOT>(smem_raw, a.dev_status, c)) return;
   auto bar = [&](int i) -> uint32_t { return c.bars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_t = (a.N + kTileM - 1) / kTileM, n_tk = (a.Nk + kTileN - 1) / kTileN;
-  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_tk);
-  const int bh = wi.bh, k0 = wi.rank * kTileN;
-  const int i_begin = a.causal ? max(0, k0 - a.cofs) / kTileM : 0;
+  const int n_t = (q.N + kTileM - 1) / kTileM;
+  const int i_begin = a.causal ? max(0, k0 - q.cofs) / kTileM : 0;
   const int n_iter = n_t - i_begin;
+  auto qy = [&](int r) { return VARLEN ? q.hh : r; };  // TMA coordinates of query row r
+  auto qz = [&](int r) { return VARLEN ? q.tq0 + r : bh; };
   const WaitCtl wc{c.abort_flag, a.dev_status, a.wait_limit_ns};
   constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DK = 256;
   const uint32_t st_k = c.sb + L::OFF_ST, st_v = c.sb + L::OFF_ST + kTile;
@@ -431,17 +502,18 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(bar(R_STAT), 2 * kTile);
     for (int b = 0; b < 4; ++b) {
-      tma_load_3d(st_k + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, k0, bh);
-      tma_load_3d(st_v + b * kBlk, &a.tm_v, bar(R_STAT), 64 * b, k0, bh);
+      tma_load_3d(st_k + b * kBlk, &a.tm_k, bar(R_STAT), 64 * b, VARLEN ? q.hh : k0, VARLEN ? q.tk0 + k0 : bh);
+      tma_load_3d(st_v + b * kBlk, &a.tm_v, bar(R_STAT), 64 * b, VARLEN ? q.hh : k0, VARLEN ? q.tk0 + k0 : bh);
     }
     Ring<NSLOT> r{c.sb + L::OFF_RING, c.bars};
     const int q_first = i_begin * kTileM;
-    bool ok = n_iter <= 0 || (load_tile(r, &a.tm_q, q_first, bh, wc) && load_tile(r, &a.tm_do, q_first, bh, wc));
+    bool ok = n_iter <= 0 || (load_tile(r, &a.tm_q, qy(q_first), qz(q_first), wc) &&
+                              load_tile(r, &a.tm_do, qy(q_first), qz(q_first), wc));
     for (int t = 0; ok && t < n_iter; ++t) {
       const int q0 = (i_begin + t) * kTileM;
-      if (t + 1 < n_iter) ok = load_tile(r, &a.tm_q, q0 + kTileM, bh, wc);
-      ok = ok && load_tile(r, &a.tm_q, q0, bh, wc);
-      if (ok && t + 1 < n_iter) ok = load_tile(r, &a.tm_do, q0 + kTileM, bh, wc);
+      if (t + 1 < n_iter) ok = load_tile(r, &a.tm_q, qy(q0 + kTileM), qz(q0 + kTileM), wc);
+      ok = ok && load_tile(r, &a.tm_q, qy(q0), qz(q0), wc);
+      if (ok && t + 1 < n_iter) ok = load_tile(r, &a.tm_do, qy(q0 + kTileM), qz(q0 + kTileM), wc);
     }
     producer_drain(r, bar(R_STAT), wc);
   } else if (warp == 1 && lane == 0) {
@@ -488,7 +560,7 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
         mbar_arrive(bar(R_SREAD));
         softmax_cols(sv, sl2, l4, 0.f, p);
       }
-      if (a.causal) mask_cols(p, k0 + row - a.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
+      if (a.causal) mask_cols(p, k0 + row - q.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
       const float4* d4 = rs.put(my_d);
       if (!(ok = mbar_wait_warp(bar(R_DPFULL), t & 1, wc))) break;
       tc_fence_after();
@@ -514,7 +586,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       tc_fence_before();
       mbar_arrive(bar(R_DSREADY));
     }
-    epilogue256<BF16>(ok, c, L::OFF_RING, t_lane + TM_DK, row, h, a.scale, bar(R_DONE), wc, &a.tm_dk, k0, bh);
+    epilogue256<BF16, VARLEN>(ok, c, L::OFF_RING, t_lane + TM_DK, row, h, a.scale, bar(R_DONE), wc, &a.tm_dk, k0, bh,
+                              a.dk_out, a.H, q.hh, q.tk0, q.Nk);
   }
   teardown256(c.tmem);
 }
@@ -525,19 +598,27 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
 constexpr int kDqSlots = 3;
 using LayoutDq = Layout256<kDqSlots, 2, 0>;
 
-template <bool BF16>
+template <bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_constant__ BwdArgs a) {
   constexpr int NSLOT = kDqSlots;
   using L = LayoutDq;
   extern __shared__ uint8_t smem_raw[];
+  const int n_t = (a.N + kTileM - 1) / kTileM;  // query tiles (of the longest sequence)
+  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const int bh = wi.bh, qt = n_t - 1 - wi.rank, q0 = qt * kTileM;
+  const Lens q = lens_of<VARLEN>(a, bh);
+  if (VARLEN && q0 >= q.N) return;  // past the sequence's queries (whole CTA)
+  if (VARLEN && q.degenerate) {     // no softmax for this sequence: zero gradients
+    zero_rows256(a.dq_out, a.H, q.hh, q.tq0, q0, q.N);
+    return;
+  }
   Cta c;
   if (!cta_setup<L, NSLOT>(smem_raw, a.dev_status, c)) return;
   auto bar = [&](int i) -> uint32_t { return c.bars + 8u * i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_t = (a.N + kTileM - 1) / kTileM;
-  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_t);
-  const int bh = wi.bh, qt = n_t - 1 - wi.rank, q0 = qt * kTileM;
-  const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
+  const int n_kv = visible_key_tiles(qt, q.Nk, a.causal, q.cofs);
+  auto ky = [&](int r) { return VARLEN ? q.hh : r; };  // TMA coordinates of key row r
+  auto kz = [&](int r) { return VARLEN ? q.tk0 + r : bh; };
   const WaitCtl wc{c.abort_flag, a.dev_status, a.wait_limit_ns};
   constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 256;
   const uint32_t st_q = c.sb + L::OFF_ST, st_do = c.sb + L::OFF_ST + kTile;
@@ -545,16 +626,16 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
   if (warp == 0 && lane == 0) {
     mbar_arrive_expect_tx(bar(R_STAT), 2 * kTile);
     for (int b = 0; b < 4; ++b) {
-      tma_load_3d(st_q + b * kBlk, &a.tm_q, bar(R_STAT), 64 * b, q0, bh);
-      tma_load_3d(st_do + b * kBlk, &a.tm_do, bar(R_STAT), 64 * b, q0, bh);
+      tma_load_3d(st_q + b * kBlk, &a.tm_q, bar(R_STAT), 64 * b, VARLEN ? q.hh : q0, VARLEN ? q.tq0 + q0 : bh);
+      tma_load_3d(st_do + b * kBlk, &a.tm_do, bar(R_STAT), 64 * b, VARLEN ? q.hh : q0, VARLEN ? q.tq0 + q0 : bh);
     }
     Ring<NSLOT> r{c.sb + L::OFF_RING, c.bars};
-    bool ok = n_kv <= 0 || (load_tile(r, &a.tm_k, 0, bh, wc) && load_tile(r, &a.tm_v, 0, bh, wc));
+    bool ok = n_kv <= 0 || (load_tile(r, &a.tm_k, ky(0), kz(0), wc) && load_tile(r, &a.tm_v, ky(0), kz(0), wc));
     for (int j = 0; ok && j < n_kv; ++j) {
       const int kr = j * kTileN;
-      if (j + 1 < n_kv) ok = load_tile(r, &a.tm_k, kr + kTileN, bh, wc);
-      ok = ok && load_tile(r, &a.tm_k, kr, bh, wc);
-      if (ok && j + 1 < n_kv) ok = load_tile(r, &a.tm_v, kr + kTileN, bh, wc);
+      if (j + 1 < n_kv) ok = load_tile(r, &a.tm_k, ky(kr + kTileN), kz(kr + kTileN), wc);
+      ok = ok && load_tile(r, &a.tm_k, ky(kr), kz(kr), wc);
+      if (ok && j + 1 < n_kv) ok = load_tile(r, &a.tm_v, ky(kr + kTileN), kz(kr + kTileN), wc);
     }
     producer_drain(r, bar(R_STAT), wc);
   } else if (warp == 1 && lane == 0) {
@@ -599,8 +680,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
         softmax_cols(sv, sl2, nullptr, lse2, p);
       }
       const int kbeg = j * kTileN + kEwCols2 * h;
-      int lim = a.Nk - kbeg;                                     // keys past the end
-      if (a.causal) lim = min(lim, grow + a.cofs - kbeg + 1);  // keys after this query
+      int lim = q.Nk - kbeg;                                     // keys past the end
+      if (a.causal) lim = min(lim, grow + q.cofs - kbeg + 1);  // keys after this query
       mask_cols(p, 0, lim);
       if (!(ok = mbar_wait_warp(bar(R_DPFULL), j & 1, wc))) break;
       tc_fence_after();
@@ -622,7 +703,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
       tc_fence_before();
       mbar_arrive(bar(R_DSREADY));
     }
-    epilogue256<BF16>(ok, c, L::OFF_RING, t_lane + TM_DQ, row, h, a.scale, bar(R_DONE), wc, &a.tm_dq, q0, bh);
+    epilogue256<BF16, VARLEN>(ok, c, L::OFF_RING, t_lane + TM_DQ, row, h, a.scale, bar(R_DONE), wc, &a.tm_dq, q0, bh,
+                              a.dq_out, a.H, q.hh, q.tq0, q.N);
   }
   teardown256(c.tmem);
 }
@@ -637,19 +719,30 @@ cudaError_t launch256(K k, int smem, int grid, const BwdArgs& a, cudaStream_t st
 
 }  // namespace
 
-cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s) {
+template <bool VARLEN>
+cudaError_t launch_dkdv256_t(const BwdArgs& a, bool bf16, cudaStream_t s) {
   const int grid = (a.Nk + kTileN - 1) / kTileN * a.BH;
-  cudaError_t e = bf16 ? launch256(bwd256_dv_kernel<true>, LayoutDv::SMEM, grid, a, s)
-                       : launch256(bwd256_dv_kernel<false>, LayoutDv::SMEM, grid, a, s);
+  cudaError_t e = bf16 ? launch256(bwd256_dv_kernel<true, VARLEN>, LayoutDv::SMEM, grid, a, s)
+                       : launch256(bwd256_dv_kernel<false, VARLEN>, LayoutDv::SMEM, grid, a, s);
   if (e != cudaSuccess) return e;
-  return bf16 ? launch256(bwd256_dk_kernel<true>, LayoutDk::SMEM, grid, a, s)
-              : launch256(bwd256_dk_kernel<false>, LayoutDk::SMEM, grid, a, s);
+  return bf16 ? launch256(bwd256_dk_kernel<true, VARLEN>, LayoutDk::SMEM, grid, a, s)
+              : launch256(bwd256_dk_kernel<false, VARLEN>, LayoutDk::SMEM, grid, a, s);
 }
 
-cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s) {
+template <bool VARLEN>
+cudaError_t launch_dq256_t(const BwdArgs& a, bool bf16, cudaStream_t s) {
   const int grid = (a.N + kTileM - 1) / kTileM * a.BH;
-  return bf16 ? launch256(bwd256_dq_kernel<true>, LayoutDq::SMEM, grid, a, s)
-              : launch256(bwd256_dq_kernel<false>, LayoutDq::SMEM, grid, a, s);
+  return bf16 ? launch256(bwd256_dq_kernel<true, VARLEN>, LayoutDq::SMEM, grid, a, s)
+              : launch256(bwd256_dq_kernel<false, VARLEN>, LayoutDq::SMEM, grid, a, s);
+}
+
+cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s) { return launch_dkdv256_t<false>(a, bf16, s); }
+cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s) { return launch_dq256_t<false>(a, bf16, s); }
+cudaError_t launch_bwd256_dkdv_varlen(const BwdArgs& a, bool bf16, cudaStream_t s) {
+  return launch_dkdv256_t<true>(a, bf16, s);
+}
+cudaError_t launch_bwd256_dq_varlen(const BwdArgs& a, bool bf16, cudaStream_t s) {
+  return launch_dq256_t<true>(a, bf16, s);
 }
 
 }  // namespace attn

@@ -140,6 +140,7 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd256_varlen(const FwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_varlen(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
@@ -155,6 +156,8 @@ cudaError_t launch_bwd_grads(const BwdArgs& a, int d, bool bf16, cudaStream_t s)
 cudaError_t launch_bwd_grads_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s);  // d = 256: dV, then dK
 cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd256_dkdv_varlen(const BwdArgs& a, bool bf16, cudaStream_t s);
+cudaError_t launch_bwd256_dq_varlen(const BwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace attn

@@ -63,7 +63,10 @@ enum : int {
   F_COUNT = 11
 };
 
-template <bool BF16>
+// VARLEN: variable-length packed sequences ([tokens][H][d], offsets cu_q, cu_k), as in
+// fwd.cu: the CTA reads its sequence's token range, loads tiles at (column, head, token)
+// coordinates, masks with the sequence's own lengths and writes O rows with plain stores.
+template <bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_constant__ FwdArgs a) {
   using L = F256Layout;
   extern __shared__ uint8_t smem_raw[];
@@ -82,7 +85,45 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_t);
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tile first
-  const int n_kv = visible_key_tiles(qt, a.Nk, a.causal, a.cofs);
+  // Lengths and positions: the sequence's own (VARLEN), else the kernel parameters, read
+  // through accessors so that the plain kernel keeps using the parameters directly.
+  int vN = 0, vNk = 0, vcofs = 0, hh = 0, tq0 = 0, tk0 = 0;
+  if constexpr (VARLEN) {
+    const SeqView sv = seq_view(a, bh);
+    vN = sv.N;
+    vNk = sv.Nk;
+    vcofs = sv.cofs;
+    hh = sv.hh;
+    tq0 = sv.tq0;
+    tk0 = sv.tk0;
+    const int N = vN;
+    if (qt * kTileM >= N) return;  // this tile lies past the sequence's end (whole CTA)
+    if (sv.degenerate) {           // no key, or causal rows that would see none: O = 0, lse = -inf
+      for (int r = threadIdx.x; r < kTileM; r += blockDim.x) {
+        const int gr = qt * kTileM + r;
+        if (gr >= N) continue;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) + ((static_cast<size_t>(tq0 + gr) * a.H + hh) * D256) * 2);
+        for (int c = 0; c < D256 / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+        a.lse[static_cast<size_t>(hh) * a.Tq + tq0 + gr] = -INFINITY;
+      }
+      return;
+    }
+  }
+  auto N_ = [&]() -> int {
+    if constexpr (VARLEN) return vN; else return a.N;
+  };
+  auto Nk_ = [&]() -> int {
+    if constexpr (VARLEN) return vNk; else return a.Nk;
+  };
+  auto cofs_ = [&]() -> int {
+    if constexpr (VARLEN) return vcofs; else return a.cofs;
+  };
+  const int n_kv = visible_key_tiles(qt, Nk_(), a.causal, cofs_());
+  // TMA coordinates of row r of Q (or K, V): (row, head-batch) or, packed, (head, token)
+  auto qy = [&](int r) { return VARLEN ? hh : r; };
+  auto qz = [&](int r) { return VARLEN ? tq0 + r : bh; };
+  auto ky = [&](int r) { return VARLEN ? hh : r; };
+  auto kz = [&](int r) { return VARLEN ? tk0 + r : bh; };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(F_Q), 1);
@@ -119,7 +160,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     prefetch_tmap(&a.tm_o);
     mbar_arrive_expect_tx(bar(F_Q), L::TILE);
     for (int kb = 0; kb < L::KB; ++kb)
-      tma_load_3d(sb + L::OFF_Q + kb * L::BLK, &a.tm_q, bar(F_Q), kb * 64, qt * kTileM, bh);
+      tma_load_3d(sb + L::OFF_Q + kb * L::BLK, &a.tm_q, bar(F_Q), kb * 64, qy(qt * kTileM), qz(qt * kTileM));
     int c = 0;
     bool ok = true;
     auto load = [&](const CUtensorMap* m, int tile) {
@@ -127,7 +168,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       if (c >= 2 && !(ok = mbar_wait(bar(F_KVEMPTY + s), ((c >> 1) - 1) & 1, wc))) return;
       mbar_arrive_expect_tx(bar(F_KVFULL + s), L::TILE);
       for (int kb = 0; kb < L::KB; ++kb)
-        tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(F_KVFULL + s), kb * 64, tile * kTileN, bh);
+        tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(F_KVFULL + s), kb * 64, ky(tile * kTileN),
+                    kz(tile * kTileN));
       ++c;
     };
     load(&a.tm_k, 0);
@@ -215,11 +257,11 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
         for (int cc = 0; cc < 128; ++cc) s[cc] = __uint_as_float(sr[cc]);
       }
       const int k0 = j * kTileN;
-      const bool tail = k0 + kTileN > a.Nk;
-      const bool diag = a.causal && (k0 + kTileN - 1 > qt * kTileM + a.cofs);
+      const bool tail = k0 + kTileN > Nk_();
+      const bool diag = a.causal && (k0 + kTileN - 1 > qt * kTileM + cofs_());
       if (tail || diag) {
-        int lim = a.Nk - k0;                                   // keys past the end of the sequence
-        if (a.causal) lim = min(lim, grow + a.cofs - k0 + 1);  // keys after this query
+        int lim = Nk_() - k0;                                   // keys past the end of the sequence
+        if (a.causal) lim = min(lim, grow + cofs_() - k0 + 1);  // keys after this query
 #pragma unroll
         for (int cc = 0; cc < kTileN; ++cc)
           if (cc >= lim) s[cc] = -INFINITY;
@@ -292,20 +334,31 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pkd[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l, __uint_as_float(o[2 * e + 1]) * inv_l);
-        const int kb = (cc * 32) / 64;
+        if constexpr (VARLEN) {  // this row of this sequence, straight to global memory
+          if (grow < N_()) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) +
+                                                  ((static_cast<size_t>(tq0 + grow) * a.H + hh) * D256 + cc * 32) * 2);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int ch = ((cc * 32) % 64) / 8 + q;
-          uint4* dst = reinterpret_cast<uint4*>(stage + kb * L::BLK + row * 128 + ((ch ^ (row & 7)) << 4));
-          *dst = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
+          }
+        } else {
+          const int kb = (cc * 32) / 64;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int ch = ((cc * 32) % 64) / 8 + q;
+            uint4* dst = reinterpret_cast<uint4*>(stage + kb * L::BLK + row * 128 + ((ch ^ (row & 7)) << 4));
+            *dst = make_uint4(pkd[4 * q], pkd[4 * q + 1], pkd[4 * q + 2], pkd[4 * q + 3]);
+          }
         }
       }
-      if (grow < a.N)  // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
-        a.lse[static_cast<size_t>(bh) * a.N + grow] = ((m == -INFINITY ? 0.f : m) + __log2f(l)) * 0.69314718055994531f;
+      if (grow < N_()) {  // natural-log logsumexp of the scaled scores: (m + log2 l) * ln 2
+        const size_t li = VARLEN ? static_cast<size_t>(hh) * a.Tq + tq0 + grow : static_cast<size_t>(bh) * a.N + grow;
+        a.lse[li] = ((m == -INFINITY ? 0.f : m) + __log2f(l)) * 0.69314718055994531f;
+      }
       fence_proxy_async_smem();
     }
     named_bar_sync(1, 128);
-    if (warp == 4 && lane == 0 && ok && !*abort_flag) {
+    if (!VARLEN && warp == 4 && lane == 0 && ok && !*abort_flag) {
       for (int kb = 0; kb < L::KB; ++kb) tma_store_3d(&a.tm_o, sb + L::OFF_Q + kb * L::BLK, kb * 64, qt * kTileM, bh);
       bulk_commit();
       bulk_wait_read_all();
@@ -320,9 +373,9 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool VARLEN = false>
 cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t st) {
-  auto k = fwd256_kernel<BF16>;
+  auto k = fwd256_kernel<BF16, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F256Layout::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -334,6 +387,10 @@ cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t st) {
 
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s) {
   return bf16 ? launch_fwd256_t<true>(a, s) : launch_fwd256_t<false>(a, s);
+}
+
+cudaError_t launch_fwd256_varlen(const FwdArgs& a, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_fwd256_t<true, true>(a, s) : launch_fwd256_t<false, true>(a, s);
 }
 
 }  // namespace attn
