@@ -416,7 +416,8 @@ def dropout_step(attn, dev):
 
 def d256_side(attn, dev):
     """Head dimension 256: B=1, H=16, N=16384, bf16, both masks; the forward alone (one
-    query tile per CTA) and the training step (forward + the three-kernel backward)."""
+    query tile per CTA) and the training step (forward + the three-kernel backward); the
+    causal step again with dropout p = 0.1 (FLOPs counted as without dropout)."""
     B, H, N, d = 1, 16, 16384, 256
     x = workloads.draw(B, H, N, d, "bf16", seed=13, with_dout=True)
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
@@ -452,6 +453,14 @@ def d256_side(attn, dev):
         out["causal" if causal else "non_causal"] = {
             "ms": round(ms, 4), "tflops": round(ff / (ms * 1e-3) / 1e12, 1),
             "step_ms": round(ms_step, 4), "step_tflops": round(fs / (ms_step * 1e-3) / 1e12, 1)}
+        if causal:
+            def step_drop():
+                attn.attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, q.dtype, True, scale, 0.1, 1234)
+                attn.attn_bwd_dropout(q, k, v, o, do, lse, dq, dk, dv, ws, nb, B, H, N, d, q.dtype, True, scale,
+                                      0.1, 1234)
+            ms_drop = timed(step_drop, 5)
+            out["causal"]["dropout_p0.1_step_ms"] = round(ms_drop, 4)
+            out["causal"]["dropout_p0.1_step_tflops"] = round(fs / (ms_drop * 1e-3) / 1e12, 1)
     return out
 
 

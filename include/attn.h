@@ -142,7 +142,7 @@ ATTN_API attn_status attn_bwd_varlen(const void *q, const void *k, const void *v
  *   O = (P o Z) V with Z = keep * 256 / (256 - t); lse is the logsumexp of the
  *   scores, as without dropout.  The backward must get the same p_drop and seed:
  *   dV = (P o Z)^T dO, dS = P o (Z o dP - D), D_i = rowsum(dO_i o O_i).
- * d in {64, 128}; square shapes.  Everything else is as for attn_fwd / attn_bwd.
+ * d in {64, 128, 256}; square shapes.  Everything else is as for attn_fwd / attn_bwd.
  * p_drop = 0 runs the plain kernels.
  */
 ATTN_API attn_status attn_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -192,7 +192,7 @@ def test_dropout_validates():
     for kw, st in [(dict(p_drop=1.0), attn.ATTN_ERR_INVALID_ARG), (dict(p_drop=-0.1), attn.ATTN_ERR_INVALID_ARG),
                    (dict(p_drop=float("nan")), attn.ATTN_ERR_INVALID_ARG),
                    (dict(p_drop=0.999), attn.ATTN_ERR_INVALID_ARG),      # round(256 p) = 256
-                   (dict(d=256), attn.ATTN_ERR_UNSUPPORTED), (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(d=192), attn.ATTN_ERR_UNSUPPORTED), (dict(d=96), attn.ATTN_ERR_UNSUPPORTED),
                    (dict(o=A[0]), attn.ATTN_ERR_INVALID_ARG)]:
         a2 = dict(fa)
         a2.update(kw)
@@ -200,7 +200,7 @@ def test_dropout_validates():
     ba = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8], workspace=A[9],
               workspace_bytes=1 << 20, B=1, H=2, N=256, d=128, dt=0, causal=1, scale=0.088, p_drop=0.1, seed=7,
               stream=0)
-    for kw, st in [(dict(p_drop=1.5), attn.ATTN_ERR_INVALID_ARG), (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+    for kw, st in [(dict(p_drop=1.5), attn.ATTN_ERR_INVALID_ARG), (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
                    (dict(dq=A[7]), attn.ATTN_ERR_INVALID_ARG)]:
         a2 = dict(ba)
         a2.update(kw)

@@ -128,13 +128,19 @@ def test_bwd256_autograd():
     check((q.grad, k.grad, v.grad), refs, "autograd")
 
 
-def test_bwd256_dropout_unsupported():
-    x = workloads.draw(1, 1, 128, D, "bf16", seed=1, with_dout=True)
+def test_bwd256_dropout_zero_is_plain():
+    """attn_bwd_dropout with p_drop = 0 gives attn_bwd's bytes at d = 256."""
+    x = workloads.draw(1, 2, 300, D, "bf16", seed=1, with_dout=True)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
-    o, lse = run_fwd(q, k, v, False)
-    nbytes = attn.attn_bwd_workspace_bytes(1, 1, 128, D)
+    o, lse = run_fwd(q, k, v, True)
+    nbytes = attn.attn_bwd_workspace_bytes(1, 2, 300, D)
     ws = torch.empty(nbytes // 4, dtype=torch.float32, device="cuda")
     g = [torch.empty_like(q) for _ in range(3)]
-    rc = attn.attn_bwd_dropout(q, k, v, o, do, lse, g[0], g[1], g[2], ws, nbytes, 1, 1, 128, D, q.dtype, 0,
-                               1 / 16, 0.1, 5)
-    assert rc == attn.ATTN_ERR_UNSUPPORTED
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_bwd_dropout(q, k, v, o, do, lse, g[0], g[1], g[2], ws, nbytes, 1, 2, 300, D, q.dtype, 1,
+                               1 / 16, 0.0, 5, status)
+    assert rc == attn.ATTN_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for a, b in zip(g, run_bwd(q, k, v, o, lse, do, True, 1 / 16)):
+        assert torch.equal(a, b)

@@ -50,7 +50,7 @@ def run_bwd_drop(q, k, v, o, lse, do, causal, scale, p, seed):
 
 
 @pytest.mark.parametrize("p", [0.1, 0.5])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [1, 127, 128, 129, 300, 513])
 def test_dropout_fwd_bwd(N, causal, d, p):
@@ -95,11 +95,12 @@ def test_dropout_fp16_and_bf16(dtype):
         assert grad_err(gg, rr) <= GRAD_REL_L2
 
 
-def test_dropout_mask_exact():
+@pytest.mark.parametrize("d", [128, 256])
+def test_dropout_mask_exact(d):
     """Q = 0 makes every visible probability 1/n; with V_j the unit vector e_j, O_ij * n is
     exactly the keep factor Z_ij of key j < d: the GPU's mask equals the oracle's, bit for bit
     of the keep decision."""
-    B, H, N, d = 1, 3, 128, 128
+    B, H, N = 1, 3, d
     for causal in (False, True):
         q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
         k = torch.randn((B, H, N, d), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
@@ -119,6 +120,34 @@ def test_dropout_mask_exact():
                     kept += zref > 0
         total = H * (N * (N + 1) // 2 if causal else N * N)
         assert abs(1 - kept / total - t / 256) < 0.02
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_dropout_dv_mask_exact(d):
+    """The backward's keep mask, read through dV = (P o Z)^T dO: with Q = 0 every visible
+    probability is 1/n_i, and with dO_i the unit vector e_i, dV_ji * n_i is the keep factor
+    Z_ij.  The key-tile kernels hold the mask by key (a transposed draw), so this checks
+    that transposition against the oracle's keep decisions."""
+    B, H, N = 1, 2, d
+    for causal in (False, True):
+        q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+        k = torch.randn((B, H, N, d), generator=torch.Generator().manual_seed(6)).to(torch.bfloat16).cuda()
+        v = torch.randn((B, H, N, d), generator=torch.Generator().manual_seed(7)).to(torch.bfloat16).cuda()
+        do = torch.eye(d, dtype=torch.bfloat16).expand(B, H, N, d).contiguous().cuda()
+        p, seed = 0.3, 0x1234567890
+        t = t_of(p)
+        o, lse = run_fwd_drop(q, k, v, causal, 0.1, p, seed)
+        _, _, dv = run_bwd_drop(q, k, v, o, lse, do, causal, 0.1, p, seed)
+        dv = f64(dv)
+        for h in range(H):
+            for i in range(N):
+                n = i + 1 if causal else N
+                for j in range(n):
+                    zref = oracle.default().dropout_factor(h, i, j, t, seed)
+                    assert (dv[0, h, j, i] * n > 0) == (zref > 0), \
+                        f"backward keep decision differs at head {h}, query {i}, key {j}"
+                for j in range(n, N):
+                    assert dv[0, h, j, i] == 0, f"masked key {j} of query {i} has a dV entry"
 
 
 def test_dropout_zero_is_plain_and_seeds_differ():
@@ -155,3 +184,28 @@ def test_dropout_training_step_sampled():
                              ("dV", f64(dv[b, h])[rows], rv)):
             e = grad_err(gg, rr)
             assert e <= GRAD_REL_L2, f"head ({b},{h}) {name} relative L2 {e:.3e}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_d256_long_sampled(causal):
+    """d = 256, B=1, H=4, N=4096, p = 0.1: sampled query rows (O, LSE, dQ) and key rows
+    (dK, dV) of two heads."""
+    B, H, N, d = 1, 4, 4096, 256
+    x = workloads.draw(B, H, N, d, "bf16", seed=43, with_dout=True)
+    scale = 1.0 / math.sqrt(d)
+    p, seed = 0.1, 0xD256
+    t = t_of(p)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = run_fwd_drop(q, k, v, causal, scale, p, seed)
+    dq, dk, dv = run_bwd_drop(q, k, v, o, lse, do, causal, scale, p, seed)
+    rows = sample_rows(N, extra=8, seed=4)
+    for h in (0, 3):
+        qb, kb, vb, dob = (x[n][0, h] for n in ("q", "k", "v", "dout"))
+        ro, rl = oracle.attn_fwd_dropout(qb, kb, vb, causal, scale, t, seed, rows=rows, bh0=h)
+        assert o_err(o[0, h], ro, rows) <= O_MAX_ABS * 256 / (256 - t)
+        assert float(np.max(np.abs(f64(lse[0, h])[rows] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+        rq, rk, rv = oracle.attn_bwd_dropout(qb, kb, vb, dob, causal, scale, t, seed, qrows=rows, kcols=rows, bh0=h)
+        for name, gg, rr in (("dQ", f64(dq[0, h])[rows], rq), ("dK", f64(dk[0, h])[rows], rk),
+                             ("dV", f64(dv[0, h])[rows], rv)):
+            e = grad_err(gg, rr)
+            assert e <= GRAD_REL_L2, f"head {h} {name} relative L2 {e:.3e}"

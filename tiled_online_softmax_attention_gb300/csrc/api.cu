@@ -119,7 +119,8 @@ void set_dropout(Args& a, const Dropout& dr) {
 }
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// d = 256 is accepted only where the caller says so (the forward).  Nk = key length.
+// d = 256 is accepted only where the caller says so (all but the FP8 and split-KV
+// forwards).  Nk = key length.
 attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale, bool allow_d256 = false,
                         int Nk = -1) {
   if (Nk < 0) Nk = N;
@@ -171,7 +172,7 @@ namespace {
 attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int Nk,
                      int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
                      const Dropout& dr = Dropout{}) {
-  attn_status st = check_sizes(B, H, N, d, dt, scale, dr.t == 0, Nk);
+  attn_status st = check_sizes(B, H, N, d, dt, scale, true, Nk);
   if (st != ATTN_OK) return st;
   if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -467,7 +468,6 @@ attn_status prepare_impl(const void* o, const void* dout, const float* lse, void
 attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                       size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
                       int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
-  if (d == 256 && dr.t > 0) return ATTN_ERR_UNSUPPORTED;  // d = 256 kernels have no dropout
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
                              workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
@@ -491,7 +491,6 @@ attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* d
 attn_status dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
                     size_t workspace_bytes, void* dq, int B, int H, int N, int Nk, int d, attn_dtype dt, int causal,
                     float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
-  if (d == 256 && dr.t > 0) return ATTN_ERR_UNSUPPORTED;  // d = 256 kernels have no dropout
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dq, qb}}, workspace,
                              workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
@@ -516,7 +515,6 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
                      const Dropout& dr = Dropout{}) {
-  if (d == 256 && dr.t > 0) return ATTN_ERR_UNSUPPORTED;  // d = 256 kernels have no dropout
   if (!lse) return ATTN_ERR_INVALID_ARG;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},

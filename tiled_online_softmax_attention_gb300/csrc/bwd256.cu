@@ -26,6 +26,11 @@
 //
 // Warp roles as in bwd.cu: warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2-3 idle,
 // four element-wise warpgroups of 32 columns each.  Every wait is bounded.
+//
+// DROP (dropout, the forward's keep rule, Z = keep * 256 / (256 - t)): dV = (P o Z)^T dO
+// and dS = P o (Z o dP - D), as in bwd.cu.  The key-tile kernels need the keep bits by
+// key row: each lane draws one query's 32 keep bytes and 32 warp ballots transpose the
+// 32 x 32 bit block, so no shared memory is spent on it.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -298,6 +303,39 @@ __device__ __forceinline__ void softmax_cols(const uint32_t (&sv)[kEwCols2], flo
   }
 }
 
+// Dropout keep bits, key-tile kernels: for this thread's key k_base + lane (k_base a
+// multiple of 16; all 32 lanes call it together), bit c set iff query q_base + c keeps
+// it.  Lane L draws query q_base + L's bits over the warp's 32 keys; ballot c collects
+// key c's bits over the 32 queries and lane c keeps it.
+__device__ __forceinline__ uint32_t keep_bits_by_key(const BwdArgs& a, int bh, int q_base, int k_base) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t jg = static_cast<uint32_t>(k_base / 16), qi = static_cast<uint32_t>(q_base + lane);
+  const uint32_t mine = dropout_keep16(jg, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) |
+                        (dropout_keep16(jg + 1, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) << 16);
+  uint32_t bits = 0;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const uint32_t b = __ballot_sync(0xffffffffu, (mine >> c) & 1u);
+    if (lane == c) bits = b;
+  }
+  return bits;
+}
+
+// Dropout keep bits, query-tile kernel: bit e set iff query i keeps key k_base + e.
+__device__ __forceinline__ uint32_t keep_bits_by_query(const BwdArgs& a, int bh, int i, int k_base) {
+  const uint32_t jg = static_cast<uint32_t>(k_base / 16);
+  return dropout_keep16(jg, static_cast<uint32_t>(i), static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) |
+         (dropout_keep16(jg + 1, static_cast<uint32_t>(i), static_cast<uint32_t>(bh), a.drop_t, a.seed_lo,
+                         a.seed_hi) << 16);
+}
+
+// dP <- Z o dP over this thread's 32 columns (bit e of keep: column e kept).
+__device__ __forceinline__ void drop_scale_cols(uint32_t (&dv)[kEwCols2], uint32_t keep, float zs) {
+#pragma unroll
+  for (int e = 0; e < kEwCols2; ++e)
+    dv[e] = __float_as_uint(((keep >> e) & 1u) ? __uint_as_float(dv[e]) * zs : 0.f);
+}
+
 // Zero p[e] for e < lo and for e >= hi (the masked columns).
 __device__ __forceinline__ void mask_cols(float (&p)[kEwCols2], int lo, int hi) {
   if (lo > 0 || hi < kEwCols2) {
@@ -374,8 +412,9 @@ __device__ __forceinline__ void epilogue256(bool ok, const Cta& c, int off_ring,
 constexpr int kDvSlots = 5;
 using LayoutDv = Layout256<kDvSlots, 1, 16 * 128>;
 
-template <bool BF16, bool VARLEN>
+template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_constant__ BwdArgs a) {
+  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   constexpr int NSLOT = kDvSlots;
   using L = LayoutDv;
   extern __shared__ uint8_t smem_raw[];
@@ -441,6 +480,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
       const int qt = i_begin + t;
       const uint32_t col = 128u * (t & 1) + kEwCols2 * h;
       const float my_l = a.lse2[static_cast<size_t>(bh) * a.Npad + qt * kTileM + kEwCols2 * h + lane];
+      uint32_t keep = 0xffffffffu;  // bit c: query column c keeps this key
+      if constexpr (DROP) keep = keep_bits_by_key(a, bh, qt * kTileM + kEwCols2 * h, k0 + 32 * wq);
       if (!(ok = mbar_wait_warp(bar(R_SFULL + (t & 1)), (t >> 1) & 1, wc))) break;
       tc_fence_after();
       const float4* l4 = rs.put(my_l);
@@ -452,8 +493,15 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
       }
       if (a.causal) mask_cols(p, k0 + row - q.cofs - qt * kTileM - kEwCols2 * h, kEwCols2);
       uint32_t pk[kEwCols2 / 2];
+      if constexpr (DROP) {  // dV takes P o Z
+        const float zs = a.drop_scale;
 #pragma unroll
-      for (int e = 0; e < kEwCols2; e += 2) pk[e / 2] = pack2<BF16>(p[e], p[e + 1]);
+        for (int e = 0; e < kEwCols2; e += 2)
+          pk[e / 2] = pack2<BF16>(((keep >> e) & 1u) ? p[e] * zs : 0.f, ((keep >> (e + 1)) & 1u) ? p[e + 1] * zs : 0.f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < kEwCols2; e += 2) pk[e / 2] = pack2<BF16>(p[e], p[e + 1]);
+      }
       tmem_st_x16(t_lane + col, pk);  // over columns this thread has read
       tmem_st_wait();
       tc_fence_before();
@@ -472,8 +520,9 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
 constexpr int kDkSlots = 3;
 using LayoutDk = Layout256<kDkSlots, 2, 16 * 128>;
 
-template <bool BF16, bool VARLEN>
+template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_constant__ BwdArgs a) {
+  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   constexpr int NSLOT = kDkSlots;
   using L = LayoutDk;
   extern __shared__ uint8_t smem_raw[];
@@ -549,6 +598,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       const int qt = i_begin + t;
       const size_t wrow = static_cast<size_t>(bh) * a.Npad + qt * kTileM + kEwCols2 * h + lane;
       const float my_l = a.lse2[wrow], my_d = a.delta[wrow];
+      uint32_t keep = 0xffffffffu;  // bit c: query column c keeps this key
+      if constexpr (DROP) keep = keep_bits_by_key(a, bh, qt * kTileM + kEwCols2 * h, k0 + 32 * wq);
       if (!(ok = mbar_wait_warp(bar(R_SFULL), t & 1, wc))) break;
       tc_fence_after();
       float p[kEwCols2];
@@ -567,6 +618,7 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       {
         uint32_t dv[kEwCols2], ds[kEwCols2 / 2];
         tmem_ld_x32(t_lane + TM_DP + kEwCols2 * h, dv);
+        if constexpr (DROP) drop_scale_cols(dv, keep, a.drop_scale);
 #pragma unroll
         for (int v = 0; v < kEwCols2 / 4; ++v) {  // paired sub and mul, two columns each
           const float4 dd = d4[v];
@@ -598,8 +650,9 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
 constexpr int kDqSlots = 3;
 using LayoutDq = Layout256<kDqSlots, 2, 0>;
 
-template <bool BF16, bool VARLEN>
+template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_constant__ BwdArgs a) {
+  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   constexpr int NSLOT = kDqSlots;
   using L = LayoutDq;
   extern __shared__ uint8_t smem_raw[];
@@ -669,6 +722,8 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
     const float lse2 = a.lse2[w], dlt = a.delta[w];
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
+      uint32_t keep = 0xffffffffu;  // bit e: this query keeps key column e
+      if constexpr (DROP) keep = keep_bits_by_query(a, bh, grow, j * kTileN + kEwCols2 * h);
       if (!(ok = mbar_wait_warp(bar(R_SFULL), j & 1, wc))) break;
       tc_fence_after();
       float p[kEwCols2];
@@ -688,6 +743,7 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
       {
         uint32_t dv[kEwCols2], ds[kEwCols2 / 2];
         tmem_ld_x32(t_lane + TM_DP + kEwCols2 * h, dv);
+        if constexpr (DROP) drop_scale_cols(dv, keep, a.drop_scale);
         const uint64_t dlt2 = f32x2_pack(dlt, dlt);
 #pragma unroll
         for (int e = 0; e < kEwCols2; e += 2) {  // paired sub and mul
@@ -719,25 +775,30 @@ cudaError_t launch256(K k, int smem, int grid, const BwdArgs& a, cudaStream_t st
 
 }  // namespace
 
-template <bool VARLEN>
+template <bool VARLEN, bool DROP = false>
 cudaError_t launch_dkdv256_t(const BwdArgs& a, bool bf16, cudaStream_t s) {
   const int grid = (a.Nk + kTileN - 1) / kTileN * a.BH;
-  cudaError_t e = bf16 ? launch256(bwd256_dv_kernel<true, VARLEN>, LayoutDv::SMEM, grid, a, s)
-                       : launch256(bwd256_dv_kernel<false, VARLEN>, LayoutDv::SMEM, grid, a, s);
+  cudaError_t e = bf16 ? launch256(bwd256_dv_kernel<true, VARLEN, DROP>, LayoutDv::SMEM, grid, a, s)
+                       : launch256(bwd256_dv_kernel<false, VARLEN, DROP>, LayoutDv::SMEM, grid, a, s);
   if (e != cudaSuccess) return e;
-  return bf16 ? launch256(bwd256_dk_kernel<true, VARLEN>, LayoutDk::SMEM, grid, a, s)
-              : launch256(bwd256_dk_kernel<false, VARLEN>, LayoutDk::SMEM, grid, a, s);
+  return bf16 ? launch256(bwd256_dk_kernel<true, VARLEN, DROP>, LayoutDk::SMEM, grid, a, s)
+              : launch256(bwd256_dk_kernel<false, VARLEN, DROP>, LayoutDk::SMEM, grid, a, s);
 }
 
-template <bool VARLEN>
+template <bool VARLEN, bool DROP = false>
 cudaError_t launch_dq256_t(const BwdArgs& a, bool bf16, cudaStream_t s) {
   const int grid = (a.N + kTileM - 1) / kTileM * a.BH;
-  return bf16 ? launch256(bwd256_dq_kernel<true, VARLEN>, LayoutDq::SMEM, grid, a, s)
-              : launch256(bwd256_dq_kernel<false, VARLEN>, LayoutDq::SMEM, grid, a, s);
+  return bf16 ? launch256(bwd256_dq_kernel<true, VARLEN, DROP>, LayoutDq::SMEM, grid, a, s)
+              : launch256(bwd256_dq_kernel<false, VARLEN, DROP>, LayoutDq::SMEM, grid, a, s);
 }
 
-cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s) { return launch_dkdv256_t<false>(a, bf16, s); }
-cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s) { return launch_dq256_t<false>(a, bf16, s); }
+// a.drop_t > 0 selects the dropout kernels.
+cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s) {
+  return a.drop_t > 0 ? launch_dkdv256_t<false, true>(a, bf16, s) : launch_dkdv256_t<false>(a, bf16, s);
+}
+cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s) {
+  return a.drop_t > 0 ? launch_dq256_t<false, true>(a, bf16, s) : launch_dq256_t<false>(a, bf16, s);
+}
 cudaError_t launch_bwd256_dkdv_varlen(const BwdArgs& a, bool bf16, cudaStream_t s) {
   return launch_dkdv256_t<true>(a, bf16, s);
 }

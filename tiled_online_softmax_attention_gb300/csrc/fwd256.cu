@@ -66,8 +66,12 @@ enum : int {
 // VARLEN: variable-length packed sequences ([tokens][H][d], offsets cu_q, cu_k), as in
 // fwd.cu: the CTA reads its sequence's token range, loads tiles at (column, head, token)
 // coordinates, masks with the sequence's own lengths and writes O rows with plain stores.
-template <bool BF16, bool VARLEN>
+// DROP: dropout on the probabilities with fwd.cu's keep rule (key j of query i in head bh
+// kept iff byte j % 16 of Philox((j / 16, i, bh, 0), seed) is >= drop_t); l sums every
+// probability and the kept ones are scaled by drop_scale at the end.
+template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_constant__ FwdArgs a) {
+  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = F256Layout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -245,6 +249,20 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int buf = j & 1;
+      // Keep masks of this row's 128 keys, drawn while S is being computed: keep[g][q]
+      // has 0xFF in byte b if key 16g + 4q + b is kept.
+      uint32_t keep[8][4];
+      if constexpr (DROP) {
+        const uint32_t tt = a.drop_t * 0x01010101u;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint32_t w[4];
+          philox4x32_10(static_cast<uint32_t>(j * (kTileN / 16) + g), static_cast<uint32_t>(grow),
+                        static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) keep[g][q] = __vcmpgeu4(w[q], tt);
+        }
+      }
       if (!mbar_wait_warp(bar(F_SFULL + buf), (j >> 1) & 1, wc)) { ok = false; break; }
       tc_fence_after();
       float s[128];
@@ -302,6 +320,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
         const float p1 = ex2(x1);
         acc2[(cc / 2) & 1] = f32x2_add(acc2[(cc / 2) & 1], f32x2_pack(p0, p1));
         pk[cc / 2] = pack2<BF16>(p0, p1);
+        if constexpr (DROP)  // both 16-bit halves: all ones if kept, zero if dropped
+          pk[cc / 2] &= __byte_perm(keep[cc / 16][(cc % 16) / 4], 0u, (cc % 4) ? 0x3322u : 0x1100u);
       }
       float rs;
       {
@@ -324,7 +344,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     ok = ok && mbar_wait_warp(bar(F_DRAIN), 0, wc);
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
+      const float inv_l = (DROP ? a.drop_scale : 1.f) / l;
       uint8_t* stage = smem + L::OFF_Q;  // every S product has read Q by now
 #pragma unroll 1
       for (int cc = 0; cc < D256 / 32; ++cc) {
@@ -373,9 +393,9 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   }
 }
 
-template <bool BF16, bool VARLEN = false>
+template <bool BF16, bool VARLEN = false, bool DROP = false>
 cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t st) {
-  auto k = fwd256_kernel<BF16, VARLEN>;
+  auto k = fwd256_kernel<BF16, VARLEN, DROP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F256Layout::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
@@ -385,7 +405,9 @@ cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+// a.drop_t > 0 selects the dropout kernel.
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s) {
+  if (a.drop_t > 0) return bf16 ? launch_fwd256_t<true, false, true>(a, s) : launch_fwd256_t<false, false, true>(a, s);
   return bf16 ? launch_fwd256_t<true>(a, s) : launch_fwd256_t<false>(a, s);
 }
 
