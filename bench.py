@@ -376,6 +376,7 @@ def long_forward(attn, dev):
     res = {"long_forward_B1_H32_N16384_d128": out}
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
     res["decode_B1_H32_Nq128_Nk32768_d128"] = decode_forward(attn, dev)
+    res["decode_B1_H16_Nq128_Nk32768_d256"] = decode_forward(attn, dev, 16, 256)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     res["d256_forward_and_step_B1_H16_N16384"] = d256_side(attn, dev)
@@ -575,12 +576,13 @@ def split_forward(attn, dev):
     return out
 
 
-def decode_forward(attn, dev):
-    """Decode-like shape: B=1, H=32, 128 new queries against 32768 keys (causal: the
-    queries are the last 128 positions), d=128.  attn_fwd_rect has one query-tile pair
-    per head (32 CTAs); attn_fwd_splitkv_rect cuts the keys into ranges.  FLOPs: two
-    Nq x Nk x d products (causal: the visible part, the last 128 rows of the triangle)."""
-    B, H, Nq, Nk, d = 1, 32, 128, 32768, 128
+def decode_forward(attn, dev, H=32, d=128):
+    """Decode-like shape: B=1, H heads, 128 new queries against 32768 keys (causal: the
+    queries are the last 128 positions), head dimension d.  attn_fwd_rect has one CTA per
+    head (a query-tile pair at d <= 128, one query tile at d = 256);
+    attn_fwd_splitkv_rect cuts the keys into ranges.  FLOPs: two Nq x Nk x d products
+    (causal: the visible part, the last 128 rows of the triangle)."""
+    B, Nq, Nk = 1, 128, 32768
     g = torch.Generator().manual_seed(17)
     q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(dev)
     k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(dev)

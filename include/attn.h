@@ -25,9 +25,9 @@
  *    Every base pointer must be 16-byte aligned.  The caller owns all memory;
  *    the library allocates nothing on the device and keeps no state between
  *    calls.
- *  - d must be 64 or 128 (the head dimensions the huaweicloud page's section
- *    five, part 2 recommends); attn_fwd also takes 256 (listed with them in its
- *    part 1).  Anything else returns ATTN_ERR_UNSUPPORTED.
+ *  - d must be 64, 128 or 256 (64 and 128 are the head dimensions the huaweicloud
+ *    page's section five, part 2 recommends; 256 is listed with them in its part
+ *    1); attn_fwd_fp8 takes 128 only.  Anything else returns ATTN_ERR_UNSUPPORTED.
  *    N >= 1 may be any value (ragged last tiles are masked, never padded in
  *    memory).  B, H >= 1 and B*H*N*d < 2^31.
  *  - causal != 0 keeps key j for query i iff j <= i (the lower triangle,
@@ -81,8 +81,7 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
  *             scores of each row, lse_i = m_i + ln l_i (the saved statistics
  *             of "Understanding FlashAttention, Part 2", section 2.2).
  *   o and lse must not overlap the inputs.
- *   d may be 64, 128 or 256 (at 256 each CTA owns one 128-row query tile; the
- *   backward entry points do not take 256).
+ *   d may be 64, 128 or 256 (at 256 each CTA owns one 128-row query tile).
  */
 ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
@@ -165,11 +164,13 @@ ATTN_API attn_status attn_bwd_dropout(const void *q, const void *k, const void *
  *   lse = M + ln sum_s e^(lse_s - M).
  * Results equal attn_fwd's up to rounding (the partials are kept in float32).
  *   n_splits  : 1..64; a pair with fewer visible key tiles than n_splits uses as
- *               many ranges as it has tiles.
+ *               many ranges as it has tiles.  (At d = 256 the unit is one query
+ *               tile instead of a pair.)
  *   workspace : device scratch of attn_fwd_splitkv_workspace_bytes(B, H, N, d,
  *               n_splits) = n_splits*B*H*N*(d+1)*4 bytes, 16-byte aligned, owned by
  *               the caller, clobbered.  It must not overlap any other argument.
- * Everything else (layouts, causal, scale, errors) is as for attn_fwd.
+ * Everything else (layouts, d in {64, 128, 256}, causal, scale, errors) is as for
+ * attn_fwd.
  */
 ATTN_API size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits);
 ATTN_API attn_status attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,

@@ -117,6 +117,8 @@ def test_stage_entry_points_validate():
 
 def test_splitkv_validates():
     assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 128, 4) == 4 * 2 * 256 * 129 * 4
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 256, 4) == 4 * 2 * 256 * 257 * 4
+    assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 192, 4) == 0
     assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 128, 0) == 0
     assert attn.attn_fwd_splitkv_workspace_bytes(1, 2, 256, 128, 65) == 0
     args = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], workspace=A[9], workspace_bytes=1 << 24, B=1, H=2,
@@ -124,7 +126,7 @@ def test_splitkv_validates():
     for kw, st in [(dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(n_splits=65), attn.ATTN_ERR_INVALID_ARG),
                    (dict(workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG), (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),
                    (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=80), attn.ATTN_ERR_UNSUPPORTED),
-                   (dict(d=256), attn.ATTN_ERR_UNSUPPORTED)]:
+                   (dict(d=256, workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG)]:  # 256 passes the d check
         a2 = dict(args)
         a2.update(kw)
         assert attn.attn_fwd_splitkv(**a2) == st, kw
@@ -134,7 +136,7 @@ def test_splitkv_rect_validates():
     args = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], workspace=A[9], workspace_bytes=1 << 24, B=1, H=2,
                 Nq=128, Nk=4096, d=128, dt=0, causal=1, scale=0.088, n_splits=4, stream=0)
     for kw, st in [(dict(Nq=600, Nk=500), attn.ATTN_ERR_INVALID_ARG),       # causal needs Nk >= Nq
-                   (dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
                    (dict(o=A[1] + 128 * 128 * 2 * 2), attn.ATTN_ERR_INVALID_ARG),  # o inside k (Nk rows)
                    (dict(workspace_bytes=4 * 2 * 128 * 129 * 4 - 4), attn.ATTN_ERR_INVALID_ARG),  # sized by Nq
                    (dict(Nk=0), attn.ATTN_ERR_INVALID_ARG)]:

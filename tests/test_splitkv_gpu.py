@@ -33,7 +33,7 @@ def run_split(q, k, v, causal, n_splits, scale=None):
 
 @pytest.mark.parametrize("n_splits", [1, 2, 3, 8])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 129, 300, 1000])
 def test_splitkv_vs_oracle(N, d, causal, n_splits):
     x = workloads.draw(1, 3, N, d, "bf16", seed=3000 + N + d + n_splits)
@@ -96,7 +96,7 @@ def draw_rect(B, H, Nq, Nk, d, seed):
 
 @pytest.mark.parametrize("n_splits", [2, 5])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("Nq,Nk", [(1, 1000), (64, 4097), (128, 3000), (200, 2000), (300, 300), (513, 700)])
 def test_splitkv_rect_vs_oracle(Nq, Nk, d, causal, n_splits):
     """Few queries against many keys (causal: the queries are the last Nq of Nk positions)."""
@@ -121,3 +121,25 @@ def test_splitkv_rect_decode_shape_sampled(causal):
         ro, rl = oracle.attn_fwd(q[0, h], k[0, h], v[0, h], causal, scale, rows=rows)
         assert o_err(o[0, h], ro, rows) <= O_MAX_ABS
         assert float(np.max(np.abs(f64(lse[0, h])[rows] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_d256_decode_shape(causal):
+    """d = 256, B=1, H=4, 128 new queries against Nk = 16384 keys, 8 and 16 ranges: all rows
+    against the unsplit attn_fwd_rect, sampled rows of two heads against the oracle."""
+    B, H, Nq, Nk, d = 1, 4, 128, 16384, 256
+    q, k, v = draw_rect(B, H, Nq, Nk, d, seed=92)
+    scale = 1.0 / math.sqrt(d)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o1 = torch.empty_like(qd)
+    l1 = torch.empty((B, H, Nq), device="cuda", dtype=torch.float32)
+    assert attn.attn_fwd_rect(qd, kd, vd, o1, l1, B, H, Nq, Nk, d, qd.dtype, causal, scale) == attn.ATTN_OK
+    rows = [0, 1, 17, 63, 64, 100, 126, 127]
+    for ns in (8, 16):
+        o, lse = run_split_rect(qd, kd, vd, causal, ns, scale)
+        assert float((o.float() - o1.float()).abs().max()) <= O_MAX_ABS
+        assert float(((lse - l1).abs() / l1.abs().clamp_min(1)).max()) <= LSE_REL
+        for h in (0, 3):
+            ro, rl = oracle.attn_fwd(q[0, h], k[0, h], v[0, h], causal, scale, rows=rows)
+            assert o_err(o[0, h], ro, rows) <= O_MAX_ABS
+            assert float(np.max(np.abs(f64(lse[0, h])[rows] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL

@@ -119,8 +119,8 @@ void set_dropout(Args& a, const Dropout& dr) {
 }
 bool aligned4(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-// d = 256 is accepted only where the caller says so (all but the FP8 and split-KV
-// forwards).  Nk = key length.
+// d = 256 is accepted only where the caller says so (all but the FP8 forward).
+// Nk = key length.
 attn_status check_sizes(int B, int H, int N, int d, attn_dtype dt, float scale, bool allow_d256 = false,
                         int Nk = -1) {
   if (Nk < 0) Nk = N;
@@ -317,7 +317,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const f
 }
 
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int n_splits) {
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128) || n_splits < 1 || n_splits > 64) return 0;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256) || n_splits < 1 || n_splits > 64) return 0;
   return static_cast<size_t>(n_splits) * B * H * N * (static_cast<size_t>(d) + 1) * sizeof(float);
 }
 
@@ -332,7 +332,7 @@ attn_status attn_fwd_splitkv_rect(const void* q, const void* k, const void* v, v
                                   void* workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk, int d,
                                   attn_dtype dt, int causal, float scale, int n_splits, int* dev_status,
                                   void* stream) {
-  attn_status st = check_sizes(B, H, Nq, d, dt, scale, false, Nk);
+  attn_status st = check_sizes(B, H, Nq, d, dt, scale, true, Nk);
   if (st != ATTN_OK) return st;
   if (causal && Nk < Nq) return ATTN_ERR_INVALID_ARG;
   if (n_splits < 1 || n_splits > 64) return ATTN_ERR_INVALID_ARG;

@@ -695,7 +695,12 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdA
     const float wgt = __expf(ls - mx);
     den += wgt;
     const float* src = a.part_o + (s * rows + r) * D + lane * PER;
-    if constexpr (PER == 4) {
+    if constexpr (PER == 8) {
+      const float4 v0 = *reinterpret_cast<const float4*>(src), v1 = *reinterpret_cast<const float4*>(src + 4);
+      const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+      for (int c = 0; c < 8; ++c) acc[c] = fmaf(wgt, vv[c], acc[c]);
+    } else if constexpr (PER == 4) {
       const float4 v = *reinterpret_cast<const float4*>(src);
       acc[0] = fmaf(wgt, v.x, acc[0]);
       acc[1] = fmaf(wgt, v.y, acc[1]);
@@ -712,7 +717,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdA
 #pragma unroll
   for (int c = 0; c < PER; c += 2) pk[c / 2] = pack2<BF16>(acc[c] * inv, acc[c + 1] * inv);
   uint8_t* dst = static_cast<uint8_t*>(a.o) + (r * D + lane * PER) * 2;
-  if constexpr (PER == 4)
+  if constexpr (PER == 8)
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  else if constexpr (PER == 4)
     *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
   else
     *reinterpret_cast<uint32_t*>(dst) = pk[0];
@@ -721,7 +728,11 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdA
 
 template <int D, bool BF16>
 cudaError_t launch_split_t(const FwdArgs& a, cudaStream_t st) {
-  cudaError_t e = launch_fwd_t<D, BF16, true>(a, st);
+  cudaError_t e;
+  if constexpr (D == 256)
+    e = launch_fwd256_split(a, BF16, st);  // the partials of fwd256.cu's kernel
+  else
+    e = launch_fwd_t<D, BF16, true>(a, st);
   if (e != cudaSuccess) return e;
   const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
   merge_kernel<D, BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(a);
@@ -736,6 +747,7 @@ cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 256) return bf16 ? launch_split_t<256, true>(a, s) : launch_split_t<256, false>(a, s);
   if (d == 128) return bf16 ? launch_split_t<128, true>(a, s) : launch_split_t<128, false>(a, s);
   return bf16 ? launch_split_t<64, true>(a, s) : launch_split_t<64, false>(a, s);
 }

@@ -69,9 +69,13 @@ enum : int {
 // DROP: dropout on the probabilities with fwd.cu's keep rule (key j of query i in head bh
 // kept iff byte j % 16 of Philox((j / 16, i, bh, 0), seed) is >= drop_t); l sums every
 // probability and the kept ones are scaled by drop_scale at the end.
-template <bool BF16, bool VARLEN, bool DROP>
+// SPLIT: as in fwd.cu, the CTA covers one of a.n_splits contiguous ranges of its query
+// tile's visible key tiles and writes the range's normalised partial O (fp32) and
+// logsumexp for the merge kernel; a range past the tile's key tiles writes lse = -inf.
+template <bool BF16, bool VARLEN, bool DROP, bool SPLIT>
 __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_constant__ FwdArgs a) {
   static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
+  static_assert(!SPLIT || (!DROP && !VARLEN), "split-KV: plain 16-bit forward");
   using L = F256Layout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -86,7 +90,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_t = (a.N + kTileM - 1) / kTileM;
-  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x), a.BH, n_t);
+  const int split = SPLIT ? static_cast<int>(blockIdx.x) % a.n_splits : 0;
+  const WorkItem wi = work_item<2>(static_cast<int>(blockIdx.x) / (SPLIT ? a.n_splits : 1), a.BH, n_t);
   const int bh = wi.bh;
   const int qt = n_t - 1 - wi.rank;  // longest causal tile first
   // Lengths and positions: the sequence's own (VARLEN), else the kernel parameters, read
@@ -122,7 +127,20 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   auto cofs_ = [&]() -> int {
     if constexpr (VARLEN) return vcofs; else return a.cofs;
   };
-  const int n_kv = visible_key_tiles(qt, Nk_(), a.causal, cofs_());
+  int n_kv = visible_key_tiles(qt, Nk_(), a.causal, cofs_());
+  int kv0 = 0;  // first key tile of this CTA's range
+  if constexpr (SPLIT) {
+    const int ns = min(a.n_splits, n_kv);  // n_kv >= 1: every query sees key 0
+    if (split >= ns) {                     // an empty range (whole CTA, before any barrier)
+      for (int r = threadIdx.x; r < kTileM; r += blockDim.x) {
+        const int grow = qt * kTileM + r;
+        if (grow < a.N) a.part_lse[(static_cast<size_t>(split) * a.BH + bh) * a.N + grow] = -INFINITY;
+      }
+      return;
+    }
+    kv0 = split * n_kv / ns;
+    n_kv = (split + 1) * n_kv / ns - kv0;
+  }
   // TMA coordinates of row r of Q (or K, V): (row, head-batch) or, packed, (head, token)
   auto qy = [&](int r) { return VARLEN ? hh : r; };
   auto qz = [&](int r) { return VARLEN ? tq0 + r : bh; };
@@ -172,8 +190,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       if (c >= 2 && !(ok = mbar_wait(bar(F_KVEMPTY + s), ((c >> 1) - 1) & 1, wc))) return;
       mbar_arrive_expect_tx(bar(F_KVFULL + s), L::TILE);
       for (int kb = 0; kb < L::KB; ++kb)
-        tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(F_KVFULL + s), kb * 64, ky(tile * kTileN),
-                    kz(tile * kTileN));
+        tma_load_3d(sb + L::OFF_KV + s * L::TILE + kb * L::BLK, m, bar(F_KVFULL + s), kb * 64,
+                    ky((kv0 + tile) * kTileN), kz((kv0 + tile) * kTileN));
       ++c;
     };
     load(&a.tm_k, 0);
@@ -257,7 +275,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
           uint32_t w[4];
-          philox4x32_10(static_cast<uint32_t>(j * (kTileN / 16) + g), static_cast<uint32_t>(grow),
+          philox4x32_10(static_cast<uint32_t>((kv0 + j) * (kTileN / 16) + g), static_cast<uint32_t>(grow),
                         static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
 #pragma unroll
           for (int q = 0; q < 4; ++q) keep[g][q] = __vcmpgeu4(w[q], tt);
@@ -274,7 +292,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc) s[cc] = __uint_as_float(sr[cc]);
       }
-      const int k0 = j * kTileN;
+      const int k0 = (kv0 + j) * kTileN;
       const bool tail = k0 + kTileN > Nk_();
       const bool diag = a.causal && (k0 + kTileN - 1 > qt * kTileM + cofs_());
       if (tail || diag) {
@@ -342,7 +360,25 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     // F_ODONE can be two phases short of the last product and a parity wait would alias.
     // (The rescale's wait above is safe: P(j-2) V precedes S(j), which softmax j has seen.)
     ok = ok && mbar_wait_warp(bar(F_DRAIN), 0, wc);
-    if (ok) {
+    if (SPLIT && ok) {  // this range's normalised partial O and logsumexp, one row per thread
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const size_t prow = (static_cast<size_t>(split) * a.BH + bh) * a.N + grow;
+#pragma unroll 1
+      for (int cc = 0; cc < D256 / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld_x32(t_lane + L::TM_O + cc * 32, o);
+        if (grow < a.N) {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D256 + cc * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                 __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+        }
+      }
+      if (grow < a.N) a.part_lse[prow] = ((m == -INFINITY ? 0.f : m) + __log2f(l)) * 0.69314718055994531f;
+    }
+    if (!SPLIT && ok) {
       tc_fence_after();
       const float inv_l = (DROP ? a.drop_scale : 1.f) / l;
       uint8_t* stage = smem + L::OFF_Q;  // every S product has read Q by now
@@ -378,7 +414,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       fence_proxy_async_smem();
     }
     named_bar_sync(1, 128);
-    if (!VARLEN && warp == 4 && lane == 0 && ok && !*abort_flag) {
+    if (!VARLEN && !SPLIT && warp == 4 && lane == 0 && ok && !*abort_flag) {
       for (int kb = 0; kb < L::KB; ++kb) tma_store_3d(&a.tm_o, sb + L::OFF_Q + kb * L::BLK, kb * 64, qt * kTileM, bh);
       bulk_commit();
       bulk_wait_read_all();
@@ -393,13 +429,13 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   }
 }
 
-template <bool BF16, bool VARLEN = false, bool DROP = false>
+template <bool BF16, bool VARLEN = false, bool DROP = false, bool SPLIT = false>
 cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t st) {
-  auto k = fwd256_kernel<BF16, VARLEN, DROP>;
+  auto k = fwd256_kernel<BF16, VARLEN, DROP, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F256Layout::SMEM);
   if (e != cudaSuccess) return e;
   const int n_t = (a.N + kTileM - 1) / kTileM;
-  k<<<dim3(n_t * a.BH), kF256Threads, F256Layout::SMEM, st>>>(a);
+  k<<<dim3(n_t * a.BH * (SPLIT ? a.n_splits : 1)), kF256Threads, F256Layout::SMEM, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -409,6 +445,11 @@ cudaError_t launch_fwd256_t(const FwdArgs& a, cudaStream_t st) {
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s) {
   if (a.drop_t > 0) return bf16 ? launch_fwd256_t<true, false, true>(a, s) : launch_fwd256_t<false, false, true>(a, s);
   return bf16 ? launch_fwd256_t<true>(a, s) : launch_fwd256_t<false>(a, s);
+}
+
+// The split-KV partials only; the caller runs the merge.
+cudaError_t launch_fwd256_split(const FwdArgs& a, bool bf16, cudaStream_t s) {
+  return bf16 ? launch_fwd256_t<true, false, false, true>(a, s) : launch_fwd256_t<false, false, false, true>(a, s);
 }
 
 cudaError_t launch_fwd256_varlen(const FwdArgs& a, bool bf16, cudaStream_t s) {
