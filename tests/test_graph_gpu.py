@@ -1,0 +1,121 @@
+"""CUDA-graph capture of the C ABI: every entry point only encodes tensor maps on the host
+and launches kernels on the caller's stream, so a forward + backward captured once into a
+CUDA graph and replayed on new input values gives the bytes of eager calls (the kernels
+are deterministic), with a clear device status word after every replay."""
+import math
+
+import pytest
+import torch
+
+import tiled_online_softmax_attention_gb300 as attn
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+class Step:
+    """Static device buffers for one forward + backward of shape (B, H, N, d)."""
+
+    def __init__(self, B, H, N, d, dtype=torch.bfloat16):
+        self.shape = (B, H, N, d)
+        self.q, self.k, self.v, self.do = (torch.empty((B, H, N, d), device="cuda", dtype=dtype) for _ in range(4))
+        self.o, self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(4))
+        self.lse = torch.empty((B, H, N), device="cuda", dtype=torch.float32)
+        self.nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+        self.ws = torch.empty(self.nbytes, device="cuda", dtype=torch.uint8)
+        self.status = torch.zeros(1, device="cuda", dtype=torch.int32)
+
+    def load(self, seed):
+        B, H, N, d = self.shape
+        x = workloads.draw(B, H, N, d, "bf16" if self.q.dtype == torch.bfloat16 else "fp16", seed=seed,
+                           with_dout=True)
+        for name in ("q", "k", "v"):
+            getattr(self, name).copy_(x[name])
+        self.do.copy_(x["dout"])
+
+    def outputs(self):
+        return [t.clone() for t in (self.o, self.lse, self.dq, self.dk, self.dv)]
+
+
+def fwd_bwd(s, causal, p_drop=0.0, seed=0):
+    B, H, N, d = s.shape
+    scale = 1.0 / math.sqrt(d)
+    if p_drop > 0:
+        rc = attn.attn_fwd_dropout(s.q, s.k, s.v, s.o, s.lse, B, H, N, d, s.q.dtype, causal, scale, p_drop, seed,
+                                   s.status)
+        assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+        rc = attn.attn_bwd_dropout(s.q, s.k, s.v, s.o, s.do, s.lse, s.dq, s.dk, s.dv, s.ws, s.nbytes, B, H, N, d,
+                                   s.q.dtype, causal, scale, p_drop, seed, s.status)
+    else:
+        rc = attn.attn_fwd(s.q, s.k, s.v, s.o, s.lse, B, H, N, d, s.q.dtype, causal, scale, s.status)
+        assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+        rc = attn.attn_bwd(s.q, s.k, s.v, s.o, s.do, s.lse, s.dq, s.dk, s.dv, s.ws, s.nbytes, B, H, N, d,
+                           s.q.dtype, causal, scale, s.status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+
+
+def check_graph_matches_eager(s, run, seeds):
+    s.load(seeds[0])
+    run()  # eager warm-up: every kernel's attributes set before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for seed in seeds:
+        s.load(seed)
+        run()
+        torch.cuda.synchronize()
+        want = s.outputs()
+        for t in (s.o, s.lse, s.dq, s.dk, s.dv):
+            t.fill_(float("nan"))
+        s.load(seed)
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(s.status.item()) == 0
+        for name, a, b in zip(("O", "lse", "dQ", "dK", "dV"), s.outputs(), want):
+            assert torch.equal(a, b), f"graph replay differs from the eager call in {name} (seed {seed})"
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_graph_fwd_bwd(d, causal):
+    s = Step(1, 3, 700, d)
+    check_graph_matches_eager(s, lambda: fwd_bwd(s, causal), seeds=[11, 12, 13])
+
+
+def test_graph_dropout():
+    s = Step(2, 2, 513, 128)
+    check_graph_matches_eager(s, lambda: fwd_bwd(s, True, p_drop=0.2, seed=99), seeds=[21, 22])
+
+
+def test_graph_splitkv_replays():
+    """The split-KV forward (partials + merge, two kernels) captured and replayed 50 times
+    gives the eager call's bytes each time."""
+    B, H, Nq, Nk, d, ns = 1, 4, 128, 8192, 128, 8
+    g0 = torch.Generator().manual_seed(5)
+    q = torch.randn((B, H, Nq, d), generator=g0).to(torch.bfloat16).cuda()
+    k = torch.randn((B, H, Nk, d), generator=g0).to(torch.bfloat16).cuda()
+    v = torch.randn((B, H, Nk, d), generator=g0).to(torch.bfloat16).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), device="cuda", dtype=torch.float32)
+    nb = attn.attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, ns)
+    ws = torch.empty(nb, device="cuda", dtype=torch.uint8)
+    status = torch.zeros(1, device="cuda", dtype=torch.int32)
+
+    def run():
+        rc = attn.attn_fwd_splitkv_rect(q, k, v, o, lse, ws, nb, B, H, Nq, Nk, d, q.dtype, True, 1 / math.sqrt(d), ns,
+                                        status)
+        assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+
+    run()
+    torch.cuda.synchronize()
+    want_o, want_l = o.clone(), lse.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for _ in range(50):
+        o.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(o, want_o) and torch.equal(lse, want_l)
