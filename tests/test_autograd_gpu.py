@@ -33,8 +33,9 @@ def test_autograd_matches_oracle(causal, Nk):
         assert grad_err(g_, r) <= GRAD_REL_L2
 
 
-def test_autograd_dropout_matches_oracle():
-    N, d = 400, 128
+@pytest.mark.parametrize("d", [128, 256])
+def test_autograd_dropout_matches_oracle(d):
+    N = 400
     x = workloads.draw(1, 2, N, d, "bf16", seed=52, with_dout=True)
     q, k, v = (x[n].cuda().requires_grad_() for n in ("q", "k", "v"))
     o = attn.attention(q, k, v, causal=True, dropout_p=0.2, seed=99)
