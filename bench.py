@@ -378,6 +378,7 @@ def long_forward(attn, dev):
     res["decode_B1_H32_Nq128_Nk32768_d128"] = decode_forward(attn, dev)
     res["decode_B1_H16_Nq128_Nk32768_d256"] = decode_forward(attn, dev, 16, 256)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
+    res["forward_d64_vs_d128_grid"] = forward_grid_sweep(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     res["d256_forward_and_step_B1_H16_N16384"] = d256_side(attn, dev)
     res["dropout_training_step_p0.1"] = dropout_step(attn, dev)
@@ -493,6 +494,40 @@ def fp8_forward(attn, dev):
         tf = workloads.fwd_flops(B, H, N, d, causal) / (ms * 1e-3) / 1e12
         out["causal" if causal else "non_causal"] = {"ms": round(ms, 4), "tflops": round(tf, 1),
                                                      "frac_of_fp8_peak": round(tf / fp8_peak, 3)}
+    return out
+
+
+def forward_grid_sweep(attn, dev):
+    """Non-causal forward at d = 64 and d = 128 over sequence length and head count (B = 1,
+    N(0,1) inputs, one call at a time after a 256 MiB L2 flush, median of 15): separates the
+    per-CTA cost of short sequences (few key tiles, few waves) from the per-key-tile rate
+    that long sequences reach.  d = 64 at N = 1024, 96 heads is the c2 shape."""
+    flush = torch.empty(256 << 20, device=dev, dtype=torch.uint8)
+    out = {}
+    for d in (64, 128):
+        for N in (1024, 4096):
+            for BH in (96, 768):
+                g = torch.Generator().manual_seed(N + BH + d)
+                q, k, v = (torch.randn((1, BH, N, d), generator=g).to(torch.bfloat16).to(dev) for _ in range(3))
+                o = torch.empty_like(q)
+                lse = torch.empty((1, BH, N), device=dev, dtype=torch.float32)
+                call = lambda: attn.attn_fwd(q, k, v, o, lse, 1, BH, N, d, q.dtype, False, 1 / math.sqrt(d))
+                for _ in range(3):
+                    call()
+                ts = []
+                for _ in range(15):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    call()
+                    b.record()
+                    torch.cuda.synchronize()
+                    ts.append(a.elapsed_time(b))
+                ms = sorted(ts)[len(ts) // 2]
+                f = workloads.fwd_flops(1, BH, N, d, False)
+                out[f"d{d}_N{N}_heads{BH}"] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1),
+                                               "ctas": BH * ((N + 255) // 256)}
+                del q, k, v, o, lse
     return out
 
 
