@@ -141,7 +141,8 @@ ATTN_API attn_status attn_bwd_varlen(const void *q, const void *k, const void *v
  *   O = (P o Z) V with Z = keep * 256 / (256 - t); lse is the logsumexp of the
  *   scores, as without dropout.  The backward must get the same p_drop and seed:
  *   dV = (P o Z)^T dO, dS = P o (Z o dP - D), D_i = rowsum(dO_i o O_i).
- * d in {64, 128, 256}; square shapes.  Everything else is as for attn_fwd / attn_bwd.
+ * d in {64, 128, 256}; square shapes (packed batches: attn_fwd_varlen_dropout below).
+ * Everything else is as for attn_fwd / attn_bwd.
  * p_drop = 0 runs the plain kernels.
  */
 ATTN_API attn_status attn_fwd_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -152,6 +153,25 @@ ATTN_API attn_status attn_bwd_dropout(const void *q, const void *k, const void *
                              void *workspace, size_t workspace_bytes,
                              int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
                              float p_drop, uint64_t seed, int *dev_status, void *stream);
+
+/*
+ * attn_fwd_varlen_dropout / attn_bwd_varlen_dropout -- attn_fwd_varlen / attn_bwd_varlen
+ * with attn_fwd_dropout's dropout.  The mask of a packed batch is that of the padded
+ * batch: element (b, h, i, j) -- sequence b, head h, query i and key j counted from the
+ * sequence's first token -- reads Philox at counter (j / 16, i, b*H + h, 0).  The
+ * backward must get the same p_drop and seed.  d in {64, 128, 256}; everything else is
+ * as for attn_fwd_varlen / attn_bwd_varlen and attn_fwd_dropout.
+ */
+ATTN_API attn_status attn_fwd_varlen_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                                    const int *cu_q, const int *cu_k, int B, int H, int max_q, int max_k,
+                                    int Tq, int Tk, int d, attn_dtype dt, int causal, float scale,
+                                    float p_drop, uint64_t seed, int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_varlen_dropout(const void *q, const void *k, const void *v, const void *o,
+                                    const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                    void *workspace, size_t workspace_bytes, const int *cu_q,
+                                    const int *cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk,
+                                    int d, attn_dtype dt, int causal, float scale, float p_drop,
+                                    uint64_t seed, int *dev_status, void *stream);
 
 /*
  * attn_fwd_splitkv -- the forward pass for shapes with too few query tiles to fill

@@ -227,3 +227,22 @@ def test_varlen_validates():
         a2 = dict(ba)
         a2.update(kw)
         assert attn.attn_bwd_varlen(**a2) == st, kw
+
+
+def test_varlen_dropout_validates():
+    fa = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], cu_q=A[5], cu_k=A[6], B=3, H=2, max_q=300, max_k=300,
+              Tq=600, Tk=600, d=128, dt=0, causal=1, scale=0.088, p_drop=0.1, seed=7, stream=0)
+    for kw, st in [(dict(p_drop=1.0), attn.ATTN_ERR_INVALID_ARG), (dict(p_drop=float("nan")), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(B=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(o=A[0]), attn.ATTN_ERR_INVALID_ARG)]:
+        a2 = dict(fa)
+        a2.update(kw)
+        assert attn.attn_fwd_varlen_dropout(**a2) == st, kw
+    ba = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8], workspace=A[9],
+              workspace_bytes=1 << 20, cu_q=A[10], cu_k=A[11], B=3, H=2, max_q=300, max_k=300, Tq=600, Tk=600, d=128,
+              dt=0, causal=1, scale=0.088, p_drop=0.1, seed=7, stream=0)
+    for kw, st in [(dict(p_drop=-0.5), attn.ATTN_ERR_INVALID_ARG), (dict(workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(dq=A[7]), attn.ATTN_ERR_INVALID_ARG), (dict(d=96), attn.ATTN_ERR_UNSUPPORTED)]:
+        a2 = dict(ba)
+        a2.update(kw)
+        assert attn.attn_bwd_varlen_dropout(**a2) == st, kw

@@ -209,3 +209,97 @@ def test_dropout_d256_long_sampled(causal):
                              ("dV", f64(dv[0, h])[rows], rv)):
             e = grad_err(gg, rr)
             assert e <= GRAD_REL_L2, f"head {h} {name} relative L2 {e:.3e}"
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+
+
+def run_varlen_drop(x, causal, scale, p, seed):
+    """attn_fwd_varlen_dropout then attn_bwd_varlen_dropout through the C ABI, guarded outputs."""
+    Tq, H, d = x["q"].shape
+    Tk = x["k"].shape[0]
+    B = x["cu_q"].numel() - 1
+    max_q = max(1, int(np.diff(x["cu_q"].numpy()).max()))
+    max_k = max(1, int(np.diff(x["cu_k"].numpy()).max()))
+    q, k, v, do, cu_q, cu_k = (x[n].cuda() for n in ("q", "k", "v", "dout", "cu_q", "cu_k"))
+    o = Guarded((Tq, H, d), q.dtype)
+    lse = Guarded((H, Tq), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_varlen_dropout(q, k, v, o.t, lse.t, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, q.dtype, causal,
+                                      scale, p, seed, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and o.intact() and lse.intact(), "forward wrote outside its outputs"
+    dq, dk, dv = Guarded((Tq, H, d), q.dtype), Guarded((Tk, H, d), q.dtype), Guarded((Tk, H, d), q.dtype)
+    nb = attn.attn_bwd_workspace_bytes(B, H, max_q, d)
+    ws = Guarded((nb // 4,), torch.float32)
+    rc = attn.attn_bwd_varlen_dropout(q, k, v, o.t, do, lse.t, dq.t, dk.t, dv.t, ws.t, nb, cu_q, cu_k, B, H, max_q,
+                                      max_k, Tq, Tk, d, q.dtype, causal, scale, p, seed, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and dq.intact() and dk.intact() and dv.intact() and ws.intact()
+    return o.t, lse.t, dq.t, dk.t, dv.t
+
+
+def oracle_varlen_dropout(x, causal, scale, t, seed):
+    """The oracle's dropout forward and backward, one sequence at a time on its [H][n][d]
+    slices as heads b*H .. b*H + H - 1 of the mask, written back in the packed layout."""
+    Tq, H, d = x["q"].shape
+    Tk = x["k"].shape[0]
+    cq, ck = x["cu_q"].numpy(), x["cu_k"].numpy()
+    ro, rl = np.zeros((Tq, H, d)), np.zeros((H, Tq))
+    rq, rk, rv = np.zeros((Tq, H, d)), np.zeros((Tk, H, d)), np.zeros((Tk, H, d))
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = int(cq[b]), int(cq[b + 1]), int(ck[b]), int(ck[b + 1])
+        if q1 == q0:
+            continue
+        sq, sk, sv, sd = (x[n][lo:hi].permute(1, 0, 2) for n, lo, hi in
+                          (("q", q0, q1), ("k", k0, k1), ("v", k0, k1), ("dout", q0, q1)))
+        o, l = oracle.attn_fwd_dropout(sq, sk, sv, causal, scale, t, seed, bh0=b * H)
+        ro[q0:q1], rl[:, q0:q1] = np.transpose(o, (1, 0, 2)), l
+        g = oracle.attn_bwd_dropout(sq, sk, sv, sd, causal, scale, t, seed, bh0=b * H)
+        rq[q0:q1], rk[k0:k1], rv[k0:k1] = (np.transpose(a, (1, 0, 2)) for a in g)
+    return ro, rl, rq, rk, rv
+
+
+VARLEN_LENS = [1, 127, 300, 0, 129, 513, 64]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("extra_keys", [False, True])
+def test_dropout_varlen_fwd_bwd(extra_keys, causal, d):
+    """Packed batches (an empty sequence included; with extra_keys, more keys than
+    queries) with p = 0.2 against the oracle's per-sequence dropout."""
+    from test_varlen_gpu import packed
+    lens_k = [n + e for n, e in zip(VARLEN_LENS, [0, 5, 100, 3, 0, 7, 200])] if extra_keys else VARLEN_LENS
+    lens_k = [max(n, 1) if q > 0 else n for n, q in zip(lens_k, VARLEN_LENS)]
+    x = packed(VARLEN_LENS, lens_k, 3, d, "bf16", seed=71 + d + causal)
+    scale, p, seed = 1.0 / math.sqrt(d), 0.2, 0x7A51
+    t = t_of(p)
+    o, lse, dq, dk, dv = run_varlen_drop(x, causal, scale, p, seed)
+    ro, rl, rq, rk, rv = oracle_varlen_dropout(x, causal, scale, t, seed)
+    assert o_err(o, ro) <= O_MAX_ABS * 256 / (256 - t), f"O error {o_err(o, ro):.3e}"
+    assert lse_err(lse, rl) <= LSE_REL
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        e = grad_err(g, r)
+        assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e} (causal={causal} d={d} extra={extra_keys})"
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_dropout_varlen_equals_padded(d):
+    """Sequences of one length packed together give attn_fwd_dropout / attn_bwd_dropout's
+    bytes on the [B][H][N][d] batch: the packed mask is the padded batch's."""
+    from test_varlen_gpu import packed
+    B, H, N = 3, 2, 300
+    x = packed([N] * B, [N] * B, H, d, "bf16", seed=9 + d)
+    scale, p, seed = 0.07, 0.3, 12345
+    o, lse, dq, dk, dv = run_varlen_drop(x, True, scale, p, seed)
+    q, k, v, do = (x[n].reshape(B, N, H, d).permute(0, 2, 1, 3).contiguous().cuda() for n in ("q", "k", "v", "dout"))
+    o2, l2 = run_fwd_drop(q, k, v, True, scale, p, seed)
+    g2 = run_bwd_drop(q, k, v, o2, l2, do, True, scale, p, seed)
+    unpack = lambda a: a.reshape(B, N, H, d).permute(0, 2, 1, 3)
+    assert torch.equal(unpack(o), o2)
+    assert torch.equal(lse.reshape(H, B, N).permute(1, 0, 2), l2)
+    for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), g2):
+        assert torch.equal(unpack(a), b), f"{name} differs from the padded batch's"

@@ -223,9 +223,15 @@ attn_status attn_fwd_rect(const void* q, const void* k, const void* v, void* o, 
   return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status, stream);
 }
 
-attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
+}  // extern "C"
+
+namespace {
+
+// The packed-batch forward, with or without dropout.
+attn_status fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
                             const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk, int d,
-                            attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+                            attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
+                            const Dropout& dr) {
   attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale, true);  // d = 256 too
   if (st != ATTN_OK) return st;
   if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
@@ -260,10 +266,32 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   a.causal = causal ? 1 : 0;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
+  set_dropout(a, dr);
   const cudaError_t e = d == 256 ? attn::launch_fwd256_varlen(a, bf16, static_cast<cudaStream_t>(stream))
                                  : attn::launch_fwd_varlen(a, d, bf16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
+                            const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk, int d,
+                            attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  return fwd_varlen_impl(q, k, v, o, lse, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, dev_status,
+                         stream, Dropout{});
+}
+
+attn_status attn_fwd_varlen_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                                    const int* cu_q, const int* cu_k, int B, int H, int max_q, int max_k, int Tq,
+                                    int Tk, int d, attn_dtype dt, int causal, float scale, float p_drop,
+                                    uint64_t seed, int* dev_status, void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
+  return fwd_varlen_impl(q, k, v, o, lse, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, dev_status,
+                         stream, dr);
 }
 
 attn_status attn_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
@@ -584,10 +612,16 @@ attn_status attn_bwd_dropout(const void* q, const void* k, const void* v, const 
                   dev_status, stream, dr);
 }
 
-attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+}  // extern "C"
+
+namespace {
+
+// The packed-batch backward, with or without dropout.
+attn_status bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
                             const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                             const int* cu_q, const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk,
-                            int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+                            int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
+                            const Dropout& dr) {
   attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale, true);  // H * tokens * d < 2^31
   if (st != ATTN_OK) return st;
   if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
@@ -617,7 +651,7 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
   if (!make_map_packed(&a.tm_q, q, H, Tq, d, bf16) || !make_map_packed(&a.tm_k, k, H, Tk, d, bf16) ||
       !make_map_packed(&a.tm_v, v, H, Tk, d, bf16) || !make_map_packed(&a.tm_do, dout, H, Tq, d, bf16))
     return ATTN_ERR_CUDA;
-  fill_bwd(a, workspace, B, H, max_q, max_k, causal, scale, dev_status);
+  fill_bwd(a, workspace, B, H, max_q, max_k, causal, scale, dev_status, dr);
   a.cofs = 0;  // per sequence, from the offsets
   a.o = o;
   a.dout = dout;
@@ -639,6 +673,29 @@ attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const v
                                         : cudaErrorLaunchFailure);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                            const int* cu_q, const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk,
+                            int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
+  return bwd_varlen_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, cu_q, cu_k, B, H, max_q,
+                         max_k, Tq, Tk, d, dt, causal, scale, dev_status, stream, Dropout{});
+}
+
+attn_status attn_bwd_varlen_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                    const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                                    size_t workspace_bytes, const int* cu_q, const int* cu_k, int B, int H,
+                                    int max_q, int max_k, int Tq, int Tk, int d, attn_dtype dt, int causal,
+                                    float scale, float p_drop, uint64_t seed, int* dev_status, void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
+  return bwd_varlen_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, cu_q, cu_k, B, H, max_q,
+                         max_k, Tq, Tk, d, dt, causal, scale, dev_status, stream, dr);
 }
 
 attn_status attn_bwd_rect(const void* q, const void* k, const void* v, const void* o, const void* dout,

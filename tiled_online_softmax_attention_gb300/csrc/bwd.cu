@@ -221,7 +221,6 @@ __device__ __forceinline__ void store_row_chunk_packed(void* base, size_t row_el
 // the kernel's __grid_constant__ parameter, so the tensor maps stay in parameter space.
 template <int D, bool BF16, bool DROP, bool VARLEN>
 __device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
-  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = DkdvLayout<D>;
   using T = BwdTiles<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -585,7 +584,6 @@ enum : int {
 // The dQ CTA for work unit `block` (its body; the kernels below launch it).
 template <int D, bool BF16, bool DROP, bool VARLEN>
 __device__ __forceinline__ void dq_body(const BwdArgs& a, int block) {
-  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   using L = DqLayout<D>;
   using T = BwdTiles<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -1001,11 +999,20 @@ cudaError_t launch_bwd_pre_varlen(const BwdArgs& a, int d, bool bf16, cudaStream
   if (d == 128) return bf16 ? launch_pre_t<128, true, true>(a, s) : launch_pre_t<128, false, true>(a, s);
   return bf16 ? launch_pre_t<64, true, true>(a, s) : launch_pre_t<64, false, true>(a, s);
 }
+// The varlen gradient launchers: a.drop_t > 0 selects the dropout kernels.
 cudaError_t launch_bwd_dkdv_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (a.drop_t > 0) {
+    if (d == 128) return bf16 ? launch_dkdv_t<128, true, true, true>(a, s) : launch_dkdv_t<128, false, true, true>(a, s);
+    return bf16 ? launch_dkdv_t<64, true, true, true>(a, s) : launch_dkdv_t<64, false, true, true>(a, s);
+  }
   if (d == 128) return bf16 ? launch_dkdv_t<128, true, false, true>(a, s) : launch_dkdv_t<128, false, false, true>(a, s);
   return bf16 ? launch_dkdv_t<64, true, false, true>(a, s) : launch_dkdv_t<64, false, false, true>(a, s);
 }
 cudaError_t launch_bwd_dq_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (a.drop_t > 0) {
+    if (d == 128) return bf16 ? launch_dq_t<128, true, true, true>(a, s) : launch_dq_t<128, false, true, true>(a, s);
+    return bf16 ? launch_dq_t<64, true, true, true>(a, s) : launch_dq_t<64, false, true, true>(a, s);
+  }
   if (d == 128) return bf16 ? launch_dq_t<128, true, false, true>(a, s) : launch_dq_t<128, false, false, true>(a, s);
   return bf16 ? launch_dq_t<64, true, false, true>(a, s) : launch_dq_t<64, false, false, true>(a, s);
 }

@@ -414,7 +414,6 @@ using LayoutDv = Layout256<kDvSlots, 1, 16 * 128>;
 
 template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_constant__ BwdArgs a) {
-  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   constexpr int NSLOT = kDvSlots;
   using L = LayoutDv;
   extern __shared__ uint8_t smem_raw[];
@@ -522,7 +521,6 @@ using LayoutDk = Layout256<kDkSlots, 2, 16 * 128>;
 
 template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_constant__ BwdArgs a) {
-  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   constexpr int NSLOT = kDkSlots;
   using L = LayoutDk;
   extern __shared__ uint8_t smem_raw[];
@@ -652,7 +650,6 @@ using LayoutDq = Layout256<kDqSlots, 2, 0>;
 
 template <bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_constant__ BwdArgs a) {
-  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   constexpr int NSLOT = kDqSlots;
   using L = LayoutDq;
   extern __shared__ uint8_t smem_raw[];
@@ -800,10 +797,10 @@ cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s) {
   return a.drop_t > 0 ? launch_dq256_t<false, true>(a, bf16, s) : launch_dq256_t<false>(a, bf16, s);
 }
 cudaError_t launch_bwd256_dkdv_varlen(const BwdArgs& a, bool bf16, cudaStream_t s) {
-  return launch_dkdv256_t<true>(a, bf16, s);
+  return a.drop_t > 0 ? launch_dkdv256_t<true, true>(a, bf16, s) : launch_dkdv256_t<true>(a, bf16, s);
 }
 cudaError_t launch_bwd256_dq_varlen(const BwdArgs& a, bool bf16, cudaStream_t s) {
-  return launch_dq256_t<true>(a, bf16, s);
+  return a.drop_t > 0 ? launch_dq256_t<true, true>(a, bf16, s) : launch_dq256_t<true>(a, bf16, s);
 }
 
 }  // namespace attn

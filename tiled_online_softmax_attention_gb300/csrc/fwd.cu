@@ -110,7 +110,8 @@ enum : int {
 // names it): P(i, j) is kept iff byte j mod 16 of Philox4x32-10 at counter
 // (j / 16, i, bh, 0), keyed by the seed, is >= a.drop_t; the row sum l keeps every
 // probability (dropout follows the softmax) and the epilogue scales O by
-// 256 / (256 - drop_t).
+// 256 / (256 - drop_t).  With packed sequences i and j are positions within the
+// sequence and bh = b * H + h, so a packed batch draws the padded batch's mask.
 //
 // VARLEN: variable-length packed sequences ([tokens][H][d] with offsets): the CTA reads
 // its sequence's token range, loads tiles at (column, head, token) coordinates, masks
@@ -128,7 +129,7 @@ template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP, bool VARLEN, bool P
 __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
   static_assert(!(FP8 && SPLIT) && (!FP8 || D == 128), "E4M3 inputs: d = 128, no split");
   static_assert(!DROP || (!FP8 && !SPLIT), "dropout: 16-bit inputs, no split");
-  static_assert(!VARLEN || (!FP8 && !SPLIT && !DROP), "packed sequences: plain 16-bit forward");
+  static_assert(!VARLEN || (!FP8 && !SPLIT), "packed sequences: 16-bit forward, no split");
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -758,7 +759,15 @@ cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t 
   return bf16 ? launch_fwd_t<64, true, false, false, true>(a, s) : launch_fwd_t<64, false, false, false, true>(a, s);
 }
 
+// a.drop_t > 0 selects the dropout kernels.
 cudaError_t launch_fwd_varlen(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (a.drop_t > 0) {
+    if (d == 128)
+      return bf16 ? launch_fwd_t<128, true, false, false, true, true>(a, s)
+                  : launch_fwd_t<128, false, false, false, true, true>(a, s);
+    return bf16 ? launch_fwd_t<64, true, false, false, true, true>(a, s)
+                : launch_fwd_t<64, false, false, false, true, true>(a, s);
+  }
   if (d == 128)
     return bf16 ? launch_fwd_t<128, true, false, false, false, true>(a, s)
                 : launch_fwd_t<128, false, false, false, false, true>(a, s);

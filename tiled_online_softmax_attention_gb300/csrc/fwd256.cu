@@ -74,7 +74,6 @@ enum : int {
 // logsumexp for the merge kernel; a range past the tile's key tiles writes lse = -inf.
 template <bool BF16, bool VARLEN, bool DROP, bool SPLIT>
 __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_constant__ FwdArgs a) {
-  static_assert(!(DROP && VARLEN), "dropout with packed sequences is not built");
   static_assert(!SPLIT || (!DROP && !VARLEN), "split-KV: plain 16-bit forward");
   using L = F256Layout;
   extern __shared__ uint8_t smem_raw[];
@@ -453,6 +452,7 @@ cudaError_t launch_fwd256_split(const FwdArgs& a, bool bf16, cudaStream_t s) {
 }
 
 cudaError_t launch_fwd256_varlen(const FwdArgs& a, bool bf16, cudaStream_t s) {
+  if (a.drop_t > 0) return bf16 ? launch_fwd256_t<true, true, true>(a, s) : launch_fwd256_t<false, true, true>(a, s);
   return bf16 ? launch_fwd256_t<true, true>(a, s) : launch_fwd256_t<false, true>(a, s);
 }
 
