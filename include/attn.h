@@ -141,7 +141,8 @@ ATTN_API attn_status attn_bwd_varlen(const void *q, const void *k, const void *v
  *   O = (P o Z) V with Z = keep * 256 / (256 - t); lse is the logsumexp of the
  *   scores, as without dropout.  The backward must get the same p_drop and seed:
  *   dV = (P o Z)^T dO, dS = P o (Z o dP - D), D_i = rowsum(dO_i o O_i).
- * d in {64, 128, 256}; square shapes (packed batches: attn_fwd_varlen_dropout below).
+ * d in {64, 128, 256}; square shapes (rectangular ones and packed batches: the
+ * entry points below).
  * Everything else is as for attn_fwd / attn_bwd.
  * p_drop = 0 runs the plain kernels.
  */
@@ -153,6 +154,21 @@ ATTN_API attn_status attn_bwd_dropout(const void *q, const void *k, const void *
                              void *workspace, size_t workspace_bytes,
                              int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
                              float p_drop, uint64_t seed, int *dev_status, void *stream);
+
+/*
+ * attn_fwd_rect_dropout / attn_bwd_rect_dropout -- attn_fwd_rect / attn_bwd_rect (Nq
+ * queries against Nk keys, causal aligned to the last key) with attn_fwd_dropout's
+ * dropout; element (bh, i, j) is query i and key j of the rectangular problem.
+ * d in {64, 128, 256}; everything else is as for attn_fwd_rect / attn_bwd_rect.
+ */
+ATTN_API attn_status attn_fwd_rect_dropout(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  int B, int H, int Nq, int Nk, int d, attn_dtype dt, int causal,
+                                  float scale, float p_drop, uint64_t seed, int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_rect_dropout(const void *q, const void *k, const void *v, const void *o,
+                                  const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                  void *workspace, size_t workspace_bytes, int B, int H, int Nq, int Nk,
+                                  int d, attn_dtype dt, int causal, float scale, float p_drop,
+                                  uint64_t seed, int *dev_status, void *stream);
 
 /*
  * attn_fwd_varlen_dropout / attn_bwd_varlen_dropout -- attn_fwd_varlen / attn_bwd_varlen

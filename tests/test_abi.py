@@ -229,6 +229,24 @@ def test_varlen_validates():
         assert attn.attn_bwd_varlen(**a2) == st, kw
 
 
+def test_rect_dropout_validates():
+    fa = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], B=1, H=2, Nq=256, Nk=512, d=128, dt=0, causal=1,
+              scale=0.088, p_drop=0.1, seed=3, stream=0)
+    for kw, st in [(dict(Nq=600), attn.ATTN_ERR_INVALID_ARG), (dict(p_drop=2.0), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(d=96), attn.ATTN_ERR_UNSUPPORTED), (dict(o=A[1] + 256 * 128 * 2 * 2), attn.ATTN_ERR_INVALID_ARG)]:
+        a2 = dict(fa)
+        a2.update(kw)
+        assert attn.attn_fwd_rect_dropout(**a2) == st, kw
+    ba = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8], workspace=A[9],
+              workspace_bytes=1 << 20, B=1, H=2, Nq=256, Nk=512, d=128, dt=0, causal=1, scale=0.088, p_drop=0.1,
+              seed=3, stream=0)
+    for kw, st in [(dict(Nq=600), attn.ATTN_ERR_INVALID_ARG), (dict(p_drop=-1.0), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(d=192), attn.ATTN_ERR_UNSUPPORTED), (dict(workspace_bytes=16), attn.ATTN_ERR_INVALID_ARG)]:
+        a2 = dict(ba)
+        a2.update(kw)
+        assert attn.attn_bwd_rect_dropout(**a2) == st, kw
+
+
 def test_varlen_dropout_validates():
     fa = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], cu_q=A[5], cu_k=A[6], B=3, H=2, max_q=300, max_k=300,
               Tq=600, Tk=600, d=128, dt=0, causal=1, scale=0.088, p_drop=0.1, seed=7, stream=0)

@@ -303,3 +303,41 @@ def test_dropout_varlen_equals_padded(d):
     assert torch.equal(lse.reshape(H, B, N).permute(1, 0, 2), l2)
     for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), g2):
         assert torch.equal(unpack(a), b), f"{name} differs from the padded batch's"
+
+
+# ---------------------------------------------------------------- rectangular shapes
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(1, 300), (100, 300), (129, 128), (200, 513), (513, 700)])
+def test_dropout_rect_fwd_bwd(Nq, Nk, causal, d):
+    """Nq queries against Nk keys (causal: the last Nq of Nk positions) with p = 0.15."""
+    if causal and Nk < Nq:
+        pytest.skip("causal needs Nk >= Nq")
+    from test_rect_gpu import draw_rect
+    x = draw_rect(1, 2, Nq, Nk, d, "bf16", seed=Nq * 7 + Nk + d)
+    scale, p, seed = 1.0 / math.sqrt(d), 0.15, 0xC0FFEE
+    t = t_of(p)
+    B, H = 1, 2
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    o, lse = Guarded((B, H, Nq, d), q.dtype), Guarded((B, H, Nq), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_rect_dropout(q, k, v, o.t, lse.t, B, H, Nq, Nk, d, q.dtype, causal, scale, p, seed, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    dq = Guarded((B, H, Nq, d), q.dtype)
+    dk, dv = Guarded((B, H, Nk, d), q.dtype), Guarded((B, H, Nk, d), q.dtype)
+    nb = attn.attn_bwd_workspace_bytes(B, H, Nq, d)
+    ws = Guarded((nb // 4,), torch.float32)
+    rc = attn.attn_bwd_rect_dropout(q, k, v, o.t, do, lse.t, dq.t, dk.t, dv.t, ws.t, nb, B, H, Nq, Nk, d, q.dtype,
+                                    causal, scale, p, seed, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and all(g.intact() for g in (o, lse, dq, dk, dv, ws))
+    ro, rl = oracle.attn_fwd_dropout(x["q"], x["k"], x["v"], causal, scale, t, seed)
+    assert o_err(o.t, ro) <= O_MAX_ABS * 256 / (256 - t), f"O error {o_err(o.t, ro):.3e}"
+    assert lse_err(lse.t, rl) <= LSE_REL
+    r = oracle.attn_bwd_dropout(x["q"], x["k"], x["v"], x["dout"], causal, scale, t, seed)
+    for name, g, rr in zip(("dQ", "dK", "dV"), (dq.t, dk.t, dv.t), r):
+        e = grad_err(g, rr)
+        assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e} ({Nq}x{Nk} causal={causal} d={d})"

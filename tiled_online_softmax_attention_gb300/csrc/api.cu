@@ -302,6 +302,14 @@ attn_status attn_fwd_dropout(const void* q, const void* k, const void* v, void* 
   return fwd_impl(q, k, v, o, lse, B, H, N, N, d, dt, causal, scale, dev_status, stream, dr);
 }
 
+attn_status attn_fwd_rect_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                  int Nq, int Nk, int d, attn_dtype dt, int causal, float scale, float p_drop,
+                                  uint64_t seed, int* dev_status, void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, dev_status, stream, dr);
+}
+
 attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, const float* q_scale,
                          const float* k_scale, const float* v_scale, void* o, float* lse, int B, int H, int N,
                          int d, attn_dtype out_dt, int causal, float scale, int* dev_status, void* stream) {
@@ -704,6 +712,17 @@ attn_status attn_bwd_rect(const void* q, const void* k, const void* v, const voi
                           int* dev_status, void* stream) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Nq, Nk, d, dt, causal, scale,
                   dev_status, stream);
+}
+
+attn_status attn_bwd_rect_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                                  size_t workspace_bytes, int B, int H, int Nq, int Nk, int d, attn_dtype dt,
+                                  int causal, float scale, float p_drop, uint64_t seed, int* dev_status,
+                                  void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, Nq, Nk, d, dt, causal, scale,
+                  dev_status, stream, dr);
 }
 
 attn_status attn_selftest_bounded_wait(int* dev_status, uint64_t limit_ns, void* stream) {
