@@ -228,6 +228,25 @@ ATTN_API attn_status attn_fwd_splitkv_rect(const void *q, const void *k, const v
                                   float scale, int n_splits, int *dev_status, void *stream);
 
 /*
+ * attn_fwd_varlen_splitkv -- attn_fwd_varlen with split-KV: each sequence's query tiles
+ * have their visible key tiles cut into n_splits ranges (1..64), each range's CTA writes
+ * a float32 partial output and logsumexp, and the merge kernel combines them (the rule
+ * of attn_fwd_splitkv).  For batches of few sequences and heads with long keys (decoding
+ * several sequences of different lengths).  Rows of a degenerate sequence get O = 0,
+ * lse = -inf as in attn_fwd_varlen; tokens outside cu_q[0] .. cu_q[B] are not written.
+ *   workspace : device scratch of attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d,
+ *               n_splits) = n_splits*Tq*H*(d+1)*4 bytes, 16-byte aligned, owned by the
+ *               caller, clobbered; it must not overlap any other argument.
+ * d in {64, 128, 256}; everything else is as for attn_fwd_varlen.
+ */
+ATTN_API size_t attn_fwd_varlen_splitkv_workspace_bytes(int H, int Tq, int d, int n_splits);
+ATTN_API attn_status attn_fwd_varlen_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                                    void *workspace, size_t workspace_bytes, const int *cu_q,
+                                    const int *cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk,
+                                    int d, attn_dtype dt, int causal, float scale, int n_splits,
+                                    int *dev_status, void *stream);
+
+/*
  * attn_fwd_fp8 -- forward pass on FP8 inputs with per-block scale factors (the FP8
  * support with block-wise scaling of "FlashAttention hardware-aware analysis"
  * (huaweicloud), section four, part 3).

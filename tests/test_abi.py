@@ -229,6 +229,23 @@ def test_varlen_validates():
         assert attn.attn_bwd_varlen(**a2) == st, kw
 
 
+def test_varlen_splitkv_validates():
+    assert attn.attn_fwd_varlen_splitkv_workspace_bytes(2, 600, 128, 4) == 4 * 600 * 2 * 129 * 4
+    assert attn.attn_fwd_varlen_splitkv_workspace_bytes(2, 600, 256, 1) == 600 * 2 * 257 * 4
+    assert attn.attn_fwd_varlen_splitkv_workspace_bytes(2, 600, 96, 4) == 0
+    assert attn.attn_fwd_varlen_splitkv_workspace_bytes(2, 600, 128, 65) == 0
+    fa = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], workspace=A[9], workspace_bytes=1 << 24, cu_q=A[5], cu_k=A[6],
+              B=3, H=2, max_q=300, max_k=300, Tq=600, Tk=600, d=128, dt=0, causal=1, scale=0.088, n_splits=4,
+              stream=0)
+    for kw, st in [(dict(n_splits=0), attn.ATTN_ERR_INVALID_ARG), (dict(n_splits=65), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(workspace_bytes=100), attn.ATTN_ERR_INVALID_ARG), (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG), (dict(d=192), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(B=0), attn.ATTN_ERR_INVALID_ARG)]:
+        a2 = dict(fa)
+        a2.update(kw)
+        assert attn.attn_fwd_varlen_splitkv(**a2) == st, kw
+
+
 def test_rect_dropout_validates():
     fa = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], B=1, H=2, Nq=256, Nk=512, d=128, dt=0, causal=1,
               scale=0.088, p_drop=0.1, seed=3, stream=0)

@@ -143,3 +143,76 @@ def test_splitkv_d256_decode_shape(causal):
             ro, rl = oracle.attn_fwd(q[0, h], k[0, h], v[0, h], causal, scale, rows=rows)
             assert o_err(o[0, h], ro, rows) <= O_MAX_ABS
             assert float(np.max(np.abs(f64(lse[0, h])[rows] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+
+
+# ---------------------------------------------------------------- packed variable-length batches
+
+
+def run_split_varlen(x, causal, n_splits, scale, Tq_pad=0):
+    """attn_fwd_varlen_splitkv through the C ABI, guarded outputs; Tq_pad extra query tokens
+    after cu_q[B] belong to no sequence and must stay as they were (NaN here)."""
+    Tq0, H, d = x["q"].shape
+    Tq = Tq0 + Tq_pad
+    Tk = x["k"].shape[0]
+    B = x["cu_q"].numel() - 1
+    max_q = max(1, int(np.diff(x["cu_q"].numpy()).max()))
+    max_k = max(1, int(np.diff(x["cu_k"].numpy()).max()))
+    q = torch.cat([x["q"], torch.zeros((Tq_pad, H, d), dtype=x["q"].dtype)]).cuda()
+    k, v, cu_q, cu_k = (x[n].cuda() for n in ("k", "v", "cu_q", "cu_k"))
+    o = Guarded((Tq, H, d), q.dtype)
+    lse = Guarded((H, Tq), torch.float32)
+    o.t.fill_(float("nan"))
+    lse.t.fill_(float("nan"))
+    nb = attn.attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d, n_splits)
+    assert nb == n_splits * Tq * H * (d + 1) * 4
+    ws = Guarded((nb // 4,), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_varlen_splitkv(q, k, v, o.t, lse.t, ws.t, nb, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d,
+                                      q.dtype, causal, scale, n_splits, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and o.intact() and lse.intact() and ws.intact(), "wrote outside its buffers"
+    return o.t, lse.t
+
+
+VARLEN_LENS = [1, 127, 300, 0, 129, 513, 64]
+
+
+@pytest.mark.parametrize("n_splits", [2, 5])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("extra_keys", [False, True])
+def test_splitkv_varlen_vs_oracle(extra_keys, causal, d, n_splits):
+    """Packed batches (an empty sequence included; with extra_keys, up to 2000 more keys than
+    queries, the decode-like case) against the oracle, and against attn_fwd_varlen."""
+    from test_varlen_gpu import packed, run_varlen
+    lens_k = [n + e for n, e in zip(VARLEN_LENS, [0, 2000, 100, 3, 700, 7, 1500])] if extra_keys else VARLEN_LENS
+    lens_k = [max(n, 1) if q > 0 else n for n, q in zip(lens_k, VARLEN_LENS)]
+    x = packed(VARLEN_LENS, lens_k, 3, d, "bf16", seed=301 + d + causal + n_splits)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_split_varlen(x, causal, n_splits, scale)
+    ro, rl = oracle.attn_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal, scale)
+    assert o_err(o, ro) <= O_MAX_ABS, f"O error {o_err(o, ro):.3e}"
+    assert lse_err(lse, rl) <= LSE_REL
+    o1, l1 = run_varlen(x, causal, scale, backward=False)
+    assert float((o.float() - o1.float()).abs().max()) <= O_MAX_ABS
+    assert float(((lse - l1).abs() / l1.abs().clamp_min(1)).max()) <= LSE_REL
+
+
+@pytest.mark.parametrize("d", [64, 256])
+def test_splitkv_varlen_degenerate_and_unowned_rows(d):
+    """A sequence without keys and a causal one with fewer keys than queries get O = 0,
+    lse = -inf through the merge; query tokens after cu_q[B] are left untouched."""
+    from test_varlen_gpu import packed
+    lens_q, lens_k = [200, 150, 300], [2000, 0, 100]
+    x = packed(lens_q, lens_k, 2, d, "bf16", seed=16)
+    o, lse = run_split_varlen(x, True, 4, 0.125, Tq_pad=37)
+    go, gl = f64(o), f64(lse)
+    cq = x["cu_q"].tolist()
+    for b in (1, 2):
+        assert np.all(go[cq[b]:cq[b + 1]] == 0) and np.all(np.isneginf(gl[:, cq[b]:cq[b + 1]]))
+    assert np.all(np.isnan(go[cq[3]:])) and np.all(np.isnan(gl[:, cq[3]:])), "a row outside every sequence was written"
+    ro, rl = oracle.attn_fwd(x["q"][:200].permute(1, 0, 2), x["k"][:2000].permute(1, 0, 2),
+                             x["v"][:2000].permute(1, 0, 2), True, 0.125)
+    assert float(np.max(np.abs(go[:200] - ro.transpose(1, 0, 2)))) <= O_MAX_ABS
+    assert float(np.max(np.abs(gl[:, :200] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL

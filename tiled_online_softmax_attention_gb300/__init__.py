@@ -16,6 +16,9 @@ current stream):
                     B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, ...)
     attn_fwd_varlen_dropout / attn_bwd_varlen_dropout: the two above plus p_drop, seed
     attn_fwd_rect_dropout / attn_bwd_rect_dropout: attn_fwd_rect / attn_bwd_rect plus p_drop, seed
+    attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d, n_splits)
+    attn_fwd_varlen_splitkv(q, k, v, o, lse, workspace, workspace_bytes, cu_q, cu_k, B, H, max_q, max_k,
+                            Tq, Tk, d, dt, causal, scale, n_splits, dev_status=None, stream=None)
     attn_fwd_dropout(q, k, v, o, lse, B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None, stream=None)
     attn_bwd_dropout(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
                      B, H, N, d, dt, causal, scale, p_drop, seed, dev_status=None, stream=None)
@@ -64,7 +67,7 @@ ATTN_BF16 = 0
 ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
-EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_varlen_dropout", "attn_bwd_varlen_dropout", "attn_fwd_rect_dropout", "attn_bwd_rect_dropout", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_rect", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
+EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_varlen_dropout", "attn_bwd_varlen_dropout", "attn_fwd_rect_dropout", "attn_bwd_rect_dropout", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_rect", "attn_fwd_varlen_splitkv_workspace_bytes", "attn_fwd_varlen_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
@@ -119,6 +122,10 @@ def load(build_if_missing: bool = True):
     lib.attn_fwd_splitkv.restype = I
     lib.attn_fwd_splitkv_rect.argtypes = [P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, I, P, P]
     lib.attn_fwd_splitkv_rect.restype = I
+    lib.attn_fwd_varlen_splitkv_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_fwd_varlen_splitkv_workspace_bytes.restype = SZ
+    lib.attn_fwd_varlen_splitkv.argtypes = [P, P, P, P, P, P, SZ, P, P, I, I, I, I, I, I, I, I, I, F, I, P, P]
+    lib.attn_fwd_varlen_splitkv.restype = I
     lib.attn_bwd_workspace_bytes.argtypes = [I, I, I, I]
     lib.attn_bwd_workspace_bytes.restype = SZ
     lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, P, P]
@@ -191,6 +198,19 @@ def attn_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_byte
                                       _ptr(dv), _ptr(workspace), int(workspace_bytes), _ptr(cu_q), _ptr(cu_k), int(B),
                                       int(H), int(max_q), int(max_k), int(Tq), int(Tk), int(d), _dt(dt),
                                       int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d, n_splits) -> int:
+    return int(load().attn_fwd_varlen_splitkv_workspace_bytes(int(H), int(Tq), int(d), int(n_splits)))
+
+
+def attn_fwd_varlen_splitkv(q, k, v, o, lse, workspace, workspace_bytes, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt,
+                            causal, scale, n_splits, dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd_varlen_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(workspace),
+                                              int(workspace_bytes), _ptr(cu_q), _ptr(cu_k), int(B), int(H),
+                                              int(max_q), int(max_k), int(Tq), int(Tk), int(d), _dt(dt),
+                                              int(bool(causal)), float(scale), int(n_splits), _ptr(dev_status),
+                                              _stream(stream)))
 
 
 def attn_fwd_rect_dropout(q, k, v, o, lse, B, H, Nq, Nk, d, dt, causal, scale, p_drop, seed, dev_status=None,

@@ -227,25 +227,33 @@ attn_status attn_fwd_rect(const void* q, const void* k, const void* v, void* o, 
 
 namespace {
 
-// The packed-batch forward, with or without dropout.
+// The packed-batch forward, with or without dropout; n_splits > 0: split-KV through the
+// workspace (no dropout then).
 attn_status fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse, const int* cu_q,
                             const int* cu_k, int B, int H, int max_q, int max_k, int Tq, int Tk, int d,
                             attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
-                            const Dropout& dr) {
+                            const Dropout& dr, void* workspace = nullptr, size_t workspace_bytes = 0,
+                            int n_splits = 0) {
   attn_status st = check_sizes(1, H, Tq > Tk ? Tq : Tk, d, dt, scale, true);  // d = 256 too
   if (st != ATTN_OK) return st;
   if (B < 1 || max_q < 1 || max_k < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(B) * H * ((max_q + 127) / 128) >= (int64_t(1) << 31)) return ATTN_ERR_INVALID_ARG;
+  if (n_splits < 0 || n_splits > 64 || (n_splits > 0 && dr.t > 0)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * H * ((max_q + 127) / 128) * (n_splits > 0 ? n_splits : 1) >= (int64_t(1) << 31))
+    return ATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned4(cu_q) ||
-      !aligned4(cu_k))
+      !aligned4(cu_k) || (n_splits > 0 && !aligned16(workspace)))
     return ATTN_ERR_INVALID_ARG;
   const size_t qb = static_cast<size_t>(Tq) * H * d * 2, kb = static_cast<size_t>(Tk) * H * d * 2;
   const size_t lb = static_cast<size_t>(H) * Tq * 4, cb = static_cast<size_t>(B + 1) * 4;
+  const size_t wb = n_splits > 0 ? attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d, n_splits) : 0;
+  if (n_splits > 0 && (wb == 0 || workspace_bytes < wb)) return ATTN_ERR_INVALID_ARG;
   for (const void* in : {q, k, v, static_cast<const void*>(cu_q), static_cast<const void*>(cu_k)}) {
     const size_t ib = in == q ? qb : (in == k || in == v) ? kb : cb;
-    if (overlaps(in, ib, o, qb) || overlaps(in, ib, lse, lb)) return ATTN_ERR_INVALID_ARG;
+    if (overlaps(in, ib, o, qb) || overlaps(in, ib, lse, lb) || (wb && overlaps(in, ib, workspace, wb)))
+      return ATTN_ERR_INVALID_ARG;
   }
   if (overlaps(o, qb, lse, lb)) return ATTN_ERR_INVALID_ARG;
+  if (wb && (overlaps(o, qb, workspace, wb) || overlaps(lse, lb, workspace, wb))) return ATTN_ERR_INVALID_ARG;
   if ((st = check_device()) != ATTN_OK) return st;
 
   attn::FwdArgs a{};
@@ -267,6 +275,14 @@ attn_status fwd_varlen_impl(const void* q, const void* k, const void* v, void* o
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
   set_dropout(a, dr);
+  if (n_splits > 0) {
+    a.n_splits = n_splits;
+    a.part_o = static_cast<float*>(workspace);
+    a.part_lse = static_cast<float*>(workspace) + static_cast<size_t>(n_splits) * Tq * H * d;
+    if (attn::launch_fwd_varlen_split(a, d, bf16, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
   const cudaError_t e = d == 256 ? attn::launch_fwd256_varlen(a, bf16, static_cast<cudaStream_t>(stream))
                                  : attn::launch_fwd_varlen(a, d, bf16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
@@ -282,6 +298,20 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
                             attn_dtype dt, int causal, float scale, int* dev_status, void* stream) {
   return fwd_varlen_impl(q, k, v, o, lse, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, dev_status,
                          stream, Dropout{});
+}
+
+size_t attn_fwd_varlen_splitkv_workspace_bytes(int H, int Tq, int d, int n_splits) {
+  if (H < 1 || Tq < 1 || (d != 64 && d != 128 && d != 256) || n_splits < 1 || n_splits > 64) return 0;
+  return static_cast<size_t>(n_splits) * Tq * H * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+attn_status attn_fwd_varlen_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                                    void* workspace, size_t workspace_bytes, const int* cu_q, const int* cu_k,
+                                    int B, int H, int max_q, int max_k, int Tq, int Tk, int d, attn_dtype dt,
+                                    int causal, float scale, int n_splits, int* dev_status, void* stream) {
+  if (n_splits < 1) return ATTN_ERR_INVALID_ARG;
+  return fwd_varlen_impl(q, k, v, o, lse, cu_q, cu_k, B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, dev_status,
+                         stream, Dropout{}, workspace, workspace_bytes, n_splits);
 }
 
 attn_status attn_fwd_varlen_dropout(const void* q, const void* k, const void* v, void* o, float* lse,

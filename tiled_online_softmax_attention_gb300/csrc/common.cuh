@@ -138,9 +138,10 @@ __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
 // Launchers (fwd.cu / bwd.cu); return the CUDA launch status.
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+cudaError_t launch_fwd_varlen_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);  // packed batches
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);
 cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s);
-cudaError_t launch_fwd256_split(const FwdArgs& a, bool bf16, cudaStream_t s);  // partials, no merge
+cudaError_t launch_fwd256_split(const FwdArgs& a, bool bf16, bool varlen, cudaStream_t s);  // partials only
 cudaError_t launch_fwd256_varlen(const FwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_varlen(const FwdArgs& a, int d, bool bf16, cudaStream_t s);

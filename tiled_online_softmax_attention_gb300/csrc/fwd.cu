@@ -120,8 +120,9 @@ enum : int {
 //
 // SPLIT: the CTA covers one of a.n_splits contiguous ranges of the pair's key tiles and
 // writes its range's normalised partial O (fp32) and logsumexp instead of the output;
-// attn_merge_kernel combines the ranges with the two-block merge of the huaweicloud
-// page's section two.
+// merge_kernel combines the ranges with the two-block merge of the huaweicloud page's
+// section two.  With VARLEN too, the partials sit in the packed layout ([split][token]
+// [head]), and a degenerate sequence's ranges are all empty (lse = -inf).
 // The CTA's body; PAD: its pair's second query tile lies wholly past the last query
 // (a sequence of an odd number of tiles, or a few queries against many keys), so only
 // tile 0 runs.  `a` is the kernel's __grid_constant__ parameter.
@@ -129,7 +130,7 @@ template <int D, bool BF16, bool SPLIT, bool FP8, bool DROP, bool VARLEN, bool P
 __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
   static_assert(!(FP8 && SPLIT) && (!FP8 || D == 128), "E4M3 inputs: d = 128, no split");
   static_assert(!DROP || (!FP8 && !SPLIT), "dropout: 16-bit inputs, no split");
-  static_assert(!VARLEN || (!FP8 && !SPLIT), "packed sequences: 16-bit forward, no split");
+  static_assert(!VARLEN || !FP8, "packed sequences: 16-bit inputs");
   using L = FwdLayout<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -177,6 +178,10 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
       for (int r = threadIdx.x; r < 2 * kTileM; r += blockDim.x) {
         const int gr = 2 * pr * kTileM + r;
         if (gr >= N) continue;
+        if constexpr (SPLIT) {  // every range is empty: the merge writes O = 0, lse = -inf
+          a.part_lse[(static_cast<size_t>(split) * a.Tq + tq0 + gr) * a.H + hh] = -INFINITY;
+          continue;
+        }
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) + ((static_cast<size_t>(tq0 + gr) * a.H + hh) * D) * 2);
         for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
         a.lse[static_cast<size_t>(hh) * a.Tq + tq0 + gr] = -INFINITY;
@@ -198,6 +203,14 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
   auto qc2 = [&](int r) { return VARLEN ? tq0 + r : bh; };
   auto kc1 = [&](int r) { return VARLEN ? hh : r; };
   auto kc2 = [&](int r) { return VARLEN ? tk0 + r : bh; };
+  // Split-KV partial row of query row r (part_lse index; part_o rows hold D floats):
+  // [split][BH][N], or packed [split][Tq][H] like O itself.
+  auto prow_of = [&](int r) -> size_t {
+    if constexpr (VARLEN)
+      return (static_cast<size_t>(split) * a.Tq + tq0 + r) * a.H + hh;
+    else
+      return (static_cast<size_t>(split) * a.BH + bh) * a.N + r;
+  };
   int n_kv[2];  // key tiles each query tile visits, starting at key tile kv0
 #pragma unroll
   for (int i = 0; i < 2; ++i) n_kv[i] = visible_key_tiles(2 * pr + i, Nk_(), a.causal, cofs_());
@@ -209,7 +222,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
     if (split >= ns) {
       for (int r = threadIdx.x; r < 2 * kTileM; r += blockDim.x) {
         const int grow = 2 * pr * kTileM + r;
-        if (grow < a.N) a.part_lse[(static_cast<size_t>(split) * a.BH + bh) * a.N + grow] = -INFINITY;
+        if (grow < N_()) a.part_lse[prow_of(grow)] = -INFINITY;
       }
       return;
     }
@@ -577,12 +590,12 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         const float mf = m_s[i * 128 + row];
         const float lf = l_s[i * 128 + row];
         const float inv_l = 1.f / lf;
-        const size_t prow = (static_cast<size_t>(split) * a.BH + bh) * a.N + q0 + row;
+        const size_t prow = prow_of(q0 + row);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
           tmem_ld_x32(t_lane + L::tm_o(i) + cc * 32, o);
-          if (q0 + row < a.N) {
+          if (q0 + row < N_()) {
             float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D + cc * 32);
 #pragma unroll
             for (int q = 0; q < 8; ++q)
@@ -590,7 +603,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
                                    __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
           }
         }
-        if (q0 + row < a.N) a.part_lse[prow] = (mf + __log2f(lf)) * 0.69314718055994531f;
+        if (q0 + row < N_()) a.part_lse[prow] = (mf + __log2f(lf)) * 0.69314718055994531f;
       }
       if (!SPLIT && ok_i) {
         tc_fence_after();
@@ -676,14 +689,22 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t st) {
 }
 
 // Merge of the split-KV partials, one warp per row: M = max_s lse_s,
-// O = sum_s e^(lse_s - M) O_s / sum_s e^(lse_s - M), lse = M + ln sum_s e^(lse_s - M).
-template <int D, bool BF16>
+// O = sum_s e^(lse_s - M) O_s / sum_s e^(lse_s - M), lse = M + ln sum_s e^(lse_s - M);
+// a row whose ranges are all empty (a degenerate packed sequence) gets O = 0, lse = -inf.
+// Rows are (bh, query) or, VARLEN, (token, head) of the packed layout; tokens outside
+// cu_q[0] .. cu_q[B] belong to no sequence and are left untouched.
+template <int D, bool BF16, bool VARLEN = false>
 __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdArgs a) {
   constexpr int PER = D / 32;  // columns per lane
   const int lane = threadIdx.x & 31;
-  const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
+  const int64_t rows = VARLEN ? static_cast<int64_t>(a.Tq) * a.H : static_cast<int64_t>(a.BH) * a.N;
   const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   if (r >= rows) return;
+  if constexpr (VARLEN) {
+    const int64_t tok = r / a.H;
+    const int B = a.BH / a.H;
+    if (tok < min(max(a.cu_q[0], 0), a.Tq) || tok >= min(max(a.cu_q[B], 0), a.Tq)) return;
+  }
   float mx = -INFINITY;
   for (int s = 0; s < a.n_splits; ++s) mx = fmaxf(mx, a.part_lse[s * rows + r]);
   float acc[PER];
@@ -713,7 +734,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdA
       acc[1] = fmaf(wgt, v.y, acc[1]);
     }
   }
-  const float inv = 1.f / den;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
   uint32_t pk[PER / 2];
 #pragma unroll
   for (int c = 0; c < PER; c += 2) pk[c / 2] = pack2<BF16>(acc[c] * inv, acc[c + 1] * inv);
@@ -724,19 +745,22 @@ __global__ void __launch_bounds__(256) merge_kernel(const __grid_constant__ FwdA
     *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
   else
     *reinterpret_cast<uint32_t*>(dst) = pk[0];
-  if (lane == 0) a.lse[r] = mx + __logf(den);
+  if (lane == 0) {
+    const int64_t li = VARLEN ? (r % a.H) * a.Tq + r / a.H : r;  // packed lse is [H][Tq]
+    a.lse[li] = den > 0.f ? mx + __logf(den) : -INFINITY;
+  }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool VARLEN = false>
 cudaError_t launch_split_t(const FwdArgs& a, cudaStream_t st) {
   cudaError_t e;
   if constexpr (D == 256)
-    e = launch_fwd256_split(a, BF16, st);  // the partials of fwd256.cu's kernel
+    e = launch_fwd256_split(a, BF16, VARLEN, st);  // the partials of fwd256.cu's kernel
   else
-    e = launch_fwd_t<D, BF16, true>(a, st);
+    e = launch_fwd_t<D, BF16, true, false, false, VARLEN>(a, st);
   if (e != cudaSuccess) return e;
-  const int64_t rows = static_cast<int64_t>(a.BH) * a.N;
-  merge_kernel<D, BF16><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(a);
+  const int64_t rows = VARLEN ? static_cast<int64_t>(a.Tq) * a.H : static_cast<int64_t>(a.BH) * a.N;
+  merge_kernel<D, BF16, VARLEN><<<static_cast<unsigned>((rows * 32 + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -751,6 +775,12 @@ cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s)
   if (d == 256) return bf16 ? launch_split_t<256, true>(a, s) : launch_split_t<256, false>(a, s);
   if (d == 128) return bf16 ? launch_split_t<128, true>(a, s) : launch_split_t<128, false>(a, s);
   return bf16 ? launch_split_t<64, true>(a, s) : launch_split_t<64, false>(a, s);
+}
+
+cudaError_t launch_fwd_varlen_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {
+  if (d == 256) return bf16 ? launch_split_t<256, true, true>(a, s) : launch_split_t<256, false, true>(a, s);
+  if (d == 128) return bf16 ? launch_split_t<128, true, true>(a, s) : launch_split_t<128, false, true>(a, s);
+  return bf16 ? launch_split_t<64, true, true>(a, s) : launch_split_t<64, false, true>(a, s);
 }
 
 cudaError_t launch_fwd_dropout(const FwdArgs& a, int d, bool bf16, cudaStream_t s) {

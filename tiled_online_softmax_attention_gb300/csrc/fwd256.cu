@@ -71,10 +71,11 @@ enum : int {
 // probability and the kept ones are scaled by drop_scale at the end.
 // SPLIT: as in fwd.cu, the CTA covers one of a.n_splits contiguous ranges of its query
 // tile's visible key tiles and writes the range's normalised partial O (fp32) and
-// logsumexp for the merge kernel; a range past the tile's key tiles writes lse = -inf.
+// logsumexp for the merge kernel; a range past the tile's key tiles writes lse = -inf
+// (with VARLEN: partials in the packed layout, every range of a degenerate sequence empty).
 template <bool BF16, bool VARLEN, bool DROP, bool SPLIT>
 __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_constant__ FwdArgs a) {
-  static_assert(!SPLIT || (!DROP && !VARLEN), "split-KV: plain 16-bit forward");
+  static_assert(!SPLIT || !DROP, "split-KV: no dropout");
   using L = F256Layout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -110,6 +111,10 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       for (int r = threadIdx.x; r < kTileM; r += blockDim.x) {
         const int gr = qt * kTileM + r;
         if (gr >= N) continue;
+        if constexpr (SPLIT) {  // every range is empty: the merge writes O = 0, lse = -inf
+          a.part_lse[(static_cast<size_t>(split) * a.Tq + tq0 + gr) * a.H + hh] = -INFINITY;
+          continue;
+        }
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.o) + ((static_cast<size_t>(tq0 + gr) * a.H + hh) * D256) * 2);
         for (int c = 0; c < D256 / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
         a.lse[static_cast<size_t>(hh) * a.Tq + tq0 + gr] = -INFINITY;
@@ -126,6 +131,14 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
   auto cofs_ = [&]() -> int {
     if constexpr (VARLEN) return vcofs; else return a.cofs;
   };
+  // Split-KV partial row of query row r (part_lse index; part_o rows hold 256 floats):
+  // [split][BH][N], or packed [split][Tq][H] like O itself.
+  auto prow_of = [&](int r) -> size_t {
+    if constexpr (VARLEN)
+      return (static_cast<size_t>(split) * a.Tq + tq0 + r) * a.H + hh;
+    else
+      return (static_cast<size_t>(split) * a.BH + bh) * a.N + r;
+  };
   int n_kv = visible_key_tiles(qt, Nk_(), a.causal, cofs_());
   int kv0 = 0;  // first key tile of this CTA's range
   if constexpr (SPLIT) {
@@ -133,7 +146,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     if (split >= ns) {                     // an empty range (whole CTA, before any barrier)
       for (int r = threadIdx.x; r < kTileM; r += blockDim.x) {
         const int grow = qt * kTileM + r;
-        if (grow < a.N) a.part_lse[(static_cast<size_t>(split) * a.BH + bh) * a.N + grow] = -INFINITY;
+        if (grow < N_()) a.part_lse[prow_of(grow)] = -INFINITY;
       }
       return;
     }
@@ -362,12 +375,12 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     if (SPLIT && ok) {  // this range's normalised partial O and logsumexp, one row per thread
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const size_t prow = (static_cast<size_t>(split) * a.BH + bh) * a.N + grow;
+      const size_t prow = prow_of(grow);
 #pragma unroll 1
       for (int cc = 0; cc < D256 / 32; ++cc) {
         uint32_t o[32];
         tmem_ld_x32(t_lane + L::TM_O + cc * 32, o);
-        if (grow < a.N) {
+        if (grow < N_()) {
           float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D256 + cc * 32);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -375,7 +388,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
                                  __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
         }
       }
-      if (grow < a.N) a.part_lse[prow] = ((m == -INFINITY ? 0.f : m) + __log2f(l)) * 0.69314718055994531f;
+      if (grow < N_()) a.part_lse[prow] = ((m == -INFINITY ? 0.f : m) + __log2f(l)) * 0.69314718055994531f;
     }
     if (!SPLIT && ok) {
       tc_fence_after();
@@ -446,8 +459,11 @@ cudaError_t launch_fwd256(const FwdArgs& a, bool bf16, cudaStream_t s) {
   return bf16 ? launch_fwd256_t<true>(a, s) : launch_fwd256_t<false>(a, s);
 }
 
-// The split-KV partials only; the caller runs the merge.
-cudaError_t launch_fwd256_split(const FwdArgs& a, bool bf16, cudaStream_t s) {
+// The split-KV partials only (of a padded or, varlen, a packed batch); the caller runs
+// the merge.
+cudaError_t launch_fwd256_split(const FwdArgs& a, bool bf16, bool varlen, cudaStream_t s) {
+  if (varlen)
+    return bf16 ? launch_fwd256_t<true, true, false, true>(a, s) : launch_fwd256_t<false, true, false, true>(a, s);
   return bf16 ? launch_fwd256_t<true, false, false, true>(a, s) : launch_fwd256_t<false, false, false, true>(a, s);
 }
 
