@@ -377,6 +377,7 @@ def long_forward(attn, dev):
     res["split_kv_B1_H1_N16384_d128"] = split_forward(attn, dev)
     res["decode_B1_H32_Nq128_Nk32768_d128"] = decode_forward(attn, dev)
     res["decode_B1_H16_Nq128_Nk32768_d256"] = decode_forward(attn, dev, 16, 256)
+    res["decode_varlen_4seqs_H8_d128"] = decode_varlen_forward(attn, dev)
     res["forward_by_workload"] = forward_by_workload(attn, dev)
     res["forward_d64_vs_d128_grid"] = forward_grid_sweep(attn, dev)
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
@@ -650,6 +651,55 @@ def decode_forward(attn, dev, H=32, d=128):
             ms = a.elapsed_time(b) / 20
             kv_gbs = 2 * B * H * Nk * d * 2 / (ms * 1e-3) / 1e9
             ent["attn_fwd_rect" if ns == 1 else f"splits_{ns}"] = {
+                "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1), "kv_read_gbs": round(kv_gbs, 1)}
+        out["causal" if causal else "non_causal"] = ent
+    return out
+
+
+def decode_varlen_forward(attn, dev):
+    """A ragged decode-like batch: 4 sequences of 128 new queries after 8192, 16384, 24576
+    and 32768 positions (keys 8320 .. 32896), H = 8, d = 128, bf16, causal and not, packed:
+    attn_fwd_varlen (one CTA per sequence and head, 32 CTAs) against
+    attn_fwd_varlen_splitkv with 4, 8 and 16 ranges.  FLOPs: the visible part of each
+    sequence's 128 x Nk scores, two products."""
+    H, d, nq = 8, 128, 128
+    lens_k = [8192 + nq, 16384 + nq, 24576 + nq, 32768 + nq]
+    B, Tq, Tk = len(lens_k), nq * len(lens_k), sum(lens_k)
+    g = torch.Generator().manual_seed(23)
+    q = torch.randn((Tq, H, d), generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn((Tk, H, d), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((Tk, H, d), generator=g).to(torch.bfloat16).to(dev)
+    cu_q = torch.arange(0, Tq + 1, nq, dtype=torch.int32, device=dev)
+    cu_k = torch.tensor([0] + list(torch.tensor(lens_k).cumsum(0).tolist()), dtype=torch.int32, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, Tq), device=dev, dtype=torch.float32)
+    sc = 1.0 / math.sqrt(d)
+    out = {}
+    for causal in (False, True):
+        visible = sum(nq * n - (nq * (nq - 1) // 2 if causal else 0) for n in lens_k)
+        f = 4.0 * H * visible * d
+        ent = {}
+        for ns in (1, 4, 8, 16):
+            nb = attn.attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d, ns)
+            ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+            if ns == 1:
+                call = lambda: attn.attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, B, H, nq, max(lens_k), Tq, Tk, d,
+                                                    q.dtype, causal, sc)
+            else:
+                call = lambda: attn.attn_fwd_varlen_splitkv(q, k, v, o, lse, ws, nb, cu_q, cu_k, B, H, nq, max(lens_k),
+                                                            Tq, Tk, d, q.dtype, causal, sc, ns)
+            for _ in range(3):
+                call()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(20):
+                call()
+            b.record()
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b) / 20
+            kv_gbs = 2 * Tk * H * d * 2 / (ms * 1e-3) / 1e9
+            ent["attn_fwd_varlen" if ns == 1 else f"splits_{ns}"] = {
                 "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1), "kv_read_gbs": round(kv_gbs, 1)}
         out["causal" if causal else "non_causal"] = ent
     return out
