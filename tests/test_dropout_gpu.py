@@ -341,3 +341,25 @@ def test_dropout_rect_fwd_bwd(Nq, Nk, causal, d):
     for name, g, rr in zip(("dQ", "dK", "dV"), (dq.t, dk.t, dv.t), r):
         e = grad_err(g, rr)
         assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e} ({Nq}x{Nk} causal={causal} d={d})"
+
+
+def _random_batches(n, seed):
+    from test_varlen_gpu import random_batches
+    return random_batches(n, seed=seed)
+
+
+@pytest.mark.parametrize("i,lens_q,lens_k,causal,d,dtype", _random_batches(20, seed=91))
+def test_dropout_varlen_random_batches(i, lens_q, lens_k, causal, d, dtype):
+    """Seeded random packed batches (1-6 sequences, empty ones included, bf16 and fp16)
+    through the dropout entry points, p drawn from {0.05, 0.3}."""
+    from test_varlen_gpu import packed
+    x = packed(list(lens_q), list(lens_k), 2, d, dtype, seed=900 + i)
+    scale, p, seed = 1.0 / math.sqrt(d), (0.05, 0.3)[i % 2], 4000 + i
+    t = t_of(p)
+    o, lse, dq, dk, dv = run_varlen_drop(x, causal, scale, p, seed)
+    ro, rl, rq, rk, rv = oracle_varlen_dropout(x, causal, scale, t, seed)
+    assert o_err(o, ro) <= O_MAX_ABS * 256 / (256 - t), f"O error {o_err(o, ro):.3e}"
+    assert lse_err(lse, rl) <= LSE_REL
+    for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        e = grad_err(g, r)
+        assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e}"

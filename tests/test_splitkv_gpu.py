@@ -216,3 +216,21 @@ def test_splitkv_varlen_degenerate_and_unowned_rows(d):
                              x["v"][:2000].permute(1, 0, 2), True, 0.125)
     assert float(np.max(np.abs(go[:200] - ro.transpose(1, 0, 2)))) <= O_MAX_ABS
     assert float(np.max(np.abs(gl[:, :200] - rl) / np.maximum(np.abs(rl), 1))) <= LSE_REL
+
+
+def _random_batches(n, seed):
+    from test_varlen_gpu import random_batches
+    return random_batches(n, seed=seed)
+
+
+@pytest.mark.parametrize("i,lens_q,lens_k,causal,d,dtype", _random_batches(20, seed=92))
+def test_splitkv_varlen_random_batches(i, lens_q, lens_k, causal, d, dtype):
+    """Seeded random packed batches (1-6 sequences, empty ones included, bf16 and fp16)
+    through split-KV with 1, 2, 3 or 7 ranges."""
+    from test_varlen_gpu import packed
+    x = packed(list(lens_q), list(lens_k), 2, d, dtype, seed=950 + i)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_split_varlen(x, causal, (1, 2, 3, 7)[i % 4], scale)
+    ro, rl = oracle.attn_fwd_varlen(x["q"], x["k"], x["v"], x["cu_q"], x["cu_k"], causal, scale)
+    assert o_err(o, ro) <= O_MAX_ABS, f"O error {o_err(o, ro):.3e}"
+    assert lse_err(lse, rl) <= LSE_REL
