@@ -546,6 +546,45 @@ def pin_dropout_bwd_finite_differences(orc):
             assert err < 1e-6, f"dropout {name} vs finite differences (causal={causal}): {err:.2e}"
 
 
+def pin_dropout_head_offset(orc):
+    """Several heads with a head offset bh0: head h of the arrays draws the mask of head
+    bh0 + h.  Forward by brute force with the keep factors of those heads; backward by
+    central differences of sum(dO * O) at the same offset (a packed batch's sequence b
+    is computed as heads b*H .. b*H + H - 1 this way)."""
+    rng = np.random.default_rng(39)
+    H, N, Nk, d, t, seed, bh0, sc = 3, 4, 6, 3, 77, 0xABC0123, 5, 0.9
+    q = rng.uniform(-1, 1, (H, N, d))
+    k = rng.uniform(-1, 1, (H, Nk, d))
+    v = rng.uniform(-2, 2, (H, Nk, d))
+    o, _ = orc.attn_fwd_dropout(q, k, v, True, sc, t, seed, bh0=bh0)
+    for h in range(H):
+        for i in range(N):
+            keys = range(i + Nk - N + 1)
+            w = {j: math.exp(sc * math.fsum(q[h][i][x] * k[h][j][x] for x in range(d))) for j in keys}
+            z = math.fsum(w.values())
+            for c in range(d):
+                ref = math.fsum(w[j] / z * orc.dropout_factor(bh0 + h, i, j, t, seed) * v[h][j][c] for j in keys)
+                assert abs(o[h][i][c] - ref) <= 1e-12 * max(1.0, abs(ref)), f"head offset O[{h},{i},{c}]"
+    H, N, Nk, d = 2, 3, 4, 2
+    q, do = (rng.normal(size=(H, N, d)) for _ in range(2))
+    k, v = (rng.normal(size=(H, Nk, d)) for _ in range(2))
+    grads = orc.attn_bwd_dropout(q, k, v, do, True, sc, t, seed, bh0=bh0)
+    hstep = 1e-6
+    for name, x, g in zip(("dQ", "dK", "dV"), (q, k, v), grads):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += hstep
+            xm[idx] -= hstep
+            ap = {"dQ": (xp, k, v), "dK": (q, xp, v), "dV": (q, k, xp)}[name]
+            am = {"dQ": (xm, k, v), "dK": (q, xm, v), "dV": (q, k, xm)}[name]
+            lp = np.sum(do * orc.attn_fwd_dropout(*ap, True, sc, t, seed, bh0=bh0)[0])
+            lm = np.sum(do * orc.attn_fwd_dropout(*am, True, sc, t, seed, bh0=bh0)[0])
+            num[idx] = (lp - lm) / (2 * hstep)
+        err = np.max(np.abs(num - g)) / max(1e-3, np.max(np.abs(g)))
+        assert err < 1e-6, f"head-offset dropout {name} vs finite differences: {err:.2e}"
+
+
 # ---------------------------------------------------------------------------
 # variable-length packed sequences
 
@@ -583,5 +622,5 @@ ALL_PINS = [
     pin_fp8_attention_brute_force, pin_rect_causal_is_a_suffix,
     pin_philox_known_answers, pin_dropout_mask_definition, pin_dropout_rate_and_unbiased,
     pin_dropout_t0_is_plain, pin_dropout_brute_force, pin_dropout_bwd_finite_differences,
-    pin_varlen_brute_force,
+    pin_dropout_head_offset, pin_varlen_brute_force,
 ]

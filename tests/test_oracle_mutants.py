@@ -47,6 +47,10 @@ MUTANTS = [
     ("dropout row term without the keep factor", "acc += p * z * dpt;", "acc += p * dpt;"),
     ("dropout dV without the keep factor", "gv[x] += p * z * doh[i * d + x];", "gv[x] += p * doh[i * d + x];"),
     ("dropout dS without the keep factor", "double ds = p * (z * dpt - c[i]);", "double ds = p * (dpt - c[i]);"),
+    ("dropout forward ignores the head offset", "double pz = exp(s[j] - m) / l * oracle_dropout_factor(bh0 + bh,",
+     "double pz = exp(s[j] - m) / l * oracle_dropout_factor(bh,"),
+    ("dropout backward ignores the head offset", "double z = oracle_dropout_factor(bh0 + bh, i, j, t, seed_lo, seed_hi);",
+     "double z = oracle_dropout_factor(bh, i, j, t, seed_lo, seed_hi);"),
 ]
 
 
