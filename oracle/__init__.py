@@ -275,6 +275,55 @@ class Oracle:
         return shp(dq, nq), shp(dk, nk), shp(dv, nk)
 
 
+    def _degenerate(self, nq: int, nk: int, causal: bool) -> bool:
+        """A packed sequence whose rows have no defined softmax: no keys, or causal with
+        fewer keys than queries (some query would see no key)."""
+        return nk == 0 or (causal and nk < nq)
+
+    def attn_fwd_varlen(self, q, k, v, cu_q, cu_k, causal: bool, scale: float):
+        """Variable-length packed attention: q [Tq, H, d], k, v [Tk, H, d], sequence b owning query
+        tokens cu_q[b] .. cu_q[b+1]-1 and key tokens cu_k[b] .. cu_k[b+1]-1.  Each sequence and head
+        is attn_fwd of its own slices (causal aligned to the sequence's last key).  A sequence
+        without keys, or causal with fewer keys than queries, gets O = 0 and lse = -inf on
+        every row (the library's stated convention for rows with no defined softmax).
+        Returns (o [Tq, H, d], lse [H, Tq])."""
+        q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+        cq, ck = _cu(cu_q), _cu(cu_k)
+        Tq, H, d = q.shape
+        o = np.zeros_like(q)
+        lse = np.zeros((H, Tq))
+        for b in range(len(cq) - 1):
+            qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+            nq, nk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+            if nq == 0:
+                continue
+            if self._degenerate(nq, nk, causal):
+                lse[:, qs] = -np.inf
+                continue
+            t = lambda x, s_: x[s_].transpose(1, 0, 2)
+            ob, lb = self.attn_fwd(t(q, qs), t(k, ks), t(v, ks), causal, scale)
+            o[qs] = ob.transpose(1, 0, 2)
+            lse[:, qs] = lb
+        return o, lse
+
+    def attn_bwd_varlen(self, q, k, v, dout, cu_q, cu_k, causal: bool, scale: float):
+        """Gradients of sum(dO * O) for attn_fwd_varlen: (dq [Tq, H, d], dk, dv [Tk, H, d]).  Each
+        sequence is attn_bwd of its own slices; a degenerate sequence (see attn_fwd_varlen) has
+        a constant output, so its gradients are zero."""
+        q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+        cq, ck = _cu(cu_q), _cu(cu_k)
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for b in range(len(cq) - 1):
+            qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+            nq, nk = cq[b + 1] - cq[b], ck[b + 1] - ck[b]
+            if nq == 0 or self._degenerate(nq, nk, causal):
+                continue
+            t = lambda x, s_: x[s_].transpose(1, 0, 2)
+            gq, gk, gv = self.attn_bwd(t(q, qs), t(k, ks), t(v, ks), t(do, qs), causal, scale)
+            dq[qs], dk[ks], dv[ks] = gq.transpose(1, 0, 2), gk.transpose(1, 0, 2), gv.transpose(1, 0, 2)
+        return dq, dk, dv
+
+
 def default() -> Oracle:
     """The oracle built from this package's source (compiled on first use)."""
     global _default
@@ -333,35 +382,12 @@ def _cu(cu):
 
 
 def attn_fwd_varlen(q, k, v, cu_q, cu_k, causal: bool, scale: float):
-    """Variable-length packed attention: q [Tq, H, d], k, v [Tk, H, d], sequence b owning query
-    tokens cu_q[b] .. cu_q[b+1]-1 and key tokens cu_k[b] .. cu_k[b+1]-1.  Each sequence and head
-    is attn_fwd of its own slices (causal aligned to the sequence's last key).  Returns
-    (o [Tq, H, d], lse [H, Tq])."""
-    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
-    cq, ck = _cu(cu_q), _cu(cu_k)
-    Tq, H, d = q.shape
-    o = np.zeros_like(q)
-    lse = np.zeros((H, Tq))
-    for b in range(len(cq) - 1):
-        qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
-        if cq[b + 1] == cq[b]:
-            continue
-        ob, lb = attn_fwd(q[qs].transpose(1, 0, 2), k[ks].transpose(1, 0, 2), v[ks].transpose(1, 0, 2), causal, scale)
-        o[qs] = ob.transpose(1, 0, 2)
-        lse[:, qs] = lb
-    return o, lse
+    return default().attn_fwd_varlen(q, k, v, cu_q, cu_k, causal, scale)
 
 
 def attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, causal: bool, scale: float):
-    """Gradients of sum(dO * O) for attn_fwd_varlen: (dq [Tq, H, d], dk, dv [Tk, H, d])."""
-    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
-    cq, ck = _cu(cu_q), _cu(cu_k)
-    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
-    for b in range(len(cq) - 1):
-        qs, ks = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
-        if cq[b + 1] == cq[b] or ck[b + 1] == ck[b]:
-            continue
-        t = lambda x, s_: x[s_].transpose(1, 0, 2)
-        gq, gk, gv = attn_bwd(t(q, qs), t(k, ks), t(v, ks), t(do, qs), causal, scale)
-        dq[qs], dk[ks], dv[ks] = gq.transpose(1, 0, 2), gk.transpose(1, 0, 2), gv.transpose(1, 0, 2)
-    return dq, dk, dv
+    return default().attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, causal, scale)
+
+
+attn_fwd_varlen.__doc__ = Oracle.attn_fwd_varlen.__doc__
+attn_bwd_varlen.__doc__ = Oracle.attn_bwd_varlen.__doc__

@@ -591,26 +591,62 @@ def pin_dropout_head_offset(orc):
 
 def pin_varlen_brute_force(orc):
     """Packed sequences [tokens, H, d] with offsets: brute force per sequence and head with
-    Python floats, including an empty sequence and, with causal, Nk > Nq per sequence."""
-    import oracle as oracle_mod
-
+    Python floats, including an empty sequence and, with causal, Nk > Nq per sequence; a
+    sequence with no keys (and, causal, one with fewer keys than queries) gives O = 0 and
+    lse = -inf on its rows."""
     rng = np.random.default_rng(38)
     H, d = 2, 3
-    cu_q, cu_k = [0, 3, 3, 8], [0, 5, 7, 13]
+    cu_q, cu_k = [0, 3, 3, 8, 10, 13], [0, 5, 7, 13, 13, 15]
     q = rng.uniform(-1, 1, (cu_q[-1], H, d))
     k = rng.uniform(-1, 1, (cu_k[-1], H, d))
     v = rng.uniform(-2, 2, (cu_k[-1], H, d))
     for causal in (False, True):
-        o, lse = oracle_mod.attn_fwd_varlen(q, k, v, cu_q, cu_k, causal, 0.8)
-        for b in range(3):
+        o, lse = orc.attn_fwd_varlen(q, k, v, cu_q, cu_k, causal, 0.8)
+        for b in range(len(cu_q) - 1):
+            nq, nk = cu_q[b + 1] - cu_q[b], cu_k[b + 1] - cu_k[b]
             for h in range(H):
                 qb = q[cu_q[b]:cu_q[b + 1], h].tolist()
                 if not qb:
+                    continue
+                if nk == 0 or (causal and nk < nq):
+                    assert np.all(o[cu_q[b]:cu_q[b + 1], h] == 0.0), f"degenerate seq {b}: O not zero"
+                    assert np.all(np.isneginf(lse[h, cu_q[b]:cu_q[b + 1]])), f"degenerate seq {b}: lse not -inf"
                     continue
                 kb, vb = k[cu_k[b]:cu_k[b + 1], h].tolist(), v[cu_k[b]:cu_k[b + 1], h].tolist()
                 bo, bl = brute_force_fwd(qb, kb, vb, causal, 0.8)
                 _close(o[cu_q[b]:cu_q[b + 1], h], bo, 1e-12, f"varlen O seq {b} head {h} causal={causal}")
                 _close(lse[h, cu_q[b]:cu_q[b + 1]], bl, 1e-12, f"varlen LSE seq {b} head {h}")
+
+
+def pin_varlen_bwd_finite_differences(orc):
+    """Central differences of L = sum(dO * O) over every element of the packed q, k and v,
+    O from the packed forward (itself pinned by brute force above), match the packed
+    backward.  The batch holds a sequence with Nk > Nq, one without queries, a square one,
+    one without keys and one with fewer keys than queries (degenerate when causal), so a
+    gradient written to the wrong slice, a sequence skipped or a mask misaligned shows up
+    as a mismatch ("Understanding FlashAttention, Part 2", section 2.4: the backward is the
+    chain rule of the forward)."""
+    rng = np.random.default_rng(44)
+    H, d = 2, 3
+    cu_q, cu_k = [0, 3, 3, 7, 9, 12], [0, 5, 7, 11, 11, 13]
+    Tq, Tk = cu_q[-1], cu_k[-1]
+    q, do = rng.normal(size=(Tq, H, d)), rng.normal(size=(Tq, H, d))
+    k, v = rng.normal(size=(Tk, H, d)), rng.normal(size=(Tk, H, d))
+    scale, h = 0.7, 1e-6
+    for causal in (False, True):
+        dq, dk, dv = orc.attn_bwd_varlen(q, k, v, do, cu_q, cu_k, causal, scale)
+        for name, x, g in (("dQ", q, dq), ("dK", k, dk), ("dV", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(*x.shape):
+                vals = []
+                for sgn in (1.0, -1.0):
+                    xs = x.copy()
+                    xs[idx] += sgn * h
+                    args = {"dQ": (xs, k, v), "dK": (q, xs, v), "dV": (q, k, xs)}[name]
+                    vals.append(np.sum(do * orc.attn_fwd_varlen(*args, cu_q, cu_k, causal, scale)[0]))
+                num[idx] = (vals[0] - vals[1]) / (2 * h)
+            err = np.max(np.abs(num - g)) / max(1e-3, np.max(np.abs(g)))
+            assert err < 1e-6, f"packed {name} vs finite differences (causal={causal}): {err:.2e}"
 
 
 ALL_PINS = [
@@ -622,5 +658,5 @@ ALL_PINS = [
     pin_fp8_attention_brute_force, pin_rect_causal_is_a_suffix,
     pin_philox_known_answers, pin_dropout_mask_definition, pin_dropout_rate_and_unbiased,
     pin_dropout_t0_is_plain, pin_dropout_brute_force, pin_dropout_bwd_finite_differences,
-    pin_dropout_head_offset, pin_varlen_brute_force,
+    pin_dropout_head_offset, pin_varlen_brute_force, pin_varlen_bwd_finite_differences,
 ]

@@ -1,6 +1,8 @@
 """Plant plausible mistakes in a private copy of the oracle's C source and check that
 the pins catch every one of them (a pin that passes a broken oracle pins nothing)."""
+import importlib.util
 import os
+import shutil
 
 import pytest
 
@@ -63,6 +65,40 @@ def test_pins_catch_mutant(tmp_path, desc, old, new):
     open(c_path, "w").write(mutated)
     lib = oracle.build(force=True, src=c_path, out=os.path.join(tmp_path, "libmutant.so"))
     orc = oracle.Oracle(lib)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, RuntimeError, ValueError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the mutant '{desc}'"
+
+
+# Mistakes in the Python composition of the packed-batch oracle (oracle/__init__.py):
+# (description, text, replacement), applied to a private copy of the module.
+PY_MUTANTS = [
+    ("packed dK taken from dV", "gq.transpose(1, 0, 2), gk.transpose(1, 0, 2), gv.transpose(1, 0, 2)",
+     "gq.transpose(1, 0, 2), gv.transpose(1, 0, 2), gv.transpose(1, 0, 2)"),
+    ("packed dK scattered into the query slice", "dq[qs], dk[ks], dv[ks] =", "dq[qs], dk[qs], dv[ks] ="),
+    ("packed backward skips sequences with Nk != Nq", "if nq == 0 or self._degenerate(nq, nk, causal):",
+     "if nq == 0 or nq != nk or self._degenerate(nq, nk, causal):"),
+    ("packed backward ignores the causal flag", "t(do, qs), causal, scale)", "t(do, qs), False, scale)"),
+    ("packed forward: degenerate rows get lse 0", "lse[:, qs] = -np.inf", "lse[:, qs] = 0.0"),
+]
+
+
+@pytest.mark.parametrize("desc,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_pins_catch_python_mutant(tmp_path, desc, old, new):
+    src = open(os.path.join(os.path.dirname(oracle.SOURCE), "__init__.py")).read()
+    assert old in src, f"mutation site for '{desc}' not found in the oracle module"
+    pkg = os.path.join(tmp_path, "oracle_mutant")
+    os.makedirs(pkg)
+    open(os.path.join(pkg, "__init__.py"), "w").write(src.replace(old, new))
+    shutil.copy(oracle.SOURCE, os.path.join(pkg, "attn_oracle.c"))
+    spec = importlib.util.spec_from_file_location("oracle_mutant_%d" % abs(hash(desc)), os.path.join(pkg, "__init__.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    orc = mod.Oracle(oracle.default().path)
     caught = []
     for pin in pins.ALL_PINS:
         try:
