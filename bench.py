@@ -76,8 +76,73 @@ def step_flops(w):
 # ---------------------------------------------------------------- clocks
 
 
-class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (read-only queries) every 2 ms
+    while the timed region runs, so that even a timed region of a few tens of
+    milliseconds collects a dozen samples or more.  The device is found by its UUID, so
+    CUDA_VISIBLE_DEVICES renumbering does not matter."""
+
+    # nvmlClocksEventReasons bits
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+    PERIOD_S = 0.002
+
+    def __init__(self, dev):
+        import ctypes
+
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return
+        self.ct = ctypes
+        self.lib = lib
+        if lib.nvmlInit_v2() != 0:
+            return
+        self.h = ctypes.c_void_p()
+        uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+        found = False
+        if uuid is not None:
+            u = str(uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            found = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.h)) == 0
+        if not found and lib.nvmlDeviceGetHandleByIndex_v2(int(dev.index or 0), ctypes.byref(self.h)) != 0:
+            return
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 else None
+        self.ok = True
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        ct, lib = self.ct, self.lib
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            t = time.time()
+            if lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(clk)) == 0:  # NVML_CLOCK_SM
+                r = int(rs.value) if get_reasons(self.h, ct.byref(rs)) == 0 else 0
+                self.samples.append((t, float(clk.value), r))
+            time.sleep(self.PERIOD_S)
+
+    def stop(self, t0, t1):
+        if not self.ok:
+            return None
+        self._stop.set()
+        self.thread.join(timeout=2)
+        rows = [(c, r) for t, c, r in self.samples if t0 <= t <= t1]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml"}
+        reasons = sorted({n for _, r in rows for n, b in self.BITS.items() if r & b})
+        return {"sm_mhz": statistics.median(c for c, _ in rows), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(rows), "source": "nvml, every 2 ms"}
+
+
+class SmiClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs
+    (used where NVML cannot be loaded directly)."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -114,13 +179,18 @@ class ClockSampler:
                 continue
             rows.append(parts)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": "nvidia-smi"}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "source": "nvidia-smi, every 100 ms"}
+
+
+def clock_sampler(dev):
+    s = NvmlClockSampler(dev)
+    return s if s.ok else SmiClockSampler(dev.index or 0)
 
 
 # ---------------------------------------------------------------- peaks and profiles
@@ -214,7 +284,7 @@ def run_ours(args, w, ws_, rank, local):
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = clock_sampler(dev) if rank == 0 else None
     if sampler is not None:
         time.sleep(0.3)
     barrier(ws_)
