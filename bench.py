@@ -3,8 +3,8 @@
 
 Workload (the fwd/bwd configuration): B=2, H=16, N=8192, d=128, BF16, causal,
 Q, K, V, dO iid N(0,1) from a fixed seed.  One step = attn_fwd followed by the
-three backward stages (prepare, dK/dV, dQ) through the C ABI, inputs resident
-in HBM.  FLOPs per step are the algorithmic count: forward 4*B*H*N^2*d plus
+three stages of attn_bwd (prepare, the fused dK/dV/dQ pass, the dQ finish)
+through the C ABI, inputs resident in HBM.  FLOPs per step are the algorithmic count: forward 4*B*H*N^2*d plus
 backward 10*B*H*N^2*d, both halved for causal.  The inputs (4 x 64 MiB) exceed
 the 129 MB L2, so no flush runs between steps.
 
@@ -205,7 +205,8 @@ def peaks():
         return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {"fwd": ["fwd.cu"], "bwd_prepare": ["bwd.cu"], "bwd_dkdv": ["bwd.cu"], "bwd_dq": ["bwd.cu"]}
+KERNEL_SOURCES = {"fwd": ["fwd.cu"], "bwd_prepare": ["bwd.cu"], "bwd_dkdvdq": ["bwd_fused.cu", "bwd_common.cuh"],
+                  "bwd_dq_finish": ["bwd_fused.cu"]}
 
 
 def source_digest(kernel: str):
@@ -256,7 +257,7 @@ def run_ours(args, w, ws_, rank, local):
         if rc != attn.ATTN_OK:
             raise RuntimeError(f"{what}: {attn.attn_status_string(rc)}")
 
-    names = ["fwd", "bwd_prepare", "bwd_dkdv", "bwd_dq"]
+    names = ["fwd", "bwd_prepare", "bwd_dkdvdq", "bwd_dq_finish"]
 
     def step(ev=None):
         if ev is not None:
@@ -267,12 +268,11 @@ def run_ours(args, w, ws_, rank, local):
         check(attn.attn_bwd_prepare(o, do, lse, wsp, nbytes, B, H, N, d, dt, stream), "attn_bwd_prepare")
         if ev is not None:
             ev[2].record(stream)
-        check(attn.attn_bwd_dkdv(q, k, v, do, wsp, nbytes, dk, dv, B, H, N, d, dt, True, scale, status, stream),
-              "attn_bwd_dkdv")
+        check(attn.attn_bwd_dkdvdq(q, k, v, do, wsp, nbytes, dk, dv, B, H, N, d, dt, True, scale, status, stream),
+              "attn_bwd_dkdvdq")
         if ev is not None:
             ev[3].record(stream)
-        check(attn.attn_bwd_dq(q, k, v, do, wsp, nbytes, dq, B, H, N, d, dt, True, scale, status, stream),
-              "attn_bwd_dq")
+        check(attn.attn_bwd_dq_finish(wsp, nbytes, dq, B, H, N, d, dt, scale, stream), "attn_bwd_dq_finish")
         if ev is not None:
             ev[4].record(stream)
 
@@ -306,8 +306,10 @@ def run_ours(args, w, ws_, rank, local):
 
     # Algorithmic FLOPs per launch (causal halves every N x N product):
     unit = 2.0 * B * H * N * N * d / 2          # one N x N x d product, causal
-    kflops = {"fwd": 2 * unit, "bwd_prepare": 0.0, "bwd_dkdv": 4 * unit, "bwd_dq": 1 * unit}
-    kbytes = {"bwd_prepare": 2 * B * H * N * d * 2 + B * H * N * 4 + nbytes}   # read O, dO, lse; write D, LSE2
+    kflops = {"fwd": 2 * unit, "bwd_prepare": 0.0, "bwd_dkdvdq": 5 * unit, "bwd_dq_finish": 0.0}
+    # read O, dO, lse; write D, LSE2 and clear the dQ accumulator (the whole workspace)
+    kbytes = {"bwd_prepare": 2 * B * H * N * d * 2 + B * H * N * 4 + nbytes,
+              "bwd_dq_finish": B * H * N * d * (4 + 2)}                         # read the accumulator, write dQ
     flops = step_flops(w)
     value = ws_ * args.steps * flops / (elapsed_ms * 1e-3) / 1e12
     pk = peaks()

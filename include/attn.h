@@ -275,12 +275,18 @@ ATTN_API attn_status attn_fwd_fp8(const void *q8, const void *k8, const void *v8
                          int *dev_status, void *stream);
 
 /*
- * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd needs:
- * two float32 vectors per row (D_i = rowsum(dO_i * O_i), and the logsumexp in
- * base 2), padded to whole 128-row tiles: 2 * B*H*ceil(N/128)*128 * 4 bytes.
- * Returns 0 for invalid sizes.
+ * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd needs: two float32
+ * values per row (D_i = rowsum(dO_i * O_i), and the logsumexp in base 2) and, for
+ * d in {64, 128}, the float32 dQ accumulator of the fused backward (d values per row),
+ * rows padded to whole 128-row tiles: (2 + d) * B*H*ceil(N/128)*128 * 4 bytes
+ * (d = 256: 2 * B*H*ceil(N/128)*128 * 4 bytes).  Returns 0 for invalid sizes.
+ *
+ * attn_bwd_deterministic_workspace_bytes -- the two per-row values only:
+ * 2 * B*H*ceil(N/128)*128 * 4 bytes (attn_bwd_deterministic and the stage entry points
+ * attn_bwd_prepare / attn_bwd_dkdv / attn_bwd_dq).
  */
 ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+ATTN_API size_t attn_bwd_deterministic_workspace_bytes(int B, int H, int N, int d);
 
 /*
  * attn_bwd -- backward pass: gradients of a loss L given dout = dL/dO.
@@ -296,15 +302,53 @@ ATTN_API size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  *                      16-byte aligned; contents need not be initialised and
  *                      are clobbered.  The caller owns it.
  *   Outputs must not overlap inputs or each other.
- *   d in {64, 128, 256}.  At d = 256 the gradients come from three kernels (dV and dK,
- *   one 128-key tile per CTA each, and dQ, one 128-query tile per CTA), each
- *   streaming its operands in 128-column halves: the same gradients, in more passes.
+ *   d in {64, 128}: one pass over each 128-key tile's query tiles computes dK, dV and
+ *   dQ from the same recomputed tiles (five N x N x d products per tile pair, the
+ *   algorithm's count); dQ is summed over the key tiles in the float32 accumulator of
+ *   the workspace with floating-point atomic additions and then rounded to dt.  The
+ *   order of those additions varies from run to run, so dQ may differ in its last bit
+ *   between two identical calls (dK and dV do not); attn_bwd_deterministic gives
+ *   identical bytes on every call, at seven products per tile pair.
+ *   d = 256: the gradients come from three kernels (dV and dK, one 128-key tile per CTA
+ *   each, and dQ, one 128-query tile per CTA), each streaming its operands in
+ *   128-column halves: deterministic, the same gradients in more passes.
  */
 ATTN_API attn_status attn_bwd(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, void *dq, void *dk, void *dv,
                      void *workspace, size_t workspace_bytes,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
                      int *dev_status, void *stream);
+
+/*
+ * attn_bwd_deterministic -- attn_bwd whose results are the same bytes on every call:
+ * dK and dV from one kernel over key tiles, dQ from one over query tiles (which
+ * recomputes S and dP in that order: seven products per tile pair instead of five), no
+ * atomics.  Workspace: attn_bwd_deterministic_workspace_bytes().  Everything else is as
+ * for attn_bwd.
+ */
+ATTN_API attn_status attn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                   const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                                   void *workspace, size_t workspace_bytes,
+                                   int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                                   int *dev_status, void *stream);
+
+/*
+ * The fused stages attn_bwd runs at d in {64, 128}, in order, on one stream, after
+ * attn_bwd_prepare with a workspace of attn_bwd_workspace_bytes() (which then also
+ * clears the dQ accumulator).  Exported so that a caller can time them one by one.
+ *
+ * attn_bwd_dkdvdq    -- dK and dV, and each key tile's share of dQ added to the
+ *                       workspace's float32 accumulator; one 128-key tile per CTA.
+ * attn_bwd_dq_finish -- dQ = scale * accumulator, rounded to dt.
+ * Argument meanings, layouts and errors are those of attn_bwd; d = 256 returns
+ * ATTN_ERR_UNSUPPORTED.
+ */
+ATTN_API attn_status attn_bwd_dkdvdq(const void *q, const void *k, const void *v, const void *dout,
+                            void *workspace, size_t workspace_bytes, void *dk, void *dv,
+                            int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                            int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_dq_finish(const void *workspace, size_t workspace_bytes, void *dq,
+                               int B, int H, int N, int d, attn_dtype dt, float scale, void *stream);
 
 /*
  * attn_bwd_rect -- attn_bwd for attn_fwd_rect's shapes: q, o, dout, dq [B][H][Nq][d],
@@ -319,15 +363,18 @@ ATTN_API attn_status attn_bwd_rect(const void *q, const void *k, const void *v, 
                           int *dev_status, void *stream);
 
 /*
- * The three stages attn_bwd runs, in order, on one stream.  They are exported
- * so that a caller can time them one by one or run the two independent
+ * The three stages attn_bwd_deterministic runs, in order, on one stream.  They are
+ * exported so that a caller can time them one by one or run the two independent
  * gradient stages on two streams once the preparation has finished.  Argument
- * meanings, layouts and errors are those of attn_bwd.
+ * meanings, layouts and errors are those of attn_bwd_deterministic (workspace of at
+ * least attn_bwd_deterministic_workspace_bytes()).
  *
  * attn_bwd_prepare -- fills the workspace: D_i = rowsum(dO_i * O_i) (the
  *   softmax-Jacobian row term of "Understanding FlashAttention, Part 2",
  *   section 2.4, Fig 18) and the logsumexp in base 2, for every row; rows of
- *   the last partial 128-row tile get D = 0 and an infinite logsumexp.
+ *   the last partial 128-row tile get D = 0 and an infinite logsumexp.  When
+ *   d is 64 or 128 and workspace_bytes >= attn_bwd_workspace_bytes(), it also
+ *   clears the fused backward's dQ accumulator (the first of attn_bwd's stages).
  * attn_bwd_dkdv -- dK and dV, one 128-key tile per CTA (reads the workspace; at
  *   d = 256 two launches, dV then dK).
  * attn_bwd_dq   -- dQ, one 128-query tile per CTA (reads the workspace).
@@ -358,16 +405,20 @@ ATTN_API attn_status attn_bwd_dq(const void *q, const void *k, const void *v, co
  * device image instead; every GPU that loads the library holds that array
  * until the process exits.  The caller still passes every input and output.
  *
- *  - Arguments, layouts and results are those of attn_bwd without the
- *    workspace pair; the results equal attn_bwd's (same kernels).
- *  - Limit: the workspace attn_bwd would need, attn_bwd_workspace_bytes(B, H,
- *    N, d) = 8 * B*H*ceil(N/128)*128 bytes, must fit in the array, i.e.
- *    B*H*ceil(N/128)*128 <= 1048576 rows (for example 128 heads of N = 8192).
- *    Larger sizes return ATTN_ERR_INVALID_ARG before anything is launched.
- *  - It calls no cudaMalloc, cudaFree or other allocating routine.  The first
- *    call on each device looks up the array's device address once, with that
- *    device current (cudaGetSymbolAddress); make that first call before any
- *    stream capture.
+ *  - Arguments and layouts are those of attn_bwd without the workspace pair.  It
+ *    runs the kernels of attn_bwd_deterministic, which need the smaller workspace,
+ *    so its results equal attn_bwd_deterministic's byte for byte.
+ *  - Limit: the workspace attn_bwd_deterministic would need,
+ *    attn_bwd_deterministic_workspace_bytes(B, H, N, d) = 8 * B*H*ceil(N/128)*128
+ *    bytes, must fit in the array, i.e. B*H*ceil(N/128)*128 <= 1048576 rows (for
+ *    example 128 heads of N = 8192).  Larger sizes return ATTN_ERR_INVALID_ARG
+ *    before anything is launched.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine.  Every call
+ *    looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress, a lookup that allocates nothing), so the address is
+ *    right for whichever device is current and stays right after a
+ *    cudaDeviceReset.  The first call on a device may load the library's device
+ *    code; make it before any stream capture.
  *  - Every call shares the one array and it keeps the last call's contents;
  *    nothing needs clearing because the preparation stage rewrites every value
  *    the gradient stages read.  Calls that overlap on the GPU (on different

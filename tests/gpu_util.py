@@ -72,16 +72,19 @@ def run_fwd_fp8(x, causal, scale=None, out_dtype=torch.bfloat16, stream=None):
     return o.t, lse.t
 
 
-def run_bwd(q, k, v, o, lse, dout, causal, scale=None, stream=None):
-    """attn_bwd through the C ABI with guarded outputs; returns (dq, dk, dv)."""
+def run_bwd(q, k, v, o, lse, dout, causal, scale=None, stream=None, deterministic=False):
+    """attn_bwd (or attn_bwd_deterministic) through the C ABI with guarded outputs; returns
+    (dq, dk, dv)."""
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     outs = [Guarded((B, H, N, d), q.dtype) for _ in range(3)]
-    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    size = attn.attn_bwd_deterministic_workspace_bytes if deterministic else attn.attn_bwd_workspace_bytes
+    call = attn.attn_bwd_deterministic if deterministic else attn.attn_bwd
+    nbytes = size(B, H, N, d)
     ws = Guarded((nbytes // 4,), torch.float32)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = attn.attn_bwd(q, k, v, o, dout, lse, outs[0].t, outs[1].t, outs[2].t, ws.t, nbytes, B, H, N, d,
-                       q.dtype, causal, scale, status, stream)
+    rc = call(q, k, v, o, dout, lse, outs[0].t, outs[1].t, outs[2].t, ws.t, nbytes, B, H, N, d,
+              q.dtype, causal, scale, status, stream)
     assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
@@ -149,3 +152,22 @@ def sample_rows(N, extra=24, seed=0):
         rows = sorted(set(rng.choice(rows, 40, replace=False).tolist()) | {0, N - 1})
     rows = sorted(set(rows) | set(rng.integers(0, N, extra).tolist()))
     return np.array(rows, dtype=np.int64)
+
+
+def dq_close(a, b) -> bool:
+    """Two dQ results of the fused backward, whose float32 accumulator adds the key tiles'
+    shares in an order that varies from run to run: equal up to the rounding that order
+    can move (one 16-bit step of the value, plus a cancellation allowance scaled by the
+    tensor's largest entry)."""
+    x, y = f64(a), f64(b)
+    tol = 2.0 ** -7 * np.abs(y) + 1e-4 * float(np.max(np.abs(y)) if y.size else 0.0)
+    return bool(np.all(np.abs(x - y) <= tol))
+
+
+def assert_same_grads(got, want, what=""):
+    """dK and dV byte for byte; dQ as dq_close allows (the fused backward's accumulator)."""
+    dq, dk, dv = got
+    rq, rk, rv = want
+    assert torch.equal(dk, rk), f"{what} dK differs"
+    assert torch.equal(dv, rv), f"{what} dV differs"
+    assert dq_close(dq, rq), f"{what} dQ differs beyond the accumulator's reordering"

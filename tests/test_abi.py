@@ -41,12 +41,17 @@ def test_status_strings():
 
 
 def test_workspace_size():
-    assert attn.attn_bwd_workspace_bytes(2, 16, 8192, 128) == 2 * 32 * 8192 * 4
-    assert attn.attn_bwd_workspace_bytes(2, 8, 4097, 128) == 2 * 16 * 4224 * 4
-    assert attn.attn_bwd_workspace_bytes(1, 1, 1, 64) == 2 * 128 * 4
+    # two float32 values per padded row, plus d float32 dQ-accumulator values for d <= 128
+    assert attn.attn_bwd_workspace_bytes(2, 16, 8192, 128) == (2 + 128) * 32 * 8192 * 4
+    assert attn.attn_bwd_workspace_bytes(2, 8, 4097, 128) == (2 + 128) * 16 * 4224 * 4
+    assert attn.attn_bwd_workspace_bytes(1, 1, 1, 64) == (2 + 64) * 128 * 4
     assert attn.attn_bwd_workspace_bytes(1, 1, 0, 64) == 0
     assert attn.attn_bwd_workspace_bytes(1, 1, 16, 96) == 0
     assert attn.attn_bwd_workspace_bytes(1, 2, 300, 256) == 2 * 2 * 384 * 4
+    assert attn.attn_bwd_deterministic_workspace_bytes(2, 16, 8192, 128) == 2 * 32 * 8192 * 4
+    assert attn.attn_bwd_deterministic_workspace_bytes(2, 8, 4097, 64) == 2 * 16 * 4224 * 4
+    assert attn.attn_bwd_deterministic_workspace_bytes(1, 2, 300, 256) == 2 * 2 * 384 * 4
+    assert attn.attn_bwd_deterministic_workspace_bytes(1, 1, 16, 96) == 0
 
 
 # fake, aligned, non-overlapping "device" addresses: validation fails before any CUDA call
@@ -89,6 +94,8 @@ def test_fwd_rejects(kw, status):
     (dict(dq=0), attn.ATTN_ERR_INVALID_ARG),
     (dict(workspace=0), attn.ATTN_ERR_INVALID_ARG),
     (dict(workspace_bytes=2 * 2 * 256 * 4 - 4), attn.ATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=(2 + 128) * 2 * 256 * 4 - 4), attn.ATTN_ERR_INVALID_ARG),  # no room for the dQ accumulator
+    (dict(dq=A[9] + 2 * 2 * 256 * 4), attn.ATTN_ERR_INVALID_ARG),  # dq inside the dQ accumulator
     (dict(dk=A[6]), attn.ATTN_ERR_INVALID_ARG),              # two outputs alias
     (dict(dv=A[2]), attn.ATTN_ERR_INVALID_ARG),              # output aliases an input
     (dict(workspace=A[0]), attn.ATTN_ERR_INVALID_ARG),       # workspace aliases an input
@@ -99,6 +106,25 @@ def test_fwd_rejects(kw, status):
 ])
 def test_bwd_rejects(kw, status):
     assert bwd(**kw) == status
+
+
+def test_deterministic_and_fused_stages_validate():
+    det = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], dq=A[6], dk=A[7], dv=A[8], workspace=A[9],
+               workspace_bytes=2 * 2 * 256 * 4 - 4, B=1, H=2, N=256, d=128, dt=0, causal=1, scale=0.088, stream=0)
+    assert attn.attn_bwd_deterministic(**det) == attn.ATTN_ERR_INVALID_ARG           # workspace one value short
+    assert attn.attn_bwd_deterministic(**dict(det, workspace_bytes=1 << 20, dk=A[6])) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd_deterministic(**dict(det, workspace_bytes=1 << 20, d=80)) == attn.ATTN_ERR_UNSUPPORTED
+    full = attn.attn_bwd_workspace_bytes(1, 2, 256, 128)
+    assert attn.attn_bwd_dkdvdq(A[0], A[1], A[2], A[4], A[9], full - 4, A[7], A[8], 1, 2, 256, 128, 0, 1, 0.1,
+                                stream=0) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd_dkdvdq(A[0], A[1], A[2], A[4], A[9], full, A[7], A[7], 1, 2, 256, 128, 0, 1, 0.1,
+                                stream=0) == attn.ATTN_ERR_INVALID_ARG                # dk == dv
+    assert attn.attn_bwd_dkdvdq(A[0], A[1], A[2], A[4], A[9], 1 << 24, A[7], A[8], 1, 2, 256, 256, 0, 1, 0.1,
+                                stream=0) == attn.ATTN_ERR_UNSUPPORTED                # no fused path at d = 256
+    assert attn.attn_bwd_dq_finish(A[9], full - 4, A[6], 1, 2, 256, 128, 0, 0.1, stream=0) == attn.ATTN_ERR_INVALID_ARG
+    assert attn.attn_bwd_dq_finish(A[9], full, A[9] + 64, 1, 2, 256, 128, 0, 0.1,
+                                   stream=0) == attn.ATTN_ERR_INVALID_ARG             # dq inside the workspace
+    assert attn.attn_bwd_dq_finish(A[9], full, A[6], 1, 2, 256, 128, 0, 0.0, stream=0) == attn.ATTN_ERR_INVALID_ARG
 
 
 def test_selftest_needs_status_pointer():

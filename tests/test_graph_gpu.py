@@ -1,7 +1,8 @@
 """CUDA-graph capture of the C ABI: every entry point only encodes tensor maps on the host
 and launches kernels on the caller's stream, so a forward + backward captured once into a
-CUDA graph and replayed on new input values gives the bytes of eager calls (the kernels
-are deterministic), with a clear device status word after every replay."""
+CUDA graph and replayed on new input values gives the bytes of eager calls (except the
+fused backward's dQ, whose float32 additions come in a varying order: equal up to that
+order), with a clear device status word after every replay."""
 import math
 
 import pytest
@@ -9,6 +10,7 @@ import torch
 
 import tiled_online_softmax_attention_gb300 as attn
 import workloads
+from gpu_util import dq_close
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +26,7 @@ class Step:
         self.nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
         self.ws = torch.empty(self.nbytes, device="cuda", dtype=torch.uint8)
         self.status = torch.zeros(1, device="cuda", dtype=torch.int32)
+        self.fused = False  # set by fwd_bwd: the fused backward (d <= 128, no dropout) ran
 
     def load(self, seed):
         B, H, N, d = self.shape
@@ -39,6 +42,7 @@ class Step:
 
 def fwd_bwd(s, causal, p_drop=0.0, seed=0):
     B, H, N, d = s.shape
+    s.fused = d != 256 and p_drop == 0
     scale = 1.0 / math.sqrt(d)
     if p_drop > 0:
         rc = attn.attn_fwd_dropout(s.q, s.k, s.v, s.o, s.lse, B, H, N, d, s.q.dtype, causal, scale, p_drop, seed,
@@ -73,7 +77,10 @@ def check_graph_matches_eager(s, run, seeds):
         torch.cuda.synchronize()
         assert int(s.status.item()) == 0
         for name, a, b in zip(("O", "lse", "dQ", "dK", "dV"), s.outputs(), want):
-            assert torch.equal(a, b), f"graph replay differs from the eager call in {name} (seed {seed})"
+            if name == "dQ" and s.fused:  # the fused backward's float32 additions come in any order
+                assert dq_close(a, b), f"graph replay differs from the eager call in dQ (seed {seed})"
+            else:
+                assert torch.equal(a, b), f"graph replay differs from the eager call in {name} (seed {seed})"
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])

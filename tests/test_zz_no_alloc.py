@@ -3,20 +3,21 @@
 Some callers cannot allocate device memory (a plugin whose host framework owns
 all device memory, an engine with a budget fixed at start-up, an FFI caller with
 no CUDA runtime of its own); this entry point takes its workspace from a fixed
-array inside the library.  Its gradients must equal those of attn_bwd, the entry
-point that takes a caller-provided workspace, on two calls in a row (the second
-call reuses the array the first one left behind).  The file is named so that
-pytest collects it last.
+array inside the library and runs the kernels of attn_bwd_deterministic.  Its
+gradients must be the bytes attn_bwd_deterministic (the entry point that takes a
+caller-provided workspace) gives, on two calls in a row (the second call reuses
+the array the first one left behind), and must match the FP64 oracle.  The file
+is named so that pytest collects it last.
 """
 import math
 
-import numpy as np
 import pytest
 import torch
 
+import oracle
 import tiled_online_softmax_attention_gb300 as attn
 import workloads
-from gpu_util import GRAD_REL_L2, Guarded, f64, grad_err, run_bwd, run_fwd
+from gpu_util import GRAD_REL_L2, Guarded, grad_err, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -34,25 +35,28 @@ def noalloc_grads(q, k, v, o, lse, do, causal, scale):
     return [g.t for g in outs]
 
 
-
-def test_noalloc_matches_attn_bwd_on_two_calls_in_a_row():
-    cases = [(1, 3, 700, 128, "bf16", True, 41), (2, 2, 300, 64, "fp16", False, 42)]
-    for (B, H, N, d, dtype, causal, seed) in cases:
-        x = workloads.draw(B, H, N, d, dtype, seed=seed, with_dout=True)
-        q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
-        scale = 1.0 / math.sqrt(d)
-        o, lse = run_fwd(q, k, v, causal, scale)
-        ref = run_bwd(q, k, v, o, lse, do, causal, scale)
+@pytest.mark.parametrize("B,H,N,d,dtype,causal,seed",
+                         [(1, 3, 700, 128, "bf16", True, 41), (2, 2, 300, 64, "fp16", False, 42)])
+def test_noalloc_matches_deterministic_on_two_calls_in_a_row(B, H, N, d, dtype, causal, seed):
+    x = workloads.draw(B, H, N, d, dtype, seed=seed, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_fwd(q, k, v, causal, scale)
+    ref = run_bwd(q, k, v, o, lse, do, causal, scale, deterministic=True)
+    for call in range(2):
         got = noalloc_grads(q, k, v, o, lse, do, causal, scale)
         for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
-            e = grad_err(g, f64(r))
-            assert e <= GRAD_REL_L2, f"{name}: attn_bwd_noalloc vs attn_bwd relative L2 {e:.3e}"
+            assert torch.equal(g, r), f"call {call + 1}: attn_bwd_noalloc {name} differs from attn_bwd_deterministic"
+    rq, rk, rv = oracle.attn_bwd(x["q"], x["k"], x["v"], x["dout"], causal, scale)
+    for name, g, r in zip(("dQ", "dK", "dV"), got, (rq, rk, rv)):
+        e = grad_err(g, r)
+        assert e <= GRAD_REL_L2, f"attn_bwd_noalloc {name} vs the oracle: relative L2 {e:.3e}"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     # 129 heads of N = 8192 need 8 * 129 * 8192 bytes, just over the 8 MiB array
     B, H, N, d = 1, 129, 8192, 64
-    assert attn.attn_bwd_workspace_bytes(B, H, N, d) > 8 * 1024 * 1024
+    assert attn.attn_bwd_deterministic_workspace_bytes(B, H, N, d) > 8 * 1024 * 1024
     t = torch.empty(16, device="cuda", dtype=torch.bfloat16)
     p = [t] * 9
     rc = attn.attn_bwd_noalloc(*p, B, H, N, d, torch.bfloat16, True, 0.125)

@@ -34,7 +34,10 @@ current stream):
     attn_bwd_workspace_bytes(B, H, N, d)
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
              B, H, N, d, dt, causal, scale, dev_status=None, stream=None)
-    attn_bwd_prepare / attn_bwd_dkdv / attn_bwd_dq   (the three stages of attn_bwd)
+    attn_bwd_prepare / attn_bwd_dkdvdq / attn_bwd_dq_finish  (the stages of attn_bwd, d <= 128)
+    attn_bwd_deterministic_workspace_bytes(B, H, N, d)
+    attn_bwd_deterministic(...)                     (attn_bwd's arguments; identical bytes every call)
+    attn_bwd_prepare / attn_bwd_dkdv / attn_bwd_dq   (the three stages of attn_bwd_deterministic)
     attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, dt, causal, scale, ...)
                                                      (attn_bwd with library-owned scratch)
     attn_status_string(status)
@@ -68,7 +71,8 @@ ATTN_FP16 = 1
 
 LIB_PATH = _build.LIB
 EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_varlen_dropout", "attn_bwd_varlen_dropout", "attn_fwd_rect_dropout", "attn_bwd_rect_dropout", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_rect", "attn_fwd_varlen_splitkv_workspace_bytes", "attn_fwd_varlen_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
-           "attn_bwd_dq", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
+           "attn_bwd_dq", "attn_bwd_deterministic_workspace_bytes", "attn_bwd_deterministic", "attn_bwd_dkdvdq",
+           "attn_bwd_dq_finish", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
 
@@ -136,6 +140,14 @@ def load(build_if_missing: bool = True):
     lib.attn_bwd_dkdv.restype = I
     lib.attn_bwd_dq.argtypes = [P, P, P, P, P, SZ, P, I, I, I, I, I, I, F, P, P]
     lib.attn_bwd_dq.restype = I
+    lib.attn_bwd_deterministic_workspace_bytes.argtypes = [I, I, I, I]
+    lib.attn_bwd_deterministic_workspace_bytes.restype = SZ
+    lib.attn_bwd_deterministic.argtypes = [P, P, P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_deterministic.restype = I
+    lib.attn_bwd_dkdvdq.argtypes = [P, P, P, P, P, SZ, P, P, I, I, I, I, I, I, F, P, P]
+    lib.attn_bwd_dkdvdq.restype = I
+    lib.attn_bwd_dq_finish.argtypes = [P, SZ, P, I, I, I, I, I, F, P]
+    lib.attn_bwd_dq_finish.restype = I
     lib.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.attn_bwd_noalloc.restype = I
     lib.attn_status_string.argtypes = [I]
@@ -332,6 +344,30 @@ def attn_bwd_dq(q, k, v, dout, workspace, workspace_bytes, dq, B, H, N, d, dt, c
                                   float(scale), _ptr(dev_status), _stream(stream)))
 
 
+def attn_bwd_deterministic_workspace_bytes(B, H, N, d) -> int:
+    return int(load().attn_bwd_deterministic_workspace_bytes(int(B), int(H), int(N), int(d)))
+
+
+def attn_bwd_deterministic(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, dt, causal,
+                           scale, dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_deterministic(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                                             _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), int(B),
+                                             int(H), int(N), int(d), _dt(dt), int(bool(causal)), float(scale),
+                                             _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_dkdvdq(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, d, dt, causal, scale,
+                    dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_dkdvdq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(workspace), int(workspace_bytes),
+                                      _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d), _dt(dt),
+                                      int(bool(causal)), float(scale), _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_dq_finish(workspace, workspace_bytes, dq, B, H, N, d, dt, scale, stream=None) -> int:
+    return int(load().attn_bwd_dq_finish(_ptr(workspace), int(workspace_bytes), _ptr(dq), int(B), int(H), int(N),
+                                         int(d), _dt(dt), float(scale), _stream(stream)))
+
+
 def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, dt, causal, scale, dev_status=None,
                      stream=None) -> int:
     return int(load().attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
@@ -404,19 +440,28 @@ def forward_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False, sca
 
 
 def backward(q, k, v, o, lse, dout, causal: bool = False, scale=None, dev_status=None, workspace=None,
-             out=None):
+             out=None, deterministic: bool = False):
     """dQ, dK, dV of sum(dout * O) for O = forward(q, k, v); q, o, dout [B, H, Nq, d], k, v
-    [B, H, Nk, d] CUDA tensors (Nk != Nq goes through attn_bwd_rect)."""
+    [B, H, Nk, d] CUDA tensors (Nk != Nq goes through attn_bwd_rect).  ``deterministic``
+    selects attn_bwd_deterministic (same bytes on every call; Nk == Nq only)."""
     import torch
 
     q, k, v, o, dout = (_check(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")))
     B, H, N, d = q.shape
     Nk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    nbytes = attn_bwd_workspace_bytes(B, H, N, d)
+    nbytes = (attn_bwd_deterministic_workspace_bytes if deterministic else attn_bwd_workspace_bytes)(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 16), device=q.device, dtype=torch.uint8)
     dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    if deterministic:
+        if Nk != N:
+            raise ValueError("deterministic backward needs Nk == Nq")
+        st = attn_bwd_deterministic(q, k, v, o, dout, lse.contiguous(), dq, dk, dv, workspace, workspace.numel(),
+                                    B, H, N, d, q.dtype, causal, scale, dev_status)
+        if st != ATTN_OK:
+            raise AttnError(st, "attn_bwd_deterministic")
+        return dq, dk, dv
     if Nk != N:
         st = attn_bwd_rect(q, k, v, o, dout, lse.contiguous(), dq, dk, dv, workspace, workspace.numel(), B, H, N, Nk,
                            d, q.dtype, causal, scale, dev_status)

@@ -441,10 +441,17 @@ attn_status attn_fwd_splitkv_rect(const void* q, const void* k, const void* v, v
   return ATTN_OK;
 }
 
-size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+size_t attn_bwd_deterministic_workspace_bytes(int B, int H, int N, int d) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
   const size_t npad = (static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM;
   return 2 * static_cast<size_t>(B) * H * npad * sizeof(float);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+  const size_t base = attn_bwd_deterministic_workspace_bytes(B, H, N, d);
+  if (base == 0 || d == 256) return base;
+  // + the fused backward's float32 dQ accumulator, d values per padded row
+  return base + base / 2 * static_cast<size_t>(d);
 }
 
 }  // extern "C"
@@ -460,10 +467,11 @@ struct Buf {
 // Validation shared by the backward entry points: every input and output 16-byte
 // aligned and non-null, no output overlapping an input, the logsumexp, the workspace
 // or another output, and (when the call writes the workspace) no input or the
-// logsumexp inside the workspace, which must hold attn_bwd_workspace_bytes().
+// logsumexp inside the workspace, which must hold `need` bytes (the workspace size of the
+// path the call takes).
 attn_status check_bwd(std::initializer_list<Buf> ins, const float* lse, std::initializer_list<Buf> outs,
                       const void* ws, size_t ws_bytes, bool ws_out, int B, int H, int N, int Nk, int d,
-                      attn_dtype dt, float scale, int causal) {
+                      attn_dtype dt, float scale, int causal, size_t need) {
   attn_status st = check_sizes(B, H, N, d, dt, scale, true, Nk);
   if (st != ATTN_OK) return st;
   if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
@@ -473,8 +481,7 @@ attn_status check_bwd(std::initializer_list<Buf> ins, const float* lse, std::ini
     if (!aligned16(b.p)) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(ws)) return ATTN_ERR_INVALID_ARG;
   if (lse && !aligned16(lse)) return ATTN_ERR_INVALID_ARG;
-  const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
-  if (ws_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (need == 0 || ws_bytes < need) return ATTN_ERR_INVALID_ARG;
   const size_t lb = static_cast<size_t>(B) * H * N * 4;
   const std::vector<Buf> o(outs);
   for (size_t i = 0; i < o.size(); ++i) {
@@ -514,15 +521,31 @@ void fill_bwd(attn::BwdArgs& a, const void* ws, int B, int H, int N, int Nk, int
 
 size_t qbytes(int B, int H, int N, int d) { return static_cast<size_t>(B) * H * N * d * 2; }
 
+// The fused backward's dQ accumulator: the d float32 values per padded row that follow
+// the two per-row values in a workspace of attn_bwd_workspace_bytes().
+float* dq_accumulator(void* ws, int B, int H, int N) {
+  const size_t npad = (static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM;
+  return static_cast<float*>(ws) + 2 * static_cast<size_t>(B) * H * npad;
+}
+
+// Fills the per-row values (and, when the workspace holds the fused backward's dQ
+// accumulator, clears the accumulator).
 attn_status prepare_impl(const void* o, const void* dout, const float* lse, void* workspace, size_t workspace_bytes,
                          int B, int H, int N, int d, attn_dtype dt, void* stream) {
   if (!lse) return ATTN_ERR_INVALID_ARG;
   const size_t qb = qbytes(B, H, N, d);
+  const size_t small = attn_bwd_deterministic_workspace_bytes(B, H, N, d);
   attn_status st = check_bwd({{o, qb}, {dout, qb}}, lse, {}, workspace, workspace_bytes, true, B, H, N, N, d, dt,
-                             1.f, 0);
+                             1.f, 0, small);
   if (st != ATTN_OK) return st;
+  const size_t full = attn_bwd_workspace_bytes(B, H, N, d);
+  const bool with_acc = d != 256 && workspace_bytes >= full;
+  if (with_acc && (overlaps(o, qb, workspace, full) || overlaps(dout, qb, workspace, full) ||
+                   overlaps(lse, static_cast<size_t>(B) * H * N * 4, workspace, full)))
+    return ATTN_ERR_INVALID_ARG;
   attn::BwdArgs a{};
   fill_bwd(a, workspace, B, H, N, N, 0, 1.f, nullptr);
+  a.dq_acc = with_acc ? dq_accumulator(workspace, B, H, N) : nullptr;
   a.o = o;
   a.dout = dout;
   a.lse = lse;
@@ -536,7 +559,8 @@ attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* d
                       int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
-                             workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
+                             workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal,
+                             attn_bwd_deterministic_workspace_bytes(B, H, N, d));
   if (st != ATTN_OK) return st;
   attn::BwdArgs a{};
   const bool bf16 = dt == ATTN_BF16;
@@ -559,7 +583,8 @@ attn_status dq_impl(const void* q, const void* k, const void* v, const void* dou
                     float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dq, qb}}, workspace,
-                             workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal);
+                             workspace_bytes, false, B, H, N, Nk, d, dt, scale, causal,
+                             attn_bwd_deterministic_workspace_bytes(B, H, N, d));
   if (st != ATTN_OK) return st;
   attn::BwdArgs a{};
   const bool bf16 = dt == ATTN_BF16;
@@ -577,16 +602,72 @@ attn_status dq_impl(const void* q, const void* k, const void* v, const void* dou
   return ATTN_OK;
 }
 
+// The fused stage: dK, dV and the dQ accumulator (the preparation pass, with the
+// accumulator cleared, must have run on the same workspace).
+attn_status fused_impl(const void* q, const void* k, const void* v, const void* dout, void* workspace,
+                       size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
+                       int causal, float scale, int* dev_status, void* stream) {
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
+  const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
+  attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
+                             workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal,
+                             attn_bwd_workspace_bytes(B, H, N, d));
+  if (st != ATTN_OK) return st;
+  attn::BwdArgs a{};
+  const bool bf16 = dt == ATTN_BF16;
+  const int BH = B * H;
+  if (!make_map(&a.tm_q, q, BH, N, d, bf16) || !make_map(&a.tm_k, k, BH, Nk, d, bf16) ||
+      !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
+      !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) || !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
+    return ATTN_ERR_CUDA;
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status);
+  a.dq_acc = dq_accumulator(workspace, B, H, N);
+  if (attn::launch_bwd_fused(a, d, bf16, false, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+// dQ = scale * accumulator, rounded to the 16-bit type.
+attn_status finish_impl(const void* workspace, size_t workspace_bytes, void* dq, int B, int H, int N, int d,
+                        attn_dtype dt, float scale, void* stream) {
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
+  const size_t qb = qbytes(B, H, N, d);
+  attn_status st = check_bwd({}, nullptr, {{dq, qb}}, workspace, workspace_bytes, false, B, H, N, N, d, dt, scale,
+                             0, attn_bwd_workspace_bytes(B, H, N, d));
+  if (st != ATTN_OK) return st;
+  attn::BwdArgs a{};
+  fill_bwd(a, workspace, B, H, N, N, 0, scale, nullptr);
+  a.dq_acc = dq_accumulator(const_cast<void*>(workspace), B, H, N);
+  a.dq = dq;
+  if (attn::launch_bwd_dq_finish(a, d, dt == ATTN_BF16, false, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+// The whole backward.  d <= 128 without dropout takes the fused path (five products per
+// tile pair, dQ through a float32 accumulator) unless the caller asks for the
+// deterministic one; dropout and d = 256 use the deterministic kernels.
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
-                     const Dropout& dr = Dropout{}) {
+                     const Dropout& dr = Dropout{}, bool deterministic = false) {
   if (!lse) return ATTN_ERR_INVALID_ARG;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
+  const size_t need = deterministic ? attn_bwd_deterministic_workspace_bytes(B, H, N, d)
+                                    : attn_bwd_workspace_bytes(B, H, N, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},
-                             workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal);
+                             workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal, need);
   if (st != ATTN_OK) return st;
-  if ((st = prepare_impl(o, dout, lse, workspace, workspace_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
+  const bool fused = !deterministic && d != 256 && dr.t == 0;
+  // the deterministic path does not read past the per-row values: prepare only those
+  const size_t prep_bytes = fused ? workspace_bytes : attn_bwd_deterministic_workspace_bytes(B, H, N, d);
+  if ((st = prepare_impl(o, dout, lse, workspace, prep_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
+  if (fused) {
+    if ((st = fused_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
+                         dev_status, stream)) != ATTN_OK)
+      return st;
+    return finish_impl(workspace, workspace_bytes, dq, B, H, N, d, dt, scale, stream);
+  }
   if (d == 256) {
     if ((st = dkdv_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
                         dev_status, stream, dr)) != ATTN_OK)
@@ -638,6 +719,26 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      void* stream) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
                   dev_status, stream);
+}
+
+attn_status attn_bwd_deterministic(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                   const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                                   size_t workspace_bytes, int B, int H, int N, int d, attn_dtype dt, int causal,
+                                   float scale, int* dev_status, void* stream) {
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
+                  dev_status, stream, Dropout{}, true);
+}
+
+attn_status attn_bwd_dkdvdq(const void* q, const void* k, const void* v, const void* dout, void* workspace,
+                            size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int d, attn_dtype dt,
+                            int causal, float scale, int* dev_status, void* stream) {
+  return fused_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, N, d, dt, causal, scale, dev_status,
+                    stream);
+}
+
+attn_status attn_bwd_dq_finish(const void* workspace, size_t workspace_bytes, void* dq, int B, int H, int N, int d,
+                               attn_dtype dt, float scale, void* stream) {
+  return finish_impl(workspace, workspace_bytes, dq, B, H, N, d, dt, scale, stream);
 }
 
 attn_status attn_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -702,6 +803,16 @@ attn_status bwd_varlen_impl(const void* q, const void* k, const void* v, const v
   a.dk_out = dk;
   a.dv_out = dv;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool fused = d != 256 && dr.t == 0;
+  if (fused) {  // the fused path: dK, dV and a float32 dQ accumulator, then dQ from it
+    a.dq_acc = dq_accumulator(workspace, B, H, max_q);
+    a.dq = dq;
+    if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess ||
+        attn::launch_bwd_fused(a, d, bf16, true, s) != cudaSuccess ||
+        attn::launch_bwd_dq_finish(a, d, bf16, true, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
   if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess) return ATTN_ERR_CUDA;
   const cudaError_t e = d == 256 ? (attn::launch_bwd256_dkdv_varlen(a, bf16, s) == cudaSuccess
                                         ? attn::launch_bwd256_dq_varlen(a, bf16, s)

@@ -1,0 +1,489 @@
+// bwd_fused.cu -- the fused backward for d = 64 and 128: one CTA per 128-key tile
+// computes dK and dV as the deterministic dK/dV kernel does and, from the same dS tile,
+// adds each query tile's dQ contribution into a float32 accumulator in the workspace.
+// Five N x N x d products per (key tile, query tile) pair -- the algorithm's count
+// ("Understanding FlashAttention, Part 2", section 2.4, Figs 16-20: dQ accumulates over
+// the key tiles while dK and dV stay with their key tile) -- against seven for the
+// deterministic two-kernel backward, which recomputes S and dP in the query-tile order.
+//
+// Per query tile t the MMA warp issues, in this order,
+//   dP^T(t) = V dO^T | dV += P^T dO | S^T(t+1) = K Q^T | dQ(t) = dS K | dK += dS^T Q
+// P^T = ex2(c S^T - LSE2) is computed while dP^T runs (as in the deterministic kernel);
+// dS^T = P^T (dP^T - D) while dV and S^T(t+1) run.  dS^T goes to a 128 x 128 16-bit
+// shared-memory tile laid out [key][query] with the 128-byte swizzle: read K-major it
+// is the A operand of dK (rows = keys), read MN-major it is the A operand of dQ (rows =
+// queries), so both products take it without a transpose.  dQ(t) accumulates in the
+// tensor-memory columns of dP^T, which are free once every element-wise thread has read
+// dP^T(t); the element-wise warps read dQ(t) out while dK(t) runs and add it to the
+// accumulator with vector reductions (red.global.add.v4.f32), and only then may dP^T(t+1)
+// take the columns back.  The element-wise order per tile is therefore
+//   read out dQ(t-1) | P^T(t) | dS^T(t)
+// so that the read-out overlaps dK(t-1) and P^T(t) overlaps dK(t-1) and dP^T(t).
+//
+// The accumulator's summation order depends on which CTA's reduction reaches a value
+// first: dQ is not bit-for-bit reproducible from run to run (dK and dV are).  The
+// deterministic kernels of bwd.cu stay available for callers that need identical bytes.
+#include <cuda_fp16.h>
+
+#include "bwd_common.cuh"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kSmemMax = 232448;  // opt-in shared memory per CTA
+constexpr int kStatusLayout = 3;  // ATTN_ERR_CUDA: the shared-memory window is misaligned
+
+// Shared memory: K, V (stationary), STAGES x (Q, dO, LSE2, D), the dS tile, barriers.
+// At d = 128 this is 226.25 KB; dynamic shared memory starts 1024-byte aligned in
+// practice and the slack below the opt-in limit covers a start misaligned by up to
+// SLACK bytes (a kernel that finds more reports ATTN_ERR_CUDA and returns at once).
+template <int D>
+struct FusedLayout {
+  using T = BwdTiles<D>;
+  static constexpr int STAGES = (D == 128) ? 2 : 3;
+  static constexpr int STAGE_BYTES = 2 * T::TILE + 2 * 512;
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = T::TILE;
+  static constexpr int OFF_ST = 2 * T::TILE;
+  static constexpr int OFF_DS = OFF_ST + STAGES * STAGE_BYTES;
+  static constexpr int DS_BYTES = kTileN * kTileM * 2;
+  static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+  static constexpr int NEED = OFF_BAR + 256;
+  static constexpr int SMEM = NEED + 1024 < kSmemMax ? NEED + 1024 : kSmemMax;
+  static constexpr int SLACK = SMEM - NEED;
+  static_assert(SLACK >= 0, "shared memory");
+  static constexpr int S_Q = 0, S_DO = T::TILE, S_L = 2 * T::TILE, S_D = 2 * T::TILE + 512;
+  // dQ(t) shares dP^T's columns (see the file header)
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TM_DQ = TM_DP, TM_COLS = 512;
+};
+
+enum : int {
+  F_KVFULL = 0,
+  F_SFULL = 1,    // S^T computed (MMA commit)
+  F_DPFULL = 2,   // dP^T computed (MMA commit)
+  F_PREADY = 3,   // P^T written to tensor memory (all element-wise threads)
+  F_DSREADY = 4,  // dS^T written to shared memory (all element-wise threads)
+  F_DQFULL = 5,   // dQ(t) computed (MMA commit)
+  F_DQFREE = 6,   // dQ(t) read out of tensor memory (all element-wise threads)
+  F_DONE = 7,
+  F_DRAIN = 8,
+  F_QFULL = 9,    // + stage
+  F_EMPTY = 12,   // + stage
+  F_COUNT = 15
+};
+static_assert(8 * F_COUNT + 16 <= 256, "barrier area");
+
+// dQ(t) of this thread's query row, columns [(D/4) h, (D/4)(h+1)), added to the
+// accumulator: 32 consecutive rows x 4 columns are contiguous, so a warp's vector
+// reduction covers 512 contiguous bytes.
+template <int D>
+__device__ __forceinline__ void dq_reduce(float* acc, size_t group_base, int h, int lane, const uint32_t* v) {
+#pragma unroll
+  for (int g = 0; g < D / 16; ++g) {
+    float* p = acc + (group_base + static_cast<size_t>((D / 16) * h + g)) * 128 + lane * 4;
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(v[4 * g])),
+                 "f"(__uint_as_float(v[4 * g + 1])), "f"(__uint_as_float(v[4 * g + 2])),
+                 "f"(__uint_as_float(v[4 * g + 3]))
+                 : "memory");
+  }
+}
+
+template <int D, bool BF16, bool VARLEN>
+__global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_constant__ BwdArgs a) {
+  using L = FusedLayout<D>;
+  using T = BwdTiles<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uintptr_t raw = reinterpret_cast<uintptr_t>(smem_raw);
+  const uintptr_t aligned = (raw + 1023) & ~static_cast<uintptr_t>(1023);
+  if (aligned - raw > static_cast<uintptr_t>(L::SLACK)) {
+    if (threadIdx.x == 0 && a.dev_status) atomicExch(a.dev_status, kStatusLayout);
+    return;
+  }
+  uint8_t* smem = reinterpret_cast<uint8_t*>(aligned);
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bars = sb + L::OFF_BAR;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_BAR + 8 * F_COUNT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_BAR + 8 * F_COUNT + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;
+  const WorkItem wi = work_item(static_cast<int>(blockIdx.x), a.BH, n_tk);
+  const int bh = wi.bh;
+  const int kt = wi.rank;  // low key tiles see the most queries: they go first
+  const int k0 = kt * kTileN;
+  int N = a.N, cofs = a.cofs, hh = 0, tq0 = 0, tk0 = 0, Nk = a.Nk;
+  if constexpr (VARLEN) {
+    const SeqView sv = seq_view(a, bh);
+    N = sv.N, Nk = sv.Nk, cofs = sv.cofs, hh = sv.hh, tq0 = sv.tq0, tk0 = sv.tk0;
+    if (k0 >= Nk) return;  // this key tile lies past the sequence's keys (whole CTA)
+    if (sv.degenerate || N <= 0) {
+      zero_rows_packed<D>(a.dk_out, a.H, hh, tk0, k0, Nk);
+      zero_rows_packed<D>(a.dv_out, a.H, hh, tk0, k0, Nk);
+      return;  // the accumulator rows stay zero: dQ = 0
+    }
+  }
+  const int n_t = (N + kTileM - 1) / kTileM;
+  const int i_begin = a.causal ? max(0, k0 - cofs) / kTileM : 0;
+  const int n_iter = n_t - i_begin;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(F_KVFULL), 1);
+    mbar_init(bar(F_SFULL), 1);
+    mbar_init(bar(F_DPFULL), 1);
+    mbar_init(bar(F_PREADY), 128 * kEw);
+    mbar_init(bar(F_DSREADY), 128 * kEw);
+    mbar_init(bar(F_DQFULL), 1);
+    mbar_init(bar(F_DQFREE), 128 * kEw);
+    mbar_init(bar(F_DONE), 1);
+    mbar_init(bar(F_DRAIN), 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(bar(F_QFULL + s), 1);
+      mbar_init(bar(F_EMPTY + s), 1);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), L::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{abort_flag, a.dev_status, a.wait_limit_ns};
+  auto stage_base = [&](int s) -> uint32_t { return sb + L::OFF_ST + s * L::STAGE_BYTES; };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&a.tm_q);
+      prefetch_tmap(&a.tm_k);
+      prefetch_tmap(&a.tm_v);
+      prefetch_tmap(&a.tm_do);
+      mbar_arrive_expect_tx(bar(F_KVFULL), 2 * T::TILE);
+      for (int kb = 0; kb < T::KB; ++kb) {
+        tma_load_3d(sb + L::OFF_K + kb * T::BLK, &a.tm_k, bar(F_KVFULL), kb * 64, VARLEN ? hh : k0,
+                    VARLEN ? tk0 + k0 : bh);
+        tma_load_3d(sb + L::OFF_V + kb * T::BLK, &a.tm_v, bar(F_KVFULL), kb * 64, VARLEN ? hh : k0,
+                    VARLEN ? tk0 + k0 : bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < n_iter; ++t) {
+        const int s = t % L::STAGES;
+        const int q0 = (i_begin + t) * kTileM;
+        if (t >= L::STAGES && !mbar_wait(bar(F_EMPTY + s), ((t / L::STAGES) - 1) & 1, wc)) break;
+        const uint32_t st = stage_base(s);
+        mbar_arrive_expect_tx(bar(F_QFULL + s), 2 * T::TILE + 1024);
+        for (int kb = 0; kb < T::KB; ++kb) {
+          tma_load_3d(st + L::S_Q + kb * T::BLK, &a.tm_q, bar(F_QFULL + s), kb * 64, VARLEN ? hh : q0,
+                      VARLEN ? tq0 + q0 : bh);
+          tma_load_3d(st + L::S_DO + kb * T::BLK, &a.tm_do, bar(F_QFULL + s), kb * 64, VARLEN ? hh : q0,
+                      VARLEN ? tq0 + q0 : bh);
+        }
+        const size_t w = static_cast<size_t>(bh) * a.Npad + q0;
+        bulk_load(st + L::S_L, a.lse2 + w, 512, bar(F_QFULL + s));
+        bulk_load(st + L::S_D, a.delta + w, 512, bar(F_QFULL + s));
+        issued = t + 1;
+      }
+      mbar_wait(bar(F_KVFULL), 0, wc);
+      for (int t = (issued > L::STAGES ? issued - L::STAGES : 0); t < issued; ++t)
+        mbar_wait(bar(F_QFULL + t % L::STAGES), (t / L::STAGES) & 1, wc);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
+      constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // K-major A x MN-major B
+      constexpr uint32_t idesc_q = idesc_f16(kTileM, D, BF16, true, true);         // MN-major A x MN-major B
+      const uint32_t ds = sb + L::OFF_DS;
+      auto issue_st = [&](int t) {
+        const uint32_t st = stage_base(t % L::STAGES);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+          mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024), sdesc_sw128(st + L::S_Q + off, 16, 1024),
+                 idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(F_SFULL));
+      };
+      bool ok = mbar_wait(bar(F_KVFULL), 0, wc);
+      if (ok && n_iter > 0 && (ok = mbar_wait(bar(F_QFULL + 0), 0, wc))) {
+        tc_fence_after();
+        issue_st(0);
+      }
+      for (int t = 0; ok && t < n_iter; ++t) {
+        const int s = t % L::STAGES;
+        const uint32_t st = stage_base(s);
+        // dP^T(t) takes dQ(t-1)'s columns once the element-wise warps have read them.
+        if (t > 0 && !(ok = mbar_wait(bar(F_DQFREE), (t - 1) & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+          mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
+                 sdesc_sw128(st + L::S_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(F_DPFULL));
+        if (!(ok = mbar_wait(bar(F_PREADY), t & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
+          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
+                 sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+        if (t + 1 < n_iter) {  // S^T(t+1) over P^T(t): issued after dV(t), which reads it
+          if (!(ok = mbar_wait(bar(F_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
+          tc_fence_after();
+          issue_st(t + 1);
+        }
+        if (!(ok = mbar_wait(bar(F_DSREADY), t & 1, wc))) break;
+        tc_fence_after();
+        // dQ(t) = dS K: A = dS read MN-major from the [key][query] tile (16-key steps of
+        // 16 rows), B = K MN-major (d contiguous).
+#pragma unroll
+        for (int k = 0; k < kTileN / 16; ++k)
+          mma_ss(tmem + L::TM_DQ, sdesc_sw128(ds + k * 2048, T::BLK, 1024),
+                 sdesc_sw128(sb + L::OFF_K + k * 2048, T::BLK, 1024), idesc_q, k > 0 ? 1u : 0u);
+        tc_commit(bar(F_DQFULL));
+        // dK += dS^T Q: A = dS^T read K-major from the same tile (16-query steps).
+#pragma unroll
+        for (int k = 0; k < kTileM / 16; ++k)
+          mma_ss(tmem + L::TM_DK, sdesc_sw128(ds + (k >> 2) * T::BLK + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(F_EMPTY + s));
+      }
+      if (ok) tc_commit(bar(F_DONE));
+      tc_commit(bar(F_DRAIN));
+      mbar_wait(bar(F_DRAIN), 0, wc);
+    }
+  } else if (warp >= 4) {
+    const int h = (warp >> 2) - 1;   // this warpgroup's 32 query columns of every tile
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;  // key row within the tile == TMEM lane (query row for dQ)
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t t_s = t_lane + L::TM_S + kEwCols * h, t_dp = t_lane + L::TM_DP + kEwCols * h;
+    const float sl2 = a.scale_log2;
+    uint8_t* ds_tile = smem + L::OFF_DS;
+    const size_t groups_per_head = static_cast<size_t>(a.Npad) / 32;
+    // Reads dQ(t) (this thread's query row, the warpgroup's D/4 columns) out of tensor
+    // memory, frees the columns and adds the values to the accumulator.
+    auto drain = [&](int t) -> bool {
+      if (!mbar_wait_warp(bar(F_DQFULL), t & 1, wc)) return false;
+      tc_fence_after();
+      uint32_t v[D / 4];
+      if constexpr (D == 128)
+        tmem_ld_x32(t_lane + L::TM_DQ + (D / 4) * h, v);
+      else
+        tmem_ld_x16(t_lane + L::TM_DQ + (D / 4) * h, v);
+      tc_fence_before();
+      mbar_arrive(bar(F_DQFREE));
+      const int q = (i_begin + t) * kTileM + row;
+      if (q < N)
+        dq_reduce<D>(a.dq_acc, (static_cast<size_t>(bh) * groups_per_head + q / 32) * (D / 4), h, lane, v);
+      return true;
+    };
+    bool ok = true;
+    for (int t = 0; t < n_iter; ++t) {
+      const int s = t % L::STAGES;
+      const int qt = i_begin + t;
+      if (t > 0 && !(ok = drain(t - 1))) break;
+      if (!(ok = mbar_wait_warp(bar(F_QFULL + s), (t / L::STAGES) & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(bar(F_SFULL), t & 1, wc))) break;
+      tc_fence_after();
+      const float4* l4 =
+          reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_L) + (kEwCols / 4) * h;
+      const float4* d4 =
+          reinterpret_cast<const float4*>(smem + L::OFF_ST + s * L::STAGE_BYTES + L::S_D) + (kEwCols / 4) * h;
+      // Query column c sees key k0 + row only if the key exists (in a packed batch the
+      // rows past the sequence's last key hold the next sequence's keys, which must not
+      // reach dQ) and, causal, if qt*128 + 32h + c + cofs >= k0 + row.
+      const int first_visible = k0 + row >= Nk ? kEwCols
+                                : a.causal    ? k0 + row - cofs - qt * kTileM - kEwCols * h
+                                              : 0;
+      float p[kEwCols];
+      {  // P^T = 2^-(lse2 - s sl2) (overlaps dK(t-1) and dP^T(t))
+        uint32_t sv[kEwCols];
+        tmem_ld_x32(t_s, sv);
+        const uint64_t nsl2 = f32x2_pack(-sl2, -sl2);
+#pragma unroll
+        for (int v = 0; v < kEwCols / 4; ++v) {
+          const float4 lv = l4[v];
+          float x0, x1, x2, x3;
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v]), __uint_as_float(sv[4 * v + 1])), nsl2,
+                                 f32x2_pack(lv.x, lv.y)), x0, x1);
+          f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(sv[4 * v + 2]), __uint_as_float(sv[4 * v + 3])), nsl2,
+                                 f32x2_pack(lv.z, lv.w)), x2, x3);
+          p[4 * v + 0] = ex2(-x0);
+          p[4 * v + 1] = ex2(-x1);
+          p[4 * v + 2] = ex2(-x2);
+          p[4 * v + 3] = ex2(-x3);
+        }
+      }
+      if (first_visible > 0) {
+#pragma unroll
+        for (int c = 0; c < kEwCols; ++c)
+          if (c < first_visible) p[c] = 0.f;
+      }
+      {
+        uint32_t pk[kEwCols / 2];
+#pragma unroll
+        for (int c = 0; c < kEwCols; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+        tmem_st_x16(t_s, pk);  // over columns this thread has read
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(F_PREADY));
+      // dS^T = P^T (dP^T - D) into the shared [key][query] tile (overlaps dV and S^T(t+1)).
+      if (!(ok = mbar_wait_warp(bar(F_DPFULL), t & 1, wc))) break;
+      tc_fence_after();
+      {
+        uint32_t dv[kEwCols], dk[kEwCols / 2];
+        tmem_ld_x32(t_dp, dv);
+#pragma unroll
+        for (int v = 0; v < kEwCols / 4; ++v) {
+          const float4 dd = d4[v];
+          float a0, a1, b0, b1;
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[4 * v], p[4 * v + 1]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[4 * v]), __uint_as_float(dv[4 * v + 1])),
+                                           f32x2_pack(dd.x, dd.y))), a0, a1);
+          f32x2_unpack(f32x2_mul(f32x2_pack(p[4 * v + 2], p[4 * v + 3]),
+                                 f32x2_sub(f32x2_pack(__uint_as_float(dv[4 * v + 2]), __uint_as_float(dv[4 * v + 3])),
+                                           f32x2_pack(dd.z, dd.w))), b0, b1);
+          dk[2 * v] = pack2<BF16>(a0, a1);
+          dk[2 * v + 1] = pack2<BF16>(b0, b1);
+        }
+        // queries 32h .. 32h+31 of key row `row`: 64 bytes in block h/2, 16-byte chunks
+        // (h%2)*4 .. +3 of the row, swizzled by the row's low three bits
+        uint8_t* base = ds_tile + (h >> 1) * T::BLK + row * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int ch = (h & 1) * 4 + c;
+          *reinterpret_cast<uint4*>(base + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(F_DSREADY));
+    }
+    if (ok && n_iter > 0) ok = drain(n_iter - 1);
+    if (ok) ok = mbar_wait_warp(bar(F_DONE), 0, wc);
+    // Epilogue: warpgroups 0-1 write dV, 2-3 write scale * dK, as the dK/dV kernel does.
+    const int which = h >> 1;
+    uint8_t* stage = smem + L::OFF_ST + (which == 0 ? L::S_DO : L::S_Q);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t col = (which == 0) ? L::TM_DV : L::TM_DK;
+      const float mul = (which == 0) ? 1.f : a.scale;
+#pragma unroll
+      for (int cc = (h & 1) * (D / 64); cc < ((h & 1) + 1) * (D / 64); ++cc) {
+        uint32_t v[32];
+        tmem_ld_x32(t_lane + col + cc * 32, v);
+        if constexpr (VARLEN) {
+          if (k0 + row < Nk)
+            store_row_chunk_packed<D, BF16>(which == 0 ? a.dv_out : a.dk_out,
+                                            (static_cast<size_t>(tk0 + k0 + row) * a.H + hh) * D, cc, v, mul);
+        } else {
+          stage_row_chunk<D, BF16>(stage, row, cc, v, mul);
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1 + which, 256);
+    if (!VARLEN && (h & 1) == 0 && (warp & 3) == 0 && lane == 0 && ok && !*abort_flag) {
+      const CUtensorMap* m = (which == 0) ? &a.tm_dv : &a.tm_dk;
+      for (int kb = 0; kb < T::KB; ++kb) tma_store_3d(m, smem_u32(stage) + kb * T::BLK, kb * 64, k0, bh);
+      bulk_commit();
+      bulk_wait_read_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TM_COLS);
+  }
+}
+
+// dQ = scale * accumulator, rounded to the 16-bit type: one block per 32-row group of a
+// head, transposed through shared memory so that both the float32 reads (512 contiguous
+// bytes per warp instruction) and the 16-bit row writes are coalesced.
+template <int D, bool BF16, bool VARLEN>
+__global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const __grid_constant__ BwdArgs a) {
+  __shared__ float tile[32][D + 4];
+  const int groups_per_head = a.Npad / 32;
+  const int g = static_cast<int>(blockIdx.x);
+  const int bh = g / groups_per_head;
+  const int r0 = (g % groups_per_head) * 32;
+  int N = a.N, hh = 0, tq0 = 0;
+  if constexpr (VARLEN) {
+    const SeqView sv = seq_view(a, bh);
+    N = sv.N, hh = sv.hh, tq0 = sv.tq0;
+  }
+  if (r0 >= N) return;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc) + static_cast<size_t>(g) * (D / 4) * 32;
+  for (int i = threadIdx.x; i < (D / 4) * 32; i += blockDim.x) {
+    const float4 x = src[i];
+    const int cg = i / 32, rr = i % 32;
+    *reinterpret_cast<float4*>(&tile[rr][cg * 4]) = x;
+  }
+  __syncthreads();
+  const float sc = a.scale;
+  for (int i = threadIdx.x; i < 32 * (D / 8); i += blockDim.x) {
+    const int rr = i / (D / 8), u = i % (D / 8);
+    const int r = r0 + rr;
+    if (r >= N) continue;
+    const float4 x0 = *reinterpret_cast<const float4*>(&tile[rr][u * 8]);
+    const float4 x1 = *reinterpret_cast<const float4*>(&tile[rr][u * 8 + 4]);
+    const uint4 out = make_uint4(pack2<BF16>(x0.x * sc, x0.y * sc), pack2<BF16>(x0.z * sc, x0.w * sc),
+                                 pack2<BF16>(x1.x * sc, x1.y * sc), pack2<BF16>(x1.z * sc, x1.w * sc));
+    size_t elem;
+    if constexpr (VARLEN)
+      elem = (static_cast<size_t>(tq0 + r) * a.H + hh) * D + u * 8;
+    else
+      elem = (static_cast<size_t>(bh) * a.N + r) * D + u * 8;
+    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dq) + elem * 2) = out;
+  }
+}
+
+template <int D, bool BF16, bool VARLEN>
+cudaError_t launch_fused_t(const BwdArgs& a, cudaStream_t st) {
+  auto k = bwd_fused_kernel<D, BF16, VARLEN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedLayout<D>::SMEM);
+  if (e != cudaSuccess) return e;
+  const int n_tk = (a.Nk + kTileN - 1) / kTileN;
+  k<<<n_tk * a.BH, kBwdThreads, FusedLayout<D>::SMEM, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16, bool VARLEN>
+cudaError_t launch_finish_t(const BwdArgs& a, cudaStream_t st) {
+  const int groups = a.BH * (a.Npad / 32);
+  bwd_dq_finish_kernel<D, BF16, VARLEN><<<groups, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_fused(const BwdArgs& a, int d, bool bf16, bool varlen, cudaStream_t s) {
+  if (varlen) {
+    if (d == 128) return bf16 ? launch_fused_t<128, true, true>(a, s) : launch_fused_t<128, false, true>(a, s);
+    return bf16 ? launch_fused_t<64, true, true>(a, s) : launch_fused_t<64, false, true>(a, s);
+  }
+  if (d == 128) return bf16 ? launch_fused_t<128, true, false>(a, s) : launch_fused_t<128, false, false>(a, s);
+  return bf16 ? launch_fused_t<64, true, false>(a, s) : launch_fused_t<64, false, false>(a, s);
+}
+
+cudaError_t launch_bwd_dq_finish(const BwdArgs& a, int d, bool bf16, bool varlen, cudaStream_t s) {
+  if (varlen) {
+    if (d == 128) return bf16 ? launch_finish_t<128, true, true>(a, s) : launch_finish_t<128, false, true>(a, s);
+    return bf16 ? launch_finish_t<64, true, true>(a, s) : launch_finish_t<64, false, true>(a, s);
+  }
+  if (d == 128) return bf16 ? launch_finish_t<128, true, false>(a, s) : launch_finish_t<128, false, false>(a, s);
+  return bf16 ? launch_finish_t<64, true, false>(a, s) : launch_finish_t<64, false, false>(a, s);
+}
+
+}  // namespace attn

@@ -85,6 +85,11 @@ struct BwdArgs {
   void* dq_out;                         // packed gradients, written row by row
   void* dk_out;
   void* dv_out;
+  // fused backward only: float32 dQ accumulator in the workspace, B*H*Npad*d values in
+  // [B*H][Npad/32][d/4][32][4] order (32 rows x 4 columns contiguous), zeroed by the
+  // preparation pass; nullptr for the deterministic kernels
+  float* dq_acc;
+  void* dq;                             // fused backward: dQ [B*H][N][d] (the finishing pass writes it)
 };
 
 // One packed sequence as a kernel sees it: lengths clamped to the caller's bounds, the
@@ -160,6 +165,10 @@ cudaError_t launch_bwd256_dkdv(const BwdArgs& a, bool bf16, cudaStream_t s);  //
 cudaError_t launch_bwd256_dq(const BwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd256_dkdv_varlen(const BwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd256_dq_varlen(const BwdArgs& a, bool bf16, cudaStream_t s);
+// The fused backward (bwd_fused.cu): dK, dV and the float32 dQ accumulator in one pass over
+// each key tile's query tiles (five products per tile pair), then dQ = scale * accumulator.
+cudaError_t launch_bwd_fused(const BwdArgs& a, int d, bool bf16, bool varlen, cudaStream_t s);
+cudaError_t launch_bwd_dq_finish(const BwdArgs& a, int d, bool bf16, bool varlen, cudaStream_t s);
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t limit_ns, cudaStream_t s);
 
 }  // namespace attn
