@@ -455,7 +455,40 @@ def long_forward(attn, dev):
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     res["d256_forward_and_step_B1_H16_N16384"] = d256_side(attn, dev)
     res["dropout_training_step_p0.1"] = dropout_step(attn, dev)
+    res["backward_fused_vs_deterministic_B2_H16_N8192"] = backward_modes(attn, dev)
     return res
+
+
+def backward_modes(attn, dev):
+    """The training-step backward alone (B=2, H=16, N=8192, d=128, causal) through attn_bwd
+    (the fused pass: five products per tile pair, dQ through a float32 accumulator) and
+    attn_bwd_deterministic (seven products, no atomics), FLOPs counted 10*B*H*N^2*d/2."""
+    w = workloads.WORKLOADS["c5"]
+    x = workloads.inputs("c5")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, True, w.scale)
+    out = {}
+    for name, call, size in (("fused", attn.attn_bwd, attn.attn_bwd_workspace_bytes),
+                             ("deterministic", attn.attn_bwd_deterministic, attn.attn_bwd_deterministic_workspace_bytes)):
+        nb = size(w.B, w.H, w.N, w.d)
+        ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+        run = lambda: call(q, k, v, o, do, lse, dq, dk, dv, ws, nb, w.B, w.H, w.N, w.d, q.dtype, True, w.scale)
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record()
+        for _ in range(reps):
+            run()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        f = workloads.bwd_flops(w.B, w.H, w.N, w.d, True)
+        out[name] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+    return out
 
 
 def dropout_step(attn, dev):
