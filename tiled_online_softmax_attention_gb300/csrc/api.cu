@@ -92,6 +92,22 @@ bool make_map_e4m3(CUtensorMap* m, const void* base, int BH, int N, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the fused backward's float32 dQ accumulator [rows][d]: box {d/4, 16} (one
+// element-wise warp's columns, half its 32 rows), swizzled like the staging area the
+// kernel writes (128-byte rows at d = 128, 64-byte rows at d = 64).
+bool make_map_acc(CUtensorMap* m, const void* base, int64_t rows, int d) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(d / 4), 16};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, d == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Dropout parameters: t = round(256 p) in 0..255 (0 = no dropout) and the 64-bit seed.
@@ -622,6 +638,7 @@ attn_status fused_impl(const void* q, const void* k, const void* v, const void* 
     return ATTN_ERR_CUDA;
   fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
   a.dq_acc = dq_accumulator(workspace, B, H, N);
+  if (!make_map_acc(&a.tm_dqacc, a.dq_acc, static_cast<int64_t>(BH) * a.Npad, d)) return ATTN_ERR_CUDA;
   if (attn::launch_bwd_fused(a, d, bf16, false, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return ATTN_ERR_CUDA;
   return ATTN_OK;
@@ -806,6 +823,7 @@ attn_status bwd_varlen_impl(const void* q, const void* k, const void* v, const v
   if (d != 256) {  // the fused path: dK, dV and a float32 dQ accumulator, then dQ from it
     a.dq_acc = dq_accumulator(workspace, B, H, max_q);
     a.dq = dq;
+    if (!make_map_acc(&a.tm_dqacc, a.dq_acc, static_cast<int64_t>(B) * H * a.Npad, d)) return ATTN_ERR_CUDA;
     if (attn::launch_bwd_pre_varlen(a, d, bf16, s) != cudaSuccess ||
         attn::launch_bwd_fused(a, d, bf16, true, s) != cudaSuccess ||
         attn::launch_bwd_dq_finish(a, d, bf16, true, s) != cudaSuccess)

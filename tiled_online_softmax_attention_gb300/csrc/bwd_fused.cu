@@ -7,18 +7,19 @@
 // deterministic two-kernel backward, which recomputes S and dP in the query-tile order.
 //
 // Per query tile t the MMA warp issues, in this order,
-//   dP^T(t) = V dO^T | dV += P^T dO | S^T(t+1) = K Q^T | dQ(t) = dS K | dK += dS^T Q
-// P^T = ex2(c S^T - LSE2) is computed while dP^T runs (as in the deterministic kernel);
-// dS^T = P^T (dP^T - D) while dV and S^T(t+1) run.  dS^T goes to a 128 x 128 16-bit
+//   dV += P^T dO | dP^T(t) = V dO^T | S^T(t+1) = K Q^T | dQ(t) = dS K | dK += dS^T Q
+// P^T(t+1) = ex2(c S^T - LSE2) is computed while dQ(t) and dK(t) run; dS^T(t) =
+// P^T (dP^T - D) while S^T(t+1) runs.  dS^T goes to a 128 x 128 16-bit
 // shared-memory tile laid out [key][query] with the 128-byte swizzle: read K-major it
 // is the A operand of dK (rows = keys), read MN-major it is the A operand of dQ (rows =
 // queries), so both products take it without a transpose.  dQ(t) accumulates in the
 // tensor-memory columns of dP^T, which are free once every element-wise thread has read
-// dP^T(t); the element-wise warps read dQ(t) out while dK(t) runs and add it to the
-// accumulator with vector reductions (red.global.add.v4.f32), and only then may dP^T(t+1)
-// take the columns back.  The element-wise order per tile is therefore
-//   read out dQ(t-1) | P^T(t) | dS^T(t)
-// so that the read-out overlaps dK(t-1) and P^T(t) overlaps dK(t-1) and dP^T(t).
+// dP^T(t); the element-wise warps read dQ(t) out while dK(t) and dV(t+1) run and add it to
+// the accumulator through per-warp staging areas and TMA bulk reductions
+// (cp.reduce.async.bulk .add.f32), and only then may
+// dP^T(t+1) take the columns back.  The element-wise order per tile is therefore
+//   P^T(t) | read out dQ(t-1) | dS^T(t)
+// and the reductions, which the memory pipeline throttles, are issued while dP^T(t) runs.
 //
 // The accumulator's summation order depends on which CTA's reduction reaches a value
 // first: dQ is not bit-for-bit reproducible from run to run (dK and dV are).  The
@@ -41,26 +42,34 @@ namespace {
 constexpr int kSmemMax = 232448;  // opt-in shared memory per CTA
 constexpr int kStatusLayout = 3;  // ATTN_ERR_CUDA: the shared-memory window is misaligned
 
-// Shared memory: K, V (stationary), STAGES x (Q, dO, LSE2, D), the dS tile, barriers.
-// At d = 128 this is 226.25 KB; dynamic shared memory starts 1024-byte aligned in
-// practice and the slack below the opt-in limit covers a start misaligned by up to
-// SLACK bytes (a kernel that finds more reports ATTN_ERR_CUDA and returns at once).
+// Shared memory: K, V (stationary), STAGES x (Q, LSE2, D), one dO tile, the dS tile, the
+// dQ staging area (2 KB per element-wise warp: half of the warp's 32 x 32 float32 share
+// of dQ(t) at a time), barriers.  dO is read only by dV(t) and dP^T(t), which run back to
+// back, so one buffer suffices: dO(t+1) is loaded once dP^T(t) is done and is not needed
+// before dV(t+1), three products later.  At d = 128 this is 226.25 KB; dynamic shared
+// memory starts 1024-byte aligned in practice and the slack below the opt-in limit
+// covers a start misaligned by up to SLACK bytes (a kernel that finds more reports
+// ATTN_ERR_CUDA and returns at once).
 template <int D>
 struct FusedLayout {
   using T = BwdTiles<D>;
   static constexpr int STAGES = (D == 128) ? 2 : 3;
-  static constexpr int STAGE_BYTES = 2 * T::TILE + 2 * 512;
+  static constexpr int STAGE_BYTES = T::TILE + 2 * 512;  // Q, LSE2, D
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = T::TILE;
   static constexpr int OFF_ST = 2 * T::TILE;
-  static constexpr int OFF_DS = OFF_ST + STAGES * STAGE_BYTES;
+  static constexpr int OFF_DO = OFF_ST + STAGES * STAGE_BYTES;
+  static constexpr int OFF_DS = OFF_DO + T::TILE;
   static constexpr int DS_BYTES = kTileN * kTileM * 2;
-  static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+  static constexpr int CHUNK = 32 * (D / 4) * 4;           // one warp's share of dQ(t): 32 rows x D/4 columns
+  static constexpr int OFF_STG = OFF_DS + DS_BYTES;
+  static constexpr int STG_BYTES = 16 * CHUNK / 2;         // half a share per element-wise warp
+  static constexpr int OFF_BAR = OFF_STG + STG_BYTES;
   static constexpr int NEED = OFF_BAR + 256;
   static constexpr int SMEM = NEED + 1024 < kSmemMax ? NEED + 1024 : kSmemMax;
   static constexpr int SLACK = SMEM - NEED;
   static_assert(SLACK >= 0, "shared memory");
-  static constexpr int S_Q = 0, S_DO = T::TILE, S_L = 2 * T::TILE, S_D = 2 * T::TILE + 512;
+  static constexpr int S_Q = 0, S_L = T::TILE, S_D = T::TILE + 512;
   // dQ(t) shares dP^T's columns (see the file header)
   static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DV = 256, TM_DK = 256 + D, TM_DQ = TM_DP, TM_COLS = 512;
 };
@@ -75,24 +84,54 @@ enum : int {
   F_DQFREE = 6,   // dQ(t) read out of tensor memory (all element-wise threads)
   F_DONE = 7,
   F_DRAIN = 8,
-  F_QFULL = 9,    // + stage
-  F_EMPTY = 12,   // + stage
-  F_COUNT = 15
+  F_DOFULL = 9,   // dO(t) loaded
+  F_DOFREE = 10,  // dP^T(t), the last reader of dO(t), done (MMA commit)
+  F_QFULL = 11,   // + stage: Q(t), LSE2, D loaded
+  F_EMPTY = 14,   // + stage: dK(t), the last reader of Q(t), done (MMA commit)
+  F_COUNT = 17
 };
 static_assert(8 * F_COUNT + 16 <= 256, "barrier area");
 
-// dQ(t) of this thread's query row, columns [(D/4) h, (D/4)(h+1)), added to the
-// accumulator: 32 consecutive rows x 4 columns are contiguous, so a warp's vector
-// reduction covers 512 contiguous bytes.
+// TMA tensor reduction (add, float32) of one staged box into the accumulator at
+// (column c0, row c1) (bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* m, uint32_t src, int c0, int c1) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(m)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+
+// This warp's share of dQ(t) -- rows 32 wq .. 32 wq + 31 of the query tile (one per lane),
+// columns (D/4) h .. (D/4)(h+1) - 1 -- added to the accumulator.  The share goes through
+// the warp's staging area in two halves of 16 rows; each half is one box of the
+// accumulator's tensor map, handed to the TMA unit as one reduction.  Before a half is
+// written, the previous reduction must have finished reading the area.  The area is
+// swizzled as the map expects (16-byte piece c of row r at piece c ^ (r mod 8) of a
+// 128-byte row at d = 128, c ^ ((r / 2) mod 4) of a 64-byte row at d = 64), which also
+// spreads the 16 lanes' stores over all banks.
 template <int D>
-__device__ __forceinline__ void dq_reduce(float* acc, size_t group_base, int h, int lane, const uint32_t* v) {
+__device__ __forceinline__ void dq_stage_reduce(const CUtensorMap* acc, int col0, int row0, uint8_t* stg, int lane,
+                                                const uint32_t* v) {
+  constexpr int ROW_BYTES = D;  // D/4 floats
+  constexpr int PIECES = D / 16;
 #pragma unroll
-  for (int g = 0; g < D / 16; ++g) {
-    float* p = acc + (group_base + static_cast<size_t>((D / 16) * h + g)) * 128 + lane * 4;
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(v[4 * g])),
-                 "f"(__uint_as_float(v[4 * g + 1])), "f"(__uint_as_float(v[4 * g + 2])),
-                 "f"(__uint_as_float(v[4 * g + 3]))
-                 : "memory");
+  for (int half = 0; half < 2; ++half) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+    if ((lane >> 4) == half) {
+      const int r = lane & 15;
+      const int sw = (D == 128) ? (r & 7) : ((r >> 1) & 3);
+#pragma unroll
+      for (int c = 0; c < PIECES; ++c)
+        *reinterpret_cast<uint4*>(stg + r * ROW_BYTES + ((c ^ sw) << 4)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) {
+      tma_reduce_add_2d(acc, smem_u32(stg), col0, row0 + 16 * half);
+      bulk_commit();
+    }
   }
 }
 
@@ -146,6 +185,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
     mbar_init(bar(F_DQFREE), 128 * kEw);
     mbar_init(bar(F_DONE), 1);
     mbar_init(bar(F_DRAIN), 1);
+    mbar_init(bar(F_DOFULL), 1);
+    mbar_init(bar(F_DOFREE), 1);
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(bar(F_QFULL + s), 1);
       mbar_init(bar(F_EMPTY + s), 1);
@@ -170,6 +211,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       prefetch_tmap(&a.tm_k);
       prefetch_tmap(&a.tm_v);
       prefetch_tmap(&a.tm_do);
+      prefetch_tmap(&a.tm_dqacc);
       mbar_arrive_expect_tx(bar(F_KVFULL), 2 * T::TILE);
       for (int kb = 0; kb < T::KB; ++kb) {
         tma_load_3d(sb + L::OFF_K + kb * T::BLK, &a.tm_k, bar(F_KVFULL), kb * 64, VARLEN ? hh : k0,
@@ -177,27 +219,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
         tma_load_3d(sb + L::OFF_V + kb * T::BLK, &a.tm_v, bar(F_KVFULL), kb * 64, VARLEN ? hh : k0,
                     VARLEN ? tk0 + k0 : bh);
       }
-      int issued = 0;
+      int issued = 0, do_issued = 0;
       for (int t = 0; t < n_iter; ++t) {
         const int s = t % L::STAGES;
         const int q0 = (i_begin + t) * kTileM;
         if (t >= L::STAGES && !mbar_wait(bar(F_EMPTY + s), ((t / L::STAGES) - 1) & 1, wc)) break;
         const uint32_t st = stage_base(s);
-        mbar_arrive_expect_tx(bar(F_QFULL + s), 2 * T::TILE + 1024);
-        for (int kb = 0; kb < T::KB; ++kb) {
+        mbar_arrive_expect_tx(bar(F_QFULL + s), T::TILE + 1024);
+        for (int kb = 0; kb < T::KB; ++kb)
           tma_load_3d(st + L::S_Q + kb * T::BLK, &a.tm_q, bar(F_QFULL + s), kb * 64, VARLEN ? hh : q0,
                       VARLEN ? tq0 + q0 : bh);
-          tma_load_3d(st + L::S_DO + kb * T::BLK, &a.tm_do, bar(F_QFULL + s), kb * 64, VARLEN ? hh : q0,
-                      VARLEN ? tq0 + q0 : bh);
-        }
         const size_t w = static_cast<size_t>(bh) * a.Npad + q0;
         bulk_load(st + L::S_L, a.lse2 + w, 512, bar(F_QFULL + s));
         bulk_load(st + L::S_D, a.delta + w, 512, bar(F_QFULL + s));
         issued = t + 1;
+        if (t > 0 && !mbar_wait(bar(F_DOFREE), (t - 1) & 1, wc)) break;
+        mbar_arrive_expect_tx(bar(F_DOFULL), T::TILE);
+        for (int kb = 0; kb < T::KB; ++kb)
+          tma_load_3d(sb + L::OFF_DO + kb * T::BLK, &a.tm_do, bar(F_DOFULL), kb * 64, VARLEN ? hh : q0,
+                      VARLEN ? tq0 + q0 : bh);
+        do_issued = t + 1;
       }
       mbar_wait(bar(F_KVFULL), 0, wc);
       for (int t = (issued > L::STAGES ? issued - L::STAGES : 0); t < issued; ++t)
         mbar_wait(bar(F_QFULL + t % L::STAGES), (t / L::STAGES) & 1, wc);
+      if (do_issued > 0) mbar_wait(bar(F_DOFULL), (do_issued - 1) & 1, wc);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -223,22 +269,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       for (int t = 0; ok && t < n_iter; ++t) {
         const int s = t % L::STAGES;
         const uint32_t st = stage_base(s);
-        // dP^T(t) takes dQ(t-1)'s columns once the element-wise warps have read them.
+        if (!(ok = mbar_wait(bar(F_PREADY), t & 1, wc) && mbar_wait(bar(F_DOFULL), t & 1, wc))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
+          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
+                 sdesc_sw128(sb + L::OFF_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+        // dP^T(t) takes dQ(t-1)'s columns once the element-wise warps have read them; dK(t-1)
+        // and dV(t) run meanwhile.
         if (t > 0 && !(ok = mbar_wait(bar(F_DQFREE), (t - 1) & 1, wc))) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
           mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
-                 sdesc_sw128(st + L::S_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+                 sdesc_sw128(sb + L::OFF_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(F_DPFULL));
-        if (!(ok = mbar_wait(bar(F_PREADY), t & 1, wc))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
-          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
-                 sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+        tc_commit(bar(F_DOFREE));
         if (t + 1 < n_iter) {  // S^T(t+1) over P^T(t): issued after dV(t), which reads it
           if (!(ok = mbar_wait(bar(F_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
           tc_fence_after();
@@ -272,9 +320,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
     const uint32_t t_s = t_lane + L::TM_S + kEwCols * h, t_dp = t_lane + L::TM_DP + kEwCols * h;
     const float sl2 = a.scale_log2;
     uint8_t* ds_tile = smem + L::OFF_DS;
-    const size_t groups_per_head = static_cast<size_t>(a.Npad) / 32;
+    uint8_t* stg = smem + L::OFF_STG + (warp - 4) * (L::CHUNK / 2);
     // Reads dQ(t) (this thread's query row, the warpgroup's D/4 columns) out of tensor
-    // memory, frees the columns and adds the values to the accumulator.
+    // memory, frees the columns and adds the warp's share to the accumulator.
     auto drain = [&](int t) -> bool {
       if (!mbar_wait_warp(bar(F_DQFULL), t & 1, wc)) return false;
       tc_fence_after();
@@ -285,16 +333,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
         tmem_ld_x16(t_lane + L::TM_DQ + (D / 4) * h, v);
       tc_fence_before();
       mbar_arrive(bar(F_DQFREE));
-      const int q = (i_begin + t) * kTileM + row;
-      if (q < N)
-        dq_reduce<D>(a.dq_acc, (static_cast<size_t>(bh) * groups_per_head + q / 32) * (D / 4), h, lane, v);
+      // rows of this warp in the accumulator: head bh's padded rows; rows past the end hold
+      // zeros (their dS is zero) and add nothing
+      dq_stage_reduce<D>(&a.tm_dqacc, (D / 4) * h, bh * a.Npad + (i_begin + t) * kTileM + 32 * wq, stg, lane, v);
       return true;
     };
     bool ok = true;
     for (int t = 0; t < n_iter; ++t) {
       const int s = t % L::STAGES;
       const int qt = i_begin + t;
-      if (t > 0 && !(ok = drain(t - 1))) break;
       uint32_t keepbits = 0xffffffffu;  // bit c: query column 32h + c keeps this thread's key
       if constexpr (DROP) {
         // lane L draws query qt*128 + 32h + L's bits over keys k0 + 32wq .. +31
@@ -319,7 +366,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
                                 : a.causal    ? k0 + row - cofs - qt * kTileM - kEwCols * h
                                               : 0;
       float p[kEwCols];
-      {  // P^T = 2^-(lse2 - s sl2) (overlaps dK(t-1) and dP^T(t))
+      {  // P^T = 2^-(lse2 - s sl2) (overlaps dQ(t-1) and dK(t-1))
         uint32_t sv[kEwCols];
         tmem_ld_x32(t_s, sv);
         const uint64_t nsl2 = f32x2_pack(-sl2, -sl2);
@@ -359,7 +406,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(F_PREADY));
-      // dS^T = P^T (dP^T - D) into the shared [key][query] tile (overlaps dV and S^T(t+1)).
+      // dQ(t-1) out of tensor memory (it completed before dK(t-1); dP^T(t) waits for it).
+      if (t > 0 && !(ok = drain(t - 1))) break;
+      // dS^T = P^T (dP^T - D) into the shared [key][query] tile (overlaps S^T(t+1)).
       if (!(ok = mbar_wait_warp(bar(F_DPFULL), t & 1, wc))) break;
       tc_fence_after();
       {
@@ -399,10 +448,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       mbar_arrive(bar(F_DSREADY));
     }
     if (ok && n_iter > 0) ok = drain(n_iter - 1);
+    if (lane == 0) bulk_wait_all();  // this warp's bulk reductions are done
     if (ok) ok = mbar_wait_warp(bar(F_DONE), 0, wc);
     // Epilogue: warpgroups 0-1 write dV, 2-3 write scale * dK, as the dK/dV kernel does.
     const int which = h >> 1;
-    uint8_t* stage = smem + L::OFF_ST + (which == 0 ? L::S_DO : L::S_Q);
+    uint8_t* stage = smem + (which == 0 ? L::OFF_DO : L::OFF_ST + L::S_Q);
     if (ok) {
       tc_fence_after();
       const uint32_t col = (which == 0) ? L::TM_DV : L::TM_DK;
@@ -438,45 +488,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
   }
 }
 
-// dQ = scale * accumulator, rounded to the 16-bit type: one block per 32-row group of a
-// head, transposed through shared memory so that both the float32 reads (512 contiguous
-// bytes per warp instruction) and the 16-bit row writes are coalesced.
+// dQ = scale * accumulator, rounded to the 16-bit type: one thread per 8 columns of a row
+// (two float32 vector loads, one 16-byte store; consecutive threads cover consecutive
+// columns, so both sides are coalesced).
 template <int D, bool BF16, bool VARLEN>
 __global__ void __launch_bounds__(256) bwd_dq_finish_kernel(const __grid_constant__ BwdArgs a) {
-  __shared__ float tile[32][D + 4];
-  const int groups_per_head = a.Npad / 32;
-  const int g = static_cast<int>(blockIdx.x);
-  const int bh = g / groups_per_head;
-  const int r0 = (g % groups_per_head) * 32;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = idx / (D / 8);
+  const int u = static_cast<int>(idx % (D / 8));
+  if (row >= static_cast<int64_t>(a.BH) * a.Npad) return;
+  const int bh = static_cast<int>(row / a.Npad), r = static_cast<int>(row % a.Npad);
   int N = a.N, hh = 0, tq0 = 0;
   if constexpr (VARLEN) {
     const SeqView sv = seq_view(a, bh);
     N = sv.N, hh = sv.hh, tq0 = sv.tq0;
   }
-  if (r0 >= N) return;
-  const float4* src = reinterpret_cast<const float4*>(a.dq_acc) + static_cast<size_t>(g) * (D / 4) * 32;
-  for (int i = threadIdx.x; i < (D / 4) * 32; i += blockDim.x) {
-    const float4 x = src[i];
-    const int cg = i / 32, rr = i % 32;
-    *reinterpret_cast<float4*>(&tile[rr][cg * 4]) = x;
-  }
-  __syncthreads();
+  if (r >= N) return;
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc + row * D + u * 8);
+  const float4 x0 = src[0], x1 = src[1];
   const float sc = a.scale;
-  for (int i = threadIdx.x; i < 32 * (D / 8); i += blockDim.x) {
-    const int rr = i / (D / 8), u = i % (D / 8);
-    const int r = r0 + rr;
-    if (r >= N) continue;
-    const float4 x0 = *reinterpret_cast<const float4*>(&tile[rr][u * 8]);
-    const float4 x1 = *reinterpret_cast<const float4*>(&tile[rr][u * 8 + 4]);
-    const uint4 out = make_uint4(pack2<BF16>(x0.x * sc, x0.y * sc), pack2<BF16>(x0.z * sc, x0.w * sc),
-                                 pack2<BF16>(x1.x * sc, x1.y * sc), pack2<BF16>(x1.z * sc, x1.w * sc));
-    size_t elem;
-    if constexpr (VARLEN)
-      elem = (static_cast<size_t>(tq0 + r) * a.H + hh) * D + u * 8;
-    else
-      elem = (static_cast<size_t>(bh) * a.N + r) * D + u * 8;
-    *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dq) + elem * 2) = out;
-  }
+  const uint4 out = make_uint4(pack2<BF16>(x0.x * sc, x0.y * sc), pack2<BF16>(x0.z * sc, x0.w * sc),
+                               pack2<BF16>(x1.x * sc, x1.y * sc), pack2<BF16>(x1.z * sc, x1.w * sc));
+  size_t elem;
+  if constexpr (VARLEN)
+    elem = (static_cast<size_t>(tq0 + r) * a.H + hh) * D + u * 8;
+  else
+    elem = (static_cast<size_t>(bh) * a.N + r) * D + u * 8;
+  *reinterpret_cast<uint4*>(static_cast<uint8_t*>(a.dq) + elem * 2) = out;
 }
 
 template <int D, bool BF16, bool VARLEN, bool DROP>
@@ -491,8 +529,8 @@ cudaError_t launch_fused_t(const BwdArgs& a, cudaStream_t st) {
 
 template <int D, bool BF16, bool VARLEN>
 cudaError_t launch_finish_t(const BwdArgs& a, cudaStream_t st) {
-  const int groups = a.BH * (a.Npad / 32);
-  bwd_dq_finish_kernel<D, BF16, VARLEN><<<groups, 256, 0, st>>>(a);
+  const int64_t threads = static_cast<int64_t>(a.BH) * a.Npad * (D / 8);
+  bwd_dq_finish_kernel<D, BF16, VARLEN><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 

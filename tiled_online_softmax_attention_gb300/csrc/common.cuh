@@ -85,10 +85,12 @@ struct BwdArgs {
   void* dq_out;                         // packed gradients, written row by row
   void* dk_out;
   void* dv_out;
-  // fused backward only: float32 dQ accumulator in the workspace, B*H*Npad*d values in
-  // [B*H][Npad/32][d/4][32][4] order (32 rows x 4 columns contiguous), zeroed by the
-  // preparation pass; nullptr for the deterministic kernels
+  // fused backward only: float32 dQ accumulator in the workspace, [B*H][Npad][d] (row
+  // major), zeroed by the preparation pass; nullptr for the deterministic kernels.  The
+  // 2-D map over it ({d, B*H*Npad}, box {d/4, 16}, 128- or 64-byte swizzle) carries the
+  // TMA bulk reductions of the fused kernel.
   float* dq_acc;
+  CUtensorMap tm_dqacc;
   void* dq;                             // fused backward: dQ [B*H][N][d] (the finishing pass writes it)
 };
 
