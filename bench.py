@@ -3,8 +3,8 @@
 
 Workload (the fwd/bwd configuration): B=2, H=16, N=8192, d=128, BF16, causal,
 Q, K, V, dO iid N(0,1) from a fixed seed.  One step = attn_fwd followed by the
-three stages of attn_bwd (prepare, the fused dK/dV/dQ pass, the dQ finish)
-through the C ABI, inputs resident in HBM.  FLOPs per step are the algorithmic count: forward 4*B*H*N^2*d plus
+three stages of attn_bwd (prepare, dK/dV, dQ) through the C ABI, inputs resident
+in HBM.  FLOPs per step are the algorithmic count: forward 4*B*H*N^2*d plus
 backward 10*B*H*N^2*d, both halved for causal.  The inputs (4 x 64 MiB) exceed
 the 129 MB L2, so no flush runs between steps.
 
@@ -205,8 +205,8 @@ def peaks():
         return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {"fwd": ["fwd.cu"], "bwd_prepare": ["bwd.cu"], "bwd_dkdvdq": ["bwd_fused.cu", "bwd_common.cuh"],
-                  "bwd_dq_finish": ["bwd_fused.cu"]}
+KERNEL_SOURCES = {"fwd": ["fwd.cu"], "bwd_prepare": ["bwd.cu"], "bwd_dkdv": ["bwd.cu", "bwd_common.cuh"],
+                  "bwd_dq": ["bwd.cu", "bwd_common.cuh"]}
 
 
 def source_digest(kernel: str):
@@ -247,7 +247,7 @@ def run_ours(args, w, ws_, rank, local):
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    nbytes = attn.attn_bwd_deterministic_workspace_bytes(B, H, N, d)  # the stages below need only this
     wsp = torch.empty(nbytes, device=dev, dtype=torch.uint8)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -257,7 +257,7 @@ def run_ours(args, w, ws_, rank, local):
         if rc != attn.ATTN_OK:
             raise RuntimeError(f"{what}: {attn.attn_status_string(rc)}")
 
-    names = ["fwd", "bwd_prepare", "bwd_dkdvdq", "bwd_dq_finish"]
+    names = ["fwd", "bwd_prepare", "bwd_dkdv", "bwd_dq"]
 
     def step(ev=None):
         if ev is not None:
@@ -268,11 +268,12 @@ def run_ours(args, w, ws_, rank, local):
         check(attn.attn_bwd_prepare(o, do, lse, wsp, nbytes, B, H, N, d, dt, stream), "attn_bwd_prepare")
         if ev is not None:
             ev[2].record(stream)
-        check(attn.attn_bwd_dkdvdq(q, k, v, do, wsp, nbytes, dk, dv, B, H, N, d, dt, True, scale, status, stream),
-              "attn_bwd_dkdvdq")
+        check(attn.attn_bwd_dkdv(q, k, v, do, wsp, nbytes, dk, dv, B, H, N, d, dt, True, scale, status, stream),
+              "attn_bwd_dkdv")
         if ev is not None:
             ev[3].record(stream)
-        check(attn.attn_bwd_dq_finish(wsp, nbytes, dq, B, H, N, d, dt, scale, stream), "attn_bwd_dq_finish")
+        check(attn.attn_bwd_dq(q, k, v, do, wsp, nbytes, dq, B, H, N, d, dt, True, scale, status, stream),
+              "attn_bwd_dq")
         if ev is not None:
             ev[4].record(stream)
 
@@ -306,10 +307,8 @@ def run_ours(args, w, ws_, rank, local):
 
     # Algorithmic FLOPs per launch (causal halves every N x N product):
     unit = 2.0 * B * H * N * N * d / 2          # one N x N x d product, causal
-    kflops = {"fwd": 2 * unit, "bwd_prepare": 0.0, "bwd_dkdvdq": 5 * unit, "bwd_dq_finish": 0.0}
-    # read O, dO, lse; write D, LSE2 and clear the dQ accumulator (the whole workspace)
-    kbytes = {"bwd_prepare": 2 * B * H * N * d * 2 + B * H * N * 4 + nbytes,
-              "bwd_dq_finish": B * H * N * d * (4 + 2)}                         # read the accumulator, write dQ
+    kflops = {"fwd": 2 * unit, "bwd_prepare": 0.0, "bwd_dkdv": 4 * unit, "bwd_dq": 1 * unit}
+    kbytes = {"bwd_prepare": 2 * B * H * N * d * 2 + B * H * N * 4 + nbytes}   # read O, dO, lse; write D, LSE2
     flops = step_flops(w)
     value = ws_ * args.steps * flops / (elapsed_ms * 1e-3) / 1e12
     pk = peaks()
@@ -455,26 +454,37 @@ def long_forward(attn, dev):
     res["fp8_forward_B1_H32_N16384_d128"] = fp8_forward(attn, dev)
     res["d256_forward_and_step_B1_H16_N16384"] = d256_side(attn, dev)
     res["dropout_training_step_p0.1"] = dropout_step(attn, dev)
-    res["backward_fused_vs_deterministic_B2_H16_N8192"] = backward_modes(attn, dev)
+    res["backward_paths_B2_H16_N8192"] = backward_modes(attn, dev)
     return res
 
 
 def backward_modes(attn, dev):
-    """The training-step backward alone (B=2, H=16, N=8192, d=128, causal) through attn_bwd
-    (the fused pass: five products per tile pair, dQ through a float32 accumulator) and
-    attn_bwd_deterministic (seven products, no atomics), FLOPs counted 10*B*H*N^2*d/2."""
+    """The training-step backward alone (B=2, H=16, N=8192, d=128, causal), FLOPs counted
+    10*B*H*N^2*d/2: attn_bwd (the two deterministic kernels as one grid), the fused pass
+    through its stages (prepare, dK/dV/dQ, dQ finish: five products per tile pair, dQ
+    through a float32 accumulator), and attn_bwd_deterministic."""
     w = workloads.WORKLOADS["c5"]
     x = workloads.inputs("c5")
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
     o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
     lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
-    attn.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, True, w.scale)
+    B, H, N, d, dt, sc = w.B, w.H, w.N, w.d, q.dtype, w.scale
+    attn.attn_fwd(q, k, v, o, lse, B, H, N, d, dt, True, sc)
+    nb = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = torch.empty(nb, device=dev, dtype=torch.uint8)
+    nbd = attn.attn_bwd_deterministic_workspace_bytes(B, H, N, d)
+
+    def fused():
+        attn.attn_bwd_prepare(o, do, lse, ws, nb, B, H, N, d, dt)
+        attn.attn_bwd_dkdvdq(q, k, v, do, ws, nb, dk, dv, B, H, N, d, dt, True, sc)
+        attn.attn_bwd_dq_finish(ws, nb, dq, B, H, N, d, dt, sc)
+
     out = {}
-    for name, call, size in (("fused", attn.attn_bwd, attn.attn_bwd_workspace_bytes),
-                             ("deterministic", attn.attn_bwd_deterministic, attn.attn_bwd_deterministic_workspace_bytes)):
-        nb = size(w.B, w.H, w.N, w.d)
-        ws = torch.empty(nb, device=dev, dtype=torch.uint8)
-        run = lambda: call(q, k, v, o, do, lse, dq, dk, dv, ws, nb, w.B, w.H, w.N, w.d, q.dtype, True, w.scale)
+    for name, run in (("attn_bwd", lambda: attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, nb, B, H, N, d, dt, True,
+                                                          sc)),
+                      ("fused_stages", fused),
+                      ("deterministic", lambda: attn.attn_bwd_deterministic(q, k, v, o, do, lse, dq, dk, dv, ws, nbd, B,
+                                                                            H, N, d, dt, True, sc))):
         for _ in range(3):
             run()
         torch.cuda.synchronize()
@@ -486,7 +496,7 @@ def backward_modes(attn, dev):
         b.record()
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / reps
-        f = workloads.bwd_flops(w.B, w.H, w.N, w.d, True)
+        f = workloads.bwd_flops(B, H, N, d, True)
         out[name] = {"ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
     return out
 

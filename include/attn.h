@@ -275,10 +275,10 @@ ATTN_API attn_status attn_fwd_fp8(const void *q8, const void *k8, const void *v8
                          int *dev_status, void *stream);
 
 /*
- * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd needs: two float32
- * values per row (D_i = rowsum(dO_i * O_i), and the logsumexp in base 2) and, for
- * d in {64, 128}, the float32 dQ accumulator of the fused backward (d values per row),
- * rows padded to whole 128-row tiles: (2 + d) * B*H*ceil(N/128)*128 * 4 bytes
+ * attn_bwd_workspace_bytes -- size of the device workspace attn_bwd and its variants
+ * need: two float32 values per row (D_i = rowsum(dO_i * O_i), and the logsumexp in base
+ * 2) and, for d in {64, 128}, the float32 dQ accumulator of the fused pass (d values per
+ * row), rows padded to whole 128-row tiles: (2 + d) * B*H*ceil(N/128)*128 * 4 bytes
  * (d = 256: 2 * B*H*ceil(N/128)*128 * 4 bytes).  Returns 0 for invalid sizes.
  *
  * attn_bwd_deterministic_workspace_bytes -- the two per-row values only:
@@ -302,13 +302,16 @@ ATTN_API size_t attn_bwd_deterministic_workspace_bytes(int B, int H, int N, int 
  *                      16-byte aligned; contents need not be initialised and
  *                      are clobbered.  The caller owns it.
  *   Outputs must not overlap inputs or each other.
- *   d in {64, 128}: one pass over each 128-key tile's query tiles computes dK, dV and
- *   dQ from the same recomputed tiles (five N x N x d products per tile pair, the
- *   algorithm's count); dQ is summed over the key tiles in the float32 accumulator of
- *   the workspace with floating-point atomic additions and then rounded to dt.  The
- *   order of those additions varies from run to run, so dQ may differ in its last bit
- *   between two identical calls (dK and dV do not); attn_bwd_deterministic gives
- *   identical bytes on every call, at seven products per tile pair.
+ *   d in {64, 128}: two kernels, dK and dV over 128-key tiles and dQ over 128-query tiles
+ *   (the second recomputes S and dP in its own tile order: seven N x N x d products per
+ *   tile pair, no atomics, the same bytes on every call), launched as one grid.  With
+ *   dropout (attn_bwd_dropout and its variants) the fused pass of attn_bwd_dkdvdq runs
+ *   instead: one pass over each key tile's query tiles gives dK, dV and that tile's
+ *   share of dQ from the same recomputed tiles (five products, the keep bits drawn once
+ *   instead of twice), dQ summed over the key tiles in the workspace's float32
+ *   accumulator by atomic reductions and then rounded to dt; the order of those
+ *   additions varies, so that dQ may differ in its last bit between identical calls.
+ *   Without dropout the two-kernel form measured faster on GB300 and is used.
  *   d = 256: the gradients come from three kernels (dV and dK, one 128-key tile per CTA
  *   each, and dQ, one 128-query tile per CTA), each streaming its operands in
  *   128-column halves: deterministic, the same gradients in more passes.
@@ -320,11 +323,10 @@ ATTN_API attn_status attn_bwd(const void *q, const void *k, const void *v, const
                      int *dev_status, void *stream);
 
 /*
- * attn_bwd_deterministic -- attn_bwd whose results are the same bytes on every call:
- * dK and dV from one kernel over key tiles, dQ from one over query tiles (which
- * recomputes S and dP in that order: seven products per tile pair instead of five), no
- * atomics.  Workspace: attn_bwd_deterministic_workspace_bytes().  Everything else is as
- * for attn_bwd.
+ * attn_bwd_deterministic -- the backward with a guarantee that its results are the same
+ * bytes on every call, whatever path attn_bwd takes: dK and dV from one kernel over key
+ * tiles, dQ from one over query tiles, no atomics.  Workspace:
+ * attn_bwd_deterministic_workspace_bytes().  Everything else is as for attn_bwd.
  */
 ATTN_API attn_status attn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
                                    const void *dout, const float *lse, void *dq, void *dk, void *dv,
@@ -333,9 +335,10 @@ ATTN_API attn_status attn_bwd_deterministic(const void *q, const void *k, const 
                                    int *dev_status, void *stream);
 
 /*
- * The fused stages attn_bwd runs at d in {64, 128}, in order, on one stream, after
+ * The fused backward (d in {64, 128}) as two stages, run in order on one stream after
  * attn_bwd_prepare with a workspace of attn_bwd_workspace_bytes() (which then also
- * clears the dQ accumulator).  Exported so that a caller can time them one by one.
+ * clears the dQ accumulator).  attn_bwd runs them for its dropout variants; they are
+ * exported so that a caller can run or time the five-product pass without dropout too.
  *
  * attn_bwd_dkdvdq    -- dK and dV, and each key tile's share of dQ added to the
  *                       workspace's float32 accumulator; one 128-key tile per CTA.

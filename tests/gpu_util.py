@@ -92,6 +92,28 @@ def run_bwd(q, k, v, o, lse, dout, causal, scale=None, stream=None, deterministi
     return tuple(g.t for g in outs)
 
 
+def run_bwd_fused(q, k, v, o, lse, dout, causal, scale=None, stream=None):
+    """The fused backward through its stage entry points (attn_bwd_prepare, attn_bwd_dkdvdq,
+    attn_bwd_dq_finish) with guarded outputs; returns (dq, dk, dv)."""
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    outs = [Guarded((B, H, N, d), q.dtype) for _ in range(3)]
+    nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_bwd_prepare(o, dout, lse, ws.t, nbytes, B, H, N, d, q.dtype, stream)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    rc = attn.attn_bwd_dkdvdq(q, k, v, dout, ws.t, nbytes, outs[1].t, outs[2].t, B, H, N, d, q.dtype, causal, scale,
+                              status, stream)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    rc = attn.attn_bwd_dq_finish(ws.t, nbytes, outs[0].t, B, H, N, d, q.dtype, scale, stream)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    assert all(g.intact() for g in outs) and ws.intact(), "the fused backward wrote outside its buffers"
+    return tuple(g.t for g in outs)
+
+
 def f64(t):
     return t.detach().double().cpu().numpy()
 

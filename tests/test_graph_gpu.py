@@ -1,8 +1,8 @@
 """CUDA-graph capture of the C ABI: every entry point only encodes tensor maps on the host
 and launches kernels on the caller's stream, so a forward + backward captured once into a
 CUDA graph and replayed on new input values gives the bytes of eager calls (except the
-fused backward's dQ, whose float32 additions come in a varying order: equal up to that
-order), with a clear device status word after every replay."""
+dQ of the fused backward that dropout takes, whose float32 additions come in a varying
+order: equal up to that order), with a clear device status word after every replay."""
 import math
 
 import pytest
@@ -26,7 +26,7 @@ class Step:
         self.nbytes = attn.attn_bwd_workspace_bytes(B, H, N, d)
         self.ws = torch.empty(self.nbytes, device="cuda", dtype=torch.uint8)
         self.status = torch.zeros(1, device="cuda", dtype=torch.int32)
-        self.fused = False  # set by fwd_bwd: the fused backward (d <= 128) ran
+        self.fused = False  # set by fwd_bwd: the fused backward (d <= 128, dropout) ran
 
     def load(self, seed):
         B, H, N, d = self.shape
@@ -42,7 +42,7 @@ class Step:
 
 def fwd_bwd(s, causal, p_drop=0.0, seed=0):
     B, H, N, d = s.shape
-    s.fused = d != 256
+    s.fused = d != 256 and p_drop > 0
     scale = 1.0 / math.sqrt(d)
     if p_drop > 0:
         rc = attn.attn_fwd_dropout(s.q, s.k, s.v, s.o, s.lse, B, H, N, d, s.q.dtype, causal, scale, p_drop, seed,

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import tiled_online_softmax_attention_gb300 as attn
-from gpu_util import GRAD_REL_L2, LSE_REL, O_MAX_ABS, Guarded, assert_same_grads, f64, grad_err, lse_err, o_err, sample_rows
+from gpu_util import GRAD_REL_L2, LSE_REL, O_MAX_ABS, Guarded, f64, grad_err, lse_err, o_err, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -112,8 +112,7 @@ def test_rect_long_prefix_sampled(causal):
 
 
 def test_rect_square_matches_attn_fwd():
-    """Nq = Nk through the rectangular entry points gives attn_fwd / attn_bwd's results (bytes, but
-    for the order of the fused backward's dQ additions)."""
+    """Nq = Nk through the rectangular entry points gives attn_fwd / attn_bwd's bytes."""
     x = draw_rect(1, 3, 700, 700, 128, "bf16", seed=3)
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
     o1, l1 = run_fwd_rect(q, k, v, True, 0.1)
@@ -121,4 +120,5 @@ def test_rect_square_matches_attn_fwd():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     g1 = run_bwd_rect(q, k, v, o1, l1, do, True, 0.1)
     g2 = attn.backward(q, k, v, o2, l2, do, True, 0.1)
-    assert_same_grads(g1, g2, "rectangular vs square:")  # dQ up to the fused accumulator's order
+    for a, b in zip(g1, g2):
+        assert torch.equal(a, b)

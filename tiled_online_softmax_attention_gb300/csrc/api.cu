@@ -661,9 +661,11 @@ attn_status finish_impl(const void* workspace, size_t workspace_bytes, void* dq,
   return ATTN_OK;
 }
 
-// The whole backward.  d <= 128 takes the fused path (five products per tile pair, dQ
-// through a float32 accumulator) unless the caller asks for the deterministic one;
-// d = 256 uses its three deterministic kernels.
+// The whole backward.  d <= 128 with dropout takes the fused path (five products per tile
+// pair, the keep bits drawn once, dQ through a float32 accumulator); without dropout the
+// two deterministic kernels measured faster on this GPU (the fused kernel's dQ reductions
+// compete with its shared-memory operand traffic) and run instead; d = 256 uses its three
+// deterministic kernels.
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
@@ -675,7 +677,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},
                              workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal, need);
   if (st != ATTN_OK) return st;
-  const bool fused = !deterministic && d != 256;
+  const bool fused = !deterministic && d != 256 && dr.t > 0;
   // the deterministic path does not read past the per-row values: prepare only those
   const size_t prep_bytes = fused ? workspace_bytes : attn_bwd_deterministic_workspace_bytes(B, H, N, d);
   if ((st = prepare_impl(o, dout, lse, workspace, prep_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
@@ -820,7 +822,7 @@ attn_status bwd_varlen_impl(const void* q, const void* k, const void* v, const v
   a.dk_out = dk;
   a.dv_out = dv;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d != 256) {  // the fused path: dK, dV and a float32 dQ accumulator, then dQ from it
+  if (d != 256 && dr.t > 0) {  // the fused path: dK, dV and a float32 dQ accumulator, then dQ from it
     a.dq_acc = dq_accumulator(workspace, B, H, max_q);
     a.dq = dq;
     if (!make_map_acc(&a.tm_dqacc, a.dq_acc, static_cast<int64_t>(B) * H * a.Npad, d)) return ATTN_ERR_CUDA;
