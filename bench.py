@@ -503,7 +503,9 @@ def backward_modes(attn, dev):
 
 def dropout_step(attn, dev):
     """The training-step workload (forward + backward) with dropout p = 0.1, against the
-    same step without dropout; FLOPs counted as without dropout."""
+    same step without dropout (the dropout entry points with p = 0), and with the keep
+    decisions drawn once (attn_fwd_dropout_bits / attn_bwd_dropout_bits); FLOPs counted as
+    without dropout."""
     w = workloads.WORKLOADS["c5"]
     x = workloads.inputs("c5")
     q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
@@ -529,6 +531,28 @@ def dropout_step(attn, dev):
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / reps
         out[f"p{p}"] = {"ms": round(ms, 4), "tflops": round(step_flops(w) / (ms * 1e-3) / 1e12, 1)}
+    # the keep decisions drawn once: the forward stores them, the backward reads them
+    nbits = attn.attn_dropout_bits_bytes(w.B, w.H, w.N, w.N)
+    bits = torch.empty(nbits, device=dev, dtype=torch.uint8)
+
+    def step_bits():
+        attn.attn_fwd_dropout_bits(q, k, v, o, lse, bits, nbits, w.B, w.H, w.N, w.d, q.dtype, True, w.scale, 0.1,
+                                   1234)
+        attn.attn_bwd_dropout_bits(q, k, v, o, do, lse, bits, nbits, dq, dk, dv, ws, nb, w.B, w.H, w.N, w.d, q.dtype,
+                                   True, w.scale, 0.1)
+    for _ in range(3):
+        step_bits()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    a.record()
+    for _ in range(reps):
+        step_bits()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    out["p0.1_keep_bits"] = {"ms": round(ms, 4), "tflops": round(step_flops(w) / (ms * 1e-3) / 1e12, 1),
+                             "keep_bits_bytes": nbits}
     return out
 
 

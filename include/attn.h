@@ -156,6 +156,38 @@ ATTN_API attn_status attn_bwd_dropout(const void *q, const void *k, const void *
                              float p_drop, uint64_t seed, int *dev_status, void *stream);
 
 /*
+ * attn_fwd_dropout_bits / attn_bwd_dropout_bits -- attn_fwd_dropout / attn_bwd_dropout
+ * with the keep decisions drawn once: the forward also stores every decision it draws
+ * into keep_bits, and the backward reads them there instead of drawing them again (the
+ * same decisions, so the results equal the drawing path's: O and lse byte for byte, dK
+ * and dV byte for byte, dQ up to the order of its float32 additions).
+ *   keep_bits      : device buffer of at least attn_dropout_bits_bytes(B, H, N, N) bytes,
+ *                    16-byte aligned, owned by the caller; written by the forward, read
+ *                    by the backward (which needs the forward's q, k, v, p and seed).
+ *                    Bit b of 32-bit word ((bh * ceil(N/128) + j) * 4 + w) * Npad + i
+ *                    (Npad = N rounded up to 128, bh = b * H + h) is the decision for
+ *                    query i and key 128 j + 32 w + b; words of key tiles a causal query
+ *                    tile never visits, and of rows past N, are not written.
+ *   p_drop         : as for attn_fwd_dropout, but at least 1/512 (round(256 p) >= 1);
+ *                    the backward takes no seed.
+ *   d in {64, 128} (d = 256: ATTN_ERR_UNSUPPORTED).  Everything else is as for
+ *   attn_fwd_dropout / attn_bwd_dropout.
+ * attn_dropout_bits_bytes -- B*H*ceil(Nk/128)*4*Npad(Nq)*4 bytes (N^2/8 per head for
+ *   Nq = Nk = N); 0 for invalid sizes.
+ */
+ATTN_API size_t attn_dropout_bits_bytes(int B, int H, int Nq, int Nk);
+ATTN_API attn_status attn_fwd_dropout_bits(const void *q, const void *k, const void *v, void *o, float *lse,
+                                  void *keep_bits, size_t keep_bits_bytes,
+                                  int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                                  float p_drop, uint64_t seed, int *dev_status, void *stream);
+ATTN_API attn_status attn_bwd_dropout_bits(const void *q, const void *k, const void *v, const void *o,
+                                  const void *dout, const float *lse, const void *keep_bits,
+                                  size_t keep_bits_bytes, void *dq, void *dk, void *dv,
+                                  void *workspace, size_t workspace_bytes,
+                                  int B, int H, int N, int d, attn_dtype dt, int causal, float scale,
+                                  float p_drop, int *dev_status, void *stream);
+
+/*
  * attn_fwd_rect_dropout / attn_bwd_rect_dropout -- attn_fwd_rect / attn_bwd_rect (Nq
  * queries against Nk keys, causal aligned to the last key) with attn_fwd_dropout's
  * dropout; element (bh, i, j) is query i and key j of the rectangular problem.

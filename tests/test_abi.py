@@ -307,3 +307,28 @@ def test_varlen_dropout_validates():
         a2 = dict(ba)
         a2.update(kw)
         assert attn.attn_bwd_varlen_dropout(**a2) == st, kw
+
+
+def test_dropout_bits_validate():
+    assert attn.attn_dropout_bits_bytes(2, 16, 8192, 8192) == 2 * 16 * 64 * 4 * 8192 * 4
+    assert attn.attn_dropout_bits_bytes(1, 1, 300, 129) == 2 * 4 * 384 * 4
+    assert attn.attn_dropout_bits_bytes(1, 1, 0, 128) == 0
+    nbits = attn.attn_dropout_bits_bytes(1, 2, 256, 256)
+    f = dict(q=A[0], k=A[1], v=A[2], o=A[3], lse=A[4], keep_bits=A[10], keep_bits_bytes=nbits, B=1, H=2, N=256, d=128,
+             dt=0, causal=1, scale=0.088, p_drop=0.1, seed=7, stream=0)
+    for kw, st in [(dict(p_drop=0.0), attn.ATTN_ERR_INVALID_ARG),        # nothing dropped: no bits to store
+                   (dict(p_drop=1.0), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(keep_bits_bytes=nbits - 4), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(keep_bits=A[10] + 4), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(keep_bits=A[3]), attn.ATTN_ERR_INVALID_ARG),     # the bits over o
+                   (dict(d=256), attn.ATTN_ERR_UNSUPPORTED)]:
+        assert attn.attn_fwd_dropout_bits(**dict(f, **kw)) == st, kw
+    b = dict(q=A[0], k=A[1], v=A[2], o=A[3], dout=A[4], lse=A[5], keep_bits=A[10], keep_bits_bytes=nbits, dq=A[6],
+             dk=A[7], dv=A[8], workspace=A[9], workspace_bytes=1 << 22, B=1, H=2, N=256, d=128, dt=0, causal=1,
+             scale=0.088, p_drop=0.1, stream=0)
+    for kw, st in [(dict(p_drop=0.001), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(keep_bits_bytes=16), attn.ATTN_ERR_INVALID_ARG),
+                   (dict(keep_bits=A[6]), attn.ATTN_ERR_INVALID_ARG),     # the bits over dq
+                   (dict(d=256), attn.ATTN_ERR_UNSUPPORTED),
+                   (dict(dk=A[6]), attn.ATTN_ERR_INVALID_ARG)]:
+        assert attn.attn_bwd_dropout_bits(**dict(b, **kw)) == st, kw

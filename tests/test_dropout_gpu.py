@@ -368,3 +368,65 @@ def test_dropout_varlen_random_batches(i, lens_q, lens_k, causal, d, dtype):
     for name, g, r in (("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
         e = grad_err(g, r)
         assert e <= GRAD_REL_L2, f"{name} relative L2 {e:.3e}"
+
+
+# ---------------------------------------------------------------- keep bits drawn once
+
+
+def run_drop_bits(q, k, v, do, causal, scale, p, seed):
+    """attn_fwd_dropout_bits then attn_bwd_dropout_bits, guarded outputs and keep bits."""
+    B, H, N, d = q.shape
+    o, lse = Guarded((B, H, N, d), q.dtype), Guarded((B, H, N), torch.float32)
+    nbits = attn.attn_dropout_bits_bytes(B, H, N, N)
+    bits = Guarded((nbits // 4,), torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = attn.attn_fwd_dropout_bits(q, k, v, o.t, lse.t, bits.t, nbits, B, H, N, d, q.dtype, causal, scale, p, seed,
+                                    status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and o.intact() and lse.intact() and bits.intact()
+    outs = [Guarded((B, H, N, d), q.dtype) for _ in range(3)]
+    nb = attn.attn_bwd_workspace_bytes(B, H, N, d)
+    ws = Guarded((nb // 4,), torch.float32)
+    rc = attn.attn_bwd_dropout_bits(q, k, v, o.t, do, lse.t, bits.t, nbits, outs[0].t, outs[1].t, outs[2].t, ws.t, nb,
+                                    B, H, N, d, q.dtype, causal, scale, p, status)
+    assert rc == attn.ATTN_OK, attn.attn_status_string(rc)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0 and all(g.intact() for g in outs) and ws.intact() and bits.intact()
+    return o.t, lse.t, bits.t, tuple(g.t for g in outs)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_bits_equal_drawing(causal, d):
+    """The stored-bits path gives the drawing path's forward bytes and its dK, dV bytes (dQ
+    up to the order of its float32 additions), matches the oracle, and every stored bit is
+    the definition's keep decision."""
+    B, H, N = 1, 2, 300
+    x = workloads.draw(B, H, N, d, "bf16", seed=5100 + d + causal, with_dout=True)
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+    scale, p, seed = 1.0 / math.sqrt(d), 0.15, 0x1234ABCD5678
+    o, lse, bits, g = run_drop_bits(q, k, v, do, causal, scale, p, seed)
+    o2, l2 = run_fwd_drop(q, k, v, causal, scale, p, seed)
+    assert torch.equal(o, o2) and torch.equal(lse, l2)
+    g2 = run_bwd_drop(q, k, v, o2, l2, do, causal, scale, p, seed)
+    assert_same_grads(g, g2, "stored bits vs drawing:")
+    t = t_of(p)
+    r = oracle.attn_bwd_dropout(x["q"], x["k"], x["v"], x["dout"], causal, scale, t, seed)
+    for name, gg, rr in zip(("dQ", "dK", "dV"), g, r):
+        assert grad_err(gg, rr) <= GRAD_REL_L2, name
+    # every written word against the definition (word ((bh * ntk + j) * 4 + w) * Npad + i)
+    words = bits.cpu().numpy().view(np.uint32)
+    ntk, npad = (N + 127) // 128, (N + 127) // 128 * 128
+    orc = oracle.default()
+    for bh in range(B * H):
+        for i in range(N):
+            nk = i + 1 if causal else N
+            for j0 in range(0, ((nk + 127) // 128) * 128, 32):
+                word = int(words[((bh * ntk + j0 // 128) * 4 + (j0 % 128) // 32) * npad + i])
+                for b in range(32):
+                    j = j0 + b
+                    if j >= N:
+                        continue
+                    want = orc.dropout_factor(bh, i, j, t, seed) > 0
+                    assert bool((word >> b) & 1) == want, f"bit (bh {bh}, query {i}, key {j})"

@@ -16,6 +16,10 @@ current stream):
                     B, H, max_q, max_k, Tq, Tk, d, dt, causal, scale, ...)
     attn_fwd_varlen_dropout / attn_bwd_varlen_dropout: the two above plus p_drop, seed
     attn_fwd_rect_dropout / attn_bwd_rect_dropout: attn_fwd_rect / attn_bwd_rect plus p_drop, seed
+    attn_dropout_bits_bytes(B, H, Nq, Nk)
+    attn_fwd_dropout_bits(q, k, v, o, lse, keep_bits, keep_bits_bytes, B, H, N, d, dt, causal, scale, p_drop, seed, ...)
+    attn_bwd_dropout_bits(q, k, v, o, dout, lse, keep_bits, keep_bits_bytes, dq, dk, dv, workspace, workspace_bytes,
+                          B, H, N, d, dt, causal, scale, p_drop, ...)   (the keep decisions drawn once)
     attn_fwd_varlen_splitkv_workspace_bytes(H, Tq, d, n_splits)
     attn_fwd_varlen_splitkv(q, k, v, o, lse, workspace, workspace_bytes, cu_q, cu_k, B, H, max_q, max_k,
                             Tq, Tk, d, dt, causal, scale, n_splits, dev_status=None, stream=None)
@@ -72,7 +76,7 @@ ATTN_FP16 = 1
 LIB_PATH = _build.LIB
 EXPORTS = ("attn_fwd", "attn_fwd_rect", "attn_bwd_rect", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_varlen_dropout", "attn_bwd_varlen_dropout", "attn_fwd_rect_dropout", "attn_bwd_rect_dropout", "attn_fwd_dropout", "attn_bwd_dropout", "attn_fwd_fp8", "attn_fwd_splitkv_workspace_bytes", "attn_fwd_splitkv", "attn_fwd_splitkv_rect", "attn_fwd_varlen_splitkv_workspace_bytes", "attn_fwd_varlen_splitkv", "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_prepare", "attn_bwd_dkdv",
            "attn_bwd_dq", "attn_bwd_deterministic_workspace_bytes", "attn_bwd_deterministic", "attn_bwd_dkdvdq",
-           "attn_bwd_dq_finish", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
+           "attn_bwd_dq_finish", "attn_dropout_bits_bytes", "attn_fwd_dropout_bits", "attn_bwd_dropout_bits", "attn_bwd_noalloc", "attn_status_string", "attn_selftest_bounded_wait")
 
 _lib = None
 
@@ -148,6 +152,12 @@ def load(build_if_missing: bool = True):
     lib.attn_bwd_dkdvdq.restype = I
     lib.attn_bwd_dq_finish.argtypes = [P, SZ, P, I, I, I, I, I, F, P]
     lib.attn_bwd_dq_finish.restype = I
+    lib.attn_dropout_bits_bytes.argtypes = [I, I, I, I]
+    lib.attn_dropout_bits_bytes.restype = SZ
+    lib.attn_fwd_dropout_bits.argtypes = [P, P, P, P, P, P, SZ, I, I, I, I, I, I, F, F, U64, P, P]
+    lib.attn_fwd_dropout_bits.restype = I
+    lib.attn_bwd_dropout_bits.argtypes = [P, P, P, P, P, P, P, SZ, P, P, P, P, SZ, I, I, I, I, I, I, F, F, P, P]
+    lib.attn_bwd_dropout_bits.restype = I
     lib.attn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P, P]
     lib.attn_bwd_noalloc.restype = I
     lib.attn_status_string.argtypes = [I]
@@ -366,6 +376,27 @@ def attn_bwd_dkdvdq(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, 
 def attn_bwd_dq_finish(workspace, workspace_bytes, dq, B, H, N, d, dt, scale, stream=None) -> int:
     return int(load().attn_bwd_dq_finish(_ptr(workspace), int(workspace_bytes), _ptr(dq), int(B), int(H), int(N),
                                          int(d), _dt(dt), float(scale), _stream(stream)))
+
+
+def attn_dropout_bits_bytes(B, H, Nq, Nk) -> int:
+    return int(load().attn_dropout_bits_bytes(int(B), int(H), int(Nq), int(Nk)))
+
+
+def attn_fwd_dropout_bits(q, k, v, o, lse, keep_bits, keep_bits_bytes, B, H, N, d, dt, causal, scale, p_drop, seed,
+                          dev_status=None, stream=None) -> int:
+    return int(load().attn_fwd_dropout_bits(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(keep_bits),
+                                            int(keep_bits_bytes), int(B), int(H), int(N), int(d), _dt(dt),
+                                            int(bool(causal)), float(scale), float(p_drop),
+                                            int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(dev_status), _stream(stream)))
+
+
+def attn_bwd_dropout_bits(q, k, v, o, dout, lse, keep_bits, keep_bits_bytes, dq, dk, dv, workspace, workspace_bytes,
+                          B, H, N, d, dt, causal, scale, p_drop, dev_status=None, stream=None) -> int:
+    return int(load().attn_bwd_dropout_bits(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                            _ptr(keep_bits), int(keep_bits_bytes), _ptr(dq), _ptr(dk), _ptr(dv),
+                                            _ptr(workspace), int(workspace_bytes), int(B), int(H), int(N), int(d),
+                                            _dt(dt), int(bool(causal)), float(scale), float(p_drop),
+                                            _ptr(dev_status), _stream(stream)))
 
 
 def attn_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, dt, causal, scale, dev_status=None,

@@ -160,6 +160,12 @@ attn_status check_device() {
   return ATTN_OK;
 }
 
+// A tensor argument and its size in bytes.
+struct Buf {
+  const void* p;
+  size_t bytes;
+};
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -187,7 +193,7 @@ namespace {
 // The forward for Nq queries against Nk keys (Nk = Nq for attn_fwd).
 attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int Nk,
                      int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
-                     const Dropout& dr = Dropout{}) {
+                     const Dropout& dr = Dropout{}, uint32_t* keep_bits = nullptr) {
   attn_status st = check_sizes(B, H, N, d, dt, scale, true, Nk);
   if (st != ATTN_OK) return st;
   if (causal && Nk < N) return ATTN_ERR_INVALID_ARG;
@@ -218,6 +224,8 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = wait_limit_ns();
   set_dropout(a, dr);
+  a.keep_bits = keep_bits;
+  a.bits_rows = static_cast<int>((static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM);
   const cudaError_t e = d == 256  ? attn::launch_fwd256(a, bf16, static_cast<cudaStream_t>(stream))
                         : dr.t > 0 ? attn::launch_fwd_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
                                    : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
@@ -348,6 +356,28 @@ attn_status attn_fwd_dropout(const void* q, const void* k, const void* v, void* 
   return fwd_impl(q, k, v, o, lse, B, H, N, N, d, dt, causal, scale, dev_status, stream, dr);
 }
 
+size_t attn_dropout_bits_bytes(int B, int H, int Nq, int Nk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 0;
+  const size_t rows = (static_cast<size_t>(Nq) + kTileM - 1) / kTileM * kTileM;
+  const size_t tiles = (static_cast<size_t>(Nk) + kTileM - 1) / kTileM;
+  return static_cast<size_t>(B) * H * tiles * 4 * rows * sizeof(uint32_t);
+}
+
+attn_status attn_fwd_dropout_bits(const void* q, const void* k, const void* v, void* o, float* lse, void* keep_bits,
+                                  size_t keep_bits_bytes, int B, int H, int N, int d, attn_dtype dt, int causal,
+                                  float scale, float p_drop, uint64_t seed, int* dev_status, void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, seed, &dr) || dr.t == 0) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_dropout_bits_bytes(B, H, N, N);
+  if (need == 0 || keep_bits_bytes < need || !aligned16(keep_bits)) return ATTN_ERR_INVALID_ARG;
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
+  const size_t qb = static_cast<size_t>(B) * H * N * d * 2, lb = static_cast<size_t>(B) * H * N * 4;
+  for (const Buf& b : {Buf{q, qb}, Buf{k, qb}, Buf{v, qb}, Buf{o, qb}, Buf{lse, lb}})
+    if (b.p && overlaps(b.p, b.bytes, keep_bits, need)) return ATTN_ERR_INVALID_ARG;
+  return fwd_impl(q, k, v, o, lse, B, H, N, N, d, dt, causal, scale, dev_status, stream, dr,
+                  static_cast<uint32_t*>(keep_bits));
+}
+
 attn_status attn_fwd_rect_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                   int Nq, int Nk, int d, attn_dtype dt, int causal, float scale, float p_drop,
                                   uint64_t seed, int* dev_status, void* stream) {
@@ -474,11 +504,6 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
 
 namespace {
 
-// A tensor argument and its size in bytes.
-struct Buf {
-  const void* p;
-  size_t bytes;
-};
 
 // Validation shared by the backward entry points: every input and output 16-byte
 // aligned and non-null, no output overlapping an input, the logsumexp, the workspace
@@ -622,7 +647,8 @@ attn_status dq_impl(const void* q, const void* k, const void* v, const void* dou
 // accumulator cleared, must have run on the same workspace).
 attn_status fused_impl(const void* q, const void* k, const void* v, const void* dout, void* workspace,
                        size_t workspace_bytes, void* dk, void* dv, int B, int H, int N, int Nk, int d, attn_dtype dt,
-                       int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{}) {
+                       int causal, float scale, int* dev_status, void* stream, const Dropout& dr = Dropout{},
+                       const uint32_t* keep_bits = nullptr) {
   if (d == 256) return ATTN_ERR_UNSUPPORTED;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {dout, qb}}, nullptr, {{dk, kb}, {dv, kb}}, workspace,
@@ -637,6 +663,8 @@ attn_status fused_impl(const void* q, const void* k, const void* v, const void* 
       !make_map(&a.tm_dk, dk, BH, Nk, d, bf16) || !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
     return ATTN_ERR_CUDA;
   fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
+  a.keep_bits = keep_bits;
+  a.bits_rows = a.Npad;
   a.dq_acc = dq_accumulator(workspace, B, H, N);
   if (!make_map_acc(&a.tm_dqacc, a.dq_acc, static_cast<int64_t>(BH) * a.Npad, d)) return ATTN_ERR_CUDA;
   if (attn::launch_bwd_fused(a, d, bf16, false, static_cast<cudaStream_t>(stream)) != cudaSuccess)
@@ -669,7 +697,7 @@ attn_status finish_impl(const void* workspace, size_t workspace_bytes, void* dq,
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
-                     const Dropout& dr = Dropout{}, bool deterministic = false) {
+                     const Dropout& dr = Dropout{}, bool deterministic = false, const uint32_t* keep_bits = nullptr) {
   if (!lse) return ATTN_ERR_INVALID_ARG;
   const size_t qb = qbytes(B, H, N, d), kb = qbytes(B, H, Nk, d);
   const size_t need = deterministic ? attn_bwd_deterministic_workspace_bytes(B, H, N, d)
@@ -683,7 +711,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if ((st = prepare_impl(o, dout, lse, workspace, prep_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
   if (fused) {
     if ((st = fused_impl(q, k, v, dout, workspace, workspace_bytes, dk, dv, B, H, N, Nk, d, dt, causal, scale,
-                         dev_status, stream, dr)) != ATTN_OK)
+                         dev_status, stream, dr, keep_bits)) != ATTN_OK)
       return st;
     return finish_impl(workspace, workspace_bytes, dq, B, H, N, d, dt, scale, stream);
   }
@@ -768,6 +796,23 @@ attn_status attn_bwd_dropout(const void* q, const void* k, const void* v, const 
   if (!dropout_from_p(p_drop, seed, &dr)) return ATTN_ERR_INVALID_ARG;
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
                   dev_status, stream, dr);
+}
+
+attn_status attn_bwd_dropout_bits(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                                  const float* lse, const void* keep_bits, size_t keep_bits_bytes, void* dq, void* dk,
+                                  void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                                  attn_dtype dt, int causal, float scale, float p_drop, int* dev_status,
+                                  void* stream) {
+  Dropout dr;
+  if (!dropout_from_p(p_drop, 0, &dr) || dr.t == 0) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_dropout_bits_bytes(B, H, N, N);
+  if (need == 0 || keep_bits_bytes < need || !aligned16(keep_bits)) return ATTN_ERR_INVALID_ARG;
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
+  const size_t qb = static_cast<size_t>(B) * H * N * d * 2;
+  for (const Buf& b : {Buf{dq, qb}, Buf{dk, qb}, Buf{dv, qb}, Buf{workspace, workspace_bytes}})
+    if (b.p && overlaps(b.p, b.bytes, keep_bits, need)) return ATTN_ERR_INVALID_ARG;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, N, d, dt, causal, scale,
+                  dev_status, stream, dr, false, static_cast<const uint32_t*>(keep_bits));
 }
 
 }  // extern "C"

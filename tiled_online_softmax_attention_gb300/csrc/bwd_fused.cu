@@ -28,8 +28,9 @@
 // DROP (dropout with the forward's keep mask, Z = keep * 256 / (256 - t)):
 //   dV = (P o Z)^T dO,  dS = P o (Z o dP - D)   (D = rowsum(dO o O) with the dropped-out O)
 // A thread owns a key and 32 queries, while one Philox call covers 16 keys of one query:
-// each lane draws one query's bits over the warp's 32 keys, and a warp transpose of the
-// 32 x 32 bit block hands every lane its key's bits over the 32 queries.
+// each lane draws one query's bits over the warp's 32 keys (or reads them, as one word,
+// from the keep bits the forward stored), and a warp transpose of the 32 x 32 bit block
+// hands every lane its key's bits over the 32 queries.
 #include <cuda_fp16.h>
 
 #include "bwd_common.cuh"
@@ -347,9 +348,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
         // lane L draws query qt*128 + 32h + L's bits over keys k0 + 32wq .. +31
         const uint32_t qi = static_cast<uint32_t>(qt * kTileM + kEwCols * h + lane);
         const uint32_t jg = static_cast<uint32_t>((k0 + 32 * wq) / 16);
-        const uint32_t mine =
-            dropout_keep16(jg, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) |
-            (dropout_keep16(jg + 1, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) << 16);
+        uint32_t mine;
+        if (a.keep_bits != nullptr)  // the forward's stored decisions (same bits, no draw)
+          mine = a.keep_bits[(static_cast<size_t>(bh) * n_tk + kt) * 4 * a.bits_rows +
+                             static_cast<size_t>(wq) * a.bits_rows + qi];
+        else
+          mine = dropout_keep16(jg, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) |
+                 (dropout_keep16(jg + 1, qi, static_cast<uint32_t>(bh), a.drop_t, a.seed_lo, a.seed_hi) << 16);
         keepbits = warp_transpose32(mine);
       }
       if (!(ok = mbar_wait_warp(bar(F_QFULL + s), (t / L::STAGES) & 1, wc))) break;

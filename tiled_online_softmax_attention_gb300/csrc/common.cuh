@@ -36,6 +36,11 @@ struct FwdArgs {
   uint32_t drop_t;
   uint32_t seed_lo, seed_hi;
   float drop_scale;                    // 256 / (256 - drop_t)
+  // dropout keep bits written by the forward (nullable; d <= 128, not packed): bit b of word
+  // ((bh * n_tk + j) * 4 + w) * bits_rows + i is the keep decision of query i and key
+  // 128 j + 32 w + b (n_tk key tiles, bits_rows = N rounded up to 128)
+  uint32_t* keep_bits;
+  int bits_rows;
   // variable-length packed sequences only: tensors [tokens][H][d] (maps over (d, H, tokens)),
   // sequence b = bh / H owns query tokens cu_q[b] .. cu_q[b+1]-1 and key tokens
   // cu_k[b] .. cu_k[b+1]-1; N and Nk are the longest lengths (grid size); lse is [H][Tq]
@@ -72,10 +77,12 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   uint64_t wait_limit_ns;
-  // dropout only, as in FwdArgs
+  // dropout only, as in FwdArgs (keep_bits: read by the fused kernel instead of drawing)
   uint32_t drop_t;
   uint32_t seed_lo, seed_hi;
   float drop_scale;
+  const uint32_t* keep_bits;
+  int bits_rows;
   // variable-length packed sequences only, as in FwdArgs (N, Nk: the longest lengths;
   // Npad: N rounded up; lse [H][Tq]; the workspace keeps [B*H][Npad])
   int H;

@@ -436,6 +436,22 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) keep[g][q] = __vcmpgeu4(w[q], tt);
         }
+        if (a.keep_bits != nullptr && grow < N_()) {
+          // The row's 128 decisions as four 32-key words for the backward: the top bit of
+          // each 0x00 / 0xFF byte of keep[g][q] gathered by one multiply (bits 7, 15, 23, 31
+          // land on 28..31 and nothing else reaches those bits).
+          uint32_t* kb = a.keep_bits + (static_cast<size_t>(bh) * n_tk + kv0 + j) * 4 * a.bits_rows + grow;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int gg = 0; gg < 2; ++gg)
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                word |= (((keep[2 * w + gg][q] & 0x80808080u) * 0x00204081u) >> 28) << (16 * gg + 4 * q);
+            kb[static_cast<size_t>(w) * a.bits_rows] = word;
+          }
+        }
       }
       if (!mbar_wait_warp(bar(B_SFULL + i), j & 1, wc)) { ok = false; break; }
       tc_fence_after();
