@@ -90,6 +90,8 @@ def test_fused_matches_deterministic(causal, d):
     assert_same_grads(g2, g1, "two fused calls:")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("N", [100, 300, 1000])
 def test_bwd_one_grid_equals_stages(N, d, causal):
     """attn_bwd_deterministic runs dK/dV and dQ as one grid; the stage entry points launch
