@@ -72,6 +72,8 @@ struct FwdLayout {
   static constexpr uint32_t TM_O = 256, TM_COLS = 512;
   static constexpr uint32_t tm_s(int i) { return 128u * i; }
   static constexpr uint32_t tm_o(int i) { return TM_O + D * i; }
+  // d = 64: the O tiles end at column 384, and S/P buffer 2 (see ROT) takes 384 .. 511
+  static constexpr uint32_t tm_sbuf(int b) { return b < 2 ? 128u * b : 384u; }
 };
 
 constexpr int kFwdThreads = 512;
@@ -96,6 +98,7 @@ enum : int {
   B_ODONE = 10,    // + tile: P_i V_j done (MMA commit)
   B_FIN = 12,      // + tile: final m, l published (softmax warpgroup)
   B_DRAIN = 14,
+  B_SFULL2 = 15,   // S/P buffer 2 computed (d = 64, ROT)
   B_KVFULL = 16,   // + slot
   B_KVEMPTY = 24,  // + slot
   B_COUNT = 32
@@ -123,6 +126,14 @@ enum : int {
 // merge_kernel combines the ranges with the two-block merge of the huaweicloud page's
 // section two.  With VARLEN too, the partials sit in the packed layout ([split][token]
 // [head]), and a degenerate sequence's ranges are all empty (lse = -inf).
+// ROT (d = 64, whole pairs): the two O tiles take only 128 tensor-memory columns, so S/P
+// has three 128-column buffers instead of one per tile.  S_i(j) goes to buffer
+// (2 j + i) mod 3; S_0(j+1) then lands in the buffer P_1(j-1) was read from and can be
+// issued before PV_0(j), and S_1(j+1) in the buffer of P_0(j), right after PV_0(j).  The
+// MMA order per key tile becomes S_0(j+1), PV_0(j), S_1(j+1), PV_1(j): a query tile's
+// next scores are ready when its softmax finishes the current tile, instead of waiting
+// for the current tile's P V and the next Q K^T (at d = 64 those products are short and
+// the chain S -> P -> PV -> S set the pace).
 // The CTA's body; PAD: its pair's second query tile lies wholly past the last query
 // (a sequence of an odd number of tiles, or a few queries against many keys), so only
 // tile 0 runs.  `a` is the kernel's __grid_constant__ parameter.
@@ -132,6 +143,14 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
   static_assert(!DROP || (!FP8 && !SPLIT), "dropout: 16-bit inputs, no split");
   static_assert(!VARLEN || !FP8, "packed sequences: 16-bit inputs");
   using L = FwdLayout<D, FP8>;
+  constexpr bool ROT = (D == 64) && !FP8 && !PAD;
+  // S/P buffer of query tile i at key step j, its completion barrier and the parity of
+  // its use (the number of earlier S products into the same buffer, mod 2)
+  auto sbuf = [](int i, int j) -> int { return ROT ? (2 * j + i) % 3 : i; };
+  auto sfull_bar = [](int b) -> int { return b < 2 ? B_SFULL + b : B_SFULL2; };
+  auto sfull_parity = [](int i, int j) -> uint32_t {
+    return ROT ? static_cast<uint32_t>(((2 * j + i) / 3) & 1) : static_cast<uint32_t>(j & 1);
+  };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -254,6 +273,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
       mbar_init(bar(B_FIN + i), kWgArrivals);
     }
     mbar_init(bar(B_DRAIN), 1);
+    if (ROT) mbar_init(bar(B_SFULL2), 1);
     for (int s = 0; s < L::NSLOT; ++s) {
       mbar_init(bar(B_KVFULL + s), 1);
       mbar_init(bar(B_KVEMPTY + s), 1);
@@ -322,10 +342,10 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
             mma_ss_f8(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
                       idesc_qk, k > 0 ? 1u : 0u);
           else
-            mma_ss(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+            mma_ss(tmem + L::tm_sbuf(sbuf(i, j)), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
                    idesc_qk, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(B_SFULL + i));
+        tc_commit(bar(sfull_bar(sbuf(i, j))));
       };
       auto issue_pv = [&](int i, int j) {
         const uint32_t vbase = sb + L::OFF_KV + ((2 * j + 1) % L::NSLOT) * L::TILE;
@@ -336,7 +356,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
             mma_ts_f8(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
                       sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
           else
-            mma_ts(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
+            mma_ts(tmem + L::tm_o(i), tmem + L::tm_sbuf(sbuf(i, j)) + k * 8,
                    sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
         tc_commit(bar(B_ODONE + i));
@@ -353,7 +373,33 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         if (has1) issue_s(1, 0);
         tc_commit(bar(B_KVEMPTY + 0));
       }
-      for (int j = 0; ok && j < n_steps; ++j) {
+      for (int j = 0; ROT && ok && j < n_steps; ++j) {
+        // S_0(j+1) | PV_0(j) | S_1(j+1) | PV_1(j)  (see ROT above)
+        const bool k_next = j + 1 < n_steps;  // K(j+1) is read by S_1(j+1) at least
+        if (k_next && !(ok = full(2 * j + 2))) break;
+        if (j + 1 < n_kv[0]) {
+          tc_fence_after();
+          issue_s(0, j + 1);
+        }
+        if (!(ok = full(2 * j + 1))) break;
+        if (j < n_kv[0]) {
+          if (!(ok = mbar_wait(bar(B_PFULL + 0), j & 1, wc) && (j == 0 || mbar_wait(bar(B_CORR + 0), (j - 1) & 1, wc))))
+            break;
+          tc_fence_after();
+          issue_pv(0, j);
+        }
+        if (k_next) {
+          tc_fence_after();
+          issue_s(1, j + 1);
+          tc_commit(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
+        }
+        if (!(ok = mbar_wait(bar(B_PFULL + 1), j & 1, wc) && (j == 0 || mbar_wait(bar(B_CORR + 1), (j - 1) & 1, wc))))
+          break;
+        tc_fence_after();
+        issue_pv(1, j);
+        tc_commit(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
+      }
+      for (int j = 0; !ROT && ok && j < n_steps; ++j) {
         bool v_ready = false, k_next_ready = false;
         if (j < n_kv[0]) {
           if (!(ok = full(2 * j + 1) && mbar_wait(bar(B_PFULL + 0), j & 1, wc) &&
@@ -397,7 +443,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const int grow = (2 * pr + i) * kTileM + row;
-    const uint32_t t_s = tmem + (static_cast<uint32_t>(wq * 32) << 16) + L::tm_s(i);
+    const uint32_t t_lane_s = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     float sl2 = a.scale_log2;
     float m = -INFINITY;  // reference max (scale*log2(e) units) used by the exponentials
     float l = 0.f;        // row sum of ex2(. - m)
@@ -453,8 +499,9 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
           }
         }
       }
-      if (!mbar_wait_warp(bar(B_SFULL + i), j & 1, wc)) { ok = false; break; }
+      if (!mbar_wait_warp(bar(sfull_bar(sbuf(i, j))), sfull_parity(i, j), wc)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t t_s = t_lane_s + L::tm_sbuf(sbuf(i, j));
       float s[128];
       {
         // Four loads in flight, one wait: a TMEM load issued while the tensor core
