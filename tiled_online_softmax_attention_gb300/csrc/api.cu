@@ -36,6 +36,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
+// Which kernel runs the d = 128 forward without dropout: the CTA-pair kernel (fwd_pair.cu)
+// when a query tile visits many key tiles on average (Nk / 128, halved under the causal
+// mask, at least 48), else the one-CTA kernel.  The pair kernel's deeper pipeline wins on
+// long rows (B=1, H=32, N=16384: 1476 against 1362 TFLOP/s), its twice as many CTAs with
+// their own start-up and epilogue lose on short ones (B=2, H=16, N=4096 causal: 855
+// against 910; N=8192 causal: even).  ATTN_FWD_CTA_PAIR=1 or =0 (read on every call)
+// forces one or the other.
+bool fwd_use_pair(int Nk, int causal) {
+  const char* s = std::getenv("ATTN_FWD_CTA_PAIR");
+  if (s && (s[0] == '0' || s[0] == '1') && s[1] == 0) return s[0] == '1';
+  const int tiles = (Nk + attn::kTileN - 1) / attn::kTileN;
+  return (causal ? tiles / 2 : tiles) >= 48;
+}
+
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* s = std::getenv("ATTN_WAIT_LIMIT_NS");
@@ -46,14 +60,15 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-// 3-D map over a [BH][N][d] 16-bit tensor: box {64, 128, 1}, 128-byte swizzle,
-// out-of-range rows read as zero and are dropped on store.
-bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16) {
+// 3-D map over a [BH][N][d] 16-bit tensor: box {64, rows, 1} (rows = 128 but for the
+// pair forward's half key tiles), 128-byte swizzle, out-of-range rows read as zero and
+// are dropped on store.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d, bool bf16, int rows = kTileM) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTileM), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -226,8 +241,11 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   set_dropout(a, dr);
   a.keep_bits = keep_bits;
   a.bits_rows = static_cast<int>((static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM);
+  const bool pair = d == 128 && dr.t == 0 && fwd_use_pair(Nk, causal);
+  if (pair && !make_map(&a.tm_kh, k, BH, Nk, d, bf16, 64)) return ATTN_ERR_CUDA;
   const cudaError_t e = d == 256  ? attn::launch_fwd256(a, bf16, static_cast<cudaStream_t>(stream))
                         : dr.t > 0 ? attn::launch_fwd_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
+                        : pair     ? attn::launch_fwd_pair(a, bf16, static_cast<cudaStream_t>(stream))
                                    : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;

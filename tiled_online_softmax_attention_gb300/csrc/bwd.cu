@@ -270,61 +270,60 @@ __device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
         mbar_wait(bar(K_QFULL + t % L::STAGES), (t / L::STAGES) & 1, wc);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
-      constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // TMEM x MN-major
-      // S^T of the next query tile goes between dV and dK: S^T(t+1) overwrites P^T(t),
-      // which dV(t) (issued before it) reads, and the element-wise warps keep P(t) in
-      // registers for dS^T(t).  So the P^T work of a tile overlaps dK(t-1) and dP^T(t),
-      // and the dS^T work overlaps dV(t) and S^T(t+1): two products each instead of one.
-      auto issue_st = [&](int t) {
-        const uint32_t st = stage_base(t % L::STAGES);
+    // The whole warp runs the issuing loop; one elected lane issues each product.
+    constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
+    constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // TMEM x MN-major
+    // S^T of the next query tile goes between dV and dK: S^T(t+1) overwrites P^T(t),
+    // which dV(t) (issued before it) reads, and the element-wise warps keep P(t) in
+    // registers for dS^T(t).  So the P^T work of a tile overlaps dK(t-1) and dP^T(t),
+    // and the dS^T work overlaps dV(t) and S^T(t+1): two products each instead of one.
+    auto issue_st = [&](int t) {
+      const uint32_t st = stage_base(t % L::STAGES);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024), sdesc_sw128(st + L::S_Q + off, 16, 1024),
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+        mma_ss_w(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024), sdesc_sw128(st + L::S_Q + off, 16, 1024),
                  idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(K_SFULL));
-      };
-      bool ok = mbar_wait(bar(K_KVFULL), 0, wc);
-      if (ok && n_iter > 0 && (ok = mbar_wait(bar(K_QFULL + 0), 0, wc))) {
-        tc_fence_after();
-        issue_st(0);
       }
-      for (int t = 0; ok && t < n_iter; ++t) {
-        const int s = t % L::STAGES;
-        const uint32_t st = stage_base(s);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
-                 sdesc_sw128(st + L::S_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(K_DPFULL));
-        if (!(ok = mbar_wait(bar(K_PREADY), t & 1, wc))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
-          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
-                 sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
-        if (t + 1 < n_iter) {
-          if (!(ok = mbar_wait(bar(K_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
-          tc_fence_after();
-          issue_st(t + 1);
-        }
-        if (!(ok = mbar_wait(bar(K_DSREADY), t & 1, wc))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k)
-          mma_ts(tmem + L::TM_DK, tmem + L::TM_DP + kEwCols * (k >> 1) + 8 * (k & 1),
-                 sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
-        tc_commit(bar(K_EMPTY + s));
-      }
-      if (ok) tc_commit(bar(K_DONE));
-      tc_commit(bar(K_DRAIN));
-      mbar_wait(bar(K_DRAIN), 0, wc);
+      tc_commit_w(bar(K_SFULL));
+    };
+    bool ok = mbar_wait_warp(bar(K_KVFULL), 0, wc);
+    if (ok && n_iter > 0 && (ok = mbar_wait_warp(bar(K_QFULL + 0), 0, wc))) {
+      tc_fence_after();
+      issue_st(0);
     }
+    for (int t = 0; ok && t < n_iter; ++t) {
+      const int s = t % L::STAGES;
+      const uint32_t st = stage_base(s);
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+        mma_ss_w(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
+                 sdesc_sw128(st + L::S_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+      }
+      tc_commit_w(bar(K_DPFULL));
+      if (!(ok = mbar_wait_warp(bar(K_PREADY), t & 1, wc))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
+        mma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
+                 sdesc_sw128(st + L::S_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+      if (t + 1 < n_iter) {
+        if (!(ok = mbar_wait_warp(bar(K_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
+        tc_fence_after();
+        issue_st(t + 1);
+      }
+      if (!(ok = mbar_wait_warp(bar(K_DSREADY), t & 1, wc))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kTileM / 16; ++k)
+        mma_ts_w(tmem + L::TM_DK, tmem + L::TM_DP + kEwCols * (k >> 1) + 8 * (k & 1),
+                 sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+      tc_commit_w(bar(K_EMPTY + s));
+    }
+    if (ok) tc_commit_w(bar(K_DONE));
+    tc_commit_w(bar(K_DRAIN));
+    mbar_wait_warp(bar(K_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1;      // this warpgroup's 32 query columns of every tile
     const int wq = warp & 3;
@@ -636,66 +635,65 @@ __device__ __forceinline__ void dq_body(const BwdArgs& a, int block) {
         mbar_wait(bar(Q_VFULL + j % L::VST), (j / L::VST) & 1, wc);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);
-      constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);
-      auto k_full = [&](int j) { return mbar_wait(bar(Q_KFULL + j % L::KST), (j / L::KST) & 1, wc); };
-      auto v_full = [&](int j) { return mbar_wait(bar(Q_VFULL + j % L::VST), (j / L::VST) & 1, wc); };
-      auto issue_s = [&](int j) {  // S = Q K^T, Q from tensor memory (16 elements = 8 columns per step)
-        const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
+    // The whole warp runs the issuing loop; one elected lane issues each product.
+    constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);
+    constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);
+    auto k_full = [&](int j) { return mbar_wait_warp(bar(Q_KFULL + j % L::KST), (j / L::KST) & 1, wc); };
+    auto v_full = [&](int j) { return mbar_wait_warp(bar(Q_VFULL + j % L::VST), (j / L::VST) & 1, wc); };
+    auto issue_s = [&](int j) {  // S = Q K^T, Q from tensor memory (16 elements = 8 columns per step)
+      const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ts(tmem + L::TM_S, tmem + L::TM_Q + 8 * k, sdesc_sw128(kbase + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(Q_SFULL));
-      };
-      auto issue_dp = [&](int j) {  // dP = dO V^T, dO from tensor memory
-        const uint32_t vbase = sb + L::OFF_V + (j % L::VST) * T::TILE;
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+        mma_ts_w(tmem + L::TM_S, tmem + L::TM_Q + 8 * k, sdesc_sw128(kbase + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+      }
+      tc_commit_w(bar(Q_SFULL));
+    };
+    auto issue_dp = [&](int j) {  // dP = dO V^T, dO from tensor memory
+      const uint32_t vbase = sb + L::OFF_V + (j % L::VST) * T::TILE;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ts(tmem + L::TM_DP, tmem + L::TM_DO + 8 * k, sdesc_sw128(vbase + off, 16, 1024), idesc_s,
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+        mma_ts_w(tmem + L::TM_DP, tmem + L::TM_DO + 8 * k, sdesc_sw128(vbase + off, 16, 1024), idesc_s,
                  k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(Q_DPFULL));
-        tc_commit(bar(Q_VEMPTY + j % L::VST));
-      };
-      bool ok = mbar_wait(bar(Q_QTM), 0, wc) && k_full(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        ok = v_full(0);
       }
-      if (ok) {
-        tc_fence_after();
-        issue_dp(0);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          // The next S may overwrite S(j) once both warpgroups have read it.
-          if (!(ok = k_full(j + 1) && mbar_wait(bar(Q_SCONS), j & 1, wc))) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        if (!(ok = mbar_wait(bar(Q_DSREADY), j & 1, wc))) break;
-        tc_fence_after();
-        const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
-#pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of warpgroup w's keys at dP + 32w
-          mma_ts(tmem + L::TM_DQ, tmem + L::TM_DP + kEwCols * (k >> 1) + 8 * (k & 1),
-                 sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g, (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit(bar(Q_KEMPTY + j % L::KST));
-        if (j + 1 < n_kv) {  // dP(j) was read before dS(j) was published
-          if (!(ok = v_full(j + 1))) break;
-          tc_fence_after();
-          issue_dp(j + 1);
-        }
-      }
-      if (ok) tc_commit(bar(Q_DONE));
-      tc_commit(bar(Q_DRAIN));
-      mbar_wait(bar(Q_DRAIN), 0, wc);
+      tc_commit_w(bar(Q_DPFULL));
+      tc_commit_w(bar(Q_VEMPTY + j % L::VST));
+    };
+    bool ok = mbar_wait_warp(bar(Q_QTM), 0, wc) && k_full(0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      ok = v_full(0);
     }
+    if (ok) {
+      tc_fence_after();
+      issue_dp(0);
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      if (j + 1 < n_kv) {
+        // The next S may overwrite S(j) once both warpgroups have read it.
+        if (!(ok = k_full(j + 1) && mbar_wait_warp(bar(Q_SCONS), j & 1, wc))) break;
+        tc_fence_after();
+        issue_s(j + 1);
+      }
+      if (!(ok = mbar_wait_warp(bar(Q_DSREADY), j & 1, wc))) break;
+      tc_fence_after();
+      const uint32_t kbase = sb + L::OFF_K + (j % L::KST) * T::TILE;
+#pragma unroll
+      for (int k = 0; k < kTileN / 16; ++k)  // 16-key steps; dS of warpgroup w's keys at dP + 32w
+        mma_ts_w(tmem + L::TM_DQ, tmem + L::TM_DP + kEwCols * (k >> 1) + 8 * (k & 1),
+                 sdesc_sw128(kbase + k * 2048, T::BLK, 1024), idesc_g, (j > 0 || k > 0) ? 1u : 0u);
+      tc_commit_w(bar(Q_KEMPTY + j % L::KST));
+      if (j + 1 < n_kv) {  // dP(j) was read before dS(j) was published
+        if (!(ok = v_full(j + 1))) break;
+        tc_fence_after();
+        issue_dp(j + 1);
+      }
+    }
+    if (ok) tc_commit_w(bar(Q_DONE));
+    tc_commit_w(bar(Q_DRAIN));
+    mbar_wait_warp(bar(Q_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1;  // this warpgroup's 32 key columns of every tile
     const int wq = warp & 3;

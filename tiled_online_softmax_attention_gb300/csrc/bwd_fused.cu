@@ -247,72 +247,71 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_fused_kernel(const __grid_
       if (do_issued > 0) mbar_wait(bar(F_DOFULL), (do_issued - 1) & 1, wc);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
-      constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // K-major A x MN-major B
-      constexpr uint32_t idesc_q = idesc_f16(kTileM, D, BF16, true, true);         // MN-major A x MN-major B
-      const uint32_t ds = sb + L::OFF_DS;
-      auto issue_st = [&](int t) {
-        const uint32_t st = stage_base(t % L::STAGES);
+    // The whole warp runs the issuing loop; one elected lane issues each product.
+    constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);  // K-major x K-major
+    constexpr uint32_t idesc_g = idesc_f16(kTileM, D, BF16, false, true);        // K-major A x MN-major B
+    constexpr uint32_t idesc_q = idesc_f16(kTileM, D, BF16, true, true);         // MN-major A x MN-major B
+    const uint32_t ds = sb + L::OFF_DS;
+    auto issue_st = [&](int t) {
+      const uint32_t st = stage_base(t % L::STAGES);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024), sdesc_sw128(st + L::S_Q + off, 16, 1024),
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+        mma_ss_w(tmem + L::TM_S, sdesc_sw128(sb + L::OFF_K + off, 16, 1024), sdesc_sw128(st + L::S_Q + off, 16, 1024),
                  idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(F_SFULL));
-      };
-      bool ok = mbar_wait(bar(F_KVFULL), 0, wc);
-      if (ok && n_iter > 0 && (ok = mbar_wait(bar(F_QFULL + 0), 0, wc))) {
-        tc_fence_after();
-        issue_st(0);
       }
-      for (int t = 0; ok && t < n_iter; ++t) {
-        const int s = t % L::STAGES;
-        const uint32_t st = stage_base(s);
-        if (!(ok = mbar_wait(bar(F_PREADY), t & 1, wc) && mbar_wait(bar(F_DOFULL), t & 1, wc))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
-          mma_ts(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
-                 sdesc_sw128(sb + L::OFF_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
-        // dP^T(t) takes dQ(t-1)'s columns once the element-wise warps have read them; dK(t-1)
-        // and dV(t) run meanwhile.
-        if (t > 0 && !(ok = mbar_wait(bar(F_DQFREE), (t - 1) & 1, wc))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
-          mma_ss(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
-                 sdesc_sw128(sb + L::OFF_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
-        }
-        tc_commit(bar(F_DPFULL));
-        tc_commit(bar(F_DOFREE));
-        if (t + 1 < n_iter) {  // S^T(t+1) over P^T(t): issued after dV(t), which reads it
-          if (!(ok = mbar_wait(bar(F_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
-          tc_fence_after();
-          issue_st(t + 1);
-        }
-        if (!(ok = mbar_wait(bar(F_DSREADY), t & 1, wc))) break;
-        tc_fence_after();
-        // dQ(t) = dS K: A = dS read MN-major from the [key][query] tile (16-key steps of
-        // 16 rows), B = K MN-major (d contiguous).
-#pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)
-          mma_ss(tmem + L::TM_DQ, sdesc_sw128(ds + k * 2048, T::BLK, 1024),
-                 sdesc_sw128(sb + L::OFF_K + k * 2048, T::BLK, 1024), idesc_q, k > 0 ? 1u : 0u);
-        tc_commit(bar(F_DQFULL));
-        // dK += dS^T Q: A = dS^T read K-major from the same tile (16-query steps).
-#pragma unroll
-        for (int k = 0; k < kTileM / 16; ++k)
-          mma_ss(tmem + L::TM_DK, sdesc_sw128(ds + (k >> 2) * T::BLK + (k & 3) * 32, 16, 1024),
-                 sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
-        tc_commit(bar(F_EMPTY + s));
-      }
-      if (ok) tc_commit(bar(F_DONE));
-      tc_commit(bar(F_DRAIN));
-      mbar_wait(bar(F_DRAIN), 0, wc);
+      tc_commit_w(bar(F_SFULL));
+    };
+    bool ok = mbar_wait_warp(bar(F_KVFULL), 0, wc);
+    if (ok && n_iter > 0 && (ok = mbar_wait_warp(bar(F_QFULL + 0), 0, wc))) {
+      tc_fence_after();
+      issue_st(0);
     }
+    for (int t = 0; ok && t < n_iter; ++t) {
+      const int s = t % L::STAGES;
+      const uint32_t st = stage_base(s);
+      if (!(ok = mbar_wait_warp(bar(F_PREADY), t & 1, wc) && mbar_wait_warp(bar(F_DOFULL), t & 1, wc))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < kTileM / 16; ++k)  // 16-query steps; P^T of warpgroup w at S^T + 32w
+        mma_ts_w(tmem + L::TM_DV, tmem + L::TM_S + kEwCols * (k >> 1) + 8 * (k & 1),
+                 sdesc_sw128(sb + L::OFF_DO + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+      // dP^T(t) takes dQ(t-1)'s columns once the element-wise warps have read them; dK(t-1)
+      // and dV(t) run meanwhile.
+      if (t > 0 && !(ok = mbar_wait_warp(bar(F_DQFREE), (t - 1) & 1, wc))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
+        mma_ss_w(tmem + L::TM_DP, sdesc_sw128(sb + L::OFF_V + off, 16, 1024),
+                 sdesc_sw128(sb + L::OFF_DO + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+      }
+      tc_commit_w(bar(F_DPFULL));
+      tc_commit_w(bar(F_DOFREE));
+      if (t + 1 < n_iter) {  // S^T(t+1) over P^T(t): issued after dV(t), which reads it
+        if (!(ok = mbar_wait_warp(bar(F_QFULL + (t + 1) % L::STAGES), ((t + 1) / L::STAGES) & 1, wc))) break;
+        tc_fence_after();
+        issue_st(t + 1);
+      }
+      if (!(ok = mbar_wait_warp(bar(F_DSREADY), t & 1, wc))) break;
+      tc_fence_after();
+      // dQ(t) = dS K: A = dS read MN-major from the [key][query] tile (16-key steps of
+      // 16 rows), B = K MN-major (d contiguous).
+#pragma unroll
+      for (int k = 0; k < kTileN / 16; ++k)
+        mma_ss_w(tmem + L::TM_DQ, sdesc_sw128(ds + k * 2048, T::BLK, 1024),
+                 sdesc_sw128(sb + L::OFF_K + k * 2048, T::BLK, 1024), idesc_q, k > 0 ? 1u : 0u);
+      tc_commit_w(bar(F_DQFULL));
+      // dK += dS^T Q: A = dS^T read K-major from the same tile (16-query steps).
+#pragma unroll
+      for (int k = 0; k < kTileM / 16; ++k)
+        mma_ss_w(tmem + L::TM_DK, sdesc_sw128(ds + (k >> 2) * T::BLK + (k & 3) * 32, 16, 1024),
+                 sdesc_sw128(st + L::S_Q + k * 2048, T::BLK, 1024), idesc_g, (t > 0 || k > 0) ? 1u : 0u);
+      tc_commit_w(bar(F_EMPTY + s));
+    }
+    if (ok) tc_commit_w(bar(F_DONE));
+    tc_commit_w(bar(F_DRAIN));
+    mbar_wait_warp(bar(F_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1;   // this warpgroup's 32 query columns of every tile
     const int wq = warp & 3;

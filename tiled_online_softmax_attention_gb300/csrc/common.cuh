@@ -13,6 +13,7 @@ constexpr int kTileN = 128;
 
 struct FwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;  // 3-D maps over [B*H][N][d], 128-byte boxes x 128 rows, 128B swizzle
+  CUtensorMap tm_kh;                   // the pair kernel (fwd_pair.cu): K with 64-row boxes (half a key tile)
   void* o;                             // [B*H][N][d] output (the merge kernel writes it directly)
   float* lse;                          // [B*H][N]
   int* dev_status;                     // nullable
@@ -151,6 +152,8 @@ __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
 
 // Launchers (fwd.cu / bwd.cu); return the CUDA launch status.
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
+// d = 128 on CTA pairs (fwd_pair.cu); needs tm_kh; not split, E4M3, dropout or packed
+cudaError_t launch_fwd_pair(const FwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_varlen_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);  // packed batches
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);

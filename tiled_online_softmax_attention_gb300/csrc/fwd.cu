@@ -32,7 +32,8 @@
 //
 // Warp roles (512 threads, four warpgroups):
 //   warpgroup 0  warp 0 TMA producer (Q0, Q1 once; then K_j, V_j into a ring),
-//                warp 1 TMEM owner and MMA issuer (one elected lane)
+//                warp 1 TMEM owner and MMA issuer (the warp runs the loop, one elected
+//                lane issues each product)
 //   warpgroup 1  softmax of query tile 0 (thread r owns row r = TMEM lane r)
 //   warpgroup 2  softmax of query tile 1
 //   warpgroup 3  correction (O rescale when a reference max moves) and the
@@ -325,12 +326,13 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
       mbar_wait(bar(B_Q + 1), 0, wc);
       for (int ld = (issued > L::NSLOT ? issued - L::NSLOT : 0); ld < issued; ++ld)
         mbar_wait(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc);
-    } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer (the whole
+      // warp runs it, one elected lane issues)
       constexpr uint32_t idesc_qk =
           FP8 ? idesc_e4m3(kTileM, kTileN, false, false) : idesc_f16(kTileM, kTileN, BF16, false, false);
       constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3(kTileM, D, false, true) : idesc_f16(kTileM, D, BF16, false, true);
-      auto full = [&](int ld) { return mbar_wait(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc); };
+      auto full = [&](int ld) { return mbar_wait_warp(bar(B_KVFULL + ld % L::NSLOT), (ld / L::NSLOT) & 1, wc); };
       auto issue_s = [&](int i, int j) {
         const uint32_t qb = sb + L::OFF_Q + i * L::OTILE;
         const uint32_t kbase = sb + L::OFF_KV + ((2 * j) % L::NSLOT) * L::TILE;
@@ -339,13 +341,13 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         for (int k = 0; k < D * L::ELEM / 32; ++k) {
           const uint32_t off = (k >> 2) * L::BLK + (k & 3) * 32;
           if constexpr (FP8)
-            mma_ss_f8(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                      idesc_qk, k > 0 ? 1u : 0u);
+            mma_ss_f8_w(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                        idesc_qk, k > 0 ? 1u : 0u);
           else
-            mma_ss(tmem + L::tm_sbuf(sbuf(i, j)), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                   idesc_qk, k > 0 ? 1u : 0u);
+            mma_ss_w(tmem + L::tm_sbuf(sbuf(i, j)), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                     idesc_qk, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(sfull_bar(sbuf(i, j))));
+        tc_commit_w(bar(sfull_bar(sbuf(i, j))));
       };
       auto issue_pv = [&](int i, int j) {
         const uint32_t vbase = sb + L::OFF_KV + ((2 * j + 1) % L::NSLOT) * L::TILE;
@@ -353,25 +355,25 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
 #pragma unroll
         for (int k = 0; k < kTileN * L::ELEM / 32; ++k) {
           if constexpr (FP8)
-            mma_ts_f8(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
-                      sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+            mma_ts_f8_w(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
+                        sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
           else
-            mma_ts(tmem + L::tm_o(i), tmem + L::tm_sbuf(sbuf(i, j)) + k * 8,
-                   sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+            mma_ts_w(tmem + L::tm_o(i), tmem + L::tm_sbuf(sbuf(i, j)) + k * 8,
+                     sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(bar(B_ODONE + i));
+        tc_commit_w(bar(B_ODONE + i));
       };
       constexpr bool has1 = !PAD;
-      bool ok = mbar_wait(bar(B_Q + 0), 0, wc) && full(0);
+      bool ok = mbar_wait_warp(bar(B_Q + 0), 0, wc) && full(0);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
-        ok = mbar_wait(bar(B_Q + 1), 0, wc);
+        ok = mbar_wait_warp(bar(B_Q + 1), 0, wc);
       }
       if (ok) {
         tc_fence_after();
         if (has1) issue_s(1, 0);
-        tc_commit(bar(B_KVEMPTY + 0));
+        tc_commit_w(bar(B_KVEMPTY + 0));
       }
       for (int j = 0; ROT && ok && j < n_steps; ++j) {
         // S_0(j+1) | PV_0(j) | S_1(j+1) | PV_1(j)  (see ROT above)
@@ -383,7 +385,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         }
         if (!(ok = full(2 * j + 1))) break;
         if (j < n_kv[0]) {
-          if (!(ok = mbar_wait(bar(B_PFULL + 0), j & 1, wc) && (j == 0 || mbar_wait(bar(B_CORR + 0), (j - 1) & 1, wc))))
+          if (!(ok = mbar_wait_warp(bar(B_PFULL + 0), j & 1, wc) && (j == 0 || mbar_wait_warp(bar(B_CORR + 0), (j - 1) & 1, wc))))
             break;
           tc_fence_after();
           issue_pv(0, j);
@@ -391,19 +393,19 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         if (k_next) {
           tc_fence_after();
           issue_s(1, j + 1);
-          tc_commit(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
+          tc_commit_w(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
         }
-        if (!(ok = mbar_wait(bar(B_PFULL + 1), j & 1, wc) && (j == 0 || mbar_wait(bar(B_CORR + 1), (j - 1) & 1, wc))))
+        if (!(ok = mbar_wait_warp(bar(B_PFULL + 1), j & 1, wc) && (j == 0 || mbar_wait_warp(bar(B_CORR + 1), (j - 1) & 1, wc))))
           break;
         tc_fence_after();
         issue_pv(1, j);
-        tc_commit(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
+        tc_commit_w(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
       }
       for (int j = 0; !ROT && ok && j < n_steps; ++j) {
         bool v_ready = false, k_next_ready = false;
         if (j < n_kv[0]) {
-          if (!(ok = full(2 * j + 1) && mbar_wait(bar(B_PFULL + 0), j & 1, wc) &&
-                     (j == 0 || mbar_wait(bar(B_CORR + 0), (j - 1) & 1, wc))))
+          if (!(ok = full(2 * j + 1) && mbar_wait_warp(bar(B_PFULL + 0), j & 1, wc) &&
+                     (j == 0 || mbar_wait_warp(bar(B_CORR + 0), (j - 1) & 1, wc))))
             break;
           v_ready = true;
           tc_fence_after();
@@ -416,25 +418,25 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
           }
         }
         if (has1) {
-          if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait(bar(B_PFULL + 1), j & 1, wc) &&
-                     (j == 0 || mbar_wait(bar(B_CORR + 1), (j - 1) & 1, wc))))
+          if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait_warp(bar(B_PFULL + 1), j & 1, wc) &&
+                     (j == 0 || mbar_wait_warp(bar(B_CORR + 1), (j - 1) & 1, wc))))
             break;
           tc_fence_after();
           issue_pv(1, j);
         }
-        tc_commit(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
+        tc_commit_w(bar(B_KVEMPTY + (2 * j + 1) % L::NSLOT));
         if (j + 1 < n_steps) {
           if (has1) {  // (without tile 1, tile 0's S(j+1) above was the slot's last use)
             if (!(ok = k_next_ready || full(2 * j + 2))) break;
             tc_fence_after();
             issue_s(1, j + 1);
           }
-          tc_commit(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
+          tc_commit_w(bar(B_KVEMPTY + (2 * j + 2) % L::NSLOT));
         }
       }
       // Drain: nothing may still write tensor memory when it is released.
-      tc_commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0, wc);
+      tc_commit_w(bar(B_DRAIN));
+      mbar_wait_warp(bar(B_DRAIN), 0, wc);
     }
   } else if (wg <= 2) {
     // ------------------------------------------------------------ softmax of tile i

@@ -258,6 +258,125 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// True in exactly one lane of the (fully converged) warp.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "+r"(pred));
+  return pred != 0;
+}
+
+// ---------------------------------------------------------------- CTA pairs
+// Two CTAs of a cluster on neighbouring SMs that share tcgen05 products
+// (cta_group::2): one thread of the even CTA issues M = 256 products whose A rows,
+// B columns and accumulators are split between the two CTAs' shared and tensor memory.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(addr), "r"(rank));
+  return d;
+}
+
+// Every thread of every CTA of the cluster; orders earlier memory operations (and
+// barrier initialisation) before anything after it in any CTA.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster (address from mapa_shared).  The default
+// (CTA-scope) release: a hand-off of tensor-memory data is ordered by tcgen05.wait::st and
+// the before_thread_sync fence ahead of it, and the cluster-scope release form measured
+// 1000-1500 cycles per arrival on this GPU (it waits for the thread's earlier memory
+// operations to become visible to the whole cluster), against ~100 for this one.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
+// Like mbar_try_wait, acquiring at cluster scope (the phase may have been completed by
+// the partner CTA's arrivals or copies).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t caddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(caddr), "r"(v) : "memory");
+}
+
+// 3-D tiled load into this CTA's shared memory whose completion is counted on an
+// mbarrier of either CTA of the pair (`cbar`, a cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* m, uint32_t cbar, int c0, int c1,
+                                                 int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(cbar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Tensor-memory allocation for pair products: one warp of each CTA of the pair executes
+// it, and both CTAs receive the same columns.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (+)= A[smem] * B[smem]^T over the pair: rows 0-127 of A and D in the issuing CTA,
+// 128-255 in its partner; B's first N/2 rows from the issuing CTA, the rest from the
+// partner (the descriptors name the same offsets in both).
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D (+)= A[tmem] * B[smem]^T over the pair, A's rows split like D's.
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the mbarrier at offset `bar` in each CTA of `cta_mask` when every pair
+// product this thread issued so far is done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- math
 
 __device__ __forceinline__ float ex2(float x) {
@@ -518,6 +637,37 @@ __device__ __forceinline__ void setmaxnreg_inc() {
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------- warp-issued forms
+// Products and commits issued by one elected lane of a converged warp.  The whole warp
+// runs the issuing code, so the descriptors are warp-uniform values that the compiler
+// keeps in uniform registers; issued from a lane-0-only branch instead, each product took
+// about 100 cycles to leave the SM sub-partition while the softmax warp beside it was
+// busy, where the tensor core needs 64 (measured on this GPU).
+__device__ __forceinline__ void mma_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (elect_one_sync()) mma_ss(d, a, b, id, acc);
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (elect_one_sync()) mma_ts(d, a, b, id, acc);
+}
+__device__ __forceinline__ void mma_ss_f8_w(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (elect_one_sync()) mma_ss_f8(d, a, b, id, acc);
+}
+__device__ __forceinline__ void mma_ts_f8_w(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (elect_one_sync()) mma_ts_f8(d, a, b, id, acc);
+}
+__device__ __forceinline__ void tc_commit_w(uint32_t bar) {
+  if (elect_one_sync()) tc_commit(bar);
+}
+__device__ __forceinline__ void mma_ss_pair_w(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (elect_one_sync()) mma_ss_pair(d, a, b, id, acc);
+}
+__device__ __forceinline__ void mma_ts_pair_w(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  if (elect_one_sync()) mma_ts_pair(d, a, b, id, acc);
+}
+__device__ __forceinline__ void tc_commit_pair_w(uint32_t bar, uint16_t cta_mask) {
+  if (elect_one_sync()) tc_commit_pair(bar, cta_mask);
 }
 
 }  // namespace attn
