@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-extra", action="store_true", help="skip the long-sequence forward side numbers")
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    p.add_argument("--forward", metavar="WORKLOAD[:causal]",
+                   help="time only attn_fwd on one named workload (c1..c5) for a kernel capture, then exit")
     return p.parse_args()
 
 
@@ -928,8 +930,44 @@ def allreduce_max(val: float, ws_, dev):
     return val
 
 
+def forward_only(args):
+    """attn_fwd alone on one named workload, --warmup untimed and --steps timed calls: the
+    command the single-kernel captures of the forward run (a JSON line with the time)."""
+    import tiled_online_softmax_attention_gb300 as api
+
+    name, _, mask = args.forward.partition(":")
+    w = workloads.WORKLOADS[name]
+    causal = mask == "causal"
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    api.load(build_if_missing=True)
+    x = workloads.inputs(name)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), device=dev, dtype=torch.float32)
+    status = torch.zeros(1, device=dev, dtype=torch.int32)
+    call = lambda: api.attn_fwd(q, k, v, o, lse, w.B, w.H, w.N, w.d, q.dtype, causal, w.scale, status)
+    for _ in range(args.warmup):
+        assert call() == 0
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / max(args.steps, 1)
+    f = workloads.fwd_flops(w.B, w.H, w.N, w.d, causal)
+    print(json.dumps({"forward": args.forward, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+                      "ms": round(ms, 4), "tflops": round(f / (ms * 1e-3) / 1e12, 1), "status": int(status.item())}),
+          flush=True)
+
+
 def main():
     args = parse()
+    if args.forward:
+        forward_only(args)
+        return
     ws_, rank, local = dist_env()
     w = workloads.WORKLOADS[WORKLOAD]
     if args.impl == "reference":

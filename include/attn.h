@@ -166,7 +166,10 @@ ATTN_API attn_status attn_bwd_dropout(const void *q, const void *k, const void *
  * with the keep decisions drawn once: the forward also stores every decision it draws
  * into keep_bits, and the backward reads them there instead of drawing them again (the
  * same decisions, so the results equal the drawing path's: O and lse byte for byte, dK
- * and dV byte for byte, dQ up to the order of its float32 additions).
+ * and dV byte for byte, dQ up to the order of the drawing path's float32 additions).
+ * With the decisions stored, drawing them twice costs nothing, so the backward runs the
+ * two deterministic kernels of attn_bwd (which read the bits), not the fused pass: the
+ * same speed on GB300, and the same dQ bytes on every call.
  *   keep_bits      : device buffer of at least attn_dropout_bits_bytes(B, H, N, N) bytes,
  *                    16-byte aligned, owned by the caller; written by the forward, read
  *                    by the backward (which needs the forward's q, k, v, p and seed).
@@ -343,8 +346,8 @@ ATTN_API size_t attn_bwd_deterministic_workspace_bytes(int B, int H, int N, int 
  *   d in {64, 128}: two kernels, dK and dV over 128-key tiles and dQ over 128-query tiles
  *   (the second recomputes S and dP in its own tile order: seven N x N x d products per
  *   tile pair, no atomics, the same bytes on every call), launched as one grid.  With
- *   dropout (attn_bwd_dropout and its variants) the fused pass of attn_bwd_dkdvdq runs
- *   instead: one pass over each key tile's query tiles gives dK, dV and that tile's
+ *   dropout drawn in the backward (attn_bwd_dropout and its variants other than
+ *   attn_bwd_dropout_bits) the fused pass of attn_bwd_dkdvdq runs instead: one pass over each key tile's query tiles gives dK, dV and that tile's
  *   share of dQ from the same recomputed tiles (five products, the keep bits drawn once
  *   instead of twice), dQ summed over the key tiles in the workspace's float32
  *   accumulator by atomic reductions and then rounded to dt; the order of those

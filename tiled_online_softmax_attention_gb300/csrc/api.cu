@@ -707,11 +707,12 @@ attn_status finish_impl(const void* workspace, size_t workspace_bytes, void* dq,
   return ATTN_OK;
 }
 
-// The whole backward.  d <= 128 with dropout takes the fused path (five products per tile
-// pair, the keep bits drawn once, dQ through a float32 accumulator); without dropout the
-// two deterministic kernels measured faster on this GPU (the fused kernel's dQ reductions
-// compete with its shared-memory operand traffic) and run instead; d = 256 uses its three
-// deterministic kernels.
+// The whole backward.  d <= 128 with dropout drawn here takes the fused path (five
+// products per tile pair, the keep bits drawn once, dQ through a float32 accumulator);
+// without dropout, or with the forward's stored keep bits (nothing to draw twice), the two
+// deterministic kernels measured as fast or faster on this GPU (the fused kernel's dQ
+// reductions compete with its shared-memory operand traffic) and run instead; d = 256
+// uses its three deterministic kernels.
 attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N,
                      int Nk, int d, attn_dtype dt, int causal, float scale, int* dev_status, void* stream,
@@ -723,7 +724,7 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   attn_status st = check_bwd({{q, qb}, {k, kb}, {v, kb}, {o, qb}, {dout, qb}}, lse, {{dq, qb}, {dk, kb}, {dv, kb}},
                              workspace, workspace_bytes, true, B, H, N, Nk, d, dt, scale, causal, need);
   if (st != ATTN_OK) return st;
-  const bool fused = !deterministic && d != 256 && dr.t > 0;
+  const bool fused = !deterministic && d != 256 && dr.t > 0 && keep_bits == nullptr;
   // the deterministic path does not read past the per-row values: prepare only those
   const size_t prep_bytes = fused ? workspace_bytes : attn_bwd_deterministic_workspace_bytes(B, H, N, d);
   if ((st = prepare_impl(o, dout, lse, workspace, prep_bytes, B, H, N, d, dt, stream)) != ATTN_OK) return st;
@@ -750,6 +751,8 @@ attn_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
       !make_map(&a.tm_dv, dv, BH, Nk, d, bf16))
     return ATTN_ERR_CUDA;
   fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
+  a.keep_bits = keep_bits;
+  a.bits_rows = a.Npad;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = dr.t > 0 ? attn::launch_bwd_grads_dropout(a, d, bf16, s) : attn::launch_bwd_grads(a, d, bf16, s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;

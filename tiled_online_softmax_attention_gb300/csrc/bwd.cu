@@ -340,20 +340,29 @@ __device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
       const int qt = i_begin + t;
       uint32_t keepbits = 0xffffffffu;  // bit c: query column c keeps this key
       if constexpr (DROP) {
-        // Lane L draws the keep bytes of query qt*128 + 32h + L for keys k0 + 32wq .. +31.
+        // Lane L takes query qt*128 + 32h + L's decisions for keys k0 + 32wq .. +31.
         const uint32_t qi = static_cast<uint32_t>(qt * kTileM + kEwCols * h + lane);
-        const uint32_t jg = static_cast<uint32_t>((k0 + 32 * wq) / 16);
-        uint32_t w0[4], w1[4];
-        philox4x32_10(jg, qi, static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w0);
-        philox4x32_10(jg + 1, qi, static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w1);
-        uint4* dst = reinterpret_cast<uint4*>(dbuf + lane * 32);
-        dst[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-        dst[1] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-        __syncwarp();
-        keepbits = 0;
+        if (!VARLEN && a.keep_bits != nullptr) {
+          // the forward's stored decisions (one 32-key word per row), transposed so that
+          // each thread holds its key's 32 queries
+          keepbits = warp_transpose32(a.keep_bits[(static_cast<size_t>(bh) * n_tk + kt) * 4 * a.bits_rows +
+                                                  static_cast<size_t>(wq) * a.bits_rows + qi]);
+        } else {
+          // drawn: lane L's keep bytes go through 1 KB of shared memory (written by query,
+          // read by key)
+          const uint32_t jg = static_cast<uint32_t>((k0 + 32 * wq) / 16);
+          uint32_t w0[4], w1[4];
+          philox4x32_10(jg, qi, static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w0);
+          philox4x32_10(jg + 1, qi, static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w1);
+          uint4* dst = reinterpret_cast<uint4*>(dbuf + lane * 32);
+          dst[0] = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+          dst[1] = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+          __syncwarp();
+          keepbits = 0;
 #pragma unroll
-        for (int c = 0; c < kEwCols; ++c) keepbits |= (dbuf[c * 32 + lane] >= a.drop_t ? 1u : 0u) << c;
-        __syncwarp();  // the buffer is rewritten for the next tile
+          for (int c = 0; c < kEwCols; ++c) keepbits |= (dbuf[c * 32 + lane] >= a.drop_t ? 1u : 0u) << c;
+          __syncwarp();  // the buffer is rewritten for the next tile
+        }
       }
       if (!(ok = mbar_wait_warp(bar(K_QFULL + s), (t / L::STAGES) & 1, wc))) break;
       if (!(ok = mbar_wait_warp(bar(K_SFULL), t & 1, wc))) break;
@@ -732,17 +741,30 @@ __device__ __forceinline__ void dq_body(const BwdArgs& a, int block) {
       mbar_arrive(bar(Q_QTM));
     }
     for (int j = 0; ok && j < n_kv; ++j) {
-      uint32_t keepw[8];  // dropout: 0xFF in byte (c % 4) of word c / 4 if key column c is kept
+      uint32_t keepw[8];  // dropout: bit 0 of byte (c % 4) of word c / 4 set if key column c is kept
       if constexpr (DROP) {
-        const uint32_t jg = static_cast<uint32_t>((j * kTileN + kEwCols * h) / 16);
-        uint32_t w[4];
-        const uint32_t tt = a.drop_t * 0x01010101u;
-        philox4x32_10(jg, static_cast<uint32_t>(grow), static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+        if (!VARLEN && a.keep_bits != nullptr) {
+          // the forward's stored word for this row and the warpgroup's 32 keys, one bit
+          // per key spread to one byte per key
+          const size_t n_tk = (a.Nk + kTileN - 1) / kTileN;
+          const uint32_t bits = a.keep_bits[(static_cast<size_t>(bh) * n_tk + j) * 4 * a.bits_rows +
+                                            static_cast<size_t>(h) * a.bits_rows + grow];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) keepw[q] = __vcmpgeu4(w[q], tt);
-        philox4x32_10(jg + 1, static_cast<uint32_t>(grow), static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t x = (bits >> (4 * q)) & 0xFu;
+            keepw[q] = (x & 1u) | ((x & 2u) << 7) | ((x & 4u) << 14) | ((x & 8u) << 21);
+          }
+        } else {
+          const uint32_t jg = static_cast<uint32_t>((j * kTileN + kEwCols * h) / 16);
+          uint32_t w[4];
+          const uint32_t tt = a.drop_t * 0x01010101u;
+          philox4x32_10(jg, static_cast<uint32_t>(grow), static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) keepw[4 + q] = __vcmpgeu4(w[q], tt);
+          for (int q = 0; q < 4; ++q) keepw[q] = __vcmpgeu4(w[q], tt);
+          philox4x32_10(jg + 1, static_cast<uint32_t>(grow), static_cast<uint32_t>(bh), 0u, a.seed_lo, a.seed_hi, w);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) keepw[4 + q] = __vcmpgeu4(w[q], tt);
+        }
       }
       if (!(ok = mbar_wait_warp(bar(Q_SFULL), j & 1, wc))) break;
       tc_fence_after();

@@ -78,7 +78,8 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   uint64_t wait_limit_ns;
-  // dropout only, as in FwdArgs (keep_bits: read by the fused kernel instead of drawing)
+  // dropout only, as in FwdArgs (keep_bits: the forward's stored decisions, read by the
+  // backward kernels instead of drawing; nullable)
   uint32_t drop_t;
   uint32_t seed_lo, seed_hi;
   float drop_scale;
