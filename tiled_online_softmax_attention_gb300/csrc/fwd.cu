@@ -93,9 +93,10 @@ constexpr float kPExp = 6.0f;
 enum : int {
   B_Q = 0,         // + tile
   B_SFULL = 2,     // + tile: S_i computed (MMA commit)
-  B_PFULL = 4,     // + tile: P_i written (softmax warpgroup)
+  B_PFULL = 4,     // + tile: P_i written (softmax warpgroup) and, but with ROT, O_i rescaled
+                   //   for it (correction warpgroup): the one hand-off P_i V_j waits for
   B_STAT = 6,      // + tile: rescale factors of this key tile published (softmax warpgroup)
-  B_CORR = 8,      // + tile: O_i rescaled if needed (correction warpgroup)
+  B_CORR = 8,      // + tile: O_i rescaled if needed (correction warpgroup; ROT only)
   B_ODONE = 10,    // + tile: P_i V_j done (MMA commit)
   B_FIN = 12,      // + tile: final m, l published (softmax warpgroup)
   B_DRAIN = 14,
@@ -267,7 +268,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(B_Q + i), 1);
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_PFULL + i), kWgArrivals);
+      mbar_init(bar(B_PFULL + i), ROT ? kWgArrivals : 2 * kWgArrivals);
       mbar_init(bar(B_STAT + i), kWgArrivals);
       mbar_init(bar(B_CORR + i), kWgArrivals);
       mbar_init(bar(B_ODONE + i), 1);
@@ -404,8 +405,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
       for (int j = 0; !ROT && ok && j < n_steps; ++j) {
         bool v_ready = false, k_next_ready = false;
         if (j < n_kv[0]) {
-          if (!(ok = full(2 * j + 1) && mbar_wait_warp(bar(B_PFULL + 0), j & 1, wc) &&
-                     (j == 0 || mbar_wait_warp(bar(B_CORR + 0), (j - 1) & 1, wc))))
+          if (!(ok = full(2 * j + 1) && mbar_wait_warp(bar(B_PFULL + 0), j & 1, wc)))
             break;
           v_ready = true;
           tc_fence_after();
@@ -418,8 +418,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
           }
         }
         if (has1) {
-          if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait_warp(bar(B_PFULL + 1), j & 1, wc) &&
-                     (j == 0 || mbar_wait_warp(bar(B_CORR + 1), (j - 1) & 1, wc))))
+          if (!(ok = (v_ready || full(2 * j + 1)) && mbar_wait_warp(bar(B_PFULL + 1), j & 1, wc)))
             break;
           tc_fence_after();
           issue_pv(1, j);
@@ -619,10 +618,18 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
     const int row = wq * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     bool ok = true;
-    for (int j = 1; ok && j < n_steps; ++j) {
+    // Without ROT the correction arrives on B_PFULL for every step, the first one too
+    // (nothing to rescale there), so that P_i V_j waits on one barrier; with ROT, S_i(j+1)
+    // is issued before P_i V_j, so the softmax's next arrival could land in the phase the
+    // correction has not yet reached, and the two hand-offs keep their own barriers.
+    for (int j = ROT ? 1 : 0; ok && j < n_steps; ++j) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         if (j >= n_kv[i]) continue;
+        if (j == 0) {
+          arrive_wg(bar(B_PFULL + i));
+          continue;
+        }
         if (!(ok = mbar_wait_warp(bar(B_STAT + i), (j - 1) & 1, wc))) break;
         const float alpha = alpha_s[i * 128 + row];
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
@@ -640,7 +647,7 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
           tmem_st_wait();
         }
         tc_fence_before();
-        arrive_wg(bar(B_CORR + i));
+        arrive_wg(bar(ROT ? B_CORR + i : B_PFULL + i));
       }
     }
     // Epilogue: O_i / l -> 16-bit -> swizzled staging over Q_i -> TMA store; logsumexp.
