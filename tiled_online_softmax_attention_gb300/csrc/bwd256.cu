@@ -175,15 +175,15 @@ __device__ __forceinline__ void producer_drain(const Ring<NSLOT>& r, uint32_t st
   for (int c = (r.c > NSLOT ? r.c - NSLOT : 0); c < r.c; ++c) mbar_wait(r.full(c), (c / NSLOT) & 1, wc);
 }
 
-// The MMA warp's side of the ring.
+// The MMA warp's side of the ring (the whole warp calls it; one elected lane issues).
 template <int NSLOT>
 struct RingUse {
   Ring<NSLOT> r;
   const WaitCtl* wc;
-  __device__ bool next() { return mbar_wait(r.full(r.c), (r.c / NSLOT) & 1, *wc); }
+  __device__ bool next() { return mbar_wait_warp(r.full(r.c), (r.c / NSLOT) & 1, *wc); }
   __device__ uint32_t addr() const { return r.slot_addr(r.c); }
   __device__ void release() {
-    tc_commit(r.empty(r.c));
+    tc_commit_w(r.empty(r.c));
     ++r.c;
   }
 };
@@ -202,12 +202,12 @@ __device__ __forceinline__ bool mma_kk256(RingUse<NSLOT>& u, uint32_t d_tmem, ui
       const int k = 8 * h + kk;
       const uint32_t aoff = (k >> 2) * kBlk + (k & 3) * 32;
       const uint32_t boff = (kk >> 2) * kBlk + (kk & 3) * 32;
-      mma_ss(d_tmem, sdesc_sw128(a_stat + aoff, 16, 1024), sdesc_sw128(b_item + boff, 16, 1024), idesc,
-             (h == 0 && kk == 0) ? 0u : 1u);
+      mma_ss_w(d_tmem, sdesc_sw128(a_stat + aoff, 16, 1024), sdesc_sw128(b_item + boff, 16, 1024), idesc,
+               (h == 0 && kk == 0) ? 0u : 1u);
     }
     u.release();
   }
-  tc_commit(done);
+  tc_commit_w(done);
   return true;
 }
 
@@ -223,8 +223,8 @@ __device__ __forceinline__ bool mma_ts256(RingUse<NSLOT>& u, uint32_t acc, uint3
     const uint32_t b_item = u.addr();
 #pragma unroll
     for (int k = 0; k < kTileM / 16; ++k)
-      mma_ts(acc + 128 * h, a_tmem + kEwCols2 * (k >> 1) + 8 * (k & 1), sdesc_sw128(b_item + k * 2048, kBlk, 1024),
-             idesc, (first && k == 0) ? 0u : 1u);
+      mma_ts_w(acc + 128 * h, a_tmem + kEwCols2 * (k >> 1) + 8 * (k & 1), sdesc_sw128(b_item + k * 2048, kBlk, 1024),
+               idesc, (first && k == 0) ? 0u : 1u);
     u.release();
   }
   return true;
@@ -451,24 +451,24 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dv_kernel(const __grid_co
       ok = ok && load_tile(r, &a.tm_do, qy(q0), qz(q0), wc);
     }
     producer_drain(r, bar(R_STAT), wc);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {  // the whole warp runs the issuing loop, one elected lane issues
     constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);
     constexpr uint32_t idesc_g = idesc_f16(kTileM, 128, BF16, false, true);
     RingUse<NSLOT> u{Ring<NSLOT>{c.sb + L::OFF_RING, c.bars}, &wc};
     const uint32_t kst = c.sb + L::OFF_ST;
-    bool ok = mbar_wait(bar(R_STAT), 0, wc);
+    bool ok = mbar_wait_warp(bar(R_STAT), 0, wc);
     if (ok && n_iter > 0) ok = mma_kk256(u, c.tmem, kst, idesc_s, bar(R_SFULL));
     for (int t = 0; ok && t < n_iter; ++t) {
       const uint32_t buf = 128u * (t & 1);
       // S^T(t+1) into the other buffer (its P^T(t-1) was read by dV(t-1), issued earlier)
       if (t + 1 < n_iter && !(ok = mma_kk256(u, c.tmem + (128u - buf), kst, idesc_s, bar(R_SFULL + ((t + 1) & 1)))))
         break;
-      if (!(ok = mbar_wait(bar(R_PREADY + (t & 1)), (t >> 1) & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(bar(R_PREADY + (t & 1)), (t >> 1) & 1, wc))) break;
       ok = mma_ts256(u, c.tmem + TM_DV, c.tmem + buf, idesc_g, t == 0);
     }
-    if (ok) tc_commit(bar(R_DONE));
-    tc_commit(bar(R_DRAIN));
-    mbar_wait(bar(R_DRAIN), 0, wc);
+    if (ok) tc_commit_w(bar(R_DONE));
+    tc_commit_w(bar(R_DRAIN));
+    mbar_wait_warp(bar(R_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1, wq = warp & 3, row = wq * 32 + lane;  // row: key within the tile
     const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -563,29 +563,29 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dk_kernel(const __grid_co
       if (ok && t + 1 < n_iter) ok = load_tile(r, &a.tm_do, qy(q0 + kTileM), qz(q0 + kTileM), wc);
     }
     producer_drain(r, bar(R_STAT), wc);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {  // the whole warp runs the issuing loop, one elected lane issues
     constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileM, BF16, false, false);
     constexpr uint32_t idesc_g = idesc_f16(kTileM, 128, BF16, false, true);
     RingUse<NSLOT> u{Ring<NSLOT>{c.sb + L::OFF_RING, c.bars}, &wc};
-    bool ok = mbar_wait(bar(R_STAT), 0, wc);
+    bool ok = mbar_wait_warp(bar(R_STAT), 0, wc);
     if (ok && n_iter > 0)
       ok = mma_kk256(u, c.tmem + TM_S, st_k, idesc_s, bar(R_SFULL)) &&
            mma_kk256(u, c.tmem + TM_DP, st_v, idesc_s, bar(R_DPFULL));
     for (int t = 0; ok && t < n_iter; ++t) {
       if (t + 1 < n_iter) {  // S^T(t+1) once S^T(t) is in registers
-        if (!(ok = mbar_wait(bar(R_SREAD), t & 1, wc))) break;
+        if (!(ok = mbar_wait_warp(bar(R_SREAD), t & 1, wc))) break;
         tc_fence_after();
         if (!(ok = mma_kk256(u, c.tmem + TM_S, st_k, idesc_s, bar(R_SFULL)))) break;
       }
-      if (!(ok = mbar_wait(bar(R_DSREADY), t & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(bar(R_DSREADY), t & 1, wc))) break;
       tc_fence_after();
       if (!(ok = mma_ts256(u, c.tmem + TM_DK, c.tmem + TM_DP, idesc_g, t == 0))) break;
       // dP^T(t+1) overwrites dS^T(t) after dK(t), issued above, has read it
       if (t + 1 < n_iter && !(ok = mma_kk256(u, c.tmem + TM_DP, st_v, idesc_s, bar(R_DPFULL)))) break;
     }
-    if (ok) tc_commit(bar(R_DONE));
-    tc_commit(bar(R_DRAIN));
-    mbar_wait(bar(R_DRAIN), 0, wc);
+    if (ok) tc_commit_w(bar(R_DONE));
+    tc_commit_w(bar(R_DRAIN));
+    mbar_wait_warp(bar(R_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1, wq = warp & 3, row = wq * 32 + lane;
     const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -688,29 +688,29 @@ __global__ void __launch_bounds__(kThreads2, 1) bwd256_dq_kernel(const __grid_co
       if (ok && j + 1 < n_kv) ok = load_tile(r, &a.tm_v, ky(kr + kTileN), kz(kr + kTileN), wc);
     }
     producer_drain(r, bar(R_STAT), wc);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {  // the whole warp runs the issuing loop, one elected lane issues
     constexpr uint32_t idesc_s = idesc_f16(kTileM, kTileN, BF16, false, false);
     constexpr uint32_t idesc_g = idesc_f16(kTileM, 128, BF16, false, true);
     RingUse<NSLOT> u{Ring<NSLOT>{c.sb + L::OFF_RING, c.bars}, &wc};
-    bool ok = mbar_wait(bar(R_STAT), 0, wc);
+    bool ok = mbar_wait_warp(bar(R_STAT), 0, wc);
     if (ok && n_kv > 0)
       ok = mma_kk256(u, c.tmem + TM_S, st_q, idesc_s, bar(R_SFULL)) &&
            mma_kk256(u, c.tmem + TM_DP, st_do, idesc_s, bar(R_DPFULL));
     for (int j = 0; ok && j < n_kv; ++j) {
       if (j + 1 < n_kv) {  // S(j+1) once S(j) is in registers
-        if (!(ok = mbar_wait(bar(R_SREAD), j & 1, wc))) break;
+        if (!(ok = mbar_wait_warp(bar(R_SREAD), j & 1, wc))) break;
         tc_fence_after();
         if (!(ok = mma_kk256(u, c.tmem + TM_S, st_q, idesc_s, bar(R_SFULL)))) break;
       }
-      if (!(ok = mbar_wait(bar(R_DSREADY), j & 1, wc))) break;
+      if (!(ok = mbar_wait_warp(bar(R_DSREADY), j & 1, wc))) break;
       tc_fence_after();
       if (!(ok = mma_ts256(u, c.tmem + TM_DQ, c.tmem + TM_DP, idesc_g, j == 0))) break;
       // dP(j+1) overwrites dS(j) after dQ(j), issued above, has read it
       if (j + 1 < n_kv && !(ok = mma_kk256(u, c.tmem + TM_DP, st_do, idesc_s, bar(R_DPFULL)))) break;
     }
-    if (ok) tc_commit(bar(R_DONE));
-    tc_commit(bar(R_DRAIN));
-    mbar_wait(bar(R_DRAIN), 0, wc);
+    if (ok) tc_commit_w(bar(R_DONE));
+    tc_commit_w(bar(R_DRAIN));
+    mbar_wait_warp(bar(R_DRAIN), 0, wc);
   } else if (warp >= 4) {
     const int h = (warp >> 2) - 1, wq = warp & 3, row = wq * 32 + lane, grow = q0 + row;
     const uint32_t t_lane = c.tmem + (static_cast<uint32_t>(wq * 32) << 16);

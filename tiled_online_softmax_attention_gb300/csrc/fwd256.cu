@@ -215,14 +215,15 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
     // Let every copy this thread started land before the CTA can exit.
     mbar_wait(bar(F_Q), 0, wc);
     for (int i = (c > L::NSLOT ? c - L::NSLOT : 0); i < c; ++i) mbar_wait(bar(F_KVFULL + (i & 1)), (i >> 1) & 1, wc);
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (the whole
+    // warp runs it, one elected lane issues)
     constexpr uint32_t idesc_qk = idesc_f16(kTileM, kTileN, BF16, false, false);
     constexpr uint32_t idesc_pv = idesc_f16(kTileM, D256, BF16, false, true);
     int c = 0;
-    auto full = [&]() -> bool { return mbar_wait(bar(F_KVFULL + (c & 1)), (c >> 1) & 1, wc); };
+    auto full = [&]() -> bool { return mbar_wait_warp(bar(F_KVFULL + (c & 1)), (c >> 1) & 1, wc); };
     auto release = [&]() {
-      tc_commit(bar(F_KVEMPTY + (c & 1)));
+      tc_commit_w(bar(F_KVEMPTY + (c & 1)));
       ++c;
     };
     auto issue_s = [&](int buf) {
@@ -230,22 +231,22 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
 #pragma unroll
       for (int k = 0; k < D256 / 16; ++k) {
         const uint32_t off = (k >> 2) * L::BLK + (k & 3) * 32;
-        mma_ss(tmem + 128u * buf, sdesc_sw128(sb + L::OFF_Q + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-               idesc_qk, k > 0 ? 1u : 0u);
+        mma_ss_w(tmem + 128u * buf, sdesc_sw128(sb + L::OFF_Q + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
+                 idesc_qk, k > 0 ? 1u : 0u);
       }
-      tc_commit(bar(F_SFULL + buf));
+      tc_commit_w(bar(F_SFULL + buf));
       release();
     };
     auto issue_pv = [&](int j) {
       const uint32_t vbase = sb + L::OFF_KV + (c & 1) * L::TILE;
 #pragma unroll
       for (int k = 0; k < kTileN / 16; ++k)
-        mma_ts(tmem + L::TM_O, tmem + 128u * (j & 1) + k * 8, sdesc_sw128(vbase + k * 2048, L::BLK, 1024), idesc_pv,
-               (j > 0 || k > 0) ? 1u : 0u);
-      tc_commit(bar(F_ODONE));
+        mma_ts_w(tmem + L::TM_O, tmem + 128u * (j & 1) + k * 8, sdesc_sw128(vbase + k * 2048, L::BLK, 1024), idesc_pv,
+                 (j > 0 || k > 0) ? 1u : 0u);
+      tc_commit_w(bar(F_ODONE));
       release();
     };
-    bool ok = mbar_wait(bar(F_Q), 0, wc) && full();
+    bool ok = mbar_wait_warp(bar(F_Q), 0, wc) && full();
     if (ok) {
       tc_fence_after();
       issue_s(0);
@@ -255,7 +256,7 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       issue_s(1);
     }
     for (int j = 0; ok && j < n_kv; ++j) {
-      if (!(ok = mbar_wait(bar(F_PFULL + (j & 1)), (j >> 1) & 1, wc) && full())) break;
+      if (!(ok = mbar_wait_warp(bar(F_PFULL + (j & 1)), (j >> 1) & 1, wc) && full())) break;
       tc_fence_after();
       issue_pv(j);
       if (j + 2 < n_kv) {
@@ -265,8 +266,8 @@ __global__ void __launch_bounds__(kF256Threads, 1) fwd256_kernel(const __grid_co
       }
     }
     // Drain: nothing may still write tensor memory when it is released.
-    tc_commit(bar(F_DRAIN));
-    mbar_wait(bar(F_DRAIN), 0, wc);
+    tc_commit_w(bar(F_DRAIN));
+    mbar_wait_warp(bar(F_DRAIN), 0, wc);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax, rescale, epilogue
     const int wq = warp & 3;
