@@ -82,12 +82,11 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
  *             of "Understanding FlashAttention, Part 2", section 2.2).
  *   o and lse must not overlap the inputs.
  *   d may be 64, 128 or 256 (at 256 each CTA owns one 128-row query tile).
- * At d = 128 the rows of long sequences (at least 48 key tiles of 128 per query tile,
- * counting half under the causal mask) run on CTA pairs: two CTAs on neighbouring SMs
- * share each product (tcgen05 cta_group::2) and each keeps three score tiles in flight;
- * shorter ones run one CTA per two query tiles.  Both give the same bytes.  The
- * environment variable ATTN_FWD_CTA_PAIR=1 or =0, read on every call, forces the pair
- * or the one-CTA kernel.
+ * At d = 128 without a causal mask, rows of at least 48 key tiles of 128 run on CTA
+ * pairs: two CTAs on neighbouring SMs share each product (tcgen05 cta_group::2) and each
+ * keeps three score tiles in flight; everything else runs one CTA per two query tiles.
+ * Both give the same bytes.  The environment variable ATTN_FWD_CTA_PAIR=1 or =0, read on
+ * every call, forces the pair or the one-CTA kernel.
  */
 ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale,

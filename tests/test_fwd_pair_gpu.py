@@ -2,7 +2,7 @@
 one-CTA kernel, which does the same arithmetic per row and must give the same bytes.
 
 ATTN_FWD_CTA_PAIR=1 / =0 forces the kernel attn_fwd and attn_fwd_rect run (by default
-the pair kernel takes only long rows).  Shapes cover one tile, ragged ends of the query
+the pair kernel takes only long rows without the causal mask).  Shapes cover one tile, ragged ends of the query
 and the key range, an odd number of query tiles (the second CTA of the last pair has no
 rows), fewer key tiles than the pair kernel's three score buffers, rectangular causal
 masks, and enough key tiles to cycle the buffers, the K/V ring and the rescale path."""

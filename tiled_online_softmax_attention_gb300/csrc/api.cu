@@ -37,17 +37,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 }
 
 // Which kernel runs the d = 128 forward without dropout: the CTA-pair kernel (fwd_pair.cu)
-// when a query tile visits many key tiles on average (Nk / 128, halved under the causal
-// mask, at least 48), else the one-CTA kernel.  The pair kernel's deeper pipeline wins on
-// long rows (B=1, H=32, N=16384: 1476 against 1362 TFLOP/s), its twice as many CTAs with
-// their own start-up and epilogue lose on short ones (B=2, H=16, N=4096 causal: 855
-// against 910; N=8192 causal: even).  ATTN_FWD_CTA_PAIR=1 or =0 (read on every call)
-// forces one or the other.
+// when the mask is not causal and every query tile visits at least 48 key tiles, else the
+// one-CTA kernel.  Measured on B=1, H=32, N=16384: pair 1513 against 1444 TFLOP/s
+// non-causal, but 1420 against 1437 causal; on B=2, H=16, N=8192 causal 1285 against 1367,
+// and N=4096 causal 853 against 955 (the pair kernel's twice as many CTAs each pay their
+// own start-up and epilogue, which the causal mask's short rows cannot amortise).
+// ATTN_FWD_CTA_PAIR=1 or =0 (read on every call) forces one or the other.
 bool fwd_use_pair(int Nk, int causal) {
   const char* s = std::getenv("ATTN_FWD_CTA_PAIR");
   if (s && (s[0] == '0' || s[0] == '1') && s[1] == 0) return s[0] == '1';
-  const int tiles = (Nk + attn::kTileN - 1) / attn::kTileN;
-  return (causal ? tiles / 2 : tiles) >= 48;
+  return !causal && (Nk + attn::kTileN - 1) / attn::kTileN >= 48;
 }
 
 uint64_t wait_limit_ns() {
