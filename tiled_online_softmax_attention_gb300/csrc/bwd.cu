@@ -164,9 +164,11 @@ enum : int {
   K_DSREADY = 4,  // dS^T written (all element-wise threads)
   K_DONE = 5,
   K_DRAIN = 6,
-  K_QFULL = 7,    // + stage
+  K_QFULL = 7,    // + stage: Q_i, LSE2_i, D_i landed
   K_EMPTY = 11,   // + stage
-  K_COUNT = 15
+  K_DOFULL = 15,  // + stage: dO_i landed (apart from Q_i: S^T(t+1), issued before dP^T(t+1),
+                  //   needs only Q_i, so the stage's dO copy is not on that product's path)
+  K_COUNT = 19
 };
 
 // The dK/dV CTA for work unit `block` (its body; the kernels below launch it).  `a` is
@@ -219,6 +221,7 @@ __device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
     for (int s = 0; s < L::STAGES; ++s) {
       mbar_init(bar(K_QFULL + s), 1);
       mbar_init(bar(K_EMPTY + s), 1);
+      mbar_init(bar(K_DOFULL + s), 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -253,21 +256,24 @@ __device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
         const int q0 = (i_begin + t) * kTileM;
         if (t >= L::STAGES && !mbar_wait(bar(K_EMPTY + s), ((t / L::STAGES) - 1) & 1, wc)) break;
         const uint32_t st = stage_base(s);
-        mbar_arrive_expect_tx(bar(K_QFULL + s), 2 * T::TILE + 1024);
-        for (int kb = 0; kb < T::KB; ++kb) {
+        mbar_arrive_expect_tx(bar(K_QFULL + s), T::TILE + 1024);
+        mbar_arrive_expect_tx(bar(K_DOFULL + s), T::TILE);
+        for (int kb = 0; kb < T::KB; ++kb)
           tma_load_3d(st + L::S_Q + kb * T::BLK, &a.tm_q, bar(K_QFULL + s), kb * 64, VARLEN ? hh : q0,
                       VARLEN ? tq0 + q0 : bh);
-          tma_load_3d(st + L::S_DO + kb * T::BLK, &a.tm_do, bar(K_QFULL + s), kb * 64, VARLEN ? hh : q0,
-                      VARLEN ? tq0 + q0 : bh);
-        }
         const size_t w = static_cast<size_t>(bh) * a.Npad + q0;
         bulk_load(st + L::S_L, a.lse2 + w, 512, bar(K_QFULL + s));
         bulk_load(st + L::S_D, a.delta + w, 512, bar(K_QFULL + s));
+        for (int kb = 0; kb < T::KB; ++kb)
+          tma_load_3d(st + L::S_DO + kb * T::BLK, &a.tm_do, bar(K_DOFULL + s), kb * 64, VARLEN ? hh : q0,
+                      VARLEN ? tq0 + q0 : bh);
         issued = t + 1;
       }
       mbar_wait(bar(K_KVFULL), 0, wc);
-      for (int t = (issued > L::STAGES ? issued - L::STAGES : 0); t < issued; ++t)
+      for (int t = (issued > L::STAGES ? issued - L::STAGES : 0); t < issued; ++t) {
         mbar_wait(bar(K_QFULL + t % L::STAGES), (t / L::STAGES) & 1, wc);
+        mbar_wait(bar(K_DOFULL + t % L::STAGES), (t / L::STAGES) & 1, wc);
+      }
     }
   } else if (warp == 1) {
     // The whole warp runs the issuing loop; one elected lane issues each product.
@@ -295,6 +301,8 @@ __device__ __forceinline__ void dkdv_body(const BwdArgs& a, int block) {
     for (int t = 0; ok && t < n_iter; ++t) {
       const int s = t % L::STAGES;
       const uint32_t st = stage_base(s);
+      if (!(ok = mbar_wait_warp(bar(K_DOFULL + s), (t / L::STAGES) & 1, wc))) break;
+      tc_fence_after();
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
         const uint32_t off = (k >> 2) * T::BLK + (k & 3) * 32;
