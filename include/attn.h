@@ -419,7 +419,10 @@ ATTN_API attn_status attn_bwd_rect(const void *q, const void *k, const void *v, 
  *   d is 64 or 128 and workspace_bytes >= attn_bwd_workspace_bytes(), it also
  *   clears the fused backward's dQ accumulator (the first of attn_bwd's stages).
  * attn_bwd_dkdv -- dK and dV, one 128-key tile per CTA (reads the workspace; at
- *   d = 256 two launches, dV then dK).
+ *   d = 256 two launches, dV then dK).  At d = 128 the environment variable
+ *   ATTN_BWD_CTA_PAIR=1, read on every call, runs it on CTA pairs instead (two key
+ *   tiles per pair of neighbouring SMs sharing each product, tcgen05 cta_group::2): the
+ *   same bytes, measured slower on this GPU, so not the default.
  * attn_bwd_dq   -- dQ, one 128-query tile per CTA (reads the workspace).
  */
 ATTN_API attn_status attn_bwd_prepare(const void *o, const void *dout, const float *lse,

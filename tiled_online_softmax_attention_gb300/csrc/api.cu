@@ -49,6 +49,16 @@ bool fwd_use_pair(int Nk, int causal) {
   return !causal && (Nk + attn::kTileN - 1) / attn::kTileN >= 48;
 }
 
+// The d = 128 dK/dV stage without dropout on CTA pairs (bwd_pair.cu) when
+// ATTN_BWD_CTA_PAIR=1 (read on every call), else the one-CTA kernel.  Both give the same
+// bytes; the pair kernel measured 0.774 against 0.716 ms on B=2, H=16, N=8192 causal and
+// 1.473 against 1.407 ms non-causal (its hand-offs cross SMs, which costs more than the
+// halved operand reads save), so it is not the default.
+bool bwd_use_pair() {
+  const char* s = std::getenv("ATTN_BWD_CTA_PAIR");
+  return s && s[0] == '1' && s[1] == 0;
+}
+
 uint64_t wait_limit_ns() {
   static uint64_t v = [] {
     const char* s = std::getenv("ATTN_WAIT_LIMIT_NS");
@@ -629,7 +639,11 @@ attn_status dkdv_impl(const void* q, const void* k, const void* v, const void* d
     return ATTN_ERR_CUDA;
   fill_bwd(a, workspace, B, H, N, Nk, causal, scale, dev_status, dr);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const cudaError_t e = d == 256 ? attn::launch_bwd256_dkdv(a, bf16, s)
+  const bool pair = d == 128 && dr.t == 0 && bwd_use_pair();
+  if (pair && (!make_map(&a.tm_qh, q, BH, N, d, bf16, 64) || !make_map(&a.tm_doh, dout, BH, N, d, bf16, 64)))
+    return ATTN_ERR_CUDA;
+  const cudaError_t e = d == 256  ? attn::launch_bwd256_dkdv(a, bf16, s)
+                        : pair    ? attn::launch_bwd_dkdv_pair(a, bf16, s)
                         : dr.t > 0 ? attn::launch_bwd_dkdv_dropout(a, d, bf16, s)
                                    : attn::launch_bwd_dkdv(a, d, bf16, s);
   if (e != cudaSuccess) return ATTN_ERR_CUDA;

@@ -63,6 +63,7 @@ __host__ __device__ __forceinline__ int visible_key_tiles(int qt, int Nk, int ca
 struct BwdArgs {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;  // inputs, as in FwdArgs
   CUtensorMap tm_dq, tm_dk, tm_dv;      // outputs
+  CUtensorMap tm_qh, tm_doh;            // the pair dK/dV kernel (bwd_pair.cu): Q and dO with 64-row boxes
   const void* o;                        // [B*H][N][d] forward output
   const void* dout;                     // [B*H][N][d]
   const float* lse;                     // [B*H][N]
@@ -171,6 +172,8 @@ cudaError_t launch_bwd_dq_varlen(const BwdArgs& a, int d, bool bf16, cudaStream_
 cudaError_t launch_bwd_pre(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dkdv(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_dq(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
+// d = 128 dK/dV on CTA pairs (bwd_pair.cu); needs tm_qh, tm_doh; not dropout or packed
+cudaError_t launch_bwd_dkdv_pair(const BwdArgs& a, bool bf16, cudaStream_t s);
 // dK/dV and dQ in one grid (the preparation pass must have run)
 cudaError_t launch_bwd_grads(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_bwd_grads_dropout(const BwdArgs& a, int d, bool bf16, cudaStream_t s);
