@@ -86,7 +86,10 @@ typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype;
  * pairs: two CTAs on neighbouring SMs share each product (tcgen05 cta_group::2) and each
  * keeps three score tiles in flight; everything else runs one CTA per two query tiles.
  * Both give the same bytes.  The environment variable ATTN_FWD_CTA_PAIR=1 or =0, read on
- * every call, forces the pair or the one-CTA kernel.
+ * every call, forces the pair or the one-CTA kernel.  At d = 64 with an even number of
+ * 128-row query tiles, ATTN_FWD_PERSIST=1 (read on every call) runs a persistent grid
+ * instead, whose CTAs take further work units from the hardware scheduler (cluster launch
+ * control); the same bytes, faster only for short rows of many heads, so not the default.
  */
 ATTN_API attn_status attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
                      int B, int H, int N, int d, attn_dtype dt, int causal, float scale,

@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libattn.so")
 BUILD = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "fwd.cu", "fwd_pair.cu", "bwd_pair.cu", "fwd256.cu", "bwd.cu", "bwd_fused.cu", "bwd256.cu", "bwd_noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_pair.cu", "fwd_persist.cu", "bwd_pair.cu", "fwd256.cu", "bwd.cu", "bwd_fused.cu", "bwd256.cu", "bwd_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

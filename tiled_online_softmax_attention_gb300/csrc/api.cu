@@ -49,6 +49,17 @@ bool fwd_use_pair(int Nk, int causal) {
   return !causal && (Nk + attn::kTileN - 1) / attn::kTileN >= 48;
 }
 
+// The d = 64 forward without dropout on the persistent grid (fwd_persist.cu) when
+// ATTN_FWD_PERSIST=1 (read on every call) and the query tiles pair up evenly.  The same
+// bytes as fwd_kernel; measured 159.7 against 172.3 us on B=32, H=12, N=1024 non-causal,
+// level on B=8, H=12, N=1024, and slower on causal and long rows (2797 against 2619 us on
+// B=1, H=32, N=16384), so it is not the default.
+bool fwd_use_persist(int N) {
+  const char* s = std::getenv("ATTN_FWD_PERSIST");
+  const bool even = ((N + attn::kTileM - 1) / attn::kTileM) % 2 == 0;
+  return even && s && s[0] == '1' && s[1] == 0;
+}
+
 // The d = 128 dK/dV stage without dropout on CTA pairs (bwd_pair.cu) when
 // ATTN_BWD_CTA_PAIR=1 (read on every call), else the one-CTA kernel.  Both give the same
 // bytes; the pair kernel measured 0.774 against 0.716 ms on B=2, H=16, N=8192 causal and
@@ -252,9 +263,11 @@ attn_status fwd_impl(const void* q, const void* k, const void* v, void* o, float
   a.bits_rows = static_cast<int>((static_cast<size_t>(N) + kTileM - 1) / kTileM * kTileM);
   const bool pair = d == 128 && dr.t == 0 && fwd_use_pair(Nk, causal);
   if (pair && !make_map(&a.tm_kh, k, BH, Nk, d, bf16, 64)) return ATTN_ERR_CUDA;
+  const bool persist = d == 64 && dr.t == 0 && fwd_use_persist(N);
   const cudaError_t e = d == 256  ? attn::launch_fwd256(a, bf16, static_cast<cudaStream_t>(stream))
                         : dr.t > 0 ? attn::launch_fwd_dropout(a, d, bf16, static_cast<cudaStream_t>(stream))
                         : pair     ? attn::launch_fwd_pair(a, bf16, static_cast<cudaStream_t>(stream))
+                        : persist  ? attn::launch_fwd_persist(a, bf16, static_cast<cudaStream_t>(stream))
                                    : attn::launch_fwd(a, d, bf16, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   return ATTN_OK;

@@ -156,6 +156,9 @@ __device__ __forceinline__ WorkItem work_item(int x, int BH, int n_units) {
 cudaError_t launch_fwd(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 // d = 128 on CTA pairs (fwd_pair.cu); needs tm_kh; not split, E4M3, dropout or packed
 cudaError_t launch_fwd_pair(const FwdArgs& a, bool bf16, cudaStream_t s);
+// d = 64 on a persistent grid (fwd_persist.cu); an even number of query tiles; not split,
+// dropout or packed
+cudaError_t launch_fwd_persist(const FwdArgs& a, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);
 cudaError_t launch_fwd_varlen_split(const FwdArgs& a, int d, bool bf16, cudaStream_t s);  // packed batches
 cudaError_t launch_fwd_fp8(const FwdArgs& a, int d, bool bf16_out, cudaStream_t s);

@@ -377,14 +377,17 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         tc_commit_w(bar(B_KVEMPTY + 0));
       }
       for (int j = 0; ROT && ok && j < n_steps; ++j) {
-        // S_0(j+1) | PV_0(j) | S_1(j+1) | PV_1(j)  (see ROT above)
+        // S_0(j+1) | PV_0(j) | S_1(j+1) | PV_1(j)  (see ROT above).  V(j) is waited for
+        // before S_0(j+1) is issued, so that nothing stands between that product and the
+        // wait for P_0(j): tile 0's softmax, which S_0(j+1) lets run on, cannot complete
+        // P_0(j+1) first (B_PFULL two phases ahead of a parity wait).
         const bool k_next = j + 1 < n_steps;  // K(j+1) is read by S_1(j+1) at least
+        if (!(ok = full(2 * j + 1))) break;
         if (k_next && !(ok = full(2 * j + 2))) break;
         if (j + 1 < n_kv[0]) {
           tc_fence_after();
           issue_s(0, j + 1);
         }
-        if (!(ok = full(2 * j + 1))) break;
         if (j < n_kv[0]) {
           if (!(ok = mbar_wait_warp(bar(B_PFULL + 0), j & 1, wc) && (j == 0 || mbar_wait_warp(bar(B_CORR + 0), (j - 1) & 1, wc))))
             break;

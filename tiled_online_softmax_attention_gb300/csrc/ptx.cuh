@@ -166,6 +166,50 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// Named barrier that also returns the AND of `v` over the participating threads, so that
+// a group of warps leaves a loop together.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// ---------------------------------------------------------------- cluster launch control
+
+// Asks the hardware scheduler to cancel the launch of one CTA of this grid that has not
+// started yet; the 16-byte answer lands at `resp` (16-byte aligned shared memory) and
+// completes 16 bytes of transaction count on `bar`.  After an answer that cancelled
+// nothing, the CTA must not ask again.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(resp), "r"(bar)
+               : "memory");
+}
+
+// The x index of the CTA an answer cancelled (this CTA now runs its work), or -1 when it
+// cancelled nothing (every CTA of the grid has started).
+__device__ __forceinline__ int clc_cancelled_x(uint32_t resp) {
+  int x;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .b64 lo, hi;\n\t.reg .pred p;\n\t"
+      "ld.shared.v2.b64 {lo, hi}, [%1];\n\t"
+      "mov.b128 r, {lo, hi};\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "mov.s32 %0, -1;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x)
+      : "r"(resp)
+      : "memory");
+  return x;
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
