@@ -104,3 +104,31 @@ def test_persist_forward_stress_inputs():
         o2, l2 = fwd(q, k, v, causal, True)
         o1, l1 = fwd(q, k, v, causal, False)
         assert torch.equal(o2, o1) and torch.equal(l2, l1)
+
+
+@pytest.mark.parametrize("persist", [False, True], ids=["one_unit", "persistent"])
+@pytest.mark.parametrize("B,H,N", [(32, 12, 1024), (8, 12, 2048)])
+def test_d64_repeated_calls_complete(B, H, N, persist):
+    """Causal d = 64 forwards of many heads, back to back: every call must finish without a
+    wait running out (the softmax of one query tile can run a key tile ahead of the
+    product issuer, so a hand-off that could complete two phases of one barrier before the
+    issuer looks would stall the CTA until the wait limit) and give the same bytes."""
+    q, k, v = draw(B, H, N, N, "bf16", seed=N + H)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    ref_o, ref_l = fwd(qd, kd, vd, True, persist)
+    old = os.environ.get("ATTN_FWD_PERSIST")
+    os.environ["ATTN_FWD_PERSIST"] = "1" if persist else "0"
+    try:
+        o = torch.empty_like(qd)
+        lse = torch.empty((B, H, N), device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(40):
+            assert attn.attn_fwd(qd, kd, vd, o, lse, B, H, N, 64, qd.dtype, True, 1 / 8, status) == attn.ATTN_OK
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+        assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)
+    finally:
+        if old is None:
+            del os.environ["ATTN_FWD_PERSIST"]
+        else:
+            os.environ["ATTN_FWD_PERSIST"] = old

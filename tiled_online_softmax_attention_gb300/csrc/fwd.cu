@@ -338,31 +338,38 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         const uint32_t qb = sb + L::OFF_Q + i * L::OTILE;
         const uint32_t kbase = sb + L::OFF_KV + ((2 * j) % L::NSLOT) * L::TILE;
         // One MMA per 32 bytes of the rows (K = 16 16-bit or 32 8-bit elements).
+        const uint32_t d_s = FP8 ? tmem + L::tm_s(i) : tmem + L::tm_sbuf(sbuf(i, j));
+        const uint32_t cb = bar(sfull_bar(sbuf(i, j)));
+        if (elect_one_sync()) {
 #pragma unroll
-        for (int k = 0; k < D * L::ELEM / 32; ++k) {
-          const uint32_t off = (k >> 2) * L::BLK + (k & 3) * 32;
-          if constexpr (FP8)
-            mma_ss_f8_w(tmem + L::tm_s(i), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                        idesc_qk, k > 0 ? 1u : 0u);
-          else
-            mma_ss_w(tmem + L::tm_sbuf(sbuf(i, j)), sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024),
-                     idesc_qk, k > 0 ? 1u : 0u);
+          for (int k = 0; k < D * L::ELEM / 32; ++k) {
+            const uint32_t off = (k >> 2) * L::BLK + (k & 3) * 32;
+            if constexpr (FP8)
+              mma_ss_f8(d_s, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+            else
+              mma_ss(d_s, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kbase + off, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
+          }
+          tc_commit(cb);
         }
-        tc_commit_w(bar(sfull_bar(sbuf(i, j))));
+        __syncwarp();
       };
       auto issue_pv = [&](int i, int j) {
         const uint32_t vbase = sb + L::OFF_KV + ((2 * j + 1) % L::NSLOT) * L::TILE;
         // One MMA per 32 keys' bytes of P (8 TMEM columns); V advances 32 / ELEM key rows.
+        const uint32_t a_p = FP8 ? tmem + L::tm_s(i) : tmem + L::tm_sbuf(sbuf(i, j));
+        if (elect_one_sync()) {
 #pragma unroll
-        for (int k = 0; k < kTileN * L::ELEM / 32; ++k) {
-          if constexpr (FP8)
-            mma_ts_f8_w(tmem + L::tm_o(i), tmem + L::tm_s(i) + k * 8,
-                        sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-          else
-            mma_ts_w(tmem + L::tm_o(i), tmem + L::tm_sbuf(sbuf(i, j)) + k * 8,
-                     sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kTileN * L::ELEM / 32; ++k) {
+            if constexpr (FP8)
+              mma_ts_f8(tmem + L::tm_o(i), a_p + k * 8, sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv,
+                        (j > 0 || k > 0) ? 1u : 0u);
+            else
+              mma_ts(tmem + L::tm_o(i), a_p + k * 8, sdesc_sw128(vbase + k * (4096 / L::ELEM), L::BLK, 1024), idesc_pv,
+                     (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(B_ODONE + i));
         }
-        tc_commit_w(bar(B_ODONE + i));
+        __syncwarp();
       };
       constexpr bool has1 = !PAD;
       bool ok = mbar_wait_warp(bar(B_Q + 0), 0, wc) && full(0);
@@ -635,9 +642,15 @@ __device__ __forceinline__ void fwd_body(const FwdArgs& a) {
         }
         if (!(ok = mbar_wait_warp(bar(B_STAT + i), (j - 1) & 1, wc))) break;
         const float alpha = alpha_s[i * 128 + row];
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          // O_i holds the sum up to key tile j-1: wait for that product, then rescale.
+        // With ROT every step waits for P_i V(j-1) first, rescaling or not: that product is
+        // issued only once the issuer has consumed B_CORR's previous phase, so this arrival
+        // can never put B_CORR two phases ahead of the issuer's parity wait (tile i's softmax,
+        // running on ahead, would otherwise let the two arrivals land back to back).
+        const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+        if (ROT || rescale)
           if (!(ok = mbar_wait_warp(bar(B_ODONE + i), (j - 1) & 1, wc))) break;
+        if (rescale) {
+          // O_i holds the sum up to key tile j-1 (that product is done): rescale.
           tc_fence_after();
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {

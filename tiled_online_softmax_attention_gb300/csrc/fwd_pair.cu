@@ -250,21 +250,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       auto full = [&](int j) { return pwait_warp(bar(P_KVFULL + j % L::NSLOT), (j / L::NSLOT) & 1, wc); };
       auto issue_s = [&](int j) {  // S(j) into buffer j mod kBuf
         const uint32_t kbase = sb + L::OFF_KV + (j % L::NSLOT) * L::SLOT;
+        if (elect_one_sync()) {
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k)
-          mma_ss_pair_w(tmem + L::tm_s(buf_of(j)), sdesc_sw128(sb + L::OFF_Q + (k >> 2) * L::QBLK + (k & 3) * 32, 16, 1024),
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss_pair(tmem + L::tm_s(buf_of(j)), sdesc_sw128(sb + L::OFF_Q + (k >> 2) * L::QBLK + (k & 3) * 32, 16, 1024),
                         sdesc_sw128(kbase + (k >> 2) * L::KBLK + (k & 3) * 32, 16, 1024), idesc_qk, k > 0 ? 1u : 0u);
-        tc_commit_pair_w(bar(P_SFULL + buf_of(j)), kBoth);
+          tc_commit_pair(bar(P_SFULL + buf_of(j)), kBoth);
+        }
+        __syncwarp();
       };
       auto issue_pv = [&](int j) {  // O += P(j) V_j; key tile j's slot is then free
         const uint32_t vbase = sb + L::OFF_KV + (j % L::NSLOT) * L::SLOT + L::HALF;
         // 16 keys per step: 8 columns of packed P, 16 rows (2 KB) of this CTA's V half
+        if (elect_one_sync()) {
 #pragma unroll
-        for (int k = 0; k < kTileN / 16; ++k)
-          mma_ts_pair_w(tmem + L::TM_O, tmem + L::tm_s(buf_of(j)) + k * 8, sdesc_sw128(vbase + k * 2048, L::HALF, 1024),
+          for (int k = 0; k < kTileN / 16; ++k)
+            mma_ts_pair(tmem + L::TM_O, tmem + L::tm_s(buf_of(j)) + k * 8, sdesc_sw128(vbase + k * 2048, L::HALF, 1024),
                         idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit_pair_w(bar(P_ODONE + buf_of(j)), kBoth);
-        tc_commit_pair_w(bar(P_KVEMPTY + j % L::NSLOT), kBoth);
+          tc_commit_pair(bar(P_ODONE + buf_of(j)), kBoth);
+          tc_commit_pair(bar(P_KVEMPTY + j % L::NSLOT), kBoth);
+        }
+        __syncwarp();
       };
       bool ok = pwait_warp(bar(P_Q), 0, wc);
       for (int j = 0; ok && j < min(kBuf, n_kv); ++j) {

@@ -259,21 +259,27 @@ __global__ void __launch_bounds__(kPThreads, 1) fwd_persist_kernel(const __grid_
           const uint32_t qb = q_base + static_cast<uint32_t>(i) * L::TILE;
           const uint32_t kbase = sb + L::OFF_KV + slot_of(2u * j) * L::TILE;
           const int b = (2 * j + i) % 3;
+          if (elect_one_sync()) {
 #pragma unroll
-          for (int k = 0; k < D * 2 / 32; ++k)
-            mma_ss_w(tmem + L::tm_sbuf(b), sdesc_sw128(qb + k * 32, 16, 1024), sdesc_sw128(kbase + k * 32, 16, 1024),
+            for (int k = 0; k < D * 2 / 32; ++k)
+              mma_ss(tmem + L::tm_sbuf(b), sdesc_sw128(qb + k * 32, 16, 1024), sdesc_sw128(kbase + k * 32, 16, 1024),
                      idesc_qk, k > 0 ? 1u : 0u);
-          tc_commit_w(bar(U_SFULL + 3 * i + b));
+            tc_commit(bar(U_SFULL + 3 * i + b));
+          }
+          __syncwarp();
         };
         auto issue_pv = [=](int i, int j) {
           const uint32_t vbase = sb + L::OFF_KV + slot_of(2u * j + 1u) * L::TILE;
           const int b = (2 * j + i) % 3;
           // One MMA per 16 keys: 8 columns of packed P, 16 rows (2 KB) of V.
+          if (elect_one_sync()) {
 #pragma unroll
-          for (int k = 0; k < kTileN / 16; ++k)
-            mma_ts_w(tmem + L::tm_o(i), tmem + L::tm_sbuf(b) + k * 8, sdesc_sw128(vbase + k * 2048, kTileM * 128, 1024),
+            for (int k = 0; k < kTileN / 16; ++k)
+              mma_ts(tmem + L::tm_o(i), tmem + L::tm_sbuf(b) + k * 8, sdesc_sw128(vbase + k * 2048, kTileM * 128, 1024),
                      idesc_pv, (j > 0 || k > 0) ? 1u : 0u);
-          tc_commit_w(bar(U_ODONE + i));
+            tc_commit(bar(U_ODONE + i));
+          }
+          __syncwarp();
         };
         // P_i V(j) may run: P written, O rescaled for it, and for j = 0 the previous
         // unit's O_i read out by its epilogue.
@@ -445,9 +451,12 @@ __global__ void __launch_bounds__(kPThreads, 1) fwd_persist_kernel(const __grid_
           if (j >= n_kv[i]) continue;
           if (!(ok = mbar_wait_warp(bar(U_STAT + i), (cum_c[i] + j - 1) & 1, wc))) break;
           const float alpha = alpha_s[(((cum_c[i] + j - 1) & 1) * 2 + i) * 128 + row];
+          // Every step waits for P_i V(j-1) first, rescaling or not: that product is issued
+          // only once the issuer has consumed U_CORR's previous phase, so this arrival can
+          // never put U_CORR two phases ahead of the issuer's parity wait.
+          if (!(ok = mbar_wait_warp(bar(U_ODONE + i), (cum_p[i] + j - 1) & 1, wc))) break;
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            // O_i holds the sum up to key tile j-1: wait for that product, then rescale.
-            if (!(ok = mbar_wait_warp(bar(U_ODONE + i), (cum_p[i] + j - 1) & 1, wc))) break;
+            // O_i holds the sum up to key tile j-1 (that product is done): rescale.
             tc_fence_after();
 #pragma unroll
             for (int cc = 0; cc < D / 16; ++cc) {

@@ -698,22 +698,23 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 }
 
 // ---------------------------------------------------------------- warp-issued forms
-// Products and commits issued by one elected lane of a converged warp.  The whole warp
+// Products and commits are issued by one elected lane of a converged warp.  The whole warp
 // runs the issuing code, so the descriptors are warp-uniform values that the compiler
 // keeps in uniform registers; issued from a lane-0-only branch instead, each product took
 // about 100 cycles to leave the SM sub-partition while the softmax warp beside it was
-// busy, where the tensor core needs 64 (measured on this GPU).
+// busy, where the tensor core needs 64 (measured on this GPU).  elect.sync picks the same
+// lane every time, so a commit tracks the MMAs issued through earlier elections.
+//
+// Two forms, each where it measured faster: the forward kernels (fwd.cu, fwd_pair.cu,
+// fwd_persist.cu) issue a product's MMAs and its commits from one elected branch, back to
+// back (2-6 % faster than one election per MMA on every forward shape); the backward and
+// d = 256 kernels issue one MMA per election through the wrappers below (the single branch
+// made dQ 2 % and the d = 256 forward 3 % slower).
 __device__ __forceinline__ void mma_ss_w(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   if (elect_one_sync()) mma_ss(d, a, b, id, acc);
 }
 __device__ __forceinline__ void mma_ts_w(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
   if (elect_one_sync()) mma_ts(d, a, b, id, acc);
-}
-__device__ __forceinline__ void mma_ss_f8_w(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-  if (elect_one_sync()) mma_ss_f8(d, a, b, id, acc);
-}
-__device__ __forceinline__ void mma_ts_f8_w(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
-  if (elect_one_sync()) mma_ts_f8(d, a, b, id, acc);
 }
 __device__ __forceinline__ void tc_commit_w(uint32_t bar) {
   if (elect_one_sync()) tc_commit(bar);
